@@ -1,0 +1,610 @@
+/*
+ * kvq_oracle.cpp -- plain, slow CPU oracle for decode attention over a paged,
+ * mixed INT2/INT4 quantized KV cache.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the
+ * benchmark's CPU-baseline leg may load this library.  It shares no code with
+ * the CUDA path (no headers, helpers, tables or constants); the only thing the
+ * two sides share is the seeded input generator in kvsynth/.
+ *
+ * What it computes, and the passage each step follows (pages are cited by
+ * title and section):
+ *   - greedy INT2/INT4 bit allocation by rho_k = (D_k(2) - D_k(4)) / (2 N_k)
+ *       [TriAxialKV, key design 2: attention-output-distortion calibration and
+ *        greedy bit-width allocation]
+ *   - asymmetric group quantization, G = 32: INT4 K and V per token, INT2 K per
+ *     channel (scale/zero shared across 32 tokens), INT2 V per token; residual
+ *     tokens that cannot fill a 32-token INT2 group stay INT4
+ *       [TriAxialKV, key design 3: custom mixed-precision cache layout and
+ *        residual fallback]
+ *   - one pool holding INT2 and INT4 pages, precision decided by page id;
+ *     INT2 pages reordered ahead of INT4 pages in each request's table; new
+ *     tokens written as INT4 at the tail
+ *       [TriAxialKV, key design 4: unified address space dual pool and the
+ *        fused Flash-Decoding operator]
+ *   - evicted slots read as a sentinel dead slot (logit -1e4, V = 0) without
+ *     moving surviving pages
+ *       [IntentKV, method 2: layout-preserving eviction, sentinel dead slot]
+ *   - softmax attention in fp64, and a split + log-sum-exp merge variant
+ *       [HyQuant, background "FlashAttention and online softmax" (m, l, acc;
+ *        O = acc / l) and Algorithm 3 split-K ReduceSoftmax]
+ *
+ * Readings of points the pages leave open (each restated where it is used):
+ *   R1 scale and zero are stored as IEEE binary16 (round to nearest even).
+ *   R2 per-token groups are 32 consecutive channels of one token and head.
+ *   R3 quantization: mn, mx exact; s32 = (mx - mn) / (2^b - 1) in fp32; s, z =
+ *      half(s32), half(mn); code = clamp(rint_even((x - z) / s), 0, 2^b - 1) in
+ *      fp32, code = 0 when s == 0; dequantization x^ = fmaf(code, s, z).
+ *   R4 INT2-tagged tokens wait in an INT4 "staging" page of their request; when
+ *      it holds 32 tokens it is requantized to INT2 from its INT4-dequantized
+ *      values, the staging page is freed and the INT2 page is appended to the
+ *      request's table.  Ids freed during one append call become reusable
+ *      after the call.  All 32 stored slots take part in the requantization;
+ *      the live mask is carried over unchanged.
+ *   R5 a page id is taken as the lowest free id of its class (INT2 ids
+ *      [0, n2), INT4 ids [n2, n2 + n4)).
+ *   R6 the dead slot's logit is -1e4 after scaling and its V is 0; slots never
+ *      written are not tokens and are skipped.
+ *   R7 the greedy scan skips a tag that does not fit the budget and continues;
+ *      the budget test is exact integer arithmetic with B = num / den.
+ */
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <set>
+#include <string>
+#include <unordered_map>
+#include <vector>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+namespace {
+
+enum { ORC_OK = 0, ORC_INVALID = 1, ORC_OOM = 2, ORC_RANGE = 3, ORC_STATE = 6 };
+constexpr int kD = 128;        // head dim
+constexpr int kP = 32;         // tokens per page
+constexpr int kG = 32;         // group size
+
+// ---------------------------------------------------------------------------
+// IEEE 754 binary16 <-> binary32, written from the format's definition:
+// 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits; subnormals below
+// 2^-14 with spacing 2^-24.  Rounding is to nearest, ties to even.
+// ---------------------------------------------------------------------------
+uint16_t f32_to_f16(float f) {
+  uint32_t x;
+  std::memcpy(&x, &f, 4);
+  const uint16_t sign = (uint16_t)((x >> 16) & 0x8000u);
+  const uint32_t ef = (x >> 23) & 0xFFu;
+  const uint32_t frac = x & 0x7FFFFFu;
+  if (ef == 0xFFu) return (uint16_t)(sign | 0x7C00u | (frac ? (0x200u | (frac >> 13)) : 0u));
+  if (ef == 0 && frac == 0) return sign;
+  // value = sig * 2^(e - 23) with sig a 24-bit integer (implicit bit included)
+  int e;
+  uint32_t sig;
+  if (ef == 0) { e = -126; sig = frac; } else { e = (int)ef - 127; sig = frac | 0x800000u; }
+  if (e > 15) return (uint16_t)(sign | 0x7C00u);
+  int drop;            // fraction bits of sig that do not fit
+  uint32_t hexp;       // biased half exponent before rounding (0 = subnormal)
+  if (e >= -14) { drop = 13; hexp = (uint32_t)(e + 15); }
+  else { drop = 13 + (-14 - e); hexp = 0; }
+  if (drop > 24) return sign;                      // below half of the smallest subnormal
+  uint32_t q = sig >> drop;
+  const uint32_t rem = sig & ((1u << drop) - 1u);
+  const uint32_t half = 1u << (drop - 1);
+  if (rem > half || (rem == half && (q & 1u))) ++q;
+  uint32_t bits;
+  if (hexp == 0) bits = q;                          // may carry into the smallest normal
+  else bits = (hexp << 10) + q - 0x400u;            // q in [0x400, 0x800]; carry bumps exponent
+  if (bits >= 0x7C00u) return (uint16_t)(sign | 0x7C00u);
+  return (uint16_t)(sign | bits);
+}
+
+float f16_to_f32(uint16_t h) {
+  const uint32_t sign = (uint32_t)(h & 0x8000u) << 16;
+  const uint32_t e = (h >> 10) & 0x1Fu;
+  const uint32_t m = h & 0x3FFu;
+  float v;
+  if (e == 0) v = std::ldexp((float)m, -24);
+  else if (e == 31) v = m ? NAN : INFINITY;
+  else v = std::ldexp((float)(m | 0x400u), (int)e - 25);
+  uint32_t b;
+  std::memcpy(&b, &v, 4);
+  b |= sign;
+  std::memcpy(&v, &b, 4);
+  return v;
+}
+
+float bf16_to_f32(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  std::memcpy(&f, &u, 4);
+  return f;
+}
+
+bool in_range(float x) { return std::isfinite(x) && std::fabs(x) <= 65504.0f; }
+
+// ---------------------------------------------------------------------------
+// Asymmetric group quantization (TriAxialKV, key design 3; reading R3).
+// x[i * stride], i < n; writes codes[i * cstride].
+// ---------------------------------------------------------------------------
+void quant_group(const float* x, int n, int stride, int bits, uint8_t* codes, int cstride,
+                 uint16_t* s_out, uint16_t* z_out) {
+  float mn = x[0], mx = x[0];
+  for (int i = 1; i < n; ++i) {
+    const float v = x[(size_t)i * stride];
+    mn = std::min(mn, v);
+    mx = std::max(mx, v);
+  }
+  const int qmax = (1 << bits) - 1;
+  volatile float range = mx - mn;                   // one fp32 rounding
+  const float s32 = range / (float)qmax;            // one fp32 rounding
+  const uint16_t sh = f32_to_f16(s32);
+  const uint16_t zh = f32_to_f16(mn);
+  const float sf = f16_to_f32(sh), zf = f16_to_f32(zh);
+  for (int i = 0; i < n; ++i) {
+    int c = 0;
+    if ((sh & 0x7FFFu) != 0) {
+      volatile float d = x[(size_t)i * stride] - zf;
+      const float u = d / sf;
+      const float r = std::nearbyint(u);            // default rounding mode: ties to even
+      c = r < 0.0f ? 0 : (r > (float)qmax ? qmax : (int)r);
+    }
+    codes[(size_t)i * cstride] = (uint8_t)c;
+  }
+  *s_out = sh;
+  *z_out = zh;
+}
+
+inline float dequant(uint8_t code, uint16_t s, uint16_t z) {
+  return std::fma((float)code, f16_to_f32(s), f16_to_f32(z));
+}
+
+// ---------------------------------------------------------------------------
+// Pool model.
+// Canonical content of one (page, kv-head) block:
+//   kc[slot][ch], vc[slot][ch]      codes, one byte each
+//   km[256]: INT4 page -> [slot][group]{s, z};  INT2 page -> [ch]{s, z}
+//   vm[256]: [slot][group]{s, z}  (V is per token at both widths)
+// ---------------------------------------------------------------------------
+struct HeadBlock {
+  uint8_t kc[kP * kD];
+  uint8_t vc[kP * kD];
+  uint16_t km[256];
+  uint16_t vm[256];
+};
+
+struct Page {
+  int32_t id = -1;
+  bool int2 = false;
+  int fill = 0;
+  uint32_t live = 0;
+  bool content = false;
+  int64_t pos[kP];
+  std::vector<HeadBlock> heads;
+};
+
+struct Req {
+  bool open = false;
+  std::vector<int32_t> table;
+  int32_t tail4 = -1, staging = -1;
+  std::vector<uint32_t> loc;      // token position -> page_id << 5 | slot
+};
+
+struct Pool {
+  int hkv = 0;
+  std::vector<int> sel;           // kv heads whose content is kept
+  int64_t n2 = 0, n4 = 0;
+  int max_req = 0, max_pages = 0;
+  std::set<int32_t> free2, free4;
+  std::unordered_map<int32_t, Page> pages;
+  std::vector<Req> reqs;
+};
+
+}  // namespace
+
+namespace {
+
+int32_t take_lowest(std::set<int32_t>& s) {
+  const int32_t id = *s.begin();
+  s.erase(s.begin());
+  return id;
+}
+
+Page& new_page(Pool* P, bool int2, bool content) {
+  const int32_t id = take_lowest(int2 ? P->free2 : P->free4);
+  Page& pg = P->pages[id];
+  pg = Page();
+  pg.id = id;
+  pg.int2 = int2;
+  pg.content = content;
+  if (content) {
+    pg.heads.resize(P->sel.size());
+    for (auto& hb : pg.heads) std::memset(&hb, 0, sizeof(HeadBlock));
+  }
+  return pg;
+}
+
+// INT4 per-token quantization of one token into `slot` (key design 3).
+void write_int4_token(const Pool* P, Page& pg, int slot, const uint16_t* k, const uint16_t* v) {
+  float xk[kD], xv[kD];
+  for (size_t j = 0; j < P->sel.size(); ++j) {
+    HeadBlock& hb = pg.heads[j];
+    for (int c = 0; c < kD; ++c) {
+      xk[c] = bf16_to_f32(k[j * kD + c]);
+      xv[c] = bf16_to_f32(v[j * kD + c]);
+    }
+    for (int gr = 0; gr < kD / kG; ++gr) {
+      quant_group(xk + gr * kG, kG, 1, 4, hb.kc + slot * kD + gr * kG, 1,
+                  &hb.km[(slot * 4 + gr) * 2], &hb.km[(slot * 4 + gr) * 2 + 1]);
+      quant_group(xv + gr * kG, kG, 1, 4, hb.vc + slot * kD + gr * kG, 1,
+                  &hb.vm[(slot * 4 + gr) * 2], &hb.vm[(slot * 4 + gr) * 2 + 1]);
+    }
+  }
+}
+
+// Requantize a full INT4 staging page into an INT2 page (key design 3; R4).
+void repack_to_int2(const Pool* P, const Page& src, Page& dst) {
+  dst.fill = kP;
+  dst.live = src.live;
+  std::memcpy(dst.pos, src.pos, sizeof(src.pos));
+  if (!src.content) return;
+  static thread_local float xk[kP * kD], xv[kP * kD];
+  for (size_t j = 0; j < P->sel.size(); ++j) {
+    const HeadBlock& a = src.heads[j];
+    HeadBlock& b = dst.heads[j];
+    for (int t = 0; t < kP; ++t)
+      for (int c = 0; c < kD; ++c) {
+        const int gr = c / kG;
+        xk[t * kD + c] = dequant(a.kc[t * kD + c], a.km[(t * 4 + gr) * 2], a.km[(t * 4 + gr) * 2 + 1]);
+        xv[t * kD + c] = dequant(a.vc[t * kD + c], a.vm[(t * 4 + gr) * 2], a.vm[(t * 4 + gr) * 2 + 1]);
+      }
+    // K: per channel, the group is the page's 32 tokens.
+    for (int c = 0; c < kD; ++c)
+      quant_group(xk + c, kP, kD, 2, b.kc + c, kD, &b.km[c * 2], &b.km[c * 2 + 1]);
+    // V: per token, 32 consecutive channels.
+    for (int t = 0; t < kP; ++t)
+      for (int gr = 0; gr < kD / kG; ++gr)
+        quant_group(xv + t * kD + gr * kG, kG, 1, 2, b.vc + t * kD + gr * kG, 1,
+                    &b.vm[(t * 4 + gr) * 2], &b.vm[(t * 4 + gr) * 2 + 1]);
+  }
+}
+
+void free_id(Pool* P, int32_t id) {
+  P->pages.erase(id);
+  if (id < P->n2) P->free2.insert(id); else P->free4.insert(id);
+}
+
+}  // namespace
+
+extern "C" {
+
+// ---- scalar helpers exposed for pins ---------------------------------------
+void orc_f32_to_f16(const float* x, uint16_t* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = f32_to_f16(x[i]);
+}
+void orc_f16_to_f32(const uint16_t* x, float* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = f16_to_f32(x[i]);
+}
+// One group of n values at `bits` (2 or 4).
+int orc_quant_group(const float* x, int n, int bits, uint16_t* s, uint16_t* z, uint8_t* codes) {
+  if (n <= 0 || (bits != 2 && bits != 4)) return ORC_INVALID;
+  for (int i = 0; i < n; ++i) if (!in_range(x[i])) return ORC_RANGE;
+  quant_group(x, n, 1, bits, codes, 1, s, z);
+  return ORC_OK;
+}
+float orc_dequant(uint8_t code, uint16_t s, uint16_t z) { return dequant(code, s, z); }
+
+// ---- greedy bit allocation (TriAxialKV key design 2; reading R7) -----------
+// bits_out[k] in {2, 4}.  Budget: sum_k N_k b_k <= (B_num / B_den) sum_k N_k.
+int orc_alloc_bits(const int64_t* N, const double* D2, const double* D4, int n_tags,
+                   int64_t B_num, int64_t B_den, uint8_t* bits_out) {
+  if (n_tags <= 0 || B_den <= 0 || B_num < 0) return ORC_INVALID;
+  int64_t total = 0;
+  for (int k = 0; k < n_tags; ++k) {
+    if (N[k] < 0) return ORC_INVALID;
+    total += N[k];
+    bits_out[k] = 2;
+  }
+  std::vector<std::pair<double, int>> order;   // (rho, tag)
+  for (int k = 0; k < n_tags; ++k)
+    if (N[k] > 0) order.push_back({(D2[k] - D4[k]) / (2.0 * (double)N[k]), k});
+  std::stable_sort(order.begin(), order.end(), [](const std::pair<double, int>& a,
+                                                  const std::pair<double, int>& b) {
+    if (a.first != b.first) return a.first > b.first;  // descending rho
+    return a.second < b.second;                         // ties: ascending tag id
+  });
+  int64_t used = 2 * total;
+  for (const auto& e : order) {
+    const int64_t extra = 2 * N[e.second];
+    if ((used + extra) * B_den <= B_num * total) {
+      bits_out[e.second] = 4;
+      used += extra;
+    }
+  }
+  return ORC_OK;
+}
+
+// ---- pool --------------------------------------------------------------------
+// sel_heads: kv heads whose codes are materialized (n_sel of them); page ids,
+// tables, fills and live masks are modelled for every head regardless.
+void* orc_pool_new(int hkv, int64_t n2, int64_t n4, int max_req, int max_pages,
+                   const int* sel_heads, int n_sel) {
+  if (hkv <= 0 || n2 < 0 || n4 < 0 || max_req <= 0 || max_pages <= 0) return nullptr;
+  Pool* P = new Pool();
+  P->hkv = hkv;
+  P->n2 = n2;
+  P->n4 = n4;
+  P->max_req = max_req;
+  P->max_pages = max_pages;
+  for (int i = 0; i < n_sel; ++i) P->sel.push_back(sel_heads[i]);
+  for (int64_t i = 0; i < n2; ++i) P->free2.insert((int32_t)i);
+  for (int64_t i = 0; i < n4; ++i) P->free4.insert((int32_t)(n2 + i));
+  P->reqs.resize(max_req);
+  return P;
+}
+
+void orc_pool_free(void* h) { delete (Pool*)h; }
+
+int orc_request_open(void* h, int32_t* id_out) {
+  Pool* P = (Pool*)h;
+  for (int r = 0; r < P->max_req; ++r)
+    if (!P->reqs[r].open) {
+      P->reqs[r] = Req();
+      P->reqs[r].open = true;
+      *id_out = r;
+      return ORC_OK;
+    }
+  return ORC_OOM;
+}
+
+int orc_request_close(void* h, int32_t id) {
+  Pool* P = (Pool*)h;
+  if (id < 0 || id >= P->max_req || !P->reqs[id].open) return ORC_INVALID;
+  for (int32_t pid : P->reqs[id].table) free_id(P, pid);
+  P->reqs[id] = Req();
+  return ORC_OK;
+}
+
+// Append n tokens in arrival order (TriAxialKV key designs 3-4; readings R4, R5).
+// k, v: bf16 bits [n][n_sel][128] for the selected heads, or both NULL to model
+// page ids and tables only.  Returns ORC_INVALID / ORC_RANGE / ORC_OOM with no
+// change to the pool.
+int orc_append(void* h, const uint16_t* k, const uint16_t* v, const int32_t* req,
+               const uint8_t* bits, int64_t n) {
+  Pool* P = (Pool*)h;
+  const bool content = (k != nullptr && v != nullptr);
+  const size_t nsel = P->sel.size();
+  for (int64_t t = 0; t < n; ++t) {
+    if (req[t] < 0 || req[t] >= P->max_req || !P->reqs[req[t]].open) return ORC_INVALID;
+    if (bits[t] != 2 && bits[t] != 4) return ORC_INVALID;
+  }
+  if (content)
+    for (int64_t i = 0; i < n * (int64_t)nsel * kD; ++i)
+      if (!in_range(bf16_to_f32(k[i])) || !in_range(bf16_to_f32(v[i]))) return ORC_RANGE;
+  // Dry run: count the pages this call takes and the table growth.
+  struct Sim { bool tail = false; int tailfill = 0; bool stag = false; int stagfill = 0; int64_t tablen = 0; };
+  std::unordered_map<int32_t, Sim> sim;
+  int64_t need4 = 0, need2 = 0;
+  for (int64_t t = 0; t < n; ++t) {
+    auto it = sim.find(req[t]);
+    if (it == sim.end()) {
+      const Req& R = P->reqs[req[t]];
+      Sim s;
+      if (R.tail4 >= 0) { s.tail = true; s.tailfill = P->pages.at(R.tail4).fill; }
+      if (R.staging >= 0) { s.stag = true; s.stagfill = P->pages.at(R.staging).fill; }
+      s.tablen = (int64_t)R.table.size();
+      it = sim.emplace(req[t], s).first;
+    }
+    Sim& s = it->second;
+    if (bits[t] == 4) {
+      if (!s.tail || s.tailfill == kP) { ++need4; ++s.tablen; s.tail = true; s.tailfill = 0; }
+      ++s.tailfill;
+    } else {
+      if (!s.stag) { ++need4; ++s.tablen; s.stag = true; s.stagfill = 0; }
+      if (++s.stagfill == kP) { ++need2; s.stag = false; }
+    }
+    if (s.tablen > P->max_pages) return ORC_OOM;
+  }
+  if (need4 > (int64_t)P->free4.size() || need2 > (int64_t)P->free2.size()) return ORC_OOM;
+
+  std::vector<int32_t> deferred;
+  for (int64_t t = 0; t < n; ++t) {
+    Req& R = P->reqs[req[t]];
+    const int64_t pos = (int64_t)R.loc.size();
+    const uint16_t* kt = content ? k + (size_t)t * nsel * kD : nullptr;
+    const uint16_t* vt = content ? v + (size_t)t * nsel * kD : nullptr;
+    int32_t& cur = (bits[t] == 4) ? R.tail4 : R.staging;
+    if (cur < 0 || P->pages.at(cur).fill == kP) {
+      Page& pg = new_page(P, false, content);
+      cur = pg.id;
+      R.table.push_back(pg.id);
+    }
+    Page& pg = P->pages.at(cur);
+    const int slot = pg.fill++;
+    pg.live |= 1u << slot;
+    pg.pos[slot] = pos;
+    if (pg.content && content) write_int4_token(P, pg, slot, kt, vt);
+    else if (pg.content) { pg.content = false; pg.heads.clear(); }
+    R.loc.push_back(((uint32_t)pg.id << 5) | (uint32_t)slot);
+    if (bits[t] == 2 && pg.fill == kP) {
+      Page& np = new_page(P, true, pg.content);
+      repack_to_int2(P, pg, np);
+      for (int s = 0; s < kP; ++s) R.loc[np.pos[s]] = ((uint32_t)np.id << 5) | (uint32_t)s;
+      R.table.erase(std::find(R.table.begin(), R.table.end(), pg.id));
+      R.table.push_back(np.id);
+      deferred.push_back(pg.id);
+      R.staging = -1;
+    }
+  }
+  for (int32_t id : deferred) free_id(P, id);
+  return ORC_OK;
+}
+
+// INT2-first stable reorder of each listed request's table (TriAxialKV key design 4, phase 1).
+int orc_reorder(void* h, const int32_t* req, int n) {
+  Pool* P = (Pool*)h;
+  for (int i = 0; i < n; ++i)
+    if (req[i] < 0 || req[i] >= P->max_req || !P->reqs[req[i]].open) return ORC_INVALID;
+  for (int i = 0; i < n; ++i) {
+    auto& tb = P->reqs[req[i]].table;
+    std::stable_partition(tb.begin(), tb.end(), [P](int32_t id) { return id < P->n2; });
+  }
+  return ORC_OK;
+}
+
+// Evict token positions (IntentKV, layout-preserving eviction): clear live bits only.
+int orc_evict(void* h, const int32_t* req, const int64_t* pos, int64_t n) {
+  Pool* P = (Pool*)h;
+  for (int64_t i = 0; i < n; ++i) {
+    if (req[i] < 0 || req[i] >= P->max_req || !P->reqs[req[i]].open) return ORC_INVALID;
+    if (pos[i] < 0 || pos[i] >= (int64_t)P->reqs[req[i]].loc.size()) return ORC_INVALID;
+  }
+  for (int64_t i = 0; i < n; ++i) {
+    const uint32_t l = P->reqs[req[i]].loc[pos[i]];
+    P->pages.at((int32_t)(l >> 5)).live &= ~(1u << (l & 31u));
+  }
+  return ORC_OK;
+}
+
+int orc_request_info(void* h, int32_t id, int32_t* n_pages, int64_t* n_tok) {
+  Pool* P = (Pool*)h;
+  if (id < 0 || id >= P->max_req || !P->reqs[id].open) return ORC_INVALID;
+  *n_pages = (int32_t)P->reqs[id].table.size();
+  *n_tok = (int64_t)P->reqs[id].loc.size();
+  return ORC_OK;
+}
+
+// Canonical export of one request, pages in table order.  Content arrays are
+// [n_pages][n_sel][32][128] (codes) and [n_pages][n_sel][256] (meta); pass NULL
+// to skip them.
+int orc_export(void* h, int32_t id, int32_t* ids, uint8_t* is_int2, uint8_t* fill, uint32_t* live,
+               uint8_t* kc, uint8_t* vc, uint16_t* km, uint16_t* vm) {
+  Pool* P = (Pool*)h;
+  if (id < 0 || id >= P->max_req || !P->reqs[id].open) return ORC_INVALID;
+  const auto& tb = P->reqs[id].table;
+  const size_t nsel = P->sel.size();
+  for (size_t i = 0; i < tb.size(); ++i) {
+    const Page& pg = P->pages.at(tb[i]);
+    ids[i] = pg.id;
+    is_int2[i] = pg.int2 ? 1 : 0;
+    fill[i] = (uint8_t)pg.fill;
+    live[i] = pg.live;
+    if (kc) {
+      if (!pg.content) return ORC_STATE;
+      for (size_t j = 0; j < nsel; ++j) {
+        const HeadBlock& hb = pg.heads[j];
+        std::memcpy(kc + (i * nsel + j) * kP * kD, hb.kc, kP * kD);
+        std::memcpy(vc + (i * nsel + j) * kP * kD, hb.vc, kP * kD);
+        std::memcpy(km + (i * nsel + j) * 256, hb.km, 512);
+        std::memcpy(vm + (i * nsel + j) * 256, hb.vm, 512);
+      }
+    }
+  }
+  return ORC_OK;
+}
+
+// Decode attention in fp64 for the listed (batch row, q head) pairs.
+// q: bf16 bits [B][Hq][128]; kv head of q head hq is hq / (Hq / Hkv).
+// n_splits <= 1: one softmax pass.  n_splits > 1: the token sequence (table
+// order, slot order) is cut into n_splits contiguous chunks; each chunk keeps
+// (m, l, acc) and the chunks are merged by log-sum-exp (HyQuant, online
+// softmax and Algorithm 3 ReduceSoftmax).  A request with no tokens gives 0.
+// out: [n_pairs][128].
+int orc_decode(void* h, const uint16_t* q, const int32_t* req, int B, int Hq, float scale,
+               const int32_t* pairs, int n_pairs, int n_splits, double* out, int n_threads) {
+  Pool* P = (Pool*)h;
+  if (Hq <= 0 || Hq % P->hkv != 0) return ORC_INVALID;
+  const int g = Hq / P->hkv;
+  for (int i = 0; i < n_pairs; ++i) {
+    const int b = pairs[2 * i], hq = pairs[2 * i + 1];
+    if (b < 0 || b >= B || hq < 0 || hq >= Hq) return ORC_INVALID;
+    const int r = req[b];
+    if (r < 0 || r >= P->max_req || !P->reqs[r].open) return ORC_INVALID;
+    if (std::find(P->sel.begin(), P->sel.end(), hq / g) == P->sel.end()) return ORC_INVALID;
+    for (int32_t pid : P->reqs[r].table) if (!P->pages.at(pid).content) return ORC_STATE;
+  }
+#ifdef _OPENMP
+  if (n_threads > 0) omp_set_num_threads(n_threads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+  for (int i = 0; i < n_pairs; ++i) {
+    const int b = pairs[2 * i], hq = pairs[2 * i + 1];
+    const Req& R = P->reqs[req[b]];
+    const int kv = hq / g;
+    const size_t j = (size_t)(std::find(P->sel.begin(), P->sel.end(), kv) - P->sel.begin());
+    double qd[kD];
+    for (int c = 0; c < kD; ++c) qd[c] = (double)bf16_to_f32(q[((size_t)b * Hq + hq) * kD + c]);
+    // Token list in table order: (logit, pointer to page block, slot, live).
+    std::vector<double> logit;
+    std::vector<std::pair<const HeadBlock*, int>> src;
+    std::vector<bool> alive;
+    for (int32_t pid : R.table) {
+      const Page& pg = P->pages.at(pid);
+      const HeadBlock& hb = pg.heads[j];
+      for (int s = 0; s < pg.fill; ++s) {
+        const bool lv = (pg.live >> s) & 1u;
+        double l = -1e4;                                   // sentinel dead slot (R6)
+        if (lv) {
+          double acc = 0.0;
+          for (int c = 0; c < kD; ++c) {
+            const int mi = pg.int2 ? c * 2 : (s * 4 + c / kG) * 2;
+            acc += qd[c] * (double)dequant(hb.kc[s * kD + c], hb.km[mi], hb.km[mi + 1]);
+          }
+          l = (double)scale * acc;
+        }
+        logit.push_back(l);
+        src.push_back({&hb, s});
+        alive.push_back(lv);
+      }
+    }
+    double* o = out + (size_t)i * kD;
+    for (int c = 0; c < kD; ++c) o[c] = 0.0;
+    const int64_t T = (int64_t)logit.size();
+    if (T == 0) continue;
+    const int S = n_splits <= 1 ? 1 : n_splits;
+    std::vector<double> ms, ls, accs;
+    for (int sp = 0; sp < S; ++sp) {
+      const int64_t a = T * sp / S, e = T * (sp + 1) / S;
+      if (a == e) continue;
+      double m = -INFINITY;
+      for (int64_t t = a; t < e; ++t) m = std::max(m, logit[t]);
+      double l = 0.0, acc[kD] = {0.0};
+      for (int64_t t = a; t < e; ++t) {
+        const double w = std::exp(logit[t] - m);
+        l += w;
+        if (!alive[t]) continue;                           // V = 0 at the dead slot
+        const HeadBlock& hb = *src[t].first;
+        const int s = src[t].second;
+        for (int c = 0; c < kD; ++c) {
+          const int mi = (s * 4 + c / kG) * 2;
+          acc[c] += w * (double)dequant(hb.vc[s * kD + c], hb.vm[mi], hb.vm[mi + 1]);
+        }
+      }
+      ms.push_back(m);
+      ls.push_back(l);
+      accs.insert(accs.end(), acc, acc + kD);
+    }
+    double M = -INFINITY;
+    for (double m : ms) M = std::max(M, m);
+    double L = 0.0;
+    for (size_t k2 = 0; k2 < ms.size(); ++k2) {
+      const double f = std::exp(ms[k2] - M);
+      L += ls[k2] * f;
+      for (int c = 0; c < kD; ++c) o[c] += accs[k2 * kD + c] * f;
+    }
+    for (int c = 0; c < kD; ++c) o[c] /= L;
+  }
+  return ORC_OK;
+}
+
+int orc_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+}  // extern "C"
