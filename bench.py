@@ -1,0 +1,319 @@
+"""Benchmark: one decode step of the mixed INT2/INT4 paged-KV path.
+
+A step = append one new token per request (INT4 quantize-on-append into the
+tail page) + INT2-first reorder + split-KV fused-dequant decode attention with
+log-sum-exp merge, over the Qwen3-8B-shaped single-layer workload (batch 8,
+32 query / 8 KV heads, head_dim 128, 32K context per request, INT2:INT4 from
+the greedy allocator at B = 3).  The metric is algorithmic KV bytes per step
+(codes + binary16 scale/zero of every page block read, table entries, q, out)
+divided by the step time.
+
+Launch: `python bench.py [--gpus 1] [--steps K] [--warmup W]`; for N > 1 under
+torchrun each rank runs its own replica of the workload (requests are
+independent; there is no data-path collective) and rank 0 reports the total.
+`--impl reference` times the CPU oracle on a bounded sample of the same
+workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "mixed INT2/INT4 paged decode: KV-bytes GB/s (% of HBM peak), µs/layer-step"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                          "-lms", "100", "-i", str(self.gpu)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def cpu_baseline(w, seconds=12.0):
+    """The oracle as it stands, on this host's cores, over one request (all
+    heads) of the same workload: KV-bytes GB/s of its decode."""
+    import oracle
+    from oracle.workload import oracle_twin_for
+    ow, pairs, nbytes = oracle_twin_for(w)
+    cores = min(os.cpu_count() or 1, len(pairs))
+    q = ow.q(0)
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        ow.P.decode(q[:1], [ow.rids[0]], w.softmax_scale, pairs=pairs, n_threads=cores)
+        reps += 1
+        if time.perf_counter() - t0 > seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": nbytes * reps / dt / 1e9, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"request 0 ({w.requests[0].n_prefill} tokens), all {w.num_q_heads} q heads, fp64 decode "
+                      f"x{reps} in {dt:.1f}s"}
+
+
+def run_reference(args):
+    """Reference arm: the CPU oracle (the only reference this path has)."""
+    ws, rank, _ = dist_setup()
+    if rank != 0:
+        return 0
+    import kvsynth
+    from oracle.workload import oracle_twin_for
+    w = kvsynth.make_workload(args.config)
+    ow, pairs, nbytes_all = oracle_twin_for(w)
+    g = w.g
+    unit_bytes = nbytes_all / w.num_kv_heads          # one kv head of request 0 (+ q/out share)
+    cores = 1
+    q = ow.q(0)
+    rng = np.random.default_rng(0)
+    for _ in range(args.warmup):
+        ow.P.decode(q[:1], [ow.rids[0]], w.softmax_scale, pairs=pairs[:1], n_threads=1)
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        p = pairs[rng.integers(0, len(pairs))][None]
+        ow.P.decode(q[:1], [ow.rids[0]], w.softmax_scale, pairs=p, n_threads=1)
+    dt = time.perf_counter() - t0
+    value = unit_bytes * args.steps / dt / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "sample": f"one (request 0, q head) pair per step, 1 of {g} heads "
+                                                     f"sharing a kv head; {w.requests[0].n_prefill} tokens"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": "one q head of request 0 per step"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--decode-impl", default="auto", choices=["auto", "simt", "mma"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import kvsynth
+    import mixed_precision_kv_gb300 as kvq
+    from mixed_precision_kv_gb300.workload import GPUWorkload
+
+    ws, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    w = kvsynth.make_workload(args.config)
+    e2e_steps = max(args.steps // 4, 10)
+    total_steps = args.warmup + args.steps + 3 + e2e_steps
+    gw = GPUWorkload(w, device=local, steps=total_steps)
+    gw.pool.set_decode_impl({"auto": 0, "simt": 1, "mma": 2}[args.decode_impl])
+    gw.prefill()
+    gw.evict()
+    gw.reorder()
+    gw.pool.sync()
+    B, Hkv, Hq = len(gw.rids), w.num_kv_heads, w.num_q_heads
+    dev = torch.device("cuda", local)
+    # Per-step inputs, resident in HBM before timing.
+    ks = torch.empty((total_steps, B, Hkv, 128), dtype=torch.bfloat16, device=dev)
+    vs = torch.empty_like(ks)
+    qs = torch.empty((total_steps, B, Hq, 128), dtype=torch.bfloat16, device=dev)
+    bits = np.zeros((total_steps, B), np.uint8)
+    for s in range(total_steps):
+        for r in range(B):
+            pos = w.requests[r].n_prefill + s
+            kvsynth.fill_bf16_dev(ks[s, r].data_ptr(), 1, Hkv, 128, w.seed, kvsynth.TENSOR_K, w.requests[r].stream,
+                                  pos, gw.chan.data_ptr())
+            kvsynth.fill_bf16_dev(vs[s, r].data_ptr(), 1, Hkv, 128, w.seed, kvsynth.TENSOR_V, w.requests[r].stream,
+                                  pos)
+            bits[s, r] = gw.bits[r][pos]
+        kvsynth.fill_bf16_dev(qs[s].data_ptr(), B, Hq, 128, w.seed, kvsynth.TENSOR_Q, s)
+    rids = np.array(gw.rids, np.int32)
+    out = torch.empty((B, Hq, 128), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(s, k=None, v=None, q=None):
+        gw.pool.append(ks[s] if k is None else k, vs[s] if v is None else v, rids, bits[s])
+        gw.pool.reorder(rids)
+        return gw.pool.decode(qs[s] if q is None else q, rids, w.softmax_scale, out=out)
+
+    for s in range(args.warmup):
+        step(s)
+    gw.pool.sync()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    s0 = args.warmup
+    # kv bytes per step (host accounting of the tables), and per-decode events
+    kv_bytes = []
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    launches0 = gw.pool.launch_count()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        start.record(stream)
+        for i in range(args.steps):
+            s = s0 + i
+            gw.pool.append(ks[s], vs[s], rids, bits[s])
+            gw.pool.reorder(rids)
+            ev[i][0].record(stream)
+            gw.pool.decode(qs[s], rids, w.softmax_scale, out=out)
+            ev[i][1].record(stream)
+            kv_bytes.append(gw.pool.last_decode_stats()["kv_bytes"])
+        end.record(stream)
+        torch.cuda.synchronize()
+    launches = gw.pool.launch_count() - launches0
+    gw.pool.sync()
+    t_ms = start.elapsed_time(end)
+    dec_ms = [a.elapsed_time(b) for a, b in ev]
+    if dist:
+        t = torch.tensor([t_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_ms = float(t.item())
+    step_bytes = float(np.mean(kv_bytes))
+    value = step_bytes * args.steps * ws / (t_ms / 1e3) / 1e9
+    dec_mean_ms = float(np.mean(dec_ms))
+    achieved = step_bytes / (dec_mean_ms / 1e3) / 1e9
+    peak, peak_kind = measured_peak()
+
+    # End to end: host (pinned) inputs copied in and the output copied out every step.
+    s_e = s0 + args.steps + 3
+    hk = ks[s_e:s_e + e2e_steps].cpu().pin_memory()
+    hv = vs[s_e:s_e + e2e_steps].cpu().pin_memory()
+    hq_ = qs[s_e:s_e + e2e_steps].cpu().pin_memory()
+    hout = torch.empty((B, Hq, 128), dtype=torch.float32).pin_memory()
+    dk = torch.empty_like(ks[0])
+    dv = torch.empty_like(vs[0])
+    dq = torch.empty_like(qs[0])
+    for i in range(3):
+        step(s0 + args.steps + i)
+    torch.cuda.synchronize()
+    e_bytes = []
+    t0 = time.perf_counter()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(e2e_steps):
+        dk.copy_(hk[i], non_blocking=True)
+        dv.copy_(hv[i], non_blocking=True)
+        dq.copy_(hq_[i], non_blocking=True)
+        step(s_e + i, dk, dv, dq)
+        hout.copy_(out, non_blocking=True)
+        e_bytes.append(gw.pool.last_decode_stats()["kv_bytes"])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e_ms = e0.elapsed_time(e1)
+    e2e_val = float(np.mean(e_bytes)) * e2e_steps * ws / (e_ms / 1e3) / 1e9
+    h2d = (dk.numel() + dv.numel() + dq.numel()) * 2
+    d2h = hout.numel() * 4
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": t_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "u4/u2 codes, f16 meta, f32 accum", "data": "synthetic",
+            "config": {"workload": w.name, "batch": B, "num_q_heads": Hq, "num_kv_heads": Hkv, "head_dim": 128,
+                       "context": w.requests[0].n_prefill, "page_tokens": 32, "budget_bits": "3.0",
+                       "decode_impl": args.decode_impl, "l2": "inputs larger than L2 (%.0f MB per step)"
+                                                             % (step_bytes / 1e6),
+                       "us_per_layer_step": t_ms / args.steps * 1e3, "decode_us": dec_mean_ms * 1e3,
+                       "pct_of_8000_gbs": value / ws / 8000 * 100},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": None, "peak_source": peak_kind,
+                         "kernel": "decode (split scan + merge), CUDA events around kv_decode_attn"},
+            "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches,
+            "clocks": clk.summary()}
+    if rank == 0 and not args.no_cpu_baseline:
+        try:
+            line["cpu_baseline"] = cpu_baseline(w)
+        except Exception as e:  # reported, not fatal
+            line["cpu_baseline"] = {"error": repr(e)}
+    if rank == 0:
+        print(json.dumps(line))
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

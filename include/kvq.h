@@ -1,0 +1,186 @@
+/*
+ * kvq.h -- C ABI of the GB300 (sm_103a) mixed INT2/INT4 paged KV cache and its
+ * decode-step attention.
+ *
+ * The problem these calls follow:
+ *   - TriAxialKV, key design 3 (custom mixed-precision cache layout and
+ *     residual fallback): asymmetric group quantization with G = 32; INT4 K
+ *     and V per token; INT2 K per channel with scale and zero shared across 32
+ *     tokens; INT2 V per token; tokens that cannot fill a 32-token INT2 group
+ *     stay INT4.
+ *   - TriAxialKV, key design 4 (unified address space dual pool and fused
+ *     Flash-Decoding): INT2 and INT4 pages live in one address range and a
+ *     page's precision follows from its id; before decoding, each request's
+ *     page table is reordered so INT2 pages precede INT4 pages; decoding splits
+ *     the sequence, dequantizes inside the attention scan and merges the splits
+ *     with a global log-sum-exp; new tokens are written as INT4 at the tail.
+ *   - HyQuant, Algorithm 3 (decode): split-K over the quantized prefix with
+ *     in-kernel dequantization, the g query heads of one KV head packed
+ *     together, and a ReduceSoftmax merge of (m, l, acc).
+ *   - IntentKV, method 2 (layout-preserving eviction): an evicted slot reads
+ *     as a sentinel dead slot whose attention contribution is zero, and no
+ *     surviving page moves.
+ *
+ * Conventions for every call:
+ *   - Return value: a kv_status_t.  On KV_ERR_INVALID_ARG and KV_ERR_OOM the
+ *     pool is left exactly as it was.  kv_last_error() gives a message for the
+ *     calling thread's last failure.
+ *   - "device" pointers are CUDA device memory on the pool's device, owned by
+ *     the caller; "host" pointers are ordinary host memory owned by the caller
+ *     and only read or written during the call.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Work is
+ *     enqueued asynchronously on it; device-side failures (an out-of-range
+ *     input value found by the quantizer, a bounded wait that expired) are
+ *     recorded in the pool and returned by kv_pool_sync().
+ *   - A pool is not thread-safe; issue its calls from one thread and keep its
+ *     device work on one stream at a time.
+ *   - No C++ exception crosses this boundary.
+ *
+ * Fixed format: head_dim 128, 32 tokens per page, group size 32.  Page block
+ * of one (page, kv head): INT2 = 3072 bytes, INT4 = 5120 bytes (codes plus
+ * binary16 scale/zero).  The physical byte order inside a block is private to
+ * the library; kv_export_request() returns the canonical content.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define KVQ_API __attribute__((visibility("default")))
+#else
+#define KVQ_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KV_OK = 0,
+  KV_ERR_INVALID_ARG = 1,     /* bad argument or size; nothing changed */
+  KV_ERR_OOM = 2,             /* pool pages, table slots or request slots exhausted; nothing changed */
+  KV_ERR_RANGE = 3,           /* an appended K/V value was NaN, Inf or |x| > 65504 */
+  KV_ERR_CUDA = 4,            /* a CUDA runtime call failed */
+  KV_ERR_DEVICE_TIMEOUT = 5,  /* a bounded device-side wait gave up */
+  KV_ERR_STATE = 6            /* call not valid in the pool's current state */
+} kv_status_t;
+
+typedef enum {
+  KV_DECODE_AUTO = 0,         /* the fastest implementation available */
+  KV_DECODE_SIMT = 1,         /* CUDA-core fp32 scan (reference/ablation kernel) */
+  KV_DECODE_MMA = 2           /* tensor-core scan */
+} kv_decode_impl_t;
+
+typedef struct kv_pool kv_pool_t;   /* opaque; owns all pool device memory, tables and workspaces */
+
+typedef struct {
+  int32_t num_kv_heads;           /* Hkv >= 1 */
+  int32_t head_dim;               /* must be 128 */
+  int32_t page_tokens;            /* must be 32 */
+  int32_t group;                  /* must be 32 */
+  int64_t n_int2_pages;           /* INT2 page ids are [0, n_int2_pages) */
+  int64_t n_int4_pages;           /* INT4 page ids are [n_int2_pages, n_int2_pages + n_int4_pages) */
+  int32_t max_requests;           /* request ids are [0, max_requests) */
+  int32_t max_pages_per_request;  /* table capacity of one request */
+  int32_t device;                 /* CUDA device ordinal */
+} kv_pool_config_t;
+
+/* Create a pool: one device allocation holding the INT2 region followed by the
+ * INT4 region (TriAxialKV key design 4), plus the device page tables.
+ * out: host pointer receiving the handle. */
+KVQ_API kv_status_t kv_pool_create(const kv_pool_config_t* cfg, kv_pool_t** out);
+
+/* Free everything the pool owns.  Synchronizes with the pool's device work. */
+KVQ_API kv_status_t kv_pool_destroy(kv_pool_t* pool);
+
+/* Open an empty request; *req_id (host) receives the lowest free request id. */
+KVQ_API kv_status_t kv_request_open(kv_pool_t* pool, int32_t* req_id);
+
+/* Close a request and return all of its pages to the free lists. */
+KVQ_API kv_status_t kv_request_close(kv_pool_t* pool, int32_t req_id);
+
+/* Quantize-on-append (TriAxialKV key designs 3 and 4).
+ *   k, v     device, bf16 [n_tok][num_kv_heads][128], tokens in arrival order.
+ *   req_ids  host, int32 [n_tok]: open request of each token.
+ *   bits     host, uint8 [n_tok]: 4 -> the request's INT4 tail page;
+ *            2 -> the request's INT4 staging page, which is requantized into a
+ *            new INT2 page (K per channel, V per token) as soon as it holds 32
+ *            tokens; that INT2 page is appended to the request's table.
+ * Page ids are the lowest free ids of their class; staging pages freed by a
+ * repack become reusable after the call.  Values are checked on the device:
+ * NaN, Inf or |x| > 65504 make kv_pool_sync() return KV_ERR_RANGE. */
+KVQ_API kv_status_t kv_append_quant(kv_pool_t* pool, const void* k, const void* v, const int32_t* req_ids,
+                            const uint8_t* bits, int64_t n_tok, void* stream);
+
+/* Phase-1 reorder (TriAxialKV key design 4): stable partition of each listed
+ * request's table so INT2 entries precede INT4 entries.  req_ids: host [n_req]. */
+KVQ_API kv_status_t kv_reorder_pages(kv_pool_t* pool, const int32_t* req_ids, int32_t n_req, void* stream);
+
+/* Layout-preserving eviction (IntentKV method 2): clear the live bit of each
+ * (request, token position) pair; the slot then reads as the sentinel dead
+ * slot (logit -1e4, V = 0).  Token positions count appended tokens from 0.
+ * req_ids: host int32 [n]; token_pos: host int64 [n].  Evicting twice is a no-op. */
+KVQ_API kv_status_t kv_evict_slots(kv_pool_t* pool, const int32_t* req_ids, const int64_t* token_pos, int64_t n,
+                           void* stream);
+
+/* Decode-step GQA attention over the page tables (TriAxialKV key design 4,
+ * HyQuant Algorithm 3).
+ *   q        device, bf16 [batch][num_q_heads][128]
+ *   req_ids  host, int32 [batch]: request of each batch row
+ *   out      device, fp32 [batch][num_q_heads][128]
+ * q head h uses kv head h / (num_q_heads / num_kv_heads); num_q_heads must be
+ * a multiple of num_kv_heads with a ratio <= 8.  A request with no tokens
+ * yields zeros.  Logits are softmax_scale * q.k^ in fp32 accumulation. */
+KVQ_API kv_status_t kv_decode_attn(kv_pool_t* pool, const void* q, const int32_t* req_ids, int32_t batch,
+                           int32_t num_q_heads, float softmax_scale, float* out, void* stream);
+
+/* Choose the decode implementation (kv_decode_impl_t). */
+KVQ_API kv_status_t kv_set_decode_impl(kv_pool_t* pool, int32_t impl);
+
+/* Wait for the pool's enqueued work; report device-side errors recorded since
+ * the last call (KV_ERR_RANGE, KV_ERR_DEVICE_TIMEOUT) or KV_ERR_CUDA. */
+KVQ_API kv_status_t kv_pool_sync(kv_pool_t* pool);
+
+/* Host outputs: number of table entries and of appended tokens of a request. */
+KVQ_API kv_status_t kv_request_info(kv_pool_t* pool, int32_t req_id, int32_t* n_pages, int64_t* n_tokens);
+
+/* Canonical, synchronous export of one request, pages in table order (host
+ * buffers sized from kv_request_info):
+ *   ids [n], is_int2 [n], fill [n] (tokens written), live [n] (bit t = slot t live)
+ *   k_codes, v_codes  uint8 [n][num_kv_heads][32][128]  (slot, channel)
+ *   k_meta            uint16 [n][num_kv_heads][256]: INT4 page -> [slot][group]{scale, zero},
+ *                     INT2 page -> [channel]{scale, zero}   (binary16 bits)
+ *   v_meta            uint16 [n][num_kv_heads][256]: [slot][group]{scale, zero}
+ * The four content pointers may all be NULL to export the table only.  Slots
+ * at or past `fill` hold unspecified content. */
+KVQ_API kv_status_t kv_export_request(kv_pool_t* pool, int32_t req_id, int32_t* ids, uint8_t* is_int2, uint8_t* fill,
+                              uint32_t* live, uint8_t* k_codes, uint8_t* v_codes, uint16_t* k_meta,
+                              uint16_t* v_meta);
+
+/* Algorithmic bytes and split count of the most recent kv_decode_attn call:
+ * codes + scale/zero of every page block read (partial INT4 pages count their
+ * filled prefix), 8 bytes per table entry, q (bf16) and out (fp32). */
+KVQ_API kv_status_t kv_last_decode_stats(kv_pool_t* pool, int64_t* kv_bytes, int32_t* n_splits, int64_t* n_pages);
+
+/* Number of kernels this pool has launched so far (host counter). */
+KVQ_API kv_status_t kv_pool_launch_count(kv_pool_t* pool, int64_t* n_launches);
+
+/* Greedy INT2/INT4 bit allocation (TriAxialKV key design 2), host only.
+ * All tags start at 2 bits; tags with N_k > 0 are ranked by
+ * rho_k = (D_k(2) - D_k(4)) / (2 N_k), descending (ties: lower tag first), and
+ * raised to 4 bits whenever sum_k N_k b_k <= (B_num / B_den) sum_k N_k still
+ * holds (a tag that does not fit is skipped).  N, D2, D4: host [n_tags];
+ * bits_out: host uint8 [n_tags]. */
+KVQ_API kv_status_t kv_alloc_bits(const int64_t* N, const double* D2, const double* D4, int32_t n_tags, int64_t B_num,
+                          int64_t B_den, uint8_t* bits_out);
+
+/* Message for the calling thread's most recent failure ("" if none). */
+KVQ_API const char* kv_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */

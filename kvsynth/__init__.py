@@ -59,6 +59,8 @@ def _host_lib():
                                           ctypes.c_uint64, ctypes.c_uint32, ctypes.c_uint32, ctypes.c_int64,
                                           ctypes.c_void_p, ctypes.c_void_p]
             lib.kvs_fill_bf16.restype = None
+            lib.kvs_fill_bf16_heads.argtypes = lib.kvs_fill_bf16.argtypes + [ctypes.c_void_p, ctypes.c_int32]
+            lib.kvs_fill_bf16_heads.restype = None
             lib.kvs_philox_blocks.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64]
             lib.kvs_philox_blocks.restype = None
             _host = lib
@@ -90,6 +92,17 @@ def fill_bf16_host(n_tok, H, D, seed, tensor, stream, tok0=0, chan_mult=None, ro
     cm = None if chan_mult is None else np.ascontiguousarray(chan_mult, dtype=np.float32)
     rm = None if row_mult is None else np.ascontiguousarray(row_mult, dtype=np.float32)
     _host_lib().kvs_fill_bf16(_ptr(out), n_tok, H, D, seed, tensor, stream, tok0, _ptr(cm), _ptr(rm))
+    return out
+
+
+def fill_bf16_host_heads(n_tok, H, D, seed, tensor, stream, heads, tok0=0, chan_mult=None, row_mult=None):
+    """Like fill_bf16_host but only for the listed heads: shape [n_tok][len(heads)][D]."""
+    heads = np.ascontiguousarray(heads, dtype=np.int32)
+    out = np.empty((n_tok, heads.size, D), dtype=np.uint16)
+    cm = None if chan_mult is None else np.ascontiguousarray(chan_mult, dtype=np.float32)
+    rm = None if row_mult is None else np.ascontiguousarray(row_mult, dtype=np.float32)
+    _host_lib().kvs_fill_bf16_heads(_ptr(out), n_tok, H, D, seed, tensor, stream, tok0, _ptr(cm), _ptr(rm),
+                                    _ptr(heads), heads.size)
     return out
 
 

@@ -1,0 +1,237 @@
+// CUDA-core decode kernel (reference / ablation path) and the split merge.
+//
+// Each CTA scans one split (a run of pages of one (batch row, kv head) unit,
+// all of one precision after the INT2-first reorder -- TriAxialKV key design
+// 4).  A warp takes one page at a time: it copies the page block to shared
+// memory, dequantizes K with fmaf(code, scale, zero) and forms the logits of
+// the g packed query heads (HyQuant Algorithm 3, GQA packing), updates the
+// online softmax state (m, l, acc) and accumulates P.V with dequantized V.
+// Dead slots (evicted or never written) take the sentinel logit -1e4 and V = 0
+// (IntentKV, sentinel dead slot).  The warps of a CTA are merged in shared
+// memory and the split's (m, l, acc) is written; a second kernel merges splits
+// with log-sum-exp (HyQuant ReduceSoftmax; TriAxialKV global LSE reduce).
+// Softmax runs in base 2: logits are pre-multiplied by log2(e).
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "kvq_internal.h"
+
+namespace kvq {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kPartStride = kHeadDim + 4;   // acc[128], m, l, 2 pad: rows stay 16-byte aligned
+constexpr float kDeadLogit2 = -1.0e4f * 1.4426950408889634f;   // -1e4 in base-2 units
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xFFFFFFFFu, x, o));
+  return x;
+}
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
+  return x;
+}
+__device__ __forceinline__ float ld_half(const uint8_t* p) {
+  return __half2float(*reinterpret_cast<const __half*>(p));
+}
+
+template <int G>
+__global__ void __launch_bounds__(kThreads) decode_simt_kernel(
+    const uint8_t* __restrict__ pool, size_t int4_off, int64_t n2, int hkv, int max_pages,
+    const Entry* __restrict__ table, const __nv_bfloat16* __restrict__ q, int hq, float scale_log2,
+    const Unit* __restrict__ units, const Split* __restrict__ splits, float* __restrict__ part) {
+  __shared__ float qs[G][kHeadDim];
+  __shared__ __align__(16) uint8_t buf[kWarps][kInt4Block];
+  __shared__ float pb[kWarps][kPage][G];
+  __shared__ float wm[kWarps][G], wl[kWarps][G];
+
+  const Split sp = splits[blockIdx.x];
+  const Unit u = units[sp.unit];
+  for (int i = threadIdx.x; i < G * kHeadDim; i += kThreads) {
+    const int h = i / kHeadDim, c = i % kHeadDim;
+    qs[h][c] = __bfloat162float(q[((size_t)u.b * hq + (size_t)u.kvh * G + h) * kHeadDim + c]);
+  }
+  __syncthreads();
+
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float m[G], l[G], acc[G][4];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    m[h] = -INFINITY;
+    l[h] = 0.0f;
+#pragma unroll
+    for (int a = 0; a < 4; ++a) acc[h][a] = 0.0f;
+  }
+  const Entry* tab = table + (size_t)u.req * max_pages;
+  uint8_t* bw = buf[w];
+  for (int pi = sp.page_begin + w; pi < sp.page_end; pi += kWarps) {
+    const Entry e = tab[pi];
+    const bool i2 = e.id < n2;
+    const uint8_t* blk = i2 ? pool + ((size_t)e.id * hkv + u.kvh) * kInt2Block
+                            : pool + int4_off + ((size_t)(e.id - n2) * hkv + u.kvh) * kInt4Block;
+    const int nbytes = i2 ? kInt2Block : kInt4Block;
+    for (int o = lane * 16; o < nbytes; o += 512)
+      *reinterpret_cast<uint4*>(bw + o) = *reinterpret_cast<const uint4*>(blk + o);
+    __syncwarp();
+
+    // ---- logits: lane = slot
+    const int t = lane;
+    float s[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) s[h] = 0.0f;
+    if (i2) {
+      for (int c = 0; c < kHeadDim; ++c) {
+        const uint32_t code = (bw[i2k_byte(t, c)] >> i2k_shift(c)) & 3u;
+        const int mi = i2k_meta_index(c);
+        const float kh = __fmaf_rn((float)code, ld_half(bw + kI2KMeta + 2 * mi), ld_half(bw + kI2KMeta + 256 + 2 * mi));
+#pragma unroll
+        for (int h = 0; h < G; ++h) s[h] = __fmaf_rn(qs[h][c], kh, s[h]);
+      }
+    } else {
+      for (int gr = 0; gr < 4; ++gr) {
+        const float sf = ld_half(bw + kI4KMeta + 16 * t + 4 * gr);
+        const float zf = ld_half(bw + kI4KMeta + 16 * t + 4 * gr + 2);
+        for (int cc = 0; cc < kGroup; ++cc) {
+          const int c = kGroup * gr + cc;
+          const uint32_t code = (bw[i4k_byte(t, c)] >> i4k_shift(c)) & 15u;
+          const float kh = __fmaf_rn((float)code, sf, zf);
+#pragma unroll
+          for (int h = 0; h < G; ++h) s[h] = __fmaf_rn(qs[h][c], kh, s[h]);
+        }
+      }
+    }
+    const bool alive = (e.live >> t) & 1u;
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const float lg = alive ? s[h] * scale_log2 : kDeadLogit2;
+      const float mnew = fmaxf(m[h], warp_max(lg));
+      const float corr = exp2f(m[h] - mnew);
+      const float p = exp2f(lg - mnew);
+      l[h] = l[h] * corr + warp_sum(p);
+      m[h] = mnew;
+      pb[w][t][h] = alive ? p : 0.0f;
+#pragma unroll
+      for (int a = 0; a < 4; ++a) acc[h][a] *= corr;
+    }
+    __syncwarp();
+
+    // ---- P.V: lane owns channels 4*lane .. 4*lane+3 (one group)
+    const int gr = lane >> 3;
+    const int vmeta = i2 ? kI2VMeta : kI4VMeta;
+    for (int t2 = 0; t2 < kPage; ++t2) {
+      const int mi = v_meta_index(t2, gr);
+      const float sf = ld_half(bw + vmeta + 2 * mi), zf = ld_half(bw + vmeta + 256 + 2 * mi);
+#pragma unroll
+      for (int a = 0; a < 4; ++a) {
+        const int c = 4 * lane + a;
+        const uint32_t code = i2 ? (bw[i2v_byte(t2, c)] >> i2v_shift(t2)) & 3u
+                                 : (bw[i4v_byte(t2, c)] >> i4v_shift(t2)) & 15u;
+        const float vh = __fmaf_rn((float)code, sf, zf);
+#pragma unroll
+        for (int h = 0; h < G; ++h) acc[h][a] = __fmaf_rn(pb[w][t2][h], vh, acc[h][a]);
+      }
+    }
+    __syncwarp();
+  }
+
+  // ---- merge the warps of this CTA
+  if (lane == 0) {
+#pragma unroll
+    for (int h = 0; h < G; ++h) { wm[w][h] = m[h]; wl[w][h] = l[h]; }
+  }
+  __syncthreads();
+  float* ab = reinterpret_cast<float*>(&buf[0][0]);   // [kWarps][G][128]
+#pragma unroll
+  for (int h = 0; h < G; ++h)
+#pragma unroll
+    for (int a = 0; a < 4; ++a) ab[(w * G + h) * kHeadDim + 4 * lane + a] = acc[h][a];
+  __syncthreads();
+  float* out = part + (size_t)blockIdx.x * G * kPartStride;
+  const int c = threadIdx.x;
+  for (int h = 0; h < G; ++h) {
+    float M = -INFINITY;
+    for (int ww = 0; ww < kWarps; ++ww) M = fmaxf(M, wm[ww][h]);
+    float L = 0.0f, A = 0.0f;
+    for (int ww = 0; ww < kWarps; ++ww) {
+      if (wm[ww][h] == -INFINITY) continue;
+      const float f = exp2f(wm[ww][h] - M);
+      L += wl[ww][h] * f;
+      A += ab[(ww * G + h) * kHeadDim + c] * f;
+    }
+    out[h * kPartStride + c] = A;
+    if (c == 0) {
+      out[h * kPartStride + kHeadDim] = M;
+      out[h * kPartStride + kHeadDim + 1] = L;
+    }
+  }
+}
+
+// One warp per (unit, head): O = sum_s acc_s 2^(m_s - M) / sum_s l_s 2^(m_s - M).
+template <int G>
+__global__ void merge_kernel(const Unit* __restrict__ units, const float* __restrict__ part, int hq,
+                             float* __restrict__ out) {
+  const Unit u = units[blockIdx.x];
+  const int h = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float* o = out + ((size_t)u.b * hq + (size_t)u.kvh * G + h) * kHeadDim + 4 * lane;
+  float M = -INFINITY;
+  for (int s = 0; s < u.n_splits; ++s)
+    M = fmaxf(M, part[((size_t)(u.split_begin + s) * G + h) * kPartStride + kHeadDim]);
+  float L = 0.0f, A[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  for (int s = 0; s < u.n_splits; ++s) {
+    const float* ps = part + ((size_t)(u.split_begin + s) * G + h) * kPartStride;
+    const float f = exp2f(ps[kHeadDim] - M);
+    L += ps[kHeadDim + 1] * f;
+    const float4 a = *reinterpret_cast<const float4*>(ps + 4 * lane);
+    A[0] += a.x * f; A[1] += a.y * f; A[2] += a.z * f; A[3] += a.w * f;
+  }
+  const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+  *reinterpret_cast<float4*>(o) = make_float4(A[0] * inv, A[1] * inv, A[2] * inv, A[3] * inv);
+}
+
+template <int G>
+cudaError_t launch_g(kv_pool* P, const void* q, int32_t hq, float scale_log2, const Unit* d_units, int n_units,
+                     const Split* d_splits, int n_splits, float* d_part, float* out, cudaStream_t s) {
+  P->launches += n_splits > 0 ? 2 : 1;
+  if (n_splits > 0)
+    decode_simt_kernel<G><<<n_splits, kThreads, 0, s>>>(
+        P->d_pool, P->int4_offset, P->cfg.n_int2_pages, P->cfg.num_kv_heads, P->cfg.max_pages_per_request,
+        P->d_table, (const __nv_bfloat16*)q, hq, scale_log2, d_units, d_splits, d_part);
+  merge_kernel<G><<<n_units, 32 * G, 0, s>>>(d_units, d_part, hq, out);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode_simt(kv_pool* P, const void* q, int32_t hq, float scale_log2, const Unit* d_units,
+                               int n_units, const Split* d_splits, int n_splits, float* d_part, float* out,
+                               cudaStream_t s) {
+  switch (hq / P->cfg.num_kv_heads) {
+    case 1: return launch_g<1>(P, q, hq, scale_log2, d_units, n_units, d_splits, n_splits, d_part, out, s);
+    case 2: return launch_g<2>(P, q, hq, scale_log2, d_units, n_units, d_splits, n_splits, d_part, out, s);
+    case 3: return launch_g<3>(P, q, hq, scale_log2, d_units, n_units, d_splits, n_splits, d_part, out, s);
+    case 4: return launch_g<4>(P, q, hq, scale_log2, d_units, n_units, d_splits, n_splits, d_part, out, s);
+    case 5: return launch_g<5>(P, q, hq, scale_log2, d_units, n_units, d_splits, n_splits, d_part, out, s);
+    case 6: return launch_g<6>(P, q, hq, scale_log2, d_units, n_units, d_splits, n_splits, d_part, out, s);
+    case 7: return launch_g<7>(P, q, hq, scale_log2, d_units, n_units, d_splits, n_splits, d_part, out, s);
+    case 8: return launch_g<8>(P, q, hq, scale_log2, d_units, n_units, d_splits, n_splits, d_part, out, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+int decode_simt_ctas_per_sm(int g) {
+  int n = 0;
+  cudaError_t e;
+  switch (g) {
+    case 1: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_simt_kernel<1>, kThreads, 0); break;
+    case 2: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_simt_kernel<2>, kThreads, 0); break;
+    case 4: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_simt_kernel<4>, kThreads, 0); break;
+    case 8: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_simt_kernel<8>, kThreads, 0); break;
+    default: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_simt_kernel<4>, kThreads, 0); break;
+  }
+  return (e == cudaSuccess && n > 0) ? n : 1;
+}
+
+}  // namespace kvq

@@ -1,0 +1,127 @@
+// Internal state of a kv_pool_t and the launch interfaces shared by the
+// library's translation units.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <set>
+#include <string>
+#include <vector>
+
+#include "../../include/kvq.h"
+#include "kvq_layout.cuh"
+
+namespace kvq {
+
+// Device status word bits (OR-ed by kernels, read and cleared by kv_pool_sync).
+constexpr uint32_t kStatusRange = 1u;
+constexpr uint32_t kStatusTimeout = 2u;
+
+// One table entry as the kernels read it.
+struct Entry {
+  int32_t id;
+  uint32_t live;
+};
+
+// Host -> device table update, applied by a scatter kernel.
+struct TableUpd {
+  uint32_t index;   // kind 0: flat entry index r * max_pages + i; kind 1: request r
+  int32_t a;        // kind 0: page id; kind 1: table length
+  uint32_t b;       // kind 0: live mask
+  uint32_t kind;
+};
+
+// Append job: one destination page and the tokens written into it this call.
+struct AppendJob {
+  int32_t page;        // INT4 page id (absolute)
+  int32_t first_slot;  // slot of the first token of this job
+  int32_t n_slots;     // tokens written by this job
+  int32_t tok_off;     // offset into the token index list
+};
+
+struct RepackJob {
+  int32_t src;  // INT4 staging page id
+  int32_t dst;  // INT2 page id
+};
+
+// Work unit of the decode: one (batch row, kv head); splits are page ranges.
+struct Unit {
+  int32_t b;            // batch row
+  int32_t req;          // request id
+  int32_t kvh;          // kv head
+  int32_t split_begin;  // first split of this unit
+  int32_t n_splits;     // number of splits (0 = no tokens)
+  int32_t pad[3];
+};
+
+struct Split {
+  int32_t unit;
+  int32_t page_begin;   // table index range [page_begin, page_end)
+  int32_t page_end;
+  int32_t is_int2;
+};
+
+struct Request {
+  bool open = false;
+  std::vector<int32_t> table;       // page ids in table order
+  int32_t tail4 = -1, staging = -1;
+  std::vector<uint32_t> loc;        // token position -> page_id << 5 | slot
+  uint64_t version = 0;             // bumped whenever the table's entries change
+};
+
+// A device buffer that grows geometrically (contents not preserved).
+struct DevBuf {
+  void* ptr = nullptr;
+  size_t cap = 0;
+};
+
+}  // namespace kvq
+
+struct kv_pool {
+  kv_pool_config_t cfg;
+  int sm_count = 0;
+  // device memory
+  uint8_t* d_pool = nullptr;          // INT2 region then INT4 region
+  size_t pool_bytes = 0;
+  size_t int4_offset = 0;             // byte offset of the INT4 region
+  kvq::Entry* d_table = nullptr;      // [max_requests][max_pages]
+  int32_t* d_ntab = nullptr;          // [max_requests]
+  uint32_t* d_status = nullptr;       // device status word
+  kvq::DevBuf upload;                 // append/scatter job arrays
+  kvq::DevBuf plan;                   // decode plan (units, splits)
+  kvq::DevBuf partials;               // decode split partials
+  // host mirror
+  std::vector<kvq::Request> reqs;
+  std::vector<uint8_t> fill;          // per page id
+  std::vector<uint32_t> live;         // per page id
+  std::vector<int32_t> pos;           // per page id x 32 slots: token position
+  std::set<int32_t> free2, free4;
+  // decode plan cache
+  std::vector<int32_t> plan_req;
+  std::vector<uint64_t> plan_ver;
+  int32_t plan_hq = 0;
+  int32_t plan_impl = -1;
+  int32_t n_units = 0, n_splits = 0;
+  size_t plan_units_off = 0, plan_splits_off = 0;
+  std::vector<int32_t> stat_req;      // request ids of the last decode (for kv_last_decode_stats)
+  int32_t stat_hq = 0;
+  int32_t decode_impl = KV_DECODE_AUTO;
+  cudaStream_t last_stream = nullptr;
+  int64_t launches = 0;               // kernels launched by this pool
+};
+
+namespace kvq {
+
+// Launchers (kvq_quant.cu)
+cudaError_t launch_append(kv_pool* P, const void* k, const void* v, const AppendJob* d_jobs, int n_jobs,
+                          const int32_t* d_toks, cudaStream_t s);
+cudaError_t launch_repack(kv_pool* P, const RepackJob* d_jobs, int n_jobs, cudaStream_t s);
+cudaError_t launch_scatter(kv_pool* P, const TableUpd* d_upd, int n, cudaStream_t s);
+
+// Launchers (kvq_decode_simt.cu / kvq_decode_mma.cu)
+cudaError_t launch_decode_simt(kv_pool* P, const void* q, int32_t hq, float scale_log2, const Unit* d_units,
+                               int n_units, const Split* d_splits, int n_splits, float* d_part, float* out,
+                               cudaStream_t s);
+int decode_simt_ctas_per_sm(int g);
+
+}  // namespace kvq

@@ -1,0 +1,97 @@
+// Physical byte layout of one (page, kv head) block.  Private to the library:
+// kv_export_request() converts it to the canonical (slot, channel) form.
+//
+// The layout is chosen for the tensor-core decode kernel's fragment ownership
+// (mma.m16n8k16, lane = 4*r + i): every lane reads its codes with 16-byte
+// shared-memory loads that hit 8 distinct 16-byte bank groups per quarter
+// warp, and one 32-bit code word unpacks into whole A-fragment registers with
+// masks alone (codes become binary16 subnormals code * 2^-24).
+//
+// INT4 block (5120 B)
+//   [   0, 2048) K codes: slot t row at 64*t; row = 4 chunks (i) x 4 groups
+//                (gr) x 4 bytes; channel c = 32*gr + 8*i + n sits in nibble n
+//                (bits 4n..4n+3) of word (i, gr).
+//   [2048, 4096) V codes, channel-major: word (channel c, slot chunk j) holds
+//                slots 8j..8j+7 in nibbles 0..7; it sits at 16-byte chunk
+//                32*((c>>2)&3) + 4*(c>>4) + j, word c&3 inside the chunk.
+//   [4096, 4608) K scale/zero: [slot][group] half2 {scale, zero}.
+//   [4608, 5120) V scale/zero: scales [group][32] half then zeros [group][32]
+//                half, slot order inside each 8-slot chunk j permuted so that
+//                position 2k holds slot 8j+k and 2k+1 holds slot 8j+k+4.
+// INT2 block (3072 B)
+//   [   0, 1024) K codes: slot t row at 32*t; channel c at byte c>>2, bits
+//                2*(c&3).
+//   [1024, 2048) V codes, channel-major: word (r, m, i) holds channels
+//                16r+2m (bytes 0, 2) and 16r+2m+1 (bytes 1, 3) for slot chunk
+//                i: byte 0/1 hold slots 8i..8i+3, bytes 2/3 slots 8i+4..8i+7,
+//                slot 8i+k at bits 2k of its byte.  The word sits at 16-byte
+//                chunk 32*(m>>2) + 4*r + i, word m&3 inside the chunk.
+//   [2048, 2560) K scales: 128 halves in pair order, then zeros in the same
+//                order.  Pair p = (i*2 + wi)*8 + j holds the channels that
+//                A-register j of code word (chunk i, word wi) carries: low half
+//                = channel 4*(8i + 4wi + (j>>2)) + (j&3), high half = that + 8.
+//   [2560, 3072) V scale/zero: as in the INT4 block.
+#pragma once
+#include <stdint.h>
+
+#ifdef __CUDACC__
+#define KVQ_HD __host__ __device__ __forceinline__
+#else
+#define KVQ_HD inline
+#endif
+
+namespace kvq {
+
+constexpr int kHeadDim = 128;
+constexpr int kPage = 32;
+constexpr int kGroup = 32;
+constexpr int kInt4Block = 5120;
+constexpr int kInt2Block = 3072;
+
+// INT4 block offsets
+constexpr int kI4KCodes = 0, kI4VCodes = 2048, kI4KMeta = 4096, kI4VMeta = 4608;
+// INT2 block offsets
+constexpr int kI2KCodes = 0, kI2VCodes = 1024, kI2KMeta = 2048, kI2VMeta = 2560;
+
+// ---- INT4 K codes: byte offset and nibble of (slot, channel)
+KVQ_HD int i4k_byte(int t, int c) {
+  const int gr = c >> 5, i = (c >> 3) & 3, n = c & 7;
+  return kI4KCodes + 64 * t + 16 * i + 4 * gr + (n >> 1);
+}
+KVQ_HD int i4k_shift(int c) { return 4 * (c & 1); }
+
+// ---- INT4 V codes
+KVQ_HD int i4v_byte(int t, int c) {
+  const int j = t >> 3, n = t & 7;
+  return kI4VCodes + 16 * (32 * ((c >> 2) & 3) + 4 * (c >> 4) + j) + 4 * (c & 3) + (n >> 1);
+}
+KVQ_HD int i4v_shift(int t) { return 4 * (t & 1); }
+
+// ---- INT2 K codes
+KVQ_HD int i2k_byte(int t, int c) { return kI2KCodes + 32 * t + (c >> 2); }
+KVQ_HD int i2k_shift(int c) { return 2 * (c & 3); }
+
+// ---- INT2 V codes
+KVQ_HD int i2v_byte(int t, int c) {
+  const int r = c >> 4, m = (c >> 1) & 7, e = c & 1;
+  const int i = t >> 3, k = t & 7;
+  return kI2VCodes + 16 * (32 * (m >> 2) + 4 * r + i) + 4 * (m & 3) + e + 2 * (k >> 2);
+}
+KVQ_HD int i2v_shift(int t) { return 2 * (t & 3); }
+
+// ---- INT2 K scale/zero: half index (0..127) of channel c in the pair order
+KVQ_HD int i2k_meta_index(int c) {
+  const int i = c >> 5, wi = (c >> 4) & 1, b = (c >> 2) & 3, pos = c & 3;
+  const int j = (b & 1) * 4 + pos;      // bytes 0,2 -> regs 0..3; bytes 1,3 -> regs 4..7
+  const int hi = b >> 1;                // bytes 2,3 are the high half
+  return 2 * ((i * 2 + wi) * 8 + j) + hi;
+}
+
+// ---- V scale/zero (both widths): half index (0..127) of (slot, group)
+KVQ_HD int v_meta_index(int t, int gr) {
+  const int j = t >> 3, k = t & 7;
+  const int pos = (k < 4) ? 2 * k : 2 * (k - 4) + 1;
+  return 32 * gr + 8 * j + pos;
+}
+
+}  // namespace kvq

@@ -1,0 +1,701 @@
+// Host side of the C ABI: pool and request management, deterministic page
+// allocation, token routing (INT4 tail / INT4 staging -> INT2 repack), INT2-
+// first reorder, eviction, export, the decode split planner and the decode
+// dispatch.  Every device step runs in the kernels of kvq_quant.cu and
+// kvq_decode_*.cu; this file only decides what they do.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <climits>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <unordered_map>
+#include <utility>
+#include <vector>
+
+#include "kvq_internal.h"
+
+using namespace kvq;
+
+namespace {
+
+thread_local std::string g_err;
+
+kv_status_t fail(kv_status_t st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return st;
+}
+
+#define KV_CUDA(call)                                                                       \
+  do {                                                                                      \
+    cudaError_t e_ = (call);                                                                \
+    if (e_ != cudaSuccess) return fail(KV_ERR_CUDA, "%s: %s", #call, cudaGetErrorString(e_)); \
+  } while (0)
+
+// Makes the pool's device current for the duration of a call.
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = true;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    if (prev != dev) ok = cudaSetDevice(dev) == cudaSuccess;
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+bool req_ok(const kv_pool* P, int32_t r) {
+  return r >= 0 && r < P->cfg.max_requests && P->reqs[r].open;
+}
+
+bool is_int2(const kv_pool* P, int32_t id) { return id < P->cfg.n_int2_pages; }
+
+int32_t take_lowest(std::set<int32_t>& s) {
+  const int32_t id = *s.begin();
+  s.erase(s.begin());
+  return id;
+}
+
+// Grow a device buffer to at least `bytes` (contents are not kept).
+kv_status_t ensure(DevBuf& b, size_t bytes) {
+  if (b.cap >= bytes) return KV_OK;
+  size_t cap = std::max<size_t>(bytes, b.cap * 2);
+  cap = (cap + 255) & ~size_t(255);
+  if (b.ptr) {
+    KV_CUDA(cudaDeviceSynchronize());
+    KV_CUDA(cudaFree(b.ptr));
+    b.ptr = nullptr;
+    b.cap = 0;
+  }
+  KV_CUDA(cudaMalloc(&b.ptr, cap));
+  b.cap = cap;
+  return KV_OK;
+}
+
+// Packs several host arrays into one upload (one H2D copy per call).
+struct Upload {
+  std::vector<uint8_t> bytes;
+  size_t add(const void* p, size_t n) {
+    const size_t off = (bytes.size() + 255) & ~size_t(255);
+    bytes.resize(off + n);
+    if (n) std::memcpy(bytes.data() + off, p, n);
+    return off;
+  }
+};
+
+kv_status_t upload(kv_pool* P, const Upload& u, cudaStream_t s) {
+  if (u.bytes.empty()) return KV_OK;
+  kv_status_t st = ensure(P->upload, u.bytes.size());
+  if (st != KV_OK) return st;
+  KV_CUDA(cudaMemcpyAsync(P->upload.ptr, u.bytes.data(), u.bytes.size(), cudaMemcpyHostToDevice, s));
+  return KV_OK;
+}
+
+// Device table rows to rewrite after a call: per request, every entry from
+// `from` to the end plus individually listed entries below it.
+struct Dirty {
+  std::unordered_map<int32_t, int32_t> from;                // request -> first index to rewrite
+  std::unordered_map<int32_t, std::vector<int32_t>> pages;  // request -> page ids whose live mask changed
+  void structural(int32_t r, int32_t idx) {
+    auto it = from.find(r);
+    if (it == from.end()) from[r] = idx; else it->second = std::min(it->second, idx);
+  }
+  void live(int32_t r, int32_t page) { pages[r].push_back(page); }
+};
+
+void emit_updates(const kv_pool* P, const Dirty& d, std::vector<TableUpd>& out) {
+  const uint32_t mp = (uint32_t)P->cfg.max_pages_per_request;
+  std::unordered_map<int32_t, int32_t> f(d.from.begin(), d.from.end());
+  for (const auto& kv : f) {
+    const auto& tb = P->reqs[kv.first].table;
+    for (int32_t i = kv.second; i < (int32_t)tb.size(); ++i)
+      out.push_back(TableUpd{(uint32_t)kv.first * mp + (uint32_t)i, tb[i], P->live[tb[i]], 0u});
+    out.push_back(TableUpd{(uint32_t)kv.first, (int32_t)tb.size(), 0u, 1u});
+  }
+  for (const auto& kv : d.pages) {
+    const auto& tb = P->reqs[kv.first].table;
+    const auto it = f.find(kv.first);
+    const int32_t lim = it == f.end() ? INT_MAX : it->second;
+    std::vector<int32_t> ids = kv.second;
+    std::sort(ids.begin(), ids.end());
+    ids.erase(std::unique(ids.begin(), ids.end()), ids.end());
+    for (int32_t i = 0; i < (int32_t)tb.size() && i < lim; ++i)
+      if (std::binary_search(ids.begin(), ids.end(), tb[i]))
+        out.push_back(TableUpd{(uint32_t)kv.first * mp + (uint32_t)i, tb[i], P->live[tb[i]], 0u});
+  }
+}
+
+// Order this call after the pool's previous work when the stream changes.
+kv_status_t order_after_previous(kv_pool* P, cudaStream_t s) {
+  if (P->last_stream != s && P->last_stream != nullptr) {
+    cudaEvent_t ev;
+    KV_CUDA(cudaEventCreateWithFlags(&ev, cudaEventDisableTiming));
+    KV_CUDA(cudaEventRecord(ev, P->last_stream));
+    KV_CUDA(cudaStreamWaitEvent(s, ev, 0));
+    KV_CUDA(cudaEventDestroy(ev));
+  }
+  P->last_stream = s;
+  return KV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* kv_last_error(void) { return g_err.c_str(); }
+
+kv_status_t kv_alloc_bits(const int64_t* N, const double* D2, const double* D4, int32_t n_tags, int64_t B_num,
+                          int64_t B_den, uint8_t* bits_out) {
+  if (!N || !D2 || !D4 || !bits_out || n_tags <= 0) return fail(KV_ERR_INVALID_ARG, "kv_alloc_bits: bad pointer or n_tags");
+  if (B_den <= 0 || B_num < 0) return fail(KV_ERR_INVALID_ARG, "kv_alloc_bits: budget must be num >= 0, den > 0");
+  int64_t total = 0;
+  for (int32_t k = 0; k < n_tags; ++k) {
+    if (N[k] < 0) return fail(KV_ERR_INVALID_ARG, "kv_alloc_bits: negative count");
+    total += N[k];
+  }
+  // Rank tags by marginal distortion saved per extra bit-token.
+  std::vector<int32_t> idx;
+  std::vector<double> rho(n_tags, 0.0);
+  for (int32_t k = 0; k < n_tags; ++k) {
+    bits_out[k] = 2;
+    if (N[k] > 0) {
+      rho[k] = (D2[k] - D4[k]) / (2.0 * (double)N[k]);
+      idx.push_back(k);
+    }
+  }
+  std::sort(idx.begin(), idx.end(), [&](int32_t a, int32_t b) {
+    return rho[a] != rho[b] ? rho[a] > rho[b] : a < b;
+  });
+  // Integer budget test: (used + 2 N_k) * den <= num * total.
+  int64_t used = 2 * total;
+  for (int32_t k : idx) {
+    if ((used + 2 * N[k]) * B_den <= B_num * total) {
+      bits_out[k] = 4;
+      used += 2 * N[k];
+    }
+  }
+  return KV_OK;
+}
+
+kv_status_t kv_pool_create(const kv_pool_config_t* cfg, kv_pool_t** out) {
+  if (!cfg || !out) return fail(KV_ERR_INVALID_ARG, "kv_pool_create: null argument");
+  *out = nullptr;
+  if (cfg->head_dim != kHeadDim || cfg->page_tokens != kPage || cfg->group != kGroup)
+    return fail(KV_ERR_INVALID_ARG, "kv_pool_create: head_dim, page_tokens and group must be 128, 32, 32");
+  if (cfg->num_kv_heads < 1 || cfg->num_kv_heads > 64)
+    return fail(KV_ERR_INVALID_ARG, "kv_pool_create: num_kv_heads must be in [1, 64]");
+  if (cfg->n_int2_pages < 0 || cfg->n_int4_pages < 1 || cfg->n_int2_pages + cfg->n_int4_pages > (int64_t(1) << 27))
+    return fail(KV_ERR_INVALID_ARG, "kv_pool_create: need n_int4_pages >= 1 and at most 2^27 pages in total");
+  if (cfg->max_requests < 1 || cfg->max_pages_per_request < 1 ||
+      (int64_t)cfg->max_requests * cfg->max_pages_per_request > (int64_t(1) << 32) - 1)
+    return fail(KV_ERR_INVALID_ARG, "kv_pool_create: bad max_requests / max_pages_per_request");
+  int ndev = 0;
+  KV_CUDA(cudaGetDeviceCount(&ndev));
+  if (cfg->device < 0 || cfg->device >= ndev) return fail(KV_ERR_INVALID_ARG, "kv_pool_create: bad device %d", cfg->device);
+  DeviceGuard dg(cfg->device);
+  if (!dg.ok) return fail(KV_ERR_CUDA, "kv_pool_create: cudaSetDevice failed");
+
+  kv_pool* P = new (std::nothrow) kv_pool();
+  if (!P) return fail(KV_ERR_OOM, "kv_pool_create: host allocation failed");
+  P->cfg = *cfg;
+  auto cleanup = [&](kv_status_t st) {
+    cudaFree(P->d_pool);
+    cudaFree(P->d_table);
+    cudaFree(P->d_ntab);
+    cudaFree(P->d_status);
+    delete P;
+    return st;
+  };
+  if (cudaDeviceGetAttribute(&P->sm_count, cudaDevAttrMultiProcessorCount, cfg->device) != cudaSuccess)
+    return cleanup(fail(KV_ERR_CUDA, "kv_pool_create: cannot query SM count"));
+  const size_t hkv = (size_t)cfg->num_kv_heads;
+  P->int4_offset = (size_t)cfg->n_int2_pages * hkv * kInt2Block;
+  P->pool_bytes = P->int4_offset + (size_t)cfg->n_int4_pages * hkv * kInt4Block;
+  if (cudaMalloc(&P->d_pool, P->pool_bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return cleanup(fail(KV_ERR_OOM, "kv_pool_create: cannot allocate %zu bytes of pool", P->pool_bytes));
+  }
+  const size_t tab = (size_t)cfg->max_requests * cfg->max_pages_per_request * sizeof(Entry);
+  if (cudaMalloc(&P->d_table, tab) != cudaSuccess || cudaMalloc(&P->d_ntab, cfg->max_requests * 4) != cudaSuccess ||
+      cudaMalloc(&P->d_status, 4) != cudaSuccess) {
+    cudaGetLastError();
+    return cleanup(fail(KV_ERR_OOM, "kv_pool_create: cannot allocate tables"));
+  }
+  if (cudaMemset(P->d_table, 0xFF, tab) != cudaSuccess || cudaMemset(P->d_ntab, 0, cfg->max_requests * 4) != cudaSuccess ||
+      cudaMemset(P->d_status, 0, 4) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)
+    return cleanup(fail(KV_ERR_CUDA, "kv_pool_create: initialisation failed"));
+  const size_t npages = (size_t)(cfg->n_int2_pages + cfg->n_int4_pages);
+  try {
+    P->reqs.resize(cfg->max_requests);
+    P->fill.assign(npages, 0);
+    P->live.assign(npages, 0);
+    P->pos.assign(npages * kPage, -1);
+    for (int64_t i = 0; i < cfg->n_int2_pages; ++i) P->free2.insert(P->free2.end(), (int32_t)i);
+    for (int64_t i = 0; i < cfg->n_int4_pages; ++i) P->free4.insert(P->free4.end(), (int32_t)(cfg->n_int2_pages + i));
+  } catch (...) {
+    return cleanup(fail(KV_ERR_OOM, "kv_pool_create: host allocation failed"));
+  }
+  *out = P;
+  return KV_OK;
+}
+
+kv_status_t kv_pool_destroy(kv_pool_t* P) {
+  if (!P) return fail(KV_ERR_INVALID_ARG, "kv_pool_destroy: null pool");
+  DeviceGuard dg(P->cfg.device);
+  cudaDeviceSynchronize();
+  cudaFree(P->d_pool);
+  cudaFree(P->d_table);
+  cudaFree(P->d_ntab);
+  cudaFree(P->d_status);
+  cudaFree(P->upload.ptr);
+  cudaFree(P->plan.ptr);
+  cudaFree(P->partials.ptr);
+  delete P;
+  return KV_OK;
+}
+
+kv_status_t kv_request_open(kv_pool_t* P, int32_t* req_id) {
+  if (!P || !req_id) return fail(KV_ERR_INVALID_ARG, "kv_request_open: null argument");
+  for (int32_t r = 0; r < P->cfg.max_requests; ++r)
+    if (!P->reqs[r].open) {
+      const uint64_t v = P->reqs[r].version;
+      P->reqs[r] = Request();
+      P->reqs[r].open = true;
+      P->reqs[r].version = v + 1;
+      *req_id = r;
+      return KV_OK;
+    }
+  return fail(KV_ERR_OOM, "kv_request_open: all %d request slots are open", P->cfg.max_requests);
+}
+
+kv_status_t kv_request_close(kv_pool_t* P, int32_t r) {
+  if (!P || !req_ok(P, r)) return fail(KV_ERR_INVALID_ARG, "kv_request_close: request %d is not open", r);
+  for (int32_t id : P->reqs[r].table) {
+    P->fill[id] = 0;
+    P->live[id] = 0;
+    (is_int2(P, id) ? P->free2 : P->free4).insert(id);
+  }
+  const uint64_t v = P->reqs[r].version;
+  P->reqs[r] = Request();
+  P->reqs[r].version = v + 1;
+  return KV_OK;
+}
+
+kv_status_t kv_request_info(kv_pool_t* P, int32_t r, int32_t* n_pages, int64_t* n_tokens) {
+  if (!P || !req_ok(P, r)) return fail(KV_ERR_INVALID_ARG, "kv_request_info: request %d is not open", r);
+  if (n_pages) *n_pages = (int32_t)P->reqs[r].table.size();
+  if (n_tokens) *n_tokens = (int64_t)P->reqs[r].loc.size();
+  return KV_OK;
+}
+
+kv_status_t kv_set_decode_impl(kv_pool_t* P, int32_t impl) {
+  if (!P || impl < KV_DECODE_AUTO || impl > KV_DECODE_MMA) return fail(KV_ERR_INVALID_ARG, "kv_set_decode_impl: bad impl");
+  P->decode_impl = impl;
+  return KV_OK;
+}
+
+kv_status_t kv_pool_sync(kv_pool_t* P) {
+  if (!P) return fail(KV_ERR_INVALID_ARG, "kv_pool_sync: null pool");
+  DeviceGuard dg(P->cfg.device);
+  if (P->last_stream) KV_CUDA(cudaStreamSynchronize(P->last_stream));
+  KV_CUDA(cudaDeviceSynchronize());
+  uint32_t st = 0;
+  KV_CUDA(cudaMemcpy(&st, P->d_status, 4, cudaMemcpyDeviceToHost));
+  if (st) KV_CUDA(cudaMemset(P->d_status, 0, 4));
+  if (st & kStatusTimeout) return fail(KV_ERR_DEVICE_TIMEOUT, "kv_pool_sync: a bounded device wait expired");
+  if (st & kStatusRange) return fail(KV_ERR_RANGE, "kv_pool_sync: an appended value was NaN, Inf or |x| > 65504");
+  return KV_OK;
+}
+
+}  // extern "C"
+
+extern "C" {
+
+kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const int32_t* req_ids,
+                            const uint8_t* bits, int64_t n_tok, void* stream) {
+  if (!P) return fail(KV_ERR_INVALID_ARG, "kv_append_quant: null pool");
+  if (n_tok < 0 || n_tok > INT32_MAX) return fail(KV_ERR_INVALID_ARG, "kv_append_quant: bad n_tok %lld", (long long)n_tok);
+  if (n_tok == 0) return KV_OK;
+  if (!k || !v || !req_ids || !bits) return fail(KV_ERR_INVALID_ARG, "kv_append_quant: null pointer");
+  for (int64_t t = 0; t < n_tok; ++t) {
+    if (!req_ok(P, req_ids[t])) return fail(KV_ERR_INVALID_ARG, "kv_append_quant: token %lld: request %d not open", (long long)t, req_ids[t]);
+    if (bits[t] != 2 && bits[t] != 4) return fail(KV_ERR_INVALID_ARG, "kv_append_quant: token %lld: bits must be 2 or 4", (long long)t);
+  }
+  // Dry run: pages taken and table growth, so that OOM changes nothing.
+  {
+    struct Sim { bool tail; int tailfill; bool stag; int stagfill; int64_t tablen; };
+    std::unordered_map<int32_t, Sim> sim;
+    int64_t need4 = 0, need2 = 0;
+    for (int64_t t = 0; t < n_tok; ++t) {
+      auto it = sim.find(req_ids[t]);
+      if (it == sim.end()) {
+        const Request& R = P->reqs[req_ids[t]];
+        Sim s{R.tail4 >= 0, R.tail4 >= 0 ? (int)P->fill[R.tail4] : 0, R.staging >= 0,
+              R.staging >= 0 ? (int)P->fill[R.staging] : 0, (int64_t)R.table.size()};
+        it = sim.emplace(req_ids[t], s).first;
+      }
+      Sim& s = it->second;
+      if (bits[t] == 4) {
+        if (!s.tail || s.tailfill == kPage) { ++need4; ++s.tablen; s.tail = true; s.tailfill = 0; }
+        ++s.tailfill;
+      } else {
+        if (!s.stag) { ++need4; ++s.tablen; s.stag = true; s.stagfill = 0; }
+        if (++s.stagfill == kPage) { ++need2; s.stag = false; }
+      }
+      if (s.tablen > P->cfg.max_pages_per_request)
+        return fail(KV_ERR_OOM, "kv_append_quant: request %d would exceed %d table entries", req_ids[t], P->cfg.max_pages_per_request);
+    }
+    if (need4 > (int64_t)P->free4.size() || need2 > (int64_t)P->free2.size())
+      return fail(KV_ERR_OOM, "kv_append_quant: needs %lld INT4 + %lld INT2 pages, %zu + %zu free", (long long)need4,
+                  (long long)need2, P->free4.size(), P->free2.size());
+  }
+  DeviceGuard dg(P->cfg.device);
+  cudaStream_t s = (cudaStream_t)stream;
+  kv_status_t st = order_after_previous(P, s);
+  if (st != KV_OK) return st;
+
+  std::vector<AppendJob> jobs;
+  std::vector<RepackJob> repacks;
+  std::vector<int32_t> tok_job((size_t)n_tok), tok_slot((size_t)n_tok);
+  std::unordered_map<int32_t, int32_t> job_of_page;
+  std::vector<int32_t> deferred;
+  Dirty dirty;
+  for (int64_t t = 0; t < n_tok; ++t) {
+    const int32_t r = req_ids[t];
+    Request& R = P->reqs[r];
+    const int64_t pos = (int64_t)R.loc.size();
+    int32_t& cur = (bits[t] == 4) ? R.tail4 : R.staging;
+    if (cur < 0 || P->fill[cur] == kPage) {
+      cur = take_lowest(P->free4);
+      P->fill[cur] = 0;
+      P->live[cur] = 0;
+      R.table.push_back(cur);
+      dirty.structural(r, (int32_t)R.table.size() - 1);
+      ++R.version;
+    }
+    const int slot = P->fill[cur]++;
+    P->live[cur] |= 1u << slot;
+    P->pos[(size_t)cur * kPage + slot] = (int32_t)pos;
+    R.loc.push_back(((uint32_t)cur << 5) | (uint32_t)slot);
+    dirty.live(r, cur);
+    auto jt = job_of_page.find(cur);
+    if (jt == job_of_page.end()) {
+      jt = job_of_page.emplace(cur, (int32_t)jobs.size()).first;
+      jobs.push_back(AppendJob{cur, slot, 0, 0});
+    }
+    ++jobs[jt->second].n_slots;
+    tok_job[t] = jt->second;
+    tok_slot[t] = slot;
+    if (bits[t] == 2 && P->fill[cur] == kPage) {
+      // 32 qualifying tokens: requantize the staging page into a new INT2 page.
+      const int32_t nid = take_lowest(P->free2);
+      P->fill[nid] = kPage;
+      P->live[nid] = P->live[cur];
+      for (int sl = 0; sl < kPage; ++sl) {
+        const int32_t p = P->pos[(size_t)cur * kPage + sl];
+        P->pos[(size_t)nid * kPage + sl] = p;
+        R.loc[p] = ((uint32_t)nid << 5) | (uint32_t)sl;
+      }
+      auto it = std::find(R.table.begin(), R.table.end(), cur);
+      dirty.structural(r, (int32_t)(it - R.table.begin()));
+      R.table.erase(it);
+      R.table.push_back(nid);
+      repacks.push_back(RepackJob{cur, nid});
+      deferred.push_back(cur);
+      cur = -1;
+      ++R.version;
+    }
+  }
+  int32_t off = 0;
+  for (auto& j : jobs) { j.tok_off = off; off += j.n_slots; }
+  std::vector<int32_t> toks((size_t)n_tok);
+  for (int64_t t = 0; t < n_tok; ++t) {
+    const AppendJob& j = jobs[tok_job[t]];
+    toks[j.tok_off + (tok_slot[t] - j.first_slot)] = (int32_t)t;
+  }
+  for (int32_t id : deferred) {
+    P->fill[id] = 0;
+    P->live[id] = 0;
+    P->free4.insert(id);
+  }
+  std::vector<TableUpd> upd;
+  emit_updates(P, dirty, upd);
+
+  Upload u;
+  const size_t o_jobs = u.add(jobs.data(), jobs.size() * sizeof(AppendJob));
+  const size_t o_toks = u.add(toks.data(), toks.size() * sizeof(int32_t));
+  const size_t o_rep = u.add(repacks.data(), repacks.size() * sizeof(RepackJob));
+  const size_t o_upd = u.add(upd.data(), upd.size() * sizeof(TableUpd));
+  if ((st = upload(P, u, s)) != KV_OK) return st;
+  uint8_t* base = (uint8_t*)P->upload.ptr;
+  KV_CUDA(launch_append(P, k, v, (const AppendJob*)(base + o_jobs), (int)jobs.size(), (const int32_t*)(base + o_toks), s));
+  KV_CUDA(launch_repack(P, (const RepackJob*)(base + o_rep), (int)repacks.size(), s));
+  KV_CUDA(launch_scatter(P, (const TableUpd*)(base + o_upd), (int)upd.size(), s));
+  return KV_OK;
+}
+
+kv_status_t kv_reorder_pages(kv_pool_t* P, const int32_t* req_ids, int32_t n_req, void* stream) {
+  if (!P || n_req < 0 || (n_req > 0 && !req_ids)) return fail(KV_ERR_INVALID_ARG, "kv_reorder_pages: bad arguments");
+  for (int32_t i = 0; i < n_req; ++i)
+    if (!req_ok(P, req_ids[i])) return fail(KV_ERR_INVALID_ARG, "kv_reorder_pages: request %d not open", req_ids[i]);
+  Dirty dirty;
+  for (int32_t i = 0; i < n_req; ++i) {
+    Request& R = P->reqs[req_ids[i]];
+    auto first_int4 = std::find_if(R.table.begin(), R.table.end(), [&](int32_t id) { return !is_int2(P, id); });
+    if (std::find_if(first_int4, R.table.end(), [&](int32_t id) { return is_int2(P, id); }) == R.table.end())
+      continue;   // already INT2-first
+    const int32_t from = (int32_t)(first_int4 - R.table.begin());
+    std::stable_partition(R.table.begin(), R.table.end(), [&](int32_t id) { return is_int2(P, id); });
+    dirty.structural(req_ids[i], from);
+    ++R.version;
+  }
+  if (dirty.from.empty()) return KV_OK;
+  DeviceGuard dg(P->cfg.device);
+  cudaStream_t s = (cudaStream_t)stream;
+  kv_status_t st = order_after_previous(P, s);
+  if (st != KV_OK) return st;
+  std::vector<TableUpd> upd;
+  emit_updates(P, dirty, upd);
+  Upload u;
+  const size_t o = u.add(upd.data(), upd.size() * sizeof(TableUpd));
+  if ((st = upload(P, u, s)) != KV_OK) return st;
+  KV_CUDA(launch_scatter(P, (const TableUpd*)((uint8_t*)P->upload.ptr + o), (int)upd.size(), s));
+  return KV_OK;
+}
+
+kv_status_t kv_evict_slots(kv_pool_t* P, const int32_t* req_ids, const int64_t* token_pos, int64_t n, void* stream) {
+  if (!P || n < 0 || (n > 0 && (!req_ids || !token_pos))) return fail(KV_ERR_INVALID_ARG, "kv_evict_slots: bad arguments");
+  for (int64_t i = 0; i < n; ++i) {
+    if (!req_ok(P, req_ids[i])) return fail(KV_ERR_INVALID_ARG, "kv_evict_slots: request %d not open", req_ids[i]);
+    if (token_pos[i] < 0 || token_pos[i] >= (int64_t)P->reqs[req_ids[i]].loc.size())
+      return fail(KV_ERR_INVALID_ARG, "kv_evict_slots: position %lld out of range", (long long)token_pos[i]);
+  }
+  Dirty dirty;
+  bool any = false;
+  for (int64_t i = 0; i < n; ++i) {
+    const uint32_t l = P->reqs[req_ids[i]].loc[token_pos[i]];
+    const int32_t id = (int32_t)(l >> 5);
+    const uint32_t bit = 1u << (l & 31u);
+    if (P->live[id] & bit) {
+      P->live[id] &= ~bit;
+      dirty.live(req_ids[i], id);
+      any = true;
+    }
+  }
+  if (!any) return KV_OK;
+  DeviceGuard dg(P->cfg.device);
+  cudaStream_t s = (cudaStream_t)stream;
+  kv_status_t st = order_after_previous(P, s);
+  if (st != KV_OK) return st;
+  std::vector<TableUpd> upd;
+  emit_updates(P, dirty, upd);
+  Upload u;
+  const size_t o = u.add(upd.data(), upd.size() * sizeof(TableUpd));
+  if ((st = upload(P, u, s)) != KV_OK) return st;
+  KV_CUDA(launch_scatter(P, (const TableUpd*)((uint8_t*)P->upload.ptr + o), (int)upd.size(), s));
+  return KV_OK;
+}
+
+kv_status_t kv_export_request(kv_pool_t* P, int32_t r, int32_t* ids, uint8_t* is2, uint8_t* fill, uint32_t* live,
+                              uint8_t* kc, uint8_t* vc, uint16_t* km, uint16_t* vm) {
+  if (!P || !req_ok(P, r)) return fail(KV_ERR_INVALID_ARG, "kv_export_request: request %d not open", r);
+  const bool content = kc || vc || km || vm;
+  if (content && !(kc && vc && km && vm)) return fail(KV_ERR_INVALID_ARG, "kv_export_request: pass all four content buffers or none");
+  const auto& tb = P->reqs[r].table;
+  const int hkv = P->cfg.num_kv_heads;
+  for (size_t i = 0; i < tb.size(); ++i) {
+    if (ids) ids[i] = tb[i];
+    if (is2) is2[i] = is_int2(P, tb[i]) ? 1 : 0;
+    if (fill) fill[i] = P->fill[tb[i]];
+    if (live) live[i] = P->live[tb[i]];
+  }
+  if (!content) return KV_OK;
+  kv_status_t st = kv_pool_sync(P);
+  if (st != KV_OK && st != KV_ERR_RANGE) return st;
+  DeviceGuard dg(P->cfg.device);
+  std::vector<uint8_t> raw((size_t)hkv * kInt4Block);
+  for (size_t i = 0; i < tb.size(); ++i) {
+    const int32_t id = tb[i];
+    const bool i2 = is_int2(P, id);
+    const size_t bs = i2 ? kInt2Block : kInt4Block;
+    const uint8_t* src = i2 ? P->d_pool + (size_t)id * hkv * kInt2Block
+                            : P->d_pool + P->int4_offset + (size_t)(id - P->cfg.n_int2_pages) * hkv * kInt4Block;
+    KV_CUDA(cudaMemcpy(raw.data(), src, bs * hkv, cudaMemcpyDeviceToHost));
+    for (int h = 0; h < hkv; ++h) {
+      const uint8_t* b = raw.data() + (size_t)h * bs;
+      const size_t o = (i * hkv + h);
+      uint8_t* kco = kc + o * kPage * kHeadDim;
+      uint8_t* vco = vc + o * kPage * kHeadDim;
+      uint16_t* kmo = km + o * 256;
+      uint16_t* vmo = vm + o * 256;
+      auto h16 = [&](int off) { uint16_t x; std::memcpy(&x, b + off, 2); return x; };
+      for (int t = 0; t < kPage; ++t)
+        for (int c = 0; c < kHeadDim; ++c) {
+          kco[t * kHeadDim + c] = i2 ? (b[i2k_byte(t, c)] >> i2k_shift(c)) & 3 : (b[i4k_byte(t, c)] >> i4k_shift(c)) & 15;
+          vco[t * kHeadDim + c] = i2 ? (b[i2v_byte(t, c)] >> i2v_shift(t)) & 3 : (b[i4v_byte(t, c)] >> i4v_shift(t)) & 15;
+        }
+      const int vbase = i2 ? kI2VMeta : kI4VMeta;
+      for (int t = 0; t < kPage; ++t)
+        for (int gr = 0; gr < 4; ++gr) {
+          vmo[(t * 4 + gr) * 2] = h16(vbase + 2 * v_meta_index(t, gr));
+          vmo[(t * 4 + gr) * 2 + 1] = h16(vbase + 256 + 2 * v_meta_index(t, gr));
+          if (!i2) {
+            kmo[(t * 4 + gr) * 2] = h16(kI4KMeta + 16 * t + 4 * gr);
+            kmo[(t * 4 + gr) * 2 + 1] = h16(kI4KMeta + 16 * t + 4 * gr + 2);
+          }
+        }
+      if (i2)
+        for (int c = 0; c < kHeadDim; ++c) {
+          kmo[c * 2] = h16(kI2KMeta + 2 * i2k_meta_index(c));
+          kmo[c * 2 + 1] = h16(kI2KMeta + 256 + 2 * i2k_meta_index(c));
+        }
+    }
+  }
+  return st;
+}
+
+}  // extern "C"
+
+namespace {
+
+// Split planner (Tangram, AOT load balancing: total CTAs from the occupancy
+// API, each work group's share of them proportional to its bytes).  Units are
+// (batch row, kv head); a unit's table is cut into maximal runs of one
+// precision (after the INT2-first reorder there are at most two), and each run
+// into near-equal page ranges of about total_bytes / (SMs x CTAs per SM)
+// bytes, so every split is pure INT2 or pure INT4 (TriAxialKV key design 4).
+kv_status_t build_plan(kv_pool* P, const int32_t* req_ids, int32_t batch, int32_t hq, int32_t impl,
+                       cudaStream_t s) {
+  const int hkv = P->cfg.num_kv_heads, g = hq / hkv;
+  bool same = P->plan_impl == impl && P->plan_hq == hq && (int32_t)P->plan_req.size() == batch;
+  for (int32_t b = 0; same && b < batch; ++b)
+    same = P->plan_req[b] == req_ids[b] && P->plan_ver[b] == P->reqs[req_ids[b]].version;
+  if (same) return KV_OK;
+
+  const int ctas = decode_simt_ctas_per_sm(g);
+  const double target = (double)P->sm_count * ctas;
+  double total = 0.0;
+  for (int32_t b = 0; b < batch; ++b)
+    for (int32_t id : P->reqs[req_ids[b]].table) total += (is_int2(P, id) ? kInt2Block : kInt4Block) * (double)hkv;
+  const double chunk = std::max(total / target, 8.0 * kInt2Block);
+
+  std::vector<Unit> units;
+  std::vector<Split> splits;
+  units.reserve((size_t)batch * hkv);
+  for (int32_t b = 0; b < batch; ++b) {
+    const auto& tb = P->reqs[req_ids[b]].table;
+    // runs of one precision
+    std::vector<std::pair<int32_t, int32_t>> runs;
+    for (int32_t i = 0; i < (int32_t)tb.size();) {
+      int32_t j = i + 1;
+      while (j < (int32_t)tb.size() && is_int2(P, tb[j]) == is_int2(P, tb[i])) ++j;
+      runs.push_back({i, j});
+      i = j;
+    }
+    for (int h = 0; h < hkv; ++h) {
+      Unit u{};
+      u.b = b;
+      u.req = req_ids[b];
+      u.kvh = h;
+      u.split_begin = (int32_t)splits.size();
+      for (const auto& rn : runs) {
+        const bool i2 = is_int2(P, tb[rn.first]);
+        const int32_t np = rn.second - rn.first;
+        const double bytes = (double)np * (i2 ? kInt2Block : kInt4Block);
+        const int32_t ns = std::max<int32_t>(1, std::min<int32_t>(np, (int32_t)std::ceil(bytes / chunk)));
+        for (int32_t k2 = 0; k2 < ns; ++k2)
+          splits.push_back(Split{(int32_t)units.size(), rn.first + (int32_t)((int64_t)np * k2 / ns),
+                                 rn.first + (int32_t)((int64_t)np * (k2 + 1) / ns), i2 ? 1 : 0});
+      }
+      u.n_splits = (int32_t)splits.size() - u.split_begin;
+      units.push_back(u);
+    }
+  }
+  Upload up;
+  const size_t ou = up.add(units.data(), units.size() * sizeof(Unit));
+  const size_t os = up.add(splits.data(), splits.size() * sizeof(Split));
+  kv_status_t st = ensure(P->plan, up.bytes.size());
+  if (st != KV_OK) return st;
+  KV_CUDA(cudaMemcpyAsync(P->plan.ptr, up.bytes.data(), up.bytes.size(), cudaMemcpyHostToDevice, s));
+  (void)ou;
+  P->plan_units_off = ou;
+  P->plan_splits_off = os;
+  P->n_units = (int32_t)units.size();
+  P->n_splits = (int32_t)splits.size();
+  P->plan_req.assign(req_ids, req_ids + batch);
+  P->plan_ver.resize(batch);
+  for (int32_t b = 0; b < batch; ++b) P->plan_ver[b] = P->reqs[req_ids[b]].version;
+  P->plan_hq = hq;
+  P->plan_impl = impl;
+  return KV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kv_status_t kv_decode_attn(kv_pool_t* P, const void* q, const int32_t* req_ids, int32_t batch, int32_t hq,
+                           float softmax_scale, float* out, void* stream) {
+  if (!P) return fail(KV_ERR_INVALID_ARG, "kv_decode_attn: null pool");
+  if (!q || !out || !req_ids || batch < 1) return fail(KV_ERR_INVALID_ARG, "kv_decode_attn: null pointer or batch < 1");
+  const int hkv = P->cfg.num_kv_heads;
+  if (hq < hkv || hq % hkv != 0 || hq / hkv > 8)
+    return fail(KV_ERR_INVALID_ARG, "kv_decode_attn: num_q_heads %d must be a multiple of %d with ratio <= 8", hq, hkv);
+  if (!std::isfinite(softmax_scale)) return fail(KV_ERR_INVALID_ARG, "kv_decode_attn: softmax_scale must be finite");
+  for (int32_t b = 0; b < batch; ++b)
+    if (!req_ok(P, req_ids[b])) return fail(KV_ERR_INVALID_ARG, "kv_decode_attn: request %d not open", req_ids[b]);
+  int32_t impl = P->decode_impl == KV_DECODE_AUTO ? KV_DECODE_SIMT : P->decode_impl;
+  if (impl == KV_DECODE_MMA) return fail(KV_ERR_STATE, "kv_decode_attn: tensor-core decode not available");
+  DeviceGuard dg(P->cfg.device);
+  cudaStream_t s = (cudaStream_t)stream;
+  kv_status_t st = order_after_previous(P, s);
+  if (st != KV_OK) return st;
+  if ((st = build_plan(P, req_ids, batch, hq, impl, s)) != KV_OK) return st;
+  const int g = hq / hkv;
+  if ((st = ensure(P->partials, (size_t)std::max(P->n_splits, 1) * g * (kHeadDim + 4) * sizeof(float))) != KV_OK)
+    return st;
+  const uint8_t* base = (const uint8_t*)P->plan.ptr;
+  const float scale_log2 = softmax_scale * 1.4426950408889634f;
+  KV_CUDA(launch_decode_simt(P, q, hq, scale_log2, (const Unit*)(base + P->plan_units_off), P->n_units,
+                             (const Split*)(base + P->plan_splits_off), P->n_splits, (float*)P->partials.ptr, out, s));
+  P->stat_req.assign(req_ids, req_ids + batch);
+  P->stat_hq = hq;
+  return KV_OK;
+}
+
+kv_status_t kv_pool_launch_count(kv_pool_t* P, int64_t* n) {
+  if (!P || !n) return fail(KV_ERR_INVALID_ARG, "kv_pool_launch_count: null argument");
+  *n = P->launches;
+  return KV_OK;
+}
+
+kv_status_t kv_last_decode_stats(kv_pool_t* P, int64_t* kv_bytes, int32_t* n_splits, int64_t* n_pages) {
+  if (!P) return fail(KV_ERR_INVALID_ARG, "kv_last_decode_stats: null pool");
+  int64_t bytes = 0, pages = 0;
+  const int64_t hkv = P->cfg.num_kv_heads;
+  for (int32_t r : P->stat_req) {
+    if (!req_ok(P, r)) continue;
+    for (int32_t id : P->reqs[r].table) {
+      bytes += is_int2(P, id) ? (int64_t)kInt2Block * hkv : (int64_t)P->fill[id] * 160 * hkv;
+      bytes += 8;
+      ++pages;
+    }
+    bytes += (int64_t)P->stat_hq * kHeadDim * (2 + 4);
+  }
+  if (kv_bytes) *kv_bytes = bytes;
+  if (n_splits) *n_splits = P->n_splits;
+  if (n_pages) *n_pages = pages * hkv;
+  return KV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,240 @@
+// Quantize-on-append (INT4 tail / staging pages), INT2 repack and table
+// scatter kernels.
+//
+// Quantization follows TriAxialKV, key design 3 (asymmetric group
+// quantization, G = 32): for a group with minimum mn and maximum mx,
+//   scale = half_rn((mx - mn) / (2^b - 1)),  zero = half_rn(mn),
+//   code  = clamp(rint((x - zero) / scale), 0, 2^b - 1)   (0 when scale == 0),
+// with IEEE fp32 subtraction and division (no fast-math, no FTZ) and binary16
+// round-to-nearest-even storage.  INT4 K and V are per token (32 consecutive
+// channels); the INT2 repack dequantizes a full 32-token staging page with
+// fmaf(code, scale, zero) and requantizes K per channel (across the 32 tokens)
+// and V per token.
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+
+#include "kvq_internal.h"
+
+namespace kvq {
+namespace {
+
+constexpr int kThreads = 128;
+
+__device__ __forceinline__ bool out_of_range(float x) { return !(fabsf(x) <= 65504.0f); }
+
+struct GroupMeta {
+  __half s, z;
+  float sf, zf;
+  bool nz;
+};
+
+__device__ __forceinline__ GroupMeta make_meta(float mn, float mx, float qmax) {
+  GroupMeta m;
+  const float s32 = __fdiv_rn(__fsub_rn(mx, mn), qmax);
+  m.s = __float2half_rn(s32);
+  m.z = __float2half_rn(mn);
+  m.sf = __half2float(m.s);
+  m.zf = __half2float(m.z);
+  m.nz = (__half_as_ushort(m.s) & 0x7FFFu) != 0;
+  return m;
+}
+
+__device__ __forceinline__ uint32_t qcode(float x, const GroupMeta& m, float qmax) {
+  if (!m.nz) return 0u;
+  const float u = __fdiv_rn(__fsub_rn(x, m.zf), m.sf);
+  const float r = fminf(fmaxf(rintf(u), 0.0f), qmax);
+  return (uint32_t)r;
+}
+
+// min / max over the 8 lanes of one 32-channel group (lanes 8*gr .. 8*gr + 7)
+__device__ __forceinline__ void group8_minmax(float& mn, float& mx) {
+#pragma unroll
+  for (int o = 1; o < 8; o <<= 1) {
+    mn = fminf(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, o));
+    mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+  }
+}
+
+__device__ __forceinline__ void st_half(uint8_t* img, int byte_off, __half h) {
+  *reinterpret_cast<__half*>(img + byte_off) = h;
+}
+
+__device__ __forceinline__ void or_bits(uint8_t* img, int byte_off, int shift, uint32_t val) {
+  atomicOr(reinterpret_cast<uint32_t*>(img) + (byte_off >> 2), val << (8 * (byte_off & 3) + shift));
+}
+
+// One CTA per (job, kv head): builds the INT4 page image in shared memory and
+// writes the whole 5120-byte block back.  A job starting at slot 0 is the
+// page's first write, so the image starts from zeros (unfilled slots then read
+// as code 0, scale 0, zero 0); later jobs start from the stored block.
+__global__ void __launch_bounds__(kThreads) append_int4_kernel(
+    uint8_t* __restrict__ pool, size_t int4_off, int64_t n2, int hkv, const __nv_bfloat16* __restrict__ k,
+    const __nv_bfloat16* __restrict__ v, const AppendJob* __restrict__ jobs, const int32_t* __restrict__ toks,
+    uint32_t* __restrict__ status) {
+  __shared__ __align__(16) uint8_t img[kInt4Block];
+  const AppendJob job = jobs[blockIdx.x];
+  const int h = blockIdx.y;
+  uint8_t* blk = pool + int4_off + ((size_t)(job.page - n2) * hkv + h) * kInt4Block;
+  uint4* img4 = reinterpret_cast<uint4*>(img);
+  const uint4* blk4 = reinterpret_cast<const uint4*>(blk);
+  for (int i = threadIdx.x; i < kInt4Block / 16; i += kThreads)
+    img4[i] = job.first_slot == 0 ? make_uint4(0, 0, 0, 0) : blk4[i];
+  __syncthreads();
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gr = lane >> 3;
+  bool bad = false;
+  for (int j = warp; j < job.n_slots; j += kThreads / 32) {
+    const int t = toks[job.tok_off + j];
+    const int slot = job.first_slot + j;
+    const size_t row = ((size_t)t * hkv + h) * kHeadDim + 4 * lane;
+    const uint2 kr = *reinterpret_cast<const uint2*>(k + row);
+    const uint2 vr = *reinterpret_cast<const uint2*>(v + row);
+    float xk[4], xv[4];
+    xk[0] = __uint_as_float(kr.x << 16); xk[1] = __uint_as_float(kr.x & 0xFFFF0000u);
+    xk[2] = __uint_as_float(kr.y << 16); xk[3] = __uint_as_float(kr.y & 0xFFFF0000u);
+    xv[0] = __uint_as_float(vr.x << 16); xv[1] = __uint_as_float(vr.x & 0xFFFF0000u);
+    xv[2] = __uint_as_float(vr.y << 16); xv[3] = __uint_as_float(vr.y & 0xFFFF0000u);
+    float kmn = xk[0], kmx = xk[0], vmn = xv[0], vmx = xv[0];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      bad |= out_of_range(xk[a]) | out_of_range(xv[a]);
+      kmn = fminf(kmn, xk[a]); kmx = fmaxf(kmx, xk[a]);
+      vmn = fminf(vmn, xv[a]); vmx = fmaxf(vmx, xv[a]);
+    }
+    group8_minmax(kmn, kmx);
+    group8_minmax(vmn, vmx);
+    const GroupMeta km = make_meta(kmn, kmx, 15.0f);
+    const GroupMeta vm = make_meta(vmn, vmx, 15.0f);
+    uint32_t ck[4], cv[4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) { ck[a] = qcode(xk[a], km, 15.0f); cv[a] = qcode(xv[a], vm, 15.0f); }
+    // K: channels 4*lane .. 4*lane+3 are nibbles 0..3 or 4..7 of one word -> 2 bytes
+    const int kb = i4k_byte(slot, 4 * lane);
+    *reinterpret_cast<uint16_t*>(img + kb) =
+        (uint16_t)(ck[0] | (ck[1] << 4) | (ck[2] << 8) | (ck[3] << 12));
+    // V: channel-major, one nibble per channel (the block started from zeros)
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      const int c = 4 * lane + a;
+      or_bits(img, i4v_byte(slot, c), i4v_shift(slot), cv[a]);
+    }
+    if ((lane & 7) == 0) {
+      st_half(img, kI4KMeta + 16 * slot + 4 * gr, km.s);
+      st_half(img, kI4KMeta + 16 * slot + 4 * gr + 2, km.z);
+      st_half(img, kI4VMeta + 2 * v_meta_index(slot, gr), vm.s);
+      st_half(img, kI4VMeta + 256 + 2 * v_meta_index(slot, gr), vm.z);
+    }
+  }
+  if (bad) atomicOr(status, kStatusRange);
+  __syncthreads();
+  uint4* out4 = reinterpret_cast<uint4*>(blk);
+  for (int i = threadIdx.x; i < kInt4Block / 16; i += kThreads) out4[i] = img4[i];
+}
+
+// One CTA per (repack job, kv head): INT4 staging block -> INT2 block.
+__global__ void __launch_bounds__(kThreads) repack_int2_kernel(uint8_t* __restrict__ pool, size_t int4_off,
+                                                              int64_t n2, int hkv,
+                                                              const RepackJob* __restrict__ jobs) {
+  __shared__ __align__(16) uint8_t src[kInt4Block];
+  __shared__ __align__(16) uint8_t dst[kInt2Block];
+  const RepackJob job = jobs[blockIdx.x];
+  const int h = blockIdx.y;
+  const uint8_t* sblk = pool + int4_off + ((size_t)(job.src - n2) * hkv + h) * kInt4Block;
+  uint8_t* dblk = pool + ((size_t)job.dst * hkv + h) * kInt2Block;
+  for (int i = threadIdx.x; i < kInt4Block / 16; i += kThreads)
+    reinterpret_cast<uint4*>(src)[i] = reinterpret_cast<const uint4*>(sblk)[i];
+  for (int i = threadIdx.x; i < kInt2Block / 16; i += kThreads)
+    reinterpret_cast<uint4*>(dst)[i] = make_uint4(0, 0, 0, 0);
+  __syncthreads();
+
+  // K: thread c owns channel c; its group is the 32 tokens of the page.
+  {
+    const int c = threadIdx.x;
+    const int gr = c >> 5;
+    float x[kPage];
+    float mn, mx;
+#pragma unroll
+    for (int t = 0; t < kPage; ++t) {
+      const uint32_t code = (src[i4k_byte(t, c)] >> i4k_shift(c)) & 15u;
+      const float sf = __half2float(*reinterpret_cast<const __half*>(src + kI4KMeta + 16 * t + 4 * gr));
+      const float zf = __half2float(*reinterpret_cast<const __half*>(src + kI4KMeta + 16 * t + 4 * gr + 2));
+      x[t] = __fmaf_rn((float)code, sf, zf);
+      mn = t ? fminf(mn, x[t]) : x[t];
+      mx = t ? fmaxf(mx, x[t]) : x[t];
+    }
+    const GroupMeta m = make_meta(mn, mx, 3.0f);
+#pragma unroll
+    for (int t = 0; t < kPage; ++t) or_bits(dst, i2k_byte(t, c), i2k_shift(c), qcode(x[t], m, 3.0f));
+    st_half(dst, kI2KMeta + 2 * i2k_meta_index(c), m.s);
+    st_half(dst, kI2KMeta + 256 + 2 * i2k_meta_index(c), m.z);
+  }
+  // V: thread -> (slot t, group gr), 32 channels each.
+  {
+    const int t = threadIdx.x >> 2, gr = threadIdx.x & 3;
+    const int mi = v_meta_index(t, gr);
+    const float sf = __half2float(*reinterpret_cast<const __half*>(src + kI4VMeta + 2 * mi));
+    const float zf = __half2float(*reinterpret_cast<const __half*>(src + kI4VMeta + 256 + 2 * mi));
+    float x[kGroup];
+    float mn, mx;
+#pragma unroll
+    for (int cc = 0; cc < kGroup; ++cc) {
+      const int c = kGroup * gr + cc;
+      const uint32_t code = (src[i4v_byte(t, c)] >> i4v_shift(t)) & 15u;
+      x[cc] = __fmaf_rn((float)code, sf, zf);
+      mn = cc ? fminf(mn, x[cc]) : x[cc];
+      mx = cc ? fmaxf(mx, x[cc]) : x[cc];
+    }
+    const GroupMeta m = make_meta(mn, mx, 3.0f);
+#pragma unroll
+    for (int cc = 0; cc < kGroup; ++cc) {
+      const int c = kGroup * gr + cc;
+      or_bits(dst, i2v_byte(t, c), i2v_shift(t), qcode(x[cc], m, 3.0f));
+    }
+    st_half(dst, kI2VMeta + 2 * mi, m.s);
+    st_half(dst, kI2VMeta + 256 + 2 * mi, m.z);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < kInt2Block / 16; i += kThreads)
+    reinterpret_cast<uint4*>(dblk)[i] = reinterpret_cast<const uint4*>(dst)[i];
+}
+
+__global__ void scatter_kernel(Entry* __restrict__ table, int32_t* __restrict__ ntab,
+                               const TableUpd* __restrict__ upd, int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const TableUpd u = upd[i];
+  if (u.kind == 0) table[u.index] = Entry{u.a, u.b};
+  else ntab[u.index] = u.a;
+}
+
+}  // namespace
+
+cudaError_t launch_append(kv_pool* P, const void* k, const void* v, const AppendJob* d_jobs, int n_jobs,
+                          const int32_t* d_toks, cudaStream_t s) {
+  if (n_jobs <= 0) return cudaSuccess;
+  dim3 grid((unsigned)n_jobs, (unsigned)P->cfg.num_kv_heads);
+  ++P->launches;
+  append_int4_kernel<<<grid, kThreads, 0, s>>>(P->d_pool, P->int4_offset, P->cfg.n_int2_pages,
+                                               P->cfg.num_kv_heads, (const __nv_bfloat16*)k,
+                                               (const __nv_bfloat16*)v, d_jobs, d_toks, P->d_status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_repack(kv_pool* P, const RepackJob* d_jobs, int n_jobs, cudaStream_t s) {
+  if (n_jobs <= 0) return cudaSuccess;
+  dim3 grid((unsigned)n_jobs, (unsigned)P->cfg.num_kv_heads);
+  ++P->launches;
+  repack_int2_kernel<<<grid, kThreads, 0, s>>>(P->d_pool, P->int4_offset, P->cfg.n_int2_pages,
+                                               P->cfg.num_kv_heads, d_jobs);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scatter(kv_pool* P, const TableUpd* d_upd, int n, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  ++P->launches;
+  scatter_kernel<<<(n + 255) / 256, 256, 0, s>>>(P->d_table, P->d_ntab, d_upd, n);
+  return cudaGetLastError();
+}
+
+}  // namespace kvq

@@ -1,0 +1,121 @@
+"""Drive a KVPool through a synthetic decode workload (kvsynth recipe).
+
+Everything here goes through the public binding: bit allocation with
+``alloc_bits``, prefill and per-step appends with ``KVPool.append``, eviction,
+reorder and decode.  Inputs are generated on the device by kvsynth's
+counter-based generator, so a CPU checker can regenerate any row it samples.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+import kvsynth
+from kvsynth.recipes import Workload, tag_counts
+
+from . import KVPool, alloc_bits
+
+
+def request_bits(w: Workload, r: int, allocator=alloc_bits) -> np.ndarray:
+    """Bit width of every token position of request r (prefill and decode steps)."""
+    spec = w.requests[r]
+    b = allocator(tag_counts(spec.tags[:spec.n_prefill]), w.D2, w.D4, spec.budget)
+    bits = b[spec.tags].astype(np.uint8)
+    if w.force_int4_decode:
+        bits[spec.n_prefill:] = 4
+    return bits
+
+
+def pool_size(w: Workload, bits_list, chunk: int, steps: int):
+    """INT2 / INT4 page counts and table capacity for a workload appended in
+    `chunk`-token calls and then `steps` one-token-per-request calls."""
+    n2 = n4 = max_tab = 0
+    for spec, bits in zip(w.requests, bits_list):
+        total = spec.n_prefill + steps
+        b2 = int((bits[:total] == 2).sum())
+        b4 = total - b2
+        n2 += b2 // 32 + 1
+        n4 += -(-b4 // 32) + 2
+        max_tab = max(max_tab, b2 // 32 + -(-b4 // 32) + 3)
+    # staging pages repacked during one call are freed only when it returns
+    n4 += chunk // 32 + len(w.requests) + 8
+    return n2, n4, max_tab
+
+
+class GPUWorkload:
+    def __init__(self, w: Workload, device: int = 0, chunk: int = 16384, steps: int | None = None):
+        import torch
+        self.w = w
+        self.device = device
+        self.chunk = chunk
+        self.steps = w.steps if steps is None else steps
+        self.bits = [request_bits(w, r) for r in range(len(w.requests))]
+        n2, n4, max_tab = pool_size(w, self.bits, chunk, self.steps)
+        self.pool = KVPool(w.num_kv_heads, n2, n4, len(w.requests), max_tab, device=device)
+        self.rids = [self.pool.open() for _ in w.requests]
+        self.dev = torch.device("cuda", device)
+        self.chan = torch.from_numpy(w.k_chan_mult).to(self.dev)
+        self.row = [None if s.row_mult is None else torch.from_numpy(s.row_mult).to(self.dev) for s in w.requests]
+        self.pos = [0] * len(w.requests)
+
+    def _gen(self, n, tensor, stream, tok0, chan, row):
+        import torch
+        H = self.w.num_kv_heads
+        out = torch.empty((n, H, 128), dtype=torch.bfloat16, device=self.dev)
+        kvsynth.fill_bf16_dev(out.data_ptr(), n, H, 128, self.w.seed, tensor, stream, tok0,
+                              chan.data_ptr() if chan is not None else 0,
+                              row[tok0:tok0 + n].data_ptr() if row is not None else 0,
+                              torch.cuda.current_stream(self.dev).cuda_stream)
+        return out
+
+    def kv_rows(self, r, tok0, n):
+        spec = self.w.requests[r]
+        k = self._gen(n, kvsynth.TENSOR_K, spec.stream, tok0, self.chan, self.row[r])
+        v = self._gen(n, kvsynth.TENSOR_V, spec.stream, tok0, None, self.row[r])
+        return k, v
+
+    def prefill(self):
+        for r, spec in enumerate(self.w.requests):
+            for t0 in range(0, spec.n_prefill, self.chunk):
+                n = min(self.chunk, spec.n_prefill - t0)
+                k, v = self.kv_rows(r, t0, n)
+                self.pool.append(k, v, np.full(n, self.rids[r], np.int32), self.bits[r][t0:t0 + n])
+            self.pos[r] = spec.n_prefill
+
+    def evict(self):
+        for r, spec in enumerate(self.w.requests):
+            if spec.evict.size:
+                self.pool.evict(np.full(spec.evict.size, self.rids[r], np.int32), spec.evict)
+
+    def reorder(self):
+        self.pool.reorder(self.rids)
+
+    def q(self, step: int):
+        import torch
+        Hq = self.w.num_q_heads
+        out = torch.empty((len(self.rids), Hq, 128), dtype=torch.bfloat16, device=self.dev)
+        kvsynth.fill_bf16_dev(out.data_ptr(), len(self.rids), Hq, 128, self.w.seed, kvsynth.TENSOR_Q, step, 0,
+                              0, 0, torch.cuda.current_stream(self.dev).cuda_stream)
+        return out
+
+    def step_inputs(self):
+        """K/V [B][Hkv][128] of the next token of every request, plus its req ids and bits."""
+        import torch
+        ks, vs = [], []
+        for r in range(len(self.rids)):
+            k, v = self.kv_rows(r, self.pos[r], 1)
+            ks.append(k)
+            vs.append(v)
+        bits = np.array([self.bits[r][self.pos[r]] for r in range(len(self.rids))], np.uint8)
+        return torch.cat(ks), torch.cat(vs), np.array(self.rids, np.int32), bits
+
+    def append_step(self, k, v, req_ids, bits):
+        self.pool.append(k, v, req_ids, bits)
+        for r in range(len(self.rids)):
+            self.pos[r] += 1
+
+    def decode(self, q, out=None):
+        return self.pool.decode(q, self.rids, self.w.softmax_scale, out=out)
+
+    def kv_bytes(self) -> int:
+        return self.pool.last_decode_stats()["kv_bytes"]
+

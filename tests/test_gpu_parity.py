@@ -1,0 +1,202 @@
+"""CUDA path vs oracle: codes, scale/zero and page tables bit-exact; attention
+outputs within max-abs 1e-3 and relative-L2 1e-4 of the fp64 oracle."""
+import numpy as np
+import pytest
+
+import kvsynth
+import oracle
+from harness import assert_outputs_close, compare_content, compare_tables
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+SEED = 4242
+SCALE = float(np.float32(1 / np.sqrt(128)))
+
+
+@pytest.fixture(scope="module")
+def kvq():
+    import __graft_entry__
+    __graft_entry__.build()
+    import mixed_precision_kv_gb300 as m
+    m.load_library()
+    return m
+
+
+class Scenario:
+    """Explicit requests (bit sequences, evictions) built on both sides with the
+    same append call boundaries."""
+
+    def __init__(self, kvq, hkv, hq, bits_list, chunk=64, evict=None, n2=None, n4=None, reorder=True,
+                 impl=None, chan_mult=None):
+        self.hkv, self.hq = hkv, hq
+        n_req = len(bits_list)
+        tot2 = sum(int((b == 2).sum()) for b in bits_list)
+        tot4 = sum(int((b == 4).sum()) for b in bits_list)
+        n2 = n2 or tot2 // 32 + 4
+        n4 = n4 or tot4 // 32 + 2 * n_req + chunk // 32 + 8
+        max_tab = max([int((b == 2).sum()) // 32 + int((b == 4).sum()) // 32 + 4 for b in bits_list] + [4])
+        self.gpu = kvq.KVPool(hkv, n2, n4, n_req, max_tab)
+        if impl is not None:
+            self.gpu.set_decode_impl(impl)
+        self.orc = oracle.OraclePool(hkv, n2, n4, n_req, max_tab)
+        self.g_ids = [self.gpu.open() for _ in bits_list]
+        self.o_ids = [self.orc.open() for _ in bits_list]
+        self.cm = chan_mult
+        dev = torch.device("cuda")
+        cm_dev = None if chan_mult is None else torch.from_numpy(chan_mult).to(dev)
+        for r, bits in enumerate(bits_list):
+            n = bits.size
+            for t0 in range(0, n, chunk):
+                m = min(chunk, n - t0)
+                kd = torch.empty((m, hkv, 128), dtype=torch.bfloat16, device=dev)
+                vd = torch.empty((m, hkv, 128), dtype=torch.bfloat16, device=dev)
+                kvsynth.fill_bf16_dev(kd.data_ptr(), m, hkv, 128, SEED, kvsynth.TENSOR_K, r, t0,
+                                      cm_dev.data_ptr() if cm_dev is not None else 0)
+                kvsynth.fill_bf16_dev(vd.data_ptr(), m, hkv, 128, SEED, kvsynth.TENSOR_V, r, t0)
+                kh = kvsynth.fill_bf16_host(m, hkv, 128, SEED, kvsynth.TENSOR_K, r, t0, chan_mult=chan_mult)
+                vh = kvsynth.fill_bf16_host(m, hkv, 128, SEED, kvsynth.TENSOR_V, r, t0)
+                self.gpu.append(kd, vd, np.full(m, self.g_ids[r]), bits[t0:t0 + m])
+                assert self.orc.append(np.full(m, self.o_ids[r]), bits[t0:t0 + m], kh, vh) == oracle.OK
+        if evict:
+            for r, pos in evict.items():
+                self.gpu.evict(np.full(len(pos), self.g_ids[r]), pos)
+                assert self.orc.evict(np.full(len(pos), self.o_ids[r]), pos) == oracle.OK
+        if reorder:
+            self.gpu.reorder(self.g_ids)
+            assert self.orc.reorder(self.o_ids) == oracle.OK
+        self.gpu.sync()
+
+    def check_content(self):
+        for g, o in zip(self.g_ids, self.o_ids):
+            compare_content(self.gpu.export(g), self.orc.export(o), list(range(self.hkv)))
+
+    def check_decode(self, step=0, what=""):
+        B = len(self.g_ids)
+        qd = torch.empty((B, self.hq, 128), dtype=torch.bfloat16, device="cuda")
+        kvsynth.fill_bf16_dev(qd.data_ptr(), B, self.hq, 128, SEED, kvsynth.TENSOR_Q, step)
+        qh = kvsynth.fill_bf16_host(B, self.hq, 128, SEED, kvsynth.TENSOR_Q, step)
+        out = self.gpu.decode(qd, self.g_ids, SCALE)
+        self.gpu.sync()
+        ref = self.orc.decode(qh, self.o_ids, SCALE).reshape(B, self.hq, 128)
+        got = out.cpu().numpy()
+        assert np.isfinite(got).all()
+        return assert_outputs_close(got, ref, what)
+
+
+def _mixed(n, p2, seed):
+    return np.where(np.random.default_rng(seed).random(n) < p2, 2, 4).astype(np.uint8)
+
+
+@pytest.mark.parametrize("n", [1, 2, 31, 32, 33, 63, 64, 65, 200])
+@pytest.mark.parametrize("p2", [0.0, 0.5, 1.0])
+def test_small_requests_codes_tables_outputs(kvq, n, p2):
+    bits = [_mixed(n, p2, n), _mixed(n + 7, p2, n + 1)]
+    sc = Scenario(kvq, 2, 8, bits, chunk=48)
+    sc.check_content()
+    sc.check_decode(what=f"n={n} p2={p2}")
+
+
+@pytest.mark.parametrize("hkv,hq", [(1, 1), (2, 4), (4, 12), (2, 16), (1, 7)])
+def test_gqa_ratios(kvq, hkv, hq):
+    bits = [_mixed(300, 0.6, 1), _mixed(97, 0.3, 2), _mixed(1, 1.0, 3)]
+    sc = Scenario(kvq, hkv, hq, bits, chunk=128)
+    sc.check_content()
+    sc.check_decode(what=f"hkv={hkv} hq={hq}")
+
+
+def test_outlier_channels_and_evictions(kvq):
+    cm = np.ones((2, 128), np.float32)
+    cm[0, [3, 77, 90, 127]] = 20.0
+    cm[1, [0, 31, 32, 64]] = 20.0
+    bits = [_mixed(1000, 0.6, 5), _mixed(640, 0.8, 6)]
+    rng = np.random.default_rng(7)
+    ev = {0: rng.choice(1000, 50, replace=False), 1: rng.choice(640, 32, replace=False)}
+    sc = Scenario(kvq, 2, 8, bits, chunk=256, evict=ev, chan_mult=cm)
+    sc.check_content()
+    sc.check_decode(what="outliers+evict")
+
+
+def test_all_dead_and_empty_requests(kvq):
+    bits = [_mixed(70, 0.5, 8), _mixed(40, 0.5, 9), np.zeros(0, np.uint8)]
+    sc = Scenario(kvq, 2, 8, bits, evict={0: np.arange(70)})
+    out_ref = sc.check_decode(what="all-dead/empty")
+    qd = torch.zeros((3, 8, 128), dtype=torch.bfloat16, device="cuda")
+    out = sc.gpu.decode(qd, sc.g_ids, SCALE).cpu().numpy()
+    assert np.array_equal(out[0], np.zeros((8, 128), np.float32))
+    assert np.array_equal(out[2], np.zeros((8, 128), np.float32))
+    assert out_ref is not None
+
+
+def test_unreordered_tables_and_interleaved_requests(kvq):
+    """Tokens of three requests interleaved in one call; no reorder (mixed runs)."""
+    rng = np.random.default_rng(10)
+    n = 900
+    req = rng.integers(0, 3, n)
+    bits = np.where(rng.random(n) < 0.55, 2, 4).astype(np.uint8)
+    hkv, hq = 2, 8
+    gpu = kvq.KVPool(hkv, 64, 64, 3, 64)
+    orc = oracle.OraclePool(hkv, 64, 64, 3, 64)
+    g = [gpu.open() for _ in range(3)]
+    o = [orc.open() for _ in range(3)]
+    kd = torch.empty((n, hkv, 128), dtype=torch.bfloat16, device="cuda")
+    vd = torch.empty_like(kd)
+    kvsynth.fill_bf16_dev(kd.data_ptr(), n, hkv, 128, SEED, kvsynth.TENSOR_K, 99)
+    kvsynth.fill_bf16_dev(vd.data_ptr(), n, hkv, 128, SEED, kvsynth.TENSOR_V, 99)
+    kh = kvsynth.fill_bf16_host(n, hkv, 128, SEED, kvsynth.TENSOR_K, 99)
+    vh = kvsynth.fill_bf16_host(n, hkv, 128, SEED, kvsynth.TENSOR_V, 99)
+    for a, b in ((0, 400), (400, 900)):
+        gpu.append(kd[a:b], vd[a:b], np.array(g)[req[a:b]], bits[a:b])
+        assert orc.append(np.array(o)[req[a:b]], bits[a:b], kh[a:b], vh[a:b]) == oracle.OK
+    gpu.sync()
+    for gi, oi in zip(g, o):
+        compare_content(gpu.export(gi), orc.export(oi), [0, 1])
+    qd = torch.empty((3, hq, 128), dtype=torch.bfloat16, device="cuda")
+    kvsynth.fill_bf16_dev(qd.data_ptr(), 3, hq, 128, SEED, kvsynth.TENSOR_Q, 0)
+    qh = kvsynth.fill_bf16_host(3, hq, 128, SEED, kvsynth.TENSOR_Q, 0)
+    out = gpu.decode(qd, g, SCALE).cpu().numpy()
+    assert_outputs_close(out, orc.decode(qh, o, SCALE).reshape(3, hq, 128), "interleaved")
+
+
+def test_close_reuse_and_oom_leave_state(kvq):
+    hkv = 1
+    gpu = kvq.KVPool(hkv, 4, 4, 2, 16)
+    orc = oracle.OraclePool(hkv, 4, 4, 2, 16)
+    a, oa = gpu.open(), orc.open()
+    k = torch.zeros((100, hkv, 128), dtype=torch.bfloat16, device="cuda")
+    bits = np.full(100, 4, np.uint8)
+    gpu.append(k, k, np.full(100, a), bits)
+    assert orc.append(np.full(100, oa), bits) == oracle.OK
+    before = gpu.export(a, content=False)
+    with pytest.raises(kvq.KVError) as e:
+        gpu.append(k[:64], k[:64], np.full(64, a), bits[:64])
+    assert e.value.status == kvq.KV_ERR_OOM
+    assert orc.append(np.full(64, oa), bits[:64]) == oracle.OOM
+    compare_tables(gpu.export(a, content=False), before)
+    gpu.close_request(a)
+    orc.close_request(oa)
+    b, ob = gpu.open(), orc.open()
+    gpu.append(k[:33], k[:33], np.full(33, b), np.full(33, 2, np.uint8))
+    assert orc.append(np.full(33, ob), np.full(33, 2, np.uint8)) == oracle.OK
+    compare_tables(gpu.export(b, content=False), orc.export(ob, content=False))
+
+
+def test_range_error_reported_by_sync(kvq):
+    gpu = kvq.KVPool(1, 4, 4, 1, 8)
+    a = gpu.open()
+    k = torch.zeros((3, 1, 128), dtype=torch.bfloat16, device="cuda")
+    k[1, 0, 5] = float("inf")
+    gpu.append(k, torch.zeros_like(k), [a] * 3, [4] * 3)
+    with pytest.raises(kvq.KVError) as e:
+        gpu.sync()
+    assert e.value.status == kvq.KV_ERR_RANGE
+    gpu.sync()   # cleared
+
+
+@pytest.mark.parametrize("p2", [0.0, 1.0, 0.6])
+def test_split_counts_do_not_change_results(kvq, p2):
+    """Long single request: many splits per unit vs the oracle."""
+    bits = [_mixed(20000, p2, 11)]
+    sc = Scenario(kvq, 1, 8, bits, chunk=4096)
+    sc.check_decode(what=f"long p2={p2}")
+    assert sc.gpu.last_decode_stats()["n_splits"] > 1
