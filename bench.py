@@ -184,9 +184,9 @@ def main():
     if ws > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
-    w = kvsynth.make_workload(args.config)
     e2e_steps = max(args.steps // 4, 10)
     total_steps = args.warmup + args.steps + 3 + e2e_steps
+    w = kvsynth.make_workload(args.config, steps=total_steps)
     gw = GPUWorkload(w, device=local, steps=total_steps)
     gw.pool.set_decode_impl({"auto": 0, "simt": 1, "mma": 2}[args.decode_impl])
     gw.prefill()
@@ -232,6 +232,7 @@ def main():
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         torch.cuda.synchronize()
+        torch.cuda.nvtx.range_push("timed")
         start.record(stream)
         for i in range(args.steps):
             s = s0 + i
@@ -243,6 +244,7 @@ def main():
             kv_bytes.append(gw.pool.last_decode_stats()["kv_bytes"])
         end.record(stream)
         torch.cuda.synchronize()
+        torch.cuda.nvtx.range_pop()
     launches = gw.pool.launch_count() - launches0
     gw.pool.sync()
     t_ms = start.elapsed_time(end)
