@@ -1,0 +1,676 @@
+// Tensor-core split decode (mma.sync m16n8k16, fp16 inputs, fp32 accumulate).
+//
+// What it computes is the same as the CUDA-core kernel: per split (a page
+// range of one (batch row, kv head) unit, one precision), the online-softmax
+// state (m, l, acc) of the g packed query heads over dequantized K and V
+// (TriAxialKV key design 4: fused Flash-Decoding with in-kernel dequant;
+// HyQuant Algorithm 3: split-K, GQA query packing, ReduceSoftmax merge), with
+// dead slots at logit -1e4 and V = 0 (IntentKV sentinel dead slot).
+//
+// How it computes it (the arithmetic is regrouped, not changed):
+//  * A code word unpacks into mma A registers with one AND + OR per register
+//    and one f16x2 subtraction: a 2- or 4-bit field at bit position p of a
+//    16-bit half, OR-ed into binary16 1024.0, is 1024 + code * 2^p exactly, and
+//    subtracting 1024 leaves code * 2^p as a normal binary16.  The power 2^p is
+//    compensated in the other operand, so every product is code * operand
+//    exactly.  (Feeding the field directly as a binary16 subnormal would save
+//    the subtraction, but the tensor core aligns products by the exponent
+//    field, so subnormal operands lose about ten bits of the sum.)
+//  * K dot products: s_t = sum_c q_c (scale * code_tc + zero).
+//      INT4 K (per-token groups): per-group accumulators, scale applied per
+//      token in fp32 afterwards, zero term sum_g zero_tg * Q_g by a small mma.
+//      INT2 K (per-channel groups): the channel scale is folded into q as an
+//      exact fp16 pair q*s = hi + lo (hi = rn(q*s), lo = fma(q, s, -hi)); the
+//      zero term sum_c q_c zero_c is one fp32 dot product per page.
+//  * P.V: out_c = sum_t p_t (scale_tg code_tc + zero_tg); p_t * scale_tg is
+//      folded as an fp16 pair (p = p_hi + p_lo, then p_hi*s exactly and p_lo*s
+//      rounded); the zero term sum_t p_t zero_tg is a small mma.
+//  * For g <= 4 the eight N columns carry (hi | lo) of the same four heads,
+//    so one mma does both halves; for g > 4 hi and lo are two mmas into the
+//    same accumulator.
+//  * q is scaled by a power of two per head so that q * scale stays inside
+//    the binary16 range, and P by a power of two so that P * scale stays out
+//    of the subnormal range (the pool tracks the largest INT2 K and V scales).
+// Pages stream through a two-stage per-warp ring filled by cp.async.bulk with
+// mbarrier completion; every wait is bounded and reports a timeout status.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "kvq_internal.h"
+
+namespace kvq {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kStages = 2;
+constexpr int kStageBytes = kInt4Block;
+constexpr int kPartStride = kHeadDim + 4;
+constexpr float kDead2 = -1.0e4f * 1.4426950408889634f;
+constexpr uint32_t kSpinLimit = 1u << 22;
+constexpr uint32_t kSign2 = 0x80008000u;
+constexpr uint32_t kM0 = 0x000F000Fu, kM1 = 0x00F000F0u;   // nibble fields at bits 0 / 4 of each half
+constexpr uint32_t kQ0 = 0x00030003u;                      // 2-bit field at bit 0 of each half
+constexpr uint32_t kMagic = 0x64006400u;                   // binary16 1024.0 in both halves
+
+struct WarpSmem {
+  uint8_t stage[kStages][kStageBytes];
+  float pbuf[8][kPage];                // P staging [head][slot]
+  unsigned long long bar[kStages];
+};
+
+struct CtaSmem {
+  WarpSmem warp[kWarps];
+  float qraw[8][kHeadDim];             // q (fp32) of the packed heads
+  float qz[8][kHeadDim];               // q in the INT2 K scale/zero pair order
+  float acol[8];                       // 2^(-E_h) * scale * log2(e)
+  int eh[8];                           // per-head power-of-two q scale
+  uint32_t bz[8][4];                   // fp16 (hi | lo) of scale*log2(e)*Q_{h,group}
+  float zv[kWarps][4][8];              // V zero-term per warp [group][col]
+  float mw[kWarps][8], lw[kWarps][8];
+};
+
+__device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// A code field OR-ed into the mantissa of binary16 1024.0 gives 1024 + field
+// exactly; subtracting 1024 leaves the field as a normal binary16 (or zero).
+__device__ __forceinline__ uint32_t unmagic(uint32_t x) {
+  uint32_t d;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(x | kMagic), "r"(kMagic));
+  return d;
+}
+__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+// pack two floats as binary16 (round to nearest even): lo -> bits 0..15
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+__device__ __forceinline__ float h_lo(uint32_t x) { return __half2float(__ushort_as_half((unsigned short)(x & 0xFFFFu))); }
+__device__ __forceinline__ float h_hi(uint32_t x) { return __half2float(__ushort_as_half((unsigned short)(x >> 16))); }
+__device__ __forceinline__ uint32_t comp(const uint4& v, int k) {
+  return k == 0 ? v.x : (k == 1 ? v.y : (k == 2 ? v.z : v.w));
+}
+// exact fp16 pair of the fp32 product x: hi = rn16(x), lo = rn16(x - hi)
+__device__ __forceinline__ void split_f16(float x, unsigned short& hi, unsigned short& lo) {
+  const __half h = __float2half_rn(x);
+  hi = __half_as_ushort(h);
+  lo = __half_as_ushort(__float2half_rn(x - __half2float(h)));
+}
+
+// ---- bulk copy + mbarrier (bounded waits) --------------------------------
+__device__ __forceinline__ void bar_init(unsigned long long* b) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(b)) : "memory");
+}
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, unsigned long long* b) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(b)), "r"(bytes) : "memory");
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(su32(dst)), "l"(src), "r"(bytes), "r"(su32(b)) : "memory");
+}
+__device__ __forceinline__ bool bar_try(unsigned long long* b, uint32_t phase) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok) : "r"(su32(b)), "r"(phase) : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool bar_wait(unsigned long long* b, uint32_t phase) {
+  for (uint32_t it = 0; it < kSpinLimit; ++it)
+    if (bar_try(b, phase)) return true;
+  return false;
+}
+
+// ---- logits of one INT4 page: lg[m][c] for tokens 16m + r + 8(c>>1), heads 2i + (c&1)
+template <int G>
+__device__ __forceinline__ void qk_int4(const uint8_t* blk, const uint32_t (&bq)[16], uint32_t bzl, int r, int i,
+                                        const float (&acol)[2], float (&lg)[2][4]) {
+#pragma unroll
+  for (int m = 0; m < 2; ++m) {
+    uint4 kw[2], km[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int t = 16 * m + r + 8 * e;
+      kw[e] = *reinterpret_cast<const uint4*>(blk + kI4KCodes + 64 * t + 16 * i);
+      km[e] = *reinterpret_cast<const uint4*>(blk + kI4KMeta + 16 * t);
+    }
+    float acc[4][4];
+#pragma unroll
+    for (int gr = 0; gr < 4; ++gr) {
+      acc[gr][0] = acc[gr][1] = acc[gr][2] = acc[gr][3] = 0.0f;
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t x0 = comp(kw[0], gr), x1 = comp(kw[1], gr);
+        if (hf) { x0 >>= 8; x1 >>= 8; }
+        mma16816(acc[gr], unmagic(x0 & kM0), unmagic(x1 & kM0), unmagic(x0 & kM1), unmagic(x1 & kM1),
+                 bq[4 * gr + 2 * hf], bq[4 * gr + 2 * hf + 1]);
+      }
+    }
+    float T[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int e = c >> 1;
+      float v = 0.0f;
+#pragma unroll
+      for (int gr = 0; gr < 4; ++gr) v = fmaf(h_lo(comp(km[e], gr)), acc[gr][c], v);
+      T[c] = v * acol[c & 1];
+    }
+    // zero term sum_g zero_tg * (scale log2e Q_g) by one mma: k-slots 0..3 hi, 4..7 lo
+    const int qq = i & 1;
+    const uint32_t az0 = __byte_perm(comp(km[0], 2 * qq), comp(km[0], 2 * qq + 1), 0x7632);
+    const uint32_t az1 = __byte_perm(comp(km[1], 2 * qq), comp(km[1], 2 * qq + 1), 0x7632);
+    mma16816(T, az0, az1, 0u, 0u, bzl, 0u);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) lg[m][c] = T[c];
+  }
+}
+
+// ---- logits of one INT2 page
+template <int G>
+__device__ __forceinline__ void qk_int2(const uint8_t* blk, const uint32_t (&bq)[16], int r, int i, bool is_lo,
+                                        const float (&acol)[2], float scale_log2, const float (*qz)[kHeadDim],
+                                        float (&lg)[2][4]) {
+  constexpr bool kComb = G <= 4;
+  uint2 kw[2][2];
+#pragma unroll
+  for (int m = 0; m < 2; ++m)
+#pragma unroll
+    for (int e = 0; e < 2; ++e)
+      kw[m][e] = *reinterpret_cast<const uint2*>(blk + kI2KCodes + 32 * (16 * m + r + 8 * e) + 8 * i);
+  uint4 sv[4];
+#pragma unroll
+  for (int x = 0; x < 4; ++x) sv[x] = *reinterpret_cast<const uint4*>(blk + kI2KMeta + 64 * i + 16 * x);
+  float acc[2][4];
+#pragma unroll
+  for (int m = 0; m < 2; ++m) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.0f;
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    const int wi = kk >> 2, jj = kk & 3, j0 = 2 * jj, j1 = 2 * jj + 1;
+    const int p0 = wi * 8 + j0, p1 = wi * 8 + j1;
+    const uint32_t s0 = comp(sv[p0 >> 2], p0 & 3), s1 = comp(sv[p1 >> 2], p1 & 3);
+    const uint32_t t0 = hmul2(bq[2 * kk], s0), t1 = hmul2(bq[2 * kk + 1], s1);
+    const uint32_t u0 = hfma2(bq[2 * kk], s0, t0 ^ kSign2), u1 = hfma2(bq[2 * kk + 1], s1, t1 ^ kSign2);
+    const uint32_t sh0 = 2 * (j0 & 3), sh1 = 2 * (j1 & 3);
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+      uint32_t x0 = wi ? kw[m][0].y : kw[m][0].x, x1 = wi ? kw[m][1].y : kw[m][1].x;
+      if (jj >= 2) { x0 >>= 8; x1 >>= 8; }
+      const uint32_t a0 = unmagic(x0 & (kQ0 << sh0)), a1 = unmagic(x1 & (kQ0 << sh0));
+      const uint32_t a2 = unmagic(x0 & (kQ0 << sh1)), a3 = unmagic(x1 & (kQ0 << sh1));
+      if (kComb) {
+        mma16816(acc[m], a0, a1, a2, a3, is_lo ? u0 : t0, is_lo ? u1 : t1);
+      } else {
+        mma16816(acc[m], a0, a1, a2, a3, t0, t1);
+        mma16816(acc[m], a0, a1, a2, a3, u0, u1);
+      }
+    }
+  }
+  // zero term Z_h = sum_c q_hc zero_c (fp32), reduced over the lanes of head h
+  float zp = 0.0f;
+  if (kComb) {
+    const int hz = r & 3, wi = r >> 2;
+    const uint4 z0 = *reinterpret_cast<const uint4*>(blk + kI2KMeta + 256 + 64 * i + 32 * wi);
+    const uint4 z1 = *reinterpret_cast<const uint4*>(blk + kI2KMeta + 256 + 64 * i + 32 * wi + 16);
+    const float* qp = qz[hz] + (i * 2 + wi) * 16;
+#pragma unroll
+    for (int x = 0; x < 8; ++x) {
+      const uint32_t z2 = x < 4 ? comp(z0, x) : comp(z1, x - 4);
+      zp = fmaf(h_lo(z2), qp[2 * x], zp);
+      zp = fmaf(h_hi(z2), qp[2 * x + 1], zp);
+    }
+    zp += __shfl_xor_sync(0xFFFFFFFFu, zp, 1);
+    zp += __shfl_xor_sync(0xFFFFFFFFu, zp, 2);
+    zp += __shfl_xor_sync(0xFFFFFFFFu, zp, 16);
+  } else {
+    const int hz = r;
+    const float* qp = qz[hz] + i * 32;
+#pragma unroll
+    for (int x4 = 0; x4 < 4; ++x4) {
+      const uint4 zz = *reinterpret_cast<const uint4*>(blk + kI2KMeta + 256 + 64 * i + 16 * x4);
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        const uint32_t z2 = comp(zz, x);
+        zp = fmaf(h_lo(z2), qp[8 * x4 + 2 * x], zp);
+        zp = fmaf(h_hi(z2), qp[8 * x4 + 2 * x + 1], zp);
+      }
+    }
+    zp += __shfl_xor_sync(0xFFFFFFFFu, zp, 1);
+    zp += __shfl_xor_sync(0xFFFFFFFFu, zp, 2);
+  }
+  const float zc0 = __shfl_sync(0xFFFFFFFFu, zp, 4 * (2 * i)) * scale_log2;
+  const float zc1 = __shfl_sync(0xFFFFFFFFu, zp, 4 * (2 * i + 1)) * scale_log2;
+#pragma unroll
+  for (int m = 0; m < 2; ++m)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      float v = acc[m][c];
+      if (kComb) v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
+      lg[m][c] = fmaf(acol[c & 1], v, (c & 1) ? zc1 : zc0);
+    }
+}
+
+// ---- online softmax update and P.V for one page (either width)
+template <int G, bool kInt2>
+__device__ __forceinline__ void softmax_pv(const uint8_t* blk, uint32_t live, int r, int i, bool is_lo, float pscale,
+                                           float (&lg)[2][4], float (&o)[8][4], float (&zv)[4], float (&mrun)[2],
+                                           float (&lsum)[2], float (*pbuf)[kPage]) {
+  constexpr bool kComb = G <= 4;
+  constexpr int vmeta = kInt2 ? kI2VMeta : kI4VMeta;
+  float corr[2];
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    float pm = -INFINITY;
+#pragma unroll
+    for (int m = 0; m < 2; ++m)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int t = 16 * m + r + 8 * e;
+        if (!((live >> t) & 1u)) lg[m][2 * e + hh] = kDead2;
+        pm = fmaxf(pm, lg[m][2 * e + hh]);
+      }
+    pm = fmaxf(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, 4));
+    pm = fmaxf(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, 8));
+    pm = fmaxf(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, 16));
+    const float mnew = fmaxf(mrun[hh], pm);
+    corr[hh] = exp2f(mrun[hh] - mnew);
+    mrun[hh] = mnew;
+    float ps = 0.0f;
+#pragma unroll
+    for (int m = 0; m < 2; ++m)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int t = 16 * m + r + 8 * e;
+        const float p = exp2f(lg[m][2 * e + hh] - mnew);
+        ps += p;
+        if (!kComb || i < 2) pbuf[2 * i + hh][t] = ((live >> t) & 1u) ? p * pscale : 0.0f;
+      }
+    lsum[hh] = lsum[hh] * corr[hh] + ps;
+  }
+  float c0 = corr[0], c1 = corr[1];
+  if (kComb) {
+    const float x0 = __shfl_xor_sync(0xFFFFFFFFu, c0, 2), x1 = __shfl_xor_sync(0xFFFFFFFFu, c1, 2);
+    if (i >= 2) { c0 = x0; c1 = x1; }
+  }
+  if (__any_sync(0xFFFFFFFFu, c0 != 1.0f || c1 != 1.0f)) {
+#pragma unroll
+    for (int m = 0; m < 8; ++m) { o[m][0] *= c0; o[m][1] *= c1; o[m][2] *= c0; o[m][3] *= c1; }
+    zv[0] *= c0; zv[1] *= c1; zv[2] *= c0; zv[3] *= c1;
+  }
+  __syncwarp();
+
+  // B operands: p of head hp at slots 8i..8i+7, pairs (8i+k, 8i+k+4)
+  const int hp = kComb ? (r & 3) : r;
+  const float4 pa = *reinterpret_cast<const float4*>(&pbuf[hp][8 * i]);
+  const float4 pb = *reinterpret_cast<const float4*>(&pbuf[hp][8 * i + 4]);
+  const float pav[4] = {pa.x, pa.y, pa.z, pa.w}, pbv[4] = {pb.x, pb.y, pb.z, pb.w};
+  uint32_t ph[4], pl[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    ph[k] = pack_h2(pav[k], pbv[k]);
+    pl[k] = pack_h2(pav[k] - h_lo(ph[k]), pbv[k] - h_hi(ph[k]));
+  }
+  // V zero term: rows = groups (lanes r < 4), k = slots
+  {
+    uint4 zz = make_uint4(0u, 0u, 0u, 0u);
+    if (r < 4) zz = *reinterpret_cast<const uint4*>(blk + vmeta + 256 + 64 * r + 16 * i);
+    if (kComb) {
+      const uint32_t b0 = is_lo ? pl[0] : ph[0], b1 = is_lo ? pl[1] : ph[1];
+      const uint32_t b2 = is_lo ? pl[2] : ph[2], b3 = is_lo ? pl[3] : ph[3];
+      mma16816(zv, zz.x, 0u, zz.y, 0u, b0, b1);
+      mma16816(zv, zz.z, 0u, zz.w, 0u, b2, b3);
+    } else {
+      mma16816(zv, zz.x, 0u, zz.y, 0u, ph[0], ph[1]);
+      mma16816(zv, zz.z, 0u, zz.w, 0u, ph[2], ph[3]);
+      mma16816(zv, zz.x, 0u, zz.y, 0u, pl[0], pl[1]);
+      mma16816(zv, zz.z, 0u, zz.w, 0u, pl[2], pl[3]);
+    }
+  }
+  uint32_t plx[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) plx[k] = (kComb && !is_lo) ? 0u : pl[k];
+#pragma unroll
+  for (int gr = 0; gr < 4; ++gr) {
+    const uint4 svv = *reinterpret_cast<const uint4*>(blk + vmeta + 64 * gr + 16 * i);
+    uint32_t sk[4] = {svv.x, svv.y, svv.z, svv.w};
+    if (kInt2) {
+      sk[1] = hmul2(sk[1], 0x34003400u);   // x 2^-2
+      sk[2] = hmul2(sk[2], 0x2C002C00u);   // x 2^-4
+      sk[3] = hmul2(sk[3], 0x24002400u);   // x 2^-6
+    } else {
+      sk[1] = hmul2(sk[1], 0x2C002C00u);
+      sk[3] = hmul2(sk[3], 0x2C002C00u);
+    }
+    uint32_t bh[4], bl[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t t = hmul2(ph[k], sk[k]);
+      const uint32_t u = hfma2(ph[k], sk[k], t ^ kSign2);
+      if (kComb) {
+        bh[k] = hfma2(plx[k], sk[k], is_lo ? u : t);
+      } else {
+        bh[k] = t;
+        bl[k] = hfma2(plx[k], sk[k], u);
+      }
+    }
+    uint32_t wv[4];
+    if (kInt2) {
+      const uint2 v2 = *reinterpret_cast<const uint2*>(blk + kI2VCodes + 16 * (32 * (gr >> 1) + 4 * r + i) + 8 * (gr & 1));
+      wv[0] = v2.x; wv[1] = v2.y;
+    } else {
+      const uint4 v4 = *reinterpret_cast<const uint4*>(blk + kI4VCodes + 16 * (32 * gr + 4 * r + i));
+      wv[0] = v4.x; wv[1] = v4.y; wv[2] = v4.z; wv[3] = v4.w;
+    }
+#pragma unroll
+    for (int mm = 0; mm < 2; ++mm) {
+      const int m = 2 * gr + mm;
+      uint32_t a[2][4];
+      if (kInt2) {
+        const uint32_t e0 = wv[mm], e1 = wv[mm] >> 8;
+        a[0][0] = unmagic(e0 & kQ0); a[0][1] = unmagic(e1 & kQ0);
+        a[0][2] = unmagic(e0 & (kQ0 << 2)); a[0][3] = unmagic(e1 & (kQ0 << 2));
+        a[1][0] = unmagic(e0 & (kQ0 << 4)); a[1][1] = unmagic(e1 & (kQ0 << 4));
+        a[1][2] = unmagic(e0 & (kQ0 << 6)); a[1][3] = unmagic(e1 & (kQ0 << 6));
+      } else {
+        const uint32_t w0 = wv[2 * mm], w1 = wv[2 * mm + 1];
+        const uint32_t x0 = w0 >> 8, x1 = w1 >> 8;
+        a[0][0] = unmagic(w0 & kM0); a[0][1] = unmagic(w1 & kM0); a[0][2] = unmagic(w0 & kM1); a[0][3] = unmagic(w1 & kM1);
+        a[1][0] = unmagic(x0 & kM0); a[1][1] = unmagic(x1 & kM0); a[1][2] = unmagic(x0 & kM1); a[1][3] = unmagic(x1 & kM1);
+      }
+      mma16816(o[m], a[0][0], a[0][1], a[0][2], a[0][3], bh[0], bh[1]);
+      mma16816(o[m], a[1][0], a[1][1], a[1][2], a[1][3], bh[2], bh[3]);
+      if (!kComb) {
+        mma16816(o[m], a[0][0], a[0][1], a[0][2], a[0][3], bl[0], bl[1]);
+        mma16816(o[m], a[1][0], a[1][1], a[1][2], a[1][3], bl[2], bl[3]);
+      }
+    }
+  }
+  __syncwarp();
+}
+
+template <int G>
+__global__ void __launch_bounds__(kThreads, 4) decode_mma_kernel(
+    const uint8_t* __restrict__ pool, size_t int4_off, int64_t n2, int hkv, int max_pages,
+    const Entry* __restrict__ table, const __nv_bfloat16* __restrict__ q, int hq, float scale_log2,
+    const Unit* __restrict__ units, const Split* __restrict__ splits, float* __restrict__ part,
+    const uint32_t* __restrict__ smax_bits, uint32_t* __restrict__ status) {
+  constexpr bool kComb = G <= 4;
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  CtaSmem& S = *reinterpret_cast<CtaSmem*>(smem_raw);
+  const Split sp = splits[blockIdx.x];
+  const Unit u = units[sp.unit];
+  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, r = lane >> 2, i = lane & 3;
+  WarpSmem& WS = S.warp[w];
+
+  // ---- prologue: q of the packed heads, per-head power-of-two scale, constants
+  for (int x = tid; x < 8 * kHeadDim; x += kThreads) {
+    const int h = x >> 7, c = x & (kHeadDim - 1);
+    S.qraw[h][c] = h < G ? __bfloat162float(q[((size_t)u.b * hq + (size_t)u.kvh * G + h) * kHeadDim + c]) : 0.0f;
+  }
+  if (lane == 0) {
+    for (int st = 0; st < kStages; ++st) bar_init(&WS.bar[st]);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  const float smax = fmaxf(__uint_as_float(smax_bits[0]), 1.0f);
+  // P is carried as p * 2^sv in the fp16 folds so that p * scale * 2^-6 stays
+  // clear of the binary16 subnormal range; 2^sv * (largest V scale) <= 2^15.
+  const float vmax = fmaxf(__uint_as_float(smax_bits[1]), 1.0f / 1024.0f);
+  const int sv = max(0, min(15, ilogbf(32768.0f / vmax)));
+  const float pscale = ldexpf(1.0f, sv);
+  for (int h = w; h < 8; h += kWarps) {
+    float mx = 0.0f, qg[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      qg[k] = S.qraw[h][lane + 32 * k];           // channel lane + 32k is in group k
+      mx = fmaxf(mx, fabsf(qg[k]));
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+#pragma unroll
+      for (int k = 0; k < 4; ++k) qg[k] += __shfl_xor_sync(0xFFFFFFFFu, qg[k], o);
+    }
+    if (lane == 0) {
+      int E = 0;
+      if (mx > 0.0f) E = max(-100, min(100, ilogbf(16384.0f / (mx * smax))));
+      S.eh[h] = E;
+      S.acol[h] = ldexpf(scale_log2, -E);
+      unsigned short hi[4], lo[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) split_f16(scale_log2 * qg[k], hi[k], lo[k]);
+      S.bz[h][0] = hi[0] | ((uint32_t)hi[1] << 16);
+      S.bz[h][1] = hi[2] | ((uint32_t)hi[3] << 16);
+      S.bz[h][2] = lo[0] | ((uint32_t)lo[1] << 16);
+      S.bz[h][3] = lo[2] | ((uint32_t)lo[3] << 16);
+    }
+  }
+  for (int x = tid; x < 8 * kHeadDim; x += kThreads) {
+    const int h = x >> 7, pidx = x & (kHeadDim - 1);
+    const int pair = pidx >> 1, hi = pidx & 1;
+    const int j = pair & 7, iw = pair >> 3;      // iw = i*2 + wi
+    const int c = 4 * (4 * iw + (j >> 2)) + (j & 3) + 8 * hi;
+    S.qz[h][pidx] = S.qraw[h][c];
+  }
+  __syncthreads();
+
+  const bool is_int2 = sp.is_int2 != 0;
+  const bool is_lo = kComb && r >= 4;
+  uint32_t bq[16];
+  if (is_int2) {
+    const int hq2 = kComb ? (r & 3) : r;
+    const int E = S.eh[hq2];
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int j = 2 * (kk & 3) + e, wi = kk >> 2;
+        const int clo = 4 * (8 * i + 4 * wi + (j >> 2)) + (j & 3);
+        const int wexp = 2 * (j & 3);
+        bq[2 * kk + e] = hq2 < G ? pack_h2(ldexpf(S.qraw[hq2][clo], E - wexp), ldexpf(S.qraw[hq2][clo + 8], E - wexp))
+                                 : 0u;
+      }
+  } else {
+    const int n = r;
+    const int E = S.eh[n];
+#pragma unroll
+    for (int gr = 0; gr < 4; ++gr)
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const int c0 = 32 * gr + 8 * i + 2 * hf, c1 = c0 + 1;
+        bq[4 * gr + 2 * hf] = n < G ? pack_h2(ldexpf(S.qraw[n][c0], E), ldexpf(S.qraw[n][c0 + 4], E)) : 0u;
+        bq[4 * gr + 2 * hf + 1] =
+            n < G ? pack_h2(ldexpf(S.qraw[n][c1], E - 4), ldexpf(S.qraw[n][c1 + 4], E - 4)) : 0u;
+      }
+  }
+  const uint32_t bzl = r < G ? S.bz[r][i] : 0u;
+  const float acol[2] = {S.acol[2 * i], S.acol[2 * i + 1]};
+
+  // ---- page loop: two-stage bulk-copy ring per warp
+  const Entry* tab = table + (size_t)u.req * max_pages;
+  const int npg = sp.page_end - sp.page_begin;
+  const int nw = npg > w ? (npg - w + kWarps - 1) / kWarps : 0;
+  const uint32_t bytes = is_int2 ? (uint32_t)kInt2Block : (uint32_t)kInt4Block;
+  auto block_of = [&](int k) -> const uint8_t* {
+    const int32_t id = tab[sp.page_begin + w + k * kWarps].id;
+    return is_int2 ? pool + ((size_t)id * hkv + u.kvh) * kInt2Block
+                   : pool + int4_off + ((size_t)(id - n2) * hkv + u.kvh) * kInt4Block;
+  };
+  if (lane == 0)
+    for (int k = 0; k < kStages && k < nw; ++k) bulk_load(WS.stage[k], block_of(k), bytes, &WS.bar[k]);
+
+  float o[8][4], zv[4] = {0.0f, 0.0f, 0.0f, 0.0f}, mrun[2] = {-INFINITY, -INFINITY}, lsum[2] = {0.0f, 0.0f};
+#pragma unroll
+  for (int m = 0; m < 8; ++m) o[m][0] = o[m][1] = o[m][2] = o[m][3] = 0.0f;
+  int k = 0;
+  bool ok = true;
+  for (; k < nw; ++k) {
+    const int st = k & (kStages - 1);
+    const uint32_t ph = (uint32_t)(k / kStages) & 1u;
+    const bool got = bar_wait(&WS.bar[st], ph);
+    if (!__all_sync(0xFFFFFFFFu, got)) { ok = false; break; }
+    const uint32_t live = tab[sp.page_begin + w + k * kWarps].live;
+    const uint8_t* blk = WS.stage[st];
+    float lg[2][4];
+    if (is_int2) {
+      qk_int2<G>(blk, bq, r, i, is_lo, acol, scale_log2, S.qz, lg);
+      softmax_pv<G, true>(blk, live, r, i, is_lo, pscale, lg, o, zv, mrun, lsum, WS.pbuf);
+    } else {
+      qk_int4<G>(blk, bq, bzl, r, i, acol, lg);
+      softmax_pv<G, false>(blk, live, r, i, is_lo, pscale, lg, o, zv, mrun, lsum, WS.pbuf);
+    }
+    if (lane == 0 && k + kStages < nw) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      bulk_load(WS.stage[st], block_of(k + kStages), bytes, &WS.bar[st]);
+    }
+  }
+  if (!ok) {
+    if (lane == 0) atomicOr(status, kStatusTimeout);
+    for (int kk = k; kk < nw && kk < k + kStages; ++kk)
+      bar_wait(&WS.bar[kk & (kStages - 1)], (uint32_t)(kk / kStages) & 1u);
+    mrun[0] = mrun[1] = -INFINITY;
+  }
+
+  // ---- per-warp epilogue: finish l, combine hi/lo columns, add the V zero term
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    lsum[hh] += __shfl_xor_sync(0xFFFFFFFFu, lsum[hh], 4);
+    lsum[hh] += __shfl_xor_sync(0xFFFFFFFFu, lsum[hh], 8);
+    lsum[hh] += __shfl_xor_sync(0xFFFFFFFFu, lsum[hh], 16);
+  }
+  if (kComb) {
+#pragma unroll
+    for (int m = 0; m < 8; ++m)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) o[m][c] += __shfl_xor_sync(0xFFFFFFFFu, o[m][c], 2);
+  }
+  if (r < 4) {
+    S.zv[w][r][2 * i] = zv[0];
+    S.zv[w][r][2 * i + 1] = zv[1];
+  }
+  __syncwarp();
+  float* accw = reinterpret_cast<float*>(WS.stage[0]);   // [8][128], the ring is idle now
+  const bool valid = !kComb || i < 2;
+  if (valid) {
+#pragma unroll
+    for (int m = 0; m < 8; ++m)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int h = 2 * i + (c & 1), ch = 16 * m + r + 8 * (c >> 1);
+        if (h < G) {
+          float zt = S.zv[w][m >> 1][h];
+          if (kComb) zt += S.zv[w][m >> 1][h + 4];
+          accw[h * kHeadDim + ch] = (o[m][c] + zt) * ldexpf(1.0f, -sv);
+        }
+      }
+    if (r == 0)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh)
+        if (2 * i + hh < G) {
+          S.mw[w][2 * i + hh] = mrun[hh];
+          S.lw[w][2 * i + hh] = lsum[hh];
+        }
+  }
+  __syncthreads();
+
+  // ---- merge the warps: one thread per channel
+  float* out = part + (size_t)blockIdx.x * G * kPartStride;
+  const int c = tid;
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int ww = 0; ww < kWarps; ++ww) M = fmaxf(M, S.mw[ww][h]);
+    float L = 0.0f, A = 0.0f;
+#pragma unroll
+    for (int ww = 0; ww < kWarps; ++ww) {
+      const float mw = S.mw[ww][h];
+      if (mw == -INFINITY) continue;
+      const float f = exp2f(mw - M);
+      L += S.lw[ww][h] * f;
+      A += reinterpret_cast<const float*>(S.warp[ww].stage[0])[h * kHeadDim + c] * f;
+    }
+    out[h * kPartStride + c] = A;
+    if (c == 0) {
+      out[h * kPartStride + kHeadDim] = M;
+      out[h * kPartStride + kHeadDim + 1] = L;
+    }
+  }
+}
+
+template <int G>
+cudaError_t launch_mma_g(kv_pool* P, const void* q, int32_t hq, float scale_log2, const Unit* d_units,
+                         const Split* d_splits, int n_splits, float* d_part, cudaStream_t s) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)sizeof(CtaSmem));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  if (n_splits <= 0) return cudaSuccess;
+  ++P->launches;
+  decode_mma_kernel<G><<<n_splits, kThreads, sizeof(CtaSmem), s>>>(
+      P->d_pool, P->int4_offset, P->cfg.n_int2_pages, P->cfg.num_kv_heads, P->cfg.max_pages_per_request, P->d_table,
+      (const __nv_bfloat16*)q, hq, scale_log2, d_units, d_splits, d_part, P->d_status + 1, P->d_status);
+  return cudaGetLastError();
+}
+
+template <int G>
+int mma_occupancy() {
+  int n = 0;
+  if (cudaFuncSetAttribute(decode_mma_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(CtaSmem)) !=
+      cudaSuccess)
+    return 1;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<G>, kThreads, sizeof(CtaSmem)) != cudaSuccess)
+    return 1;
+  return n > 0 ? n : 1;
+}
+
+}  // namespace
+
+cudaError_t launch_decode_mma(kv_pool* P, const void* q, int32_t hq, float scale_log2, const Unit* d_units, int n_units,
+                              const Split* d_splits, int n_splits, float* d_part, float* out, cudaStream_t s) {
+  cudaError_t e;
+  switch (hq / P->cfg.num_kv_heads) {
+    case 1: e = launch_mma_g<1>(P, q, hq, scale_log2, d_units, d_splits, n_splits, d_part, s); break;
+    case 2: e = launch_mma_g<2>(P, q, hq, scale_log2, d_units, d_splits, n_splits, d_part, s); break;
+    case 3: e = launch_mma_g<3>(P, q, hq, scale_log2, d_units, d_splits, n_splits, d_part, s); break;
+    case 4: e = launch_mma_g<4>(P, q, hq, scale_log2, d_units, d_splits, n_splits, d_part, s); break;
+    case 5: e = launch_mma_g<5>(P, q, hq, scale_log2, d_units, d_splits, n_splits, d_part, s); break;
+    case 6: e = launch_mma_g<6>(P, q, hq, scale_log2, d_units, d_splits, n_splits, d_part, s); break;
+    case 7: e = launch_mma_g<7>(P, q, hq, scale_log2, d_units, d_splits, n_splits, d_part, s); break;
+    case 8: e = launch_mma_g<8>(P, q, hq, scale_log2, d_units, d_splits, n_splits, d_part, s); break;
+    default: return cudaErrorInvalidValue;
+  }
+  if (e != cudaSuccess) return e;
+  return launch_merge(P, hq / P->cfg.num_kv_heads, d_units, n_units, d_part, hq, out, s);
+}
+
+int decode_mma_ctas_per_sm(int g) {
+  switch (g) {
+    case 1: return mma_occupancy<1>();
+    case 2: return mma_occupancy<2>();
+    case 3: return mma_occupancy<3>();
+    case 4: return mma_occupancy<4>();
+    case 5: return mma_occupancy<5>();
+    case 6: return mma_occupancy<6>();
+    case 7: return mma_occupancy<7>();
+    default: return mma_occupancy<8>();
+  }
+}
+
+}  // namespace kvq

@@ -194,16 +194,33 @@ __global__ void merge_kernel(const Unit* __restrict__ units, const float* __rest
 template <int G>
 cudaError_t launch_g(kv_pool* P, const void* q, int32_t hq, float scale_log2, const Unit* d_units, int n_units,
                      const Split* d_splits, int n_splits, float* d_part, float* out, cudaStream_t s) {
-  P->launches += n_splits > 0 ? 2 : 1;
-  if (n_splits > 0)
+  if (n_splits > 0) {
+    ++P->launches;
     decode_simt_kernel<G><<<n_splits, kThreads, 0, s>>>(
         P->d_pool, P->int4_offset, P->cfg.n_int2_pages, P->cfg.num_kv_heads, P->cfg.max_pages_per_request,
         P->d_table, (const __nv_bfloat16*)q, hq, scale_log2, d_units, d_splits, d_part);
-  merge_kernel<G><<<n_units, 32 * G, 0, s>>>(d_units, d_part, hq, out);
-  return cudaGetLastError();
+  }
+  return launch_merge(P, G, d_units, n_units, d_part, hq, out, s);
 }
 
 }  // namespace
+
+cudaError_t launch_merge(kv_pool* P, int g, const Unit* d_units, int n_units, const float* d_part, int hq, float* out,
+                         cudaStream_t s) {
+  ++P->launches;
+  switch (g) {
+    case 1: merge_kernel<1><<<n_units, 32, 0, s>>>(d_units, d_part, hq, out); break;
+    case 2: merge_kernel<2><<<n_units, 64, 0, s>>>(d_units, d_part, hq, out); break;
+    case 3: merge_kernel<3><<<n_units, 96, 0, s>>>(d_units, d_part, hq, out); break;
+    case 4: merge_kernel<4><<<n_units, 128, 0, s>>>(d_units, d_part, hq, out); break;
+    case 5: merge_kernel<5><<<n_units, 160, 0, s>>>(d_units, d_part, hq, out); break;
+    case 6: merge_kernel<6><<<n_units, 192, 0, s>>>(d_units, d_part, hq, out); break;
+    case 7: merge_kernel<7><<<n_units, 224, 0, s>>>(d_units, d_part, hq, out); break;
+    case 8: merge_kernel<8><<<n_units, 256, 0, s>>>(d_units, d_part, hq, out); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
 
 cudaError_t launch_decode_simt(kv_pool* P, const void* q, int32_t hq, float scale_log2, const Unit* d_units,
                                int n_units, const Split* d_splits, int n_splits, float* d_part, float* out,

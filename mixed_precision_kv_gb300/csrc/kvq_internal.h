@@ -86,7 +86,7 @@ struct kv_pool {
   size_t int4_offset = 0;             // byte offset of the INT4 region
   kvq::Entry* d_table = nullptr;      // [max_requests][max_pages]
   int32_t* d_ntab = nullptr;          // [max_requests]
-  uint32_t* d_status = nullptr;       // device status word
+  uint32_t* d_status = nullptr;       // [0] status bits, [1] largest INT2 K scale, [2] largest V scale (fp32 bits)
   kvq::DevBuf upload;                 // append/scatter job arrays
   kvq::DevBuf plan;                   // decode plan (units, splits)
   kvq::DevBuf partials;               // decode split partials
@@ -123,5 +123,11 @@ cudaError_t launch_decode_simt(kv_pool* P, const void* q, int32_t hq, float scal
                                int n_units, const Split* d_splits, int n_splits, float* d_part, float* out,
                                cudaStream_t s);
 int decode_simt_ctas_per_sm(int g);
+cudaError_t launch_decode_mma(kv_pool* P, const void* q, int32_t hq, float scale_log2, const Unit* d_units, int n_units,
+                              const Split* d_splits, int n_splits, float* d_part, float* out, cudaStream_t s);
+int decode_mma_ctas_per_sm(int g);
+// Split merge: out[b][h][:] = sum_s acc_s 2^(m_s - M) / sum_s l_s 2^(m_s - M) over the unit's splits.
+cudaError_t launch_merge(kv_pool* P, int g, const Unit* d_units, int n_units, const float* d_part, int hq, float* out,
+                         cudaStream_t s);
 
 }  // namespace kvq

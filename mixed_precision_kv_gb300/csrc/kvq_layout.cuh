@@ -12,8 +12,11 @@
 //                (gr) x 4 bytes; channel c = 32*gr + 8*i + n sits in nibble n
 //                (bits 4n..4n+3) of word (i, gr).
 //   [2048, 4096) V codes, channel-major: word (channel c, slot chunk j) holds
-//                slots 8j..8j+7 in nibbles 0..7; it sits at 16-byte chunk
-//                32*((c>>2)&3) + 4*(c>>4) + j, word c&3 inside the chunk.
+//                slots 8j..8j+7 in nibbles 0..7.  With c = 16m + 8e + r
+//                (m < 8, e < 2, r < 8) it sits at 16-byte chunk
+//                32*(m>>1) + 4*r + j, word 2*(m&1) + e inside the chunk, so the
+//                16 channels of one tensor-core M tile (16m .. 16m+15) stay in
+//                one 32-channel group.
 //   [4096, 4608) K scale/zero: [slot][group] half2 {scale, zero}.
 //   [4608, 5120) V scale/zero: scales [group][32] half then zeros [group][32]
 //                half, slot order inside each 8-slot chunk j permuted so that
@@ -22,8 +25,8 @@
 //   [   0, 1024) K codes: slot t row at 32*t; channel c at byte c>>2, bits
 //                2*(c&3).
 //   [1024, 2048) V codes, channel-major: word (r, m, i) holds channels
-//                16r+2m (bytes 0, 2) and 16r+2m+1 (bytes 1, 3) for slot chunk
-//                i: byte 0/1 hold slots 8i..8i+3, bytes 2/3 slots 8i+4..8i+7,
+//                16m+r (bytes 0, 2) and 16m+r+8 (bytes 1, 3) for slot chunk i:
+//                byte 0/1 hold slots 8i..8i+3, bytes 2/3 slots 8i+4..8i+7,
 //                slot 8i+k at bits 2k of its byte.  The word sits at 16-byte
 //                chunk 32*(m>>2) + 4*r + i, word m&3 inside the chunk.
 //   [2048, 2560) K scales: 128 halves in pair order, then zeros in the same
@@ -63,7 +66,8 @@ KVQ_HD int i4k_shift(int c) { return 4 * (c & 1); }
 // ---- INT4 V codes
 KVQ_HD int i4v_byte(int t, int c) {
   const int j = t >> 3, n = t & 7;
-  return kI4VCodes + 16 * (32 * ((c >> 2) & 3) + 4 * (c >> 4) + j) + 4 * (c & 3) + (n >> 1);
+  const int m = c >> 4, e = (c >> 3) & 1, r = c & 7;
+  return kI4VCodes + 16 * (32 * (m >> 1) + 4 * r + j) + 4 * (2 * (m & 1) + e) + (n >> 1);
 }
 KVQ_HD int i4v_shift(int t) { return 4 * (t & 1); }
 
@@ -73,7 +77,7 @@ KVQ_HD int i2k_shift(int c) { return 2 * (c & 3); }
 
 // ---- INT2 V codes
 KVQ_HD int i2v_byte(int t, int c) {
-  const int r = c >> 4, m = (c >> 1) & 7, e = c & 1;
+  const int m = c >> 4, e = (c >> 3) & 1, r = c & 7;
   const int i = t >> 3, k = t & 7;
   return kI2VCodes + 16 * (32 * (m >> 2) + 4 * r + i) + 4 * (m & 3) + e + 2 * (k >> 2);
 }

@@ -227,12 +227,12 @@ kv_status_t kv_pool_create(const kv_pool_config_t* cfg, kv_pool_t** out) {
   }
   const size_t tab = (size_t)cfg->max_requests * cfg->max_pages_per_request * sizeof(Entry);
   if (cudaMalloc(&P->d_table, tab) != cudaSuccess || cudaMalloc(&P->d_ntab, cfg->max_requests * 4) != cudaSuccess ||
-      cudaMalloc(&P->d_status, 4) != cudaSuccess) {
+      cudaMalloc(&P->d_status, 16) != cudaSuccess) {
     cudaGetLastError();
     return cleanup(fail(KV_ERR_OOM, "kv_pool_create: cannot allocate tables"));
   }
   if (cudaMemset(P->d_table, 0xFF, tab) != cudaSuccess || cudaMemset(P->d_ntab, 0, cfg->max_requests * 4) != cudaSuccess ||
-      cudaMemset(P->d_status, 0, 4) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)
+      cudaMemset(P->d_status, 0, 16) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)
     return cleanup(fail(KV_ERR_CUDA, "kv_pool_create: initialisation failed"));
   const size_t npages = (size_t)(cfg->n_int2_pages + cfg->n_int4_pages);
   try {
@@ -582,7 +582,7 @@ kv_status_t build_plan(kv_pool* P, const int32_t* req_ids, int32_t batch, int32_
     same = P->plan_req[b] == req_ids[b] && P->plan_ver[b] == P->reqs[req_ids[b]].version;
   if (same) return KV_OK;
 
-  const int ctas = decode_simt_ctas_per_sm(g);
+  const int ctas = impl == KV_DECODE_MMA ? decode_mma_ctas_per_sm(g) : decode_simt_ctas_per_sm(g);
   const double target = (double)P->sm_count * ctas;
   double total = 0.0;
   for (int32_t b = 0; b < batch; ++b)
@@ -654,8 +654,7 @@ kv_status_t kv_decode_attn(kv_pool_t* P, const void* q, const int32_t* req_ids, 
   if (!std::isfinite(softmax_scale)) return fail(KV_ERR_INVALID_ARG, "kv_decode_attn: softmax_scale must be finite");
   for (int32_t b = 0; b < batch; ++b)
     if (!req_ok(P, req_ids[b])) return fail(KV_ERR_INVALID_ARG, "kv_decode_attn: request %d not open", req_ids[b]);
-  int32_t impl = P->decode_impl == KV_DECODE_AUTO ? KV_DECODE_SIMT : P->decode_impl;
-  if (impl == KV_DECODE_MMA) return fail(KV_ERR_STATE, "kv_decode_attn: tensor-core decode not available");
+  const int32_t impl = P->decode_impl == KV_DECODE_AUTO ? KV_DECODE_MMA : P->decode_impl;
   DeviceGuard dg(P->cfg.device);
   cudaStream_t s = (cudaStream_t)stream;
   kv_status_t st = order_after_previous(P, s);
@@ -666,8 +665,12 @@ kv_status_t kv_decode_attn(kv_pool_t* P, const void* q, const int32_t* req_ids, 
     return st;
   const uint8_t* base = (const uint8_t*)P->plan.ptr;
   const float scale_log2 = softmax_scale * 1.4426950408889634f;
-  KV_CUDA(launch_decode_simt(P, q, hq, scale_log2, (const Unit*)(base + P->plan_units_off), P->n_units,
-                             (const Split*)(base + P->plan_splits_off), P->n_splits, (float*)P->partials.ptr, out, s));
+  const Unit* du = (const Unit*)(base + P->plan_units_off);
+  const Split* dsp = (const Split*)(base + P->plan_splits_off);
+  if (impl == KV_DECODE_MMA)
+    KV_CUDA(launch_decode_mma(P, q, hq, scale_log2, du, P->n_units, dsp, P->n_splits, (float*)P->partials.ptr, out, s));
+  else
+    KV_CUDA(launch_decode_simt(P, q, hq, scale_log2, du, P->n_units, dsp, P->n_splits, (float*)P->partials.ptr, out, s));
   P->stat_req.assign(req_ids, req_ids + batch);
   P->stat_hq = hq;
   return KV_OK;

@@ -119,6 +119,13 @@ __global__ void __launch_bounds__(kThreads) append_int4_kernel(
       const int c = 4 * lane + a;
       or_bits(img, i4v_byte(slot, c), i4v_shift(slot), cv[a]);
     }
+    {
+      // running maximum of V scales (non-negative floats order as their bits)
+      float vmx = vm.sf;
+      vmx = fmaxf(vmx, __shfl_xor_sync(0xFFFFFFFFu, vmx, 8));
+      vmx = fmaxf(vmx, __shfl_xor_sync(0xFFFFFFFFu, vmx, 16));
+      if (lane == 0) atomicMax(status + 2, __float_as_uint(vmx));
+    }
     if ((lane & 7) == 0) {
       st_half(img, kI4KMeta + 16 * slot + 4 * gr, km.s);
       st_half(img, kI4KMeta + 16 * slot + 4 * gr + 2, km.z);
@@ -135,7 +142,8 @@ __global__ void __launch_bounds__(kThreads) append_int4_kernel(
 // One CTA per (repack job, kv head): INT4 staging block -> INT2 block.
 __global__ void __launch_bounds__(kThreads) repack_int2_kernel(uint8_t* __restrict__ pool, size_t int4_off,
                                                               int64_t n2, int hkv,
-                                                              const RepackJob* __restrict__ jobs) {
+                                                              const RepackJob* __restrict__ jobs,
+                                                              uint32_t* __restrict__ smax_bits) {
   __shared__ __align__(16) uint8_t src[kInt4Block];
   __shared__ __align__(16) uint8_t dst[kInt2Block];
   const RepackJob job = jobs[blockIdx.x];
@@ -168,6 +176,11 @@ __global__ void __launch_bounds__(kThreads) repack_int2_kernel(uint8_t* __restri
     for (int t = 0; t < kPage; ++t) or_bits(dst, i2k_byte(t, c), i2k_shift(c), qcode(x[t], m, 3.0f));
     st_half(dst, kI2KMeta + 2 * i2k_meta_index(c), m.s);
     st_half(dst, kI2KMeta + 256 + 2 * i2k_meta_index(c), m.z);
+    // running maximum of INT2 K scales (non-negative floats order as their bits)
+    float smx = m.sf;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) smx = fmaxf(smx, __shfl_xor_sync(0xFFFFFFFFu, smx, o));
+    if ((threadIdx.x & 31) == 0) atomicMax(smax_bits, __float_as_uint(smx));
   }
   // V: thread -> (slot t, group gr), 32 channels each.
   {
@@ -193,6 +206,10 @@ __global__ void __launch_bounds__(kThreads) repack_int2_kernel(uint8_t* __restri
     }
     st_half(dst, kI2VMeta + 2 * mi, m.s);
     st_half(dst, kI2VMeta + 256 + 2 * mi, m.z);
+    float vmx = m.sf;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) vmx = fmaxf(vmx, __shfl_xor_sync(0xFFFFFFFFu, vmx, o));
+    if ((threadIdx.x & 31) == 0) atomicMax(smax_bits + 1, __float_as_uint(vmx));
   }
   __syncthreads();
   for (int i = threadIdx.x; i < kInt2Block / 16; i += kThreads)
@@ -226,7 +243,7 @@ cudaError_t launch_repack(kv_pool* P, const RepackJob* d_jobs, int n_jobs, cudaS
   dim3 grid((unsigned)n_jobs, (unsigned)P->cfg.num_kv_heads);
   ++P->launches;
   repack_int2_kernel<<<grid, kThreads, 0, s>>>(P->d_pool, P->int4_offset, P->cfg.n_int2_pages,
-                                               P->cfg.num_kv_heads, d_jobs);
+                                               P->cfg.num_kv_heads, d_jobs, P->d_status + 1);
   return cudaGetLastError();
 }
 

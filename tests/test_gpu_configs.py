@@ -1,0 +1,157 @@
+"""The five decode workloads, CUDA path vs oracle.
+
+Small instances are compared in full (every code, scale/zero, table entry and
+output).  Full-size instances are compared on every request's page table
+(bit-exact) and on sampled (request, kv head) units whose codes and outputs
+the oracle computes one by one.
+"""
+import numpy as np
+import pytest
+
+import kvsynth
+from harness import OracleWorkload, assert_outputs_close, compare_content, compare_tables
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def kvq():
+    import __graft_entry__
+    __graft_entry__.build()
+    import mixed_precision_kv_gb300 as m
+    m.load_library()
+    return m
+
+
+def _pair(w, chunk, steps=None, sel_heads=None, content_reqs=None, impl=None):
+    from mixed_precision_kv_gb300.workload import GPUWorkload, pool_size
+    gw = GPUWorkload(w, chunk=chunk, steps=steps)
+    if impl is not None:
+        gw.pool.set_decode_impl(impl)
+    ow = OracleWorkload(w, pool_size(w, gw.bits, chunk, gw.steps), chunk, sel_heads=sel_heads,
+                        content_reqs=content_reqs)
+    for a, b in zip(gw.bits, ow.bits):
+        assert np.array_equal(a, b)
+    return gw, ow
+
+
+def _build(gw, ow):
+    gw.prefill()
+    ow.prefill()
+    gw.evict()
+    ow.evict()
+    gw.reorder()
+    ow.reorder()
+    gw.pool.sync()
+
+
+def _check_all(gw, ow, reqs=None, content=True):
+    for r in (range(len(gw.rids)) if reqs is None else reqs):
+        ge = gw.pool.export(gw.rids[r], content=content)
+        oe = ow.P.export(ow.rids[r], content=content)
+        if content:
+            compare_content(ge, oe, ow.sel)
+        else:
+            compare_tables(ge, oe)
+
+
+def _decode_check(gw, ow, step, pairs=None, what=""):
+    out = gw.decode(gw.q(step)).cpu().numpy()
+    gw.pool.sync()
+    q = ow.q(step)
+    if pairs is None:
+        ref = ow.decode(q).reshape(out.shape)
+        got = out
+    else:
+        ref = ow.decode(q, pairs=pairs)
+        got = np.stack([out[b, h] for b, h in pairs])
+    assert np.isfinite(got).all()
+    return assert_outputs_close(got, ref, what)
+
+
+@pytest.mark.parametrize("impl", [1, 2])
+def test_config1_full(kvq, impl):
+    w = kvsynth.make_workload(1)
+    gw, ow = _pair(w, chunk=512, impl=impl)
+    _build(gw, ow)
+    _check_all(gw, ow)
+    frac2 = (gw.bits[0][:2048] == 2).mean()
+    assert 0.5 <= frac2 <= 0.8
+    _decode_check(gw, ow, 0, what="config 1")
+
+
+@pytest.mark.parametrize("cfg,kw", [
+    (2, dict(n_req=3, ctx=4000)),
+    (3, dict(n_req=2, ctx=6000)),
+    (4, dict(n_req=6, ctx_range=(300, 6000))),
+])
+def test_configs_small_full_compare(kvq, cfg, kw):
+    w = kvsynth.make_workload(cfg, **kw)
+    gw, ow = _pair(w, chunk=1024)
+    _build(gw, ow)
+    _check_all(gw, ow)
+    _decode_check(gw, ow, 0, what=f"config {cfg} small")
+
+
+def test_config5_loop_small(kvq):
+    """Append one token per request per step, repack at 32 qualifying tokens,
+    reorder, decode: tables every step, codes and outputs along the way."""
+    w = kvsynth.make_workload(5, n_req=6, ctx_range=(100, 1500), steps=70)
+    gw, ow = _pair(w, chunk=512)
+    _build(gw, ow)
+    repacks = 0
+    for step in range(w.steps):
+        k, v, rids, bits = gw.step_inputs()
+        gw.append_step(k, v, rids, bits)
+        ow.append_step()
+        gw.reorder()
+        ow.reorder()
+        _check_all(gw, ow, content=(step % 10 == 9))
+        _decode_check(gw, ow, step, what=f"config 5 step {step}")
+        repacks += int((bits == 2).sum())
+    assert repacks > 32
+
+
+def _sampled(w, rng, n_units):
+    """Sample (request, kv head) units; return the sampled requests, heads and (b, q head) pairs."""
+    reqs = sorted(set(rng.choice(len(w.requests), n_units, replace=False).tolist()))
+    heads = sorted(set(rng.choice(w.num_kv_heads, 2, replace=False).tolist()))
+    g = w.g
+    pairs = [(b, h * g + j) for b in reqs for h in heads for j in range(g)]
+    return reqs, heads, pairs
+
+
+@pytest.mark.parametrize("cfg", [2, 3])
+def test_configs_full_size_sampled(kvq, cfg):
+    w = kvsynth.make_workload(cfg)
+    rng = np.random.default_rng(cfg)
+    reqs, heads, pairs = _sampled(w, rng, 1)
+    gw, ow = _pair(w, chunk=16384, sel_heads=heads, content_reqs=reqs)
+    _build(gw, ow)
+    _check_all(gw, ow, content=False)                 # every table, bit-exact
+    _check_all(gw, ow, reqs=reqs, content=True)       # sampled codes and scale/zero
+    q = ow.q(0)
+    out = gw.decode(gw.q(0)).cpu().numpy()
+    ref = ow.decode(q, pairs=np.array(pairs, np.int32), n_threads=0)
+    got = np.stack([out[b, h] for b, h in pairs])
+    assert_outputs_close(got, ref, f"config {cfg} full size, sampled")
+
+
+def test_config4_full_size_sampled(kvq):
+    w = kvsynth.make_workload(4)
+    rng = np.random.default_rng(44)
+    # one short and one long request
+    lens = np.array([r.n_prefill for r in w.requests])
+    reqs = sorted({int(np.argmin(lens)), int(np.argmax(lens))})
+    heads = [1, 6]
+    pairs = [(b, h * w.g + j) for b in reqs for h in heads for j in range(w.g)]
+    gw, ow = _pair(w, chunk=16384, sel_heads=heads, content_reqs=reqs)
+    _build(gw, ow)
+    _check_all(gw, ow, content=False)
+    _check_all(gw, ow, reqs=reqs, content=True)
+    out = gw.decode(gw.q(0)).cpu().numpy()
+    ref = ow.decode(ow.q(0), pairs=np.array(pairs, np.int32))
+    got = np.stack([out[b, h] for b, h in pairs])
+    assert_outputs_close(got, ref, "config 4 full size, sampled")
+    assert rng is not None

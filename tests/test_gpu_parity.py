@@ -14,6 +14,9 @@ SEED = 4242
 SCALE = float(np.float32(1 / np.sqrt(128)))
 
 
+IMPLS = [1, 2]   # KV_DECODE_SIMT, KV_DECODE_MMA
+
+
 @pytest.fixture(scope="module")
 def kvq():
     import __graft_entry__
@@ -88,38 +91,42 @@ def _mixed(n, p2, seed):
     return np.where(np.random.default_rng(seed).random(n) < p2, 2, 4).astype(np.uint8)
 
 
+@pytest.mark.parametrize("impl", IMPLS)
 @pytest.mark.parametrize("n", [1, 2, 31, 32, 33, 63, 64, 65, 200])
 @pytest.mark.parametrize("p2", [0.0, 0.5, 1.0])
-def test_small_requests_codes_tables_outputs(kvq, n, p2):
+def test_small_requests_codes_tables_outputs(kvq, n, p2, impl):
     bits = [_mixed(n, p2, n), _mixed(n + 7, p2, n + 1)]
-    sc = Scenario(kvq, 2, 8, bits, chunk=48)
+    sc = Scenario(kvq, 2, 8, bits, chunk=48, impl=impl)
     sc.check_content()
-    sc.check_decode(what=f"n={n} p2={p2}")
+    sc.check_decode(what=f"n={n} p2={p2} impl={impl}")
 
 
-@pytest.mark.parametrize("hkv,hq", [(1, 1), (2, 4), (4, 12), (2, 16), (1, 7)])
-def test_gqa_ratios(kvq, hkv, hq):
+@pytest.mark.parametrize("impl", IMPLS)
+@pytest.mark.parametrize("hkv,hq", [(1, 1), (2, 4), (4, 12), (2, 16), (1, 7), (1, 2), (1, 3), (1, 5), (1, 6), (1, 8)])
+def test_gqa_ratios(kvq, hkv, hq, impl):
     bits = [_mixed(300, 0.6, 1), _mixed(97, 0.3, 2), _mixed(1, 1.0, 3)]
-    sc = Scenario(kvq, hkv, hq, bits, chunk=128)
+    sc = Scenario(kvq, hkv, hq, bits, chunk=128, impl=impl)
     sc.check_content()
-    sc.check_decode(what=f"hkv={hkv} hq={hq}")
+    sc.check_decode(what=f"hkv={hkv} hq={hq} impl={impl}")
 
 
-def test_outlier_channels_and_evictions(kvq):
+@pytest.mark.parametrize("impl", IMPLS)
+def test_outlier_channels_and_evictions(kvq, impl):
     cm = np.ones((2, 128), np.float32)
     cm[0, [3, 77, 90, 127]] = 20.0
     cm[1, [0, 31, 32, 64]] = 20.0
     bits = [_mixed(1000, 0.6, 5), _mixed(640, 0.8, 6)]
     rng = np.random.default_rng(7)
     ev = {0: rng.choice(1000, 50, replace=False), 1: rng.choice(640, 32, replace=False)}
-    sc = Scenario(kvq, 2, 8, bits, chunk=256, evict=ev, chan_mult=cm)
+    sc = Scenario(kvq, 2, 8, bits, chunk=256, evict=ev, chan_mult=cm, impl=impl)
     sc.check_content()
     sc.check_decode(what="outliers+evict")
 
 
-def test_all_dead_and_empty_requests(kvq):
+@pytest.mark.parametrize("impl", IMPLS)
+def test_all_dead_and_empty_requests(kvq, impl):
     bits = [_mixed(70, 0.5, 8), _mixed(40, 0.5, 9), np.zeros(0, np.uint8)]
-    sc = Scenario(kvq, 2, 8, bits, evict={0: np.arange(70)})
+    sc = Scenario(kvq, 2, 8, bits, evict={0: np.arange(70)}, impl=impl)
     out_ref = sc.check_decode(what="all-dead/empty")
     qd = torch.zeros((3, 8, 128), dtype=torch.bfloat16, device="cuda")
     out = sc.gpu.decode(qd, sc.g_ids, SCALE).cpu().numpy()
@@ -193,10 +200,11 @@ def test_range_error_reported_by_sync(kvq):
     gpu.sync()   # cleared
 
 
+@pytest.mark.parametrize("impl", IMPLS)
 @pytest.mark.parametrize("p2", [0.0, 1.0, 0.6])
-def test_split_counts_do_not_change_results(kvq, p2):
+def test_split_counts_do_not_change_results(kvq, p2, impl):
     """Long single request: many splits per unit vs the oracle."""
     bits = [_mixed(20000, p2, 11)]
-    sc = Scenario(kvq, 1, 8, bits, chunk=4096)
+    sc = Scenario(kvq, 1, 8, bits, chunk=4096, impl=impl)
     sc.check_decode(what=f"long p2={p2}")
     assert sc.gpu.last_decode_stats()["n_splits"] > 1
