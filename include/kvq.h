@@ -136,6 +136,28 @@ KVQ_API kv_status_t kv_evict_slots(kv_pool_t* pool, const int32_t* req_ids, cons
 KVQ_API kv_status_t kv_decode_attn(kv_pool_t* pool, const void* q, const int32_t* req_ids, int32_t batch,
                            int32_t num_q_heads, float softmax_scale, float* out, void* stream);
 
+/* Decode that allocates no device memory.  The pages have no counterpart for
+ * this call; it exists for callers that cannot call cudaMalloc while they
+ * decode: code whose device memory is owned entirely by another allocator or
+ * a fixed budget (a framework's caching allocator, a serving loop that
+ * reserved all memory up front), and latency-critical loops where a
+ * cudaMalloc/cudaFree, which may synchronize the device, is not acceptable.
+ * Same arguments, results and error rules as kv_decode_attn, except:
+ *   - the split plan and split partials live in one fixed 8 MiB array inside
+ *     the library (held on every GPU that loads it until the process exits)
+ *     instead of pool buffers that grow with cudaMalloc;
+ *   - batch x num_kv_heads must be <= 4096 and the plan must fit the array;
+ *     otherwise KV_ERR_INVALID_ARG with a message, before any device work;
+ *   - the first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress); make that first call before any stream capture;
+ *   - every call shares the array: calls whose device work overlaps (other
+ *     streams, other pools) race, so serialize them on one stream;
+ *   - the pool's own stream ordering and kv_last_decode_stats are not updated:
+ *     issue it on the stream that carries the pool's other work.
+ * The caller still provides q, out and the pool, as for kv_decode_attn. */
+KVQ_API kv_status_t kv_decode_attn_noalloc(kv_pool_t* pool, const void* q, const int32_t* req_ids, int32_t batch,
+                                           int32_t num_q_heads, float softmax_scale, float* out, void* stream);
+
 /* Choose the decode implementation (kv_decode_impl_t). */
 KVQ_API kv_status_t kv_set_decode_impl(kv_pool_t* pool, int32_t impl);
 

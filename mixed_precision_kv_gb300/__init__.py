@@ -25,7 +25,7 @@ HEAD_DIM, PAGE_TOKENS, GROUP = 128, 32, 32
 EXPORTED = ["kv_pool_create", "kv_pool_destroy", "kv_request_open", "kv_request_close", "kv_append_quant",
             "kv_reorder_pages", "kv_evict_slots", "kv_decode_attn", "kv_set_decode_impl", "kv_pool_sync",
             "kv_request_info", "kv_export_request", "kv_last_decode_stats", "kv_pool_launch_count", "kv_alloc_bits",
-            "kv_last_error"]
+            "kv_last_error", "kv_decode_attn_noalloc"]
 
 _P = ctypes.c_void_p
 _I32, _I64 = ctypes.c_int32, ctypes.c_int64
@@ -64,6 +64,7 @@ def load_library(path: str = LIB_PATH):
             "kv_reorder_pages": [_P, _P, _I32, _P],
             "kv_evict_slots": [_P, _P, _P, _I64, _P],
             "kv_decode_attn": [_P, _P, _P, _I32, _I32, ctypes.c_float, _P, _P],
+            "kv_decode_attn_noalloc": [_P, _P, _P, _I32, _I32, ctypes.c_float, _P, _P],
             "kv_set_decode_impl": [_P, _I32],
             "kv_pool_sync": [_P],
             "kv_request_info": [_P, _I32, _P, _P],
@@ -198,6 +199,21 @@ class KVPool:
         _check(load_library().kv_decode_attn(self._h, ctypes.c_void_p(q.data_ptr()), _ptr(req_ids), B, Hq,
                                              float(softmax_scale), ctypes.c_void_p(out.data_ptr()),
                                              _stream(stream)), "kv_decode_attn")
+        return out
+
+    def decode_noalloc(self, q, req_ids, softmax_scale, out, stream=None):
+        """kv_decode_attn_noalloc: like decode(), but the library allocates no device
+        memory (fixed internal scratch); the caller passes a preallocated `out`."""
+        import torch
+        req_ids = _np(req_ids, np.int32)
+        B, Hq, D = q.shape
+        if q.dtype != torch.bfloat16 or not q.is_cuda or not q.is_contiguous() or D != HEAD_DIM or B != req_ids.size:
+            raise ValueError("q must be a contiguous CUDA bf16 tensor [B][Hq][128] with B == len(req_ids)")
+        if out.dtype != torch.float32 or not out.is_contiguous() or tuple(out.shape) != (B, Hq, D):
+            raise ValueError("out must be a contiguous fp32 tensor shaped like q")
+        _check(load_library().kv_decode_attn_noalloc(self._h, ctypes.c_void_p(q.data_ptr()), _ptr(req_ids), B, Hq,
+                                                     float(softmax_scale), ctypes.c_void_p(out.data_ptr()),
+                                                     _stream(stream)), "kv_decode_attn_noalloc")
         return out
 
     def set_decode_impl(self, impl):

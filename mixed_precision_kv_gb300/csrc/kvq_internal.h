@@ -112,6 +112,9 @@ struct kv_pool {
 
 namespace kvq {
 
+// Sets the message kv_last_error() returns on this thread (kvq_pool.cu).
+void set_last_error(const char* msg);
+
 // Launchers (kvq_quant.cu)
 cudaError_t launch_append(kv_pool* P, const void* k, const void* v, const AppendJob* d_jobs, int n_jobs,
                           const int32_t* d_toks, cudaStream_t s);

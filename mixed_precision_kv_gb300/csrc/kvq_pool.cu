@@ -150,6 +150,8 @@ kv_status_t order_after_previous(kv_pool* P, cudaStream_t s) {
 
 }  // namespace
 
+void kvq::set_last_error(const char* msg) { g_err = msg; }
+
 extern "C" {
 
 const char* kv_last_error(void) { return g_err.c_str(); }
