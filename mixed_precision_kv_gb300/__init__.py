@@ -25,7 +25,7 @@ HEAD_DIM, PAGE_TOKENS, GROUP = 128, 32, 32
 EXPORTED = ["kv_pool_create", "kv_pool_destroy", "kv_request_open", "kv_request_close", "kv_append_quant",
             "kv_reorder_pages", "kv_evict_slots", "kv_decode_attn", "kv_set_decode_impl", "kv_pool_sync",
             "kv_request_info", "kv_export_request", "kv_last_decode_stats", "kv_pool_launch_count", "kv_alloc_bits",
-            "kv_last_error", "kv_decode_attn_noalloc"]
+            "kv_last_error", "kv_decode_attn_noalloc", "kv_decode_timing"]
 
 _P = ctypes.c_void_p
 _I32, _I64 = ctypes.c_int32, ctypes.c_int64
@@ -71,6 +71,7 @@ def load_library(path: str = LIB_PATH):
             "kv_export_request": [_P, _I32, _P, _P, _P, _P, _P, _P, _P, _P],
             "kv_last_decode_stats": [_P, _P, _P, _P],
             "kv_pool_launch_count": [_P, _P],
+            "kv_decode_timing": [_P, _I32, _P, _P, _P],
             "kv_alloc_bits": [_P, _P, _P, _I32, _I64, _I64, _P],
         }
         for name, args in sig.items():
@@ -242,6 +243,16 @@ class KVPool:
                                                 _ptr(d.get("vc")), _ptr(d.get("km")), _ptr(d.get("vm"))),
                "kv_export_request")
         return d
+
+    def decode_timing(self, enable=True):
+        """(Re)start or stop device timing of the decode kernels; returns
+        (n_calls, mean scan ms, mean scan+merge ms) recorded since the last start."""
+        n = ctypes.c_int64()
+        a = ctypes.c_float()
+        b = ctypes.c_float()
+        _check(load_library().kv_decode_timing(self._h, int(bool(enable)), ctypes.byref(n), ctypes.byref(a),
+                                               ctypes.byref(b)), "kv_decode_timing")
+        return n.value, a.value, b.value
 
     def launch_count(self) -> int:
         n = ctypes.c_int64()

@@ -33,6 +33,7 @@
 //    of the subnormal range (the pool tracks the largest INT2 K and V scales).
 // Pages stream through a two-stage per-warp ring filled by cp.async.bulk with
 // mbarrier completion; every wait is bounded and reports a timeout status.
+// 3 CTAs of 4 warps per SM (168 registers, no spills).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -48,7 +49,6 @@ constexpr int kStageBytes = kInt4Block;
 constexpr int kPartStride = kHeadDim + 4;
 constexpr float kDead2 = -1.0e4f * 1.4426950408889634f;
 constexpr uint32_t kSpinLimit = 1u << 22;
-constexpr uint32_t kSign2 = 0x80008000u;
 constexpr uint32_t kM0 = 0x000F000Fu, kM1 = 0x00F000F0u;   // nibble fields at bits 0 / 4 of each half
 constexpr uint32_t kQ0 = 0x00030003u;                      // 2-bit field at bit 0 of each half
 constexpr uint32_t kMagic = 0x64006400u;                   // binary16 1024.0 in both halves
@@ -88,6 +88,11 @@ __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
 __device__ __forceinline__ uint32_t unmagic(uint32_t x) {
   uint32_t d;
   asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(x | kMagic), "r"(kMagic));
+  return d;
+}
+__device__ __forceinline__ uint32_t hneg2(uint32_t a) {
+  uint32_t d;
+  asm("neg.f16x2 %0, %1;" : "=r"(d) : "r"(a));
   return d;
 }
 __device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
@@ -185,6 +190,7 @@ __device__ __forceinline__ void qk_int2(const uint8_t* blk, const uint32_t (&bq)
                                         const float (&acol)[2], float scale_log2, const float (*qz)[kHeadDim],
                                         float (&lg)[2][4]) {
   constexpr bool kComb = G <= 4;
+  const uint32_t lomask = is_lo ? 0xFFFFFFFFu : 0u;
   uint2 kw[2][2];
 #pragma unroll
   for (int m = 0; m < 2; ++m)
@@ -194,16 +200,23 @@ __device__ __forceinline__ void qk_int2(const uint8_t* blk, const uint32_t (&bq)
   uint4 sv[4];
 #pragma unroll
   for (int x = 0; x < 4; ++x) sv[x] = *reinterpret_cast<const uint4*>(blk + kI2KMeta + 64 * i + 16 * x);
-  float acc[2][4];
+  // four independent accumulators per M tile (k-step parity x hi/lo pass) so
+  // that consecutive mmas do not wait on each other
+  float acc[2][4][4];
 #pragma unroll
-  for (int m = 0; m < 2; ++m) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.0f;
+  for (int m = 0; m < 2; ++m)
+#pragma unroll
+    for (int x = 0; x < 4; ++x) acc[m][x][0] = acc[m][x][1] = acc[m][x][2] = acc[m][x][3] = 0.0f;
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
     const int wi = kk >> 2, jj = kk & 3, j0 = 2 * jj, j1 = 2 * jj + 1;
     const int p0 = wi * 8 + j0, p1 = wi * 8 + j1;
     const uint32_t s0 = comp(sv[p0 >> 2], p0 & 3), s1 = comp(sv[p1 >> 2], p1 & 3);
-    const uint32_t t0 = hmul2(bq[2 * kk], s0), t1 = hmul2(bq[2 * kk + 1], s1);
-    const uint32_t u0 = hfma2(bq[2 * kk], s0, t0 ^ kSign2), u1 = hfma2(bq[2 * kk + 1], s1, t1 ^ kSign2);
+    // hi = rn(q s); lo = rn(q s - hi) (exact).  With (hi | lo) columns, lanes of
+    // the lo columns subtract hi and lanes of the hi columns subtract 0.
+    uint32_t t0 = hmul2(bq[2 * kk], s0), t1 = hmul2(bq[2 * kk + 1], s1);
+    if (kComb) { t0 &= lomask; t1 &= lomask; }
+    const uint32_t u0 = hfma2(bq[2 * kk], s0, hneg2(t0)), u1 = hfma2(bq[2 * kk + 1], s1, hneg2(t1));
     const uint32_t sh0 = 2 * (j0 & 3), sh1 = 2 * (j1 & 3);
 #pragma unroll
     for (int m = 0; m < 2; ++m) {
@@ -212,10 +225,10 @@ __device__ __forceinline__ void qk_int2(const uint8_t* blk, const uint32_t (&bq)
       const uint32_t a0 = unmagic(x0 & (kQ0 << sh0)), a1 = unmagic(x1 & (kQ0 << sh0));
       const uint32_t a2 = unmagic(x0 & (kQ0 << sh1)), a3 = unmagic(x1 & (kQ0 << sh1));
       if (kComb) {
-        mma16816(acc[m], a0, a1, a2, a3, is_lo ? u0 : t0, is_lo ? u1 : t1);
+        mma16816(acc[m][kk & 3], a0, a1, a2, a3, u0, u1);
       } else {
-        mma16816(acc[m], a0, a1, a2, a3, t0, t1);
-        mma16816(acc[m], a0, a1, a2, a3, u0, u1);
+        mma16816(acc[m][2 * (kk & 1)], a0, a1, a2, a3, t0, t1);
+        mma16816(acc[m][2 * (kk & 1) + 1], a0, a1, a2, a3, u0, u1);
       }
     }
   }
@@ -257,7 +270,7 @@ __device__ __forceinline__ void qk_int2(const uint8_t* blk, const uint32_t (&bq)
   for (int m = 0; m < 2; ++m)
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      float v = acc[m][c];
+      float v = (acc[m][0][c] + acc[m][1][c]) + (acc[m][2][c] + acc[m][3][c]);
       if (kComb) v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
       lg[m][c] = fmaf(acol[c & 1], v, (c & 1) ? zc1 : zc0);
     }
@@ -270,6 +283,7 @@ __device__ __forceinline__ void softmax_pv(const uint8_t* blk, uint32_t live, in
                                            float (&lsum)[2], float (*pbuf)[kPage]) {
   constexpr bool kComb = G <= 4;
   constexpr int vmeta = kInt2 ? kI2VMeta : kI4VMeta;
+  const bool full = live == 0xFFFFFFFFu;   // warp-uniform: no dead slot on this page
   float corr[2];
 #pragma unroll
   for (int hh = 0; hh < 2; ++hh) {
@@ -279,7 +293,7 @@ __device__ __forceinline__ void softmax_pv(const uint8_t* blk, uint32_t live, in
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int t = 16 * m + r + 8 * e;
-        if (!((live >> t) & 1u)) lg[m][2 * e + hh] = kDead2;
+        if (!full && !((live >> t) & 1u)) lg[m][2 * e + hh] = kDead2;
         pm = fmaxf(pm, lg[m][2 * e + hh]);
       }
     pm = fmaxf(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, 4));
@@ -296,7 +310,7 @@ __device__ __forceinline__ void softmax_pv(const uint8_t* blk, uint32_t live, in
         const int t = 16 * m + r + 8 * e;
         const float p = exp2f(lg[m][2 * e + hh] - mnew);
         ps += p;
-        if (!kComb || i < 2) pbuf[2 * i + hh][t] = ((live >> t) & 1u) ? p * pscale : 0.0f;
+        if (!kComb || i < 2) pbuf[2 * i + hh][t] = (full || ((live >> t) & 1u)) ? p * pscale : 0.0f;
       }
     lsum[hh] = lsum[hh] * corr[hh] + ps;
   }
@@ -327,43 +341,52 @@ __device__ __forceinline__ void softmax_pv(const uint8_t* blk, uint32_t live, in
   {
     uint4 zz = make_uint4(0u, 0u, 0u, 0u);
     if (r < 4) zz = *reinterpret_cast<const uint4*>(blk + vmeta + 256 + 64 * r + 16 * i);
+    float zt[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     if (kComb) {
       const uint32_t b0 = is_lo ? pl[0] : ph[0], b1 = is_lo ? pl[1] : ph[1];
       const uint32_t b2 = is_lo ? pl[2] : ph[2], b3 = is_lo ? pl[3] : ph[3];
-      mma16816(zv, zz.x, 0u, zz.y, 0u, b0, b1);
-      mma16816(zv, zz.z, 0u, zz.w, 0u, b2, b3);
+      mma16816(zt, zz.x, 0u, zz.y, 0u, b0, b1);
+      mma16816(zt, zz.z, 0u, zz.w, 0u, b2, b3);
     } else {
-      mma16816(zv, zz.x, 0u, zz.y, 0u, ph[0], ph[1]);
-      mma16816(zv, zz.z, 0u, zz.w, 0u, ph[2], ph[3]);
-      mma16816(zv, zz.x, 0u, zz.y, 0u, pl[0], pl[1]);
-      mma16816(zv, zz.z, 0u, zz.w, 0u, pl[2], pl[3]);
+      mma16816(zt, zz.x, 0u, zz.y, 0u, ph[0], ph[1]);
+      mma16816(zt, zz.z, 0u, zz.w, 0u, ph[2], ph[3]);
+      mma16816(zt, zz.x, 0u, zz.y, 0u, pl[0], pl[1]);
+      mma16816(zt, zz.z, 0u, zz.w, 0u, pl[2], pl[3]);
     }
-  }
-  uint32_t plx[4];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) plx[k] = (kComb && !is_lo) ? 0u : pl[k];
+    for (int c = 0; c < 4; ++c) zv[c] += zt[c];
+  }
+  // Fold operands: B = fma(x1, s, fma(x2, s, -(x3 * s))).  Hi columns (and the
+  // hi pass of g > 4): x3 = 0, x2 = p_hi, x1 = 0 -> rn(p_hi s).  Lo columns:
+  // x3 = x2 = p_hi, x1 = p_lo -> rn(p_lo s + (p_hi s - rn(p_hi s))).
+  uint32_t x3[4], x1[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    x3[k] = (kComb && !is_lo) ? 0u : ph[k];
+    x1[k] = (kComb && !is_lo) ? 0u : pl[k];
+  }
 #pragma unroll
   for (int gr = 0; gr < 4; ++gr) {
     const uint4 svv = *reinterpret_cast<const uint4*>(blk + vmeta + 64 * gr + 16 * i);
     uint32_t sk[4] = {svv.x, svv.y, svv.z, svv.w};
     if (kInt2) {
-      sk[1] = hmul2(sk[1], 0x34003400u);   // x 2^-2
+      sk[1] = hmul2(sk[1], 0x34003400u);   // x 2^-2 (the code field sits at bit 2)
       sk[2] = hmul2(sk[2], 0x2C002C00u);   // x 2^-4
       sk[3] = hmul2(sk[3], 0x24002400u);   // x 2^-6
     } else {
-      sk[1] = hmul2(sk[1], 0x2C002C00u);
+      sk[1] = hmul2(sk[1], 0x2C002C00u);   // x 2^-4 (nibble at bit 4)
       sk[3] = hmul2(sk[3], 0x2C002C00u);
     }
     uint32_t bh[4], bl[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const uint32_t t = hmul2(ph[k], sk[k]);
-      const uint32_t u = hfma2(ph[k], sk[k], t ^ kSign2);
+      const uint32_t t = hmul2(x3[k], sk[k]);
+      const uint32_t u = hfma2(ph[k], sk[k], hneg2(t));
       if (kComb) {
-        bh[k] = hfma2(plx[k], sk[k], is_lo ? u : t);
+        bh[k] = hfma2(x1[k], sk[k], u);
       } else {
         bh[k] = t;
-        bl[k] = hfma2(plx[k], sk[k], u);
+        bl[k] = hfma2(x1[k], sk[k], u);
       }
     }
     uint32_t wv[4];
@@ -390,87 +413,29 @@ __device__ __forceinline__ void softmax_pv(const uint8_t* blk, uint32_t live, in
         a[0][0] = unmagic(w0 & kM0); a[0][1] = unmagic(w1 & kM0); a[0][2] = unmagic(w0 & kM1); a[0][3] = unmagic(w1 & kM1);
         a[1][0] = unmagic(x0 & kM0); a[1][1] = unmagic(x1 & kM0); a[1][2] = unmagic(x0 & kM1); a[1][3] = unmagic(x1 & kM1);
       }
-      mma16816(o[m], a[0][0], a[0][1], a[0][2], a[0][3], bh[0], bh[1]);
-      mma16816(o[m], a[1][0], a[1][1], a[1][2], a[1][3], bh[2], bh[3]);
+      // This page's products go to a fresh accumulator, added to the running
+      // sum in fp32: the tensor core aligns products to the accumulator's
+      // magnitude, so accumulating many pages in place would truncate the
+      // small late contributions.
+      float t[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      mma16816(t, a[0][0], a[0][1], a[0][2], a[0][3], bh[0], bh[1]);
+      mma16816(t, a[1][0], a[1][1], a[1][2], a[1][3], bh[2], bh[3]);
       if (!kComb) {
-        mma16816(o[m], a[0][0], a[0][1], a[0][2], a[0][3], bl[0], bl[1]);
-        mma16816(o[m], a[1][0], a[1][1], a[1][2], a[1][3], bl[2], bl[3]);
+        mma16816(t, a[0][0], a[0][1], a[0][2], a[0][3], bl[0], bl[1]);
+        mma16816(t, a[1][0], a[1][1], a[1][2], a[1][3], bl[2], bl[3]);
       }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) o[m][c] += t[c];
     }
   }
   __syncwarp();
 }
 
+// q fragments (B operands of the K dot products) for one page precision.
 template <int G>
-__global__ void __launch_bounds__(kThreads, 4) decode_mma_kernel(
-    const uint8_t* __restrict__ pool, size_t int4_off, int64_t n2, int hkv, int max_pages,
-    const Entry* __restrict__ table, const __nv_bfloat16* __restrict__ q, int hq, float scale_log2,
-    const Unit* __restrict__ units, const Split* __restrict__ splits, float* __restrict__ part,
-    const uint32_t* __restrict__ smax_bits, uint32_t* __restrict__ status) {
+__device__ __forceinline__ void build_bq(const CtaSmem& S, bool int2, int r, int i, uint32_t (&bq)[16]) {
   constexpr bool kComb = G <= 4;
-  extern __shared__ __align__(128) uint8_t smem_raw[];
-  CtaSmem& S = *reinterpret_cast<CtaSmem*>(smem_raw);
-  const Split sp = splits[blockIdx.x];
-  const Unit u = units[sp.unit];
-  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, r = lane >> 2, i = lane & 3;
-  WarpSmem& WS = S.warp[w];
-
-  // ---- prologue: q of the packed heads, per-head power-of-two scale, constants
-  for (int x = tid; x < 8 * kHeadDim; x += kThreads) {
-    const int h = x >> 7, c = x & (kHeadDim - 1);
-    S.qraw[h][c] = h < G ? __bfloat162float(q[((size_t)u.b * hq + (size_t)u.kvh * G + h) * kHeadDim + c]) : 0.0f;
-  }
-  if (lane == 0) {
-    for (int st = 0; st < kStages; ++st) bar_init(&WS.bar[st]);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  __syncthreads();
-  const float smax = fmaxf(__uint_as_float(smax_bits[0]), 1.0f);
-  // P is carried as p * 2^sv in the fp16 folds so that p * scale * 2^-6 stays
-  // clear of the binary16 subnormal range; 2^sv * (largest V scale) <= 2^15.
-  const float vmax = fmaxf(__uint_as_float(smax_bits[1]), 1.0f / 1024.0f);
-  const int sv = max(0, min(15, ilogbf(32768.0f / vmax)));
-  const float pscale = ldexpf(1.0f, sv);
-  for (int h = w; h < 8; h += kWarps) {
-    float mx = 0.0f, qg[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      qg[k] = S.qraw[h][lane + 32 * k];           // channel lane + 32k is in group k
-      mx = fmaxf(mx, fabsf(qg[k]));
-    }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
-#pragma unroll
-      for (int k = 0; k < 4; ++k) qg[k] += __shfl_xor_sync(0xFFFFFFFFu, qg[k], o);
-    }
-    if (lane == 0) {
-      int E = 0;
-      if (mx > 0.0f) E = max(-100, min(100, ilogbf(16384.0f / (mx * smax))));
-      S.eh[h] = E;
-      S.acol[h] = ldexpf(scale_log2, -E);
-      unsigned short hi[4], lo[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) split_f16(scale_log2 * qg[k], hi[k], lo[k]);
-      S.bz[h][0] = hi[0] | ((uint32_t)hi[1] << 16);
-      S.bz[h][1] = hi[2] | ((uint32_t)hi[3] << 16);
-      S.bz[h][2] = lo[0] | ((uint32_t)lo[1] << 16);
-      S.bz[h][3] = lo[2] | ((uint32_t)lo[3] << 16);
-    }
-  }
-  for (int x = tid; x < 8 * kHeadDim; x += kThreads) {
-    const int h = x >> 7, pidx = x & (kHeadDim - 1);
-    const int pair = pidx >> 1, hi = pidx & 1;
-    const int j = pair & 7, iw = pair >> 3;      // iw = i*2 + wi
-    const int c = 4 * (4 * iw + (j >> 2)) + (j & 3) + 8 * hi;
-    S.qz[h][pidx] = S.qraw[h][c];
-  }
-  __syncthreads();
-
-  const bool is_int2 = sp.is_int2 != 0;
-  const bool is_lo = kComb && r >= 4;
-  uint32_t bq[16];
-  if (is_int2) {
+  if (int2) {
     const int hq2 = kComb ? (r & 3) : r;
     const int E = S.eh[hq2];
 #pragma unroll
@@ -496,124 +461,231 @@ __global__ void __launch_bounds__(kThreads, 4) decode_mma_kernel(
             n < G ? pack_h2(ldexpf(S.qraw[n][c1], E - 4), ldexpf(S.qraw[n][c1 + 4], E - 4)) : 0u;
       }
   }
-  const uint32_t bzl = r < G ? S.bz[r][i] : 0u;
-  const float acol[2] = {S.acol[2 * i], S.acol[2 * i + 1]};
+}
 
-  // ---- page loop: two-stage bulk-copy ring per warp
-  const Entry* tab = table + (size_t)u.req * max_pages;
-  const int npg = sp.page_end - sp.page_begin;
-  const int nw = npg > w ? (npg - w + kWarps - 1) / kWarps : 0;
-  const uint32_t bytes = is_int2 ? (uint32_t)kInt2Block : (uint32_t)kInt4Block;
-  auto block_of = [&](int k) -> const uint8_t* {
-    const int32_t id = tab[sp.page_begin + w + k * kWarps].id;
-    return is_int2 ? pool + ((size_t)id * hkv + u.kvh) * kInt2Block
-                   : pool + int4_off + ((size_t)(id - n2) * hkv + u.kvh) * kInt4Block;
-  };
-  if (lane == 0)
-    for (int k = 0; k < kStages && k < nw; ++k) bulk_load(WS.stage[k], block_of(k), bytes, &WS.bar[k]);
+// Persistent scan: CTA b owns segments [cta_split[b], cta_split[b+1]), each a
+// page range of one unit; the ranges are cut so every CTA gets about the same
+// cost.  Pages of either precision may share a segment: precision is uniform
+// per page, and a warp rebuilds its q fragments when it changes.
+template <int G>
+__global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(
+    const uint8_t* __restrict__ pool, size_t int4_off, int64_t n2, int hkv, int max_pages,
+    const Entry* __restrict__ table, const __nv_bfloat16* __restrict__ q, int hq, float scale_log2,
+    const Unit* __restrict__ units, const Split* __restrict__ splits, const int32_t* __restrict__ cta_split,
+    float* __restrict__ part, const uint32_t* __restrict__ smax_bits, uint32_t* __restrict__ status) {
+  constexpr bool kComb = G <= 4;
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  CtaSmem& S = *reinterpret_cast<CtaSmem*>(smem_raw);
+  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, r = lane >> 2, i = lane & 3;
+  WarpSmem& WS = S.warp[w];
+  if (lane == 0) {
+    for (int st = 0; st < kStages; ++st) bar_init(&WS.bar[st]);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  const float smax = fmaxf(__uint_as_float(smax_bits[0]), 1.0f);
+  // P is carried as p * 2^sv in the fp16 folds so that p * scale stays clear
+  // of the binary16 subnormal range; 2^sv * (largest V scale) <= 2^15.
+  const float vmax = fmaxf(__uint_as_float(smax_bits[1]), 1.0f / 1024.0f);
+  const int sv = max(0, min(15, ilogbf(32768.0f / vmax)));
+  const float pscale = ldexpf(1.0f, sv);
+  const bool is_lo = kComb && r >= 4;
+  uint32_t cnt = 0;   // bulk loads this warp has issued so far (all consumed at segment ends)
+  const int seg_end = cta_split[blockIdx.x + 1];
+  for (int sg = cta_split[blockIdx.x]; sg < seg_end; ++sg) {
+    const Split sp = splits[sg];
+    const Unit u = units[sp.unit];
+    __syncthreads();   // the previous segment's merge has finished reading shared memory
 
-  float o[8][4], zv[4] = {0.0f, 0.0f, 0.0f, 0.0f}, mrun[2] = {-INFINITY, -INFINITY}, lsum[2] = {0.0f, 0.0f};
-#pragma unroll
-  for (int m = 0; m < 8; ++m) o[m][0] = o[m][1] = o[m][2] = o[m][3] = 0.0f;
-  int k = 0;
-  bool ok = true;
-  for (; k < nw; ++k) {
-    const int st = k & (kStages - 1);
-    const uint32_t ph = (uint32_t)(k / kStages) & 1u;
-    const bool got = bar_wait(&WS.bar[st], ph);
-    if (!__all_sync(0xFFFFFFFFu, got)) { ok = false; break; }
-    const uint32_t live = tab[sp.page_begin + w + k * kWarps].live;
-    const uint8_t* blk = WS.stage[st];
-    float lg[2][4];
-    if (is_int2) {
-      qk_int2<G>(blk, bq, r, i, is_lo, acol, scale_log2, S.qz, lg);
-      softmax_pv<G, true>(blk, live, r, i, is_lo, pscale, lg, o, zv, mrun, lsum, WS.pbuf);
-    } else {
-      qk_int4<G>(blk, bq, bzl, r, i, acol, lg);
-      softmax_pv<G, false>(blk, live, r, i, is_lo, pscale, lg, o, zv, mrun, lsum, WS.pbuf);
+    // ---- unit prologue: q of the packed heads, per-head power-of-two scale, constants
+    for (int x = tid; x < 8 * kHeadDim; x += kThreads) {
+      const int h = x >> 7, c = x & (kHeadDim - 1);
+      S.qraw[h][c] = h < G ? __bfloat162float(q[((size_t)u.b * hq + (size_t)u.kvh * G + h) * kHeadDim + c]) : 0.0f;
     }
-    if (lane == 0 && k + kStages < nw) {
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      bulk_load(WS.stage[st], block_of(k + kStages), bytes, &WS.bar[st]);
+    __syncthreads();
+    for (int h = w; h < 8; h += kWarps) {
+      float mx = 0.0f, qg[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        qg[k] = S.qraw[h][lane + 32 * k];           // channel lane + 32k is in group k
+        mx = fmaxf(mx, fabsf(qg[k]));
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+#pragma unroll
+        for (int k = 0; k < 4; ++k) qg[k] += __shfl_xor_sync(0xFFFFFFFFu, qg[k], o);
+      }
+      if (lane == 0) {
+        int E = 0;
+        if (mx > 0.0f) E = max(-100, min(100, ilogbf(16384.0f / (mx * smax))));
+        S.eh[h] = E;
+        S.acol[h] = ldexpf(scale_log2, -E);
+        unsigned short hi[4], lo[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) split_f16(scale_log2 * qg[k], hi[k], lo[k]);
+        S.bz[h][0] = hi[0] | ((uint32_t)hi[1] << 16);
+        S.bz[h][1] = hi[2] | ((uint32_t)hi[3] << 16);
+        S.bz[h][2] = lo[0] | ((uint32_t)lo[1] << 16);
+        S.bz[h][3] = lo[2] | ((uint32_t)lo[3] << 16);
+      }
     }
-  }
-  if (!ok) {
-    if (lane == 0) atomicOr(status, kStatusTimeout);
-    for (int kk = k; kk < nw && kk < k + kStages; ++kk)
-      bar_wait(&WS.bar[kk & (kStages - 1)], (uint32_t)(kk / kStages) & 1u);
-    mrun[0] = mrun[1] = -INFINITY;
-  }
+    for (int x = tid; x < 8 * kHeadDim; x += kThreads) {
+      const int h = x >> 7, pidx = x & (kHeadDim - 1);
+      const int pair = pidx >> 1, hi = pidx & 1;
+      const int j = pair & 7, iw = pair >> 3;      // iw = i*2 + wi
+      const int c = 4 * (4 * iw + (j >> 2)) + (j & 3) + 8 * hi;
+      S.qz[h][pidx] = S.qraw[h][c];
+    }
+    __syncthreads();
+    const uint32_t bzl = r < G ? S.bz[r][i] : 0u;
+    const float acol[2] = {S.acol[2 * i], S.acol[2 * i + 1]};
 
-  // ---- per-warp epilogue: finish l, combine hi/lo columns, add the V zero term
+    // ---- page loop: two-stage bulk-copy ring per warp
+    const Entry* tab = table + (size_t)u.req * max_pages;
+    const int npg = sp.page_end - sp.page_begin;
+    const int nw = npg > w ? (npg - w + kWarps - 1) / kWarps : 0;
+    // Table entries of the pages in flight, loaded when their copy is issued
+    // (all lanes load the same 8 bytes), so the per-page read is not exposed.
+    static_assert(kStages == 2, "the entry ring below holds two entries");
+    Entry ent0 = Entry{0, 0u}, ent1 = Entry{0, 0u};    // registers, not an indexed (local-memory) array
+    auto ent_get = [&](uint32_t st) { return st ? ent1 : ent0; };
+    auto ent_set = [&](uint32_t st, Entry v) {
+      if (st) ent1 = v; else ent0 = v;
+    };
+    auto issue = [&](int k) {
+      const int32_t id = ent_get((cnt + (uint32_t)k) & (kStages - 1)).id;
+      const bool i2 = id < n2;
+      const uint8_t* src = i2 ? pool + ((size_t)id * hkv + u.kvh) * kInt2Block
+                              : pool + int4_off + ((size_t)(id - n2) * hkv + u.kvh) * kInt4Block;
+      const uint32_t st = (cnt + (uint32_t)k) & (kStages - 1);
+      bulk_load(WS.stage[st], src, i2 ? (uint32_t)kInt2Block : (uint32_t)kInt4Block, &WS.bar[st]);
+    };
 #pragma unroll
-  for (int hh = 0; hh < 2; ++hh) {
-    lsum[hh] += __shfl_xor_sync(0xFFFFFFFFu, lsum[hh], 4);
-    lsum[hh] += __shfl_xor_sync(0xFFFFFFFFu, lsum[hh], 8);
-    lsum[hh] += __shfl_xor_sync(0xFFFFFFFFu, lsum[hh], 16);
-  }
-  if (kComb) {
+    for (int k = 0; k < kStages; ++k)
+      if (k < nw) ent_set((cnt + (uint32_t)k) & (kStages - 1), tab[sp.page_begin + w + k * kWarps]);
+    if (lane == 0) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // stages were read/written generically
+      for (int k = 0; k < kStages && k < nw; ++k) issue(k);
+    }
+    float o[8][4], zv[4] = {0.0f, 0.0f, 0.0f, 0.0f}, mrun[2] = {-INFINITY, -INFINITY}, lsum[2] = {0.0f, 0.0f};
 #pragma unroll
-    for (int m = 0; m < 8; ++m)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) o[m][c] += __shfl_xor_sync(0xFFFFFFFFu, o[m][c], 2);
-  }
-  if (r < 4) {
-    S.zv[w][r][2 * i] = zv[0];
-    S.zv[w][r][2 * i + 1] = zv[1];
-  }
-  __syncwarp();
-  float* accw = reinterpret_cast<float*>(WS.stage[0]);   // [8][128], the ring is idle now
-  const bool valid = !kComb || i < 2;
-  if (valid) {
-#pragma unroll
-    for (int m = 0; m < 8; ++m)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int h = 2 * i + (c & 1), ch = 16 * m + r + 8 * (c >> 1);
-        if (h < G) {
-          float zt = S.zv[w][m >> 1][h];
-          if (kComb) zt += S.zv[w][m >> 1][h + 4];
-          accw[h * kHeadDim + ch] = (o[m][c] + zt) * ldexpf(1.0f, -sv);
+    for (int m = 0; m < 8; ++m) o[m][0] = o[m][1] = o[m][2] = o[m][3] = 0.0f;
+    uint32_t bq[16];
+    int cur = -1;                      // precision the bq fragments were built for
+    int k = 0;
+    bool ok = true;
+    for (; k < nw; ++k) {
+      const uint32_t c = cnt + (uint32_t)k;
+      const uint32_t st = c & (kStages - 1);
+      const bool got = bar_wait(&WS.bar[st], (c / kStages) & 1u);
+      if (!__all_sync(0xFFFFFFFFu, got)) { ok = false; break; }
+      const Entry e = ent_get(st);
+      const bool i2 = e.id < n2;
+      if ((int)i2 != cur) {
+        build_bq<G>(S, i2, r, i, bq);
+        cur = (int)i2;
+      }
+      const uint8_t* blk = WS.stage[st];
+      float lg[2][4];
+      if (i2) {
+        qk_int2<G>(blk, bq, r, i, is_lo, acol, scale_log2, S.qz, lg);
+        softmax_pv<G, true>(blk, e.live, r, i, is_lo, pscale, lg, o, zv, mrun, lsum, WS.pbuf);
+      } else {
+        qk_int4<G>(blk, bq, bzl, r, i, acol, lg);
+        softmax_pv<G, false>(blk, e.live, r, i, is_lo, pscale, lg, o, zv, mrun, lsum, WS.pbuf);
+      }
+      if (k + kStages < nw) {
+        ent_set(st, tab[sp.page_begin + w + (k + kStages) * kWarps]);
+        if (lane == 0) {
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          issue(k + kStages);
         }
       }
-    if (r == 0)
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh)
-        if (2 * i + hh < G) {
-          S.mw[w][2 * i + hh] = mrun[hh];
-          S.lw[w][2 * i + hh] = lsum[hh];
-        }
-  }
-  __syncthreads();
+    }
+    if (!ok) {
+      if (lane == 0) atomicOr(status, kStatusTimeout);
+      const int issued = nw < k + kStages ? nw : k + kStages;
+      for (int kk = k; kk < issued; ++kk) {
+        const uint32_t c = cnt + (uint32_t)kk;
+        bar_wait(&WS.bar[c & (kStages - 1)], (c / kStages) & 1u);
+      }
+      mrun[0] = mrun[1] = -INFINITY;
+    }
+    cnt += (uint32_t)nw;
 
-  // ---- merge the warps: one thread per channel
-  float* out = part + (size_t)blockIdx.x * G * kPartStride;
-  const int c = tid;
+    // ---- per-warp epilogue: finish l, combine hi/lo columns, add the V zero term
 #pragma unroll
-  for (int h = 0; h < G; ++h) {
-    float M = -INFINITY;
-#pragma unroll
-    for (int ww = 0; ww < kWarps; ++ww) M = fmaxf(M, S.mw[ww][h]);
-    float L = 0.0f, A = 0.0f;
-#pragma unroll
-    for (int ww = 0; ww < kWarps; ++ww) {
-      const float mw = S.mw[ww][h];
-      if (mw == -INFINITY) continue;
-      const float f = exp2f(mw - M);
-      L += S.lw[ww][h] * f;
-      A += reinterpret_cast<const float*>(S.warp[ww].stage[0])[h * kHeadDim + c] * f;
+    for (int hh = 0; hh < 2; ++hh) {
+      lsum[hh] += __shfl_xor_sync(0xFFFFFFFFu, lsum[hh], 4);
+      lsum[hh] += __shfl_xor_sync(0xFFFFFFFFu, lsum[hh], 8);
+      lsum[hh] += __shfl_xor_sync(0xFFFFFFFFu, lsum[hh], 16);
     }
-    out[h * kPartStride + c] = A;
-    if (c == 0) {
-      out[h * kPartStride + kHeadDim] = M;
-      out[h * kPartStride + kHeadDim + 1] = L;
+    if (kComb) {
+#pragma unroll
+      for (int m = 0; m < 8; ++m)
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) o[m][cc] += __shfl_xor_sync(0xFFFFFFFFu, o[m][cc], 2);
     }
+    if (r < 4) {
+      S.zv[w][r][2 * i] = zv[0];
+      S.zv[w][r][2 * i + 1] = zv[1];
+    }
+    __syncwarp();
+    float* accw = reinterpret_cast<float*>(WS.stage[0]);   // [8][128], the ring is idle now
+    const bool valid = !kComb || i < 2;
+    const float oscale = ldexpf(1.0f, -sv);
+    if (valid) {
+#pragma unroll
+      for (int m = 0; m < 8; ++m)
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          const int h = 2 * i + (cc & 1), ch = 16 * m + r + 8 * (cc >> 1);
+          if (h < G) {
+            float zt = S.zv[w][m >> 1][h];
+            if (kComb) zt += S.zv[w][m >> 1][h + 4];
+            accw[h * kHeadDim + ch] = (o[m][cc] + zt) * oscale;
+          }
+        }
+      if (r == 0)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+          if (2 * i + hh < G) {
+            S.mw[w][2 * i + hh] = mrun[hh];
+            S.lw[w][2 * i + hh] = lsum[hh];
+          }
+    }
+    const bool all_ok = __syncthreads_and(ok) != 0;
+
+    // ---- merge the warps: one thread per channel
+    float* out = part + (size_t)sg * G * kPartStride;
+    const int ch = tid;
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      float M = -INFINITY;
+#pragma unroll
+      for (int ww = 0; ww < kWarps; ++ww) M = fmaxf(M, S.mw[ww][h]);
+      float L = 0.0f, A = 0.0f;
+#pragma unroll
+      for (int ww = 0; ww < kWarps; ++ww) {
+        const float mw = S.mw[ww][h];
+        if (mw == -INFINITY) continue;
+        const float f = exp2f(mw - M);
+        L += S.lw[ww][h] * f;
+        A += reinterpret_cast<const float*>(S.warp[ww].stage[0])[h * kHeadDim + ch] * f;
+      }
+      out[h * kPartStride + ch] = A;
+      if (ch == 0) {
+        out[h * kPartStride + kHeadDim] = M;
+        out[h * kPartStride + kHeadDim + 1] = L;
+      }
+    }
+    if (!all_ok) break;
   }
 }
 
 template <int G>
 cudaError_t launch_mma_g(kv_pool* P, const void* q, int32_t hq, float scale_log2, const Unit* d_units,
-                         const Split* d_splits, int n_splits, float* d_part, cudaStream_t s) {
+                         const Split* d_splits, const int32_t* d_cta, int n_ctas, float* d_part, cudaStream_t s) {
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -621,11 +693,11 @@ cudaError_t launch_mma_g(kv_pool* P, const void* q, int32_t hq, float scale_log2
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  if (n_splits <= 0) return cudaSuccess;
+  if (n_ctas <= 0) return cudaSuccess;
   ++P->launches;
-  decode_mma_kernel<G><<<n_splits, kThreads, sizeof(CtaSmem), s>>>(
+  decode_mma_kernel<G><<<n_ctas, kThreads, sizeof(CtaSmem), s>>>(
       P->d_pool, P->int4_offset, P->cfg.n_int2_pages, P->cfg.num_kv_heads, P->cfg.max_pages_per_request, P->d_table,
-      (const __nv_bfloat16*)q, hq, scale_log2, d_units, d_splits, d_part, P->d_status + 1, P->d_status);
+      (const __nv_bfloat16*)q, hq, scale_log2, d_units, d_splits, d_cta, d_part, P->d_status + 1, P->d_status);
   return cudaGetLastError();
 }
 
@@ -643,20 +715,22 @@ int mma_occupancy() {
 }  // namespace
 
 cudaError_t launch_decode_mma(kv_pool* P, const void* q, int32_t hq, float scale_log2, const Unit* d_units, int n_units,
-                              const Split* d_splits, int n_splits, float* d_part, float* out, cudaStream_t s) {
+                              const Split* d_splits, const int32_t* d_cta, int n_ctas, float* d_part, float* out,
+                              cudaStream_t s) {
   cudaError_t e;
   switch (hq / P->cfg.num_kv_heads) {
-    case 1: e = launch_mma_g<1>(P, q, hq, scale_log2, d_units, d_splits, n_splits, d_part, s); break;
-    case 2: e = launch_mma_g<2>(P, q, hq, scale_log2, d_units, d_splits, n_splits, d_part, s); break;
-    case 3: e = launch_mma_g<3>(P, q, hq, scale_log2, d_units, d_splits, n_splits, d_part, s); break;
-    case 4: e = launch_mma_g<4>(P, q, hq, scale_log2, d_units, d_splits, n_splits, d_part, s); break;
-    case 5: e = launch_mma_g<5>(P, q, hq, scale_log2, d_units, d_splits, n_splits, d_part, s); break;
-    case 6: e = launch_mma_g<6>(P, q, hq, scale_log2, d_units, d_splits, n_splits, d_part, s); break;
-    case 7: e = launch_mma_g<7>(P, q, hq, scale_log2, d_units, d_splits, n_splits, d_part, s); break;
-    case 8: e = launch_mma_g<8>(P, q, hq, scale_log2, d_units, d_splits, n_splits, d_part, s); break;
+    case 1: e = launch_mma_g<1>(P, q, hq, scale_log2, d_units, d_splits, d_cta, n_ctas, d_part, s); break;
+    case 2: e = launch_mma_g<2>(P, q, hq, scale_log2, d_units, d_splits, d_cta, n_ctas, d_part, s); break;
+    case 3: e = launch_mma_g<3>(P, q, hq, scale_log2, d_units, d_splits, d_cta, n_ctas, d_part, s); break;
+    case 4: e = launch_mma_g<4>(P, q, hq, scale_log2, d_units, d_splits, d_cta, n_ctas, d_part, s); break;
+    case 5: e = launch_mma_g<5>(P, q, hq, scale_log2, d_units, d_splits, d_cta, n_ctas, d_part, s); break;
+    case 6: e = launch_mma_g<6>(P, q, hq, scale_log2, d_units, d_splits, d_cta, n_ctas, d_part, s); break;
+    case 7: e = launch_mma_g<7>(P, q, hq, scale_log2, d_units, d_splits, d_cta, n_ctas, d_part, s); break;
+    case 8: e = launch_mma_g<8>(P, q, hq, scale_log2, d_units, d_splits, d_cta, n_ctas, d_part, s); break;
     default: return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess) return e;
+  if (P->merge_event && (e = cudaEventRecord(P->merge_event, s)) != cudaSuccess) return e;
   return launch_merge(P, hq / P->cfg.num_kv_heads, d_units, n_units, d_part, hq, out, s);
 }
 

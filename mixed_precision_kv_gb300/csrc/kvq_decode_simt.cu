@@ -42,13 +42,16 @@ template <int G>
 __global__ void __launch_bounds__(kThreads) decode_simt_kernel(
     const uint8_t* __restrict__ pool, size_t int4_off, int64_t n2, int hkv, int max_pages,
     const Entry* __restrict__ table, const __nv_bfloat16* __restrict__ q, int hq, float scale_log2,
-    const Unit* __restrict__ units, const Split* __restrict__ splits, float* __restrict__ part) {
+    const Unit* __restrict__ units, const Split* __restrict__ splits, const int32_t* __restrict__ cta_split,
+    float* __restrict__ part) {
   __shared__ float qs[G][kHeadDim];
   __shared__ __align__(16) uint8_t buf[kWarps][kInt4Block];
   __shared__ float pb[kWarps][kPage][G];
   __shared__ float wm[kWarps][G], wl[kWarps][G];
 
-  const Split sp = splits[blockIdx.x];
+  for (int sg = cta_split[blockIdx.x]; sg < cta_split[blockIdx.x + 1]; ++sg) {
+  __syncthreads();
+  const Split sp = splits[sg];
   const Unit u = units[sp.unit];
   for (int i = threadIdx.x; i < G * kHeadDim; i += kThreads) {
     const int h = i / kHeadDim, c = i % kHeadDim;
@@ -149,7 +152,7 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(
 #pragma unroll
     for (int a = 0; a < 4; ++a) ab[(w * G + h) * kHeadDim + 4 * lane + a] = acc[h][a];
   __syncthreads();
-  float* out = part + (size_t)blockIdx.x * G * kPartStride;
+  float* out = part + (size_t)sg * G * kPartStride;
   const int c = threadIdx.x;
   for (int h = 0; h < G; ++h) {
     float M = -INFINITY;
@@ -167,38 +170,61 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(
       out[h * kPartStride + kHeadDim + 1] = L;
     }
   }
+  }
 }
 
 // One warp per (unit, head): O = sum_s acc_s 2^(m_s - M) / sum_s l_s 2^(m_s - M).
+// Lanes first take the splits' m in parallel (warp max), then every lane
+// weighs its four channels of each split; the split loads are independent so
+// they overlap instead of forming a dependent chain.
 template <int G>
 __global__ void merge_kernel(const Unit* __restrict__ units, const float* __restrict__ part, int hq,
                              float* __restrict__ out) {
   const Unit u = units[blockIdx.x];
   const int h = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float* o = out + ((size_t)u.b * hq + (size_t)u.kvh * G + h) * kHeadDim + 4 * lane;
+  const float* base = part + ((size_t)u.split_begin * G + h) * kPartStride;
+  const size_t rs = (size_t)G * kPartStride;          // stride between splits
+  const int n = u.n_splits;
   float M = -INFINITY;
-  for (int s = 0; s < u.n_splits; ++s)
-    M = fmaxf(M, part[((size_t)(u.split_begin + s) * G + h) * kPartStride + kHeadDim]);
-  float L = 0.0f, A[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-  for (int s = 0; s < u.n_splits; ++s) {
-    const float* ps = part + ((size_t)(u.split_begin + s) * G + h) * kPartStride;
-    const float f = exp2f(ps[kHeadDim] - M);
-    L += ps[kHeadDim + 1] * f;
-    const float4 a = *reinterpret_cast<const float4*>(ps + 4 * lane);
-    A[0] += a.x * f; A[1] += a.y * f; A[2] += a.z * f; A[3] += a.w * f;
+  for (int s = lane; s < n; s += 32) M = fmaxf(M, base[s * rs + kHeadDim]);
+#pragma unroll
+  for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, off));
+  float L = 0.0f, A0 = 0.0f, A1 = 0.0f, A2 = 0.0f, A3 = 0.0f;
+  for (int s0 = 0; s0 < n; s0 += 32) {
+    const int s = s0 + lane;
+    float f = 0.0f;
+    if (s < n) {
+      f = exp2f(base[s * rs + kHeadDim] - M);
+      L += f * base[s * rs + kHeadDim + 1];
+    }
+    const int cnt = min(32, n - s0);
+#pragma unroll 4
+    for (int j = 0; j < cnt; ++j) {
+      const float fj = __shfl_sync(0xFFFFFFFFu, f, j);
+      const float4 a = *reinterpret_cast<const float4*>(base + (size_t)(s0 + j) * rs + 4 * lane);
+      A0 = fmaf(a.x, fj, A0); A1 = fmaf(a.y, fj, A1); A2 = fmaf(a.z, fj, A2); A3 = fmaf(a.w, fj, A3);
+    }
   }
+#pragma unroll
+  for (int off = 16; off; off >>= 1) L += __shfl_xor_sync(0xFFFFFFFFu, L, off);
   const float inv = L > 0.0f ? 1.0f / L : 0.0f;
-  *reinterpret_cast<float4*>(o) = make_float4(A[0] * inv, A[1] * inv, A[2] * inv, A[3] * inv);
+  *reinterpret_cast<float4*>(o) = make_float4(A0 * inv, A1 * inv, A2 * inv, A3 * inv);
 }
 
 template <int G>
 cudaError_t launch_g(kv_pool* P, const void* q, int32_t hq, float scale_log2, const Unit* d_units, int n_units,
-                     const Split* d_splits, int n_splits, float* d_part, float* out, cudaStream_t s) {
-  if (n_splits > 0) {
+                     const Split* d_splits, const int32_t* d_cta, int n_ctas, float* d_part, float* out,
+                     cudaStream_t s) {
+  if (n_ctas > 0) {
     ++P->launches;
-    decode_simt_kernel<G><<<n_splits, kThreads, 0, s>>>(
+    decode_simt_kernel<G><<<n_ctas, kThreads, 0, s>>>(
         P->d_pool, P->int4_offset, P->cfg.n_int2_pages, P->cfg.num_kv_heads, P->cfg.max_pages_per_request,
-        P->d_table, (const __nv_bfloat16*)q, hq, scale_log2, d_units, d_splits, d_part);
+        P->d_table, (const __nv_bfloat16*)q, hq, scale_log2, d_units, d_splits, d_cta, d_part);
+  }
+  if (P->merge_event) {
+    const cudaError_t e = cudaEventRecord(P->merge_event, s);
+    if (e != cudaSuccess) return e;
   }
   return launch_merge(P, G, d_units, n_units, d_part, hq, out, s);
 }
@@ -223,17 +249,17 @@ cudaError_t launch_merge(kv_pool* P, int g, const Unit* d_units, int n_units, co
 }
 
 cudaError_t launch_decode_simt(kv_pool* P, const void* q, int32_t hq, float scale_log2, const Unit* d_units,
-                               int n_units, const Split* d_splits, int n_splits, float* d_part, float* out,
-                               cudaStream_t s) {
+                               int n_units, const Split* d_splits, const int32_t* d_cta, int n_ctas, float* d_part,
+                               float* out, cudaStream_t s) {
   switch (hq / P->cfg.num_kv_heads) {
-    case 1: return launch_g<1>(P, q, hq, scale_log2, d_units, n_units, d_splits, n_splits, d_part, out, s);
-    case 2: return launch_g<2>(P, q, hq, scale_log2, d_units, n_units, d_splits, n_splits, d_part, out, s);
-    case 3: return launch_g<3>(P, q, hq, scale_log2, d_units, n_units, d_splits, n_splits, d_part, out, s);
-    case 4: return launch_g<4>(P, q, hq, scale_log2, d_units, n_units, d_splits, n_splits, d_part, out, s);
-    case 5: return launch_g<5>(P, q, hq, scale_log2, d_units, n_units, d_splits, n_splits, d_part, out, s);
-    case 6: return launch_g<6>(P, q, hq, scale_log2, d_units, n_units, d_splits, n_splits, d_part, out, s);
-    case 7: return launch_g<7>(P, q, hq, scale_log2, d_units, n_units, d_splits, n_splits, d_part, out, s);
-    case 8: return launch_g<8>(P, q, hq, scale_log2, d_units, n_units, d_splits, n_splits, d_part, out, s);
+    case 1: return launch_g<1>(P, q, hq, scale_log2, d_units, n_units, d_splits, d_cta, n_ctas, d_part, out, s);
+    case 2: return launch_g<2>(P, q, hq, scale_log2, d_units, n_units, d_splits, d_cta, n_ctas, d_part, out, s);
+    case 3: return launch_g<3>(P, q, hq, scale_log2, d_units, n_units, d_splits, d_cta, n_ctas, d_part, out, s);
+    case 4: return launch_g<4>(P, q, hq, scale_log2, d_units, n_units, d_splits, d_cta, n_ctas, d_part, out, s);
+    case 5: return launch_g<5>(P, q, hq, scale_log2, d_units, n_units, d_splits, d_cta, n_ctas, d_part, out, s);
+    case 6: return launch_g<6>(P, q, hq, scale_log2, d_units, n_units, d_splits, d_cta, n_ctas, d_part, out, s);
+    case 7: return launch_g<7>(P, q, hq, scale_log2, d_units, n_units, d_splits, d_cta, n_ctas, d_part, out, s);
+    case 8: return launch_g<8>(P, q, hq, scale_log2, d_units, n_units, d_splits, d_cta, n_ctas, d_part, out, s);
     default: return cudaErrorInvalidValue;
   }
 }

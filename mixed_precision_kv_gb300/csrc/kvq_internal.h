@@ -44,7 +44,8 @@ struct RepackJob {
   int32_t dst;  // INT2 page id
 };
 
-// Work unit of the decode: one (batch row, kv head); splits are page ranges.
+// Work unit of the decode: one (batch row, kv head).  Its splits (page ranges,
+// one partial each) are contiguous in the split list.
 struct Unit {
   int32_t b;            // batch row
   int32_t req;          // request id
@@ -54,11 +55,27 @@ struct Unit {
   int32_t pad[3];
 };
 
+// A split: a page range of one unit, scanned by one CTA.  A CTA scans the
+// contiguous split range [cta_split[cta], cta_split[cta + 1]).
 struct Split {
   int32_t unit;
   int32_t page_begin;   // table index range [page_begin, page_end)
   int32_t page_end;
-  int32_t is_int2;
+  int32_t cta;
+};
+
+// Planner cost of one page: its block bytes plus this fixed term for the
+// scan's per-page compute.
+constexpr double kPageCost = 2048.0;
+constexpr int64_t kMinPagesPerCta = 16;
+constexpr int64_t kTimingRing = 2048;
+
+// Decode plan on the host (see plan_decode).
+struct HostPlan {
+  std::vector<Unit> units;
+  std::vector<Split> splits;
+  std::vector<int32_t> cta_split;   // n_ctas + 1 entries
+  int64_t n_ctas() const { return (int64_t)cta_split.size() - 1; }
 };
 
 struct Request {
@@ -102,12 +119,17 @@ struct kv_pool {
   int32_t plan_hq = 0;
   int32_t plan_impl = -1;
   int32_t n_units = 0, n_splits = 0;
-  size_t plan_units_off = 0, plan_splits_off = 0;
+  size_t plan_units_off = 0, plan_splits_off = 0, plan_cta_off = 0;
+  int32_t n_ctas = 0;
   std::vector<int32_t> stat_req;      // request ids of the last decode (for kv_last_decode_stats)
   int32_t stat_hq = 0;
   int32_t decode_impl = KV_DECODE_AUTO;
   cudaStream_t last_stream = nullptr;
   int64_t launches = 0;               // kernels launched by this pool
+  bool timing = false;                // record events around the decode kernels
+  int64_t timed_calls = 0;            // decode calls recorded since timing started
+  std::vector<cudaEvent_t> tev;       // ring of [before scan, after scan, after merge] per call
+  cudaEvent_t merge_event = nullptr;  // recorded by the launchers between scan and merge when timing
 };
 
 namespace kvq {
@@ -121,13 +143,19 @@ cudaError_t launch_append(kv_pool* P, const void* k, const void* v, const Append
 cudaError_t launch_repack(kv_pool* P, const RepackJob* d_jobs, int n_jobs, cudaStream_t s);
 cudaError_t launch_scatter(kv_pool* P, const TableUpd* d_upd, int n, cudaStream_t s);
 
+// Balanced decode plan: units (batch row, kv head) in order, their pages cut
+// into n_ctas contiguous ranges of about equal cost (bytes + a fixed per-page
+// term), each range split further at unit boundaries (kvq_pool.cu).
+void plan_decode(const kv_pool* P, const int32_t* req_ids, int32_t batch, int64_t n_ctas, HostPlan& out);
+
 // Launchers (kvq_decode_simt.cu / kvq_decode_mma.cu)
 cudaError_t launch_decode_simt(kv_pool* P, const void* q, int32_t hq, float scale_log2, const Unit* d_units,
-                               int n_units, const Split* d_splits, int n_splits, float* d_part, float* out,
-                               cudaStream_t s);
+                               int n_units, const Split* d_splits, const int32_t* d_cta, int n_ctas, float* d_part,
+                               float* out, cudaStream_t s);
 int decode_simt_ctas_per_sm(int g);
 cudaError_t launch_decode_mma(kv_pool* P, const void* q, int32_t hq, float scale_log2, const Unit* d_units, int n_units,
-                              const Split* d_splits, int n_splits, float* d_part, float* out, cudaStream_t s);
+                              const Split* d_splits, const int32_t* d_cta, int n_ctas, float* d_part, float* out,
+                              cudaStream_t s);
 int decode_mma_ctas_per_sm(int g);
 // Split merge: out[b][h][:] = sum_s acc_s 2^(m_s - M) / sum_s l_s 2^(m_s - M) over the unit's splits.
 cudaError_t launch_merge(kv_pool* P, int g, const Unit* d_units, int n_units, const float* d_part, int hq, float* out,

@@ -89,66 +89,28 @@ extern "C" kv_status_t kv_decode_attn_noalloc(kv_pool_t* P, const void* q, const
   if (scratch_address(P->cfg.device, &scratch) != cudaSuccess)
     return nfail(KV_ERR_CUDA, "kv_decode_attn_noalloc: cudaGetSymbolAddress of the scratch array failed");
 
-  // Plan: same policy as kv_decode_attn (pure-precision runs cut into
-  // near-equal page ranges of about total / (SMs x CTAs per SM) bytes), with
-  // the split count capped so plan + partials fit the scratch.
+  // Plan: the same balanced plan as kv_decode_attn, with the CTA count capped
+  // so that plan + partials fit the scratch (a plan of n CTAs has at most
+  // n + units - 1 splits).
   const int32_t impl = P->decode_impl == KV_DECODE_AUTO ? KV_DECODE_MMA : P->decode_impl;
   const int ctas = impl == KV_DECODE_MMA ? decode_mma_ctas_per_sm(g) : decode_simt_ctas_per_sm(g);
   const size_t part_bytes = (size_t)g * (kHeadDim + 4) * sizeof(float);
   const size_t units_bytes = align256((size_t)n_units * sizeof(Unit));
-  const int64_t max_splits = (int64_t)((kScratchBytes - units_bytes - 512) / (sizeof(Split) + part_bytes));
-  struct Run { int32_t b, begin, end; bool i2; };
-  std::vector<Run> runs;
-  double total = 0.0;
-  for (int32_t b = 0; b < batch; ++b) {
-    const auto& tb = P->reqs[req_ids[b]].table;
-    for (int32_t i = 0; i < (int32_t)tb.size();) {
-      const bool i2 = tb[i] < P->cfg.n_int2_pages;
-      int32_t j = i + 1;
-      while (j < (int32_t)tb.size() && (tb[j] < P->cfg.n_int2_pages) == i2) ++j;
-      runs.push_back(Run{b, i, j, i2});
-      total += (double)(j - i) * (i2 ? kInt2Block : kInt4Block) * hkv;
-      i = j;
-    }
-  }
-  const int64_t min_splits = (int64_t)runs.size() * hkv;
-  if (min_splits > max_splits)
-    return nfail(KV_ERR_INVALID_ARG, "kv_decode_attn_noalloc: the tables hold more precision runs than the fixed scratch can plan");
-  const double target = std::min<double>((double)P->sm_count * ctas, (double)(max_splits - min_splits) + 1.0);
-  const double chunk = std::max(total / std::max(target, 1.0), 8.0 * kInt2Block);
-
-  std::vector<Unit> units((size_t)n_units);
-  std::vector<Split> splits;
-  size_t ri = 0;
-  for (int32_t b = 0; b < batch; ++b) {
-    const size_t r0 = ri;
-    while (ri < runs.size() && runs[ri].b == b) ++ri;
-    for (int h = 0; h < hkv; ++h) {
-      Unit& u = units[(size_t)b * hkv + h];
-      u = Unit{};
-      u.b = b;
-      u.req = req_ids[b];
-      u.kvh = h;
-      u.split_begin = (int32_t)splits.size();
-      for (size_t k = r0; k < ri; ++k) {
-        const int32_t np = runs[k].end - runs[k].begin;
-        const double bytes = (double)np * (runs[k].i2 ? kInt2Block : kInt4Block);
-        const int32_t ns = std::max<int32_t>(1, std::min<int32_t>(np, (int32_t)std::ceil(bytes / chunk)));
-        for (int32_t s = 0; s < ns; ++s)
-          splits.push_back(Split{(int32_t)((size_t)b * hkv + h), runs[k].begin + (int32_t)((int64_t)np * s / ns),
-                                 runs[k].begin + (int32_t)((int64_t)np * (s + 1) / ns), runs[k].i2 ? 1 : 0});
-      }
-      u.n_splits = (int32_t)splits.size() - u.split_begin;
-    }
-  }
-  if ((int64_t)splits.size() > max_splits)
+  const int64_t budget = (int64_t)((kScratchBytes - units_bytes - 1024) / (sizeof(Split) + sizeof(int32_t) + part_bytes));
+  const int64_t n_ctas = std::min<int64_t>((int64_t)P->sm_count * ctas, budget - n_units);
+  if (n_ctas < 1)
     return nfail(KV_ERR_INVALID_ARG, "kv_decode_attn_noalloc: the plan does not fit the fixed scratch");
-
+  HostPlan hp;
+  plan_decode(P, req_ids, batch, n_ctas, hp);
   const size_t splits_off = units_bytes;
-  const size_t part_off = align256(splits_off + splits.size() * sizeof(Split));
+  const size_t cta_off = align256(splits_off + hp.splits.size() * sizeof(Split));
+  const size_t part_off = align256(cta_off + hp.cta_split.size() * sizeof(int32_t));
+  if (part_off + hp.splits.size() * part_bytes > kScratchBytes)
+    return nfail(KV_ERR_INVALID_ARG, "kv_decode_attn_noalloc: the plan does not fit the fixed scratch");
   std::vector<uint8_t> host(part_off, 0);
-  std::memcpy(host.data(), units.data(), units.size() * sizeof(Unit));
-  if (!splits.empty()) std::memcpy(host.data() + splits_off, splits.data(), splits.size() * sizeof(Split));
+  std::memcpy(host.data(), hp.units.data(), hp.units.size() * sizeof(Unit));
+  if (!hp.splits.empty()) std::memcpy(host.data() + splits_off, hp.splits.data(), hp.splits.size() * sizeof(Split));
+  std::memcpy(host.data() + cta_off, hp.cta_split.data(), hp.cta_split.size() * sizeof(int32_t));
   cudaStream_t s = (cudaStream_t)stream;
   uint8_t* base = (uint8_t*)scratch;
   if (cudaMemcpyAsync(base, host.data(), part_off, cudaMemcpyHostToDevice, s) != cudaSuccess)
@@ -157,9 +119,9 @@ extern "C" kv_status_t kv_decode_attn_noalloc(kv_pool_t* P, const void* q, const
   const cudaError_t e =
       impl == KV_DECODE_MMA
           ? launch_decode_mma(P, q, hq, scale_log2, (const Unit*)base, (int)n_units, (const Split*)(base + splits_off),
-                              (int)splits.size(), (float*)(base + part_off), out, s)
+                              (const int32_t*)(base + cta_off), (int)hp.n_ctas(), (float*)(base + part_off), out, s)
           : launch_decode_simt(P, q, hq, scale_log2, (const Unit*)base, (int)n_units, (const Split*)(base + splits_off),
-                               (int)splits.size(), (float*)(base + part_off), out, s);
+                               (const int32_t*)(base + cta_off), (int)hp.n_ctas(), (float*)(base + part_off), out, s);
   if (e != cudaSuccess) return nfail(KV_ERR_CUDA, cudaGetErrorString(e));
   return KV_OK;
 }

@@ -152,6 +152,55 @@ kv_status_t order_after_previous(kv_pool* P, cudaStream_t s) {
 
 void kvq::set_last_error(const char* msg) { g_err = msg; }
 
+void kvq::plan_decode(const kv_pool* P, const int32_t* req_ids, int32_t batch, int64_t n_ctas, HostPlan& out) {
+  const int hkv = P->cfg.num_kv_heads;
+  const int64_t n2 = P->cfg.n_int2_pages;
+  auto cost = [&](int32_t id) { return (id < n2 ? (double)kInt2Block : (double)kInt4Block) + kPageCost; };
+  double total = 0.0;
+  int64_t pages = 0;
+  for (int32_t b = 0; b < batch; ++b)
+    for (int32_t id : P->reqs[req_ids[b]].table) {
+      total += cost(id) * hkv;
+      pages += hkv;
+    }
+  // at least kMinPagesPerCta pages per CTA, so small batches do not pay a
+  // unit prologue per page
+  const int64_t n = std::max<int64_t>(1, std::min<int64_t>(n_ctas, pages / kMinPagesPerCta));
+  out.units.assign((size_t)batch * hkv, Unit{});
+  out.splits.clear();
+  out.cta_split.assign((size_t)n + 1, 0);
+  int64_t cur = 0;        // CTA receiving the current split
+  double cum = 0.0;       // cost before the current page
+  for (int32_t b = 0; b < batch; ++b) {
+    const auto& tb = P->reqs[req_ids[b]].table;
+    for (int h = 0; h < hkv; ++h) {
+      const int32_t ui = b * hkv + h;
+      Unit& u = out.units[ui];
+      u.b = b;
+      u.req = req_ids[b];
+      u.kvh = h;
+      u.split_begin = (int32_t)out.splits.size();
+      bool open = false;
+      for (int32_t i = 0; i < (int32_t)tb.size(); ++i) {
+        const int64_t j = std::min<int64_t>(n - 1, (int64_t)(cum * (double)n / total));
+        if (j > cur) {
+          open = false;
+          while (cur < j) out.cta_split[++cur] = (int32_t)out.splits.size();
+        }
+        if (!open) {
+          out.splits.push_back(Split{ui, i, i + 1, (int32_t)cur});
+          open = true;
+        } else {
+          out.splits.back().page_end = i + 1;
+        }
+        cum += cost(tb[i]);
+      }
+      u.n_splits = (int32_t)out.splits.size() - u.split_begin;
+    }
+  }
+  while (cur < n) out.cta_split[++cur] = (int32_t)out.splits.size();
+}
+
 extern "C" {
 
 const char* kv_last_error(void) { return g_err.c_str(); }
@@ -262,6 +311,8 @@ kv_status_t kv_pool_destroy(kv_pool_t* P) {
   cudaFree(P->upload.ptr);
   cudaFree(P->plan.ptr);
   cudaFree(P->partials.ptr);
+  for (cudaEvent_t e : P->tev)
+    if (e) cudaEventDestroy(e);
   delete P;
   return KV_OK;
 }
@@ -570,12 +621,13 @@ kv_status_t kv_export_request(kv_pool_t* P, int32_t r, int32_t* ids, uint8_t* is
 
 namespace {
 
-// Split planner (Tangram, AOT load balancing: total CTAs from the occupancy
-// API, each work group's share of them proportional to its bytes).  Units are
-// (batch row, kv head); a unit's table is cut into maximal runs of one
-// precision (after the INT2-first reorder there are at most two), and each run
-// into near-equal page ranges of about total_bytes / (SMs x CTAs per SM)
-// bytes, so every split is pure INT2 or pure INT4 (TriAxialKV key design 4).
+// Split planner (Tangram, ahead-of-time load balancing: the CTA count comes
+// from the occupancy API and work is partitioned before the launch).  All
+// (batch row, kv head) units' pages, in order, are cut into n_ctas contiguous
+// ranges of about equal cost; a range that crosses unit boundaries becomes one
+// split per unit.  Cost of a page = its block bytes + a fixed per-page term
+// for the scan's compute, so INT2 and INT4 pages are weighed fairly.
+
 kv_status_t build_plan(kv_pool* P, const int32_t* req_ids, int32_t batch, int32_t hq, int32_t impl,
                        cudaStream_t s) {
   const int hkv = P->cfg.num_kv_heads, g = hq / hkv;
@@ -585,55 +637,21 @@ kv_status_t build_plan(kv_pool* P, const int32_t* req_ids, int32_t batch, int32_
   if (same) return KV_OK;
 
   const int ctas = impl == KV_DECODE_MMA ? decode_mma_ctas_per_sm(g) : decode_simt_ctas_per_sm(g);
-  const double target = (double)P->sm_count * ctas;
-  double total = 0.0;
-  for (int32_t b = 0; b < batch; ++b)
-    for (int32_t id : P->reqs[req_ids[b]].table) total += (is_int2(P, id) ? kInt2Block : kInt4Block) * (double)hkv;
-  const double chunk = std::max(total / target, 8.0 * kInt2Block);
-
-  std::vector<Unit> units;
-  std::vector<Split> splits;
-  units.reserve((size_t)batch * hkv);
-  for (int32_t b = 0; b < batch; ++b) {
-    const auto& tb = P->reqs[req_ids[b]].table;
-    // runs of one precision
-    std::vector<std::pair<int32_t, int32_t>> runs;
-    for (int32_t i = 0; i < (int32_t)tb.size();) {
-      int32_t j = i + 1;
-      while (j < (int32_t)tb.size() && is_int2(P, tb[j]) == is_int2(P, tb[i])) ++j;
-      runs.push_back({i, j});
-      i = j;
-    }
-    for (int h = 0; h < hkv; ++h) {
-      Unit u{};
-      u.b = b;
-      u.req = req_ids[b];
-      u.kvh = h;
-      u.split_begin = (int32_t)splits.size();
-      for (const auto& rn : runs) {
-        const bool i2 = is_int2(P, tb[rn.first]);
-        const int32_t np = rn.second - rn.first;
-        const double bytes = (double)np * (i2 ? kInt2Block : kInt4Block);
-        const int32_t ns = std::max<int32_t>(1, std::min<int32_t>(np, (int32_t)std::ceil(bytes / chunk)));
-        for (int32_t k2 = 0; k2 < ns; ++k2)
-          splits.push_back(Split{(int32_t)units.size(), rn.first + (int32_t)((int64_t)np * k2 / ns),
-                                 rn.first + (int32_t)((int64_t)np * (k2 + 1) / ns), i2 ? 1 : 0});
-      }
-      u.n_splits = (int32_t)splits.size() - u.split_begin;
-      units.push_back(u);
-    }
-  }
+  HostPlan hp;
+  plan_decode(P, req_ids, batch, (int64_t)P->sm_count * ctas, hp);
   Upload up;
-  const size_t ou = up.add(units.data(), units.size() * sizeof(Unit));
-  const size_t os = up.add(splits.data(), splits.size() * sizeof(Split));
+  const size_t ou = up.add(hp.units.data(), hp.units.size() * sizeof(Unit));
+  const size_t os = up.add(hp.splits.data(), hp.splits.size() * sizeof(Split));
+  const size_t oc = up.add(hp.cta_split.data(), hp.cta_split.size() * sizeof(int32_t));
   kv_status_t st = ensure(P->plan, up.bytes.size());
   if (st != KV_OK) return st;
   KV_CUDA(cudaMemcpyAsync(P->plan.ptr, up.bytes.data(), up.bytes.size(), cudaMemcpyHostToDevice, s));
-  (void)ou;
   P->plan_units_off = ou;
   P->plan_splits_off = os;
-  P->n_units = (int32_t)units.size();
-  P->n_splits = (int32_t)splits.size();
+  P->plan_cta_off = oc;
+  P->n_units = (int32_t)hp.units.size();
+  P->n_splits = (int32_t)hp.splits.size();
+  P->n_ctas = (int32_t)hp.n_ctas();
   P->plan_req.assign(req_ids, req_ids + batch);
   P->plan_ver.resize(batch);
   for (int32_t b = 0; b < batch; ++b) P->plan_ver[b] = P->reqs[req_ids[b]].version;
@@ -669,12 +687,53 @@ kv_status_t kv_decode_attn(kv_pool_t* P, const void* q, const int32_t* req_ids, 
   const float scale_log2 = softmax_scale * 1.4426950408889634f;
   const Unit* du = (const Unit*)(base + P->plan_units_off);
   const Split* dsp = (const Split*)(base + P->plan_splits_off);
+  const int32_t* dct = (const int32_t*)(base + P->plan_cta_off);
+  cudaEvent_t* tv = P->timing ? &P->tev[3 * (size_t)(P->timed_calls % kTimingRing)] : nullptr;
+  if (tv) KV_CUDA(cudaEventRecord(tv[0], s));
+  P->merge_event = tv ? tv[1] : nullptr;
   if (impl == KV_DECODE_MMA)
-    KV_CUDA(launch_decode_mma(P, q, hq, scale_log2, du, P->n_units, dsp, P->n_splits, (float*)P->partials.ptr, out, s));
+    KV_CUDA(launch_decode_mma(P, q, hq, scale_log2, du, P->n_units, dsp, dct, P->n_ctas, (float*)P->partials.ptr, out, s));
   else
-    KV_CUDA(launch_decode_simt(P, q, hq, scale_log2, du, P->n_units, dsp, P->n_splits, (float*)P->partials.ptr, out, s));
+    KV_CUDA(launch_decode_simt(P, q, hq, scale_log2, du, P->n_units, dsp, dct, P->n_ctas, (float*)P->partials.ptr, out, s));
+  if (tv) {
+    KV_CUDA(cudaEventRecord(tv[2], s));
+    ++P->timed_calls;
+  }
+  P->merge_event = nullptr;
   P->stat_req.assign(req_ids, req_ids + batch);
   P->stat_hq = hq;
+  return KV_OK;
+}
+
+kv_status_t kv_decode_timing(kv_pool_t* P, int32_t enable, int64_t* n_calls, float* scan_ms, float* decode_ms) {
+  if (!P) return fail(KV_ERR_INVALID_ARG, "kv_decode_timing: null pool");
+  DeviceGuard dg(P->cfg.device);
+  if (n_calls) *n_calls = P->timed_calls;
+  if (scan_ms) *scan_ms = -1.0f;
+  if (decode_ms) *decode_ms = -1.0f;
+  if (P->timed_calls > 0 && (scan_ms || decode_ms)) {
+    const int64_t n = std::min<int64_t>(P->timed_calls, kTimingRing);
+    const int64_t last = (P->timed_calls - 1) % kTimingRing;
+    KV_CUDA(cudaEventSynchronize(P->tev[3 * (size_t)last + 2]));
+    double a = 0.0, b = 0.0;
+    for (int64_t k = 0; k < n; ++k) {
+      float x = 0.0f, y = 0.0f;
+      KV_CUDA(cudaEventElapsedTime(&x, P->tev[3 * (size_t)k], P->tev[3 * (size_t)k + 1]));
+      KV_CUDA(cudaEventElapsedTime(&y, P->tev[3 * (size_t)k], P->tev[3 * (size_t)k + 2]));
+      a += x;
+      b += y;
+    }
+    if (scan_ms) *scan_ms = (float)(a / (double)n);
+    if (decode_ms) *decode_ms = (float)(b / (double)n);
+  }
+  if (enable) {
+    if (P->tev.empty()) {
+      P->tev.assign(3 * (size_t)kTimingRing, nullptr);
+      for (auto& e : P->tev) KV_CUDA(cudaEventCreate(&e));
+    }
+    P->timed_calls = 0;
+  }
+  P->timing = enable != 0;
   return KV_OK;
 }
 
