@@ -62,10 +62,12 @@ struct WarpSmem {
 struct CtaSmem {
   WarpSmem warp[kWarps];
   float qraw[8][kHeadDim];             // q (fp32) of the packed heads
-  float qz[8][kHeadDim];               // q in the INT2 K scale/zero pair order
+  uint32_t qzh[8][kHeadDim / 2];       // 2^Ez q as binary16 pairs in the INT2 K scale/zero pair order
+  float qzs[8];                        // 2^(-Ez) * scale * log2(e)
+  uint4 bqn[kWarps][4][32];            // INT2 K: negated q fragments (g <= 4: lo columns only, else 0)
   float acol[8];                       // 2^(-E_h) * scale * log2(e)
   int eh[8];                           // per-head power-of-two q scale
-  uint32_t bz[8][4];                   // fp16 (hi | lo) of scale*log2(e)*Q_{h,group}
+  uint32_t bz[8][4];                   // fp16 pairs: hi(Q0,Q1), hi(Q2,Q3), lo(Q0,Q1), lo(Q2,Q3) of scale*log2(e)*Q_{h,group}
   float zv[kWarps][4][8];              // V zero-term per warp [group][col]
   float mw[kWarps][8], lw[kWarps][8];
 };
@@ -90,11 +92,6 @@ __device__ __forceinline__ uint32_t unmagic(uint32_t x) {
   asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(x | kMagic), "r"(kMagic));
   return d;
 }
-__device__ __forceinline__ uint32_t hneg2(uint32_t a) {
-  uint32_t d;
-  asm("neg.f16x2 %0, %1;" : "=r"(d) : "r"(a));
-  return d;
-}
 __device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
   uint32_t d;
   asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
@@ -106,8 +103,31 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
   return d;
 }
-__device__ __forceinline__ float h_lo(uint32_t x) { return __half2float(__ushort_as_half((unsigned short)(x & 0xFFFFu))); }
-__device__ __forceinline__ float h_hi(uint32_t x) { return __half2float(__ushort_as_half((unsigned short)(x >> 16))); }
+// binary16 halves of a 32-bit register as fp32 (exact)
+__device__ __forceinline__ float h_lo(uint32_t x) {
+  float f;
+  asm("{.reg .f16 l, h;\n mov.b32 {l, h}, %1;\n cvt.f32.f16 %0, l;}" : "=f"(f) : "r"(x));
+  return f;
+}
+__device__ __forceinline__ float h_hi(uint32_t x) {
+  float f;
+  asm("{.reg .f16 l, h;\n mov.b32 {l, h}, %1;\n cvt.f32.f16 %0, h;}" : "=f"(f) : "r"(x));
+  return f;
+}
+// acc + lo(a) * lo(b) + hi(a) * hi(b): binary16 products are exact in fp32,
+// each addition rounds once.
+__device__ __forceinline__ float fma2_f16_f32(uint32_t a, uint32_t b, float acc) {
+  asm("{.reg .f16 al, ah, bl, bh;\n mov.b32 {al, ah}, %1;\n mov.b32 {bl, bh}, %2;\n"
+      " fma.rn.f32.f16 %0, al, bl, %0;\n fma.rn.f32.f16 %0, ah, bh, %0;}"
+      : "+f"(acc) : "r"(a), "r"(b));
+  return acc;
+}
+// 2^x (flushes results below 2^-126 to zero; 2^-inf = 0)
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 __device__ __forceinline__ uint32_t comp(const uint4& v, int k) {
   return k == 0 ? v.x : (k == 1 ? v.y : (k == 2 ? v.z : v.w));
 }
@@ -142,8 +162,9 @@ __device__ __forceinline__ bool bar_wait(unsigned long long* b, uint32_t phase) 
 
 // ---- logits of one INT4 page: lg[m][c] for tokens 16m + r + 8(c>>1), heads 2i + (c&1)
 template <int G>
-__device__ __forceinline__ void qk_int4(const uint8_t* blk, const uint32_t (&bq)[16], uint32_t bzl, int r, int i,
+__device__ __forceinline__ void qk_int4(const uint8_t* blk, const uint32_t (&bq)[16], const uint32_t (&bz)[2],
                                         const float (&acol)[2], float (&lg)[2][4]) {
+  const int lane = threadIdx.x & 31, r = lane >> 2, i = lane & 3;
 #pragma unroll
   for (int m = 0; m < 2; ++m) {
     uint4 kw[2], km[2];
@@ -174,11 +195,13 @@ __device__ __forceinline__ void qk_int4(const uint8_t* blk, const uint32_t (&bq)
       for (int gr = 0; gr < 4; ++gr) v = fmaf(h_lo(comp(km[e], gr)), acc[gr][c], v);
       T[c] = v * acol[c & 1];
     }
-    // zero term sum_g zero_tg * (scale log2e Q_g) by one mma: k-slots 0..3 hi, 4..7 lo
-    const int qq = i & 1;
-    const uint32_t az0 = __byte_perm(comp(km[0], 2 * qq), comp(km[0], 2 * qq + 1), 0x7632);
-    const uint32_t az1 = __byte_perm(comp(km[1], 2 * qq), comp(km[1], 2 * qq + 1), 0x7632);
-    mma16816(T, az0, az1, 0u, 0u, bzl, 0u);
+    // zero term sum_g zero_tg * (scale log2e Q_g) by one mma: every lane feeds
+    // (zero_0, zero_1) in k-slots 2i, 2i+1 and (zero_2, zero_3) in 2i+8, 2i+9;
+    // B rows 0, 1 / 8, 9 hold the hi parts of Q, rows 2, 3 / 10, 11 the lo
+    // parts, the other rows zero.
+    const uint32_t az0 = __byte_perm(km[0].x, km[0].y, 0x7632), az2 = __byte_perm(km[0].z, km[0].w, 0x7632);
+    const uint32_t az1 = __byte_perm(km[1].x, km[1].y, 0x7632), az3 = __byte_perm(km[1].z, km[1].w, 0x7632);
+    mma16816(T, az0, az1, az2, az3, bz[0], bz[1]);
 #pragma unroll
     for (int c = 0; c < 4; ++c) lg[m][c] = T[c];
   }
@@ -186,11 +209,10 @@ __device__ __forceinline__ void qk_int4(const uint8_t* blk, const uint32_t (&bq)
 
 // ---- logits of one INT2 page
 template <int G>
-__device__ __forceinline__ void qk_int2(const uint8_t* blk, const uint32_t (&bq)[16], int r, int i, bool is_lo,
-                                        const float (&acol)[2], float scale_log2, const float (*qz)[kHeadDim],
-                                        float (&lg)[2][4]) {
+__device__ __forceinline__ void qk_int2(const uint8_t* blk, const uint32_t (&bq)[16], const uint4* bqn4,
+                                        const float (&acol)[2], const CtaSmem& S, float (&lg)[2][4]) {
   constexpr bool kComb = G <= 4;
-  const uint32_t lomask = is_lo ? 0xFFFFFFFFu : 0u;
+  const int lane = threadIdx.x & 31, r = lane >> 2, i = lane & 3;
   uint2 kw[2][2];
 #pragma unroll
   for (int m = 0; m < 2; ++m)
@@ -212,11 +234,13 @@ __device__ __forceinline__ void qk_int2(const uint8_t* blk, const uint32_t (&bq)
     const int wi = kk >> 2, jj = kk & 3, j0 = 2 * jj, j1 = 2 * jj + 1;
     const int p0 = wi * 8 + j0, p1 = wi * 8 + j1;
     const uint32_t s0 = comp(sv[p0 >> 2], p0 & 3), s1 = comp(sv[p1 >> 2], p1 & 3);
-    // hi = rn(q s); lo = rn(q s - hi) (exact).  With (hi | lo) columns, lanes of
-    // the lo columns subtract hi and lanes of the hi columns subtract 0.
-    uint32_t t0 = hmul2(bq[2 * kk], s0), t1 = hmul2(bq[2 * kk + 1], s1);
-    if (kComb) { t0 &= lomask; t1 &= lomask; }
-    const uint32_t u0 = hfma2(bq[2 * kk], s0, hneg2(t0)), u1 = hfma2(bq[2 * kk + 1], s1, hneg2(t1));
+    // hi = rn(q s); lo = q s - hi (exact).  bqn holds -q where the lo part is
+    // wanted and 0 elsewhere, so u = fma(q, s, rn(bqn s)) is lo or hi.
+    const uint4 nq = bqn4[(kk >> 1) * 32 + lane];
+    const uint32_t n0 = (kk & 1) ? nq.z : nq.x, n1 = (kk & 1) ? nq.w : nq.y;
+    const uint32_t u0 = hfma2(bq[2 * kk], s0, hmul2(n0, s0)), u1 = hfma2(bq[2 * kk + 1], s1, hmul2(n1, s1));
+    uint32_t t0 = 0u, t1 = 0u;
+    if (!kComb) { t0 = hmul2(bq[2 * kk], s0); t1 = hmul2(bq[2 * kk + 1], s1); }
     const uint32_t sh0 = 2 * (j0 & 3), sh1 = 2 * (j1 & 3);
 #pragma unroll
     for (int m = 0; m < 2; ++m) {
@@ -232,40 +256,44 @@ __device__ __forceinline__ void qk_int2(const uint8_t* blk, const uint32_t (&bq)
       }
     }
   }
-  // zero term Z_h = sum_c q_hc zero_c (fp32), reduced over the lanes of head h
+  // zero term Z_h = sum_c q_hc zero_c (fp32 sums of exact binary16 products),
+  // reduced over the lanes of head h
   float zp = 0.0f;
+  int hz;
   if (kComb) {
-    const int hz = r & 3, wi = r >> 2;
-    const uint4 z0 = *reinterpret_cast<const uint4*>(blk + kI2KMeta + 256 + 64 * i + 32 * wi);
-    const uint4 z1 = *reinterpret_cast<const uint4*>(blk + kI2KMeta + 256 + 64 * i + 32 * wi + 16);
-    const float* qp = qz[hz] + (i * 2 + wi) * 16;
+    const int wi = r >> 2;
+    hz = r & 3;
+    const uint4* zs = reinterpret_cast<const uint4*>(blk + kI2KMeta + 256 + 64 * i + 32 * wi);
+    const uint4* qs = reinterpret_cast<const uint4*>(&S.qzh[hz][(i * 2 + wi) * 8]);
 #pragma unroll
-    for (int x = 0; x < 8; ++x) {
-      const uint32_t z2 = x < 4 ? comp(z0, x) : comp(z1, x - 4);
-      zp = fmaf(h_lo(z2), qp[2 * x], zp);
-      zp = fmaf(h_hi(z2), qp[2 * x + 1], zp);
+    for (int x4 = 0; x4 < 2; ++x4) {
+      const uint4 zz = zs[x4], qq = qs[x4];
+      zp = fma2_f16_f32(zz.x, qq.x, zp);
+      zp = fma2_f16_f32(zz.y, qq.y, zp);
+      zp = fma2_f16_f32(zz.z, qq.z, zp);
+      zp = fma2_f16_f32(zz.w, qq.w, zp);
     }
     zp += __shfl_xor_sync(0xFFFFFFFFu, zp, 1);
     zp += __shfl_xor_sync(0xFFFFFFFFu, zp, 2);
     zp += __shfl_xor_sync(0xFFFFFFFFu, zp, 16);
   } else {
-    const int hz = r;
-    const float* qp = qz[hz] + i * 32;
+    hz = r;
+    const uint4* zs = reinterpret_cast<const uint4*>(blk + kI2KMeta + 256 + 64 * i);
+    const uint4* qs = reinterpret_cast<const uint4*>(&S.qzh[hz][i * 16]);
 #pragma unroll
     for (int x4 = 0; x4 < 4; ++x4) {
-      const uint4 zz = *reinterpret_cast<const uint4*>(blk + kI2KMeta + 256 + 64 * i + 16 * x4);
-#pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        const uint32_t z2 = comp(zz, x);
-        zp = fmaf(h_lo(z2), qp[8 * x4 + 2 * x], zp);
-        zp = fmaf(h_hi(z2), qp[8 * x4 + 2 * x + 1], zp);
-      }
+      const uint4 zz = zs[x4], qq = qs[x4];
+      zp = fma2_f16_f32(zz.x, qq.x, zp);
+      zp = fma2_f16_f32(zz.y, qq.y, zp);
+      zp = fma2_f16_f32(zz.z, qq.z, zp);
+      zp = fma2_f16_f32(zz.w, qq.w, zp);
     }
     zp += __shfl_xor_sync(0xFFFFFFFFu, zp, 1);
     zp += __shfl_xor_sync(0xFFFFFFFFu, zp, 2);
   }
-  const float zc0 = __shfl_sync(0xFFFFFFFFu, zp, 4 * (2 * i)) * scale_log2;
-  const float zc1 = __shfl_sync(0xFFFFFFFFu, zp, 4 * (2 * i + 1)) * scale_log2;
+  zp *= S.qzs[hz];
+  const float zc0 = __shfl_sync(0xFFFFFFFFu, zp, 4 * (2 * i));
+  const float zc1 = __shfl_sync(0xFFFFFFFFu, zp, 4 * (2 * i + 1));
 #pragma unroll
   for (int m = 0; m < 2; ++m)
 #pragma unroll
@@ -284,41 +312,51 @@ __device__ __forceinline__ void softmax_pv(const uint8_t* blk, uint32_t live, in
   constexpr bool kComb = G <= 4;
   constexpr int vmeta = kInt2 ? kI2VMeta : kI4VMeta;
   const bool full = live == 0xFFFFFFFFu;   // warp-uniform: no dead slot on this page
-  float corr[2];
-#pragma unroll
-  for (int hh = 0; hh < 2; ++hh) {
-    float pm = -INFINITY;
+  if (!full) {
 #pragma unroll
     for (int m = 0; m < 2; ++m)
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int t = 16 * m + r + 8 * e;
-        if (!full && !((live >> t) & 1u)) lg[m][2 * e + hh] = kDead2;
-        pm = fmaxf(pm, lg[m][2 * e + hh]);
-      }
+      for (int e = 0; e < 2; ++e)
+        if (!((live >> (16 * m + r + 8 * e)) & 1u)) lg[m][2 * e] = lg[m][2 * e + 1] = kDead2;
+  }
+  // Lanes i and i ^ 2 hold the same logits for g <= 4, so their softmax
+  // state (and the rescale factor of their accumulator columns) agree.
+  float corr[2], pv[2][2][2];
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    float pm = fmaxf(fmaxf(lg[0][hh], lg[0][2 + hh]), fmaxf(lg[1][hh], lg[1][2 + hh]));
     pm = fmaxf(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, 4));
     pm = fmaxf(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, 8));
     pm = fmaxf(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, 16));
     const float mnew = fmaxf(mrun[hh], pm);
-    corr[hh] = exp2f(mrun[hh] - mnew);
+    corr[hh] = ex2(mrun[hh] - mnew);
     mrun[hh] = mnew;
     float ps = 0.0f;
 #pragma unroll
     for (int m = 0; m < 2; ++m)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const int t = 16 * m + r + 8 * e;
-        const float p = exp2f(lg[m][2 * e + hh] - mnew);
-        ps += p;
-        if (!kComb || i < 2) pbuf[2 * i + hh][t] = (full || ((live >> t) & 1u)) ? p * pscale : 0.0f;
+        pv[hh][m][e] = ex2(lg[m][2 * e + hh] - mnew);
+        ps += pv[hh][m][e];
       }
     lsum[hh] = lsum[hh] * corr[hh] + ps;
   }
-  float c0 = corr[0], c1 = corr[1];
-  if (kComb) {
-    const float x0 = __shfl_xor_sync(0xFFFFFFFFu, c0, 2), x1 = __shfl_xor_sync(0xFFFFFFFFu, c1, 2);
-    if (i >= 2) { c0 = x0; c1 = x1; }
+  if (!full) {   // dead slots carry V = 0
+#pragma unroll
+    for (int m = 0; m < 2; ++m)
+#pragma unroll
+      for (int e = 0; e < 2; ++e)
+        if (!((live >> (16 * m + r + 8 * e)) & 1u)) pv[0][m][e] = pv[1][m][e] = 0.0f;
   }
+  if (!kComb || i < 2) {
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+      for (int m = 0; m < 2; ++m)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) pbuf[2 * i + hh][16 * m + r + 8 * e] = pv[hh][m][e] * pscale;
+  }
+  const float c0 = corr[0], c1 = corr[1];
   if (__any_sync(0xFFFFFFFFu, c0 != 1.0f || c1 != 1.0f)) {
 #pragma unroll
     for (int m = 0; m < 8; ++m) { o[m][0] *= c0; o[m][1] *= c1; o[m][2] *= c0; o[m][3] *= c1; }
@@ -356,14 +394,17 @@ __device__ __forceinline__ void softmax_pv(const uint8_t* blk, uint32_t live, in
 #pragma unroll
     for (int c = 0; c < 4; ++c) zv[c] += zt[c];
   }
-  // Fold operands: B = fma(x1, s, fma(x2, s, -(x3 * s))).  Hi columns (and the
-  // hi pass of g > 4): x3 = 0, x2 = p_hi, x1 = 0 -> rn(p_hi s).  Lo columns:
-  // x3 = x2 = p_hi, x1 = p_lo -> rn(p_lo s + (p_hi s - rn(p_hi s))).
+  // Fold operands: u = fma(p_hi, s, rn(x3 * s)) with x3 = -p_hi where the lo
+  // part is wanted (else 0), then lo = rn(p_lo s + u):
+  //   g <= 4, hi columns: x3 = x1 = 0 -> B = rn(p_hi s);
+  //   lo columns (and the lo pass of g > 4): x3 = -p_hi, x1 = p_lo ->
+  //   B = rn(p_lo s + (p_hi s - rn(p_hi s))).
+  const uint32_t lomask = (!kComb || is_lo) ? 0xFFFFFFFFu : 0u;
   uint32_t x3[4], x1[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    x3[k] = (kComb && !is_lo) ? 0u : ph[k];
-    x1[k] = (kComb && !is_lo) ? 0u : pl[k];
+    x3[k] = (ph[k] ^ 0x80008000u) & lomask;
+    x1[k] = pl[k] & lomask;
   }
 #pragma unroll
   for (int gr = 0; gr < 4; ++gr) {
@@ -380,12 +421,11 @@ __device__ __forceinline__ void softmax_pv(const uint8_t* blk, uint32_t live, in
     uint32_t bh[4], bl[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const uint32_t t = hmul2(x3[k], sk[k]);
-      const uint32_t u = hfma2(ph[k], sk[k], hneg2(t));
+      const uint32_t u = hfma2(ph[k], sk[k], hmul2(x3[k], sk[k]));
       if (kComb) {
         bh[k] = hfma2(x1[k], sk[k], u);
       } else {
-        bh[k] = t;
+        bh[k] = hmul2(ph[k], sk[k]);
         bl[k] = hfma2(x1[k], sk[k], u);
       }
     }
@@ -433,8 +473,9 @@ __device__ __forceinline__ void softmax_pv(const uint8_t* blk, uint32_t live, in
 
 // q fragments (B operands of the K dot products) for one page precision.
 template <int G>
-__device__ __forceinline__ void build_bq(const CtaSmem& S, bool int2, int r, int i, uint32_t (&bq)[16]) {
+__device__ __forceinline__ void build_bq(CtaSmem& S, bool int2, int w, bool is_lo, uint32_t (&bq)[16]) {
   constexpr bool kComb = G <= 4;
+  const int lane = threadIdx.x & 31, r = lane >> 2, i = lane & 3;
   if (int2) {
     const int hq2 = kComb ? (r & 3) : r;
     const int E = S.eh[hq2];
@@ -448,8 +489,15 @@ __device__ __forceinline__ void build_bq(const CtaSmem& S, bool int2, int r, int
         bq[2 * kk + e] = hq2 < G ? pack_h2(ldexpf(S.qraw[hq2][clo], E - wexp), ldexpf(S.qraw[hq2][clo + 8], E - wexp))
                                  : 0u;
       }
+    // negated copies for the exact hi/lo split (g <= 4: lo columns only)
+    __syncwarp();
+    uint32_t* nb = reinterpret_cast<uint32_t*>(&S.bqn[w][0][0]);
+#pragma unroll
+    for (int x = 0; x < 16; ++x)
+      nb[((x >> 2) * 32 + lane) * 4 + (x & 3)] = (!kComb || is_lo) ? (bq[x] ^ 0x80008000u) : 0u;
+    __syncwarp();
   } else {
-    const int n = r;
+    const int n = kComb ? (r & 3) : r;   // g <= 4: columns 4..7 repeat heads 0..3
     const int E = S.eh[n];
 #pragma unroll
     for (int gr = 0; gr < 4; ++gr)
@@ -528,17 +576,27 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(
         S.bz[h][2] = lo[0] | ((uint32_t)lo[1] << 16);
         S.bz[h][3] = lo[2] | ((uint32_t)lo[3] << 16);
       }
-    }
-    for (int x = tid; x < 8 * kHeadDim; x += kThreads) {
-      const int h = x >> 7, pidx = x & (kHeadDim - 1);
-      const int pair = pidx >> 1, hi = pidx & 1;
-      const int j = pair & 7, iw = pair >> 3;      // iw = i*2 + wi
-      const int c = 4 * (4 * iw + (j >> 2)) + (j & 3) + 8 * hi;
-      S.qz[h][pidx] = S.qraw[h][c];
+      // q as binary16 pairs in the INT2 K scale/zero pair order for the zero
+      // term, scaled by 2^Ez so that max |q| lies in [2^14, 2^15)
+      const int Ez = mx > 0.0f ? max(-100, min(100, 14 - ilogbf(mx))) : 0;
+      for (int pr = lane; pr < kHeadDim / 2; pr += 32) {
+        const int j = pr & 7, iw = pr >> 3;        // iw = chunk i * 2 + word wi
+        const int c = 4 * (4 * iw + (j >> 2)) + (j & 3);
+        S.qzh[h][pr] = pack_h2(ldexpf(S.qraw[h][c], Ez), ldexpf(S.qraw[h][c + 8], Ez));
+      }
+      if (lane == 0) S.qzs[h] = ldexpf(scale_log2, -Ez);
     }
     __syncthreads();
-    const uint32_t bzl = r < G ? S.bz[r][i] : 0u;
-    const float acol[2] = {S.acol[2 * i], S.acol[2 * i + 1]};
+    // g <= 4: lanes i and i ^ 2 carry the same two heads (columns 4..7 repeat
+    // heads 0..3 for INT4 K; the hi/lo columns are summed for INT2 K)
+    const int hp2 = kComb ? 2 * (i & 1) : 2 * i;
+    const int hz = kComb ? (r & 3) : r;
+    uint32_t bz[2] = {0u, 0u};
+    if (hz < G && i < 2) {
+      bz[0] = S.bz[hz][2 * i];
+      bz[1] = S.bz[hz][2 * i + 1];
+    }
+    const float acol[2] = {S.acol[hp2], S.acol[hp2 + 1]};
 
     // ---- page loop: two-stage bulk-copy ring per warp
     const Entry* tab = table + (size_t)u.req * max_pages;
@@ -582,16 +640,16 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(
       const Entry e = ent_get(st);
       const bool i2 = e.id < n2;
       if ((int)i2 != cur) {
-        build_bq<G>(S, i2, r, i, bq);
+        build_bq<G>(S, i2, w, is_lo, bq);
         cur = (int)i2;
       }
       const uint8_t* blk = WS.stage[st];
       float lg[2][4];
       if (i2) {
-        qk_int2<G>(blk, bq, r, i, is_lo, acol, scale_log2, S.qz, lg);
+        qk_int2<G>(blk, bq, &S.bqn[w][0][0], acol, S, lg);
         softmax_pv<G, true>(blk, e.live, r, i, is_lo, pscale, lg, o, zv, mrun, lsum, WS.pbuf);
       } else {
-        qk_int4<G>(blk, bq, bzl, r, i, acol, lg);
+        qk_int4<G>(blk, bq, bz, acol, lg);
         softmax_pv<G, false>(blk, e.live, r, i, is_lo, pscale, lg, o, zv, mrun, lsum, WS.pbuf);
       }
       if (k + kStages < nw) {
@@ -669,7 +727,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(
       for (int ww = 0; ww < kWarps; ++ww) {
         const float mw = S.mw[ww][h];
         if (mw == -INFINITY) continue;
-        const float f = exp2f(mw - M);
+        const float f = ex2(mw - M);
         L += S.lw[ww][h] * f;
         A += reinterpret_cast<const float*>(S.warp[ww].stage[0])[h * kHeadDim + ch] * f;
       }
