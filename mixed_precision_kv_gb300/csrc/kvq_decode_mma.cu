@@ -8,14 +8,14 @@
 // dead slots at logit -1e4 and V = 0 (IntentKV sentinel dead slot).
 //
 // How it computes it (the arithmetic is regrouped, not changed):
-//  * A code word unpacks into mma A registers with one AND + OR per register
-//    and one f16x2 subtraction: a 2- or 4-bit field at bit position p of a
-//    16-bit half, OR-ed into binary16 1024.0, is 1024 + code * 2^p exactly, and
-//    subtracting 1024 leaves code * 2^p as a normal binary16.  The power 2^p is
-//    compensated in the other operand, so every product is code * operand
-//    exactly.  (Feeding the field directly as a binary16 subnormal would save
-//    the subtraction, but the tensor core aligns products by the exponent
-//    field, so subnormal operands lose about ten bits of the sum.)
+//  * A code word unpacks into mma A registers with one shift and one AND per
+//    register: a 2- or 4-bit field at bits p.. of both 16-bit halves (zero
+//    elsewhere) is the binary16 subnormal code * 2^(p-24).  The tensor core
+//    keeps full precision for subnormal operands whose top set bit is at bit
+//    7 or above, so fields sit at p = 6 or 8 (2-bit) and p = 4 or 6 (4-bit).
+//    The factor 2^(6-p) is carried by the other operand (q fragments, or P
+//    for INT2 V slot pairs at p = 8), and the common 2^-18 by the fp32 scale
+//    applied to the sums.
 //  * K dot products: s_t = sum_c q_c (scale * code_tc + zero).
 //      INT4 K (per-token groups): per-group accumulators, scale applied per
 //      token in fp32 afterwards, zero term sum_g zero_tg * Q_g by a small mma.
@@ -49,9 +49,11 @@ constexpr int kStageBytes = kInt4Block;
 constexpr int kPartStride = kHeadDim + 4;
 constexpr float kDead2 = -1.0e4f * 1.4426950408889634f;
 constexpr uint32_t kSpinLimit = 1u << 22;
-constexpr uint32_t kM0 = 0x000F000Fu, kM1 = 0x00F000F0u;   // nibble fields at bits 0 / 4 of each half
-constexpr uint32_t kQ0 = 0x00030003u;                      // 2-bit field at bit 0 of each half
-constexpr uint32_t kMagic = 0x64006400u;                   // binary16 1024.0 in both halves
+constexpr uint32_t kN4 = 0x00F000F0u;   // 4-bit field at bit 4 of each half
+constexpr uint32_t kN6 = 0x03C003C0u;   // 4-bit field at bit 6 of each half
+constexpr uint32_t kC6 = 0x00C000C0u;   // 2-bit field at bit 6 of each half
+constexpr uint32_t kC8 = 0x03000300u;   // 2-bit field at bit 8 of each half
+constexpr float kCodeUnit = 262144.0f;  // 2^18: a field at bit 6 is code * 2^-18
 
 struct WarpSmem {
   uint8_t stage[kStages][kStageBytes];
@@ -65,8 +67,8 @@ struct CtaSmem {
   uint32_t qzh[8][kHeadDim / 2];       // 2^Ez q as binary16 pairs in the INT2 K scale/zero pair order
   float qzs[8];                        // 2^(-Ez) * scale * log2(e)
   uint4 bqn[kWarps][4][32];            // INT2 K: negated q fragments (g <= 4: lo columns only, else 0)
-  float acol[8];                       // 2^(-E_h) * scale * log2(e)
-  int eh[8];                           // per-head power-of-two q scale
+  float acol2[8], acol4[8];            // 2^(18 - E) * scale * log2(e) for INT2 / INT4 K pages
+  int eh2[8], eh4[8];                  // per-head power-of-two q scales E for INT2 / INT4 K pages
   uint32_t bz[8][4];                   // fp16 pairs: hi(Q0,Q1), hi(Q2,Q3), lo(Q0,Q1), lo(Q2,Q3) of scale*log2(e)*Q_{h,group}
   float zv[kWarps][4][8];              // V zero-term per warp [group][col]
   float mw[kWarps][8], lw[kWarps][8];
@@ -85,13 +87,15 @@ __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
   asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
   return d;
 }
-// A code field OR-ed into the mantissa of binary16 1024.0 gives 1024 + field
-// exactly; subtracting 1024 leaves the field as a normal binary16 (or zero).
-__device__ __forceinline__ uint32_t unmagic(uint32_t x) {
-  uint32_t d;
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(x | kMagic), "r"(kMagic));
-  return d;
+__device__ __forceinline__ uint32_t rotr8(uint32_t x) { return __funnelshift_r(x, x, 8); }
+// INT2 code word variants: variant jj puts two 2-bit fields of each half at
+// bits 6 and 8.  Scale/zero pair index (register j of the pair order) of the
+// field at bit 6 and at bit 8 of variant jj.
+__device__ __forceinline__ uint32_t i2_variant(uint32_t x, int jj) {
+  return jj == 0 ? x : (jj == 1 ? (x >> 4) : (jj == 2 ? (x << 4) : rotr8(x)));
 }
+__host__ __device__ constexpr int i2_reg6(int jj) { return jj == 0 ? 3 : (jj == 1 ? 5 : (jj == 2 ? 1 : 7)); }
+__host__ __device__ constexpr int i2_reg8(int jj) { return jj == 0 ? 4 : (jj == 1 ? 6 : (jj == 2 ? 2 : 0)); }
 __device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
   uint32_t d;
   asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
@@ -178,13 +182,11 @@ __device__ __forceinline__ void qk_int4(const uint8_t* blk, const uint32_t (&bq)
 #pragma unroll
     for (int gr = 0; gr < 4; ++gr) {
       acc[gr][0] = acc[gr][1] = acc[gr][2] = acc[gr][3] = 0.0f;
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t x0 = comp(kw[0], gr), x1 = comp(kw[1], gr);
-        if (hf) { x0 >>= 8; x1 >>= 8; }
-        mma16816(acc[gr], unmagic(x0 & kM0), unmagic(x1 & kM0), unmagic(x0 & kM1), unmagic(x1 & kM1),
-                 bq[4 * gr + 2 * hf], bq[4 * gr + 2 * hf + 1]);
-      }
+      const uint32_t x0 = comp(kw[0], gr), x1 = comp(kw[1], gr);   // tokens r, r + 8
+      // k-step 0: nibbles 0/4 at p = 6, nibbles 1/5 at p = 4; k-step 1: 2/6 and 3/7 at p = 6
+      mma16816(acc[gr], (x0 << 6) & kN6, (x1 << 6) & kN6, x0 & kN4, x1 & kN4, bq[4 * gr], bq[4 * gr + 1]);
+      mma16816(acc[gr], (x0 >> 2) & kN6, (x1 >> 2) & kN6, (x0 >> 6) & kN6, (x1 >> 6) & kN6, bq[4 * gr + 2],
+               bq[4 * gr + 3]);
     }
     float T[4];
 #pragma unroll
@@ -231,8 +233,8 @@ __device__ __forceinline__ void qk_int2(const uint8_t* blk, const uint32_t (&bq)
     for (int x = 0; x < 4; ++x) acc[m][x][0] = acc[m][x][1] = acc[m][x][2] = acc[m][x][3] = 0.0f;
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
-    const int wi = kk >> 2, jj = kk & 3, j0 = 2 * jj, j1 = 2 * jj + 1;
-    const int p0 = wi * 8 + j0, p1 = wi * 8 + j1;
+    const int wi = kk >> 2, jj = kk & 3;
+    const int p0 = wi * 8 + i2_reg6(jj), p1 = wi * 8 + i2_reg8(jj);
     const uint32_t s0 = comp(sv[p0 >> 2], p0 & 3), s1 = comp(sv[p1 >> 2], p1 & 3);
     // hi = rn(q s); lo = q s - hi (exact).  bqn holds -q where the lo part is
     // wanted and 0 elsewhere, so u = fma(q, s, rn(bqn s)) is lo or hi.
@@ -241,13 +243,11 @@ __device__ __forceinline__ void qk_int2(const uint8_t* blk, const uint32_t (&bq)
     const uint32_t u0 = hfma2(bq[2 * kk], s0, hmul2(n0, s0)), u1 = hfma2(bq[2 * kk + 1], s1, hmul2(n1, s1));
     uint32_t t0 = 0u, t1 = 0u;
     if (!kComb) { t0 = hmul2(bq[2 * kk], s0); t1 = hmul2(bq[2 * kk + 1], s1); }
-    const uint32_t sh0 = 2 * (j0 & 3), sh1 = 2 * (j1 & 3);
 #pragma unroll
     for (int m = 0; m < 2; ++m) {
-      uint32_t x0 = wi ? kw[m][0].y : kw[m][0].x, x1 = wi ? kw[m][1].y : kw[m][1].x;
-      if (jj >= 2) { x0 >>= 8; x1 >>= 8; }
-      const uint32_t a0 = unmagic(x0 & (kQ0 << sh0)), a1 = unmagic(x1 & (kQ0 << sh0));
-      const uint32_t a2 = unmagic(x0 & (kQ0 << sh1)), a3 = unmagic(x1 & (kQ0 << sh1));
+      const uint32_t x0 = i2_variant(wi ? kw[m][0].y : kw[m][0].x, jj);   // token 16m + r
+      const uint32_t x1 = i2_variant(wi ? kw[m][1].y : kw[m][1].x, jj);   // token 16m + r + 8
+      const uint32_t a0 = x0 & kC6, a1 = x1 & kC6, a2 = x0 & kC8, a3 = x1 & kC8;
       if (kComb) {
         mma16816(acc[m][kk & 3], a0, a1, a2, a3, u0, u1);
       } else {
@@ -349,12 +349,14 @@ __device__ __forceinline__ void softmax_pv(const uint8_t* blk, uint32_t live, in
         if (!((live >> (16 * m + r + 8 * e)) & 1u)) pv[0][m][e] = pv[1][m][e] = 0.0f;
   }
   if (!kComb || i < 2) {
+    // INT2 V: even slots pair with code fields at p = 8, so their P carries 2^-2
+    const float pmul = (kInt2 && !(r & 1)) ? 0.25f * pscale : pscale;
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
       for (int m = 0; m < 2; ++m)
 #pragma unroll
-        for (int e = 0; e < 2; ++e) pbuf[2 * i + hh][16 * m + r + 8 * e] = pv[hh][m][e] * pscale;
+        for (int e = 0; e < 2; ++e) pbuf[2 * i + hh][16 * m + r + 8 * e] = pv[hh][m][e] * pmul;
   }
   const float c0 = corr[0], c1 = corr[1];
   if (__any_sync(0xFFFFFFFFu, c0 != 1.0f || c1 != 1.0f)) {
@@ -379,6 +381,10 @@ __device__ __forceinline__ void softmax_pv(const uint8_t* blk, uint32_t live, in
   {
     uint4 zz = make_uint4(0u, 0u, 0u, 0u);
     if (r < 4) zz = *reinterpret_cast<const uint4*>(blk + vmeta + 256 + 64 * r + 16 * i);
+    if (kInt2) {   // undo the 2^-2 of the even slots' P: words 0 and 2 hold slot pairs (8i, 8i+4), (8i+2, 8i+6)
+      zz.x = hmul2(zz.x, 0x44004400u);
+      zz.z = hmul2(zz.z, 0x44004400u);
+    }
     float zt[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     if (kComb) {
       const uint32_t b0 = is_lo ? pl[0] : ph[0], b1 = is_lo ? pl[1] : ph[1];
@@ -409,15 +415,7 @@ __device__ __forceinline__ void softmax_pv(const uint8_t* blk, uint32_t live, in
 #pragma unroll
   for (int gr = 0; gr < 4; ++gr) {
     const uint4 svv = *reinterpret_cast<const uint4*>(blk + vmeta + 64 * gr + 16 * i);
-    uint32_t sk[4] = {svv.x, svv.y, svv.z, svv.w};
-    if (kInt2) {
-      sk[1] = hmul2(sk[1], 0x34003400u);   // x 2^-2 (the code field sits at bit 2)
-      sk[2] = hmul2(sk[2], 0x2C002C00u);   // x 2^-4
-      sk[3] = hmul2(sk[3], 0x24002400u);   // x 2^-6
-    } else {
-      sk[1] = hmul2(sk[1], 0x2C002C00u);   // x 2^-4 (nibble at bit 4)
-      sk[3] = hmul2(sk[3], 0x2C002C00u);
-    }
+    const uint32_t sk[4] = {svv.x, svv.y, svv.z, svv.w};
     uint32_t bh[4], bl[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -442,16 +440,17 @@ __device__ __forceinline__ void softmax_pv(const uint8_t* blk, uint32_t live, in
       const int m = 2 * gr + mm;
       uint32_t a[2][4];
       if (kInt2) {
-        const uint32_t e0 = wv[mm], e1 = wv[mm] >> 8;
-        a[0][0] = unmagic(e0 & kQ0); a[0][1] = unmagic(e1 & kQ0);
-        a[0][2] = unmagic(e0 & (kQ0 << 2)); a[0][3] = unmagic(e1 & (kQ0 << 2));
-        a[1][0] = unmagic(e0 & (kQ0 << 4)); a[1][1] = unmagic(e1 & (kQ0 << 4));
-        a[1][2] = unmagic(e0 & (kQ0 << 6)); a[1][3] = unmagic(e1 & (kQ0 << 6));
+        // channel 16m+r in bytes 0/2, 16m+r+8 in bytes 1/3 (see the layout)
+        const uint32_t x = wv[mm], xr = x >> 4, xl = x << 4, xo = rotr8(x);
+        a[0][0] = xo & kC8; a[0][1] = x & kC8;     // slots (8i, 8i+4), p = 8
+        a[0][2] = xl & kC6; a[0][3] = xr & kC6;    // slots (8i+1, 8i+5), p = 6
+        a[1][0] = xl & kC8; a[1][1] = xr & kC8;    // slots (8i+2, 8i+6), p = 8
+        a[1][2] = x & kC6; a[1][3] = xo & kC6;     // slots (8i+3, 8i+7), p = 6
       } else {
-        const uint32_t w0 = wv[2 * mm], w1 = wv[2 * mm + 1];
-        const uint32_t x0 = w0 >> 8, x1 = w1 >> 8;
-        a[0][0] = unmagic(w0 & kM0); a[0][1] = unmagic(w1 & kM0); a[0][2] = unmagic(w0 & kM1); a[0][3] = unmagic(w1 & kM1);
-        a[1][0] = unmagic(x0 & kM0); a[1][1] = unmagic(x1 & kM0); a[1][2] = unmagic(x0 & kM1); a[1][3] = unmagic(x1 & kM1);
+        // slot 8i+k in nibble k; nibbles k and k+4 moved to bit 6 of each half
+        const uint32_t w0 = wv[2 * mm], w1 = wv[2 * mm + 1];   // channels 16m+r, 16m+r+8
+        a[0][0] = (w0 << 6) & kN6; a[0][1] = (w1 << 6) & kN6; a[0][2] = (w0 << 2) & kN6; a[0][3] = (w1 << 2) & kN6;
+        a[1][0] = (w0 >> 2) & kN6; a[1][1] = (w1 >> 2) & kN6; a[1][2] = (w0 >> 6) & kN6; a[1][3] = (w1 >> 6) & kN6;
       }
       // This page's products go to a fresh accumulator, added to the running
       // sum in fp32: the tensor core aligns products to the accumulator's
@@ -478,16 +477,19 @@ __device__ __forceinline__ void build_bq(CtaSmem& S, bool int2, int w, bool is_l
   const int lane = threadIdx.x & 31, r = lane >> 2, i = lane & 3;
   if (int2) {
     const int hq2 = kComb ? (r & 3) : r;
-    const int E = S.eh[hq2];
+    const int E = S.eh2[hq2];
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const int j = 2 * (kk & 3) + e, wi = kk >> 2;
-        const int clo = 4 * (8 * i + 4 * wi + (j >> 2)) + (j & 3);
-        const int wexp = 2 * (j & 3);
-        bq[2 * kk + e] = hq2 < G ? pack_h2(ldexpf(S.qraw[hq2][clo], E - wexp), ldexpf(S.qraw[hq2][clo + 8], E - wexp))
-                                 : 0u;
+        // k-slots of a0/a1 (e = 0) hold the field at bit 6, those of a2/a3 the
+        // field at bit 8 (factor 2^-2); register 0 has its halves swapped
+        const int jj = kk & 3, wi = kk >> 2;
+        const int j = e ? i2_reg8(jj) : i2_reg6(jj);
+        const int c = 4 * (8 * i + 4 * wi + (j >> 2)) + (j & 3);
+        const int clo = j == 0 ? c + 8 : c, chi = j == 0 ? c : c + 8;
+        const int ex = E - 2 * e;
+        bq[2 * kk + e] = hq2 < G ? pack_h2(ldexpf(S.qraw[hq2][clo], ex), ldexpf(S.qraw[hq2][chi], ex)) : 0u;
       }
     // negated copies for the exact hi/lo split (g <= 4: lo columns only)
     __syncwarp();
@@ -498,15 +500,18 @@ __device__ __forceinline__ void build_bq(CtaSmem& S, bool int2, int w, bool is_l
     __syncwarp();
   } else {
     const int n = kComb ? (r & 3) : r;   // g <= 4: columns 4..7 repeat heads 0..3
-    const int E = S.eh[n];
+    const int E = S.eh4[n];
 #pragma unroll
     for (int gr = 0; gr < 4; ++gr)
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
+        // nibbles (2hf, 2hf+4) at bit 6; nibbles (2hf+1, 2hf+5) at bit 4 for
+        // hf = 0 (factor 2^2), at bit 6 for hf = 1
         const int c0 = 32 * gr + 8 * i + 2 * hf, c1 = c0 + 1;
+        const int e1 = hf == 0 ? E + 2 : E;
         bq[4 * gr + 2 * hf] = n < G ? pack_h2(ldexpf(S.qraw[n][c0], E), ldexpf(S.qraw[n][c0 + 4], E)) : 0u;
         bq[4 * gr + 2 * hf + 1] =
-            n < G ? pack_h2(ldexpf(S.qraw[n][c1], E - 4), ldexpf(S.qraw[n][c1 + 4], E - 4)) : 0u;
+            n < G ? pack_h2(ldexpf(S.qraw[n][c1], e1), ldexpf(S.qraw[n][c1 + 4], e1)) : 0u;
       }
   }
 }
@@ -564,10 +569,17 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(
         for (int k = 0; k < 4; ++k) qg[k] += __shfl_xor_sync(0xFFFFFFFFu, qg[k], o);
       }
       if (lane == 0) {
-        int E = 0;
-        if (mx > 0.0f) E = max(-100, min(100, ilogbf(16384.0f / (mx * smax))));
-        S.eh[h] = E;
-        S.acol[h] = ldexpf(scale_log2, -E);
+        int E2 = 0, E4 = 0;
+        if (mx > 0.0f) {
+          // INT2 K folds q * scale: |q * scale| * 2^E2 <= 2^14
+          E2 = max(-100, min(100, ilogbf(16384.0f / (mx * smax))));
+          // INT4 K: |q| * 2^E4 < 2^13 (q of the bit-4 fields carries another 2^2)
+          E4 = max(-100, min(100, 12 - ilogbf(mx)));
+        }
+        S.eh2[h] = E2;
+        S.eh4[h] = E4;
+        S.acol2[h] = ldexpf(scale_log2, 18 - E2);
+        S.acol4[h] = ldexpf(scale_log2, 18 - E4);
         unsigned short hi[4], lo[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) split_f16(scale_log2 * qg[k], hi[k], lo[k]);
@@ -582,7 +594,8 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(
       for (int pr = lane; pr < kHeadDim / 2; pr += 32) {
         const int j = pr & 7, iw = pr >> 3;        // iw = chunk i * 2 + word wi
         const int c = 4 * (4 * iw + (j >> 2)) + (j & 3);
-        S.qzh[h][pr] = pack_h2(ldexpf(S.qraw[h][c], Ez), ldexpf(S.qraw[h][c + 8], Ez));
+        const int clo = j == 0 ? c + 8 : c, chi = j == 0 ? c : c + 8;   // pair 0 is stored swapped
+        S.qzh[h][pr] = pack_h2(ldexpf(S.qraw[h][clo], Ez), ldexpf(S.qraw[h][chi], Ez));
       }
       if (lane == 0) S.qzs[h] = ldexpf(scale_log2, -Ez);
     }
@@ -596,7 +609,8 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(
       bz[0] = S.bz[hz][2 * i];
       bz[1] = S.bz[hz][2 * i + 1];
     }
-    const float acol[2] = {S.acol[hp2], S.acol[hp2 + 1]};
+    const float acol2[2] = {S.acol2[hp2], S.acol2[hp2 + 1]};
+    const float acol4[2] = {S.acol4[hp2], S.acol4[hp2 + 1]};
 
     // ---- page loop: two-stage bulk-copy ring per warp
     const Entry* tab = table + (size_t)u.req * max_pages;
@@ -646,10 +660,10 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(
       const uint8_t* blk = WS.stage[st];
       float lg[2][4];
       if (i2) {
-        qk_int2<G>(blk, bq, &S.bqn[w][0][0], acol, S, lg);
+        qk_int2<G>(blk, bq, &S.bqn[w][0][0], acol2, S, lg);
         softmax_pv<G, true>(blk, e.live, r, i, is_lo, pscale, lg, o, zv, mrun, lsum, WS.pbuf);
       } else {
-        qk_int4<G>(blk, bq, bz, acol, lg);
+        qk_int4<G>(blk, bq, bz, acol4, lg);
         softmax_pv<G, false>(blk, e.live, r, i, is_lo, pscale, lg, o, zv, mrun, lsum, WS.pbuf);
       }
       if (k + kStages < nw) {
@@ -701,7 +715,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(
           if (h < G) {
             float zt = S.zv[w][m >> 1][h];
             if (kComb) zt += S.zv[w][m >> 1][h + 4];
-            accw[h * kHeadDim + ch] = (o[m][cc] + zt) * oscale;
+            accw[h * kHeadDim + ch] = fmaf(o[m][cc], kCodeUnit, zt) * oscale;
           }
         }
       if (r == 0)

@@ -5,7 +5,9 @@
 // (mma.m16n8k16, lane = 4*r + i): every lane reads its codes with 16-byte
 // shared-memory loads that hit 8 distinct 16-byte bank groups per quarter
 // warp, and one 32-bit code word unpacks into whole A-fragment registers with
-// masks alone (codes become binary16 subnormals code * 2^-24).
+// a shift and a mask each: a field at bits p..p+w-1 of both 16-bit halves is
+// the binary16 subnormal code * 2^(p-24) (p >= 4, so the field's top bit is at
+// bit 7 or above).
 //
 // INT4 block (5120 B)
 //   [   0, 2048) K codes: slot t row at 64*t; row = 4 chunks (i) x 4 groups
@@ -27,12 +29,16 @@
 //   [1024, 2048) V codes, channel-major: word (r, m, i) holds channels
 //                16m+r (bytes 0, 2) and 16m+r+8 (bytes 1, 3) for slot chunk i:
 //                byte 0/1 hold slots 8i..8i+3, bytes 2/3 slots 8i+4..8i+7,
-//                slot 8i+k at bits 2k of its byte.  The word sits at 16-byte
-//                chunk 32*(m>>2) + 4*r + i, word m&3 inside the chunk.
+//                slot 8i+k at bits 2k of its byte, except that channel
+//                16m+r keeps slot 8i in byte 2 and slot 8i+4 in byte 0 (a
+//                byte rotation of the word then lines both up with channel
+//                16m+r+8).  The word sits at 16-byte chunk 32*(m>>2) + 4*r + i,
+//                word m&3 inside the chunk.
 //   [2048, 2560) K scales: 128 halves in pair order, then zeros in the same
 //                order.  Pair p = (i*2 + wi)*8 + j holds the channels that
 //                A-register j of code word (chunk i, word wi) carries: low half
-//                = channel 4*(8i + 4wi + (j>>2)) + (j&3), high half = that + 8.
+//                = channel 4*(8i + 4wi + (j>>2)) + (j&3), high half = that + 8;
+//                pair j = 0 has the two halves the other way round.
 //   [2560, 3072) V scale/zero: as in the INT4 block.
 #pragma once
 #include <stdint.h>
@@ -79,7 +85,8 @@ KVQ_HD int i2k_shift(int c) { return 2 * (c & 3); }
 KVQ_HD int i2v_byte(int t, int c) {
   const int m = c >> 4, e = (c >> 3) & 1, r = c & 7;
   const int i = t >> 3, k = t & 7;
-  return kI2VCodes + 16 * (32 * (m >> 2) + 4 * r + i) + 4 * (m & 3) + e + 2 * (k >> 2);
+  const int half = (k >> 2) ^ ((e == 0 && (k & 3) == 0) ? 1 : 0);
+  return kI2VCodes + 16 * (32 * (m >> 2) + 4 * r + i) + 4 * (m & 3) + e + 2 * half;
 }
 KVQ_HD int i2v_shift(int t) { return 2 * (t & 3); }
 
@@ -87,7 +94,7 @@ KVQ_HD int i2v_shift(int t) { return 2 * (t & 3); }
 KVQ_HD int i2k_meta_index(int c) {
   const int i = c >> 5, wi = (c >> 4) & 1, b = (c >> 2) & 3, pos = c & 3;
   const int j = (b & 1) * 4 + pos;      // bytes 0,2 -> regs 0..3; bytes 1,3 -> regs 4..7
-  const int hi = b >> 1;                // bytes 2,3 are the high half
+  const int hi = (b >> 1) ^ (j == 0 ? 1 : 0);   // bytes 2,3 are the high half (swapped for j = 0)
   return 2 * ((i * 2 + wi) * 8 + j) + hi;
 }
 
