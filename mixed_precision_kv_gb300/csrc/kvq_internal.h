@@ -64,9 +64,16 @@ struct Split {
   int32_t cta;
 };
 
-// Planner cost of one page: its block bytes plus this fixed term for the
-// scan's per-page compute.
-constexpr double kPageCost = 2048.0;
+// Planner cost of one page by precision, proportional to the scan kernel's
+// time per page.  The tensor-core scan is bound by instruction issue, and an
+// INT2 page takes about 1.1x the time of an INT4 page (all-INT2 vs all-INT4
+// pools of the 32K-token batch-8 step); the CUDA-core scan is charged its
+// block bytes plus 2048.
+struct PageCost {
+  double int2, int4;
+};
+constexpr PageCost kMmaPageCost{1.10, 1.00};
+constexpr PageCost kSimtPageCost{3072.0 + 2048.0, 5120.0 + 2048.0};
 constexpr int64_t kMinPagesPerCta = 16;
 constexpr int64_t kTimingRing = 2048;
 
@@ -146,7 +153,8 @@ cudaError_t launch_scatter(kv_pool* P, const TableUpd* d_upd, int n, cudaStream_
 // Balanced decode plan: units (batch row, kv head) in order, their pages cut
 // into n_ctas contiguous ranges of about equal cost (bytes + a fixed per-page
 // term), each range split further at unit boundaries (kvq_pool.cu).
-void plan_decode(const kv_pool* P, const int32_t* req_ids, int32_t batch, int64_t n_ctas, HostPlan& out);
+void plan_decode(const kv_pool* P, const int32_t* req_ids, int32_t batch, int64_t n_ctas, PageCost cost,
+                 HostPlan& out);
 
 // Launchers (kvq_decode_simt.cu / kvq_decode_mma.cu)
 cudaError_t launch_decode_simt(kv_pool* P, const void* q, int32_t hq, float scale_log2, const Unit* d_units,

@@ -152,10 +152,11 @@ kv_status_t order_after_previous(kv_pool* P, cudaStream_t s) {
 
 void kvq::set_last_error(const char* msg) { g_err = msg; }
 
-void kvq::plan_decode(const kv_pool* P, const int32_t* req_ids, int32_t batch, int64_t n_ctas, HostPlan& out) {
+void kvq::plan_decode(const kv_pool* P, const int32_t* req_ids, int32_t batch, int64_t n_ctas, PageCost pc,
+                       HostPlan& out) {
   const int hkv = P->cfg.num_kv_heads;
   const int64_t n2 = P->cfg.n_int2_pages;
-  auto cost = [&](int32_t id) { return (id < n2 ? (double)kInt2Block : (double)kInt4Block) + kPageCost; };
+  auto cost = [&](int32_t id) { return id < n2 ? pc.int2 : pc.int4; };
   double total = 0.0;
   int64_t pages = 0;
   for (int32_t b = 0; b < batch; ++b)
@@ -625,8 +626,8 @@ namespace {
 // from the occupancy API and work is partitioned before the launch).  All
 // (batch row, kv head) units' pages, in order, are cut into n_ctas contiguous
 // ranges of about equal cost; a range that crosses unit boundaries becomes one
-// split per unit.  Cost of a page = its block bytes + a fixed per-page term
-// for the scan's compute, so INT2 and INT4 pages are weighed fairly.
+// split per unit.  A page costs what the chosen scan kernel spends on a page
+// of its precision (PageCost), so INT2 and INT4 pages are weighed fairly.
 
 kv_status_t build_plan(kv_pool* P, const int32_t* req_ids, int32_t batch, int32_t hq, int32_t impl,
                        cudaStream_t s) {
@@ -638,7 +639,8 @@ kv_status_t build_plan(kv_pool* P, const int32_t* req_ids, int32_t batch, int32_
 
   const int ctas = impl == KV_DECODE_MMA ? decode_mma_ctas_per_sm(g) : decode_simt_ctas_per_sm(g);
   HostPlan hp;
-  plan_decode(P, req_ids, batch, (int64_t)P->sm_count * ctas, hp);
+  plan_decode(P, req_ids, batch, (int64_t)P->sm_count * ctas, impl == KV_DECODE_MMA ? kMmaPageCost : kSimtPageCost,
+              hp);
   Upload up;
   const size_t ou = up.add(hp.units.data(), hp.units.size() * sizeof(Unit));
   const size_t os = up.add(hp.splits.data(), hp.splits.size() * sizeof(Split));
