@@ -25,15 +25,16 @@
 //  * P.V: out_c = sum_t p_t (scale_tg code_tc + zero_tg); p_t * scale_tg is
 //      folded as an fp16 pair (p = p_hi + p_lo, then p_hi*s exactly and p_lo*s
 //      rounded); the zero term sum_t p_t zero_tg is a small mma.
-//  * For g <= 4 the eight N columns carry (hi | lo) of the same four heads,
-//    so one mma does both halves; for g > 4 hi and lo are two mmas into the
-//    same accumulator.
+//  * For g <= 4 the eight N columns are (head, part) pairs: hi / lo of the
+//    exact split (INT2 K, P.V) or even / odd channel group (INT4 K), so one
+//    mma does both parts and each lane owns one head; for g > 4 hi and lo
+//    are two mmas.
 //  * q is scaled by a power of two per head so that q * scale stays inside
 //    the binary16 range, and P by a power of two so that P * scale stays out
 //    of the subnormal range (the pool tracks the largest INT2 K and V scales).
 // Pages stream through a two-stage per-warp ring filled by cp.async.bulk with
 // mbarrier completion; every wait is bounded and reports a timeout status.
-// 3 CTAs of 4 warps per SM (168 registers, no spills).
+// 3 CTAs of 4 warps per SM.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -66,7 +67,8 @@ struct CtaSmem {
   float qraw[8][kHeadDim];             // q (fp32) of the packed heads
   uint32_t qzh[8][kHeadDim / 2];       // 2^Ez q as binary16 pairs in the INT2 K scale/zero pair order
   float qzs[8];                        // 2^(-Ez) * scale * log2(e)
-  uint4 bqn[kWarps][4][32];            // INT2 K: negated q fragments (g <= 4: lo columns only, else 0)
+  uint4 bq2[4][32], bqn[4][32];        // INT2 K q fragments [word / 4][lane], negated copies (lo columns)
+  uint4 bq4[4][32];                    // INT4 K q fragments
   float acol2[8], acol4[8];            // 2^(18 - E) * scale * log2(e) for INT2 / INT4 K pages
   int eh2[8], eh4[8];                  // per-head power-of-two q scales E for INT2 / INT4 K pages
   uint32_t bz[8][4];                   // fp16 pairs: hi(Q0,Q1), hi(Q2,Q3), lo(Q0,Q1), lo(Q2,Q3) of scale*log2(e)*Q_{h,group}
@@ -164,11 +166,32 @@ __device__ __forceinline__ bool bar_wait(unsigned long long* b, uint32_t phase) 
   return false;
 }
 
-// ---- logits of one INT4 page: lg[m][c] for tokens 16m + r + 8(c>>1), heads 2i + (c&1)
+// Lanes and heads.  A lane is (r, i) = (lane >> 2, lane & 3); its C fragment
+// holds rows r and r + 8 of columns 2i and 2i + 1.  For g <= 4 ("paired
+// columns") the eight N columns are (head, part) pairs, column n = 2 * head +
+// part, where part is hi / lo of an exact fp16 split (INT2 K, P.V) or the
+// even / odd channel group (INT4 K): lane (r, i) then owns head i and both
+// parts meet in its registers.  For g > 4 the columns are heads and a lane
+// owns heads 2i and 2i + 1.  NH = heads per lane.
 template <int G>
-__device__ __forceinline__ void qk_int4(const uint8_t* blk, const uint32_t (&bq)[16], const uint32_t (&bz)[2],
-                                        const float (&acol)[2], float (&lg)[2][4]) {
+struct Cols {
+  static constexpr bool kPair = G <= 4;
+  static constexpr int NH = kPair ? 1 : 2;
+};
+
+// ---- logits of one INT4 page: lg[m][e][hh] for token 16m + r + 8e and the
+// lane's head hh (log2 units, scale folded in)
+template <int G>
+__device__ __forceinline__ void qk_int4(const uint8_t* blk, const uint4* bq4, const uint32_t (&bz)[2],
+                                        const float (&acol)[Cols<G>::NH], float (&lg)[2][2][Cols<G>::NH]) {
+  constexpr bool kPair = Cols<G>::kPair;
   const int lane = threadIdx.x & 31, r = lane >> 2, i = lane & 3;
+  uint32_t bq[16];
+#pragma unroll
+  for (int x4 = 0; x4 < 4; ++x4) {
+    const uint4 b = bq4[x4 * 32 + lane];
+    bq[4 * x4] = b.x; bq[4 * x4 + 1] = b.y; bq[4 * x4 + 2] = b.z; bq[4 * x4 + 3] = b.w;
+  }
 #pragma unroll
   for (int m = 0; m < 2; ++m) {
     uint4 kw[2], km[2];
@@ -178,42 +201,69 @@ __device__ __forceinline__ void qk_int4(const uint8_t* blk, const uint32_t (&bq)
       kw[e] = *reinterpret_cast<const uint4*>(blk + kI4KCodes + 64 * t + 16 * i);
       km[e] = *reinterpret_cast<const uint4*>(blk + kI4KMeta + 16 * t);
     }
-    float acc[4][4];
-#pragma unroll
-    for (int gr = 0; gr < 4; ++gr) {
-      acc[gr][0] = acc[gr][1] = acc[gr][2] = acc[gr][3] = 0.0f;
+    // Group gr's k-steps: nibbles 0/4 at p = 6, 1/5 at p = 4, then 2/6 and 3/7 at p = 6.
+    auto group_mma = [&](float (&acc)[4], int gr) {
       const uint32_t x0 = comp(kw[0], gr), x1 = comp(kw[1], gr);   // tokens r, r + 8
-      // k-step 0: nibbles 0/4 at p = 6, nibbles 1/5 at p = 4; k-step 1: 2/6 and 3/7 at p = 6
-      mma16816(acc[gr], (x0 << 6) & kN6, (x1 << 6) & kN6, x0 & kN4, x1 & kN4, bq[4 * gr], bq[4 * gr + 1]);
-      mma16816(acc[gr], (x0 >> 2) & kN6, (x1 >> 2) & kN6, (x0 >> 6) & kN6, (x1 >> 6) & kN6, bq[4 * gr + 2],
+      mma16816(acc, (x0 << 6) & kN6, (x1 << 6) & kN6, x0 & kN4, x1 & kN4, bq[4 * gr], bq[4 * gr + 1]);
+      mma16816(acc, (x0 >> 2) & kN6, (x1 >> 2) & kN6, (x0 >> 6) & kN6, (x1 >> 6) & kN6, bq[4 * gr + 2],
                bq[4 * gr + 3]);
-    }
-    float T[4];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const int e = c >> 1;
-      float v = 0.0f;
-#pragma unroll
-      for (int gr = 0; gr < 4; ++gr) v = fmaf(h_lo(comp(km[e], gr)), acc[gr][c], v);
-      T[c] = v * acol[c & 1];
-    }
+    };
     // zero term sum_g zero_tg * (scale log2e Q_g) by one mma: every lane feeds
     // (zero_0, zero_1) in k-slots 2i, 2i+1 and (zero_2, zero_3) in 2i+8, 2i+9;
     // B rows 0, 1 / 8, 9 hold the hi parts of Q, rows 2, 3 / 10, 11 the lo
     // parts, the other rows zero.
     const uint32_t az0 = __byte_perm(km[0].x, km[0].y, 0x7632), az2 = __byte_perm(km[0].z, km[0].w, 0x7632);
     const uint32_t az1 = __byte_perm(km[1].x, km[1].y, 0x7632), az3 = __byte_perm(km[1].z, km[1].w, 0x7632);
-    mma16816(T, az0, az1, az2, az3, bz[0], bz[1]);
+    if constexpr (kPair) {
+      // acc[0]: groups 0 / 1 in columns 2h / 2h+1, acc[1]: groups 2 / 3
+      float acc[2][4];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) lg[m][c] = T[c];
+      for (int pr = 0; pr < 2; ++pr) {
+        acc[pr][0] = acc[pr][1] = acc[pr][2] = acc[pr][3] = 0.0f;
+        group_mma(acc[pr], 2 * pr);
+        group_mma(acc[pr], 2 * pr + 1);
+      }
+      float T[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float v = h_lo(km[e].x) * acc[0][2 * e];
+        v = fmaf(h_lo(km[e].y), acc[0][2 * e + 1], v);
+        v = fmaf(h_lo(km[e].z), acc[1][2 * e], v);
+        v = fmaf(h_lo(km[e].w), acc[1][2 * e + 1], v);
+        T[2 * e] = v * acol[0];
+      }
+      mma16816(T, az0, az1, az2, az3, bz[0], bz[1]);   // B: even columns only
+      lg[m][0][0] = T[0];
+      lg[m][1][0] = T[2];
+    } else {
+      float acc[4][4];
+#pragma unroll
+      for (int gr = 0; gr < 4; ++gr) {
+        acc[gr][0] = acc[gr][1] = acc[gr][2] = acc[gr][3] = 0.0f;
+        group_mma(acc[gr], gr);
+      }
+      float T[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int e = c >> 1;
+        float v = 0.0f;
+#pragma unroll
+        for (int gr = 0; gr < 4; ++gr) v = fmaf(h_lo(comp(km[e], gr)), acc[gr][c], v);
+        T[c] = v * acol[c & 1];
+      }
+      mma16816(T, az0, az1, az2, az3, bz[0], bz[1]);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) lg[m][c >> 1][c & 1] = T[c];
+    }
   }
 }
 
-// ---- logits of one INT2 page
+// ---- logits of one INT2 page (same layout as qk_int4)
 template <int G>
-__device__ __forceinline__ void qk_int2(const uint8_t* blk, const uint32_t (&bq)[16], const uint4* bqn4,
-                                        const float (&acol)[2], const CtaSmem& S, float (&lg)[2][4]) {
-  constexpr bool kComb = G <= 4;
+__device__ __forceinline__ void qk_int2(const uint8_t* blk, const uint4* bq2, const uint4* bqn,
+                                        const float (&acol)[Cols<G>::NH], const CtaSmem& S,
+                                        float (&lg)[2][2][Cols<G>::NH]) {
+  constexpr bool kPair = Cols<G>::kPair;
   const int lane = threadIdx.x & 31, r = lane >> 2, i = lane & 3;
   uint2 kw[2][2];
 #pragma unroll
@@ -224,35 +274,34 @@ __device__ __forceinline__ void qk_int2(const uint8_t* blk, const uint32_t (&bq)
   uint4 sv[4];
 #pragma unroll
   for (int x = 0; x < 4; ++x) sv[x] = *reinterpret_cast<const uint4*>(blk + kI2KMeta + 64 * i + 16 * x);
-  // four independent accumulators per M tile (k-step parity x hi/lo pass) so
-  // that consecutive mmas do not wait on each other
-  float acc[2][4][4];
+  // two accumulators per M tile so that consecutive mmas do not wait on each
+  // other (g <= 4: alternating k-steps; g > 4: the hi and the lo pass)
+  float acc[2][2][4];
 #pragma unroll
   for (int m = 0; m < 2; ++m)
 #pragma unroll
-    for (int x = 0; x < 4; ++x) acc[m][x][0] = acc[m][x][1] = acc[m][x][2] = acc[m][x][3] = 0.0f;
+    for (int x = 0; x < 2; ++x) acc[m][x][0] = acc[m][x][1] = acc[m][x][2] = acc[m][x][3] = 0.0f;
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
     const int wi = kk >> 2, jj = kk & 3;
     const int p0 = wi * 8 + i2_reg6(jj), p1 = wi * 8 + i2_reg8(jj);
     const uint32_t s0 = comp(sv[p0 >> 2], p0 & 3), s1 = comp(sv[p1 >> 2], p1 & 3);
+    const uint4 qq = bq2[(kk >> 1) * 32 + lane], nq = bqn[(kk >> 1) * 32 + lane];
+    const uint32_t q0 = (kk & 1) ? qq.z : qq.x, q1 = (kk & 1) ? qq.w : qq.y;
+    const uint32_t n0 = (kk & 1) ? nq.z : nq.x, n1 = (kk & 1) ? nq.w : nq.y;
     // hi = rn(q s); lo = q s - hi (exact).  bqn holds -q where the lo part is
     // wanted and 0 elsewhere, so u = fma(q, s, rn(bqn s)) is lo or hi.
-    const uint4 nq = bqn4[(kk >> 1) * 32 + lane];
-    const uint32_t n0 = (kk & 1) ? nq.z : nq.x, n1 = (kk & 1) ? nq.w : nq.y;
-    const uint32_t u0 = hfma2(bq[2 * kk], s0, hmul2(n0, s0)), u1 = hfma2(bq[2 * kk + 1], s1, hmul2(n1, s1));
-    uint32_t t0 = 0u, t1 = 0u;
-    if (!kComb) { t0 = hmul2(bq[2 * kk], s0); t1 = hmul2(bq[2 * kk + 1], s1); }
+    const uint32_t u0 = hfma2(q0, s0, hmul2(n0, s0)), u1 = hfma2(q1, s1, hmul2(n1, s1));
 #pragma unroll
     for (int m = 0; m < 2; ++m) {
       const uint32_t x0 = i2_variant(wi ? kw[m][0].y : kw[m][0].x, jj);   // token 16m + r
       const uint32_t x1 = i2_variant(wi ? kw[m][1].y : kw[m][1].x, jj);   // token 16m + r + 8
       const uint32_t a0 = x0 & kC6, a1 = x1 & kC6, a2 = x0 & kC8, a3 = x1 & kC8;
-      if (kComb) {
-        mma16816(acc[m][kk & 3], a0, a1, a2, a3, u0, u1);
+      if constexpr (kPair) {
+        mma16816(acc[m][kk & 1], a0, a1, a2, a3, u0, u1);
       } else {
-        mma16816(acc[m][2 * (kk & 1)], a0, a1, a2, a3, t0, t1);
-        mma16816(acc[m][2 * (kk & 1) + 1], a0, a1, a2, a3, u0, u1);
+        mma16816(acc[m][0], a0, a1, a2, a3, hmul2(q0, s0), hmul2(q1, s1));
+        mma16816(acc[m][1], a0, a1, a2, a3, u0, u1);
       }
     }
   }
@@ -260,18 +309,18 @@ __device__ __forceinline__ void qk_int2(const uint8_t* blk, const uint32_t (&bq)
   // reduced over the lanes of head h
   float zp = 0.0f;
   int hz;
-  if (kComb) {
+  if constexpr (kPair) {
     const int wi = r >> 2;
     hz = r & 3;
     const uint4* zs = reinterpret_cast<const uint4*>(blk + kI2KMeta + 256 + 64 * i + 32 * wi);
     const uint4* qs = reinterpret_cast<const uint4*>(&S.qzh[hz][(i * 2 + wi) * 8]);
 #pragma unroll
     for (int x4 = 0; x4 < 2; ++x4) {
-      const uint4 zz = zs[x4], qq = qs[x4];
-      zp = fma2_f16_f32(zz.x, qq.x, zp);
-      zp = fma2_f16_f32(zz.y, qq.y, zp);
-      zp = fma2_f16_f32(zz.z, qq.z, zp);
-      zp = fma2_f16_f32(zz.w, qq.w, zp);
+      const uint4 zz = zs[x4], qz = qs[x4];
+      zp = fma2_f16_f32(zz.x, qz.x, zp);
+      zp = fma2_f16_f32(zz.y, qz.y, zp);
+      zp = fma2_f16_f32(zz.z, qz.z, zp);
+      zp = fma2_f16_f32(zz.w, qz.w, zp);
     }
     zp += __shfl_xor_sync(0xFFFFFFFFu, zp, 1);
     zp += __shfl_xor_sync(0xFFFFFFFFu, zp, 2);
@@ -282,49 +331,61 @@ __device__ __forceinline__ void qk_int2(const uint8_t* blk, const uint32_t (&bq)
     const uint4* qs = reinterpret_cast<const uint4*>(&S.qzh[hz][i * 16]);
 #pragma unroll
     for (int x4 = 0; x4 < 4; ++x4) {
-      const uint4 zz = zs[x4], qq = qs[x4];
-      zp = fma2_f16_f32(zz.x, qq.x, zp);
-      zp = fma2_f16_f32(zz.y, qq.y, zp);
-      zp = fma2_f16_f32(zz.z, qq.z, zp);
-      zp = fma2_f16_f32(zz.w, qq.w, zp);
+      const uint4 zz = zs[x4], qz = qs[x4];
+      zp = fma2_f16_f32(zz.x, qz.x, zp);
+      zp = fma2_f16_f32(zz.y, qz.y, zp);
+      zp = fma2_f16_f32(zz.z, qz.z, zp);
+      zp = fma2_f16_f32(zz.w, qz.w, zp);
     }
     zp += __shfl_xor_sync(0xFFFFFFFFu, zp, 1);
     zp += __shfl_xor_sync(0xFFFFFFFFu, zp, 2);
   }
   zp *= S.qzs[hz];
-  const float zc0 = __shfl_sync(0xFFFFFFFFu, zp, 4 * (2 * i));
-  const float zc1 = __shfl_sync(0xFFFFFFFFu, zp, 4 * (2 * i + 1));
+  if constexpr (kPair) {
+    const float zc = __shfl_sync(0xFFFFFFFFu, zp, 4 * i);   // head i lives on lanes with r & 3 = i
 #pragma unroll
-  for (int m = 0; m < 2; ++m)
+    for (int m = 0; m < 2; ++m)
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      float v = (acc[m][0][c] + acc[m][1][c]) + (acc[m][2][c] + acc[m][3][c]);
-      if (kComb) v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
-      lg[m][c] = fmaf(acol[c & 1], v, (c & 1) ? zc1 : zc0);
-    }
+      for (int e = 0; e < 2; ++e) {
+        const float v = (acc[m][0][2 * e] + acc[m][0][2 * e + 1]) + (acc[m][1][2 * e] + acc[m][1][2 * e + 1]);
+        lg[m][e][0] = fmaf(acol[0], v, zc);
+      }
+  } else {
+    const float zc[2] = {__shfl_sync(0xFFFFFFFFu, zp, 4 * (2 * i)), __shfl_sync(0xFFFFFFFFu, zp, 4 * (2 * i + 1))};
+#pragma unroll
+    for (int m = 0; m < 2; ++m)
+#pragma unroll
+      for (int e = 0; e < 2; ++e)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+          lg[m][e][hh] = fmaf(acol[hh], acc[m][0][2 * e + hh] + acc[m][1][2 * e + hh], zc[hh]);
+  }
 }
 
 // ---- online softmax update and P.V for one page (either width)
 template <int G, bool kInt2>
-__device__ __forceinline__ void softmax_pv(const uint8_t* blk, uint32_t live, int r, int i, bool is_lo, float pscale,
-                                           float (&lg)[2][4], float (&o)[8][4], float (&zv)[4], float (&mrun)[2],
-                                           float (&lsum)[2], float (*pbuf)[kPage]) {
-  constexpr bool kComb = G <= 4;
+__device__ __forceinline__ void softmax_pv(const uint8_t* blk, uint32_t live, float pscale,
+                                           float (&lg)[2][2][Cols<G>::NH], float (&o)[8][4], float (&zv)[4],
+                                           float (&mrun)[Cols<G>::NH], float (&lsum)[Cols<G>::NH],
+                                           float (*pbuf)[kPage]) {
+  constexpr bool kPair = Cols<G>::kPair;
+  constexpr int NH = Cols<G>::NH;
   constexpr int vmeta = kInt2 ? kI2VMeta : kI4VMeta;
+  const int lane = threadIdx.x & 31, r = lane >> 2, i = lane & 3;
   const bool full = live == 0xFFFFFFFFu;   // warp-uniform: no dead slot on this page
   if (!full) {
 #pragma unroll
     for (int m = 0; m < 2; ++m)
 #pragma unroll
       for (int e = 0; e < 2; ++e)
-        if (!((live >> (16 * m + r + 8 * e)) & 1u)) lg[m][2 * e] = lg[m][2 * e + 1] = kDead2;
-  }
-  // Lanes i and i ^ 2 hold the same logits for g <= 4, so their softmax
-  // state (and the rescale factor of their accumulator columns) agree.
-  float corr[2], pv[2][2][2];
+        if (!((live >> (16 * m + r + 8 * e)) & 1u))
 #pragma unroll
-  for (int hh = 0; hh < 2; ++hh) {
-    float pm = fmaxf(fmaxf(lg[0][hh], lg[0][2 + hh]), fmaxf(lg[1][hh], lg[1][2 + hh]));
+          for (int hh = 0; hh < NH; ++hh) lg[m][e][hh] = kDead2;
+  }
+  float corr[NH], pv[2][2][NH];
+#pragma unroll
+  for (int hh = 0; hh < NH; ++hh) {
+    float pm = fmaxf(fmaxf(lg[0][0][hh], lg[0][1][hh]), fmaxf(lg[1][0][hh], lg[1][1][hh]));
     pm = fmaxf(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, 4));
     pm = fmaxf(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, 8));
     pm = fmaxf(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, 16));
@@ -336,8 +397,8 @@ __device__ __forceinline__ void softmax_pv(const uint8_t* blk, uint32_t live, in
     for (int m = 0; m < 2; ++m)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        pv[hh][m][e] = ex2(lg[m][2 * e + hh] - mnew);
-        ps += pv[hh][m][e];
+        pv[m][e][hh] = ex2(lg[m][e][hh] - mnew);
+        ps += pv[m][e][hh];
       }
     lsum[hh] = lsum[hh] * corr[hh] + ps;
   }
@@ -346,19 +407,24 @@ __device__ __forceinline__ void softmax_pv(const uint8_t* blk, uint32_t live, in
     for (int m = 0; m < 2; ++m)
 #pragma unroll
       for (int e = 0; e < 2; ++e)
-        if (!((live >> (16 * m + r + 8 * e)) & 1u)) pv[0][m][e] = pv[1][m][e] = 0.0f;
+        if (!((live >> (16 * m + r + 8 * e)) & 1u))
+#pragma unroll
+          for (int hh = 0; hh < NH; ++hh) pv[m][e][hh] = 0.0f;
   }
-  if (!kComb || i < 2) {
+  {
     // INT2 V: even slots pair with code fields at p = 8, so their P carries 2^-2
     const float pmul = (kInt2 && !(r & 1)) ? 0.25f * pscale : pscale;
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh)
+    for (int hh = 0; hh < NH; ++hh) {
+      const int h = kPair ? i : 2 * i + hh;
+      if (h < G)
 #pragma unroll
-      for (int m = 0; m < 2; ++m)
+        for (int m = 0; m < 2; ++m)
 #pragma unroll
-        for (int e = 0; e < 2; ++e) pbuf[2 * i + hh][16 * m + r + 8 * e] = pv[hh][m][e] * pmul;
+          for (int e = 0; e < 2; ++e) pbuf[h][16 * m + r + 8 * e] = pv[m][e][hh] * pmul;
+    }
   }
-  const float c0 = corr[0], c1 = corr[1];
+  const float c0 = corr[0], c1 = corr[NH - 1];
   if (__any_sync(0xFFFFFFFFu, c0 != 1.0f || c1 != 1.0f)) {
 #pragma unroll
     for (int m = 0; m < 8; ++m) { o[m][0] *= c0; o[m][1] *= c1; o[m][2] *= c0; o[m][3] *= c1; }
@@ -366,8 +432,9 @@ __device__ __forceinline__ void softmax_pv(const uint8_t* blk, uint32_t live, in
   }
   __syncwarp();
 
-  // B operands: p of head hp at slots 8i..8i+7, pairs (8i+k, 8i+k+4)
-  const int hp = kComb ? (r & 3) : r;
+  // B operands: p of the head of column r at slots 8i..8i+7, pairs (8i+k, 8i+k+4)
+  const int hp = kPair ? (r >> 1) : r;
+  const bool lo_col = kPair && (r & 1);
   const float4 pa = *reinterpret_cast<const float4*>(&pbuf[hp][8 * i]);
   const float4 pb = *reinterpret_cast<const float4*>(&pbuf[hp][8 * i + 4]);
   const float pav[4] = {pa.x, pa.y, pa.z, pa.w}, pbv[4] = {pb.x, pb.y, pb.z, pb.w};
@@ -386,11 +453,9 @@ __device__ __forceinline__ void softmax_pv(const uint8_t* blk, uint32_t live, in
       zz.z = hmul2(zz.z, 0x44004400u);
     }
     float zt[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    if (kComb) {
-      const uint32_t b0 = is_lo ? pl[0] : ph[0], b1 = is_lo ? pl[1] : ph[1];
-      const uint32_t b2 = is_lo ? pl[2] : ph[2], b3 = is_lo ? pl[3] : ph[3];
-      mma16816(zt, zz.x, 0u, zz.y, 0u, b0, b1);
-      mma16816(zt, zz.z, 0u, zz.w, 0u, b2, b3);
+    if constexpr (kPair) {
+      mma16816(zt, zz.x, 0u, zz.y, 0u, lo_col ? pl[0] : ph[0], lo_col ? pl[1] : ph[1]);
+      mma16816(zt, zz.z, 0u, zz.w, 0u, lo_col ? pl[2] : ph[2], lo_col ? pl[3] : ph[3]);
     } else {
       mma16816(zt, zz.x, 0u, zz.y, 0u, ph[0], ph[1]);
       mma16816(zt, zz.z, 0u, zz.w, 0u, ph[2], ph[3]);
@@ -405,7 +470,7 @@ __device__ __forceinline__ void softmax_pv(const uint8_t* blk, uint32_t live, in
   //   g <= 4, hi columns: x3 = x1 = 0 -> B = rn(p_hi s);
   //   lo columns (and the lo pass of g > 4): x3 = -p_hi, x1 = p_lo ->
   //   B = rn(p_lo s + (p_hi s - rn(p_hi s))).
-  const uint32_t lomask = (!kComb || is_lo) ? 0xFFFFFFFFu : 0u;
+  const uint32_t lomask = (!kPair || lo_col) ? 0xFFFFFFFFu : 0u;
   uint32_t x3[4], x1[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
@@ -420,7 +485,7 @@ __device__ __forceinline__ void softmax_pv(const uint8_t* blk, uint32_t live, in
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const uint32_t u = hfma2(ph[k], sk[k], hmul2(x3[k], sk[k]));
-      if (kComb) {
+      if constexpr (kPair) {
         bh[k] = hfma2(x1[k], sk[k], u);
       } else {
         bh[k] = hmul2(ph[k], sk[k]);
@@ -459,7 +524,7 @@ __device__ __forceinline__ void softmax_pv(const uint8_t* blk, uint32_t live, in
       float t[4] = {0.0f, 0.0f, 0.0f, 0.0f};
       mma16816(t, a[0][0], a[0][1], a[0][2], a[0][3], bh[0], bh[1]);
       mma16816(t, a[1][0], a[1][1], a[1][2], a[1][3], bh[2], bh[3]);
-      if (!kComb) {
+      if constexpr (!kPair) {
         mma16816(t, a[0][0], a[0][1], a[0][2], a[0][3], bl[0], bl[1]);
         mma16816(t, a[1][0], a[1][1], a[1][2], a[1][3], bl[2], bl[3]);
       }
@@ -470,63 +535,49 @@ __device__ __forceinline__ void softmax_pv(const uint8_t* blk, uint32_t live, in
   __syncwarp();
 }
 
-// q fragments (B operands of the K dot products) for one page precision.
+// ---- q fragments (B operands of the K dot products), built once per segment
+// INT2 K word x = 2 kk + e of lane L: k-slots of a0/a1 (e = 0) hold the field
+// at bit 6, those of a2/a3 (e = 1) the field at bit 8 (factor 2^-2);
+// register 0 of the pair order has its halves swapped.
 template <int G>
-__device__ __forceinline__ void build_bq(CtaSmem& S, bool int2, int w, bool is_lo, uint32_t (&bq)[16]) {
-  constexpr bool kComb = G <= 4;
-  const int lane = threadIdx.x & 31, r = lane >> 2, i = lane & 3;
-  if (int2) {
-    const int hq2 = kComb ? (r & 3) : r;
-    const int E = S.eh2[hq2];
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        // k-slots of a0/a1 (e = 0) hold the field at bit 6, those of a2/a3 the
-        // field at bit 8 (factor 2^-2); register 0 has its halves swapped
-        const int jj = kk & 3, wi = kk >> 2;
-        const int j = e ? i2_reg8(jj) : i2_reg6(jj);
-        const int c = 4 * (8 * i + 4 * wi + (j >> 2)) + (j & 3);
-        const int clo = j == 0 ? c + 8 : c, chi = j == 0 ? c : c + 8;
-        const int ex = E - 2 * e;
-        bq[2 * kk + e] = hq2 < G ? pack_h2(ldexpf(S.qraw[hq2][clo], ex), ldexpf(S.qraw[hq2][chi], ex)) : 0u;
-      }
-    // negated copies for the exact hi/lo split (g <= 4: lo columns only)
-    __syncwarp();
-    uint32_t* nb = reinterpret_cast<uint32_t*>(&S.bqn[w][0][0]);
-#pragma unroll
-    for (int x = 0; x < 16; ++x)
-      nb[((x >> 2) * 32 + lane) * 4 + (x & 3)] = (!kComb || is_lo) ? (bq[x] ^ 0x80008000u) : 0u;
-    __syncwarp();
-  } else {
-    const int n = kComb ? (r & 3) : r;   // g <= 4: columns 4..7 repeat heads 0..3
-    const int E = S.eh4[n];
-#pragma unroll
-    for (int gr = 0; gr < 4; ++gr)
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        // nibbles (2hf, 2hf+4) at bit 6; nibbles (2hf+1, 2hf+5) at bit 4 for
-        // hf = 0 (factor 2^2), at bit 6 for hf = 1
-        const int c0 = 32 * gr + 8 * i + 2 * hf, c1 = c0 + 1;
-        const int e1 = hf == 0 ? E + 2 : E;
-        bq[4 * gr + 2 * hf] = n < G ? pack_h2(ldexpf(S.qraw[n][c0], E), ldexpf(S.qraw[n][c0 + 4], E)) : 0u;
-        bq[4 * gr + 2 * hf + 1] =
-            n < G ? pack_h2(ldexpf(S.qraw[n][c1], e1), ldexpf(S.qraw[n][c1 + 4], e1)) : 0u;
-      }
-  }
+__device__ __forceinline__ uint32_t frag_q2(const CtaSmem& S, int L, int x) {
+  const int r = L >> 2, i = L & 3;
+  const int h = Cols<G>::kPair ? (r >> 1) : r;
+  if (h >= G) return 0u;
+  const int kk = x >> 1, e = x & 1, jj = kk & 3, wi = kk >> 2;
+  const int j = e ? i2_reg8(jj) : i2_reg6(jj);
+  const int c = 4 * (8 * i + 4 * wi + (j >> 2)) + (j & 3);
+  const int clo = j == 0 ? c + 8 : c, chi = j == 0 ? c : c + 8;
+  const int ex = S.eh2[h] - 2 * e;
+  return pack_h2(ldexpf(S.qraw[h][clo], ex), ldexpf(S.qraw[h][chi], ex));
+}
+// INT4 K word x = 4 gr + 2 hf + e of lane L: nibbles (2hf + e, 2hf + e + 4)
+// of group gr's words; the bit-4 field (hf = 0, e = 1) carries 2^2.  With
+// paired columns, column 2h + part holds the groups of parity part.
+template <int G>
+__device__ __forceinline__ uint32_t frag_q4(const CtaSmem& S, int L, int x) {
+  const int r = L >> 2, i = L & 3;
+  const int gr = x >> 2, hf = (x >> 1) & 1, e = x & 1;
+  if (Cols<G>::kPair && (gr & 1) != (r & 1)) return 0u;
+  const int h = Cols<G>::kPair ? (r >> 1) : r;
+  if (h >= G) return 0u;
+  const int c = 32 * gr + 8 * i + 2 * hf + e;
+  const int ex = S.eh4[h] + ((hf == 0 && e == 1) ? 2 : 0);
+  return pack_h2(ldexpf(S.qraw[h][c], ex), ldexpf(S.qraw[h][c + 4], ex));
 }
 
 // Persistent scan: CTA b owns segments [cta_split[b], cta_split[b+1]), each a
 // page range of one unit; the ranges are cut so every CTA gets about the same
-// cost.  Pages of either precision may share a segment: precision is uniform
-// per page, and a warp rebuilds its q fragments when it changes.
+// cost.  Pages of either precision may share a segment (precision is uniform
+// per page; the q fragments of both are built in the segment prologue).
 template <int G>
 __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(
     const uint8_t* __restrict__ pool, size_t int4_off, int64_t n2, int hkv, int max_pages,
     const Entry* __restrict__ table, const __nv_bfloat16* __restrict__ q, int hq, float scale_log2,
     const Unit* __restrict__ units, const Split* __restrict__ splits, const int32_t* __restrict__ cta_split,
     float* __restrict__ part, const uint32_t* __restrict__ smax_bits, uint32_t* __restrict__ status) {
-  constexpr bool kComb = G <= 4;
+  constexpr bool kPair = Cols<G>::kPair;
+  constexpr int NH = Cols<G>::NH;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   CtaSmem& S = *reinterpret_cast<CtaSmem*>(smem_raw);
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, r = lane >> 2, i = lane & 3;
@@ -541,7 +592,6 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(
   const float vmax = fmaxf(__uint_as_float(smax_bits[1]), 1.0f / 1024.0f);
   const int sv = max(0, min(15, ilogbf(32768.0f / vmax)));
   const float pscale = ldexpf(1.0f, sv);
-  const bool is_lo = kComb && r >= 4;
   uint32_t cnt = 0;   // bulk loads this warp has issued so far (all consumed at segment ends)
   const int seg_end = cta_split[blockIdx.x + 1];
   for (int sg = cta_split[blockIdx.x]; sg < seg_end; ++sg) {
@@ -549,7 +599,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(
     const Unit u = units[sp.unit];
     __syncthreads();   // the previous segment's merge has finished reading shared memory
 
-    // ---- unit prologue: q of the packed heads, per-head power-of-two scale, constants
+    // ---- unit prologue: q of the packed heads, per-head power-of-two scales, fragments
     for (int x = tid; x < 8 * kHeadDim; x += kThreads) {
       const int h = x >> 7, c = x & (kHeadDim - 1);
       S.qraw[h][c] = h < G ? __bfloat162float(q[((size_t)u.b * hq + (size_t)u.kvh * G + h) * kHeadDim + c]) : 0.0f;
@@ -600,17 +650,38 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(
       if (lane == 0) S.qzs[h] = ldexpf(scale_log2, -Ez);
     }
     __syncthreads();
-    // g <= 4: lanes i and i ^ 2 carry the same two heads (columns 4..7 repeat
-    // heads 0..3 for INT4 K; the hi/lo columns are summed for INT2 K)
-    const int hp2 = kComb ? 2 * (i & 1) : 2 * i;
-    const int hz = kComb ? (r & 3) : r;
-    uint32_t bz[2] = {0u, 0u};
-    if (hz < G && i < 2) {
-      bz[0] = S.bz[hz][2 * i];
-      bz[1] = S.bz[hz][2 * i + 1];
+    {
+      // q fragments of every lane: [x >> 2][lane][x & 3] for word x = 0..15
+      uint32_t* f2 = reinterpret_cast<uint32_t*>(&S.bq2[0][0]);
+      uint32_t* fn = reinterpret_cast<uint32_t*>(&S.bqn[0][0]);
+      uint32_t* f4 = reinterpret_cast<uint32_t*>(&S.bq4[0][0]);
+      for (int y = tid; y < 16 * 32; y += kThreads) {
+        const int x = 4 * (y >> 7) + (y & 3), L = (y >> 2) & 31;
+        const uint32_t v2 = frag_q2<G>(S, L, x);
+        f2[y] = v2;
+        // negated copy for the exact hi/lo split (g <= 4: lo columns only)
+        fn[y] = (!kPair || ((L >> 2) & 1)) ? (v2 ^ 0x80008000u) : 0u;
+        f4[y] = frag_q4<G>(S, L, x);
+      }
     }
-    const float acol2[2] = {S.acol2[hp2], S.acol2[hp2 + 1]};
-    const float acol4[2] = {S.acol4[hp2], S.acol4[hp2 + 1]};
+    __syncthreads();
+    uint32_t bz[2] = {0u, 0u};
+    {
+      // INT4 K zero term B fragment: column r; with paired columns only the
+      // even columns (part 0) carry Q
+      const int hb = kPair ? (r >> 1) : r;
+      if (hb < G && i < 2 && (!kPair || !(r & 1))) {
+        bz[0] = S.bz[hb][2 * i];
+        bz[1] = S.bz[hb][2 * i + 1];
+      }
+    }
+    float acol2[NH], acol4[NH];
+#pragma unroll
+    for (int hh = 0; hh < NH; ++hh) {
+      const int h = kPair ? i : 2 * i + hh;
+      acol2[hh] = S.acol2[h];
+      acol4[hh] = S.acol4[h];
+    }
 
     // ---- page loop: two-stage bulk-copy ring per warp
     const Entry* tab = table + (size_t)u.req * max_pages;
@@ -639,11 +710,14 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // stages were read/written generically
       for (int k = 0; k < kStages && k < nw; ++k) issue(k);
     }
-    float o[8][4], zv[4] = {0.0f, 0.0f, 0.0f, 0.0f}, mrun[2] = {-INFINITY, -INFINITY}, lsum[2] = {0.0f, 0.0f};
+    float o[8][4], zv[4] = {0.0f, 0.0f, 0.0f, 0.0f}, mrun[NH], lsum[NH];
+#pragma unroll
+    for (int hh = 0; hh < NH; ++hh) {
+      mrun[hh] = -INFINITY;
+      lsum[hh] = 0.0f;
+    }
 #pragma unroll
     for (int m = 0; m < 8; ++m) o[m][0] = o[m][1] = o[m][2] = o[m][3] = 0.0f;
-    uint32_t bq[16];
-    int cur = -1;                      // precision the bq fragments were built for
     int k = 0;
     bool ok = true;
     for (; k < nw; ++k) {
@@ -652,19 +726,14 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(
       const bool got = bar_wait(&WS.bar[st], (c / kStages) & 1u);
       if (!__all_sync(0xFFFFFFFFu, got)) { ok = false; break; }
       const Entry e = ent_get(st);
-      const bool i2 = e.id < n2;
-      if ((int)i2 != cur) {
-        build_bq<G>(S, i2, w, is_lo, bq);
-        cur = (int)i2;
-      }
       const uint8_t* blk = WS.stage[st];
-      float lg[2][4];
-      if (i2) {
-        qk_int2<G>(blk, bq, &S.bqn[w][0][0], acol2, S, lg);
-        softmax_pv<G, true>(blk, e.live, r, i, is_lo, pscale, lg, o, zv, mrun, lsum, WS.pbuf);
+      float lg[2][2][NH];
+      if (e.id < n2) {
+        qk_int2<G>(blk, &S.bq2[0][0], &S.bqn[0][0], acol2, S, lg);
+        softmax_pv<G, true>(blk, e.live, pscale, lg, o, zv, mrun, lsum, WS.pbuf);
       } else {
-        qk_int4<G>(blk, bq, bz, acol4, lg);
-        softmax_pv<G, false>(blk, e.live, r, i, is_lo, pscale, lg, o, zv, mrun, lsum, WS.pbuf);
+        qk_int4<G>(blk, &S.bq4[0][0], bz, acol4, lg);
+        softmax_pv<G, false>(blk, e.live, pscale, lg, o, zv, mrun, lsum, WS.pbuf);
       }
       if (k + kStages < nw) {
         ent_set(st, tab[sp.page_begin + w + (k + kStages) * kWarps]);
@@ -681,42 +750,49 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(
         const uint32_t c = cnt + (uint32_t)kk;
         bar_wait(&WS.bar[c & (kStages - 1)], (c / kStages) & 1u);
       }
-      mrun[0] = mrun[1] = -INFINITY;
+#pragma unroll
+      for (int hh = 0; hh < NH; ++hh) mrun[hh] = -INFINITY;
     }
     cnt += (uint32_t)nw;
 
-    // ---- per-warp epilogue: finish l, combine hi/lo columns, add the V zero term
+    // ---- per-warp epilogue: finish l, combine the column parts, add the V zero term
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
+    for (int hh = 0; hh < NH; ++hh) {
       lsum[hh] += __shfl_xor_sync(0xFFFFFFFFu, lsum[hh], 4);
       lsum[hh] += __shfl_xor_sync(0xFFFFFFFFu, lsum[hh], 8);
       lsum[hh] += __shfl_xor_sync(0xFFFFFFFFu, lsum[hh], 16);
     }
-    if (kComb) {
-#pragma unroll
-      for (int m = 0; m < 8; ++m)
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) o[m][cc] += __shfl_xor_sync(0xFFFFFFFFu, o[m][cc], 2);
-    }
     if (r < 4) {
-      S.zv[w][r][2 * i] = zv[0];
-      S.zv[w][r][2 * i + 1] = zv[1];
+      if (kPair) {
+        S.zv[w][r][i] = zv[0] + zv[1];
+      } else {
+        S.zv[w][r][2 * i] = zv[0];
+        S.zv[w][r][2 * i + 1] = zv[1];
+      }
     }
     __syncwarp();
     float* accw = reinterpret_cast<float*>(WS.stage[0]);   // [8][128], the ring is idle now
-    const bool valid = !kComb || i < 2;
     const float oscale = ldexpf(1.0f, -sv);
-    if (valid) {
+    if constexpr (kPair) {
+      if (i < G) {
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+          const float zt = S.zv[w][m >> 1][i];
+          accw[i * kHeadDim + 16 * m + r] = fmaf(o[m][0] + o[m][1], kCodeUnit, zt) * oscale;
+          accw[i * kHeadDim + 16 * m + r + 8] = fmaf(o[m][2] + o[m][3], kCodeUnit, zt) * oscale;
+        }
+        if (r == 0) {
+          S.mw[w][i] = mrun[0];
+          S.lw[w][i] = lsum[0];
+        }
+      }
+    } else {
 #pragma unroll
       for (int m = 0; m < 8; ++m)
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
           const int h = 2 * i + (cc & 1), ch = 16 * m + r + 8 * (cc >> 1);
-          if (h < G) {
-            float zt = S.zv[w][m >> 1][h];
-            if (kComb) zt += S.zv[w][m >> 1][h + 4];
-            accw[h * kHeadDim + ch] = fmaf(o[m][cc], kCodeUnit, zt) * oscale;
-          }
+          if (h < G) accw[h * kHeadDim + ch] = fmaf(o[m][cc], kCodeUnit, S.zv[w][m >> 1][h]) * oscale;
         }
       if (r == 0)
 #pragma unroll
