@@ -34,7 +34,7 @@
 //    of the subnormal range (the pool tracks the largest INT2 K and V scales).
 // Pages stream through a two-stage per-warp ring filled by cp.async.bulk with
 // mbarrier completion; every wait is bounded and reports a timeout status.
-// 3 CTAs of 4 warps per SM.
+// 4 CTAs of 4 warps per SM (128 registers per thread).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -45,6 +45,7 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr int kThreads = 32 * kWarps;
+constexpr int kCtasPerSm = 4;          // resident CTAs the register budget is sized for
 constexpr int kStages = 2;
 constexpr int kStageBytes = kInt4Block;
 constexpr int kPartStride = kHeadDim + 4;
@@ -58,13 +59,15 @@ constexpr float kCodeUnit = 262144.0f;  // 2^18: a field at bit 6 is code * 2^-1
 
 struct WarpSmem {
   uint8_t stage[kStages][kStageBytes];
-  float pbuf[8][kPage];                // P staging [head][slot]
   unsigned long long bar[kStages];
 };
 
 struct CtaSmem {
   WarpSmem warp[kWarps];
-  float qraw[8][kHeadDim];             // q (fp32) of the packed heads
+  union {
+    float qraw[8][kHeadDim];           // q (fp32) of the packed heads: segment prologue only
+    float pbuf[kWarps][8][kPage];      // P staging per warp [head][slot]: page loop only
+  };
   uint32_t qzh[8][kHeadDim / 2];       // 2^Ez q as binary16 pairs in the INT2 K scale/zero pair order
   float qzs[8];                        // 2^(-Ez) * scale * log2(e)
   uint4 bq2[4][32], bqn[4][32];        // INT2 K q fragments [word / 4][lane], negated copies (lo columns)
@@ -314,14 +317,16 @@ __device__ __forceinline__ void qk_int2(const uint8_t* blk, const uint4* bq2, co
     hz = r & 3;
     const uint4* zs = reinterpret_cast<const uint4*>(blk + kI2KMeta + 256 + 64 * i + 32 * wi);
     const uint4* qs = reinterpret_cast<const uint4*>(&S.qzh[hz][(i * 2 + wi) * 8]);
+    float zq[4] = {0.0f, 0.0f, 0.0f, 0.0f};   // independent partial sums
 #pragma unroll
     for (int x4 = 0; x4 < 2; ++x4) {
       const uint4 zz = zs[x4], qz = qs[x4];
-      zp = fma2_f16_f32(zz.x, qz.x, zp);
-      zp = fma2_f16_f32(zz.y, qz.y, zp);
-      zp = fma2_f16_f32(zz.z, qz.z, zp);
-      zp = fma2_f16_f32(zz.w, qz.w, zp);
+      zq[0] = fma2_f16_f32(zz.x, qz.x, zq[0]);
+      zq[1] = fma2_f16_f32(zz.y, qz.y, zq[1]);
+      zq[2] = fma2_f16_f32(zz.z, qz.z, zq[2]);
+      zq[3] = fma2_f16_f32(zz.w, qz.w, zq[3]);
     }
+    zp = (zq[0] + zq[1]) + (zq[2] + zq[3]);
     zp += __shfl_xor_sync(0xFFFFFFFFu, zp, 1);
     zp += __shfl_xor_sync(0xFFFFFFFFu, zp, 2);
     zp += __shfl_xor_sync(0xFFFFFFFFu, zp, 16);
@@ -329,14 +334,16 @@ __device__ __forceinline__ void qk_int2(const uint8_t* blk, const uint4* bq2, co
     hz = r;
     const uint4* zs = reinterpret_cast<const uint4*>(blk + kI2KMeta + 256 + 64 * i);
     const uint4* qs = reinterpret_cast<const uint4*>(&S.qzh[hz][i * 16]);
+    float zq[4] = {0.0f, 0.0f, 0.0f, 0.0f};   // independent partial sums
 #pragma unroll
     for (int x4 = 0; x4 < 4; ++x4) {
       const uint4 zz = zs[x4], qz = qs[x4];
-      zp = fma2_f16_f32(zz.x, qz.x, zp);
-      zp = fma2_f16_f32(zz.y, qz.y, zp);
-      zp = fma2_f16_f32(zz.z, qz.z, zp);
-      zp = fma2_f16_f32(zz.w, qz.w, zp);
+      zq[0] = fma2_f16_f32(zz.x, qz.x, zq[0]);
+      zq[1] = fma2_f16_f32(zz.y, qz.y, zq[1]);
+      zq[2] = fma2_f16_f32(zz.z, qz.z, zq[2]);
+      zq[3] = fma2_f16_f32(zz.w, qz.w, zq[3]);
     }
+    zp = (zq[0] + zq[1]) + (zq[2] + zq[3]);
     zp += __shfl_xor_sync(0xFFFFFFFFu, zp, 1);
     zp += __shfl_xor_sync(0xFFFFFFFFu, zp, 2);
   }
@@ -571,7 +578,7 @@ __device__ __forceinline__ uint32_t frag_q4(const CtaSmem& S, int L, int x) {
 // cost.  Pages of either precision may share a segment (precision is uniform
 // per page; the q fragments of both are built in the segment prologue).
 template <int G>
-__global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_mma_kernel(
     const uint8_t* __restrict__ pool, size_t int4_off, int64_t n2, int hkv, int max_pages,
     const Entry* __restrict__ table, const __nv_bfloat16* __restrict__ q, int hq, float scale_log2,
     const Unit* __restrict__ units, const Split* __restrict__ splits, const int32_t* __restrict__ cta_split,
@@ -687,28 +694,23 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(
     const Entry* tab = table + (size_t)u.req * max_pages;
     const int npg = sp.page_end - sp.page_begin;
     const int nw = npg > w ? (npg - w + kWarps - 1) / kWarps : 0;
-    // Table entries of the pages in flight, loaded when their copy is issued
-    // (all lanes load the same 8 bytes), so the per-page read is not exposed.
-    static_assert(kStages == 2, "the entry ring below holds two entries");
-    Entry ent0 = Entry{0, 0u}, ent1 = Entry{0, 0u};    // registers, not an indexed (local-memory) array
-    auto ent_get = [&](uint32_t st) { return st ? ent1 : ent0; };
-    auto ent_set = [&](uint32_t st, Entry v) {
-      if (st) ent1 = v; else ent0 = v;
-    };
-    auto issue = [&](int k) {
-      const int32_t id = ent_get((cnt + (uint32_t)k) & (kStages - 1)).id;
-      const bool i2 = id < n2;
-      const uint8_t* src = i2 ? pool + ((size_t)id * hkv + u.kvh) * kInt2Block
-                              : pool + int4_off + ((size_t)(id - n2) * hkv + u.kvh) * kInt4Block;
+    // Table entries of this warp's pages k, k+1, k+2 (all lanes hold the same
+    // 8 bytes): page k+2's copy is issued after page k is consumed, and the
+    // entry of page k+3 is read then, a page's compute ahead of its use.
+    static_assert(kStages == 2, "the entry ring below serves a two-stage copy ring");
+    auto ent_load = [&](int k) { return k < nw ? tab[sp.page_begin + w + k * kWarps] : Entry{0, 0u}; };
+    Entry ent0 = ent_load(0), ent1 = ent_load(1), ent2 = ent_load(2);   // registers, rotated per page
+    auto issue = [&](int k, const Entry& en) {
+      const bool i2 = en.id < n2;
+      const uint8_t* src = i2 ? pool + ((size_t)en.id * hkv + u.kvh) * kInt2Block
+                              : pool + int4_off + ((size_t)(en.id - n2) * hkv + u.kvh) * kInt4Block;
       const uint32_t st = (cnt + (uint32_t)k) & (kStages - 1);
       bulk_load(WS.stage[st], src, i2 ? (uint32_t)kInt2Block : (uint32_t)kInt4Block, &WS.bar[st]);
     };
-#pragma unroll
-    for (int k = 0; k < kStages; ++k)
-      if (k < nw) ent_set((cnt + (uint32_t)k) & (kStages - 1), tab[sp.page_begin + w + k * kWarps]);
     if (lane == 0) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // stages were read/written generically
-      for (int k = 0; k < kStages && k < nw; ++k) issue(k);
+      if (nw > 0) issue(0, ent0);
+      if (nw > 1) issue(1, ent1);
     }
     float o[8][4], zv[4] = {0.0f, 0.0f, 0.0f, 0.0f}, mrun[NH], lsum[NH];
 #pragma unroll
@@ -725,23 +727,23 @@ __global__ void __launch_bounds__(kThreads, 3) decode_mma_kernel(
       const uint32_t st = c & (kStages - 1);
       const bool got = bar_wait(&WS.bar[st], (c / kStages) & 1u);
       if (!__all_sync(0xFFFFFFFFu, got)) { ok = false; break; }
-      const Entry e = ent_get(st);
+      const Entry e = ent0;
       const uint8_t* blk = WS.stage[st];
       float lg[2][2][NH];
       if (e.id < n2) {
         qk_int2<G>(blk, &S.bq2[0][0], &S.bqn[0][0], acol2, S, lg);
-        softmax_pv<G, true>(blk, e.live, pscale, lg, o, zv, mrun, lsum, WS.pbuf);
+        softmax_pv<G, true>(blk, e.live, pscale, lg, o, zv, mrun, lsum, S.pbuf[w]);
       } else {
         qk_int4<G>(blk, &S.bq4[0][0], bz, acol4, lg);
-        softmax_pv<G, false>(blk, e.live, pscale, lg, o, zv, mrun, lsum, WS.pbuf);
+        softmax_pv<G, false>(blk, e.live, pscale, lg, o, zv, mrun, lsum, S.pbuf[w]);
       }
-      if (k + kStages < nw) {
-        ent_set(st, tab[sp.page_begin + w + (k + kStages) * kWarps]);
-        if (lane == 0) {
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          issue(k + kStages);
-        }
+      if (k + kStages < nw && lane == 0) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        issue(k + kStages, ent2);
       }
+      ent0 = ent1;
+      ent1 = ent2;
+      ent2 = ent_load(k + 3);
     }
     if (!ok) {
       if (lane == 0) atomicOr(status, kStatusTimeout);
