@@ -91,18 +91,36 @@ def _check(rc, what):
 
 
 def _np(a, dtype):
+    if type(a) is np.ndarray and a.dtype == dtype and a.flags.c_contiguous:
+        return a
     return np.ascontiguousarray(np.asarray(a), dtype=dtype)
 
 
 def _ptr(a):
-    return None if a is None else ctypes.c_void_p(a.ctypes.data)
+    return None if a is None else a.ctypes.data
 
 
-def _stream(stream):
-    import torch
-    if stream is None:
-        stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream)
+_torch = None
+_raw_stream = None
+
+
+def _torch_mod():
+    global _torch, _raw_stream
+    if _torch is None:
+        import torch
+        _raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        _torch = torch
+    return _torch
+
+
+def _stream(stream, device):
+    """cudaStream_t (as an int) of `stream`, or of torch's current stream on `device`."""
+    if stream is not None:
+        return stream.cuda_stream
+    torch = _torch_mod()
+    if _raw_stream is not None:
+        return _raw_stream(device)
+    return torch.cuda.current_stream(device).cuda_stream
 
 
 def alloc_bits(N, D2, D4, budget):
@@ -126,6 +144,7 @@ class KVPool:
         h = _P()
         _check(L.kv_pool_create(ctypes.byref(cfg), ctypes.byref(h)), "kv_pool_create")
         self._h = h
+        self._L = L
         self.num_kv_heads = num_kv_heads
         self.n_int2_pages = n_int2_pages
         self.device = device
@@ -163,20 +182,22 @@ class KVPool:
         if n:
             self._check_kv(k, n)
             self._check_kv(v, n)
-        _check(load_library().kv_append_quant(self._h, ctypes.c_void_p(k.data_ptr() if n else 0),
-                                              ctypes.c_void_p(v.data_ptr() if n else 0), _ptr(req_ids), _ptr(bits),
-                                              n, _stream(stream)), "kv_append_quant")
+        rc = self._L.kv_append_quant(self._h, k.data_ptr() if n else None, v.data_ptr() if n else None,
+                                     req_ids.ctypes.data, bits.ctypes.data, n, _stream(stream, self.device))
+        if rc:
+            _check(rc, "kv_append_quant")
 
     def _check_kv(self, t, n):
-        import torch
-        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or \
-                tuple(t.shape) != (n, self.num_kv_heads, HEAD_DIM):
+        torch = _torch_mod()
+        if t.dtype is not torch.bfloat16 or not t.is_cuda or t.shape != (n, self.num_kv_heads, HEAD_DIM) or \
+                not t.is_contiguous():
             raise ValueError(f"expected a contiguous CUDA bf16 tensor [{n}][{self.num_kv_heads}][128]")
 
     def reorder(self, req_ids, stream=None):
         req_ids = _np(req_ids, np.int32)
-        _check(load_library().kv_reorder_pages(self._h, _ptr(req_ids), req_ids.size, _stream(stream)),
-               "kv_reorder_pages")
+        rc = self._L.kv_reorder_pages(self._h, req_ids.ctypes.data, req_ids.size, _stream(stream, self.device))
+        if rc:
+            _check(rc, "kv_reorder_pages")
 
     def evict(self, req_ids, token_pos, stream=None):
         req_ids = _np(req_ids, np.int32)
@@ -184,22 +205,24 @@ class KVPool:
         if req_ids.size != token_pos.size:
             raise ValueError("req_ids and token_pos differ in length")
         _check(load_library().kv_evict_slots(self._h, _ptr(req_ids), _ptr(token_pos), req_ids.size,
-                                             _stream(stream)), "kv_evict_slots")
+                                             _stream(stream, self.device)), "kv_evict_slots")
 
     def decode(self, q, req_ids, softmax_scale, out=None, stream=None):
         """q: torch bf16 CUDA [B][Hq][128] -> out fp32 [B][Hq][128]."""
-        import torch
+        torch = _torch_mod()
         req_ids = _np(req_ids, np.int32)
         B, Hq, D = q.shape
-        if q.dtype != torch.bfloat16 or not q.is_cuda or not q.is_contiguous() or D != HEAD_DIM or B != req_ids.size:
+        if q.dtype is not torch.bfloat16 or not q.is_cuda or D != HEAD_DIM or B != req_ids.size or \
+                not q.is_contiguous():
             raise ValueError("q must be a contiguous CUDA bf16 tensor [B][Hq][128] with B == len(req_ids)")
         if out is None:
             out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
-        elif out.dtype != torch.float32 or not out.is_contiguous() or tuple(out.shape) != (B, Hq, D):
-            raise ValueError("out must be a contiguous fp32 tensor shaped like q")
-        _check(load_library().kv_decode_attn(self._h, ctypes.c_void_p(q.data_ptr()), _ptr(req_ids), B, Hq,
-                                             float(softmax_scale), ctypes.c_void_p(out.data_ptr()),
-                                             _stream(stream)), "kv_decode_attn")
+        elif out.dtype is not torch.float32 or out.shape != q.shape or not out.is_cuda or not out.is_contiguous():
+            raise ValueError("out must be a contiguous fp32 CUDA tensor shaped like q")
+        rc = self._L.kv_decode_attn(self._h, q.data_ptr(), req_ids.ctypes.data, B, Hq, softmax_scale,
+                                    out.data_ptr(), _stream(stream, self.device))
+        if rc:
+            _check(rc, "kv_decode_attn")
         return out
 
     def decode_noalloc(self, q, req_ids, softmax_scale, out, stream=None):
@@ -214,7 +237,7 @@ class KVPool:
             raise ValueError("out must be a contiguous fp32 tensor shaped like q")
         _check(load_library().kv_decode_attn_noalloc(self._h, ctypes.c_void_p(q.data_ptr()), _ptr(req_ids), B, Hq,
                                                      float(softmax_scale), ctypes.c_void_p(out.data_ptr()),
-                                                     _stream(stream)), "kv_decode_attn_noalloc")
+                                                     _stream(stream, self.device)), "kv_decode_attn_noalloc")
         return out
 
     def set_decode_impl(self, impl):
