@@ -582,7 +582,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_mma_kernel(
     const uint8_t* __restrict__ pool, size_t int4_off, int64_t n2, int hkv, int max_pages,
     const Entry* __restrict__ table, const __nv_bfloat16* __restrict__ q, int hq, float scale_log2,
     const Unit* __restrict__ units, const Split* __restrict__ splits, const int32_t* __restrict__ cta_split,
-    float* __restrict__ part, const uint32_t* __restrict__ smax_bits, uint32_t* __restrict__ status) {
+    const int32_t* __restrict__ ntab, float* __restrict__ part, const uint32_t* __restrict__ smax_bits,
+    uint32_t* __restrict__ status) {
   constexpr bool kPair = Cols<G>::kPair;
   constexpr int NH = Cols<G>::NH;
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -692,7 +693,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_mma_kernel(
 
     // ---- page loop: two-stage bulk-copy ring per warp
     const Entry* tab = table + (size_t)u.req * max_pages;
-    const int npg = sp.page_end - sp.page_begin;
+    const int npg = (sp.page_end >= 0 ? sp.page_end : ntab[u.req]) - sp.page_begin;
     const int nw = npg > w ? (npg - w + kWarps - 1) / kWarps : 0;
     // Table entries of this warp's pages k, k+1, k+2 (all lanes hold the same
     // 8 bytes): page k+2's copy is issued after page k is consumed, and the
@@ -847,7 +848,8 @@ cudaError_t launch_mma_g(kv_pool* P, const void* q, int32_t hq, float scale_log2
   ++P->launches;
   decode_mma_kernel<G><<<n_ctas, kThreads, sizeof(CtaSmem), s>>>(
       P->d_pool, P->int4_offset, P->cfg.n_int2_pages, P->cfg.num_kv_heads, P->cfg.max_pages_per_request, P->d_table,
-      (const __nv_bfloat16*)q, hq, scale_log2, d_units, d_splits, d_cta, d_part, P->d_status + 1, P->d_status);
+      (const __nv_bfloat16*)q, hq, scale_log2, d_units, d_splits, d_cta, P->d_ntab, d_part, P->d_status + 1,
+      P->d_status);
   return cudaGetLastError();
 }
 

@@ -43,7 +43,7 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(
     const uint8_t* __restrict__ pool, size_t int4_off, int64_t n2, int hkv, int max_pages,
     const Entry* __restrict__ table, const __nv_bfloat16* __restrict__ q, int hq, float scale_log2,
     const Unit* __restrict__ units, const Split* __restrict__ splits, const int32_t* __restrict__ cta_split,
-    float* __restrict__ part) {
+    const int32_t* __restrict__ ntab, float* __restrict__ part) {
   __shared__ float qs[G][kHeadDim];
   __shared__ __align__(16) uint8_t buf[kWarps][kInt4Block];
   __shared__ float pb[kWarps][kPage][G];
@@ -53,6 +53,7 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(
   __syncthreads();
   const Split sp = splits[sg];
   const Unit u = units[sp.unit];
+  const int page_end = sp.page_end >= 0 ? sp.page_end : ntab[u.req];
   for (int i = threadIdx.x; i < G * kHeadDim; i += kThreads) {
     const int h = i / kHeadDim, c = i % kHeadDim;
     qs[h][c] = __bfloat162float(q[((size_t)u.b * hq + (size_t)u.kvh * G + h) * kHeadDim + c]);
@@ -70,7 +71,7 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(
   }
   const Entry* tab = table + (size_t)u.req * max_pages;
   uint8_t* bw = buf[w];
-  for (int pi = sp.page_begin + w; pi < sp.page_end; pi += kWarps) {
+  for (int pi = sp.page_begin + w; pi < page_end; pi += kWarps) {
     const Entry e = tab[pi];
     const bool i2 = e.id < n2;
     const uint8_t* blk = i2 ? pool + ((size_t)e.id * hkv + u.kvh) * kInt2Block
@@ -195,7 +196,8 @@ __global__ void merge_kernel(const Unit* __restrict__ units, const float* __rest
     const int s = s0 + lane;
     float f = 0.0f;
     if (s < n) {
-      f = exp2f(base[s * rs + kHeadDim] - M);
+      const float m = base[s * rs + kHeadDim];
+      f = m == -INFINITY ? 0.0f : exp2f(m - M);   // an empty split adds nothing
       L += f * base[s * rs + kHeadDim + 1];
     }
     const int cnt = min(32, n - s0);
@@ -220,7 +222,7 @@ cudaError_t launch_g(kv_pool* P, const void* q, int32_t hq, float scale_log2, co
     ++P->launches;
     decode_simt_kernel<G><<<n_ctas, kThreads, 0, s>>>(
         P->d_pool, P->int4_offset, P->cfg.n_int2_pages, P->cfg.num_kv_heads, P->cfg.max_pages_per_request,
-        P->d_table, (const __nv_bfloat16*)q, hq, scale_log2, d_units, d_splits, d_cta, d_part);
+        P->d_table, (const __nv_bfloat16*)q, hq, scale_log2, d_units, d_splits, d_cta, P->d_ntab, d_part);
   }
   if (P->merge_event) {
     const cudaError_t e = cudaEventRecord(P->merge_event, s);

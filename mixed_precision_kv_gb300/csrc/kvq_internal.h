@@ -34,9 +34,20 @@ struct TableUpd {
 // Append job: one destination page and the tokens written into it this call.
 struct AppendJob {
   int32_t page;        // INT4 page id (absolute)
-  int32_t first_slot;  // slot of the first token of this job
+  int32_t first_slot;  // slot of the first token of this job (0: the page is new, its block starts from zeros)
   int32_t n_slots;     // tokens written by this job
   int32_t tok_off;     // offset into the token index list
+  int32_t tab_index;   // flat index of the page's table entry after the call (-1: not in a table)
+  uint32_t live;       // the page's live mask after the call
+  int32_t ntab_req;    // request whose table length to set (-1: none)
+  int32_t ntab_len;    // that length
+};
+
+// The jobs of a small append call, passed to the kernel by value (no copy).
+struct SmallAppend {
+  static constexpr int kMaxJobs = 32, kMaxToks = 128;
+  AppendJob jobs[kMaxJobs];
+  int32_t toks[kMaxToks];
 };
 
 struct RepackJob {
@@ -60,7 +71,7 @@ struct Unit {
 struct Split {
   int32_t unit;
   int32_t page_begin;   // table index range [page_begin, page_end)
-  int32_t page_end;
+  int32_t page_end;     // < 0: to the end of the request's table (its device length at launch)
   int32_t cta;
 };
 
@@ -122,7 +133,8 @@ struct kv_pool {
   std::set<int32_t> free2, free4;
   // decode plan cache
   std::vector<int32_t> plan_req;
-  std::vector<uint64_t> plan_ver;
+  std::vector<int32_t> plan_len;      // table lengths of plan_req when the plan was built
+  int32_t plan_slack = 0;             // pages a table may grow before the plan is rebuilt
   int32_t plan_hq = 0;
   int32_t plan_impl = -1;
   int32_t n_units = 0, n_splits = 0;
@@ -146,7 +158,7 @@ void set_last_error(const char* msg);
 
 // Launchers (kvq_quant.cu)
 cudaError_t launch_append(kv_pool* P, const void* k, const void* v, const AppendJob* d_jobs, int n_jobs,
-                          const int32_t* d_toks, cudaStream_t s);
+                          const int32_t* d_toks, const SmallAppend* small, cudaStream_t s);
 cudaError_t launch_repack(kv_pool* P, const RepackJob* d_jobs, int n_jobs, cudaStream_t s);
 cudaError_t launch_scatter(kv_pool* P, const TableUpd* d_upd, int n, cudaStream_t s);
 

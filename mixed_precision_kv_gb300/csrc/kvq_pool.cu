@@ -197,6 +197,9 @@ void kvq::plan_decode(const kv_pool* P, const int32_t* req_ids, int32_t batch, i
         cum += cost(tb[i]);
       }
       u.n_splits = (int32_t)out.splits.size() - u.split_begin;
+      // the unit's last split runs to the end of the table, so pages appended
+      // after planning are scanned too (by the CTA that owns the tail)
+      if (u.n_splits > 0) out.splits.back().page_end = -1;
     }
   }
   while (cur < n) out.cta_split[++cur] = (int32_t)out.splits.size();
@@ -419,14 +422,18 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
   if (st != KV_OK) return st;
 
   std::vector<AppendJob> jobs;
+  std::vector<int32_t> job_req;                        // request of each job
+  std::vector<std::pair<int32_t, int32_t>> touched;   // (request, table length before the call)
   std::vector<RepackJob> repacks;
   std::vector<int32_t> tok_job((size_t)n_tok), tok_slot((size_t)n_tok);
   std::unordered_map<int32_t, int32_t> job_of_page;
   std::vector<int32_t> deferred;
-  Dirty dirty;
+  Dirty dirty;   // table rewrites the append kernel does not cover (repacks)
   for (int64_t t = 0; t < n_tok; ++t) {
     const int32_t r = req_ids[t];
     Request& R = P->reqs[r];
+    if (std::find_if(touched.begin(), touched.end(), [&](const auto& x) { return x.first == r; }) == touched.end())
+      touched.emplace_back(r, (int32_t)R.table.size());
     const int64_t pos = (int64_t)R.loc.size();
     int32_t& cur = (bits[t] == 4) ? R.tail4 : R.staging;
     if (cur < 0 || P->fill[cur] == kPage) {
@@ -434,18 +441,17 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
       P->fill[cur] = 0;
       P->live[cur] = 0;
       R.table.push_back(cur);
-      dirty.structural(r, (int32_t)R.table.size() - 1);
       ++R.version;
     }
     const int slot = P->fill[cur]++;
     P->live[cur] |= 1u << slot;
     P->pos[(size_t)cur * kPage + slot] = (int32_t)pos;
     R.loc.push_back(((uint32_t)cur << 5) | (uint32_t)slot);
-    dirty.live(r, cur);
     auto jt = job_of_page.find(cur);
     if (jt == job_of_page.end()) {
       jt = job_of_page.emplace(cur, (int32_t)jobs.size()).first;
-      jobs.push_back(AppendJob{cur, slot, 0, 0});
+      jobs.push_back(AppendJob{cur, slot, 0, 0, -1, 0u, -1, 0});
+      job_req.push_back(r);
     }
     ++jobs[jt->second].n_slots;
     tok_job[t] = jt->second;
@@ -482,17 +488,45 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
     P->live[id] = 0;
     P->free4.insert(id);
   }
+  // Table entries the append kernel writes: each job's page where it sits in
+  // the final table (pages added at the end or filled in place), and the
+  // final table length of every request that grew.
+  const uint32_t mp = (uint32_t)P->cfg.max_pages_per_request;
+  for (size_t j = 0; j < jobs.size(); ++j) {
+    AppendJob& J = jobs[j];
+    const int32_t r = job_req[j];
+    const auto& tb = P->reqs[r].table;
+    const auto it = std::find(tb.rbegin(), tb.rend(), J.page);   // appended pages sit near the end
+    if (it != tb.rend()) {
+      J.tab_index = (int32_t)(r * mp + (uint32_t)(tb.rend() - it - 1));
+      J.live = P->live[J.page];
+    }
+    for (const auto& x : touched)
+      if (x.first == r && (int32_t)tb.size() != x.second) {
+        J.ntab_req = r;
+        J.ntab_len = (int32_t)tb.size();
+      }
+  }
   std::vector<TableUpd> upd;
   emit_updates(P, dirty, upd);
 
+  const bool small = jobs.size() <= (size_t)SmallAppend::kMaxJobs && n_tok <= SmallAppend::kMaxToks;
   Upload u;
-  const size_t o_jobs = u.add(jobs.data(), jobs.size() * sizeof(AppendJob));
-  const size_t o_toks = u.add(toks.data(), toks.size() * sizeof(int32_t));
+  const size_t o_jobs = small ? 0 : u.add(jobs.data(), jobs.size() * sizeof(AppendJob));
+  const size_t o_toks = small ? 0 : u.add(toks.data(), toks.size() * sizeof(int32_t));
   const size_t o_rep = u.add(repacks.data(), repacks.size() * sizeof(RepackJob));
   const size_t o_upd = u.add(upd.data(), upd.size() * sizeof(TableUpd));
   if ((st = upload(P, u, s)) != KV_OK) return st;
   uint8_t* base = (uint8_t*)P->upload.ptr;
-  KV_CUDA(launch_append(P, k, v, (const AppendJob*)(base + o_jobs), (int)jobs.size(), (const int32_t*)(base + o_toks), s));
+  if (small) {
+    SmallAppend sa;
+    std::copy(jobs.begin(), jobs.end(), sa.jobs);
+    std::copy(toks.begin(), toks.end(), sa.toks);
+    KV_CUDA(launch_append(P, k, v, nullptr, (int)jobs.size(), nullptr, &sa, s));
+  } else {
+    KV_CUDA(launch_append(P, k, v, (const AppendJob*)(base + o_jobs), (int)jobs.size(), (const int32_t*)(base + o_toks),
+                          nullptr, s));
+  }
   KV_CUDA(launch_repack(P, (const RepackJob*)(base + o_rep), (int)repacks.size(), s));
   KV_CUDA(launch_scatter(P, (const TableUpd*)(base + o_upd), (int)upd.size(), s));
   return KV_OK;
@@ -632,9 +666,16 @@ namespace {
 kv_status_t build_plan(kv_pool* P, const int32_t* req_ids, int32_t batch, int32_t hq, int32_t impl,
                        cudaStream_t s) {
   const int hkv = P->cfg.num_kv_heads, g = hq / hkv;
+  // A plan stays valid while the batch is the same and no table has shrunk:
+  // splits are table index ranges and each unit's last one is open-ended.
+  // Tables that grew add their new pages to the tail CTA, so the plan is
+  // rebuilt once a table has grown past the slack (or an empty table gained
+  // pages, which has no split yet).
   bool same = P->plan_impl == impl && P->plan_hq == hq && (int32_t)P->plan_req.size() == batch;
-  for (int32_t b = 0; same && b < batch; ++b)
-    same = P->plan_req[b] == req_ids[b] && P->plan_ver[b] == P->reqs[req_ids[b]].version;
+  for (int32_t b = 0; same && b < batch; ++b) {
+    const int32_t len = (int32_t)P->reqs[req_ids[b]].table.size(), len0 = P->plan_len[b];
+    same = P->plan_req[b] == req_ids[b] && len >= len0 && len - len0 <= P->plan_slack && (len0 > 0 || len == 0);
+  }
   if (same) return KV_OK;
 
   const int ctas = impl == KV_DECODE_MMA ? decode_mma_ctas_per_sm(g) : decode_simt_ctas_per_sm(g);
@@ -655,8 +696,14 @@ kv_status_t build_plan(kv_pool* P, const int32_t* req_ids, int32_t batch, int32_
   P->n_splits = (int32_t)hp.splits.size();
   P->n_ctas = (int32_t)hp.n_ctas();
   P->plan_req.assign(req_ids, req_ids + batch);
-  P->plan_ver.resize(batch);
-  for (int32_t b = 0; b < batch; ++b) P->plan_ver[b] = P->reqs[req_ids[b]].version;
+  P->plan_len.resize(batch);
+  int64_t total_pages = 0;
+  for (int32_t b = 0; b < batch; ++b) {
+    P->plan_len[b] = (int32_t)P->reqs[req_ids[b]].table.size();
+    total_pages += (int64_t)P->plan_len[b] * hkv;
+  }
+  // growth a tail CTA absorbs before the plan is rebuilt: 5% of a CTA's share
+  P->plan_slack = (int32_t)std::max<int64_t>(1, total_pages / std::max<int64_t>(1, P->n_ctas) / 20);
   P->plan_hq = hq;
   P->plan_impl = impl;
   return KV_OK;

@@ -63,80 +63,100 @@ __device__ __forceinline__ void or_bits(uint8_t* img, int byte_off, int shift, u
   atomicOr(reinterpret_cast<uint32_t*>(img) + (byte_off >> 2), val << (8 * (byte_off & 3) + shift));
 }
 
-// One CTA per (job, kv head): builds the INT4 page image in shared memory and
-// writes the whole 5120-byte block back.  A job starting at slot 0 is the
-// page's first write, so the image starts from zeros (unfilled slots then read
-// as code 0, scale 0, zero 0); later jobs start from the stored block.
+// Quantize one token (a warp: lane = channels 4*lane .. 4*lane+3) into slot
+// `slot` of an INT4 block image `img` (shared or global memory).  V nibbles
+// are OR-ed in: the block's unfilled slots hold zeros.
+__device__ __forceinline__ bool quantize_token(uint8_t* img, const __nv_bfloat16* __restrict__ k,
+                                               const __nv_bfloat16* __restrict__ v, int t, int slot, int h, int hkv,
+                                               uint32_t* __restrict__ status) {
+  const int lane = threadIdx.x & 31, gr = lane >> 3;
+  const size_t row = ((size_t)t * hkv + h) * kHeadDim + 4 * lane;
+  const uint2 kr = *reinterpret_cast<const uint2*>(k + row);
+  const uint2 vr = *reinterpret_cast<const uint2*>(v + row);
+  float xk[4], xv[4];
+  xk[0] = __uint_as_float(kr.x << 16); xk[1] = __uint_as_float(kr.x & 0xFFFF0000u);
+  xk[2] = __uint_as_float(kr.y << 16); xk[3] = __uint_as_float(kr.y & 0xFFFF0000u);
+  xv[0] = __uint_as_float(vr.x << 16); xv[1] = __uint_as_float(vr.x & 0xFFFF0000u);
+  xv[2] = __uint_as_float(vr.y << 16); xv[3] = __uint_as_float(vr.y & 0xFFFF0000u);
+  bool bad = false;
+  float kmn = xk[0], kmx = xk[0], vmn = xv[0], vmx = xv[0];
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    bad |= out_of_range(xk[a]) | out_of_range(xv[a]);
+    kmn = fminf(kmn, xk[a]); kmx = fmaxf(kmx, xk[a]);
+    vmn = fminf(vmn, xv[a]); vmx = fmaxf(vmx, xv[a]);
+  }
+  group8_minmax(kmn, kmx);
+  group8_minmax(vmn, vmx);
+  const GroupMeta km = make_meta(kmn, kmx, 15.0f);
+  const GroupMeta vm = make_meta(vmn, vmx, 15.0f);
+  uint32_t ck[4], cv[4];
+#pragma unroll
+  for (int a = 0; a < 4; ++a) { ck[a] = qcode(xk[a], km, 15.0f); cv[a] = qcode(xv[a], vm, 15.0f); }
+  // K: channels 4*lane .. 4*lane+3 are nibbles 0..3 or 4..7 of one word -> 2 bytes
+  const int kb = i4k_byte(slot, 4 * lane);
+  *reinterpret_cast<uint16_t*>(img + kb) = (uint16_t)(ck[0] | (ck[1] << 4) | (ck[2] << 8) | (ck[3] << 12));
+  // V: channel-major, one nibble per channel
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const int c = 4 * lane + a;
+    or_bits(img, i4v_byte(slot, c), i4v_shift(slot), cv[a]);
+  }
+  {
+    // running maximum of V scales (non-negative floats order as their bits)
+    float m = vm.sf;
+    m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 8));
+    m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 16));
+    if (lane == 0) atomicMax(status + 2, __float_as_uint(m));
+  }
+  if ((lane & 7) == 0) {
+    st_half(img, kI4KMeta + 16 * slot + 4 * gr, km.s);
+    st_half(img, kI4KMeta + 16 * slot + 4 * gr + 2, km.z);
+    st_half(img, kI4VMeta + 2 * v_meta_index(slot, gr), vm.s);
+    st_half(img, kI4VMeta + 256 + 2 * v_meta_index(slot, gr), vm.z);
+  }
+  return bad;
+}
+
+// One CTA per (job, kv head), a warp per token.  A new page (job starting at
+// slot 0) is built as an image in shared memory from zeros and written whole,
+// so its unfilled slots read as code 0, scale 0, zero 0; a page that already
+// holds tokens gets only its new slots written in place (the V words by
+// atomic OR).  The kv-head-0 CTA also writes the page's table entry and the
+// request's table length, so an append that only fills or adds tail pages
+// needs no separate table update.
+template <bool kByValue>
 __global__ void __launch_bounds__(kThreads) append_int4_kernel(
     uint8_t* __restrict__ pool, size_t int4_off, int64_t n2, int hkv, const __nv_bfloat16* __restrict__ k,
     const __nv_bfloat16* __restrict__ v, const AppendJob* __restrict__ jobs, const int32_t* __restrict__ toks,
-    uint32_t* __restrict__ status) {
+    Entry* __restrict__ table, int32_t* __restrict__ ntab, uint32_t* __restrict__ status,
+    const __grid_constant__ SmallAppend small) {
   __shared__ __align__(16) uint8_t img[kInt4Block];
-  const AppendJob job = jobs[blockIdx.x];
+  const AppendJob job = kByValue ? small.jobs[blockIdx.x] : jobs[blockIdx.x];
+  const int32_t* tk = kByValue ? small.toks : toks;
   const int h = blockIdx.y;
   uint8_t* blk = pool + int4_off + ((size_t)(job.page - n2) * hkv + h) * kInt4Block;
-  uint4* img4 = reinterpret_cast<uint4*>(img);
-  const uint4* blk4 = reinterpret_cast<const uint4*>(blk);
-  for (int i = threadIdx.x; i < kInt4Block / 16; i += kThreads)
-    img4[i] = job.first_slot == 0 ? make_uint4(0, 0, 0, 0) : blk4[i];
-  __syncthreads();
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gr = lane >> 3;
+  const bool fresh = job.first_slot == 0;
+  const int warp = threadIdx.x >> 5;
   bool bad = false;
-  for (int j = warp; j < job.n_slots; j += kThreads / 32) {
-    const int t = toks[job.tok_off + j];
-    const int slot = job.first_slot + j;
-    const size_t row = ((size_t)t * hkv + h) * kHeadDim + 4 * lane;
-    const uint2 kr = *reinterpret_cast<const uint2*>(k + row);
-    const uint2 vr = *reinterpret_cast<const uint2*>(v + row);
-    float xk[4], xv[4];
-    xk[0] = __uint_as_float(kr.x << 16); xk[1] = __uint_as_float(kr.x & 0xFFFF0000u);
-    xk[2] = __uint_as_float(kr.y << 16); xk[3] = __uint_as_float(kr.y & 0xFFFF0000u);
-    xv[0] = __uint_as_float(vr.x << 16); xv[1] = __uint_as_float(vr.x & 0xFFFF0000u);
-    xv[2] = __uint_as_float(vr.y << 16); xv[3] = __uint_as_float(vr.y & 0xFFFF0000u);
-    float kmn = xk[0], kmx = xk[0], vmn = xv[0], vmx = xv[0];
-#pragma unroll
-    for (int a = 0; a < 4; ++a) {
-      bad |= out_of_range(xk[a]) | out_of_range(xv[a]);
-      kmn = fminf(kmn, xk[a]); kmx = fmaxf(kmx, xk[a]);
-      vmn = fminf(vmn, xv[a]); vmx = fmaxf(vmx, xv[a]);
-    }
-    group8_minmax(kmn, kmx);
-    group8_minmax(vmn, vmx);
-    const GroupMeta km = make_meta(kmn, kmx, 15.0f);
-    const GroupMeta vm = make_meta(vmn, vmx, 15.0f);
-    uint32_t ck[4], cv[4];
-#pragma unroll
-    for (int a = 0; a < 4; ++a) { ck[a] = qcode(xk[a], km, 15.0f); cv[a] = qcode(xv[a], vm, 15.0f); }
-    // K: channels 4*lane .. 4*lane+3 are nibbles 0..3 or 4..7 of one word -> 2 bytes
-    const int kb = i4k_byte(slot, 4 * lane);
-    *reinterpret_cast<uint16_t*>(img + kb) =
-        (uint16_t)(ck[0] | (ck[1] << 4) | (ck[2] << 8) | (ck[3] << 12));
-    // V: channel-major, one nibble per channel (the block started from zeros)
-#pragma unroll
-    for (int a = 0; a < 4; ++a) {
-      const int c = 4 * lane + a;
-      or_bits(img, i4v_byte(slot, c), i4v_shift(slot), cv[a]);
-    }
-    {
-      // running maximum of V scales (non-negative floats order as their bits)
-      float vmx = vm.sf;
-      vmx = fmaxf(vmx, __shfl_xor_sync(0xFFFFFFFFu, vmx, 8));
-      vmx = fmaxf(vmx, __shfl_xor_sync(0xFFFFFFFFu, vmx, 16));
-      if (lane == 0) atomicMax(status + 2, __float_as_uint(vmx));
-    }
-    if ((lane & 7) == 0) {
-      st_half(img, kI4KMeta + 16 * slot + 4 * gr, km.s);
-      st_half(img, kI4KMeta + 16 * slot + 4 * gr + 2, km.z);
-      st_half(img, kI4VMeta + 2 * v_meta_index(slot, gr), vm.s);
-      st_half(img, kI4VMeta + 256 + 2 * v_meta_index(slot, gr), vm.z);
-    }
+  if (fresh) {
+    uint4* img4 = reinterpret_cast<uint4*>(img);
+    for (int i = threadIdx.x; i < kInt4Block / 16; i += kThreads) img4[i] = make_uint4(0, 0, 0, 0);
+    __syncthreads();
+    for (int j = warp; j < job.n_slots; j += kThreads / 32)
+      bad |= quantize_token(img, k, v, tk[job.tok_off + j], job.first_slot + j, h, hkv, status);
+    __syncthreads();
+    uint4* out4 = reinterpret_cast<uint4*>(blk);
+    for (int i = threadIdx.x; i < kInt4Block / 16; i += kThreads) out4[i] = img4[i];
+  } else {
+    for (int j = warp; j < job.n_slots; j += kThreads / 32)
+      bad |= quantize_token(blk, k, v, tk[job.tok_off + j], job.first_slot + j, h, hkv, status);
   }
   if (bad) atomicOr(status, kStatusRange);
-  __syncthreads();
-  uint4* out4 = reinterpret_cast<uint4*>(blk);
-  for (int i = threadIdx.x; i < kInt4Block / 16; i += kThreads) out4[i] = img4[i];
+  if (h == 0 && threadIdx.x == 0) {
+    if (job.tab_index >= 0) table[job.tab_index] = Entry{job.page, job.live};
+    if (job.ntab_req >= 0) ntab[job.ntab_req] = job.ntab_len;
+  }
 }
 
 // One CTA per (repack job, kv head): INT4 staging block -> INT2 block.
@@ -228,13 +248,22 @@ __global__ void scatter_kernel(Entry* __restrict__ table, int32_t* __restrict__ 
 }  // namespace
 
 cudaError_t launch_append(kv_pool* P, const void* k, const void* v, const AppendJob* d_jobs, int n_jobs,
-                          const int32_t* d_toks, cudaStream_t s) {
+                          const int32_t* d_toks, const SmallAppend* small, cudaStream_t s) {
   if (n_jobs <= 0) return cudaSuccess;
   dim3 grid((unsigned)n_jobs, (unsigned)P->cfg.num_kv_heads);
   ++P->launches;
-  append_int4_kernel<<<grid, kThreads, 0, s>>>(P->d_pool, P->int4_offset, P->cfg.n_int2_pages,
-                                               P->cfg.num_kv_heads, (const __nv_bfloat16*)k,
-                                               (const __nv_bfloat16*)v, d_jobs, d_toks, P->d_status);
+  if (small) {
+    append_int4_kernel<true><<<grid, kThreads, 0, s>>>(P->d_pool, P->int4_offset, P->cfg.n_int2_pages,
+                                                       P->cfg.num_kv_heads, (const __nv_bfloat16*)k,
+                                                       (const __nv_bfloat16*)v, nullptr, nullptr, P->d_table,
+                                                       P->d_ntab, P->d_status, *small);
+  } else {
+    static const SmallAppend none{};
+    append_int4_kernel<false><<<grid, kThreads, 0, s>>>(P->d_pool, P->int4_offset, P->cfg.n_int2_pages,
+                                                        P->cfg.num_kv_heads, (const __nv_bfloat16*)k,
+                                                        (const __nv_bfloat16*)v, d_jobs, d_toks, P->d_table,
+                                                        P->d_ntab, P->d_status, none);
+  }
   return cudaGetLastError();
 }
 

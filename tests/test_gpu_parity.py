@@ -208,3 +208,52 @@ def test_split_counts_do_not_change_results(kvq, p2, impl):
     sc = Scenario(kvq, 1, 8, bits, chunk=4096, impl=impl)
     sc.check_decode(what=f"long p2={p2}")
     assert sc.gpu.last_decode_stats()["n_splits"] > 1
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_plan_reuse_across_growth(kvq, impl):
+    """Decode, grow the tables (an empty request gains its first pages, others
+    grow by a few pages, then by many), decode again: every call must scan
+    every page, whether the decode plan was reused or rebuilt."""
+    hkv, hq = 2, 8
+    gpu = kvq.KVPool(hkv, 64, 64, 3, 64)
+    orc = oracle.OraclePool(hkv, 64, 64, 3, 64)
+    g = [gpu.open() for _ in range(3)]
+    o = [orc.open() for _ in range(3)]
+    gpu.set_decode_impl(impl)
+    lens = [300, 40, 0]
+    pos = [0, 0, 0]
+
+    def grow(r, n, stream):
+        if n == 0:
+            return
+        bits = _mixed(n, 0.5, 100 + stream)
+        kd = torch.empty((n, hkv, 128), dtype=torch.bfloat16, device="cuda")
+        vd = torch.empty_like(kd)
+        kvsynth.fill_bf16_dev(kd.data_ptr(), n, hkv, 128, SEED, kvsynth.TENSOR_K, r, pos[r])
+        kvsynth.fill_bf16_dev(vd.data_ptr(), n, hkv, 128, SEED, kvsynth.TENSOR_V, r, pos[r])
+        kh = kvsynth.fill_bf16_host(n, hkv, 128, SEED, kvsynth.TENSOR_K, r, pos[r])
+        vh = kvsynth.fill_bf16_host(n, hkv, 128, SEED, kvsynth.TENSOR_V, r, pos[r])
+        gpu.append(kd, vd, np.full(n, g[r]), bits)
+        assert orc.append(np.full(n, o[r]), bits, kh, vh) == oracle.OK
+        pos[r] += n
+
+    def check(step, what):
+        qd = torch.empty((3, hq, 128), dtype=torch.bfloat16, device="cuda")
+        kvsynth.fill_bf16_dev(qd.data_ptr(), 3, hq, 128, SEED, kvsynth.TENSOR_Q, step)
+        qh = kvsynth.fill_bf16_host(3, hq, 128, SEED, kvsynth.TENSOR_Q, step)
+        out = gpu.decode(qd, g, SCALE).cpu().numpy()
+        gpu.sync()
+        assert_outputs_close(out, orc.decode(qh, o, SCALE).reshape(3, hq, 128), what)
+
+    for r in range(3):
+        grow(r, lens[r], r)
+    gpu.reorder(g)
+    assert orc.reorder(o) == oracle.OK
+    check(0, "initial (request 2 empty)")
+    for step, add in enumerate(([5, 33, 70], [1, 1, 1], [3, 0, 2], [400, 200, 300]), start=1):
+        for r in range(3):
+            grow(r, add[r], 10 * step + r)
+        gpu.reorder(g)
+        assert orc.reorder(o) == oracle.OK
+        check(step, f"after growth {add}")
