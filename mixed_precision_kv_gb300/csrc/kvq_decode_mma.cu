@@ -265,7 +265,7 @@ __device__ __forceinline__ void qk_int4(const uint8_t* blk, const uint4* bq4, co
 template <int G>
 __device__ __forceinline__ void qk_int2(const uint8_t* blk, const uint4* bq2, const uint4* bqn,
                                         const float (&acol)[Cols<G>::NH], const CtaSmem& S,
-                                        float (&lg)[2][2][Cols<G>::NH]) {
+                                        float (&lg)[2][2][Cols<G>::NH], float (&zc)[Cols<G>::NH]) {
   constexpr bool kPair = Cols<G>::kPair;
   const int lane = threadIdx.x & 31, r = lane >> 2, i = lane & 3;
   uint2 kw[2][2];
@@ -309,14 +309,13 @@ __device__ __forceinline__ void qk_int2(const uint8_t* blk, const uint4* bq2, co
     }
   }
   // zero term Z_h = sum_c q_hc zero_c (fp32 sums of exact binary16 products),
-  // reduced over the lanes of head h
-  float zp = 0.0f;
-  int hz;
+  // returned per head (the softmax adds it to the page's logits as a scalar,
+  // so its reduction overlaps the max reduction instead of preceding it)
   if constexpr (kPair) {
-    const int wi = r >> 2;
-    hz = r & 3;
-    const uint4* zs = reinterpret_cast<const uint4*>(blk + kI2KMeta + 256 + 64 * i + 32 * wi);
-    const uint4* qs = reinterpret_cast<const uint4*>(&S.qzh[hz][(i * 2 + wi) * 8]);
+    // lane (r, i) sums head i over scale/zero pairs 8r .. 8r+7; the lanes of
+    // one head (r = 0..7) reduce, and every lane ends with its own head's Z
+    const uint4* zs = reinterpret_cast<const uint4*>(blk + kI2KMeta + 256 + 32 * r);
+    const uint4* qs = reinterpret_cast<const uint4*>(&S.qzh[i][8 * r]);
     float zq[4] = {0.0f, 0.0f, 0.0f, 0.0f};   // independent partial sums
 #pragma unroll
     for (int x4 = 0; x4 < 2; ++x4) {
@@ -326,14 +325,23 @@ __device__ __forceinline__ void qk_int2(const uint8_t* blk, const uint4* bq2, co
       zq[2] = fma2_f16_f32(zz.z, qz.z, zq[2]);
       zq[3] = fma2_f16_f32(zz.w, qz.w, zq[3]);
     }
-    zp = (zq[0] + zq[1]) + (zq[2] + zq[3]);
-    zp += __shfl_xor_sync(0xFFFFFFFFu, zp, 1);
-    zp += __shfl_xor_sync(0xFFFFFFFFu, zp, 2);
+    float zp = (zq[0] + zq[1]) + (zq[2] + zq[3]);
+    zp += __shfl_xor_sync(0xFFFFFFFFu, zp, 4);
+    zp += __shfl_xor_sync(0xFFFFFFFFu, zp, 8);
     zp += __shfl_xor_sync(0xFFFFFFFFu, zp, 16);
+    zc[0] = zp * S.qzs[i];
+#pragma unroll
+    for (int m = 0; m < 2; ++m)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float v = (acc[m][0][2 * e] + acc[m][0][2 * e + 1]) + (acc[m][1][2 * e] + acc[m][1][2 * e + 1]);
+        lg[m][e][0] = acol[0] * v;
+      }
   } else {
-    hz = r;
+    // lane (r, i) sums head r over chunk i; the 4 lanes of a head reduce and
+    // the lanes of heads 2i, 2i+1 fetch theirs
     const uint4* zs = reinterpret_cast<const uint4*>(blk + kI2KMeta + 256 + 64 * i);
-    const uint4* qs = reinterpret_cast<const uint4*>(&S.qzh[hz][i * 16]);
+    const uint4* qs = reinterpret_cast<const uint4*>(&S.qzh[r][i * 16]);
     float zq[4] = {0.0f, 0.0f, 0.0f, 0.0f};   // independent partial sums
 #pragma unroll
     for (int x4 = 0; x4 < 4; ++x4) {
@@ -343,36 +351,26 @@ __device__ __forceinline__ void qk_int2(const uint8_t* blk, const uint4* bq2, co
       zq[2] = fma2_f16_f32(zz.z, qz.z, zq[2]);
       zq[3] = fma2_f16_f32(zz.w, qz.w, zq[3]);
     }
-    zp = (zq[0] + zq[1]) + (zq[2] + zq[3]);
+    float zp = (zq[0] + zq[1]) + (zq[2] + zq[3]);
     zp += __shfl_xor_sync(0xFFFFFFFFu, zp, 1);
     zp += __shfl_xor_sync(0xFFFFFFFFu, zp, 2);
-  }
-  zp *= S.qzs[hz];
-  if constexpr (kPair) {
-    const float zc = __shfl_sync(0xFFFFFFFFu, zp, 4 * i);   // head i lives on lanes with r & 3 = i
-#pragma unroll
-    for (int m = 0; m < 2; ++m)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const float v = (acc[m][0][2 * e] + acc[m][0][2 * e + 1]) + (acc[m][1][2 * e] + acc[m][1][2 * e + 1]);
-        lg[m][e][0] = fmaf(acol[0], v, zc);
-      }
-  } else {
-    const float zc[2] = {__shfl_sync(0xFFFFFFFFu, zp, 4 * (2 * i)), __shfl_sync(0xFFFFFFFFu, zp, 4 * (2 * i + 1))};
+    zp *= S.qzs[r];
+    zc[0] = __shfl_sync(0xFFFFFFFFu, zp, 4 * (2 * i));
+    zc[1] = __shfl_sync(0xFFFFFFFFu, zp, 4 * (2 * i + 1));
 #pragma unroll
     for (int m = 0; m < 2; ++m)
 #pragma unroll
       for (int e = 0; e < 2; ++e)
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh)
-          lg[m][e][hh] = fmaf(acol[hh], acc[m][0][2 * e + hh] + acc[m][1][2 * e + hh], zc[hh]);
+        for (int hh = 0; hh < 2; ++hh) lg[m][e][hh] = acol[hh] * (acc[m][0][2 * e + hh] + acc[m][1][2 * e + hh]);
   }
 }
 
 // ---- online softmax update and P.V for one page (either width)
 template <int G, bool kInt2>
 __device__ __forceinline__ void softmax_pv(const uint8_t* blk, uint32_t live, float pscale,
-                                           float (&lg)[2][2][Cols<G>::NH], float (&o)[8][4], float (&zv)[4],
+                                           float (&lg)[2][2][Cols<G>::NH], const float (&zc)[Cols<G>::NH],
+                                           float (&o)[8][4], float (&zv)[4],
                                            float (&mrun)[Cols<G>::NH], float (&lsum)[Cols<G>::NH],
                                            float (*pbuf)[kPage]) {
   constexpr bool kPair = Cols<G>::kPair;
@@ -387,8 +385,9 @@ __device__ __forceinline__ void softmax_pv(const uint8_t* blk, uint32_t live, fl
       for (int e = 0; e < 2; ++e)
         if (!((live >> (16 * m + r + 8 * e)) & 1u))
 #pragma unroll
-          for (int hh = 0; hh < NH; ++hh) lg[m][e][hh] = kDead2;
+          for (int hh = 0; hh < NH; ++hh) lg[m][e][hh] = kDead2 - zc[hh];
   }
+  // the page's logits are lg + zc (zc: a per-head constant of the page)
   float corr[NH], pv[2][2][NH];
 #pragma unroll
   for (int hh = 0; hh < NH; ++hh) {
@@ -396,15 +395,16 @@ __device__ __forceinline__ void softmax_pv(const uint8_t* blk, uint32_t live, fl
     pm = fmaxf(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, 4));
     pm = fmaxf(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, 8));
     pm = fmaxf(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, 16));
-    const float mnew = fmaxf(mrun[hh], pm);
+    const float mnew = fmaxf(mrun[hh], pm + zc[hh]);
     corr[hh] = ex2(mrun[hh] - mnew);
     mrun[hh] = mnew;
+    const float mo = mnew - zc[hh];
     float ps = 0.0f;
 #pragma unroll
     for (int m = 0; m < 2; ++m)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        pv[m][e][hh] = ex2(lg[m][e][hh] - mnew);
+        pv[m][e][hh] = ex2(lg[m][e][hh] - mo);
         ps += pv[m][e][hh];
       }
     lsum[hh] = lsum[hh] * corr[hh] + ps;
@@ -730,13 +730,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_mma_kernel(
       if (!__all_sync(0xFFFFFFFFu, got)) { ok = false; break; }
       const Entry e = ent0;
       const uint8_t* blk = WS.stage[st];
-      float lg[2][2][NH];
+      float lg[2][2][NH], zc[NH];
       if (e.id < n2) {
-        qk_int2<G>(blk, &S.bq2[0][0], &S.bqn[0][0], acol2, S, lg);
-        softmax_pv<G, true>(blk, e.live, pscale, lg, o, zv, mrun, lsum, S.pbuf[w]);
+        qk_int2<G>(blk, &S.bq2[0][0], &S.bqn[0][0], acol2, S, lg, zc);
+        softmax_pv<G, true>(blk, e.live, pscale, lg, zc, o, zv, mrun, lsum, S.pbuf[w]);
       } else {
         qk_int4<G>(blk, &S.bq4[0][0], bz, acol4, lg);
-        softmax_pv<G, false>(blk, e.live, pscale, lg, o, zv, mrun, lsum, S.pbuf[w]);
+#pragma unroll
+        for (int hh = 0; hh < NH; ++hh) zc[hh] = 0.0f;
+        softmax_pv<G, false>(blk, e.live, pscale, lg, zc, o, zv, mrun, lsum, S.pbuf[w]);
       }
       if (k + kStages < nw && lane == 0) {
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

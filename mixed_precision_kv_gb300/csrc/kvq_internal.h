@@ -76,14 +76,15 @@ struct Split {
 };
 
 // Planner cost of one page by precision, proportional to the scan kernel's
-// time per page.  The tensor-core scan is bound by instruction issue, and an
-// INT2 page takes about 1.1x the time of an INT4 page (all-INT2 vs all-INT4
-// pools of the 32K-token batch-8 step); the CUDA-core scan is charged its
-// block bytes plus 2048.
+// time per page.  The tensor-core scan is bound by instruction issue, not by
+// bytes: an INT2 page takes the same time as an INT4 page for g <= 4 and
+// 1.1x for g > 4 (all-INT2 vs all-INT4 pools of the 32K-token batch-8 and
+// 100K-token batch-16 steps); the CUDA-core scan is charged its block bytes
+// plus 2048.
 struct PageCost {
   double int2, int4;
 };
-constexpr PageCost kMmaPageCost{1.10, 1.00};
+inline PageCost mma_page_cost(int g) { return g <= 4 ? PageCost{1.00, 1.00} : PageCost{1.10, 1.00}; }
 constexpr PageCost kSimtPageCost{3072.0 + 2048.0, 5120.0 + 2048.0};
 constexpr int64_t kMinPagesPerCta = 16;
 constexpr int64_t kTimingRing = 2048;

@@ -101,7 +101,7 @@ extern "C" kv_status_t kv_decode_attn_noalloc(kv_pool_t* P, const void* q, const
   if (n_ctas < 1)
     return nfail(KV_ERR_INVALID_ARG, "kv_decode_attn_noalloc: the plan does not fit the fixed scratch");
   HostPlan hp;
-  plan_decode(P, req_ids, batch, n_ctas, impl == KV_DECODE_MMA ? kMmaPageCost : kSimtPageCost, hp);
+  plan_decode(P, req_ids, batch, n_ctas, impl == KV_DECODE_MMA ? mma_page_cost(g) : kSimtPageCost, hp);
   const size_t splits_off = units_bytes;
   const size_t cta_off = align256(splits_off + hp.splits.size() * sizeof(Split));
   const size_t part_off = align256(cta_off + hp.cta_split.size() * sizeof(int32_t));

@@ -680,7 +680,7 @@ kv_status_t build_plan(kv_pool* P, const int32_t* req_ids, int32_t batch, int32_
 
   const int ctas = impl == KV_DECODE_MMA ? decode_mma_ctas_per_sm(g) : decode_simt_ctas_per_sm(g);
   HostPlan hp;
-  plan_decode(P, req_ids, batch, (int64_t)P->sm_count * ctas, impl == KV_DECODE_MMA ? kMmaPageCost : kSimtPageCost,
+  plan_decode(P, req_ids, batch, (int64_t)P->sm_count * ctas, impl == KV_DECODE_MMA ? mma_page_cost(g) : kSimtPageCost,
               hp);
   Upload up;
   const size_t ou = up.add(hp.units.data(), hp.units.size() * sizeof(Unit));
