@@ -57,10 +57,13 @@ constexpr uint32_t kC6 = 0x00C000C0u;   // 2-bit field at bit 6 of each half
 constexpr uint32_t kC8 = 0x03000300u;   // 2-bit field at bit 8 of each half
 constexpr float kCodeUnit = 262144.0f;  // 2^18: a field at bit 6 is code * 2^-18
 
-struct WarpSmem {
+// Every warp's stages start on a 16-byte boundary (bulk-copy destinations and
+// 16-byte shared loads require it), whatever the stage count.
+struct alignas(16) WarpSmem {
   uint8_t stage[kStages][kStageBytes];
   unsigned long long bar[kStages];
 };
+static_assert(sizeof(WarpSmem) % 16 == 0 && kStageBytes % 16 == 0, "stage buffers must stay 16-byte aligned");
 
 struct CtaSmem {
   WarpSmem warp[kWarps];
