@@ -186,10 +186,13 @@ KVQ_API kv_status_t kv_export_request(kv_pool_t* pool, int32_t req_id, int32_t* 
  * filled prefix), 8 bytes per table entry, q (bf16) and out (fp32). */
 KVQ_API kv_status_t kv_last_decode_stats(kv_pool_t* pool, int64_t* kv_bytes, int32_t* n_splits, int64_t* n_pages);
 
-/* Device-time measurement of the decode kernels.  enable = 1 starts (or
- * restarts) recording: every later kv_decode_attn call records CUDA events on
- * its stream before the split scan, between scan and merge, and after the
- * merge (the last 2048 calls are kept).  enable = 0 stops recording.  On
+/* Device-time measurement of the decode kernels.  enable = N >= 1 starts (or
+ * restarts) recording: every N-th later kv_decode_attn call (the first, the
+ * (N+1)-th, ...) records CUDA events on its stream before the split scan,
+ * between scan and merge, and after the merge (the last 2048 recorded calls
+ * are kept).  The event between scan and merge keeps the merge from being
+ * set up while the scan drains, so sampling (N > 1) leaves the other calls
+ * undisturbed.  enable = 0 stops recording; enable < 0 is KV_ERR_INVALID_ARG.  On
  * return (host outputs, each may be NULL): *n_calls = calls recorded since the
  * last start (at most 2048 are averaged), *scan_ms / *decode_ms = mean duration
  * of the scan kernel / of scan + merge over them (waits for the last call's

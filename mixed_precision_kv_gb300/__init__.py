@@ -267,14 +267,15 @@ class KVPool:
                "kv_export_request")
         return d
 
-    def decode_timing(self, enable=True):
-        """(Re)start or stop device timing of the decode kernels; returns
-        (n_calls, mean scan ms, mean scan+merge ms) recorded since the last start."""
+    def decode_timing(self, enable=True, every=1):
+        """(Re)start (recording every `every`-th decode call) or stop device timing
+        of the decode kernels; returns (n_calls, mean scan ms, mean scan+merge ms)
+        recorded since the last start."""
         n = ctypes.c_int64()
         a = ctypes.c_float()
         b = ctypes.c_float()
-        _check(load_library().kv_decode_timing(self._h, int(bool(enable)), ctypes.byref(n), ctypes.byref(a),
-                                               ctypes.byref(b)), "kv_decode_timing")
+        _check(load_library().kv_decode_timing(self._h, int(every) if enable else 0, ctypes.byref(n),
+                                               ctypes.byref(a), ctypes.byref(b)), "kv_decode_timing")
         return n.value, a.value, b.value
 
     def launch_count(self) -> int:

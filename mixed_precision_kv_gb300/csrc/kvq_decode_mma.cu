@@ -593,6 +593,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_mma_kernel(
   CtaSmem& S = *reinterpret_cast<CtaSmem*>(smem_raw);
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, r = lane >> 2, i = lane & 3;
   WarpSmem& WS = S.warp[w];
+  asm volatile("griddepcontrol.launch_dependents;");   // the merge may be scheduled as CTAs retire
   if (lane == 0) {
     for (int st = 0; st < kStages; ++st) bar_init(&WS.bar[st]);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");

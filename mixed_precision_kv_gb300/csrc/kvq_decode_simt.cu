@@ -44,6 +44,7 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(
     const Entry* __restrict__ table, const __nv_bfloat16* __restrict__ q, int hq, float scale_log2,
     const Unit* __restrict__ units, const Split* __restrict__ splits, const int32_t* __restrict__ cta_split,
     const int32_t* __restrict__ ntab, float* __restrict__ part) {
+  asm volatile("griddepcontrol.launch_dependents;");   // the merge may be scheduled as CTAs retire
   __shared__ float qs[G][kHeadDim];
   __shared__ __align__(16) uint8_t buf[kWarps][kInt4Block];
   __shared__ float pb[kWarps][kPage][G];
@@ -181,6 +182,9 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(
 template <int G>
 __global__ void merge_kernel(const Unit* __restrict__ units, const float* __restrict__ part, int hq,
                              float* __restrict__ out) {
+  // Launched as a programmatic dependent of the scan: wait until the scan grid
+  // has completed and its partials are visible (immediate for a plain launch).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const Unit u = units[blockIdx.x];
   const int h = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float* o = out + ((size_t)u.b * hq + (size_t)u.kvh * G + h) * kHeadDim + 4 * lane;
@@ -236,18 +240,29 @@ cudaError_t launch_g(kv_pool* P, const void* q, int32_t hq, float scale_log2, co
 cudaError_t launch_merge(kv_pool* P, int g, const Unit* d_units, int n_units, const float* d_part, int hq, float* out,
                          cudaStream_t s) {
   ++P->launches;
+  // Programmatic dependent launch: the merge grid is set up while the scan
+  // grid drains; its griddepcontrol.wait orders it after the scan's results.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)n_units);
+  cfg.blockDim = dim3((unsigned)(32 * g));
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   switch (g) {
-    case 1: merge_kernel<1><<<n_units, 32, 0, s>>>(d_units, d_part, hq, out); break;
-    case 2: merge_kernel<2><<<n_units, 64, 0, s>>>(d_units, d_part, hq, out); break;
-    case 3: merge_kernel<3><<<n_units, 96, 0, s>>>(d_units, d_part, hq, out); break;
-    case 4: merge_kernel<4><<<n_units, 128, 0, s>>>(d_units, d_part, hq, out); break;
-    case 5: merge_kernel<5><<<n_units, 160, 0, s>>>(d_units, d_part, hq, out); break;
-    case 6: merge_kernel<6><<<n_units, 192, 0, s>>>(d_units, d_part, hq, out); break;
-    case 7: merge_kernel<7><<<n_units, 224, 0, s>>>(d_units, d_part, hq, out); break;
-    case 8: merge_kernel<8><<<n_units, 256, 0, s>>>(d_units, d_part, hq, out); break;
+    case 1: return cudaLaunchKernelEx(&cfg, merge_kernel<1>, d_units, d_part, hq, out);
+    case 2: return cudaLaunchKernelEx(&cfg, merge_kernel<2>, d_units, d_part, hq, out);
+    case 3: return cudaLaunchKernelEx(&cfg, merge_kernel<3>, d_units, d_part, hq, out);
+    case 4: return cudaLaunchKernelEx(&cfg, merge_kernel<4>, d_units, d_part, hq, out);
+    case 5: return cudaLaunchKernelEx(&cfg, merge_kernel<5>, d_units, d_part, hq, out);
+    case 6: return cudaLaunchKernelEx(&cfg, merge_kernel<6>, d_units, d_part, hq, out);
+    case 7: return cudaLaunchKernelEx(&cfg, merge_kernel<7>, d_units, d_part, hq, out);
+    case 8: return cudaLaunchKernelEx(&cfg, merge_kernel<8>, d_units, d_part, hq, out);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 cudaError_t launch_decode_simt(kv_pool* P, const void* q, int32_t hq, float scale_log2, const Unit* d_units,

@@ -147,6 +147,8 @@ struct kv_pool {
   cudaStream_t last_stream = nullptr;
   int64_t launches = 0;               // kernels launched by this pool
   bool timing = false;                // record events around the decode kernels
+  int32_t timing_every = 1;           // record every timing_every-th decode call
+  int64_t timing_seen = 0;            // decode calls since timing started
   int64_t timed_calls = 0;            // decode calls recorded since timing started
   std::vector<cudaEvent_t> tev;       // ring of [before scan, after scan, after merge] per call
   cudaEvent_t merge_event = nullptr;  // recorded by the launchers between scan and merge when timing

@@ -737,7 +737,8 @@ kv_status_t kv_decode_attn(kv_pool_t* P, const void* q, const int32_t* req_ids, 
   const Unit* du = (const Unit*)(base + P->plan_units_off);
   const Split* dsp = (const Split*)(base + P->plan_splits_off);
   const int32_t* dct = (const int32_t*)(base + P->plan_cta_off);
-  cudaEvent_t* tv = P->timing ? &P->tev[3 * (size_t)(P->timed_calls % kTimingRing)] : nullptr;
+  const bool rec = P->timing && (P->timing_seen++ % P->timing_every) == 0;
+  cudaEvent_t* tv = rec ? &P->tev[3 * (size_t)(P->timed_calls % kTimingRing)] : nullptr;
   if (tv) KV_CUDA(cudaEventRecord(tv[0], s));
   P->merge_event = tv ? tv[1] : nullptr;
   if (impl == KV_DECODE_MMA)
@@ -775,12 +776,15 @@ kv_status_t kv_decode_timing(kv_pool_t* P, int32_t enable, int64_t* n_calls, flo
     if (scan_ms) *scan_ms = (float)(a / (double)n);
     if (decode_ms) *decode_ms = (float)(b / (double)n);
   }
+  if (enable < 0) return fail(KV_ERR_INVALID_ARG, "kv_decode_timing: enable must be >= 0");
   if (enable) {
     if (P->tev.empty()) {
       P->tev.assign(3 * (size_t)kTimingRing, nullptr);
       for (auto& e : P->tev) KV_CUDA(cudaEventCreate(&e));
     }
     P->timed_calls = 0;
+    P->timing_seen = 0;
+    P->timing_every = enable;
   }
   P->timing = enable != 0;
   return KV_OK;

@@ -257,3 +257,20 @@ def test_plan_reuse_across_growth(kvq, impl):
         gpu.reorder(g)
         assert orc.reorder(o) == oracle.OK
         check(step, f"after growth {add}")
+
+
+def test_decode_timing_samples_every_nth_call(kvq):
+    bits = [_mixed(200, 0.5, 21), _mixed(90, 0.5, 22)]
+    sc = Scenario(kvq, 2, 8, bits)
+    qd = torch.zeros((2, 8, 128), dtype=torch.bfloat16, device="cuda")
+    n0, _, _ = sc.gpu.decode_timing(True, every=3)
+    for _ in range(7):
+        sc.gpu.decode(qd, sc.g_ids, SCALE)
+    n, scan_ms, dec_ms = sc.gpu.decode_timing(False)
+    assert n == 3                                   # calls 1, 4 and 7
+    assert 0.0 < scan_ms <= dec_ms
+    sc.gpu.decode_timing(True)                      # restart: counts from zero, every call
+    sc.gpu.decode(qd, sc.g_ids, SCALE)
+    n, _, _ = sc.gpu.decode_timing(False)
+    assert n == 1
+    assert kvq.load_library().kv_decode_timing(sc.gpu.handle, -1, None, None, None) == kvq.KV_ERR_INVALID_ARG
