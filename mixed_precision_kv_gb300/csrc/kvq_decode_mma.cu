@@ -593,6 +593,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_mma_kernel(
   CtaSmem& S = *reinterpret_cast<CtaSmem*>(smem_raw);
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, r = lane >> 2, i = lane & 3;
   WarpSmem& WS = S.warp[w];
+  asm volatile("griddepcontrol.wait;" ::: "memory");   // the appends before this decode are done
   asm volatile("griddepcontrol.launch_dependents;");   // the merge may be scheduled as CTAs retire
   if (lane == 0) {
     for (int st = 0; st < kStages; ++st) bar_init(&WS.bar[st]);
@@ -852,11 +853,11 @@ cudaError_t launch_mma_g(kv_pool* P, const void* q, int32_t hq, float scale_log2
   }
   if (n_ctas <= 0) return cudaSuccess;
   ++P->launches;
-  decode_mma_kernel<G><<<n_ctas, kThreads, sizeof(CtaSmem), s>>>(
-      P->d_pool, P->int4_offset, P->cfg.n_int2_pages, P->cfg.num_kv_heads, P->cfg.max_pages_per_request, P->d_table,
-      (const __nv_bfloat16*)q, hq, scale_log2, d_units, d_splits, d_cta, P->d_ntab, d_part, P->d_status + 1,
-      P->d_status);
-  return cudaGetLastError();
+  const uint32_t* smax = P->d_status + 1;
+  return launch_pdl(decode_mma_kernel<G>, dim3((unsigned)n_ctas), dim3(kThreads), sizeof(CtaSmem), s,
+                    (const uint8_t*)P->d_pool, P->int4_offset, (int64_t)P->cfg.n_int2_pages, P->cfg.num_kv_heads,
+                    P->cfg.max_pages_per_request, (const Entry*)P->d_table, (const __nv_bfloat16*)q, (int)hq,
+                    scale_log2, d_units, d_splits, d_cta, (const int32_t*)P->d_ntab, d_part, smax, P->d_status);
 }
 
 template <int G>

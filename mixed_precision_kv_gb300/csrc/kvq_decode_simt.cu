@@ -44,6 +44,7 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(
     const Entry* __restrict__ table, const __nv_bfloat16* __restrict__ q, int hq, float scale_log2,
     const Unit* __restrict__ units, const Split* __restrict__ splits, const int32_t* __restrict__ cta_split,
     const int32_t* __restrict__ ntab, float* __restrict__ part) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");   // the appends before this decode are done
   asm volatile("griddepcontrol.launch_dependents;");   // the merge may be scheduled as CTAs retire
   __shared__ float qs[G][kHeadDim];
   __shared__ __align__(16) uint8_t buf[kWarps][kInt4Block];
@@ -185,6 +186,7 @@ __global__ void merge_kernel(const Unit* __restrict__ units, const float* __rest
   // Launched as a programmatic dependent of the scan: wait until the scan grid
   // has completed and its partials are visible (immediate for a plain launch).
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");   // the next call's kernels may be staged
   const Unit u = units[blockIdx.x];
   const int h = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float* o = out + ((size_t)u.b * hq + (size_t)u.kvh * G + h) * kHeadDim + 4 * lane;
@@ -224,9 +226,12 @@ cudaError_t launch_g(kv_pool* P, const void* q, int32_t hq, float scale_log2, co
                      cudaStream_t s) {
   if (n_ctas > 0) {
     ++P->launches;
-    decode_simt_kernel<G><<<n_ctas, kThreads, 0, s>>>(
-        P->d_pool, P->int4_offset, P->cfg.n_int2_pages, P->cfg.num_kv_heads, P->cfg.max_pages_per_request,
-        P->d_table, (const __nv_bfloat16*)q, hq, scale_log2, d_units, d_splits, d_cta, P->d_ntab, d_part);
+    const cudaError_t e = launch_pdl(decode_simt_kernel<G>, dim3((unsigned)n_ctas), dim3(kThreads), 0, s,
+                                     (const uint8_t*)P->d_pool, P->int4_offset, (int64_t)P->cfg.n_int2_pages,
+                                     P->cfg.num_kv_heads, P->cfg.max_pages_per_request, (const Entry*)P->d_table,
+                                     (const __nv_bfloat16*)q, (int)hq, scale_log2, d_units, d_splits, d_cta,
+                                     (const int32_t*)P->d_ntab, d_part);
+    if (e != cudaSuccess) return e;
   }
   if (P->merge_event) {
     const cudaError_t e = cudaEventRecord(P->merge_event, s);

@@ -6,6 +6,7 @@
 
 #include <set>
 #include <string>
+#include <utility>
 #include <vector>
 
 #include "../../include/kvq.h"
@@ -155,6 +156,26 @@ struct kv_pool {
 };
 
 namespace kvq {
+
+// Launch with programmatic stream serialization: the grid may be staged while
+// the previous kernel of the stream drains.  Every kernel launched this way
+// executes griddepcontrol.wait before it touches memory that earlier work in
+// the stream reads or writes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Sets the message kv_last_error() returns on this thread (kvq_pool.cu).
 void set_last_error(const char* msg);

@@ -132,6 +132,8 @@ __global__ void __launch_bounds__(kThreads) append_int4_kernel(
     Entry* __restrict__ table, int32_t* __restrict__ ntab, uint32_t* __restrict__ status,
     const __grid_constant__ SmallAppend small) {
   __shared__ __align__(16) uint8_t img[kInt4Block];
+  asm volatile("griddepcontrol.wait;" ::: "memory");   // earlier work on the stream (the previous decode) is done
+  asm volatile("griddepcontrol.launch_dependents;");
   const AppendJob job = kByValue ? small.jobs[blockIdx.x] : jobs[blockIdx.x];
   const int32_t* tk = kByValue ? small.toks : toks;
   const int h = blockIdx.y;
@@ -252,19 +254,16 @@ cudaError_t launch_append(kv_pool* P, const void* k, const void* v, const Append
   if (n_jobs <= 0) return cudaSuccess;
   dim3 grid((unsigned)n_jobs, (unsigned)P->cfg.num_kv_heads);
   ++P->launches;
-  if (small) {
-    append_int4_kernel<true><<<grid, kThreads, 0, s>>>(P->d_pool, P->int4_offset, P->cfg.n_int2_pages,
-                                                       P->cfg.num_kv_heads, (const __nv_bfloat16*)k,
-                                                       (const __nv_bfloat16*)v, nullptr, nullptr, P->d_table,
-                                                       P->d_ntab, P->d_status, *small);
-  } else {
-    static const SmallAppend none{};
-    append_int4_kernel<false><<<grid, kThreads, 0, s>>>(P->d_pool, P->int4_offset, P->cfg.n_int2_pages,
-                                                        P->cfg.num_kv_heads, (const __nv_bfloat16*)k,
-                                                        (const __nv_bfloat16*)v, d_jobs, d_toks, P->d_table,
-                                                        P->d_ntab, P->d_status, none);
-  }
-  return cudaGetLastError();
+  const AppendJob* no_jobs = nullptr;
+  const int32_t* no_toks = nullptr;
+  if (small)
+    return launch_pdl(append_int4_kernel<true>, grid, dim3(kThreads), 0, s, P->d_pool, P->int4_offset,
+                      P->cfg.n_int2_pages, P->cfg.num_kv_heads, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v,
+                      no_jobs, no_toks, P->d_table, P->d_ntab, P->d_status, *small);
+  static const SmallAppend none{};
+  return launch_pdl(append_int4_kernel<false>, grid, dim3(kThreads), 0, s, P->d_pool, P->int4_offset,
+                    P->cfg.n_int2_pages, P->cfg.num_kv_heads, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v,
+                    d_jobs, d_toks, P->d_table, P->d_ntab, P->d_status, none);
 }
 
 cudaError_t launch_repack(kv_pool* P, const RepackJob* d_jobs, int n_jobs, cudaStream_t s) {
