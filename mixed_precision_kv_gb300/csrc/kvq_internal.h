@@ -4,7 +4,6 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include <set>
 #include <string>
 #include <utility>
 #include <vector>
@@ -54,6 +53,14 @@ struct SmallAppend {
 struct RepackJob {
   int32_t src;  // INT4 staging page id
   int32_t dst;  // INT2 page id
+};
+
+// Direct INT2 job: 32 tokens of one request that fill a staging page within a
+// single call, quantized to INT4, dequantized and requantized to INT2 in one
+// kernel (the staging page is never written).
+struct DirectJob {
+  int32_t dst;      // INT2 page id
+  int32_t tok_off;  // offset of its 32 token indices (slot order)
 };
 
 // Work unit of the decode: one (batch row, kv head).  Its splits (page ranges,
@@ -106,6 +113,43 @@ struct Request {
   uint64_t version = 0;             // bumped whenever the table's entries change
 };
 
+// Free page ids of one class, handed out lowest id first (a bitset with a
+// hint at the lowest word that may hold a free id).
+class FreeIds {
+ public:
+  void init(int32_t first, int32_t n) {
+    first_ = first;
+    bits_.assign((size_t)((n + 63) / 64), ~0ull);
+    if (n % 64) bits_.back() = (1ull << (n % 64)) - 1;
+    count_ = (size_t)n;
+    lo_ = 0;
+  }
+  size_t size() const { return count_; }
+  bool empty() const { return count_ == 0; }
+  void insert(int32_t id) {
+    const int32_t x = id - first_;
+    uint64_t& wd = bits_[(size_t)(x >> 6)];
+    const uint64_t b = 1ull << (x & 63);
+    if (!(wd & b)) {
+      wd |= b;
+      ++count_;
+      if ((size_t)(x >> 6) < lo_) lo_ = (size_t)(x >> 6);
+    }
+  }
+  int32_t take_lowest() {   // caller ensures !empty()
+    while (bits_[lo_] == 0) ++lo_;
+    const int b = __builtin_ctzll(bits_[lo_]);
+    bits_[lo_] &= bits_[lo_] - 1;
+    --count_;
+    return first_ + (int32_t)(lo_ * 64) + b;
+  }
+
+ private:
+  std::vector<uint64_t> bits_;
+  size_t count_ = 0, lo_ = 0;
+  int32_t first_ = 0;
+};
+
 // A device buffer that grows geometrically (contents not preserved).
 struct DevBuf {
   void* ptr = nullptr;
@@ -132,7 +176,9 @@ struct kv_pool {
   std::vector<uint8_t> fill;          // per page id
   std::vector<uint32_t> live;         // per page id
   std::vector<int32_t> pos;           // per page id x 32 slots: token position
-  std::set<int32_t> free2, free4;
+  kvq::FreeIds free2, free4;
+  std::vector<int32_t> call_slot;     // per request: index of its state inside the running append call (-1 outside)
+  std::vector<int32_t> page_job;      // per page id: its append job inside the running call (-1 outside)
   // decode plan cache
   std::vector<int32_t> plan_req;
   std::vector<int32_t> plan_len;      // table lengths of plan_req when the plan was built
@@ -184,6 +230,8 @@ void set_last_error(const char* msg);
 cudaError_t launch_append(kv_pool* P, const void* k, const void* v, const AppendJob* d_jobs, int n_jobs,
                           const int32_t* d_toks, const SmallAppend* small, cudaStream_t s);
 cudaError_t launch_repack(kv_pool* P, const RepackJob* d_jobs, int n_jobs, cudaStream_t s);
+cudaError_t launch_direct_int2(kv_pool* P, const void* k, const void* v, const DirectJob* d_jobs, int n_jobs,
+                               const int32_t* d_toks, cudaStream_t s);
 cudaError_t launch_scatter(kv_pool* P, const TableUpd* d_upd, int n, cudaStream_t s);
 
 // Balanced decode plan: units (batch row, kv head) in order, their pages cut

@@ -60,11 +60,6 @@ bool req_ok(const kv_pool* P, int32_t r) {
 
 bool is_int2(const kv_pool* P, int32_t id) { return id < P->cfg.n_int2_pages; }
 
-int32_t take_lowest(std::set<int32_t>& s) {
-  const int32_t id = *s.begin();
-  s.erase(s.begin());
-  return id;
-}
 
 // Grow a device buffer to at least `bytes` (contents are not kept).
 kv_status_t ensure(DevBuf& b, size_t bytes) {
@@ -295,8 +290,8 @@ kv_status_t kv_pool_create(const kv_pool_config_t* cfg, kv_pool_t** out) {
     P->fill.assign(npages, 0);
     P->live.assign(npages, 0);
     P->pos.assign(npages * kPage, -1);
-    for (int64_t i = 0; i < cfg->n_int2_pages; ++i) P->free2.insert(P->free2.end(), (int32_t)i);
-    for (int64_t i = 0; i < cfg->n_int4_pages; ++i) P->free4.insert(P->free4.end(), (int32_t)(cfg->n_int2_pages + i));
+    P->free2.init(0, (int32_t)cfg->n_int2_pages);
+    P->free4.init((int32_t)cfg->n_int2_pages, (int32_t)cfg->n_int4_pages);
   } catch (...) {
     return cleanup(fail(KV_ERR_OOM, "kv_pool_create: host allocation failed"));
   }
@@ -384,81 +379,133 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
   if (n_tok < 0 || n_tok > INT32_MAX) return fail(KV_ERR_INVALID_ARG, "kv_append_quant: bad n_tok %lld", (long long)n_tok);
   if (n_tok == 0) return KV_OK;
   if (!k || !v || !req_ids || !bits) return fail(KV_ERR_INVALID_ARG, "kv_append_quant: null pointer");
-  for (int64_t t = 0; t < n_tok; ++t) {
-    if (!req_ok(P, req_ids[t])) return fail(KV_ERR_INVALID_ARG, "kv_append_quant: token %lld: request %d not open", (long long)t, req_ids[t]);
-    if (bits[t] != 2 && bits[t] != 4) return fail(KV_ERR_INVALID_ARG, "kv_append_quant: token %lld: bits must be 2 or 4", (long long)t);
-  }
+  // Per-request state of this call, found through a pool-wide slot index.
+  struct CallReq {
+    int32_t r;
+    int32_t old_len;       // table length before the call
+    int32_t q_left;        // INT2-tagged tokens of r not yet routed in this call
+    int32_t tail_job;      // append job of the current INT4 tail page (-1: none yet)
+    int32_t stag_job;      // append job of the current staging page (-1: none / direct)
+    bool stag_direct;      // the current staging page fills within this call: quantized directly to INT2
+    int32_t ngrp;          // tokens collected for it so far
+    int32_t grp[kPage];    // their token indices, in slot order
+    // dry-run state
+    bool tail; int tailfill; bool stag; int stagfill; int64_t tablen;
+  };
+  std::vector<CallReq> cr;
+  if (P->call_slot.size() != (size_t)P->cfg.max_requests) P->call_slot.assign((size_t)P->cfg.max_requests, -1);
+  auto slot_of = [&](int32_t r) -> CallReq& {
+    int32_t& sl = P->call_slot[(size_t)r];
+    if (sl < 0) {
+      const Request& R = P->reqs[r];
+      sl = (int32_t)cr.size();
+      CallReq c{};
+      c.r = r;
+      c.old_len = (int32_t)R.table.size();
+      c.tail_job = c.stag_job = -1;
+      c.tail = R.tail4 >= 0;
+      c.tailfill = c.tail ? (int)P->fill[R.tail4] : 0;
+      c.stag = R.staging >= 0;
+      c.stagfill = c.stag ? (int)P->fill[R.staging] : 0;
+      c.tablen = (int64_t)R.table.size();
+      cr.push_back(c);
+    }
+    return cr[(size_t)sl];
+  };
+  struct ResetSlots {
+    kv_pool* P;
+    std::vector<CallReq>* cr;
+    ~ResetSlots() { for (const auto& c : *cr) P->call_slot[(size_t)c.r] = -1; }
+  } reset_slots{P, &cr};
+
   // Dry run: pages taken and table growth, so that OOM changes nothing.
   {
-    struct Sim { bool tail; int tailfill; bool stag; int stagfill; int64_t tablen; };
-    std::unordered_map<int32_t, Sim> sim;
     int64_t need4 = 0, need2 = 0;
     for (int64_t t = 0; t < n_tok; ++t) {
-      auto it = sim.find(req_ids[t]);
-      if (it == sim.end()) {
-        const Request& R = P->reqs[req_ids[t]];
-        Sim s{R.tail4 >= 0, R.tail4 >= 0 ? (int)P->fill[R.tail4] : 0, R.staging >= 0,
-              R.staging >= 0 ? (int)P->fill[R.staging] : 0, (int64_t)R.table.size()};
-        it = sim.emplace(req_ids[t], s).first;
-      }
-      Sim& s = it->second;
+      if (!req_ok(P, req_ids[t]))
+        return fail(KV_ERR_INVALID_ARG, "kv_append_quant: token %lld: request %d not open", (long long)t, req_ids[t]);
+      if (bits[t] != 2 && bits[t] != 4)
+        return fail(KV_ERR_INVALID_ARG, "kv_append_quant: token %lld: bits must be 2 or 4", (long long)t);
+      CallReq& c = slot_of(req_ids[t]);
       if (bits[t] == 4) {
-        if (!s.tail || s.tailfill == kPage) { ++need4; ++s.tablen; s.tail = true; s.tailfill = 0; }
-        ++s.tailfill;
+        if (!c.tail || c.tailfill == kPage) { ++need4; ++c.tablen; c.tail = true; c.tailfill = 0; }
+        ++c.tailfill;
       } else {
-        if (!s.stag) { ++need4; ++s.tablen; s.stag = true; s.stagfill = 0; }
-        if (++s.stagfill == kPage) { ++need2; s.stag = false; }
+        ++c.q_left;
+        if (!c.stag) { ++need4; ++c.tablen; c.stag = true; c.stagfill = 0; }
+        if (++c.stagfill == kPage) { ++need2; c.stag = false; }
       }
-      if (s.tablen > P->cfg.max_pages_per_request)
+      if (c.tablen > P->cfg.max_pages_per_request)
         return fail(KV_ERR_OOM, "kv_append_quant: request %d would exceed %d table entries", req_ids[t], P->cfg.max_pages_per_request);
     }
     if (need4 > (int64_t)P->free4.size() || need2 > (int64_t)P->free2.size())
       return fail(KV_ERR_OOM, "kv_append_quant: needs %lld INT4 + %lld INT2 pages, %zu + %zu free", (long long)need4,
                   (long long)need2, P->free4.size(), P->free2.size());
   }
+  for (const auto& c : cr) {
+    Request& R = P->reqs[c.r];
+    R.loc.reserve(R.loc.size() + (size_t)n_tok);
+  }
   DeviceGuard dg(P->cfg.device);
   cudaStream_t s = (cudaStream_t)stream;
   kv_status_t st = order_after_previous(P, s);
   if (st != KV_OK) return st;
 
+  // Routing in token order (page ids are taken exactly as the per-token rules
+  // dictate).  A staging page that starts empty and is filled within this
+  // call is never materialised: its 32 tokens go to a direct job that
+  // quantizes them to INT4, dequantizes and requantizes to INT2 in one kernel
+  // (the same values the staging page and its repack would give).
   std::vector<AppendJob> jobs;
   std::vector<int32_t> job_req;                        // request of each job
-  std::vector<std::pair<int32_t, int32_t>> touched;   // (request, table length before the call)
   std::vector<RepackJob> repacks;
-  std::vector<int32_t> tok_job((size_t)n_tok), tok_slot((size_t)n_tok);
-  std::unordered_map<int32_t, int32_t> job_of_page;
+  std::vector<DirectJob> directs;
+  std::vector<int32_t> dtoks;                          // 32 token indices per direct job
+  std::vector<int32_t> tok_job((size_t)n_tok, -1), tok_slot((size_t)n_tok);
   std::vector<int32_t> deferred;
   Dirty dirty;   // table rewrites the append kernel does not cover (repacks)
   for (int64_t t = 0; t < n_tok; ++t) {
     const int32_t r = req_ids[t];
     Request& R = P->reqs[r];
-    if (std::find_if(touched.begin(), touched.end(), [&](const auto& x) { return x.first == r; }) == touched.end())
-      touched.emplace_back(r, (int32_t)R.table.size());
+    CallReq& c = cr[(size_t)P->call_slot[(size_t)r]];
     const int64_t pos = (int64_t)R.loc.size();
-    int32_t& cur = (bits[t] == 4) ? R.tail4 : R.staging;
+    const bool b4 = bits[t] == 4;
+    int32_t& cur = b4 ? R.tail4 : R.staging;
     if (cur < 0 || P->fill[cur] == kPage) {
-      cur = take_lowest(P->free4);
+      cur = P->free4.take_lowest();
       P->fill[cur] = 0;
       P->live[cur] = 0;
       R.table.push_back(cur);
       ++R.version;
+      if (b4) {
+        c.tail_job = -1;
+      } else {
+        c.stag_job = -1;
+        c.stag_direct = c.q_left >= kPage;
+        c.ngrp = 0;
+      }
     }
     const int slot = P->fill[cur]++;
     P->live[cur] |= 1u << slot;
     P->pos[(size_t)cur * kPage + slot] = (int32_t)pos;
     R.loc.push_back(((uint32_t)cur << 5) | (uint32_t)slot);
-    auto jt = job_of_page.find(cur);
-    if (jt == job_of_page.end()) {
-      jt = job_of_page.emplace(cur, (int32_t)jobs.size()).first;
-      jobs.push_back(AppendJob{cur, slot, 0, 0, -1, 0u, -1, 0});
-      job_req.push_back(r);
+    if (!b4) --c.q_left;
+    if (!b4 && c.stag_direct) {
+      c.grp[c.ngrp++] = (int32_t)t;
+    } else {
+      int32_t& jb = b4 ? c.tail_job : c.stag_job;
+      if (jb < 0) {
+        jb = (int32_t)jobs.size();
+        jobs.push_back(AppendJob{cur, slot, 0, 0, -1, 0u, -1, 0});
+        job_req.push_back(r);
+      }
+      ++jobs[(size_t)jb].n_slots;
+      tok_job[t] = jb;
+      tok_slot[t] = slot;
     }
-    ++jobs[jt->second].n_slots;
-    tok_job[t] = jt->second;
-    tok_slot[t] = slot;
-    if (bits[t] == 2 && P->fill[cur] == kPage) {
+    if (!b4 && P->fill[cur] == kPage) {
       // 32 qualifying tokens: requantize the staging page into a new INT2 page.
-      const int32_t nid = take_lowest(P->free2);
+      const int32_t nid = P->free2.take_lowest();
       P->fill[nid] = kPage;
       P->live[nid] = P->live[cur];
       for (int sl = 0; sl < kPage; ++sl) {
@@ -466,22 +513,32 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
         P->pos[(size_t)nid * kPage + sl] = p;
         R.loc[p] = ((uint32_t)nid << 5) | (uint32_t)sl;
       }
-      auto it = std::find(R.table.begin(), R.table.end(), cur);
+      const auto rit = std::find(R.table.rbegin(), R.table.rend(), cur);   // the staging page sits near the end
+      const auto it = std::next(rit).base();
       dirty.structural(r, (int32_t)(it - R.table.begin()));
       R.table.erase(it);
       R.table.push_back(nid);
-      repacks.push_back(RepackJob{cur, nid});
+      if (c.stag_direct) {
+        directs.push_back(DirectJob{nid, (int32_t)dtoks.size()});
+        dtoks.insert(dtoks.end(), c.grp, c.grp + kPage);
+        c.ngrp = 0;
+      } else {
+        repacks.push_back(RepackJob{cur, nid});
+      }
       deferred.push_back(cur);
       cur = -1;
+      c.stag_job = -1;
+      c.stag_direct = false;
       ++R.version;
     }
   }
   int32_t off = 0;
   for (auto& j : jobs) { j.tok_off = off; off += j.n_slots; }
-  std::vector<int32_t> toks((size_t)n_tok);
+  std::vector<int32_t> toks((size_t)off);
   for (int64_t t = 0; t < n_tok; ++t) {
-    const AppendJob& j = jobs[tok_job[t]];
-    toks[j.tok_off + (tok_slot[t] - j.first_slot)] = (int32_t)t;
+    if (tok_job[t] < 0) continue;   // routed to a direct job
+    const AppendJob& j = jobs[(size_t)tok_job[t]];
+    toks[(size_t)(j.tok_off + (tok_slot[t] - j.first_slot))] = (int32_t)t;
   }
   for (int32_t id : deferred) {
     P->fill[id] = 0;
@@ -492,29 +549,50 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
   // the final table (pages added at the end or filled in place), and the
   // final table length of every request that grew.
   const uint32_t mp = (uint32_t)P->cfg.max_pages_per_request;
-  for (size_t j = 0; j < jobs.size(); ++j) {
-    AppendJob& J = jobs[j];
-    const int32_t r = job_req[j];
-    const auto& tb = P->reqs[r].table;
-    const auto it = std::find(tb.rbegin(), tb.rend(), J.page);   // appended pages sit near the end
-    if (it != tb.rend()) {
-      J.tab_index = (int32_t)(r * mp + (uint32_t)(tb.rend() - it - 1));
-      J.live = P->live[J.page];
-    }
-    for (const auto& x : touched)
-      if (x.first == r && (int32_t)tb.size() != x.second) {
+  {
+    // A job's page is in its request's final table unless a repack removed it
+    // (freed above, fill 0).  Appended pages sit near the end of the table, so
+    // one backward scan per request finds them all.
+    if (P->page_job.size() != P->fill.size()) P->page_job.assign(P->fill.size(), -1);
+    std::vector<int32_t> need(cr.size(), 0);
+    for (size_t j = 0; j < jobs.size(); ++j) {
+      AppendJob& J = jobs[j];
+      const int32_t r = job_req[j];
+      const int32_t ci = P->call_slot[(size_t)r];
+      const int32_t len = (int32_t)P->reqs[r].table.size();
+      if (len != cr[(size_t)ci].old_len) {
         J.ntab_req = r;
-        J.ntab_len = (int32_t)tb.size();
+        J.ntab_len = len;
       }
+      if (P->fill[J.page] > 0) {
+        P->page_job[(size_t)J.page] = (int32_t)j;
+        J.live = P->live[J.page];
+        ++need[(size_t)ci];
+      }
+    }
+    for (size_t ci = 0; ci < cr.size(); ++ci) {
+      const int32_t r = cr[ci].r;
+      const auto& tb = P->reqs[r].table;
+      for (int32_t i = (int32_t)tb.size() - 1; i >= 0 && need[ci] > 0; --i) {
+        const int32_t j = P->page_job[(size_t)tb[i]];
+        if (j >= 0 && job_req[(size_t)j] == r) {
+          jobs[(size_t)j].tab_index = (int32_t)(r * mp + (uint32_t)i);
+          --need[ci];
+        }
+      }
+    }
+    for (const auto& J : jobs) P->page_job[(size_t)J.page] = -1;
   }
   std::vector<TableUpd> upd;
   emit_updates(P, dirty, upd);
 
-  const bool small = jobs.size() <= (size_t)SmallAppend::kMaxJobs && n_tok <= SmallAppend::kMaxToks;
+  const bool small = jobs.size() <= (size_t)SmallAppend::kMaxJobs && off <= SmallAppend::kMaxToks;
   Upload u;
   const size_t o_jobs = small ? 0 : u.add(jobs.data(), jobs.size() * sizeof(AppendJob));
   const size_t o_toks = small ? 0 : u.add(toks.data(), toks.size() * sizeof(int32_t));
   const size_t o_rep = u.add(repacks.data(), repacks.size() * sizeof(RepackJob));
+  const size_t o_dir = u.add(directs.data(), directs.size() * sizeof(DirectJob));
+  const size_t o_dtok = u.add(dtoks.data(), dtoks.size() * sizeof(int32_t));
   const size_t o_upd = u.add(upd.data(), upd.size() * sizeof(TableUpd));
   if ((st = upload(P, u, s)) != KV_OK) return st;
   uint8_t* base = (uint8_t*)P->upload.ptr;
@@ -527,6 +605,8 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
     KV_CUDA(launch_append(P, k, v, (const AppendJob*)(base + o_jobs), (int)jobs.size(), (const int32_t*)(base + o_toks),
                           nullptr, s));
   }
+  KV_CUDA(launch_direct_int2(P, k, v, (const DirectJob*)(base + o_dir), (int)directs.size(),
+                             (const int32_t*)(base + o_dtok), s));
   KV_CUDA(launch_repack(P, (const RepackJob*)(base + o_rep), (int)repacks.size(), s));
   KV_CUDA(launch_scatter(P, (const TableUpd*)(base + o_upd), (int)upd.size(), s));
   return KV_OK;

@@ -161,23 +161,12 @@ __global__ void __launch_bounds__(kThreads) append_int4_kernel(
   }
 }
 
-// One CTA per (repack job, kv head): INT4 staging block -> INT2 block.
-__global__ void __launch_bounds__(kThreads) repack_int2_kernel(uint8_t* __restrict__ pool, size_t int4_off,
-                                                              int64_t n2, int hkv,
-                                                              const RepackJob* __restrict__ jobs,
-                                                              uint32_t* __restrict__ smax_bits) {
-  __shared__ __align__(16) uint8_t src[kInt4Block];
-  __shared__ __align__(16) uint8_t dst[kInt2Block];
-  const RepackJob job = jobs[blockIdx.x];
-  const int h = blockIdx.y;
-  const uint8_t* sblk = pool + int4_off + ((size_t)(job.src - n2) * hkv + h) * kInt4Block;
-  uint8_t* dblk = pool + ((size_t)job.dst * hkv + h) * kInt2Block;
-  for (int i = threadIdx.x; i < kInt4Block / 16; i += kThreads)
-    reinterpret_cast<uint4*>(src)[i] = reinterpret_cast<const uint4*>(sblk)[i];
-  for (int i = threadIdx.x; i < kInt2Block / 16; i += kThreads)
-    reinterpret_cast<uint4*>(dst)[i] = make_uint4(0, 0, 0, 0);
-  __syncthreads();
-
+// Requantize a 32-token INT4 block image (shared memory) into an INT2 block
+// image (shared memory, zeroed): K per channel across the 32 tokens, V per
+// token and group, both from the INT4-dequantized values fmaf(code, scale,
+// zero); tracks the largest INT2 K and V scales.  128 threads.
+__device__ __forceinline__ void repack_image(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
+                                             uint32_t* __restrict__ smax_bits) {
   // K: thread c owns channel c; its group is the 32 tokens of the page.
   {
     const int c = threadIdx.x;
@@ -233,7 +222,53 @@ __global__ void __launch_bounds__(kThreads) repack_int2_kernel(uint8_t* __restri
     for (int o = 16; o; o >>= 1) vmx = fmaxf(vmx, __shfl_xor_sync(0xFFFFFFFFu, vmx, o));
     if ((threadIdx.x & 31) == 0) atomicMax(smax_bits + 1, __float_as_uint(vmx));
   }
+}
+
+// One CTA per (repack job, kv head): INT4 staging block -> INT2 block.
+__global__ void __launch_bounds__(kThreads) repack_int2_kernel(uint8_t* __restrict__ pool, size_t int4_off,
+                                                              int64_t n2, int hkv,
+                                                              const RepackJob* __restrict__ jobs,
+                                                              uint32_t* __restrict__ smax_bits) {
+  __shared__ __align__(16) uint8_t src[kInt4Block];
+  __shared__ __align__(16) uint8_t dst[kInt2Block];
+  const RepackJob job = jobs[blockIdx.x];
+  const int h = blockIdx.y;
+  const uint8_t* sblk = pool + int4_off + ((size_t)(job.src - n2) * hkv + h) * kInt4Block;
+  uint8_t* dblk = pool + ((size_t)job.dst * hkv + h) * kInt2Block;
+  for (int i = threadIdx.x; i < kInt4Block / 16; i += kThreads)
+    reinterpret_cast<uint4*>(src)[i] = reinterpret_cast<const uint4*>(sblk)[i];
+  for (int i = threadIdx.x; i < kInt2Block / 16; i += kThreads)
+    reinterpret_cast<uint4*>(dst)[i] = make_uint4(0, 0, 0, 0);
   __syncthreads();
+  repack_image(src, dst, smax_bits);
+  __syncthreads();
+  for (int i = threadIdx.x; i < kInt2Block / 16; i += kThreads)
+    reinterpret_cast<uint4*>(dblk)[i] = reinterpret_cast<const uint4*>(dst)[i];
+}
+
+// One CTA per (direct job, kv head): 32 tokens that fill a fresh staging page
+// within one call.  The staging page's INT4 image is built in shared memory
+// exactly as the append kernel builds a new page (a warp per token), then
+// requantized to INT2 as the repack kernel does; only the INT2 block is
+// written to memory.
+__global__ void __launch_bounds__(kThreads) direct_int2_kernel(
+    uint8_t* __restrict__ pool, int hkv, const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
+    const DirectJob* __restrict__ jobs, const int32_t* __restrict__ toks, uint32_t* __restrict__ status) {
+  __shared__ __align__(16) uint8_t img[kInt4Block];
+  __shared__ __align__(16) uint8_t dst[kInt2Block];
+  const DirectJob job = jobs[blockIdx.x];
+  const int h = blockIdx.y;
+  for (int i = threadIdx.x; i < kInt4Block / 16; i += kThreads) reinterpret_cast<uint4*>(img)[i] = make_uint4(0, 0, 0, 0);
+  for (int i = threadIdx.x; i < kInt2Block / 16; i += kThreads) reinterpret_cast<uint4*>(dst)[i] = make_uint4(0, 0, 0, 0);
+  __syncthreads();
+  bool bad = false;
+  for (int j = threadIdx.x >> 5; j < kPage; j += kThreads / 32)
+    bad |= quantize_token(img, k, v, toks[job.tok_off + j], j, h, hkv, status);
+  if (bad) atomicOr(status, kStatusRange);
+  __syncthreads();
+  repack_image(img, dst, status + 1);
+  __syncthreads();
+  uint8_t* dblk = pool + ((size_t)job.dst * hkv + h) * kInt2Block;
   for (int i = threadIdx.x; i < kInt2Block / 16; i += kThreads)
     reinterpret_cast<uint4*>(dblk)[i] = reinterpret_cast<const uint4*>(dst)[i];
 }
@@ -272,6 +307,16 @@ cudaError_t launch_repack(kv_pool* P, const RepackJob* d_jobs, int n_jobs, cudaS
   ++P->launches;
   repack_int2_kernel<<<grid, kThreads, 0, s>>>(P->d_pool, P->int4_offset, P->cfg.n_int2_pages,
                                                P->cfg.num_kv_heads, d_jobs, P->d_status + 1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_direct_int2(kv_pool* P, const void* k, const void* v, const DirectJob* d_jobs, int n_jobs,
+                               const int32_t* d_toks, cudaStream_t s) {
+  if (n_jobs <= 0) return cudaSuccess;
+  dim3 grid((unsigned)n_jobs, (unsigned)P->cfg.num_kv_heads);
+  ++P->launches;
+  direct_int2_kernel<<<grid, kThreads, 0, s>>>(P->d_pool, P->cfg.num_kv_heads, (const __nv_bfloat16*)k,
+                                               (const __nv_bfloat16*)v, d_jobs, d_toks, P->d_status);
   return cudaGetLastError();
 }
 
