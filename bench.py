@@ -199,6 +199,59 @@ def run_reference(args):
     return 0
 
 
+def run_prefill(args):
+    """Prefill of the workload's prompts (16K-token append calls), inputs
+    resident in HBM: bf16 K and V rows read, page blocks written."""
+    import torch
+    import kvsynth
+    from mixed_precision_kv_gb300.workload import GPUWorkload
+    ws, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    w = kvsynth.make_workload(args.config)
+    H = w.num_kv_heads
+    chunk = 16384
+    times = []
+    for rep_i in range(args.warmup + args.steps):
+        gw = GPUWorkload(w, device=local, chunk=chunk)
+        calls = []
+        for r, spec in enumerate(w.requests):
+            for t0 in range(0, spec.n_prefill, chunk):
+                n = min(chunk, spec.n_prefill - t0)
+                k, v = gw.kv_rows(r, t0, n)
+                calls.append((k, v, np.full(n, gw.rids[r], np.int32), np.ascontiguousarray(gw.bits[r][t0:t0 + n])))
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for k, v, rid, b in calls:
+            gw.pool.append(k, v, rid, b)
+        e1.record()
+        torch.cuda.synchronize()
+        if rep_i >= args.warmup:
+            times.append(e0.elapsed_time(e1))
+        n_tok = sum(s.n_prefill for s in w.requests)
+        n_pages = sum(gw.pool.info(rid)[0] for rid in gw.rids)
+        n2 = sum(int((gw.pool.export(rid, content=False)["is_int2"] == 1).sum()) for rid in gw.rids)
+        del gw, calls
+        torch.cuda.empty_cache()
+    t_ms = float(np.median(times))
+    in_bytes = n_tok * H * 128 * 2 * 2
+    blk_bytes = (n2 * 3072 + (n_pages - n2) * 5120) * H
+    peak, peak_kind = measured_peak()
+    achieved = (in_bytes + blk_bytes) / (t_ms / 1e3) / 1e9
+    line = {"metric": "prefill quantization: bf16 K/V bytes in + page blocks out, GB/s", "value": achieved,
+            "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in, u4/u2 + f16 out",
+            "data": "synthetic",
+            "config": {"workload": w.name, "mode": "prefill", "tokens": n_tok, "num_kv_heads": H, "chunk": chunk,
+                       "tokens_per_s": n_tok / (t_ms / 1e3), "in_bytes": in_bytes, "out_bytes": blk_bytes},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": None, "peak_source": peak_kind,
+                         "kernel": "whole prefill (append, direct INT2, repack, table scatter; host routing)"}}
+    if rank == 0:
+        print(json.dumps(line))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -208,9 +261,14 @@ def main():
     ap.add_argument("--config", type=int, default=2)
     ap.add_argument("--decode-impl", default="auto", choices=["auto", "simt", "mma"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--mode", default="decode", choices=["decode", "prefill"],
+                    help="decode: the decode-step line (default); prefill: bulk quantization of the workload's "
+                         "prompts through kv_append_quant")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.mode == "prefill":
+        return run_prefill(args)
 
     import torch
     import kvsynth
