@@ -143,7 +143,8 @@ KVQ_API kv_status_t kv_decode_attn(kv_pool_t* pool, const void* q, const int32_t
  * reserved all memory up front), and latency-critical loops where a
  * cudaMalloc/cudaFree, which may synchronize the device, is not acceptable.
  * Same arguments, results and error rules as kv_decode_attn, except:
- *   - the split plan and split partials live in one fixed 8 MiB array inside
+ *   - the split plan, the per-unit q operands and the split partials live in
+ *     one fixed 64 MiB array inside
  *     the library (held on every GPU that loads it until the process exits)
  *     instead of pool buffers that grow with cudaMalloc;
  *   - batch x num_kv_heads must be <= 4096 and the plan must fit the array;

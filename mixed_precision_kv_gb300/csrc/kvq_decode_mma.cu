@@ -32,9 +32,19 @@
 //  * q is scaled by a power of two per head so that q * scale stays inside
 //    the binary16 range, and P by a power of two so that P * scale stays out
 //    of the subnormal range (the pool tracks the largest INT2 K and V scales).
+// Work layout: every warp is an independent worker.  The plan cuts all
+// (unit, page) pairs into one contiguous, equal-cost range per warp; a warp
+// walks its range across unit boundaries, writes one partial (m, l, acc) per
+// unit it touched and never waits for another warp.  The q fragments of a
+// unit are built once per call by frag_kernel and read through L1, so a unit
+// boundary costs a partial store, not a prologue.  One CTA of 16 warps per SM
+// (128 registers per thread): warps of one CTA are scheduled alike, so equal
+// costs give equal finish times.
 // Pages stream through a two-stage per-warp ring filled by cp.async.bulk with
-// mbarrier completion; every wait is bounded and reports a timeout status.
-// 4 CTAs of 4 warps per SM (128 registers per thread).
+// mbarrier completion; the ring runs across unit boundaries.  Every wait is
+// bounded and reports a timeout status.
+#include <algorithm>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -43,9 +53,8 @@
 namespace kvq {
 namespace {
 
-constexpr int kWarps = 4;
+constexpr int kWarps = kMmaWarpsPerCta;
 constexpr int kThreads = 32 * kWarps;
-constexpr int kCtasPerSm = 4;          // resident CTAs the register budget is sized for
 constexpr int kStages = 2;
 constexpr int kStageBytes = kInt4Block;
 constexpr int kPartStride = kHeadDim + 4;
@@ -57,29 +66,32 @@ constexpr uint32_t kC6 = 0x00C000C0u;   // 2-bit field at bit 6 of each half
 constexpr uint32_t kC8 = 0x03000300u;   // 2-bit field at bit 8 of each half
 constexpr float kCodeUnit = 262144.0f;  // 2^18: a field at bit 6 is code * 2^-18
 
-// Every warp's stages start on a 16-byte boundary (bulk-copy destinations and
-// 16-byte shared loads require it), whatever the stage count.
+// One warp's shared memory: its copy ring and its P staging buffer.  Every
+// stage starts on a 16-byte boundary (bulk-copy destinations and 16-byte
+// shared loads require it).
 struct alignas(16) WarpSmem {
   uint8_t stage[kStages][kStageBytes];
+  float pbuf[8][kPage];                // P [head][slot] of the current page; V zero terms at a flush
   unsigned long long bar[kStages];
 };
 static_assert(sizeof(WarpSmem) % 16 == 0 && kStageBytes % 16 == 0, "stage buffers must stay 16-byte aligned");
 
-struct CtaSmem {
-  WarpSmem warp[kWarps];
-  union {
-    float qraw[8][kHeadDim];           // q (fp32) of the packed heads: segment prologue only
-    float pbuf[kWarps][8][kPage];      // P staging per warp [head][slot]: page loop only
-  };
-  uint32_t qzh[8][kHeadDim / 2];       // 2^Ez q as binary16 pairs in the INT2 K scale/zero pair order
-  float qzs[8];                        // 2^(-Ez) * scale * log2(e)
+// q-side operands of one unit (batch row, kv head), built by frag_kernel.
+struct alignas(16) UnitFrag {
   uint4 bq2[4][32], bqn[4][32];        // INT2 K q fragments [word / 4][lane], negated copies (lo columns)
   uint4 bq4[4][32];                    // INT4 K q fragments
+  uint32_t qzh[8][kHeadDim / 2];       // 2^Ez q as binary16 pairs in the INT2 K scale/zero pair order
   float acol2[8], acol4[8];            // 2^(18 - E) * scale * log2(e) for INT2 / INT4 K pages
-  int eh2[8], eh4[8];                  // per-head power-of-two q scales E for INT2 / INT4 K pages
+  float qzs[8];                        // 2^(-Ez) * scale * log2(e)
   uint32_t bz[8][4];                   // fp16 pairs: hi(Q0,Q1), hi(Q2,Q3), lo(Q0,Q1), lo(Q2,Q3) of scale*log2(e)*Q_{h,group}
-  float zv[kWarps][4][8];              // V zero-term per warp [group][col]
-  float mw[kWarps][8], lw[kWarps][8];
+};
+static_assert(sizeof(UnitFrag) % 16 == 0, "unit fragments are copied as 16-byte words");
+
+// frag_kernel's shared memory
+struct FragSmem {
+  float qraw[8][kHeadDim];             // q (fp32) of the packed heads
+  int eh2[8], eh4[8];                  // per-head power-of-two q scales E for INT2 / INT4 K pages
+  UnitFrag f;
 };
 
 __device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -140,6 +152,8 @@ __device__ __forceinline__ float ex2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// x * 2^e for |e| <= 126, rounded once (as ldexpf): 2^e is a normal float
+__device__ __forceinline__ float pow2_scale(float x, int e) { return x * __int_as_float((e + 127) << 23); }
 __device__ __forceinline__ uint32_t comp(const uint4& v, int k) {
   return k == 0 ? v.x : (k == 1 ? v.y : (k == 2 ? v.z : v.w));
 }
@@ -195,7 +209,7 @@ __device__ __forceinline__ void qk_int4(const uint8_t* blk, const uint4* bq4, co
   uint32_t bq[16];
 #pragma unroll
   for (int x4 = 0; x4 < 4; ++x4) {
-    const uint4 b = bq4[x4 * 32 + lane];
+    const uint4 b = __ldg(&bq4[x4 * 32 + lane]);
     bq[4 * x4] = b.x; bq[4 * x4 + 1] = b.y; bq[4 * x4 + 2] = b.z; bq[4 * x4 + 3] = b.w;
   }
 #pragma unroll
@@ -266,9 +280,9 @@ __device__ __forceinline__ void qk_int4(const uint8_t* blk, const uint4* bq4, co
 
 // ---- logits of one INT2 page (same layout as qk_int4)
 template <int G>
-__device__ __forceinline__ void qk_int2(const uint8_t* blk, const uint4* bq2, const uint4* bqn,
-                                        const float (&acol)[Cols<G>::NH], const CtaSmem& S,
-                                        float (&lg)[2][2][Cols<G>::NH], float (&zc)[Cols<G>::NH]) {
+__device__ __forceinline__ void qk_int2(const uint8_t* blk, const UnitFrag* __restrict__ F,
+                                        const float (&acol)[Cols<G>::NH], float (&lg)[2][2][Cols<G>::NH],
+                                        float (&zc)[Cols<G>::NH]) {
   constexpr bool kPair = Cols<G>::kPair;
   const int lane = threadIdx.x & 31, r = lane >> 2, i = lane & 3;
   uint2 kw[2][2];
@@ -292,7 +306,7 @@ __device__ __forceinline__ void qk_int2(const uint8_t* blk, const uint4* bq2, co
     const int wi = kk >> 2, jj = kk & 3;
     const int p0 = wi * 8 + i2_reg6(jj), p1 = wi * 8 + i2_reg8(jj);
     const uint32_t s0 = comp(sv[p0 >> 2], p0 & 3), s1 = comp(sv[p1 >> 2], p1 & 3);
-    const uint4 qq = bq2[(kk >> 1) * 32 + lane], nq = bqn[(kk >> 1) * 32 + lane];
+    const uint4 qq = __ldg(&F->bq2[kk >> 1][lane]), nq = __ldg(&F->bqn[kk >> 1][lane]);
     const uint32_t q0 = (kk & 1) ? qq.z : qq.x, q1 = (kk & 1) ? qq.w : qq.y;
     const uint32_t n0 = (kk & 1) ? nq.z : nq.x, n1 = (kk & 1) ? nq.w : nq.y;
     // hi = rn(q s); lo = q s - hi (exact).  bqn holds -q where the lo part is
@@ -318,11 +332,11 @@ __device__ __forceinline__ void qk_int2(const uint8_t* blk, const uint4* bq2, co
     // lane (r, i) sums head i over scale/zero pairs 8r .. 8r+7; the lanes of
     // one head (r = 0..7) reduce, and every lane ends with its own head's Z
     const uint4* zs = reinterpret_cast<const uint4*>(blk + kI2KMeta + 256 + 32 * r);
-    const uint4* qs = reinterpret_cast<const uint4*>(&S.qzh[i][8 * r]);
+    const uint4* qs = reinterpret_cast<const uint4*>(&F->qzh[i][8 * r]);
     float zq[4] = {0.0f, 0.0f, 0.0f, 0.0f};   // independent partial sums
 #pragma unroll
     for (int x4 = 0; x4 < 2; ++x4) {
-      const uint4 zz = zs[x4], qz = qs[x4];
+      const uint4 zz = zs[x4], qz = __ldg(&qs[x4]);
       zq[0] = fma2_f16_f32(zz.x, qz.x, zq[0]);
       zq[1] = fma2_f16_f32(zz.y, qz.y, zq[1]);
       zq[2] = fma2_f16_f32(zz.z, qz.z, zq[2]);
@@ -332,7 +346,7 @@ __device__ __forceinline__ void qk_int2(const uint8_t* blk, const uint4* bq2, co
     zp += __shfl_xor_sync(0xFFFFFFFFu, zp, 4);
     zp += __shfl_xor_sync(0xFFFFFFFFu, zp, 8);
     zp += __shfl_xor_sync(0xFFFFFFFFu, zp, 16);
-    zc[0] = zp * S.qzs[i];
+    zc[0] = zp * __ldg(&F->qzs[i]);
 #pragma unroll
     for (int m = 0; m < 2; ++m)
 #pragma unroll
@@ -344,11 +358,11 @@ __device__ __forceinline__ void qk_int2(const uint8_t* blk, const uint4* bq2, co
     // lane (r, i) sums head r over chunk i; the 4 lanes of a head reduce and
     // the lanes of heads 2i, 2i+1 fetch theirs
     const uint4* zs = reinterpret_cast<const uint4*>(blk + kI2KMeta + 256 + 64 * i);
-    const uint4* qs = reinterpret_cast<const uint4*>(&S.qzh[r][i * 16]);
+    const uint4* qs = reinterpret_cast<const uint4*>(&F->qzh[r][i * 16]);
     float zq[4] = {0.0f, 0.0f, 0.0f, 0.0f};   // independent partial sums
 #pragma unroll
     for (int x4 = 0; x4 < 4; ++x4) {
-      const uint4 zz = zs[x4], qz = qs[x4];
+      const uint4 zz = zs[x4], qz = __ldg(&qs[x4]);
       zq[0] = fma2_f16_f32(zz.x, qz.x, zq[0]);
       zq[1] = fma2_f16_f32(zz.y, qz.y, zq[1]);
       zq[2] = fma2_f16_f32(zz.z, qz.z, zq[2]);
@@ -357,7 +371,7 @@ __device__ __forceinline__ void qk_int2(const uint8_t* blk, const uint4* bq2, co
     float zp = (zq[0] + zq[1]) + (zq[2] + zq[3]);
     zp += __shfl_xor_sync(0xFFFFFFFFu, zp, 1);
     zp += __shfl_xor_sync(0xFFFFFFFFu, zp, 2);
-    zp *= S.qzs[r];
+    zp *= __ldg(&F->qzs[r]);
     zc[0] = __shfl_sync(0xFFFFFFFFu, zp, 4 * (2 * i));
     zc[1] = __shfl_sync(0xFFFFFFFFu, zp, 4 * (2 * i + 1));
 #pragma unroll
@@ -545,12 +559,12 @@ __device__ __forceinline__ void softmax_pv(const uint8_t* blk, uint32_t live, fl
   __syncwarp();
 }
 
-// ---- q fragments (B operands of the K dot products), built once per segment
+// ---- q fragments (B operands of the K dot products), built once per unit
 // INT2 K word x = 2 kk + e of lane L: k-slots of a0/a1 (e = 0) hold the field
 // at bit 6, those of a2/a3 (e = 1) the field at bit 8 (factor 2^-2);
 // register 0 of the pair order has its halves swapped.
 template <int G>
-__device__ __forceinline__ uint32_t frag_q2(const CtaSmem& S, int L, int x) {
+__device__ __forceinline__ uint32_t frag_q2(const FragSmem& S, int L, int x) {
   const int r = L >> 2, i = L & 3;
   const int h = Cols<G>::kPair ? (r >> 1) : r;
   if (h >= G) return 0u;
@@ -559,13 +573,13 @@ __device__ __forceinline__ uint32_t frag_q2(const CtaSmem& S, int L, int x) {
   const int c = 4 * (8 * i + 4 * wi + (j >> 2)) + (j & 3);
   const int clo = j == 0 ? c + 8 : c, chi = j == 0 ? c : c + 8;
   const int ex = S.eh2[h] - 2 * e;
-  return pack_h2(ldexpf(S.qraw[h][clo], ex), ldexpf(S.qraw[h][chi], ex));
+  return pack_h2(pow2_scale(S.qraw[h][clo], ex), pow2_scale(S.qraw[h][chi], ex));
 }
 // INT4 K word x = 4 gr + 2 hf + e of lane L: nibbles (2hf + e, 2hf + e + 4)
 // of group gr's words; the bit-4 field (hf = 0, e = 1) carries 2^2.  With
 // paired columns, column 2h + part holds the groups of parity part.
 template <int G>
-__device__ __forceinline__ uint32_t frag_q4(const CtaSmem& S, int L, int x) {
+__device__ __forceinline__ uint32_t frag_q4(const FragSmem& S, int L, int x) {
   const int r = L >> 2, i = L & 3;
   const int gr = x >> 2, hf = (x >> 1) & 1, e = x & 1;
   if (Cols<G>::kPair && (gr & 1) != (r & 1)) return 0u;
@@ -573,227 +587,237 @@ __device__ __forceinline__ uint32_t frag_q4(const CtaSmem& S, int L, int x) {
   if (h >= G) return 0u;
   const int c = 32 * gr + 8 * i + 2 * hf + e;
   const int ex = S.eh4[h] + ((hf == 0 && e == 1) ? 2 : 0);
-  return pack_h2(ldexpf(S.qraw[h][c], ex), ldexpf(S.qraw[h][c + 4], ex));
+  return pack_h2(pow2_scale(S.qraw[h][c], ex), pow2_scale(S.qraw[h][c + 4], ex));
 }
 
-// Persistent scan: CTA b owns segments [cta_split[b], cta_split[b+1]), each a
-// page range of one unit; the ranges are cut so every CTA gets about the same
-// cost.  Pages of either precision may share a segment (precision is uniform
-// per page; the q fragments of both are built in the segment prologue).
+// ---- per-unit q operands: one CTA of 8 warps per unit (batch row, kv head).
+// It computes what the scan needs on the q side of a unit: the per-head
+// power-of-two scales, the mma B fragments of both K formats, the INT2 K
+// zero-term pairs and the INT4 K zero-term fragments.
 template <int G>
-__global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_mma_kernel(
+__global__ void __launch_bounds__(256) frag_kernel(const __nv_bfloat16* __restrict__ q, int hq, float scale_log2,
+                                                   const Unit* __restrict__ units,
+                                                   const uint32_t* __restrict__ smax_bits,
+                                                   UnitFrag* __restrict__ frags) {
+  constexpr bool kPair = Cols<G>::kPair;
+  __shared__ FragSmem S;
+  asm volatile("griddepcontrol.wait;" ::: "memory");   // the appends before this decode are done (scale maxima)
+  asm volatile("griddepcontrol.launch_dependents;");   // the scan may be staged
+  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+  const Unit u = units[blockIdx.x];
+  const float smax = fmaxf(__uint_as_float(smax_bits[0]), 1.0f);
+  {
+    // thread (h, 4 channels); q needs only its element alignment
+    const int h = tid >> 5, c = 4 * (tid & 31);
+    float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    if (h < G) {
+      const __nv_bfloat16* qh = q + ((size_t)u.b * hq + (size_t)u.kvh * G + h) * kHeadDim + c;
+      v = make_float4(__bfloat162float(qh[0]), __bfloat162float(qh[1]), __bfloat162float(qh[2]),
+                      __bfloat162float(qh[3]));
+    }
+    *reinterpret_cast<float4*>(&S.qraw[h][c]) = v;
+  }
+  __syncthreads();
+  {
+    const int h = w;
+    float mx = 0.0f, qg[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      qg[k] = S.qraw[h][lane + 32 * k];           // channel lane + 32k is in group k
+      mx = fmaxf(mx, fabsf(qg[k]));
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+#pragma unroll
+      for (int k = 0; k < 4; ++k) qg[k] += __shfl_xor_sync(0xFFFFFFFFu, qg[k], o);
+    }
+    if (lane == 0) {
+      int E2 = 0, E4 = 0;
+      if (mx > 0.0f) {
+        // INT2 K folds q * scale: |q * scale| * 2^E2 <= 2^14
+        E2 = max(-100, min(100, ilogbf(16384.0f / (mx * smax))));
+        // INT4 K: |q| * 2^E4 < 2^13 (q of the bit-4 fields carries another 2^2)
+        E4 = max(-100, min(100, 12 - ilogbf(mx)));
+      }
+      S.eh2[h] = E2;
+      S.eh4[h] = E4;
+      S.f.acol2[h] = pow2_scale(scale_log2, 18 - E2);
+      S.f.acol4[h] = pow2_scale(scale_log2, 18 - E4);
+      unsigned short hi[4], lo[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) split_f16(scale_log2 * qg[k], hi[k], lo[k]);
+      S.f.bz[h][0] = hi[0] | ((uint32_t)hi[1] << 16);
+      S.f.bz[h][1] = hi[2] | ((uint32_t)hi[3] << 16);
+      S.f.bz[h][2] = lo[0] | ((uint32_t)lo[1] << 16);
+      S.f.bz[h][3] = lo[2] | ((uint32_t)lo[3] << 16);
+    }
+    // q as binary16 pairs in the INT2 K scale/zero pair order for the zero
+    // term, scaled by 2^Ez so that max |q| lies in [2^14, 2^15)
+    const int Ez = mx > 0.0f ? max(-100, min(100, 14 - ilogbf(mx))) : 0;
+    for (int pr = lane; pr < kHeadDim / 2; pr += 32) {
+      const int j = pr & 7, iw = pr >> 3;        // iw = chunk i * 2 + word wi
+      const int c = 4 * (4 * iw + (j >> 2)) + (j & 3);
+      const int clo = j == 0 ? c + 8 : c, chi = j == 0 ? c : c + 8;   // pair 0 is stored swapped
+      S.f.qzh[h][pr] = pack_h2(pow2_scale(S.qraw[h][clo], Ez), pow2_scale(S.qraw[h][chi], Ez));
+    }
+    if (lane == 0) S.f.qzs[h] = pow2_scale(scale_log2, -Ez);
+  }
+  __syncthreads();
+  {
+    // q fragments of every lane: [x >> 2][lane][x & 3] for word x = 0..15
+    uint32_t* f2 = reinterpret_cast<uint32_t*>(&S.f.bq2[0][0]);
+    uint32_t* fn = reinterpret_cast<uint32_t*>(&S.f.bqn[0][0]);
+    uint32_t* f4 = reinterpret_cast<uint32_t*>(&S.f.bq4[0][0]);
+    for (int y = tid; y < 16 * 32; y += 256) {
+      const int x = 4 * (y >> 7) + (y & 3), L = (y >> 2) & 31;
+      const uint32_t v2 = frag_q2<G>(S, L, x);
+      f2[y] = v2;
+      // negated copy for the exact hi/lo split (g <= 4: lo columns only)
+      fn[y] = (!kPair || ((L >> 2) & 1)) ? (v2 ^ 0x80008000u) : 0u;
+      f4[y] = frag_q4<G>(S, L, x);
+    }
+  }
+  __syncthreads();
+  const uint4* src = reinterpret_cast<const uint4*>(&S.f);
+  uint4* dst = reinterpret_cast<uint4*>(frags + blockIdx.x);
+  for (int x = tid; x < (int)(sizeof(UnitFrag) / 16); x += 256) dst[x] = src[x];
+}
+
+// ---- persistent scan: warp gw = blockIdx.x * kWarps + w of the n_workers
+// workers owns the splits [wsplit[gw], wsplit[gw + 1]): contiguous page ranges
+// of consecutive units, cut so that every warp gets about the same cost.  The
+// warp writes one partial per split.
+template <int G>
+__global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(
     const uint8_t* __restrict__ pool, size_t int4_off, int64_t n2, int hkv, int max_pages,
-    const Entry* __restrict__ table, const __nv_bfloat16* __restrict__ q, int hq, float scale_log2,
-    const Unit* __restrict__ units, const Split* __restrict__ splits, const int32_t* __restrict__ cta_split,
-    const int32_t* __restrict__ ntab, float* __restrict__ part, const uint32_t* __restrict__ smax_bits,
-    uint32_t* __restrict__ status) {
+    const Entry* __restrict__ table, const UnitFrag* __restrict__ frags, const Split* __restrict__ splits,
+    const int32_t* __restrict__ wsplit, int n_workers, const int32_t* __restrict__ ntab, float* __restrict__ part,
+    const uint32_t* __restrict__ smax_bits, uint32_t* __restrict__ status) {
   constexpr bool kPair = Cols<G>::kPair;
   constexpr int NH = Cols<G>::NH;
   extern __shared__ __align__(128) uint8_t smem_raw[];
-  CtaSmem& S = *reinterpret_cast<CtaSmem*>(smem_raw);
-  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, r = lane >> 2, i = lane & 3;
-  WarpSmem& WS = S.warp[w];
-  asm volatile("griddepcontrol.wait;" ::: "memory");   // the appends before this decode are done
-  asm volatile("griddepcontrol.launch_dependents;");   // the merge may be scheduled as CTAs retire
-  if (lane == 0) {
-    for (int st = 0; st < kStages; ++st) bar_init(&WS.bar[st]);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  const float smax = fmaxf(__uint_as_float(smax_bits[0]), 1.0f);
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, r = lane >> 2, i = lane & 3;
+  WarpSmem& WS = reinterpret_cast<WarpSmem*>(smem_raw)[w];
+  // neighbouring workers share an SM: they scan the same one or two units, so
+  // the q operands they read stay in that SM's L1
+  const int gw = blockIdx.x * kWarps + w;
+  // the plan is copied in before the launch (not by a kernel): read it first
+  const int s_begin = gw < n_workers ? wsplit[gw] : 0, s_end = gw < n_workers ? wsplit[gw + 1] : 0;
+  asm volatile("griddepcontrol.wait;" ::: "memory");   // fragments, and the appends before them, are done
+  asm volatile("griddepcontrol.launch_dependents;");   // the merge may be staged
+  if (s_begin >= s_end) return;   // no CTA-wide barrier below: idle warps may leave
   // P is carried as p * 2^sv in the fp16 folds so that p * scale stays clear
   // of the binary16 subnormal range; 2^sv * (largest V scale) <= 2^15.
   const float vmax = fmaxf(__uint_as_float(smax_bits[1]), 1.0f / 1024.0f);
   const int sv = max(0, min(15, ilogbf(32768.0f / vmax)));
-  const float pscale = ldexpf(1.0f, sv);
-  uint32_t cnt = 0;   // bulk loads this warp has issued so far (all consumed at segment ends)
-  const int seg_end = cta_split[blockIdx.x + 1];
-  for (int sg = cta_split[blockIdx.x]; sg < seg_end; ++sg) {
-    const Split sp = splits[sg];
-    const Unit u = units[sp.unit];
-    __syncthreads();   // the previous segment's merge has finished reading shared memory
+  const float pscale = ldexpf(1.0f, sv), oscale = ldexpf(1.0f, -sv);
+  if (lane == 0) {
+    for (int st = 0; st < kStages; ++st) bar_init(&WS.bar[st]);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncwarp();
 
-    // ---- unit prologue: q of the packed heads, per-head power-of-two scales, fragments
-    for (int x = tid; x < 8 * kHeadDim; x += kThreads) {
-      const int h = x >> 7, c = x & (kHeadDim - 1);
-      S.qraw[h][c] = h < G ? __bfloat162float(q[((size_t)u.b * hq + (size_t)u.kvh * G + h) * kHeadDim + c]) : 0.0f;
+  // ---- the warp's page stream.  A ticket is one page: its table entry and
+  // tag = split << 6 | kv head (num_kv_heads <= 64); id < 0 ends the stream.
+  struct Ticket {
+    int32_t id;
+    uint32_t live;
+    int32_t tag;
+  };
+  // entry reader: split, scan-order walk (position so.p, end lend), kv head
+  int lsg = s_begin, lend = 0, lkvh = 0;
+  ScanOrder so;
+  const Entry* ltab = table;
+  auto enter = [&](int sg) {
+    const Split sp = splits[sg];
+    ltab = table + (size_t)sp.req * max_pages;
+    so.start(sp.page_begin, sp.n_pos, sp.n_lead);
+    lend = sp.page_end >= 0 ? sp.page_end : ntab[sp.req];   // open-ended: the table's length now
+    lkvh = sp.unit % hkv;
+  };
+  enter(lsg);
+  auto next_ticket = [&]() -> Ticket {
+    while (so.p >= lend) {
+      if (lsg + 1 >= s_end) return Ticket{-1, 0u, 0};
+      enter(++lsg);
     }
-    __syncthreads();
-    for (int h = w; h < 8; h += kWarps) {
-      float mx = 0.0f, qg[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        qg[k] = S.qraw[h][lane + 32 * k];           // channel lane + 32k is in group k
-        mx = fmaxf(mx, fabsf(qg[k]));
-      }
-#pragma unroll
-      for (int o = 16; o; o >>= 1) {
-        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
-#pragma unroll
-        for (int k = 0; k < 4; ++k) qg[k] += __shfl_xor_sync(0xFFFFFFFFu, qg[k], o);
-      }
-      if (lane == 0) {
-        int E2 = 0, E4 = 0;
-        if (mx > 0.0f) {
-          // INT2 K folds q * scale: |q * scale| * 2^E2 <= 2^14
-          E2 = max(-100, min(100, ilogbf(16384.0f / (mx * smax))));
-          // INT4 K: |q| * 2^E4 < 2^13 (q of the bit-4 fields carries another 2^2)
-          E4 = max(-100, min(100, 12 - ilogbf(mx)));
-        }
-        S.eh2[h] = E2;
-        S.eh4[h] = E4;
-        S.acol2[h] = ldexpf(scale_log2, 18 - E2);
-        S.acol4[h] = ldexpf(scale_log2, 18 - E4);
-        unsigned short hi[4], lo[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) split_f16(scale_log2 * qg[k], hi[k], lo[k]);
-        S.bz[h][0] = hi[0] | ((uint32_t)hi[1] << 16);
-        S.bz[h][1] = hi[2] | ((uint32_t)hi[3] << 16);
-        S.bz[h][2] = lo[0] | ((uint32_t)lo[1] << 16);
-        S.bz[h][3] = lo[2] | ((uint32_t)lo[3] << 16);
-      }
-      // q as binary16 pairs in the INT2 K scale/zero pair order for the zero
-      // term, scaled by 2^Ez so that max |q| lies in [2^14, 2^15)
-      const int Ez = mx > 0.0f ? max(-100, min(100, 14 - ilogbf(mx))) : 0;
-      for (int pr = lane; pr < kHeadDim / 2; pr += 32) {
-        const int j = pr & 7, iw = pr >> 3;        // iw = chunk i * 2 + word wi
-        const int c = 4 * (4 * iw + (j >> 2)) + (j & 3);
-        const int clo = j == 0 ? c + 8 : c, chi = j == 0 ? c : c + 8;   // pair 0 is stored swapped
-        S.qzh[h][pr] = pack_h2(ldexpf(S.qraw[h][clo], Ez), ldexpf(S.qraw[h][chi], Ez));
-      }
-      if (lane == 0) S.qzs[h] = ldexpf(scale_log2, -Ez);
-    }
-    __syncthreads();
-    {
-      // q fragments of every lane: [x >> 2][lane][x & 3] for word x = 0..15
-      uint32_t* f2 = reinterpret_cast<uint32_t*>(&S.bq2[0][0]);
-      uint32_t* fn = reinterpret_cast<uint32_t*>(&S.bqn[0][0]);
-      uint32_t* f4 = reinterpret_cast<uint32_t*>(&S.bq4[0][0]);
-      for (int y = tid; y < 16 * 32; y += kThreads) {
-        const int x = 4 * (y >> 7) + (y & 3), L = (y >> 2) & 31;
-        const uint32_t v2 = frag_q2<G>(S, L, x);
-        f2[y] = v2;
-        // negated copy for the exact hi/lo split (g <= 4: lo columns only)
-        fn[y] = (!kPair || ((L >> 2) & 1)) ? (v2 ^ 0x80008000u) : 0u;
-        f4[y] = frag_q4<G>(S, L, x);
-      }
-    }
-    __syncthreads();
-    uint32_t bz[2] = {0u, 0u};
-    {
-      // INT4 K zero term B fragment: column r; with paired columns only the
-      // even columns (part 0) carry Q
-      const int hb = kPair ? (r >> 1) : r;
-      if (hb < G && i < 2 && (!kPair || !(r & 1))) {
-        bz[0] = S.bz[hb][2 * i];
-        bz[1] = S.bz[hb][2 * i + 1];
-      }
-    }
-    float acol2[NH], acol4[NH];
+    const Entry e = ltab[so.next()];
+    return Ticket{e.id, e.live, (lsg << 6) | lkvh};
+  };
+  // copy number n goes to stage n & 1 and completes phase (n >> 1) & 1
+  auto issue = [&](const Ticket& t, uint32_t n) {   // lane 0
+    const int kvh = t.tag & 63;
+    const bool i2 = t.id < n2;
+    const uint8_t* src = i2 ? pool + ((size_t)t.id * hkv + kvh) * kInt2Block
+                            : pool + int4_off + ((size_t)(t.id - n2) * hkv + kvh) * kInt4Block;
+    const uint32_t st = n & (kStages - 1);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the stage was read generically
+    bulk_load(WS.stage[st], src, i2 ? (uint32_t)kInt2Block : (uint32_t)kInt4Block, &WS.bar[st]);
+  };
+  static_assert(kStages == 2, "the ticket ring below serves a two-stage copy ring");
+  Ticket t0 = next_ticket(), t1 = next_ticket(), t2 = next_ticket();   // pages c, c+1 (copies issued), c+2
+  if (lane == 0) {
+    if (t0.id >= 0) issue(t0, 0u);
+    if (t1.id >= 0) issue(t1, 1u);
+  }
+
+  // ---- state of the split being scanned
+  const UnitFrag* F = frags;
+  float acol2[NH], acol4[NH];
+  uint32_t bz[2];
+  float o[8][4], zv[4], mrun[NH], lsum[NH];
+  auto begin_split = [&](int sg) {
+    F = frags + splits[sg].unit;
 #pragma unroll
     for (int hh = 0; hh < NH; ++hh) {
       const int h = kPair ? i : 2 * i + hh;
-      acol2[hh] = S.acol2[h];
-      acol4[hh] = S.acol4[h];
-    }
-
-    // ---- page loop: two-stage bulk-copy ring per warp
-    const Entry* tab = table + (size_t)u.req * max_pages;
-    const int npg = (sp.page_end >= 0 ? sp.page_end : ntab[u.req]) - sp.page_begin;
-    const int nw = npg > w ? (npg - w + kWarps - 1) / kWarps : 0;
-    // Table entries of this warp's pages k, k+1, k+2 (all lanes hold the same
-    // 8 bytes): page k+2's copy is issued after page k is consumed, and the
-    // entry of page k+3 is read then, a page's compute ahead of its use.
-    static_assert(kStages == 2, "the entry ring below serves a two-stage copy ring");
-    auto ent_load = [&](int k) { return k < nw ? tab[sp.page_begin + w + k * kWarps] : Entry{0, 0u}; };
-    Entry ent0 = ent_load(0), ent1 = ent_load(1), ent2 = ent_load(2);   // registers, rotated per page
-    auto issue = [&](int k, const Entry& en) {
-      const bool i2 = en.id < n2;
-      const uint8_t* src = i2 ? pool + ((size_t)en.id * hkv + u.kvh) * kInt2Block
-                              : pool + int4_off + ((size_t)(en.id - n2) * hkv + u.kvh) * kInt4Block;
-      const uint32_t st = (cnt + (uint32_t)k) & (kStages - 1);
-      bulk_load(WS.stage[st], src, i2 ? (uint32_t)kInt2Block : (uint32_t)kInt4Block, &WS.bar[st]);
-    };
-    if (lane == 0) {
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // stages were read/written generically
-      if (nw > 0) issue(0, ent0);
-      if (nw > 1) issue(1, ent1);
-    }
-    float o[8][4], zv[4] = {0.0f, 0.0f, 0.0f, 0.0f}, mrun[NH], lsum[NH];
-#pragma unroll
-    for (int hh = 0; hh < NH; ++hh) {
+      acol2[hh] = __ldg(&F->acol2[h]);
+      acol4[hh] = __ldg(&F->acol4[h]);
       mrun[hh] = -INFINITY;
       lsum[hh] = 0.0f;
     }
+    // INT4 K zero term B fragment: column r; with paired columns only the
+    // even columns (part 0) carry Q
+    const int hb = kPair ? (r >> 1) : r;
+    const bool has = hb < G && i < 2 && (!kPair || !(r & 1));
+    bz[0] = has ? __ldg(&F->bz[hb][2 * i]) : 0u;
+    bz[1] = has ? __ldg(&F->bz[hb][2 * i + 1]) : 0u;
 #pragma unroll
     for (int m = 0; m < 8; ++m) o[m][0] = o[m][1] = o[m][2] = o[m][3] = 0.0f;
-    int k = 0;
-    bool ok = true;
-    for (; k < nw; ++k) {
-      const uint32_t c = cnt + (uint32_t)k;
-      const uint32_t st = c & (kStages - 1);
-      const bool got = bar_wait(&WS.bar[st], (c / kStages) & 1u);
-      if (!__all_sync(0xFFFFFFFFu, got)) { ok = false; break; }
-      const Entry e = ent0;
-      const uint8_t* blk = WS.stage[st];
-      float lg[2][2][NH], zc[NH];
-      if (e.id < n2) {
-        qk_int2<G>(blk, &S.bq2[0][0], &S.bqn[0][0], acol2, S, lg, zc);
-        softmax_pv<G, true>(blk, e.live, pscale, lg, zc, o, zv, mrun, lsum, S.pbuf[w]);
-      } else {
-        qk_int4<G>(blk, &S.bq4[0][0], bz, acol4, lg);
-#pragma unroll
-        for (int hh = 0; hh < NH; ++hh) zc[hh] = 0.0f;
-        softmax_pv<G, false>(blk, e.live, pscale, lg, zc, o, zv, mrun, lsum, S.pbuf[w]);
-      }
-      if (k + kStages < nw && lane == 0) {
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        issue(k + kStages, ent2);
-      }
-      ent0 = ent1;
-      ent1 = ent2;
-      ent2 = ent_load(k + 3);
-    }
-    if (!ok) {
-      if (lane == 0) atomicOr(status, kStatusTimeout);
-      const int issued = nw < k + kStages ? nw : k + kStages;
-      for (int kk = k; kk < issued; ++kk) {
-        const uint32_t c = cnt + (uint32_t)kk;
-        bar_wait(&WS.bar[c & (kStages - 1)], (c / kStages) & 1u);
-      }
-#pragma unroll
-      for (int hh = 0; hh < NH; ++hh) mrun[hh] = -INFINITY;
-    }
-    cnt += (uint32_t)nw;
-
-    // ---- per-warp epilogue: finish l, combine the column parts, add the V zero term
+    zv[0] = zv[1] = zv[2] = zv[3] = 0.0f;
+  };
+  // partial of split sg: finish l, combine the column parts, add the V zero term
+  auto flush = [&](int sg) {
 #pragma unroll
     for (int hh = 0; hh < NH; ++hh) {
       lsum[hh] += __shfl_xor_sync(0xFFFFFFFFu, lsum[hh], 4);
       lsum[hh] += __shfl_xor_sync(0xFFFFFFFFu, lsum[hh], 8);
       lsum[hh] += __shfl_xor_sync(0xFFFFFFFFu, lsum[hh], 16);
     }
+    float* zb = &WS.pbuf[0][0];   // [group][column]
+    __syncwarp();
     if (r < 4) {
       if (kPair) {
-        S.zv[w][r][i] = zv[0] + zv[1];
+        zb[r * 8 + i] = zv[0] + zv[1];
       } else {
-        S.zv[w][r][2 * i] = zv[0];
-        S.zv[w][r][2 * i + 1] = zv[1];
+        zb[r * 8 + 2 * i] = zv[0];
+        zb[r * 8 + 2 * i + 1] = zv[1];
       }
     }
     __syncwarp();
-    float* accw = reinterpret_cast<float*>(WS.stage[0]);   // [8][128], the ring is idle now
-    const float oscale = ldexpf(1.0f, -sv);
+    float* out = part + (size_t)sg * G * kPartStride;
     if constexpr (kPair) {
       if (i < G) {
 #pragma unroll
         for (int m = 0; m < 8; ++m) {
-          const float zt = S.zv[w][m >> 1][i];
-          accw[i * kHeadDim + 16 * m + r] = fmaf(o[m][0] + o[m][1], kCodeUnit, zt) * oscale;
-          accw[i * kHeadDim + 16 * m + r + 8] = fmaf(o[m][2] + o[m][3], kCodeUnit, zt) * oscale;
+          const float zt = zb[(m >> 1) * 8 + i];
+          out[i * kPartStride + 16 * m + r] = fmaf(o[m][0] + o[m][1], kCodeUnit, zt) * oscale;
+          out[i * kPartStride + 16 * m + r + 8] = fmaf(o[m][2] + o[m][3], kCodeUnit, zt) * oscale;
         }
         if (r == 0) {
-          S.mw[w][i] = mrun[0];
-          S.lw[w][i] = lsum[0];
+          out[i * kPartStride + kHeadDim] = mrun[0];
+          out[i * kPartStride + kHeadDim + 1] = lsum[0];
         }
       }
     } else {
@@ -802,108 +826,163 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_mma_kernel(
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
           const int h = 2 * i + (cc & 1), ch = 16 * m + r + 8 * (cc >> 1);
-          if (h < G) accw[h * kHeadDim + ch] = fmaf(o[m][cc], kCodeUnit, S.zv[w][m >> 1][h]) * oscale;
+          if (h < G) out[h * kPartStride + ch] = fmaf(o[m][cc], kCodeUnit, zb[(m >> 1) * 8 + h]) * oscale;
         }
       if (r == 0)
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh)
           if (2 * i + hh < G) {
-            S.mw[w][2 * i + hh] = mrun[hh];
-            S.lw[w][2 * i + hh] = lsum[hh];
+            out[(2 * i + hh) * kPartStride + kHeadDim] = mrun[hh];
+            out[(2 * i + hh) * kPartStride + kHeadDim + 1] = lsum[hh];
           }
     }
-    const bool all_ok = __syncthreads_and(ok) != 0;
-
-    // ---- merge the warps: one thread per channel
+    __syncwarp();   // zb is P staging again for the next page
+  };
+  // partial of a split that adds nothing (no page scanned, or a timed-out scan)
+  auto flush_empty = [&](int sg) {
     float* out = part + (size_t)sg * G * kPartStride;
-    const int ch = tid;
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      float M = -INFINITY;
-#pragma unroll
-      for (int ww = 0; ww < kWarps; ++ww) M = fmaxf(M, S.mw[ww][h]);
-      float L = 0.0f, A = 0.0f;
-#pragma unroll
-      for (int ww = 0; ww < kWarps; ++ww) {
-        const float mw = S.mw[ww][h];
-        if (mw == -INFINITY) continue;
-        const float f = ex2(mw - M);
-        L += S.lw[ww][h] * f;
-        A += reinterpret_cast<const float*>(S.warp[ww].stage[0])[h * kHeadDim + ch] * f;
-      }
-      out[h * kPartStride + ch] = A;
-      if (ch == 0) {
-        out[h * kPartStride + kHeadDim] = M;
-        out[h * kPartStride + kHeadDim + 1] = L;
-      }
+    for (int x = lane; x < G * kPartStride; x += 32) out[x] = (x % kPartStride) == kHeadDim ? -INFINITY : 0.0f;
+  };
+
+  // ---- page loop
+  int csg = -1;        // split being scanned
+  uint32_t c = 0;      // copies consumed
+  bool ok = true;
+  while (t0.id >= 0) {
+    const int sg = t0.tag >> 6;
+    if (sg != csg) {
+      if (csg >= 0) flush(csg);
+      for (int x = csg < 0 ? s_begin : csg + 1; x < sg; ++x) flush_empty(x);
+      csg = sg;
+      begin_split(sg);
     }
-    if (!all_ok) break;
+    const uint32_t st = c & (kStages - 1);
+    const bool got = bar_wait(&WS.bar[st], (c >> 1) & 1u);
+    if (!__all_sync(0xFFFFFFFFu, got)) {
+      ok = false;
+      break;
+    }
+    const uint8_t* blk = WS.stage[st];
+    float lg[2][2][NH], zc[NH];
+    if (t0.id < n2) {
+      qk_int2<G>(blk, F, acol2, lg, zc);
+      softmax_pv<G, true>(blk, t0.live, pscale, lg, zc, o, zv, mrun, lsum, WS.pbuf);
+    } else {
+      qk_int4<G>(blk, &F->bq4[0][0], bz, acol4, lg);
+#pragma unroll
+      for (int hh = 0; hh < NH; ++hh) zc[hh] = 0.0f;
+      softmax_pv<G, false>(blk, t0.live, pscale, lg, zc, o, zv, mrun, lsum, WS.pbuf);
+    }
+    ++c;
+    if (t2.id >= 0 && lane == 0) issue(t2, c + 1);
+    t0 = t1;
+    t1 = t2;
+    t2 = next_ticket();
   }
+  if (!ok) {
+    if (lane == 0) atomicOr(status, kStatusTimeout);
+    // let the copies in flight land before the warp leaves
+    if (t0.id >= 0) bar_wait(&WS.bar[c & (kStages - 1)], (c >> 1) & 1u);
+    if (t1.id >= 0) bar_wait(&WS.bar[(c + 1) & (kStages - 1)], ((c + 1) >> 1) & 1u);
+    for (int x = csg; x < s_end; ++x) flush_empty(x);
+    return;
+  }
+  if (csg >= 0) flush(csg);
+  for (int x = csg < 0 ? s_begin : csg + 1; x < s_end; ++x) flush_empty(x);
+}
+
+constexpr int kScanSmem = kWarps * (int)sizeof(WarpSmem);
+
+// The scan reads its q operands and its spilled registers through L1, which
+// shares the SM's memory with shared memory: ask for the smallest shared
+// carveout that holds one CTA (the default takes the largest, leaving L1 too
+// small for 16 warps' q operands; the scan then ran up to 1.45x slower).
+template <int G>
+cudaError_t set_scan_attributes() {
+  cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, kScanSmem);
+  if (e != cudaSuccess) return e;
+  int dev = 0, per_sm = 0, reserved = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev)) != cudaSuccess) return e;
+  if (per_sm <= 0) return cudaErrorInvalidValue;
+  const int pct = std::min(100, (int)(((int64_t)(kScanSmem + reserved) * 100 + per_sm - 1) / per_sm));
+  return cudaFuncSetAttribute(decode_mma_kernel<G>, cudaFuncAttributePreferredSharedMemoryCarveout, pct);
 }
 
 template <int G>
-cudaError_t launch_mma_g(kv_pool* P, const void* q, int32_t hq, float scale_log2, const Unit* d_units,
-                         const Split* d_splits, const int32_t* d_cta, int n_ctas, float* d_part, cudaStream_t s) {
+cudaError_t launch_mma_g(kv_pool* P, const void* q, int32_t hq, float scale_log2, const Unit* d_units, int n_units,
+                         const Split* d_splits, const int32_t* d_wsplit, int n_workers, void* d_frags, float* d_part,
+                         cudaStream_t s) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)sizeof(CtaSmem));
+    const cudaError_t e = set_scan_attributes<G>();
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  if (n_ctas <= 0) return cudaSuccess;
-  ++P->launches;
+  if (n_workers <= 0 || n_units <= 0) return cudaSuccess;
   const uint32_t* smax = P->d_status + 1;
-  return launch_pdl(decode_mma_kernel<G>, dim3((unsigned)n_ctas), dim3(kThreads), sizeof(CtaSmem), s,
+  P->launches += 2;
+  cudaError_t e = launch_pdl(frag_kernel<G>, dim3((unsigned)n_units), dim3(256), 0, s, (const __nv_bfloat16*)q,
+                             (int)hq, scale_log2, d_units, smax, (UnitFrag*)d_frags);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = (unsigned)((n_workers + kWarps - 1) / kWarps);
+  return launch_pdl(decode_mma_kernel<G>, dim3(grid), dim3(kThreads), (size_t)kScanSmem, s,
                     (const uint8_t*)P->d_pool, P->int4_offset, (int64_t)P->cfg.n_int2_pages, P->cfg.num_kv_heads,
-                    P->cfg.max_pages_per_request, (const Entry*)P->d_table, (const __nv_bfloat16*)q, (int)hq,
-                    scale_log2, d_units, d_splits, d_cta, (const int32_t*)P->d_ntab, d_part, smax, P->d_status);
+                    P->cfg.max_pages_per_request, (const Entry*)P->d_table, (const UnitFrag*)d_frags, d_splits,
+                    d_wsplit, n_workers, (const int32_t*)P->d_ntab, d_part, smax, P->d_status);
 }
 
 template <int G>
 int mma_occupancy() {
   int n = 0;
-  if (cudaFuncSetAttribute(decode_mma_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(CtaSmem)) !=
-      cudaSuccess)
-    return 1;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<G>, kThreads, sizeof(CtaSmem)) != cudaSuccess)
+  if (set_scan_attributes<G>() != cudaSuccess) return 1;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<G>, kThreads, kScanSmem) != cudaSuccess)
     return 1;
   return n > 0 ? n : 1;
 }
 
 }  // namespace
 
+size_t decode_mma_frag_bytes() { return sizeof(UnitFrag); }
+
 cudaError_t launch_decode_mma(kv_pool* P, const void* q, int32_t hq, float scale_log2, const Unit* d_units, int n_units,
-                              const Split* d_splits, const int32_t* d_cta, int n_ctas, float* d_part, float* out,
-                              cudaStream_t s) {
+                              const Split* d_splits, const int32_t* d_wsplit, int n_workers, void* d_frags,
+                              float* d_part, float* out, cudaStream_t s) {
   cudaError_t e;
+#define KVQ_MMA_CASE(g)                                                                                          \
+  case g:                                                                                                        \
+    e = launch_mma_g<g>(P, q, hq, scale_log2, d_units, n_units, d_splits, d_wsplit, n_workers, d_frags, d_part, s); \
+    break;
   switch (hq / P->cfg.num_kv_heads) {
-    case 1: e = launch_mma_g<1>(P, q, hq, scale_log2, d_units, d_splits, d_cta, n_ctas, d_part, s); break;
-    case 2: e = launch_mma_g<2>(P, q, hq, scale_log2, d_units, d_splits, d_cta, n_ctas, d_part, s); break;
-    case 3: e = launch_mma_g<3>(P, q, hq, scale_log2, d_units, d_splits, d_cta, n_ctas, d_part, s); break;
-    case 4: e = launch_mma_g<4>(P, q, hq, scale_log2, d_units, d_splits, d_cta, n_ctas, d_part, s); break;
-    case 5: e = launch_mma_g<5>(P, q, hq, scale_log2, d_units, d_splits, d_cta, n_ctas, d_part, s); break;
-    case 6: e = launch_mma_g<6>(P, q, hq, scale_log2, d_units, d_splits, d_cta, n_ctas, d_part, s); break;
-    case 7: e = launch_mma_g<7>(P, q, hq, scale_log2, d_units, d_splits, d_cta, n_ctas, d_part, s); break;
-    case 8: e = launch_mma_g<8>(P, q, hq, scale_log2, d_units, d_splits, d_cta, n_ctas, d_part, s); break;
+    KVQ_MMA_CASE(1)
+    KVQ_MMA_CASE(2)
+    KVQ_MMA_CASE(3)
+    KVQ_MMA_CASE(4)
+    KVQ_MMA_CASE(5)
+    KVQ_MMA_CASE(6)
+    KVQ_MMA_CASE(7)
+    KVQ_MMA_CASE(8)
     default: return cudaErrorInvalidValue;
   }
+#undef KVQ_MMA_CASE
   if (e != cudaSuccess) return e;
   if (P->merge_event && (e = cudaEventRecord(P->merge_event, s)) != cudaSuccess) return e;
   return launch_merge(P, hq / P->cfg.num_kv_heads, d_units, n_units, d_part, hq, out, s);
 }
 
-int decode_mma_ctas_per_sm(int g) {
+int decode_mma_workers_per_sm(int g) {
   switch (g) {
-    case 1: return mma_occupancy<1>();
-    case 2: return mma_occupancy<2>();
-    case 3: return mma_occupancy<3>();
-    case 4: return mma_occupancy<4>();
-    case 5: return mma_occupancy<5>();
-    case 6: return mma_occupancy<6>();
-    case 7: return mma_occupancy<7>();
-    default: return mma_occupancy<8>();
+    case 1: return kWarps * mma_occupancy<1>();
+    case 2: return kWarps * mma_occupancy<2>();
+    case 3: return kWarps * mma_occupancy<3>();
+    case 4: return kWarps * mma_occupancy<4>();
+    case 5: return kWarps * mma_occupancy<5>();
+    case 6: return kWarps * mma_occupancy<6>();
+    case 7: return kWarps * mma_occupancy<7>();
+    default: return kWarps * mma_occupancy<8>();
   }
 }
 
 }  // namespace kvq
+

@@ -176,48 +176,63 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(
   }
 }
 
-// One warp per (unit, head): O = sum_s acc_s 2^(m_s - M) / sum_s l_s 2^(m_s - M).
-// Lanes first take the splits' m in parallel (warp max), then every lane
-// weighs its four channels of each split; the split loads are independent so
-// they overlap instead of forming a dependent chain.
+// One CTA of 4 warps per (unit, head): O = sum_s acc_s 2^(m_s - M) / sum_s
+// l_s 2^(m_s - M).  The block first takes the largest m over the unit's
+// splits, then warp w weighs splits w, w + 4, ... (each lane four channels)
+// and the four warps' sums are added in shared memory.  A unit may have tens
+// of splits (one per warp of the tensor-core scan that touched it); spreading
+// them over four warps keeps the dependent load rounds few.
 template <int G>
-__global__ void merge_kernel(const Unit* __restrict__ units, const float* __restrict__ part, int hq,
-                             float* __restrict__ out) {
+__global__ void __launch_bounds__(128) merge_kernel(const Unit* __restrict__ units, const float* __restrict__ part,
+                                                    int hq, float* __restrict__ out) {
   // Launched as a programmatic dependent of the scan: wait until the scan grid
   // has completed and its partials are visible (immediate for a plain launch).
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");   // the next call's kernels may be staged
-  const Unit u = units[blockIdx.x];
-  const int h = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float* o = out + ((size_t)u.b * hq + (size_t)u.kvh * G + h) * kHeadDim + 4 * lane;
-  const float* base = part + ((size_t)u.split_begin * G + h) * kPartStride;
+  __shared__ float red[4], lpart[4];
+  __shared__ float4 apart[4][32];
+  const int ui = blockIdx.x / G, h = blockIdx.x - ui * G;
+  const Unit u = units[ui];
+  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
   const size_t rs = (size_t)G * kPartStride;          // stride between splits
+  const float* base = part + ((size_t)u.split_begin * G + h) * kPartStride;
   const int n = u.n_splits;
   float M = -INFINITY;
-  for (int s = lane; s < n; s += 32) M = fmaxf(M, base[s * rs + kHeadDim]);
+  for (int s = tid; s < n; s += 128) M = fmaxf(M, base[s * rs + kHeadDim]);
 #pragma unroll
   for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, off));
-  float L = 0.0f, A0 = 0.0f, A1 = 0.0f, A2 = 0.0f, A3 = 0.0f;
-  for (int s0 = 0; s0 < n; s0 += 32) {
-    const int s = s0 + lane;
-    float f = 0.0f;
-    if (s < n) {
-      const float m = base[s * rs + kHeadDim];
-      f = m == -INFINITY ? 0.0f : exp2f(m - M);   // an empty split adds nothing
-      L += f * base[s * rs + kHeadDim + 1];
-    }
-    const int cnt = min(32, n - s0);
+  if (lane == 0) red[w] = M;
+  __syncthreads();
+  M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  float L = 0.0f;
+  float4 A = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll 4
-    for (int j = 0; j < cnt; ++j) {
-      const float fj = __shfl_sync(0xFFFFFFFFu, f, j);
-      const float4 a = *reinterpret_cast<const float4*>(base + (size_t)(s0 + j) * rs + 4 * lane);
-      A0 = fmaf(a.x, fj, A0); A1 = fmaf(a.y, fj, A1); A2 = fmaf(a.z, fj, A2); A3 = fmaf(a.w, fj, A3);
-    }
+  for (int s = w; s < n; s += 4) {
+    const float* ps = base + (size_t)s * rs;
+    const float m = ps[kHeadDim];
+    const float4 a = *reinterpret_cast<const float4*>(ps + 4 * lane);
+    const float f = m == -INFINITY ? 0.0f : exp2f(m - M);   // an empty split adds nothing
+    L = fmaf(f, ps[kHeadDim + 1], L);
+    A.x = fmaf(a.x, f, A.x);
+    A.y = fmaf(a.y, f, A.y);
+    A.z = fmaf(a.z, f, A.z);
+    A.w = fmaf(a.w, f, A.w);
   }
+  apart[w][lane] = A;
+  if (lane == 0) lpart[w] = L;
+  __syncthreads();
+  if (w == 0) {
+    float4 t = apart[0][lane];
 #pragma unroll
-  for (int off = 16; off; off >>= 1) L += __shfl_xor_sync(0xFFFFFFFFu, L, off);
-  const float inv = L > 0.0f ? 1.0f / L : 0.0f;
-  *reinterpret_cast<float4*>(o) = make_float4(A0 * inv, A1 * inv, A2 * inv, A3 * inv);
+    for (int k = 1; k < 4; ++k) {
+      const float4 b = apart[k][lane];
+      t.x += b.x; t.y += b.y; t.z += b.z; t.w += b.w;
+    }
+    const float Lt = (lpart[0] + lpart[1]) + (lpart[2] + lpart[3]);
+    const float inv = Lt > 0.0f ? 1.0f / Lt : 0.0f;
+    float* o = out + ((size_t)u.b * hq + (size_t)u.kvh * G + h) * kHeadDim + 4 * lane;
+    *reinterpret_cast<float4*>(o) = make_float4(t.x * inv, t.y * inv, t.z * inv, t.w * inv);
+  }
 }
 
 template <int G>
@@ -251,8 +266,8 @@ cudaError_t launch_merge(kv_pool* P, int g, const Unit* d_units, int n_units, co
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)n_units);
-  cfg.blockDim = dim3((unsigned)(32 * g));
+  cfg.gridDim = dim3((unsigned)(n_units * g));
+  cfg.blockDim = dim3(128u);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
   cfg.attrs = attr;

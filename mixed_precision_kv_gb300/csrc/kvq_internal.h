@@ -74,35 +74,74 @@ struct Unit {
   int32_t pad[3];
 };
 
-// A split: a page range of one unit, scanned by one CTA.  A CTA scans the
-// contiguous split range [cta_split[cta], cta_split[cta + 1]).
+// A split: a range of one unit's pages in scan order, scanned by one worker
+// (a CTA of the CUDA-core scan, a warp of the tensor-core scan).  Worker k
+// scans the contiguous split range [cta_split[k], cta_split[k + 1]).
 struct Split {
   int32_t unit;
-  int32_t page_begin;   // table index range [page_begin, page_end)
+  int32_t page_begin;   // scan-order position range [page_begin, page_end)
   int32_t page_end;     // < 0: to the end of the request's table (its device length at launch)
-  int32_t cta;
+  int32_t req;          // request id of the unit
+  int32_t n_pos;        // the unit's table length when planned
+  int32_t n_lead;       // leading table entries spread evenly through the scan order (0: table order)
+  int32_t pad[2];
+};
+
+// Scan order of a unit: position p < n visits table index
+//   lead  floor(p m / n)                 if floor((p+1) m / n) > floor(p m / n)
+//   tail  m + p - floor((p+1) m / n)     otherwise,
+// a bijection of [0, n) that spreads the m leading entries (the INT2 pages of
+// a table sorted INT2-first) evenly among the others, so that every position
+// range holds both precisions in the table's proportion; positions >= n
+// (pages appended after planning) visit themselves.  Walked incrementally:
+// a = floor(p m / n), rem = p m mod n.
+struct ScanOrder {
+  int32_t p, n, m, a, rem;
+  __host__ __device__ void start(int32_t p0, int32_t n_, int32_t m_) {
+    p = p0;
+    n = n_;
+    m = m_;
+    const int64_t pm = (int64_t)p0 * m_;
+    a = (n_ > 0 && p0 < n_) ? (int32_t)(pm / n_) : 0;
+    rem = (n_ > 0 && p0 < n_) ? (int32_t)(pm % n_) : 0;
+  }
+  __host__ __device__ int32_t next() {   // table index of position p, then p + 1
+    int32_t idx = p;
+    if (p < n) {
+      rem += m;
+      if (rem >= n) {
+        rem -= n;
+        idx = a++;
+      } else {
+        idx = m + (p - a);
+      }
+    }
+    ++p;
+    return idx;
+  }
 };
 
 // Planner cost of one page by precision, proportional to the scan kernel's
-// time per page.  The tensor-core scan is bound by instruction issue, not by
-// bytes: an INT2 page takes the same time as an INT4 page for g <= 4 and
-// 1.1x for g > 4 (all-INT2 vs all-INT4 pools of the 32K-token batch-8 and
-// 100K-token batch-16 steps); the CUDA-core scan is charged its block bytes
-// plus 2048.
+// time per page.  In the tensor-core scan an INT2 page costs more issue
+// slots than an INT4 page: fitted to per-warp scan times of the 32K-token
+// batch-8 (g = 4) and 100K-token batch-16 (g = 8) steps, an INT2 page takes
+// 1.18x and 1.5x an INT4 page.  The CUDA-core scan is charged its block
+// bytes plus 2048.
 struct PageCost {
   double int2, int4;
 };
-inline PageCost mma_page_cost(int g) { return g <= 4 ? PageCost{1.00, 1.00} : PageCost{1.10, 1.00}; }
+inline PageCost mma_page_cost(int g) { return g <= 4 ? PageCost{1.18, 1.00} : PageCost{1.50, 1.00}; }
 constexpr PageCost kSimtPageCost{3072.0 + 2048.0, 5120.0 + 2048.0};
-constexpr int64_t kMinPagesPerCta = 16;
+constexpr int64_t kMinPagesPerCta = 16;    // CUDA-core scan: pages per CTA at least
+constexpr int64_t kMinPagesPerWarp = 4;    // tensor-core scan: pages per warp at least
 constexpr int64_t kTimingRing = 2048;
 
 // Decode plan on the host (see plan_decode).
 struct HostPlan {
   std::vector<Unit> units;
   std::vector<Split> splits;
-  std::vector<int32_t> cta_split;   // n_ctas + 1 entries
-  int64_t n_ctas() const { return (int64_t)cta_split.size() - 1; }
+  std::vector<int32_t> cta_split;   // n_workers + 1 entries
+  int64_t n_ctas() const { return (int64_t)cta_split.size() - 1; }   // workers
 };
 
 struct Request {
@@ -111,6 +150,7 @@ struct Request {
   int32_t tail4 = -1, staging = -1;
   std::vector<uint32_t> loc;        // token position -> page_id << 5 | slot
   uint64_t version = 0;             // bumped whenever the table's entries change
+  uint64_t ordered_version = ~0ull; // version at which the table was last seen INT2-first
 };
 
 // Free page ids of one class, handed out lowest id first (a bitset with a
@@ -169,8 +209,20 @@ struct kv_pool {
   int32_t* d_ntab = nullptr;          // [max_requests]
   uint32_t* d_status = nullptr;       // [0] status bits, [1] largest INT2 K scale, [2] largest V scale (fp32 bits)
   kvq::DevBuf upload;                 // append/scatter job arrays
+  // pinned host staging of host-to-device copies (a ring: a slot is reused
+  // once the copy recorded on its event has run)
+  struct PinnedSlot {
+    void* ptr = nullptr;
+    size_t cap = 0;
+    cudaEvent_t ev = nullptr;
+    bool pending = false;
+  };
+  static constexpr int kPinnedSlots = 4;
+  PinnedSlot pinned[kPinnedSlots];
+  int pinned_next = 0;
   kvq::DevBuf plan;                   // decode plan (units, splits)
   kvq::DevBuf partials;               // decode split partials
+  kvq::DevBuf frags;                  // per-unit q operands of the tensor-core scan
   // host mirror
   std::vector<kvq::Request> reqs;
   std::vector<uint8_t> fill;          // per page id
@@ -235,20 +287,26 @@ cudaError_t launch_direct_int2(kv_pool* P, const void* k, const void* v, const D
 cudaError_t launch_scatter(kv_pool* P, const TableUpd* d_upd, int n, cudaStream_t s);
 
 // Balanced decode plan: units (batch row, kv head) in order, their pages cut
-// into n_ctas contiguous ranges of about equal cost (bytes + a fixed per-page
-// term), each range split further at unit boundaries (kvq_pool.cu).
-void plan_decode(const kv_pool* P, const int32_t* req_ids, int32_t batch, int64_t n_ctas, PageCost cost,
-                 HostPlan& out);
+// into n_workers contiguous ranges of about equal cost (at least min_pages
+// pages each), each range split further at unit boundaries (kvq_pool.cu).
+// spread: splits walk each unit in its ScanOrder (INT2 pages interleaved);
+// otherwise in table order.
+void plan_decode(const kv_pool* P, const int32_t* req_ids, int32_t batch, int64_t n_workers, int64_t min_pages,
+                 PageCost cost, bool spread, HostPlan& out);
 
 // Launchers (kvq_decode_simt.cu / kvq_decode_mma.cu)
 cudaError_t launch_decode_simt(kv_pool* P, const void* q, int32_t hq, float scale_log2, const Unit* d_units,
                                int n_units, const Split* d_splits, const int32_t* d_cta, int n_ctas, float* d_part,
                                float* out, cudaStream_t s);
 int decode_simt_ctas_per_sm(int g);
+// Tensor-core scan: workers are warps; d_frags holds decode_mma_frag_bytes()
+// per unit (the q operands its per-unit kernel builds before the scan).
 cudaError_t launch_decode_mma(kv_pool* P, const void* q, int32_t hq, float scale_log2, const Unit* d_units, int n_units,
-                              const Split* d_splits, const int32_t* d_cta, int n_ctas, float* d_part, float* out,
-                              cudaStream_t s);
-int decode_mma_ctas_per_sm(int g);
+                              const Split* d_splits, const int32_t* d_wsplit, int n_workers, void* d_frags,
+                              float* d_part, float* out, cudaStream_t s);
+int decode_mma_workers_per_sm(int g);
+constexpr int kMmaWarpsPerCta = 16;
+size_t decode_mma_frag_bytes();
 // Split merge: out[b][h][:] = sum_s acc_s 2^(m_s - M) / sum_s l_s 2^(m_s - M) over the unit's splits.
 cudaError_t launch_merge(kv_pool* P, int g, const Unit* d_units, int n_units, const float* d_part, int hq, float* out,
                          cudaStream_t s);

@@ -19,13 +19,14 @@
 namespace kvq {
 namespace {
 
-// Scratch for one call: the units and splits of the plan, then the split
-// partials (g x 132 floats per split).  Every GPU that loads the library
+// Scratch for one call: the units of the plan, the per-unit q operands of the
+// tensor-core scan, the splits, then the split partials (g x 132 floats per
+// split).  Every GPU that loads the library
 // holds this array until the process exits.  Nothing in it has to start at
 // zero: the plan is copied in by each call and every partial the merge reads
 // is written by the scan kernel of the same call.  Calls whose device work
 // overlaps (different streams, or another pool) race on it.
-constexpr size_t kScratchBytes = size_t(8) << 20;
+constexpr size_t kScratchBytes = size_t(64) << 20;
 constexpr int kMaxUnits = 4096;
 __device__ __align__(256) uint8_t g_noalloc_scratch[kScratchBytes];
 
@@ -89,37 +90,45 @@ extern "C" kv_status_t kv_decode_attn_noalloc(kv_pool_t* P, const void* q, const
   if (scratch_address(P->cfg.device, &scratch) != cudaSuccess)
     return nfail(KV_ERR_CUDA, "kv_decode_attn_noalloc: cudaGetSymbolAddress of the scratch array failed");
 
-  // Plan: the same balanced plan as kv_decode_attn, with the CTA count capped
-  // so that plan + partials fit the scratch (a plan of n CTAs has at most
-  // n + units - 1 splits).
+  // Plan: the same balanced plan as kv_decode_attn, with the worker count
+  // capped so that plan + partials fit the scratch (a plan of n workers has
+  // at most n + units - 1 splits).
   const int32_t impl = P->decode_impl == KV_DECODE_AUTO ? KV_DECODE_MMA : P->decode_impl;
-  const int ctas = impl == KV_DECODE_MMA ? decode_mma_ctas_per_sm(g) : decode_simt_ctas_per_sm(g);
+  const bool mma = impl == KV_DECODE_MMA;
+  const int per_sm = mma ? decode_mma_workers_per_sm(g) : decode_simt_ctas_per_sm(g);
   const size_t part_bytes = (size_t)g * (kHeadDim + 4) * sizeof(float);
   const size_t units_bytes = align256((size_t)n_units * sizeof(Unit));
-  const int64_t budget = (int64_t)((kScratchBytes - units_bytes - 1024) / (sizeof(Split) + sizeof(int32_t) + part_bytes));
-  const int64_t n_ctas = std::min<int64_t>((int64_t)P->sm_count * ctas, budget - n_units);
-  if (n_ctas < 1)
+  const size_t frags_bytes = mma ? align256((size_t)n_units * decode_mma_frag_bytes()) : 0;
+  const int64_t budget = (int64_t)((kScratchBytes - units_bytes - frags_bytes - 1024) /
+                                   (sizeof(Split) + sizeof(int32_t) + part_bytes));
+  const int64_t n_workers = std::min<int64_t>((int64_t)P->sm_count * per_sm, budget - n_units);
+  if (n_workers < 1)
     return nfail(KV_ERR_INVALID_ARG, "kv_decode_attn_noalloc: the plan does not fit the fixed scratch");
   HostPlan hp;
-  plan_decode(P, req_ids, batch, n_ctas, impl == KV_DECODE_MMA ? mma_page_cost(g) : kSimtPageCost, hp);
+  plan_decode(P, req_ids, batch, n_workers, mma ? kMinPagesPerWarp : kMinPagesPerCta,
+              mma ? mma_page_cost(g) : kSimtPageCost, mma, hp);
+  // layout: units, splits, worker split ranges (the uploaded part), then the
+  // per-unit q operands and the partials (written on the device)
   const size_t splits_off = units_bytes;
   const size_t cta_off = align256(splits_off + hp.splits.size() * sizeof(Split));
-  const size_t part_off = align256(cta_off + hp.cta_split.size() * sizeof(int32_t));
+  const size_t frags_off = align256(cta_off + hp.cta_split.size() * sizeof(int32_t));
+  const size_t part_off = frags_off + frags_bytes;
   if (part_off + hp.splits.size() * part_bytes > kScratchBytes)
     return nfail(KV_ERR_INVALID_ARG, "kv_decode_attn_noalloc: the plan does not fit the fixed scratch");
-  std::vector<uint8_t> host(part_off, 0);
+  std::vector<uint8_t> host(frags_off, 0);
   std::memcpy(host.data(), hp.units.data(), hp.units.size() * sizeof(Unit));
   if (!hp.splits.empty()) std::memcpy(host.data() + splits_off, hp.splits.data(), hp.splits.size() * sizeof(Split));
   std::memcpy(host.data() + cta_off, hp.cta_split.data(), hp.cta_split.size() * sizeof(int32_t));
   cudaStream_t s = (cudaStream_t)stream;
   uint8_t* base = (uint8_t*)scratch;
-  if (cudaMemcpyAsync(base, host.data(), part_off, cudaMemcpyHostToDevice, s) != cudaSuccess)
+  if (cudaMemcpyAsync(base, host.data(), frags_off, cudaMemcpyHostToDevice, s) != cudaSuccess)
     return nfail(KV_ERR_CUDA, "kv_decode_attn_noalloc: plan upload failed");
   const float scale_log2 = softmax_scale * 1.4426950408889634f;
   const cudaError_t e =
       impl == KV_DECODE_MMA
           ? launch_decode_mma(P, q, hq, scale_log2, (const Unit*)base, (int)n_units, (const Split*)(base + splits_off),
-                              (const int32_t*)(base + cta_off), (int)hp.n_ctas(), (float*)(base + part_off), out, s)
+                              (const int32_t*)(base + cta_off), (int)hp.n_ctas(), base + frags_off,
+                              (float*)(base + part_off), out, s)
           : launch_decode_simt(P, q, hq, scale_log2, (const Unit*)base, (int)n_units, (const Split*)(base + splits_off),
                                (const int32_t*)(base + cta_off), (int)hp.n_ctas(), (float*)(base + part_off), out, s);
   if (e != cudaSuccess) return nfail(KV_ERR_CUDA, cudaGetErrorString(e));

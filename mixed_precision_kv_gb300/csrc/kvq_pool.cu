@@ -88,12 +88,40 @@ struct Upload {
   }
 };
 
+// Host-to-device copy through a pinned staging slot.  A copy from pageable
+// memory first waits for the stream to drain, which would stall the queue of
+// calls the host keeps ahead of the GPU; from pinned memory it is queued like
+// a kernel.  A slot is reused after its previous copy has run (normally long
+// before: the ring has kPinnedSlots slots).
+kv_status_t h2d(kv_pool* P, void* dst, const void* src, size_t n, cudaStream_t s) {
+  if (n == 0) return KV_OK;
+  kv_pool::PinnedSlot& sl = P->pinned[P->pinned_next];
+  P->pinned_next = (P->pinned_next + 1) % kv_pool::kPinnedSlots;
+  if (sl.pending) {
+    KV_CUDA(cudaEventSynchronize(sl.ev));
+    sl.pending = false;
+  }
+  if (sl.cap < n) {
+    if (sl.ptr) KV_CUDA(cudaFreeHost(sl.ptr));
+    sl.ptr = nullptr;
+    sl.cap = 0;
+    const size_t cap = std::max(n + n / 2, size_t(1) << 16);
+    KV_CUDA(cudaMallocHost(&sl.ptr, cap));
+    sl.cap = cap;
+  }
+  if (!sl.ev) KV_CUDA(cudaEventCreateWithFlags(&sl.ev, cudaEventDisableTiming));
+  std::memcpy(sl.ptr, src, n);
+  KV_CUDA(cudaMemcpyAsync(dst, sl.ptr, n, cudaMemcpyHostToDevice, s));
+  KV_CUDA(cudaEventRecord(sl.ev, s));
+  sl.pending = true;
+  return KV_OK;
+}
+
 kv_status_t upload(kv_pool* P, const Upload& u, cudaStream_t s) {
   if (u.bytes.empty()) return KV_OK;
   kv_status_t st = ensure(P->upload, u.bytes.size());
   if (st != KV_OK) return st;
-  KV_CUDA(cudaMemcpyAsync(P->upload.ptr, u.bytes.data(), u.bytes.size(), cudaMemcpyHostToDevice, s));
-  return KV_OK;
+  return h2d(P, P->upload.ptr, u.bytes.data(), u.bytes.size(), s);
 }
 
 // Device table rows to rewrite after a call: per request, every entry from
@@ -147,28 +175,54 @@ kv_status_t order_after_previous(kv_pool* P, cudaStream_t s) {
 
 void kvq::set_last_error(const char* msg) { g_err = msg; }
 
-void kvq::plan_decode(const kv_pool* P, const int32_t* req_ids, int32_t batch, int64_t n_ctas, PageCost pc,
-                       HostPlan& out) {
+void kvq::plan_decode(const kv_pool* P, const int32_t* req_ids, int32_t batch, int64_t n_ctas, int64_t min_pages,
+                       PageCost pc, bool spread, HostPlan& out) {
   const int hkv = P->cfg.num_kv_heads;
   const int64_t n2 = P->cfg.n_int2_pages;
   auto cost = [&](int32_t id) { return id < n2 ? pc.int2 : pc.int4; };
+  // Per request: the cost of its first i pages in scan order (shared by the
+  // request's kv heads), so that worker boundaries are found by binary search
+  // instead of a walk over every (page, kv head).
+  std::vector<int64_t> off((size_t)batch + 1, 0);
+  std::vector<int32_t> lead((size_t)batch, 0);
+  for (int32_t b = 0; b < batch; ++b) {
+    const auto& tb = P->reqs[req_ids[b]].table;
+    if (spread)
+      for (int32_t id : tb) lead[b] += id < n2 ? 1 : 0;
+    off[b + 1] = off[b] + (int64_t)tb.size() + 1;
+  }
+  std::vector<double> pre((size_t)off[batch]);
   double total = 0.0;
   int64_t pages = 0;
-  for (int32_t b = 0; b < batch; ++b)
-    for (int32_t id : P->reqs[req_ids[b]].table) {
-      total += cost(id) * hkv;
-      pages += hkv;
+  for (int32_t b = 0; b < batch; ++b) {
+    const auto& tb = P->reqs[req_ids[b]].table;
+    const int32_t npos = (int32_t)tb.size();
+    double* pb = &pre[off[b]];
+    ScanOrder so;
+    so.start(0, npos, lead[b]);
+    double c = 0.0;
+    pb[0] = 0.0;
+    for (int32_t i = 0; i < npos; ++i) {
+      c += cost(tb[so.next()]);
+      pb[i + 1] = c;
     }
-  // at least kMinPagesPerCta pages per CTA, so small batches do not pay a
-  // unit prologue per page
-  const int64_t n = std::max<int64_t>(1, std::min<int64_t>(n_ctas, pages / kMinPagesPerCta));
+    total += c * hkv;
+    pages += (int64_t)npos * hkv;
+  }
+  // at least min_pages pages per worker, so small batches do not pay a
+  // worker's fixed cost per page
+  const int64_t n = std::max<int64_t>(1, std::min<int64_t>(n_ctas, pages / std::max<int64_t>(1, min_pages)));
   out.units.assign((size_t)batch * hkv, Unit{});
   out.splits.clear();
   out.cta_split.assign((size_t)n + 1, 0);
-  int64_t cur = 0;        // CTA receiving the current split
-  double cum = 0.0;       // cost before the current page
+  // page at cost offset c (cost of everything before it) goes to worker floor(c n / total)
+  const double scale = total > 0.0 ? (double)n / total : 0.0;
+  auto worker = [&](double c) { return std::min<int64_t>(n - 1, (int64_t)(c * scale)); };
+  int64_t cur = 0;        // worker receiving the current split
+  double U = 0.0;         // cost before the current unit
   for (int32_t b = 0; b < batch; ++b) {
-    const auto& tb = P->reqs[req_ids[b]].table;
+    const int32_t npos = (int32_t)P->reqs[req_ids[b]].table.size();
+    const double* pb = &pre[off[b]];
     for (int h = 0; h < hkv; ++h) {
       const int32_t ui = b * hkv + h;
       Unit& u = out.units[ui];
@@ -176,24 +230,24 @@ void kvq::plan_decode(const kv_pool* P, const int32_t* req_ids, int32_t batch, i
       u.req = req_ids[b];
       u.kvh = h;
       u.split_begin = (int32_t)out.splits.size();
-      bool open = false;
-      for (int32_t i = 0; i < (int32_t)tb.size(); ++i) {
-        const int64_t j = std::min<int64_t>(n - 1, (int64_t)(cum * (double)n / total));
-        if (j > cur) {
-          open = false;
-          while (cur < j) out.cta_split[++cur] = (int32_t)out.splits.size();
+      int32_t i = 0;
+      while (i < npos) {
+        const int64_t j = worker(U + pb[i]);
+        while (cur < j) out.cta_split[++cur] = (int32_t)out.splits.size();
+        // first position after i that belongs to a later worker (npos: none)
+        int32_t lo = i + 1, hi = npos;
+        while (lo < hi) {
+          const int32_t mid = lo + (hi - lo) / 2;
+          if (worker(U + pb[mid]) > j) hi = mid;
+          else lo = mid + 1;
         }
-        if (!open) {
-          out.splits.push_back(Split{ui, i, i + 1, (int32_t)cur});
-          open = true;
-        } else {
-          out.splits.back().page_end = i + 1;
-        }
-        cum += cost(tb[i]);
+        out.splits.push_back(Split{ui, i, lo, req_ids[b], npos, lead[b], {0, 0}});
+        i = lo;
       }
+      U += pb[npos];
       u.n_splits = (int32_t)out.splits.size() - u.split_begin;
       // the unit's last split runs to the end of the table, so pages appended
-      // after planning are scanned too (by the CTA that owns the tail)
+      // after planning are scanned too (by the worker that owns the tail)
       if (u.n_splits > 0) out.splits.back().page_end = -1;
     }
   }
@@ -310,8 +364,13 @@ kv_status_t kv_pool_destroy(kv_pool_t* P) {
   cudaFree(P->upload.ptr);
   cudaFree(P->plan.ptr);
   cudaFree(P->partials.ptr);
+  cudaFree(P->frags.ptr);
   for (cudaEvent_t e : P->tev)
     if (e) cudaEventDestroy(e);
+  for (auto& sl : P->pinned) {
+    if (sl.ptr) cudaFreeHost(sl.ptr);
+    if (sl.ev) cudaEventDestroy(sl.ev);
+  }
   delete P;
   return KV_OK;
 }
@@ -442,9 +501,12 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
       return fail(KV_ERR_OOM, "kv_append_quant: needs %lld INT4 + %lld INT2 pages, %zu + %zu free", (long long)need4,
                   (long long)need2, P->free4.size(), P->free2.size());
   }
+  // room for this call's tokens in each position map; growth is geometric
+  // (reserving just the new size on every call would copy the whole map)
   for (const auto& c : cr) {
     Request& R = P->reqs[c.r];
-    R.loc.reserve(R.loc.size() + (size_t)n_tok);
+    const size_t need = R.loc.size() + (size_t)n_tok;
+    if (R.loc.capacity() < need) R.loc.reserve(std::max(need, 2 * R.loc.capacity()));
   }
   DeviceGuard dg(P->cfg.device);
   cudaStream_t s = (cudaStream_t)stream;
@@ -619,13 +681,15 @@ kv_status_t kv_reorder_pages(kv_pool_t* P, const int32_t* req_ids, int32_t n_req
   Dirty dirty;
   for (int32_t i = 0; i < n_req; ++i) {
     Request& R = P->reqs[req_ids[i]];
+    if (R.ordered_version == R.version) continue;   // unchanged since it was last found INT2-first
     auto first_int4 = std::find_if(R.table.begin(), R.table.end(), [&](int32_t id) { return !is_int2(P, id); });
-    if (std::find_if(first_int4, R.table.end(), [&](int32_t id) { return is_int2(P, id); }) == R.table.end())
-      continue;   // already INT2-first
-    const int32_t from = (int32_t)(first_int4 - R.table.begin());
-    std::stable_partition(R.table.begin(), R.table.end(), [&](int32_t id) { return is_int2(P, id); });
-    dirty.structural(req_ids[i], from);
-    ++R.version;
+    if (std::find_if(first_int4, R.table.end(), [&](int32_t id) { return is_int2(P, id); }) != R.table.end()) {
+      const int32_t from = (int32_t)(first_int4 - R.table.begin());
+      std::stable_partition(R.table.begin(), R.table.end(), [&](int32_t id) { return is_int2(P, id); });
+      dirty.structural(req_ids[i], from);
+      ++R.version;
+    }
+    R.ordered_version = R.version;
   }
   if (dirty.from.empty()) return KV_OK;
   DeviceGuard dg(P->cfg.device);
@@ -758,17 +822,18 @@ kv_status_t build_plan(kv_pool* P, const int32_t* req_ids, int32_t batch, int32_
   }
   if (same) return KV_OK;
 
-  const int ctas = impl == KV_DECODE_MMA ? decode_mma_ctas_per_sm(g) : decode_simt_ctas_per_sm(g);
+  const bool mma = impl == KV_DECODE_MMA;
+  const int per_sm = mma ? decode_mma_workers_per_sm(g) : decode_simt_ctas_per_sm(g);
   HostPlan hp;
-  plan_decode(P, req_ids, batch, (int64_t)P->sm_count * ctas, impl == KV_DECODE_MMA ? mma_page_cost(g) : kSimtPageCost,
-              hp);
+  plan_decode(P, req_ids, batch, (int64_t)P->sm_count * per_sm, mma ? kMinPagesPerWarp : kMinPagesPerCta,
+              mma ? mma_page_cost(g) : kSimtPageCost, mma, hp);
   Upload up;
   const size_t ou = up.add(hp.units.data(), hp.units.size() * sizeof(Unit));
   const size_t os = up.add(hp.splits.data(), hp.splits.size() * sizeof(Split));
   const size_t oc = up.add(hp.cta_split.data(), hp.cta_split.size() * sizeof(int32_t));
   kv_status_t st = ensure(P->plan, up.bytes.size());
   if (st != KV_OK) return st;
-  KV_CUDA(cudaMemcpyAsync(P->plan.ptr, up.bytes.data(), up.bytes.size(), cudaMemcpyHostToDevice, s));
+  if ((st = h2d(P, P->plan.ptr, up.bytes.data(), up.bytes.size(), s)) != KV_OK) return st;
   P->plan_units_off = ou;
   P->plan_splits_off = os;
   P->plan_cta_off = oc;
@@ -782,7 +847,7 @@ kv_status_t build_plan(kv_pool* P, const int32_t* req_ids, int32_t batch, int32_
     P->plan_len[b] = (int32_t)P->reqs[req_ids[b]].table.size();
     total_pages += (int64_t)P->plan_len[b] * hkv;
   }
-  // growth a tail CTA absorbs before the plan is rebuilt: 5% of a CTA's share
+  // growth a tail worker absorbs before the plan is rebuilt: 5% of a worker's share
   P->plan_slack = (int32_t)std::max<int64_t>(1, total_pages / std::max<int64_t>(1, P->n_ctas) / 20);
   P->plan_hq = hq;
   P->plan_impl = impl;
@@ -812,6 +877,8 @@ kv_status_t kv_decode_attn(kv_pool_t* P, const void* q, const int32_t* req_ids, 
   const int g = hq / hkv;
   if ((st = ensure(P->partials, (size_t)std::max(P->n_splits, 1) * g * (kHeadDim + 4) * sizeof(float))) != KV_OK)
     return st;
+  if (impl == KV_DECODE_MMA && (st = ensure(P->frags, (size_t)std::max(P->n_units, 1) * decode_mma_frag_bytes())) != KV_OK)
+    return st;
   const uint8_t* base = (const uint8_t*)P->plan.ptr;
   const float scale_log2 = softmax_scale * 1.4426950408889634f;
   const Unit* du = (const Unit*)(base + P->plan_units_off);
@@ -822,7 +889,8 @@ kv_status_t kv_decode_attn(kv_pool_t* P, const void* q, const int32_t* req_ids, 
   if (tv) KV_CUDA(cudaEventRecord(tv[0], s));
   P->merge_event = tv ? tv[1] : nullptr;
   if (impl == KV_DECODE_MMA)
-    KV_CUDA(launch_decode_mma(P, q, hq, scale_log2, du, P->n_units, dsp, dct, P->n_ctas, (float*)P->partials.ptr, out, s));
+    KV_CUDA(launch_decode_mma(P, q, hq, scale_log2, du, P->n_units, dsp, dct, P->n_ctas, P->frags.ptr,
+                              (float*)P->partials.ptr, out, s));
   else
     KV_CUDA(launch_decode_simt(P, q, hq, scale_log2, du, P->n_units, dsp, dct, P->n_ctas, (float*)P->partials.ptr, out, s));
   if (tv) {
