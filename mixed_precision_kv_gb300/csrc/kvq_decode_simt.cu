@@ -176,59 +176,81 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(
   }
 }
 
-// One CTA of 4 warps per (unit, head): O = sum_s acc_s 2^(m_s - M) / sum_s
-// l_s 2^(m_s - M).  The block first takes the largest m over the unit's
-// splits, then warp w weighs splits w, w + 4, ... (each lane four channels)
-// and the four warps' sums are added in shared memory.  A unit may have tens
-// of splits (one per warp of the tensor-core scan that touched it); spreading
-// them over four warps keeps the dependent load rounds few.
+// One CTA of 8 warps per (unit, head): O = sum_s acc_s 2^(m_s - M) / sum_s
+// l_s 2^(m_s - M).  Warp w takes splits w, w + 8, ...: its lanes read those
+// splits' m and l at once (lane j: the j-th), the warp takes their maximum
+// M_w and weights f = 2^(m - M_w), then every lane adds its four channels of
+// each split with the weight fetched by shuffle.  The eight warps' (M_w, L_w,
+// A_w) are combined in shared memory.  A unit may have tens of splits (one
+// per warp of the tensor-core scan that touched it); this order keeps the
+// dependent load rounds at two.
 template <int G>
-__global__ void __launch_bounds__(128) merge_kernel(const Unit* __restrict__ units, const float* __restrict__ part,
+__global__ void __launch_bounds__(256) merge_kernel(const Unit* __restrict__ units, const float* __restrict__ part,
                                                     int hq, float* __restrict__ out) {
   // Launched as a programmatic dependent of the scan: wait until the scan grid
   // has completed and its partials are visible (immediate for a plain launch).
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");   // the next call's kernels may be staged
-  __shared__ float red[4], lpart[4];
-  __shared__ float4 apart[4][32];
+  constexpr int kW = 8;
+  __shared__ float mpart[kW], lpart[kW];
+  __shared__ float4 apart[kW][32];
   const int ui = blockIdx.x / G, h = blockIdx.x - ui * G;
   const Unit u = units[ui];
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
   const size_t rs = (size_t)G * kPartStride;          // stride between splits
   const float* base = part + ((size_t)u.split_begin * G + h) * kPartStride;
   const int n = u.n_splits;
-  float M = -INFINITY;
-  for (int s = tid; s < n; s += 128) M = fmaxf(M, base[s * rs + kHeadDim]);
-#pragma unroll
-  for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, off));
-  if (lane == 0) red[w] = M;
-  __syncthreads();
-  M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
-  float L = 0.0f;
+  float Mw = -INFINITY, Lw = 0.0f;
   float4 A = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-#pragma unroll 4
-  for (int s = w; s < n; s += 4) {
-    const float* ps = base + (size_t)s * rs;
-    const float m = ps[kHeadDim];
-    const float4 a = *reinterpret_cast<const float4*>(ps + 4 * lane);
-    const float f = m == -INFINITY ? 0.0f : exp2f(m - M);   // an empty split adds nothing
-    L = fmaf(f, ps[kHeadDim + 1], L);
-    A.x = fmaf(a.x, f, A.x);
-    A.y = fmaf(a.y, f, A.y);
-    A.z = fmaf(a.z, f, A.z);
-    A.w = fmaf(a.w, f, A.w);
+  for (int s0 = w; s0 < n; s0 += kW * 32) {           // 32 of the warp's splits per round
+    const int s = s0 + kW * lane;
+    float m = -INFINITY, l = 0.0f;
+    if (s < n) {
+      m = base[s * rs + kHeadDim];
+      l = base[s * rs + kHeadDim + 1];
+    }
+    float mx = m;
+#pragma unroll
+    for (int off = 16; off; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
+    const float Mn = fmaxf(Mw, mx);
+    const float c = Mn == -INFINITY ? 1.0f : exp2f(Mw - Mn);   // rescale what earlier rounds added
+    const float f = m == -INFINITY ? 0.0f : exp2f(m - Mn);     // an empty split adds nothing
+    float lf = f * l;
+#pragma unroll
+    for (int off = 16; off; off >>= 1) lf += __shfl_xor_sync(0xFFFFFFFFu, lf, off);
+    Lw = Lw * c + lf;
+    A.x *= c; A.y *= c; A.z *= c; A.w *= c;
+    Mw = Mn;
+    const int cnt = min(32, (n - s0 + kW - 1) / kW);
+#pragma unroll 8
+    for (int j = 0; j < cnt; ++j) {
+      const float fj = __shfl_sync(0xFFFFFFFFu, f, j);
+      const float4 a = *reinterpret_cast<const float4*>(base + (size_t)(s0 + kW * j) * rs + 4 * lane);
+      A.x = fmaf(a.x, fj, A.x);
+      A.y = fmaf(a.y, fj, A.y);
+      A.z = fmaf(a.z, fj, A.z);
+      A.w = fmaf(a.w, fj, A.w);
+    }
   }
   apart[w][lane] = A;
-  if (lane == 0) lpart[w] = L;
+  if (lane == 0) {
+    mpart[w] = Mw;
+    lpart[w] = Lw;
+  }
   __syncthreads();
   if (w == 0) {
-    float4 t = apart[0][lane];
+    float M = mpart[0];
 #pragma unroll
-    for (int k = 1; k < 4; ++k) {
+    for (int k = 1; k < kW; ++k) M = fmaxf(M, mpart[k]);
+    float4 t = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    float Lt = 0.0f;
+#pragma unroll
+    for (int k = 0; k < kW; ++k) {
+      const float g = mpart[k] == -INFINITY ? 0.0f : exp2f(mpart[k] - M);
       const float4 b = apart[k][lane];
-      t.x += b.x; t.y += b.y; t.z += b.z; t.w += b.w;
+      t.x = fmaf(b.x, g, t.x); t.y = fmaf(b.y, g, t.y); t.z = fmaf(b.z, g, t.z); t.w = fmaf(b.w, g, t.w);
+      Lt = fmaf(lpart[k], g, Lt);
     }
-    const float Lt = (lpart[0] + lpart[1]) + (lpart[2] + lpart[3]);
     const float inv = Lt > 0.0f ? 1.0f / Lt : 0.0f;
     float* o = out + ((size_t)u.b * hq + (size_t)u.kvh * G + h) * kHeadDim + 4 * lane;
     *reinterpret_cast<float4*>(o) = make_float4(t.x * inv, t.y * inv, t.z * inv, t.w * inv);
@@ -267,7 +289,7 @@ cudaError_t launch_merge(kv_pool* P, int g, const Unit* d_units, int n_units, co
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(n_units * g));
-  cfg.blockDim = dim3(128u);
+  cfg.blockDim = dim3(256u);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
   cfg.attrs = attr;
