@@ -157,6 +157,24 @@ __device__ __forceinline__ float pow2_scale(float x, int e) { return x * __int_a
 __device__ __forceinline__ uint32_t comp(const uint4& v, int k) {
   return k == 0 ? v.x : (k == 1 ? v.y : (k == 2 ? v.z : v.w));
 }
+// Packed fp32 pairs (one f32x2 instruction for two IEEE operations, each
+// rounded as its scalar form): (a0, a1) += (b0, b1), (a0, a1) *= (b0, b1),
+// (a0 - b0, a1 - b1).
+__device__ __forceinline__ void add2(float& a0, float& a1, float b0, float b1) {
+  asm("{.reg .b64 x, y;\n mov.b64 x, {%0, %1};\n mov.b64 y, {%2, %3};\n add.rn.f32x2 x, x, y;\n"
+      " mov.b64 {%0, %1}, x;}"
+      : "+f"(a0), "+f"(a1) : "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void mul2(float& a0, float& a1, float b0, float b1) {
+  asm("{.reg .b64 x, y;\n mov.b64 x, {%0, %1};\n mov.b64 y, {%2, %3};\n mul.rn.f32x2 x, x, y;\n"
+      " mov.b64 {%0, %1}, x;}"
+      : "+f"(a0), "+f"(a1) : "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void sub2(float a0, float a1, float b0, float b1, float& d0, float& d1) {
+  asm("{.reg .b64 x, y;\n mov.b64 x, {%2, %3};\n mov.b64 y, {%4, %5};\n sub.rn.f32x2 x, x, y;\n"
+      " mov.b64 {%0, %1}, x;}"
+      : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
 // exact fp16 pair of the fp32 product x: hi = rn16(x), lo = rn16(x - hi)
 __device__ __forceinline__ void split_f16(float x, unsigned short& hi, unsigned short& lo) {
   const __half h = __float2half_rn(x);
@@ -451,8 +469,12 @@ __device__ __forceinline__ void softmax_pv(const uint8_t* blk, uint32_t live, fl
   const float c0 = corr[0], c1 = corr[NH - 1];
   if (__any_sync(0xFFFFFFFFu, c0 != 1.0f || c1 != 1.0f)) {
 #pragma unroll
-    for (int m = 0; m < 8; ++m) { o[m][0] *= c0; o[m][1] *= c1; o[m][2] *= c0; o[m][3] *= c1; }
-    zv[0] *= c0; zv[1] *= c1; zv[2] *= c0; zv[3] *= c1;
+    for (int m = 0; m < 8; ++m) {
+      mul2(o[m][0], o[m][1], c0, c1);
+      mul2(o[m][2], o[m][3], c0, c1);
+    }
+    mul2(zv[0], zv[1], c0, c1);
+    mul2(zv[2], zv[3], c0, c1);
   }
   __syncwarp();
 
@@ -466,7 +488,9 @@ __device__ __forceinline__ void softmax_pv(const uint8_t* blk, uint32_t live, fl
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     ph[k] = pack_h2(pav[k], pbv[k]);
-    pl[k] = pack_h2(pav[k] - h_lo(ph[k]), pbv[k] - h_hi(ph[k]));
+    float ra, rb;
+    sub2(pav[k], pbv[k], h_lo(ph[k]), h_hi(ph[k]), ra, rb);
+    pl[k] = pack_h2(ra, rb);
   }
   // V zero term: rows = groups (lanes r < 4), k = slots
   {
@@ -486,8 +510,8 @@ __device__ __forceinline__ void softmax_pv(const uint8_t* blk, uint32_t live, fl
       mma16816(zt, zz.x, 0u, zz.y, 0u, pl[0], pl[1]);
       mma16816(zt, zz.z, 0u, zz.w, 0u, pl[2], pl[3]);
     }
-#pragma unroll
-    for (int c = 0; c < 4; ++c) zv[c] += zt[c];
+    add2(zv[0], zv[1], zt[0], zt[1]);
+    add2(zv[2], zv[3], zt[2], zt[3]);
   }
   // Fold operands: u = fma(p_hi, s, rn(x3 * s)) with x3 = -p_hi where the lo
   // part is wanted (else 0), then lo = rn(p_lo s + u):
@@ -552,8 +576,8 @@ __device__ __forceinline__ void softmax_pv(const uint8_t* blk, uint32_t live, fl
         mma16816(t, a[0][0], a[0][1], a[0][2], a[0][3], bl[0], bl[1]);
         mma16816(t, a[1][0], a[1][1], a[1][2], a[1][3], bl[2], bl[3]);
       }
-#pragma unroll
-      for (int c = 0; c < 4; ++c) o[m][c] += t[c];
+      add2(o[m][0], o[m][1], t[0], t[1]);
+      add2(o[m][2], o[m][3], t[2], t[3]);
     }
   }
   __syncwarp();
@@ -718,48 +742,88 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(
   }
   __syncwarp();
 
-  // ---- the warp's page stream.  A ticket is one page: its table entry and
-  // tag = split << 6 | kv head (num_kv_heads <= 64); id < 0 ends the stream.
+  // ---- the warp's page stream, read in batches of up to 32 pages: lane j of
+  // a batch holds stream page bbase + j (its table entry, the address of its
+  // block and tag = split << 6 | kv head; num_kv_heads <= 64), found with the
+  // scan order in closed form, so that a page costs a few shuffles.  A batch
+  // stops at the end of a split.  A ticket is one page; id < 0 ends the stream.
   struct Ticket {
     int32_t id;
     uint32_t live;
     int32_t tag;
   };
-  // entry reader: split, scan-order walk (position so.p, end lend), kv head
-  int lsg = s_begin, lend = 0, lkvh = 0;
-  ScanOrder so;
+  int lsg = s_begin, lpos = 0, lend = 0, lkvh = 0, ln = 0, lm = 0;   // reader: split, next position, end, ...
   const Entry* ltab = table;
   auto enter = [&](int sg) {
     const Split sp = splits[sg];
     ltab = table + (size_t)sp.req * max_pages;
-    so.start(sp.page_begin, sp.n_pos, sp.n_lead);
+    lpos = sp.page_begin;
+    ln = sp.n_pos;
+    lm = sp.n_lead;
     lend = sp.page_end >= 0 ? sp.page_end : ntab[sp.req];   // open-ended: the table's length now
     lkvh = sp.unit % hkv;
   };
   enter(lsg);
-  auto next_ticket = [&]() -> Ticket {
-    while (so.p >= lend) {
-      if (lsg + 1 >= s_end) return Ticket{-1, 0u, 0};
-      enter(++lsg);
+  int bbase = 0, bcount = 0;   // the batch holds stream pages [bbase, bbase + bcount)
+  int32_t bid = -1, btag = 0;
+  uint32_t blive = 0u;
+  unsigned long long bsrc = 0ull;
+  auto refill = [&](int k) {
+    while (lpos >= lend && lsg + 1 < s_end) enter(++lsg);
+    const int nb = max(0, min(32, lend - lpos));
+    bbase = k;
+    bcount = nb;
+    bid = -1;
+    if (lane < nb) {
+      // scan-order position p -> table index: the next INT2-first entry when
+      // floor((p+1) m / n) > floor(p m / n), else the next of the others
+      const int p = lpos + lane;
+      int idx = p;
+      if (p < ln) {
+        const int64_t n64 = ln;
+        const int a0 = (int)((int64_t)p * lm / n64), a1 = (int)((int64_t)(p + 1) * lm / n64);
+        idx = a1 > a0 ? a0 : lm + p - a1;
+      }
+      const Entry e = ltab[idx];
+      bid = e.id;
+      blive = e.live;
+      btag = (lsg << 6) | lkvh;
+      const uint8_t* src = e.id < n2 ? pool + ((size_t)e.id * hkv + lkvh) * kInt2Block
+                                     : pool + int4_off + ((size_t)(e.id - n2) * hkv + lkvh) * kInt4Block;
+      bsrc = (unsigned long long)(uintptr_t)src;
     }
-    const Entry e = ltab[so.next()];
-    return Ticket{e.id, e.live, (lsg << 6) | lkvh};
+    lpos += nb;
+  };
+  bool more = true;   // the stream may hold pages past the current batch
+  // ticket of stream page k (k >= bbase; refills when k is past the batch)
+  auto ticket = [&](int k, unsigned long long& src) -> Ticket {
+    if (k >= bbase + bcount) {
+      if (!more) return Ticket{-1, 0u, 0};
+      refill(k);
+      if (bcount == 0) {
+        more = false;
+        return Ticket{-1, 0u, 0};
+      }
+    }
+    const int j = k - bbase;
+    src = __shfl_sync(0xFFFFFFFFu, bsrc, j);
+    return Ticket{__shfl_sync(0xFFFFFFFFu, bid, j), __shfl_sync(0xFFFFFFFFu, blive, j),
+                  __shfl_sync(0xFFFFFFFFu, btag, j)};
   };
   // copy number n goes to stage n & 1 and completes phase (n >> 1) & 1
-  auto issue = [&](const Ticket& t, uint32_t n) {   // lane 0
-    const int kvh = t.tag & 63;
-    const bool i2 = t.id < n2;
-    const uint8_t* src = i2 ? pool + ((size_t)t.id * hkv + kvh) * kInt2Block
-                            : pool + int4_off + ((size_t)(t.id - n2) * hkv + kvh) * kInt4Block;
+  auto issue = [&](const Ticket& t, unsigned long long src, uint32_t n) {   // lane 0
     const uint32_t st = n & (kStages - 1);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the stage was read generically
-    bulk_load(WS.stage[st], src, i2 ? (uint32_t)kInt2Block : (uint32_t)kInt4Block, &WS.bar[st]);
+    bulk_load(WS.stage[st], (const void*)(uintptr_t)src, t.id < n2 ? (uint32_t)kInt2Block : (uint32_t)kInt4Block,
+              &WS.bar[st]);
   };
   static_assert(kStages == 2, "the ticket ring below serves a two-stage copy ring");
-  Ticket t0 = next_ticket(), t1 = next_ticket(), t2 = next_ticket();   // pages c, c+1 (copies issued), c+2
+  unsigned long long src0 = 0ull, src1 = 0ull;
+  Ticket t0 = ticket(0, src0);
+  Ticket t1 = t0.id >= 0 ? ticket(1, src1) : Ticket{-1, 0u, 0};   // pages c, c+1 (copies issued)
   if (lane == 0) {
-    if (t0.id >= 0) issue(t0, 0u);
-    if (t1.id >= 0) issue(t1, 1u);
+    if (t0.id >= 0) issue(t0, src0, 0u);
+    if (t1.id >= 0) issue(t1, src1, 1u);
   }
 
   // ---- state of the split being scanned
@@ -874,10 +938,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(
       softmax_pv<G, false>(blk, t0.live, pscale, lg, zc, o, zv, mrun, lsum, WS.pbuf);
     }
     ++c;
-    if (t2.id >= 0 && lane == 0) issue(t2, c + 1);
+    unsigned long long src2 = 0ull;
+    const Ticket t2 = t1.id >= 0 ? ticket((int)c + 1, src2) : Ticket{-1, 0u, 0};   // page c + 2 of the old c
+    if (t2.id >= 0 && lane == 0) issue(t2, src2, c + 1);
     t0 = t1;
     t1 = t2;
-    t2 = next_ticket();
   }
   if (!ok) {
     if (lane == 0) atomicOr(status, kStatusTimeout);
