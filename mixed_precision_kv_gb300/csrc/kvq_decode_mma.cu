@@ -324,12 +324,25 @@ __device__ __forceinline__ void qk_int2(const uint8_t* blk, const UnitFrag* __re
     const int wi = kk >> 2, jj = kk & 3;
     const int p0 = wi * 8 + i2_reg6(jj), p1 = wi * 8 + i2_reg8(jj);
     const uint32_t s0 = comp(sv[p0 >> 2], p0 & 3), s1 = comp(sv[p1 >> 2], p1 & 3);
-    const uint4 qq = __ldg(&F->bq2[kk >> 1][lane]), nq = __ldg(&F->bqn[kk >> 1][lane]);
+    const uint4 qq = __ldg(&F->bq2[kk >> 1][lane]);
     const uint32_t q0 = (kk & 1) ? qq.z : qq.x, q1 = (kk & 1) ? qq.w : qq.y;
-    const uint32_t n0 = (kk & 1) ? nq.z : nq.x, n1 = (kk & 1) ? nq.w : nq.y;
-    // hi = rn(q s); lo = q s - hi (exact).  bqn holds -q where the lo part is
-    // wanted and 0 elsewhere, so u = fma(q, s, rn(bqn s)) is lo or hi.
-    const uint32_t u0 = hfma2(q0, s0, hmul2(n0, s0)), u1 = hfma2(q1, s1, hmul2(n1, s1));
+    // hi = rn(q s); lo = q s - hi (exact: the rounding error of an fp16 product)
+    uint32_t b0, b1, u0, u1;
+    if constexpr (kPair) {
+      // bqn holds -q where the lo part is wanted and 0 elsewhere, so
+      // u = fma(q, s, rn(bqn s)) is lo or hi
+      const uint4 nq = __ldg(&F->bqn[kk >> 1][lane]);
+      const uint32_t n0 = (kk & 1) ? nq.z : nq.x, n1 = (kk & 1) ? nq.w : nq.y;
+      u0 = hfma2(q0, s0, hmul2(n0, s0));
+      u1 = hfma2(q1, s1, hmul2(n1, s1));
+      b0 = b1 = 0u;
+    } else {
+      // lo = fma(q, s, -hi), with -hi = rn(-q s) by sign symmetry
+      b0 = hmul2(q0, s0);
+      b1 = hmul2(q1, s1);
+      u0 = hfma2(q0, s0, b0 ^ 0x80008000u);
+      u1 = hfma2(q1, s1, b1 ^ 0x80008000u);
+    }
 #pragma unroll
     for (int m = 0; m < 2; ++m) {
       const uint32_t x0 = i2_variant(wi ? kw[m][0].y : kw[m][0].x, jj);   // token 16m + r
@@ -338,7 +351,7 @@ __device__ __forceinline__ void qk_int2(const uint8_t* blk, const UnitFrag* __re
       if constexpr (kPair) {
         mma16816(acc[m][kk & 1], a0, a1, a2, a3, u0, u1);
       } else {
-        mma16816(acc[m][0], a0, a1, a2, a3, hmul2(q0, s0), hmul2(q1, s1));
+        mma16816(acc[m][0], a0, a1, a2, a3, b0, b1);
         mma16816(acc[m][1], a0, a1, a2, a3, u0, u1);
       }
     }
