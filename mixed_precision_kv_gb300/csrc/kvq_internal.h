@@ -133,7 +133,7 @@ struct PageCost {
 inline PageCost mma_page_cost(int g) { return g <= 4 ? PageCost{1.18, 1.00} : PageCost{1.50, 1.00}; }
 constexpr PageCost kSimtPageCost{3072.0 + 2048.0, 5120.0 + 2048.0};
 constexpr int64_t kMinPagesPerCta = 16;    // CUDA-core scan: pages per CTA at least
-constexpr int64_t kMinPagesPerWarp = 4;    // tensor-core scan: pages per warp at least
+constexpr int64_t kMinPagesPerWarp = 1;    // tensor-core scan: pages per warp at least (small batches: more warps, less latency)
 constexpr int64_t kTimingRing = 2048;
 
 // Decode plan on the host (see plan_decode).
