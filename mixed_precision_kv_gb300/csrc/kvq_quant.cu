@@ -46,6 +46,26 @@ __device__ __forceinline__ uint32_t qcode(float x, const GroupMeta& m, float qma
   return (uint32_t)r;
 }
 
+// The same code without a division in the common case.  rs = approximate
+// reciprocal of m.sf (relative error < 2^-22), so q0 = u * rs lies within
+// 4e-6 of the correctly rounded quotient fl(u / s) for |u / s| < 64 (here
+// |u / s| <= qmax + 1).  When q0 is more than 1e-5 from every half-integer,
+// fl(u / s) rounds to the same integer; otherwise the quotient is computed
+// exactly.  Same result as qcode, bit for bit.
+__device__ __forceinline__ float approx_rcp(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ uint32_t qcode_fast(float x, const GroupMeta& m, float rs, float qmax) {
+  if (!m.nz) return 0u;
+  const float u = __fsub_rn(x, m.zf);
+  const float q0 = u * rs;
+  float c = rintf(q0);
+  if (!(fabsf(fabsf(q0 - c) - 0.5f) > 1e-5f)) c = rintf(__fdiv_rn(u, m.sf));
+  return (uint32_t)fminf(fmaxf(c, 0.0f), qmax);
+}
+
 // min / max over the 8 lanes of one 32-channel group (lanes 8*gr .. 8*gr + 7)
 __device__ __forceinline__ void group8_minmax(float& mn, float& mx) {
 #pragma unroll
@@ -66,9 +86,13 @@ __device__ __forceinline__ void or_bits(uint8_t* img, int byte_off, int shift, u
 // Quantize one token (a warp: lane = channels 4*lane .. 4*lane+3) into slot
 // `slot` of an INT4 block image `img` (shared or global memory).  V nibbles
 // are OR-ed in: the block's unfilled slots hold zeros.
+// With vcodes (shared memory, [slot][channel] bytes) the V codes go there
+// for a later word-wise packing (pack_i4v) instead of being OR-ed into img.
+// vmax: the warp's running maximum of V scales (one atomic per warp at the
+// end instead of one per token on the pool's single maximum word).
 __device__ __forceinline__ bool quantize_token(uint8_t* img, const __nv_bfloat16* __restrict__ k,
                                                const __nv_bfloat16* __restrict__ v, int t, int slot, int h, int hkv,
-                                               uint32_t* __restrict__ status) {
+                                               float& vmax, uint8_t* vcodes = nullptr) {
   const int lane = threadIdx.x & 31, gr = lane >> 3;
   const size_t row = ((size_t)t * hkv + h) * kHeadDim + 4 * lane;
   const uint2 kr = *reinterpret_cast<const uint2*>(k + row);
@@ -91,24 +115,26 @@ __device__ __forceinline__ bool quantize_token(uint8_t* img, const __nv_bfloat16
   const GroupMeta km = make_meta(kmn, kmx, 15.0f);
   const GroupMeta vm = make_meta(vmn, vmx, 15.0f);
   uint32_t ck[4], cv[4];
+  const float krs = approx_rcp(km.sf), vrs = approx_rcp(vm.sf);
 #pragma unroll
-  for (int a = 0; a < 4; ++a) { ck[a] = qcode(xk[a], km, 15.0f); cv[a] = qcode(xv[a], vm, 15.0f); }
+  for (int a = 0; a < 4; ++a) {
+    ck[a] = qcode_fast(xk[a], km, krs, 15.0f);
+    cv[a] = qcode_fast(xv[a], vm, vrs, 15.0f);
+  }
   // K: channels 4*lane .. 4*lane+3 are nibbles 0..3 or 4..7 of one word -> 2 bytes
   const int kb = i4k_byte(slot, 4 * lane);
   *reinterpret_cast<uint16_t*>(img + kb) = (uint16_t)(ck[0] | (ck[1] << 4) | (ck[2] << 8) | (ck[3] << 12));
   // V: channel-major, one nibble per channel
+  if (vcodes) {
+    *reinterpret_cast<uint32_t*>(vcodes + kHeadDim * slot + 4 * lane) = cv[0] | (cv[1] << 8) | (cv[2] << 16) | (cv[3] << 24);
+  } else {
 #pragma unroll
-  for (int a = 0; a < 4; ++a) {
-    const int c = 4 * lane + a;
-    or_bits(img, i4v_byte(slot, c), i4v_shift(slot), cv[a]);
+    for (int a = 0; a < 4; ++a) {
+      const int c = 4 * lane + a;
+      or_bits(img, i4v_byte(slot, c), i4v_shift(slot), cv[a]);
+    }
   }
-  {
-    // running maximum of V scales (non-negative floats order as their bits)
-    float m = vm.sf;
-    m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 8));
-    m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 16));
-    if (lane == 0) atomicMax(status + 2, __float_as_uint(m));
-  }
+  vmax = fmaxf(vmax, vm.sf);   // per lane; reduced over the warp by flush_vmax
   if ((lane & 7) == 0) {
     st_half(img, kI4KMeta + 16 * slot + 4 * gr, km.s);
     st_half(img, kI4KMeta + 16 * slot + 4 * gr + 2, km.z);
@@ -116,6 +142,26 @@ __device__ __forceinline__ bool quantize_token(uint8_t* img, const __nv_bfloat16
     st_half(img, kI4VMeta + 256 + 2 * v_meta_index(slot, gr), vm.z);
   }
   return bad;
+}
+
+// One atomic per warp for the pool's running maximum of V scales
+// (non-negative floats order as their bits).
+__device__ __forceinline__ void flush_vmax(float vmax, uint32_t* __restrict__ status) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xFFFFFFFFu, vmax, o));
+  if ((threadIdx.x & 31) == 0 && vmax > 0.0f) atomicMax(status + 2, __float_as_uint(vmax));
+}
+
+// INT4 V words from [slot][channel] code bytes: word (channel c, slot chunk j)
+// holds slots 8j .. 8j+7 in nibbles 0..7; every word is built by one thread.
+__device__ __forceinline__ void pack_i4v(uint8_t* __restrict__ img, const uint8_t* __restrict__ vcodes) {
+  for (int x = threadIdx.x; x < kHeadDim * (kPage / 8); x += kThreads) {
+    const int c = x & (kHeadDim - 1), j = x >> 7;
+    uint32_t w = 0u;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) w |= (uint32_t)vcodes[kHeadDim * (8 * j + k) + c] << (4 * k);
+    *reinterpret_cast<uint32_t*>(img + i4v_byte(8 * j, c)) = w;
+  }
 }
 
 // One CTA per (job, kv head), a warp per token.  A new page (job starting at
@@ -132,6 +178,7 @@ __global__ void __launch_bounds__(kThreads) append_int4_kernel(
     Entry* __restrict__ table, int32_t* __restrict__ ntab, uint32_t* __restrict__ status,
     const __grid_constant__ SmallAppend small) {
   __shared__ __align__(16) uint8_t img[kInt4Block];
+  __shared__ __align__(16) uint8_t vcodes[kPage * kHeadDim];   // V codes of a new page, packed after
   asm volatile("griddepcontrol.wait;" ::: "memory");   // earlier work on the stream (the previous decode) is done
   asm volatile("griddepcontrol.launch_dependents;");
   const AppendJob job = kByValue ? small.jobs[blockIdx.x] : jobs[blockIdx.x];
@@ -141,19 +188,25 @@ __global__ void __launch_bounds__(kThreads) append_int4_kernel(
   const bool fresh = job.first_slot == 0;
   const int warp = threadIdx.x >> 5;
   bool bad = false;
+  float vmax = 0.0f;
   if (fresh) {
     uint4* img4 = reinterpret_cast<uint4*>(img);
     for (int i = threadIdx.x; i < kInt4Block / 16; i += kThreads) img4[i] = make_uint4(0, 0, 0, 0);
+    for (int i = threadIdx.x; i < kPage * kHeadDim / 16; i += kThreads)
+      reinterpret_cast<uint4*>(vcodes)[i] = make_uint4(0, 0, 0, 0);
     __syncthreads();
     for (int j = warp; j < job.n_slots; j += kThreads / 32)
-      bad |= quantize_token(img, k, v, tk[job.tok_off + j], job.first_slot + j, h, hkv, status);
+      bad |= quantize_token(img, k, v, tk[job.tok_off + j], job.first_slot + j, h, hkv, vmax, vcodes);
+    __syncthreads();
+    pack_i4v(img, vcodes);
     __syncthreads();
     uint4* out4 = reinterpret_cast<uint4*>(blk);
     for (int i = threadIdx.x; i < kInt4Block / 16; i += kThreads) out4[i] = img4[i];
   } else {
     for (int j = warp; j < job.n_slots; j += kThreads / 32)
-      bad |= quantize_token(blk, k, v, tk[job.tok_off + j], job.first_slot + j, h, hkv, status);
+      bad |= quantize_token(blk, k, v, tk[job.tok_off + j], job.first_slot + j, h, hkv, vmax);
   }
+  flush_vmax(vmax, status);
   if (bad) atomicOr(status, kStatusRange);
   if (h == 0 && threadIdx.x == 0) {
     if (job.tab_index >= 0) table[job.tab_index] = Entry{job.page, job.live};
@@ -162,11 +215,13 @@ __global__ void __launch_bounds__(kThreads) append_int4_kernel(
 }
 
 // Requantize a 32-token INT4 block image (shared memory) into an INT2 block
-// image (shared memory, zeroed): K per channel across the 32 tokens, V per
-// token and group, both from the INT4-dequantized values fmaf(code, scale,
-// zero); tracks the largest INT2 K and V scales.  128 threads.
+// image (shared memory): K per channel across the 32 tokens, V per token and
+// group, both from the INT4-dequantized values fmaf(code, scale, zero); tracks
+// the largest INT2 K and V scales.  The codes go through `codes` ([slot]
+// [channel] bytes, shared memory) and are packed so that every output byte is
+// written by one thread.  128 threads.
 __device__ __forceinline__ void repack_image(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
-                                             uint32_t* __restrict__ smax_bits) {
+                                             uint32_t* __restrict__ smax_bits, uint8_t* __restrict__ codes) {
   // K: thread c owns channel c; its group is the 32 tokens of the page.
   {
     const int c = threadIdx.x;
@@ -183,8 +238,9 @@ __device__ __forceinline__ void repack_image(const uint8_t* __restrict__ src, ui
       mx = t ? fmaxf(mx, x[t]) : x[t];
     }
     const GroupMeta m = make_meta(mn, mx, 3.0f);
+    const float rs = approx_rcp(m.sf);
 #pragma unroll
-    for (int t = 0; t < kPage; ++t) or_bits(dst, i2k_byte(t, c), i2k_shift(c), qcode(x[t], m, 3.0f));
+    for (int t = 0; t < kPage; ++t) codes[kHeadDim * t + c] = (uint8_t)qcode_fast(x[t], m, rs, 3.0f);
     st_half(dst, kI2KMeta + 2 * i2k_meta_index(c), m.s);
     st_half(dst, kI2KMeta + 256 + 2 * i2k_meta_index(c), m.z);
     // running maximum of INT2 K scales (non-negative floats order as their bits)
@@ -193,6 +249,14 @@ __device__ __forceinline__ void repack_image(const uint8_t* __restrict__ src, ui
     for (int o = 16; o; o >>= 1) smx = fmaxf(smx, __shfl_xor_sync(0xFFFFFFFFu, smx, o));
     if ((threadIdx.x & 31) == 0) atomicMax(smax_bits, __float_as_uint(smx));
   }
+  __syncthreads();
+  // K codes: byte (slot t, b) holds channels 4b .. 4b+3
+  for (int x = threadIdx.x; x < kPage * (kHeadDim / 4); x += kThreads) {
+    const int t = x >> 5, b = x & 31;
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(codes + kHeadDim * t + 4 * b);
+    dst[i2k_byte(t, 4 * b)] = (uint8_t)((w & 3u) | ((w >> 6) & 0xCu) | ((w >> 12) & 0x30u) | ((w >> 18) & 0xC0u));
+  }
+  __syncthreads();
   // V: thread -> (slot t, group gr), 32 channels each.
   {
     const int t = threadIdx.x >> 2, gr = threadIdx.x & 3;
@@ -210,17 +274,36 @@ __device__ __forceinline__ void repack_image(const uint8_t* __restrict__ src, ui
       mx = cc ? fmaxf(mx, x[cc]) : x[cc];
     }
     const GroupMeta m = make_meta(mn, mx, 3.0f);
+    const float rs = approx_rcp(m.sf);
 #pragma unroll
-    for (int cc = 0; cc < kGroup; ++cc) {
-      const int c = kGroup * gr + cc;
-      or_bits(dst, i2v_byte(t, c), i2v_shift(t), qcode(x[cc], m, 3.0f));
-    }
+    for (int cc = 0; cc < kGroup; ++cc) codes[kHeadDim * t + kGroup * gr + cc] = (uint8_t)qcode_fast(x[cc], m, rs, 3.0f);
     st_half(dst, kI2VMeta + 2 * mi, m.s);
     st_half(dst, kI2VMeta + 256 + 2 * mi, m.z);
     float vmx = m.sf;
 #pragma unroll
     for (int o = 16; o; o >>= 1) vmx = fmaxf(vmx, __shfl_xor_sync(0xFFFFFFFFu, vmx, o));
     if ((threadIdx.x & 31) == 0) atomicMax(smax_bits + 1, __float_as_uint(vmx));
+  }
+  __syncthreads();
+  // V codes: the 8 slots of chunk i of channel c fill two bytes (4 slots each)
+  for (int x = threadIdx.x; x < kHeadDim * (kPage / 8); x += kThreads) {
+    const int c = x & (kHeadDim - 1), i = x >> 7;
+    const int b0 = i2v_byte(8 * i, c);
+    int b1 = b0;
+    uint32_t v0 = 0u, v1 = 0u;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int t = 8 * i + k, b = i2v_byte(t, c);
+      const uint32_t code = (uint32_t)codes[kHeadDim * t + c] << i2v_shift(t);
+      if (b == b0) {
+        v0 |= code;
+      } else {
+        v1 |= code;
+        b1 = b;
+      }
+    }
+    dst[b0] = (uint8_t)v0;
+    dst[b1] = (uint8_t)v1;
   }
 }
 
@@ -231,6 +314,7 @@ __global__ void __launch_bounds__(kThreads) repack_int2_kernel(uint8_t* __restri
                                                               uint32_t* __restrict__ smax_bits) {
   __shared__ __align__(16) uint8_t src[kInt4Block];
   __shared__ __align__(16) uint8_t dst[kInt2Block];
+  __shared__ __align__(16) uint8_t codes[kPage * kHeadDim];
   const RepackJob job = jobs[blockIdx.x];
   const int h = blockIdx.y;
   const uint8_t* sblk = pool + int4_off + ((size_t)(job.src - n2) * hkv + h) * kInt4Block;
@@ -240,7 +324,7 @@ __global__ void __launch_bounds__(kThreads) repack_int2_kernel(uint8_t* __restri
   for (int i = threadIdx.x; i < kInt2Block / 16; i += kThreads)
     reinterpret_cast<uint4*>(dst)[i] = make_uint4(0, 0, 0, 0);
   __syncthreads();
-  repack_image(src, dst, smax_bits);
+  repack_image(src, dst, smax_bits, codes);
   __syncthreads();
   for (int i = threadIdx.x; i < kInt2Block / 16; i += kThreads)
     reinterpret_cast<uint4*>(dblk)[i] = reinterpret_cast<const uint4*>(dst)[i];
@@ -256,17 +340,19 @@ __global__ void __launch_bounds__(kThreads) direct_int2_kernel(
     const DirectJob* __restrict__ jobs, const int32_t* __restrict__ toks, uint32_t* __restrict__ status) {
   __shared__ __align__(16) uint8_t img[kInt4Block];
   __shared__ __align__(16) uint8_t dst[kInt2Block];
+  __shared__ __align__(16) uint8_t codes[kPage * kHeadDim];
   const DirectJob job = jobs[blockIdx.x];
   const int h = blockIdx.y;
-  for (int i = threadIdx.x; i < kInt4Block / 16; i += kThreads) reinterpret_cast<uint4*>(img)[i] = make_uint4(0, 0, 0, 0);
-  for (int i = threadIdx.x; i < kInt2Block / 16; i += kThreads) reinterpret_cast<uint4*>(dst)[i] = make_uint4(0, 0, 0, 0);
-  __syncthreads();
   bool bad = false;
-  for (int j = threadIdx.x >> 5; j < kPage; j += kThreads / 32)
-    bad |= quantize_token(img, k, v, toks[job.tok_off + j], j, h, hkv, status);
+  float vmax = 0.0f;
+  for (int j = threadIdx.x >> 5; j < kPage; j += kThreads / 32)   // every slot is written: no zeroing
+    bad |= quantize_token(img, k, v, toks[job.tok_off + j], j, h, hkv, vmax, codes);
+  flush_vmax(vmax, status);
   if (bad) atomicOr(status, kStatusRange);
   __syncthreads();
-  repack_image(img, dst, status + 1);
+  pack_i4v(img, codes);
+  __syncthreads();
+  repack_image(img, dst, status + 1, codes);
   __syncthreads();
   uint8_t* dblk = pool + ((size_t)job.dst * hkv + h) * kInt2Block;
   for (int i = threadIdx.x; i < kInt2Block / 16; i += kThreads)
