@@ -477,8 +477,52 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
     ~ResetSlots() { for (const auto& c : *cr) P->call_slot[(size_t)c.r] = -1; }
   } reset_slots{P, &cr};
 
+  // Bulk path: every token of the call belongs to one request (a prefill
+  // chunk).  The per-token rules below then reduce to whole runs: INT4 tokens
+  // fill the tail page and new pages of 32; INT2 tokens fill the open staging
+  // page, then groups of 32 that complete within the call (direct INT2 jobs),
+  // then one partial staging page.  Page ids are taken in the same token
+  // order as the per-token loop takes them, so both paths give the same pool.
+  bool bulk = n_tok >= kPage;
+  for (int64_t t = 1; bulk && t < n_tok; ++t) bulk = req_ids[t] == req_ids[0];
+  std::vector<int32_t> i4, i2;                // the call's INT4 / INT2 token indices, in order
+  int64_t b_cap4 = 0, b_new4 = 0, b_e = 0, b_ndirect = 0, b_rem = 0;
+  int b_f4 = 0, b_s0 = 0;
+  bool b_repack = false;
+  if (bulk && !req_ok(P, req_ids[0])) bulk = false;   // the per-token path reports the error
+  if (bulk) {
+    i4.reserve((size_t)n_tok);
+    i2.reserve((size_t)n_tok);
+    for (int64_t t = 0; bulk && t < n_tok; ++t) {
+      if (bits[t] == 4) i4.push_back((int32_t)t);
+      else if (bits[t] == 2) i2.push_back((int32_t)t);
+      else bulk = false;   // the per-token path reports the error (and any earlier one)
+    }
+  }
+  if (bulk) {
+    const int32_t r = req_ids[0];
+    const Request& R = P->reqs[r];
+    const int64_t n4 = (int64_t)i4.size(), n2 = (int64_t)i2.size();
+    const bool tail_open = R.tail4 >= 0 && P->fill[R.tail4] < kPage;
+    b_f4 = tail_open ? (int)P->fill[R.tail4] : 0;
+    b_cap4 = tail_open ? std::min<int64_t>(n4, kPage - b_f4) : 0;
+    b_new4 = (n4 - b_cap4 + kPage - 1) / kPage;
+    b_s0 = R.staging >= 0 ? (int)P->fill[R.staging] : 0;
+    b_e = R.staging >= 0 ? std::min<int64_t>(n2, kPage - b_s0) : 0;
+    b_repack = R.staging >= 0 && b_s0 + b_e == kPage;
+    b_ndirect = (n2 - b_e) / kPage;
+    b_rem = (n2 - b_e) % kPage;
+    const int64_t opens = b_new4 + b_ndirect + (b_rem > 0 ? 1 : 0);
+    const int64_t need4 = opens, need2 = b_ndirect + (b_repack ? 1 : 0);
+    if ((int64_t)R.table.size() + opens > P->cfg.max_pages_per_request)
+      return fail(KV_ERR_OOM, "kv_append_quant: request %d would exceed %d table entries", r, P->cfg.max_pages_per_request);
+    if (need4 > (int64_t)P->free4.size() || need2 > (int64_t)P->free2.size())
+      return fail(KV_ERR_OOM, "kv_append_quant: needs %lld INT4 + %lld INT2 pages, %zu + %zu free", (long long)need4,
+                  (long long)need2, P->free4.size(), P->free2.size());
+    slot_of(r);
+  }
   // Dry run: pages taken and table growth, so that OOM changes nothing.
-  {
+  if (!bulk) {
     int64_t need4 = 0, need2 = 0;
     for (int64_t t = 0; t < n_tok; ++t) {
       if (!req_ok(P, req_ids[t]))
@@ -523,9 +567,114 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
   std::vector<RepackJob> repacks;
   std::vector<DirectJob> directs;
   std::vector<int32_t> dtoks;                          // 32 token indices per direct job
-  std::vector<int32_t> tok_job((size_t)n_tok, -1), tok_slot((size_t)n_tok);
+  std::vector<int32_t> toks;                           // token indices of the append jobs, job by job in slot order
   std::vector<int32_t> deferred;
   Dirty dirty;   // table rewrites the append kernel does not cover (repacks)
+  if (bulk) {
+    const int32_t r = req_ids[0];
+    Request& R = P->reqs[r];
+    const int64_t n4 = (int64_t)i4.size(), n2 = (int64_t)i2.size();
+    const int64_t T0 = (int64_t)R.loc.size();
+    R.loc.resize((size_t)(T0 + n_tok));
+    auto put = [&](int32_t page, int slot, int32_t t) {
+      P->pos[(size_t)page * kPage + slot] = (int32_t)(T0 + t);
+      R.loc[(size_t)(T0 + t)] = ((uint32_t)page << 5) | (uint32_t)slot;
+    };
+    auto slots = [](int first, int64_t n) { return (uint32_t)((n >= kPage ? 0xFFFFFFFFull : ((1ull << n) - 1)) << first); };
+    // an append job over tokens idx[a .. a+n) into slots first .. of page
+    auto add_job = [&](int32_t page, int first, const std::vector<int32_t>& idx, int64_t a, int64_t n) {
+      jobs.push_back(AppendJob{page, first, (int32_t)n, (int32_t)toks.size(), -1, 0u, -1, 0});
+      job_req.push_back(r);
+      for (int64_t q = 0; q < n; ++q) {
+        put(page, first + (int)q, idx[(size_t)(a + q)]);
+        toks.push_back(idx[(size_t)(a + q)]);
+      }
+      P->fill[page] = (uint8_t)(first + n);
+      P->live[page] |= slots(first, n);
+    };
+    // INT4 pages and staging pages take ids in the token order of their
+    // first token; INT2 pages in the order their groups complete
+    std::vector<int32_t> id4((size_t)b_new4), idS((size_t)(b_ndirect + (b_rem > 0 ? 1 : 0)));
+    {
+      size_t a = 0, b = 0;
+      while (a < id4.size() || b < idS.size()) {
+        const int32_t ta = a < id4.size() ? i4[(size_t)(b_cap4 + kPage * (int64_t)a)] : INT32_MAX;
+        const int32_t tb = b < idS.size() ? i2[(size_t)(b_e + kPage * (int64_t)b)] : INT32_MAX;
+        if (ta < tb) id4[a++] = P->free4.take_lowest();
+        else idS[b++] = P->free4.take_lowest();
+      }
+    }
+    const int32_t nid_rep = b_repack ? P->free2.take_lowest() : -1;
+    std::vector<int32_t> idD((size_t)b_ndirect);
+    for (auto& x : idD) x = P->free2.take_lowest();
+    // table entries appended in this call, with the token that appends them
+    std::vector<std::pair<int32_t, int32_t>> app;   // (token, page id)
+    // INT4: the open tail page, then new pages
+    if (b_cap4 > 0) add_job(R.tail4, b_f4, i4, 0, b_cap4);
+    for (int64_t q = 0; q < b_new4; ++q) {
+      const int64_t a = b_cap4 + kPage * q;
+      const int32_t pg = id4[(size_t)q];
+      P->fill[pg] = 0;
+      P->live[pg] = 0u;
+      add_job(pg, 0, i4, a, std::min<int64_t>(kPage, n4 - a));
+      app.emplace_back(i4[(size_t)a], pg);
+    }
+    if (b_new4 > 0) R.tail4 = id4[(size_t)(b_new4 - 1)];
+    // INT2: the open staging page
+    if (b_e > 0) add_job(R.staging, b_s0, i2, 0, b_e);
+    if (b_repack) {
+      const int32_t sp = R.staging;
+      P->fill[nid_rep] = kPage;
+      P->live[nid_rep] = P->live[sp];
+      for (int sl = 0; sl < kPage; ++sl) {
+        const int32_t pp = P->pos[(size_t)sp * kPage + sl];
+        P->pos[(size_t)nid_rep * kPage + sl] = pp;
+        R.loc[(size_t)pp] = ((uint32_t)nid_rep << 5) | (uint32_t)sl;
+      }
+      const auto rit = std::find(R.table.rbegin(), R.table.rend(), sp);
+      const auto it = std::next(rit).base();
+      dirty.structural(r, (int32_t)(it - R.table.begin()));
+      R.table.erase(it);
+      repacks.push_back(RepackJob{sp, nid_rep});
+      deferred.push_back(sp);
+      app.emplace_back(i2[(size_t)(b_e - 1)], nid_rep);
+      R.staging = -1;
+    }
+    // groups of 32 completed in this call: direct INT2 jobs (their staging
+    // ids are taken and freed, as the per-token path does)
+    for (int64_t g = 0; g < b_ndirect; ++g) {
+      const int64_t a = b_e + kPage * g;
+      const int32_t sg = idS[(size_t)g], nid = idD[(size_t)g];
+      for (int sl = 0; sl < kPage; ++sl) {
+        const int32_t t = i2[(size_t)(a + sl)];
+        P->pos[(size_t)sg * kPage + sl] = (int32_t)(T0 + t);
+        put(nid, sl, t);
+      }
+      P->fill[sg] = kPage;
+      P->live[sg] = 0xFFFFFFFFu;
+      P->fill[nid] = kPage;
+      P->live[nid] = 0xFFFFFFFFu;
+      directs.push_back(DirectJob{nid, (int32_t)dtoks.size()});
+      dtoks.insert(dtoks.end(), i2.begin() + a, i2.begin() + a + kPage);
+      deferred.push_back(sg);
+      app.emplace_back(i2[(size_t)(a + kPage - 1)], nid);
+    }
+    if (b_ndirect > 0 && !b_repack) dirty.structural(r, (int32_t)R.table.size());
+    // the last, partial staging page
+    if (b_rem > 0) {
+      const int64_t a = b_e + kPage * b_ndirect;
+      const int32_t sp = idS[(size_t)b_ndirect];
+      P->fill[sp] = 0;
+      P->live[sp] = 0u;
+      add_job(sp, 0, i2, a, b_rem);
+      app.emplace_back(i2[(size_t)a], sp);
+      R.staging = sp;
+    }
+    std::sort(app.begin(), app.end());
+    for (const auto& x : app) R.table.push_back(x.second);
+    if (!app.empty() || b_repack) ++R.version;
+  } else {
+  std::vector<int32_t> tok_job((size_t)n_tok, -1), tok_slot((size_t)n_tok);
   for (int64_t t = 0; t < n_tok; ++t) {
     const int32_t r = req_ids[t];
     Request& R = P->reqs[r];
@@ -596,12 +745,14 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
   }
   int32_t off = 0;
   for (auto& j : jobs) { j.tok_off = off; off += j.n_slots; }
-  std::vector<int32_t> toks((size_t)off);
+  toks.assign((size_t)off, 0);
   for (int64_t t = 0; t < n_tok; ++t) {
     if (tok_job[t] < 0) continue;   // routed to a direct job
     const AppendJob& j = jobs[(size_t)tok_job[t]];
     toks[(size_t)(j.tok_off + (tok_slot[t] - j.first_slot))] = (int32_t)t;
   }
+  }   // per-token path
+  const int32_t off = (int32_t)toks.size();
   for (int32_t id : deferred) {
     P->fill[id] = 0;
     P->live[id] = 0;
