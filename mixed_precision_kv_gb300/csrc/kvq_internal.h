@@ -220,6 +220,10 @@ struct kv_pool {
   static constexpr int kPinnedSlots = 4;
   PinnedSlot pinned[kPinnedSlots];
   int pinned_next = 0;
+  // host scratch reused by every call (kept at capacity: fresh vectors cost
+  // an allocation and first-touch page faults per call)
+  std::vector<int32_t> scr_i4, scr_i2, scr_toks, scr_dtoks;
+  std::vector<uint8_t> scr_upload;
   kvq::DevBuf plan;                   // decode plan (units, splits)
   kvq::DevBuf partials;               // decode split partials
   kvq::DevBuf frags;                  // per-unit q operands of the tensor-core scan

@@ -79,7 +79,8 @@ kv_status_t ensure(DevBuf& b, size_t bytes) {
 
 // Packs several host arrays into one upload (one H2D copy per call).
 struct Upload {
-  std::vector<uint8_t> bytes;
+  std::vector<uint8_t>& bytes;   // the pool's scratch, emptied here
+  explicit Upload(std::vector<uint8_t>& b) : bytes(b) { bytes.clear(); }
   size_t add(const void* p, size_t n) {
     const size_t off = (bytes.size() + 255) & ~size_t(255);
     bytes.resize(off + n);
@@ -484,20 +485,36 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
   // then one partial staging page.  Page ids are taken in the same token
   // order as the per-token loop takes them, so both paths give the same pool.
   bool bulk = n_tok >= kPage;
-  for (int64_t t = 1; bulk && t < n_tok; ++t) bulk = req_ids[t] == req_ids[0];
-  std::vector<int32_t> i4, i2;                // the call's INT4 / INT2 token indices, in order
+  std::vector<int32_t>& i4 = P->scr_i4;       // the call's INT4 / INT2 token indices, in order
+  std::vector<int32_t>& i2 = P->scr_i2;
+  i4.clear();
+  i2.clear();
   int64_t b_cap4 = 0, b_new4 = 0, b_e = 0, b_ndirect = 0, b_rem = 0;
   int b_f4 = 0, b_s0 = 0;
   bool b_repack = false;
   if (bulk && !req_ok(P, req_ids[0])) bulk = false;   // the per-token path reports the error
   if (bulk) {
-    i4.reserve((size_t)n_tok);
-    i2.reserve((size_t)n_tok);
-    for (int64_t t = 0; bulk && t < n_tok; ++t) {
-      if (bits[t] == 4) i4.push_back((int32_t)t);
-      else if (bits[t] == 2) i2.push_back((int32_t)t);
-      else bulk = false;   // the per-token path reports the error (and any earlier one)
+    // one pass: same request throughout, bits valid; raw pointers and local
+    // counts (stores through vectors next to uint8_t loads defeat registers)
+    i4.resize((size_t)n_tok);
+    i2.resize((size_t)n_tok);
+    int32_t* p4 = i4.data();
+    int32_t* p2 = i2.data();
+    const int32_t r0 = req_ids[0];
+    int64_t c4 = 0, c2 = 0;
+    bool ok = true;
+    for (int64_t t = 0; t < n_tok; ++t) {
+      const uint32_t b = bits[t];
+      ok &= (req_ids[t] == r0) & ((b == 2u) | (b == 4u));
+      p4[c4] = (int32_t)t;
+      p2[c2] = (int32_t)t;
+      c4 += b == 4u;
+      c2 += b != 4u;
     }
+    // invalid input: the per-token path reports the error (and any earlier one)
+    bulk = ok;
+    i4.resize((size_t)c4);
+    i2.resize((size_t)c2);
   }
   if (bulk) {
     const int32_t r = req_ids[0];
@@ -566,8 +583,10 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
   std::vector<int32_t> job_req;                        // request of each job
   std::vector<RepackJob> repacks;
   std::vector<DirectJob> directs;
-  std::vector<int32_t> dtoks;                          // 32 token indices per direct job
-  std::vector<int32_t> toks;                           // token indices of the append jobs, job by job in slot order
+  std::vector<int32_t>& dtoks = P->scr_dtoks;          // 32 token indices per direct job
+  std::vector<int32_t>& toks = P->scr_toks;            // token indices of the append jobs, job by job in slot order
+  dtoks.clear();
+  toks.clear();
   std::vector<int32_t> deferred;
   Dirty dirty;   // table rewrites the append kernel does not cover (repacks)
   if (bulk) {
@@ -582,13 +601,24 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
     };
     auto slots = [](int first, int64_t n) { return (uint32_t)((n >= kPage ? 0xFFFFFFFFull : ((1ull << n) - 1)) << first); };
     // an append job over tokens idx[a .. a+n) into slots first .. of page
+    toks.resize((size_t)n_tok);   // at most every token; trimmed below
+    size_t ntoks = 0;
+    int32_t* const pos = P->pos.data();
+    uint32_t* const loc = R.loc.data();
     auto add_job = [&](int32_t page, int first, const std::vector<int32_t>& idx, int64_t a, int64_t n) {
-      jobs.push_back(AppendJob{page, first, (int32_t)n, (int32_t)toks.size(), -1, 0u, -1, 0});
+      jobs.push_back(AppendJob{page, first, (int32_t)n, (int32_t)ntoks, -1, 0u, -1, 0});
       job_req.push_back(r);
+      const int32_t* src = idx.data() + a;
+      int32_t* dst = toks.data() + ntoks;
+      int32_t* pp = pos + (size_t)page * kPage + first;
+      const uint32_t base = ((uint32_t)page << 5) | (uint32_t)first;
       for (int64_t q = 0; q < n; ++q) {
-        put(page, first + (int)q, idx[(size_t)(a + q)]);
-        toks.push_back(idx[(size_t)(a + q)]);
+        const int32_t t = src[q];
+        dst[q] = t;
+        pp[q] = (int32_t)(T0 + t);
+        loc[T0 + t] = base + (uint32_t)q;
       }
+      ntoks += (size_t)n;
       P->fill[page] = (uint8_t)(first + n);
       P->live[page] |= slots(first, n);
     };
@@ -670,6 +700,7 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
       app.emplace_back(i2[(size_t)a], sp);
       R.staging = sp;
     }
+    toks.resize(ntoks);
     std::sort(app.begin(), app.end());
     for (const auto& x : app) R.table.push_back(x.second);
     if (!app.empty() || b_repack) ++R.version;
@@ -800,7 +831,7 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
   emit_updates(P, dirty, upd);
 
   const bool small = jobs.size() <= (size_t)SmallAppend::kMaxJobs && off <= SmallAppend::kMaxToks;
-  Upload u;
+  Upload u(P->scr_upload);
   const size_t o_jobs = small ? 0 : u.add(jobs.data(), jobs.size() * sizeof(AppendJob));
   const size_t o_toks = small ? 0 : u.add(toks.data(), toks.size() * sizeof(int32_t));
   const size_t o_rep = u.add(repacks.data(), repacks.size() * sizeof(RepackJob));
@@ -849,7 +880,7 @@ kv_status_t kv_reorder_pages(kv_pool_t* P, const int32_t* req_ids, int32_t n_req
   if (st != KV_OK) return st;
   std::vector<TableUpd> upd;
   emit_updates(P, dirty, upd);
-  Upload u;
+  Upload u(P->scr_upload);
   const size_t o = u.add(upd.data(), upd.size() * sizeof(TableUpd));
   if ((st = upload(P, u, s)) != KV_OK) return st;
   KV_CUDA(launch_scatter(P, (const TableUpd*)((uint8_t*)P->upload.ptr + o), (int)upd.size(), s));
@@ -882,7 +913,7 @@ kv_status_t kv_evict_slots(kv_pool_t* P, const int32_t* req_ids, const int64_t* 
   if (st != KV_OK) return st;
   std::vector<TableUpd> upd;
   emit_updates(P, dirty, upd);
-  Upload u;
+  Upload u(P->scr_upload);
   const size_t o = u.add(upd.data(), upd.size() * sizeof(TableUpd));
   if ((st = upload(P, u, s)) != KV_OK) return st;
   KV_CUDA(launch_scatter(P, (const TableUpd*)((uint8_t*)P->upload.ptr + o), (int)upd.size(), s));
@@ -978,7 +1009,7 @@ kv_status_t build_plan(kv_pool* P, const int32_t* req_ids, int32_t batch, int32_
   HostPlan hp;
   plan_decode(P, req_ids, batch, (int64_t)P->sm_count * per_sm, mma ? kMinPagesPerWarp : kMinPagesPerCta,
               mma ? mma_page_cost(g) : kSimtPageCost, mma, hp);
-  Upload up;
+  Upload up(P->scr_upload);
   const size_t ou = up.add(hp.units.data(), hp.units.size() * sizeof(Unit));
   const size_t os = up.add(hp.splits.data(), hp.splits.size() * sizeof(Split));
   const size_t oc = up.add(hp.cta_split.data(), hp.cta_split.size() * sizeof(int32_t));
