@@ -223,7 +223,6 @@ struct kv_pool {
   // host scratch reused by every call (kept at capacity: fresh vectors cost
   // an allocation and first-touch page faults per call)
   std::vector<int32_t> scr_i4, scr_i2, scr_toks, scr_dtoks;
-  std::vector<uint8_t> scr_upload;
   kvq::DevBuf plan;                   // decode plan (units, splits)
   kvq::DevBuf partials;               // decode split partials
   kvq::DevBuf frags;                  // per-unit q operands of the tensor-core scan

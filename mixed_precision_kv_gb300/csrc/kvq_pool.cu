@@ -77,14 +77,22 @@ kv_status_t ensure(DevBuf& b, size_t bytes) {
   return KV_OK;
 }
 
-// Packs several host arrays into one upload (one H2D copy per call).
+// Several host arrays laid out for one upload (one H2D copy per call); the
+// arrays are copied straight into the pinned staging buffer by h2d (they must
+// stay alive until then).
 struct Upload {
-  std::vector<uint8_t>& bytes;   // the pool's scratch, emptied here
-  explicit Upload(std::vector<uint8_t>& b) : bytes(b) { bytes.clear(); }
-  size_t add(const void* p, size_t n) {
-    const size_t off = (bytes.size() + 255) & ~size_t(255);
-    bytes.resize(off + n);
-    if (n) std::memcpy(bytes.data() + off, p, n);
+  struct Piece {
+    const void* p;
+    size_t n, off;
+  };
+  static constexpr int kMaxPieces = 8;
+  Piece pieces[kMaxPieces];
+  int n_pieces = 0;
+  size_t size = 0;
+  size_t add(const void* p, size_t n) {   // byte offset of the array in the upload
+    const size_t off = (size + 255) & ~size_t(255);
+    pieces[n_pieces++] = Piece{p, n, off};
+    size = off + n;
     return off;
   }
 };
@@ -94,7 +102,8 @@ struct Upload {
 // calls the host keeps ahead of the GPU; from pinned memory it is queued like
 // a kernel.  A slot is reused after its previous copy has run (normally long
 // before: the ring has kPinnedSlots slots).
-kv_status_t h2d(kv_pool* P, void* dst, const void* src, size_t n, cudaStream_t s) {
+kv_status_t h2d(kv_pool* P, void* dst, const Upload& u, cudaStream_t s) {
+  const size_t n = u.size;
   if (n == 0) return KV_OK;
   kv_pool::PinnedSlot& sl = P->pinned[P->pinned_next];
   P->pinned_next = (P->pinned_next + 1) % kv_pool::kPinnedSlots;
@@ -111,7 +120,8 @@ kv_status_t h2d(kv_pool* P, void* dst, const void* src, size_t n, cudaStream_t s
     sl.cap = cap;
   }
   if (!sl.ev) KV_CUDA(cudaEventCreateWithFlags(&sl.ev, cudaEventDisableTiming));
-  std::memcpy(sl.ptr, src, n);
+  for (int i = 0; i < u.n_pieces; ++i)
+    if (u.pieces[i].n) std::memcpy((uint8_t*)sl.ptr + u.pieces[i].off, u.pieces[i].p, u.pieces[i].n);
   KV_CUDA(cudaMemcpyAsync(dst, sl.ptr, n, cudaMemcpyHostToDevice, s));
   KV_CUDA(cudaEventRecord(sl.ev, s));
   sl.pending = true;
@@ -119,10 +129,10 @@ kv_status_t h2d(kv_pool* P, void* dst, const void* src, size_t n, cudaStream_t s
 }
 
 kv_status_t upload(kv_pool* P, const Upload& u, cudaStream_t s) {
-  if (u.bytes.empty()) return KV_OK;
-  kv_status_t st = ensure(P->upload, u.bytes.size());
+  if (u.size == 0) return KV_OK;
+  kv_status_t st = ensure(P->upload, u.size);
   if (st != KV_OK) return st;
-  return h2d(P, P->upload.ptr, u.bytes.data(), u.bytes.size(), s);
+  return h2d(P, P->upload.ptr, u, s);
 }
 
 // Device table rows to rewrite after a call: per request, every entry from
@@ -684,8 +694,7 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
       P->live[sg] = 0xFFFFFFFFu;
       P->fill[nid] = kPage;
       P->live[nid] = 0xFFFFFFFFu;
-      directs.push_back(DirectJob{nid, (int32_t)dtoks.size()});
-      dtoks.insert(dtoks.end(), i2.begin() + a, i2.begin() + a + kPage);
+      directs.push_back(DirectJob{nid, (int32_t)a});   // its tokens: i2[a .. a+32), uploaded whole
       deferred.push_back(sg);
       app.emplace_back(i2[(size_t)(a + kPage - 1)], nid);
     }
@@ -831,12 +840,13 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
   emit_updates(P, dirty, upd);
 
   const bool small = jobs.size() <= (size_t)SmallAppend::kMaxJobs && off <= SmallAppend::kMaxToks;
-  Upload u(P->scr_upload);
+  Upload u;
   const size_t o_jobs = small ? 0 : u.add(jobs.data(), jobs.size() * sizeof(AppendJob));
   const size_t o_toks = small ? 0 : u.add(toks.data(), toks.size() * sizeof(int32_t));
   const size_t o_rep = u.add(repacks.data(), repacks.size() * sizeof(RepackJob));
   const size_t o_dir = u.add(directs.data(), directs.size() * sizeof(DirectJob));
-  const size_t o_dtok = u.add(dtoks.data(), dtoks.size() * sizeof(int32_t));
+  const std::vector<int32_t>& dtok_list = bulk ? i2 : dtoks;   // the bulk path indexes the INT2 token list
+  const size_t o_dtok = u.add(dtok_list.data(), (directs.empty() ? 0 : dtok_list.size()) * sizeof(int32_t));
   const size_t o_upd = u.add(upd.data(), upd.size() * sizeof(TableUpd));
   if ((st = upload(P, u, s)) != KV_OK) return st;
   uint8_t* base = (uint8_t*)P->upload.ptr;
@@ -880,7 +890,7 @@ kv_status_t kv_reorder_pages(kv_pool_t* P, const int32_t* req_ids, int32_t n_req
   if (st != KV_OK) return st;
   std::vector<TableUpd> upd;
   emit_updates(P, dirty, upd);
-  Upload u(P->scr_upload);
+  Upload u;
   const size_t o = u.add(upd.data(), upd.size() * sizeof(TableUpd));
   if ((st = upload(P, u, s)) != KV_OK) return st;
   KV_CUDA(launch_scatter(P, (const TableUpd*)((uint8_t*)P->upload.ptr + o), (int)upd.size(), s));
@@ -913,7 +923,7 @@ kv_status_t kv_evict_slots(kv_pool_t* P, const int32_t* req_ids, const int64_t* 
   if (st != KV_OK) return st;
   std::vector<TableUpd> upd;
   emit_updates(P, dirty, upd);
-  Upload u(P->scr_upload);
+  Upload u;
   const size_t o = u.add(upd.data(), upd.size() * sizeof(TableUpd));
   if ((st = upload(P, u, s)) != KV_OK) return st;
   KV_CUDA(launch_scatter(P, (const TableUpd*)((uint8_t*)P->upload.ptr + o), (int)upd.size(), s));
@@ -1009,13 +1019,13 @@ kv_status_t build_plan(kv_pool* P, const int32_t* req_ids, int32_t batch, int32_
   HostPlan hp;
   plan_decode(P, req_ids, batch, (int64_t)P->sm_count * per_sm, mma ? kMinPagesPerWarp : kMinPagesPerCta,
               mma ? mma_page_cost(g) : kSimtPageCost, mma, hp);
-  Upload up(P->scr_upload);
+  Upload up;
   const size_t ou = up.add(hp.units.data(), hp.units.size() * sizeof(Unit));
   const size_t os = up.add(hp.splits.data(), hp.splits.size() * sizeof(Split));
   const size_t oc = up.add(hp.cta_split.data(), hp.cta_split.size() * sizeof(int32_t));
-  kv_status_t st = ensure(P->plan, up.bytes.size());
+  kv_status_t st = ensure(P->plan, up.size);
   if (st != KV_OK) return st;
-  if ((st = h2d(P, P->plan.ptr, up.bytes.data(), up.bytes.size(), s)) != KV_OK) return st;
+  if ((st = h2d(P, P->plan.ptr, up, s)) != KV_OK) return st;
   P->plan_units_off = ou;
   P->plan_splits_off = os;
   P->plan_cta_off = oc;
