@@ -91,6 +91,24 @@ def _mixed(n, p2, seed):
     return np.where(np.random.default_rng(seed).random(n) < p2, 2, 4).astype(np.uint8)
 
 
+def test_bulk_append_every_run(kvq):
+    """Two one-request calls of 80 tokens laid out so that the second call
+    completes the open tail page and opens a new one, completes the open
+    staging page (repack), fills a 32-token group within the call (direct INT2)
+    and leaves a partial staging page, with INT2 and INT4 tokens alternating
+    (their page opens interleave).  Codes, tables and outputs against the
+    oracle, which follows the per-token rules."""
+    first = np.array([4, 2] * 30 + [4] * 20, np.uint8)      # 50 INT4 (tail 32 + 18), 30 INT2 (staging 30)
+    second = np.array([2, 4] * 40, np.uint8)                 # 40 INT2: 2 + 32 + 6; 40 INT4: 14 + 26
+    bits = [np.concatenate([first, second])]
+    sc = Scenario(kvq, 2, 8, bits, chunk=80)
+    sc.check_content()
+    sc.check_decode(what="bulk runs")
+    ex = sc.gpu.export(sc.g_ids[0], content=False)
+    assert int(ex["is_int2"].sum()) == 2                     # the repacked staging page and the direct group
+    assert int((ex["fill"] < 32).sum()) == 2                 # the partial INT4 tail and the partial staging page
+
+
 @pytest.mark.parametrize("impl", IMPLS)
 @pytest.mark.parametrize("n", [1, 2, 31, 32, 33, 63, 64, 65, 200])
 @pytest.mark.parametrize("p2", [0.0, 0.5, 1.0])
