@@ -39,19 +39,13 @@ __device__ __forceinline__ GroupMeta make_meta(float mn, float mx, float qmax) {
   return m;
 }
 
-__device__ __forceinline__ uint32_t qcode(float x, const GroupMeta& m, float qmax) {
-  if (!m.nz) return 0u;
-  const float u = __fdiv_rn(__fsub_rn(x, m.zf), m.sf);
-  const float r = fminf(fmaxf(rintf(u), 0.0f), qmax);
-  return (uint32_t)r;
-}
-
-// The same code without a division in the common case.  rs = approximate
+// code = clamp(rint(fl((x - zero) / scale)), 0, qmax) (0 when scale == 0),
+// without a division in the common case.  rs = approximate
 // reciprocal of m.sf (relative error < 2^-22), so q0 = u * rs lies within
 // 4e-6 of the correctly rounded quotient fl(u / s) for |u / s| < 64 (here
 // |u / s| <= qmax + 1).  When q0 is more than 1e-5 from every half-integer,
 // fl(u / s) rounds to the same integer; otherwise the quotient is computed
-// exactly.  Same result as qcode, bit for bit.
+// exactly.  Same result as the division form, bit for bit.
 __device__ __forceinline__ float approx_rcp(float x) {
   float y;
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -90,13 +84,21 @@ __device__ __forceinline__ void or_bits(uint8_t* img, int byte_off, int shift, u
 // for a later word-wise packing (pack_i4v) instead of being OR-ed into img.
 // vmax: the warp's running maximum of V scales (one atomic per warp at the
 // end instead of one per token on the pool's single maximum word).
-__device__ __forceinline__ bool quantize_token(uint8_t* img, const __nv_bfloat16* __restrict__ k,
-                                               const __nv_bfloat16* __restrict__ v, int t, int slot, int h, int hkv,
-                                               float& vmax, uint8_t* vcodes = nullptr) {
+// A token's K and V rows of one kv head, as each lane holds them (4 bf16
+// channels 4*lane .. 4*lane+3 of each).
+struct RawRows {
+  uint2 kr, vr;
+};
+__device__ __forceinline__ RawRows load_rows(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
+                                             int t, int h, int hkv) {
+  const size_t row = ((size_t)t * hkv + h) * kHeadDim + 4 * (threadIdx.x & 31);
+  return RawRows{*reinterpret_cast<const uint2*>(k + row), *reinterpret_cast<const uint2*>(v + row)};
+}
+
+__device__ __forceinline__ bool quantize_rows(uint8_t* img, const RawRows& rr, int slot, float& vmax,
+                                              uint8_t* vcodes = nullptr) {
   const int lane = threadIdx.x & 31, gr = lane >> 3;
-  const size_t row = ((size_t)t * hkv + h) * kHeadDim + 4 * lane;
-  const uint2 kr = *reinterpret_cast<const uint2*>(k + row);
-  const uint2 vr = *reinterpret_cast<const uint2*>(v + row);
+  const uint2 kr = rr.kr, vr = rr.vr;
   float xk[4], xv[4];
   xk[0] = __uint_as_float(kr.x << 16); xk[1] = __uint_as_float(kr.x & 0xFFFF0000u);
   xk[2] = __uint_as_float(kr.y << 16); xk[3] = __uint_as_float(kr.y & 0xFFFF0000u);
@@ -144,6 +146,29 @@ __device__ __forceinline__ bool quantize_token(uint8_t* img, const __nv_bfloat16
   return bad;
 }
 
+// The tokens j = warp, warp + W, ... < n of a job (W = warps per CTA), each
+// into slot first + j: their indices are read at once (lane q holds the q-th)
+// and the next token's rows are loaded while the current one is quantized.
+template <int W>
+__device__ __forceinline__ bool quantize_tokens(uint8_t* img, const __nv_bfloat16* __restrict__ k,
+                                                const __nv_bfloat16* __restrict__ v,
+                                                const int32_t* __restrict__ tk, int n, int first, int h, int hkv,
+                                                float& vmax, uint8_t* vcodes) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int mine = n > warp ? (n - warp + W - 1) / W : 0;   // <= 32 / W
+  const int t_l = lane < mine ? tk[warp + W * lane] : 0;
+  bool bad = false;
+  if (mine == 0) return bad;
+  RawRows cur = load_rows(k, v, __shfl_sync(0xFFFFFFFFu, t_l, 0), h, hkv);
+  for (int q = 0; q < mine; ++q) {
+    RawRows nxt = cur;
+    if (q + 1 < mine) nxt = load_rows(k, v, __shfl_sync(0xFFFFFFFFu, t_l, q + 1), h, hkv);
+    bad |= quantize_rows(img, cur, first + warp + W * q, vmax, vcodes);
+    cur = nxt;
+  }
+  return bad;
+}
+
 // One atomic per warp for the pool's running maximum of V scales
 // (non-negative floats order as their bits).
 __device__ __forceinline__ void flush_vmax(float vmax, uint32_t* __restrict__ status) {
@@ -186,7 +211,6 @@ __global__ void __launch_bounds__(kThreads) append_int4_kernel(
   const int h = blockIdx.y;
   uint8_t* blk = pool + int4_off + ((size_t)(job.page - n2) * hkv + h) * kInt4Block;
   const bool fresh = job.first_slot == 0;
-  const int warp = threadIdx.x >> 5;
   bool bad = false;
   float vmax = 0.0f;
   if (fresh) {
@@ -195,16 +219,16 @@ __global__ void __launch_bounds__(kThreads) append_int4_kernel(
     for (int i = threadIdx.x; i < kPage * kHeadDim / 16; i += kThreads)
       reinterpret_cast<uint4*>(vcodes)[i] = make_uint4(0, 0, 0, 0);
     __syncthreads();
-    for (int j = warp; j < job.n_slots; j += kThreads / 32)
-      bad |= quantize_token(img, k, v, tk[job.tok_off + j], job.first_slot + j, h, hkv, vmax, vcodes);
+    bad |= quantize_tokens<kThreads / 32>(img, k, v, tk + job.tok_off, job.n_slots, job.first_slot, h, hkv, vmax,
+                                          vcodes);
     __syncthreads();
     pack_i4v(img, vcodes);
     __syncthreads();
     uint4* out4 = reinterpret_cast<uint4*>(blk);
     for (int i = threadIdx.x; i < kInt4Block / 16; i += kThreads) out4[i] = img4[i];
   } else {
-    for (int j = warp; j < job.n_slots; j += kThreads / 32)
-      bad |= quantize_token(blk, k, v, tk[job.tok_off + j], job.first_slot + j, h, hkv, vmax);
+    bad |= quantize_tokens<kThreads / 32>(blk, k, v, tk + job.tok_off, job.n_slots, job.first_slot, h, hkv, vmax,
+                                          nullptr);
   }
   flush_vmax(vmax, status);
   if (bad) atomicOr(status, kStatusRange);
@@ -345,8 +369,8 @@ __global__ void __launch_bounds__(kThreads) direct_int2_kernel(
   const int h = blockIdx.y;
   bool bad = false;
   float vmax = 0.0f;
-  for (int j = threadIdx.x >> 5; j < kPage; j += kThreads / 32)   // every slot is written: no zeroing
-    bad |= quantize_token(img, k, v, toks[job.tok_off + j], j, h, hkv, vmax, codes);
+  // every slot is written: no zeroing
+  bad |= quantize_tokens<kThreads / 32>(img, k, v, toks + job.tok_off, kPage, 0, h, hkv, vmax, codes);
   flush_vmax(vmax, status);
   if (bad) atomicOr(status, kStatusRange);
   __syncthreads();
