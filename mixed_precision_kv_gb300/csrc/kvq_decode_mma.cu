@@ -638,10 +638,10 @@ __global__ void __launch_bounds__(256) frag_kernel(const __nv_bfloat16* __restri
                                                    UnitFrag* __restrict__ frags) {
   constexpr bool kPair = Cols<G>::kPair;
   __shared__ FragSmem S;
+  const Unit u = units[blockIdx.x];   // the plan is copied in before the launch (not by a kernel): read it first
   asm volatile("griddepcontrol.wait;" ::: "memory");   // the appends before this decode are done (scale maxima)
   asm volatile("griddepcontrol.launch_dependents;");   // the scan may be staged
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
-  const Unit u = units[blockIdx.x];
   const float smax = fmaxf(__uint_as_float(smax_bits[0]), 1.0f);
   {
     // thread (h, 4 channels); q needs only its element alignment

@@ -187,21 +187,51 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(
 template <int G>
 __global__ void __launch_bounds__(256) merge_kernel(const Unit* __restrict__ units, const float* __restrict__ part,
                                                     int hq, float* __restrict__ out) {
-  // Launched as a programmatic dependent of the scan: wait until the scan grid
-  // has completed and its partials are visible (immediate for a plain launch).
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;");   // the next call's kernels may be staged
   constexpr int kW = 8;
   __shared__ float mpart[kW], lpart[kW];
   __shared__ float4 apart[kW][32];
   const int ui = blockIdx.x / G, h = blockIdx.x - ui * G;
-  const Unit u = units[ui];
+  const Unit u = units[ui];   // the plan is copied in before the launch (not by a kernel): read it first
+  // Launched as a programmatic dependent of the scan: wait until the scan grid
+  // has completed and its partials are visible (immediate for a plain launch).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");   // the next call's kernels may be staged
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
   const size_t rs = (size_t)G * kPartStride;          // stride between splits
   const float* base = part + ((size_t)u.split_begin * G + h) * kPartStride;
   const int n = u.n_splits;
   float Mw = -INFINITY, Lw = 0.0f;
   float4 A = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  constexpr int kOne = 8;   // splits per warp read in one round (units of up to kW * kOne splits)
+  if (n <= kW * kOne) {
+    // every load of the warp's splits at once, then the weights
+    const int mine = n > w ? (n - w + kW - 1) / kW : 0;
+    float m[kOne], l[kOne];
+    float4 a[kOne];
+#pragma unroll
+    for (int j = 0; j < kOne; ++j) {
+      m[j] = -INFINITY;
+      l[j] = 0.0f;
+      a[j] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      if (j < mine) {
+        const float* ps = base + (size_t)(w + kW * j) * rs;
+        m[j] = ps[kHeadDim];
+        l[j] = ps[kHeadDim + 1];
+        a[j] = *reinterpret_cast<const float4*>(ps + 4 * lane);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kOne; ++j) Mw = fmaxf(Mw, m[j]);
+#pragma unroll
+    for (int j = 0; j < kOne; ++j) {
+      const float f = m[j] == -INFINITY ? 0.0f : exp2f(m[j] - Mw);   // an empty split adds nothing
+      Lw = fmaf(f, l[j], Lw);
+      A.x = fmaf(a[j].x, f, A.x);
+      A.y = fmaf(a[j].y, f, A.y);
+      A.z = fmaf(a[j].z, f, A.z);
+      A.w = fmaf(a[j].w, f, A.w);
+    }
+  } else
   for (int s0 = w; s0 < n; s0 += kW * 32) {           // 32 of the warp's splits per round
     const int s = s0 + kW * lane;
     float m = -INFINITY, l = 0.0f;
