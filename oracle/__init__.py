@@ -55,6 +55,9 @@ def lib():
                 "orc_append": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64]),
                 "orc_reorder": (ctypes.c_int, [_P, _P, ctypes.c_int]),
                 "orc_evict": (ctypes.c_int, [_P, _P, _P, _I64]),
+                "orc_evict_head": (ctypes.c_int, [_P, _P, _P, _P, _I64]),
+                "orc_fp_append": (ctypes.c_int, [_P, _I32, _P, _P, _I64]),
+                "orc_fp_drop": (ctypes.c_int, [_P, _I32, _I64, _I64]),
                 "orc_request_info": (ctypes.c_int, [_P, _I32, _P, _P]),
                 "orc_export": (ctypes.c_int, [_P, _I32, _P, _P, _P, _P, _P, _P, _P, _P]),
                 "orc_decode": (ctypes.c_int, [_P, _P, _P, ctypes.c_int, ctypes.c_int, _F32, _P, ctypes.c_int,
@@ -174,6 +177,23 @@ class OraclePool:
         req_ids = np.ascontiguousarray(req_ids, dtype=np.int32)
         pos = np.ascontiguousarray(pos, dtype=np.int64)
         return lib().orc_evict(self.h, _p(req_ids), _p(pos), req_ids.size)
+
+    def evict_head(self, req_ids, pos, kv_heads):
+        """Exclude each (request, position) for one kv head only."""
+        req_ids = np.ascontiguousarray(req_ids, dtype=np.int32)
+        pos = np.ascontiguousarray(pos, dtype=np.int64)
+        kv_heads = np.ascontiguousarray(kv_heads, dtype=np.int32)
+        return lib().orc_evict_head(self.h, _p(req_ids), _p(pos), _p(kv_heads), req_ids.size)
+
+    def fp_append(self, rid, k, v):
+        """Full-precision tokens; k, v: bf16 bits [n][len(sel)][128]."""
+        k = np.ascontiguousarray(k, dtype=np.uint16)
+        v = np.ascontiguousarray(v, dtype=np.uint16)
+        assert k.shape == v.shape and k.shape[1:] == (len(self.sel), 128)
+        return lib().orc_fp_append(self.h, rid, _p(k), _p(v), k.shape[0])
+
+    def fp_drop(self, rid, first, n):
+        return lib().orc_fp_drop(self.h, rid, first, n)
 
     def info(self, rid):
         n_pages = np.zeros(1, dtype=np.int32)

@@ -28,6 +28,15 @@
  *   - softmax attention in fp64, and a split + log-sum-exp merge variant
  *       [HyQuant, background "FlashAttention and online softmax" (m, l, acc;
  *        O = acc / l) and Algorithm 3 split-K ReduceSoftmax]
+ *   - full-precision segments: each key position belongs to exactly one of
+ *     the quantized set, the vertical-line set or the window of its head; the
+ *     vertical-line, staging and window tokens are kept in bf16 and scanned
+ *     after the quantized prefix with the same softmax state; the quantized
+ *     copy of a position held in full precision for one head is excluded for
+ *     that head only
+ *       [HyQuant, core method (K = K_VL u K_Win u K_Q, mutually exclusive),
+ *        Algorithm 3 (decode: quantized prefix, vertical lines, staging
+ *        buffer, window) and Algorithm 4 (FREEZE)]
  *
  * Readings of points the pages leave open (each restated where it is used):
  *   R1 scale and zero are stored as IEEE binary16 (round to nearest even).
@@ -47,6 +56,14 @@
  *      written are not tokens and are skipped.
  *   R7 the greedy scan skips a tag that does not fit the budget and continues;
  *      the budget test is exact integer arithmetic with B = num / den.
+ *   R8 a request's full-precision tokens form one ordered list per kv head
+ *      (the caller decides which are vertical-line, staging or window
+ *      tokens; every head holds the same count, its own rows); they follow
+ *      the quantized tokens in the token sequence; their logit is
+ *      scale * q . k and their value v, both read from bf16.  Dropping
+ *      tokens keeps the order of the rest.
+ *   R9 a slot excluded for one head reads, for that head, as the sentinel
+ *      dead slot of R6.
  */
 #include <algorithm>
 #include <cmath>
@@ -180,6 +197,7 @@ struct Page {
   bool int2 = false;
   int fill = 0;
   uint32_t live = 0;
+  std::vector<uint32_t> hdead;    // per kv head: slots excluded for that head only (R9)
   bool content = false;
   int64_t pos[kP];
   std::vector<HeadBlock> heads;
@@ -190,6 +208,8 @@ struct Req {
   std::vector<int32_t> table;
   int32_t tail4 = -1, staging = -1;
   std::vector<uint32_t> loc;      // token position -> page_id << 5 | slot
+  int64_t n_fp = 0;               // full-precision tokens (R8)
+  std::vector<uint16_t> fpk, fpv; // their bf16 bits [n_fp][n_sel][128]
 };
 
 struct Pool {
@@ -218,6 +238,7 @@ Page& new_page(Pool* P, bool int2, bool content) {
   pg = Page();
   pg.id = id;
   pg.int2 = int2;
+  pg.hdead.assign((size_t)P->hkv, 0u);
   pg.content = content;
   if (content) {
     pg.heads.resize(P->sel.size());
@@ -248,6 +269,7 @@ void write_int4_token(const Pool* P, Page& pg, int slot, const uint16_t* k, cons
 void repack_to_int2(const Pool* P, const Page& src, Page& dst) {
   dst.fill = kP;
   dst.live = src.live;
+  dst.hdead = src.hdead;
   std::memcpy(dst.pos, src.pos, sizeof(src.pos));
   if (!src.content) return;
   static thread_local float xk[kP * kD], xv[kP * kD];
@@ -468,6 +490,49 @@ int orc_evict(void* h, const int32_t* req, const int64_t* pos, int64_t n) {
   return ORC_OK;
 }
 
+// Exclude token positions for one kv head each (HyQuant: a vertical-line
+// token of a head leaves that head's quantized set; R9).
+int orc_evict_head(void* h, const int32_t* req, const int64_t* pos, const int32_t* kvh, int64_t n) {
+  Pool* P = (Pool*)h;
+  for (int64_t i = 0; i < n; ++i) {
+    if (req[i] < 0 || req[i] >= P->max_req || !P->reqs[req[i]].open) return ORC_INVALID;
+    if (pos[i] < 0 || pos[i] >= (int64_t)P->reqs[req[i]].loc.size()) return ORC_INVALID;
+    if (kvh[i] < 0 || kvh[i] >= P->hkv) return ORC_INVALID;
+  }
+  for (int64_t i = 0; i < n; ++i) {
+    const uint32_t l = P->reqs[req[i]].loc[pos[i]];
+    P->pages.at((int32_t)(l >> 5)).hdead[(size_t)kvh[i]] |= 1u << (l & 31u);
+  }
+  return ORC_OK;
+}
+
+// Append n full-precision tokens to a request's list (R8).  k, v: bf16 bits
+// [n][n_sel][128], the rows of the selected heads.
+int orc_fp_append(void* h, int32_t id, const uint16_t* k, const uint16_t* v, int64_t n) {
+  Pool* P = (Pool*)h;
+  if (id < 0 || id >= P->max_req || !P->reqs[id].open || n < 0 || (n > 0 && (!k || !v))) return ORC_INVALID;
+  Req& R = P->reqs[id];
+  const size_t m = (size_t)n * P->sel.size() * kD;
+  R.fpk.insert(R.fpk.end(), k, k + m);
+  R.fpv.insert(R.fpv.end(), v, v + m);
+  R.n_fp += n;
+  return ORC_OK;
+}
+
+// Remove full-precision tokens [first, first + n) of a request's list; the
+// rest keep their order (R8).
+int orc_fp_drop(void* h, int32_t id, int64_t first, int64_t n) {
+  Pool* P = (Pool*)h;
+  if (id < 0 || id >= P->max_req || !P->reqs[id].open) return ORC_INVALID;
+  Req& R = P->reqs[id];
+  if (first < 0 || n < 0 || first + n > R.n_fp) return ORC_INVALID;
+  const size_t row = P->sel.size() * kD;
+  R.fpk.erase(R.fpk.begin() + (ptrdiff_t)(first * row), R.fpk.begin() + (ptrdiff_t)((first + n) * row));
+  R.fpv.erase(R.fpv.begin() + (ptrdiff_t)(first * row), R.fpv.begin() + (ptrdiff_t)((first + n) * row));
+  R.n_fp -= n;
+  return ORC_OK;
+}
+
 int orc_request_info(void* h, int32_t id, int32_t* n_pages, int64_t* n_tok) {
   Pool* P = (Pool*)h;
   if (id < 0 || id >= P->max_req || !P->reqs[id].open) return ORC_INVALID;
@@ -508,7 +573,8 @@ int orc_export(void* h, int32_t id, int32_t* ids, uint8_t* is_int2, uint8_t* fil
 // Decode attention in fp64 for the listed (batch row, q head) pairs.
 // q: bf16 bits [B][Hq][128]; kv head of q head hq is hq / (Hq / Hkv).
 // n_splits <= 1: one softmax pass.  n_splits > 1: the token sequence (table
-// order, slot order) is cut into n_splits contiguous chunks; each chunk keeps
+// order, slot order, then the full-precision list) is cut into n_splits
+// contiguous chunks; each chunk keeps
 // (m, l, acc) and the chunks are merged by log-sum-exp (HyQuant, online
 // softmax and Algorithm 3 ReduceSoftmax).  A request with no tokens gives 0.
 // out: [n_pairs][128].
@@ -536,15 +602,19 @@ int orc_decode(void* h, const uint16_t* q, const int32_t* req, int B, int Hq, fl
     const size_t j = (size_t)(std::find(P->sel.begin(), P->sel.end(), kv) - P->sel.begin());
     double qd[kD];
     for (int c = 0; c < kD; ++c) qd[c] = (double)bf16_to_f32(q[((size_t)b * Hq + hq) * kD + c]);
-    // Token list in table order: (logit, pointer to page block, slot, live).
+    // Token list: the quantized tokens in table order, then the
+    // full-precision tokens in list order (R8).  Per token: logit, source of
+    // V (page block and slot, or a bf16 row), live.
     std::vector<double> logit;
     std::vector<std::pair<const HeadBlock*, int>> src;
+    std::vector<const uint16_t*> fprow;
     std::vector<bool> alive;
     for (int32_t pid : R.table) {
       const Page& pg = P->pages.at(pid);
       const HeadBlock& hb = pg.heads[j];
+      const uint32_t live = pg.live & ~pg.hdead[(size_t)kv];   // R9
       for (int s = 0; s < pg.fill; ++s) {
-        const bool lv = (pg.live >> s) & 1u;
+        const bool lv = (live >> s) & 1u;
         double l = -1e4;                                   // sentinel dead slot (R6)
         if (lv) {
           double acc = 0.0;
@@ -556,8 +626,19 @@ int orc_decode(void* h, const uint16_t* q, const int32_t* req, int B, int Hq, fl
         }
         logit.push_back(l);
         src.push_back({&hb, s});
+        fprow.push_back(nullptr);
         alive.push_back(lv);
       }
+    }
+    const size_t nsel = P->sel.size();
+    for (int64_t t = 0; t < R.n_fp; ++t) {
+      const uint16_t* kr = R.fpk.data() + ((size_t)t * nsel + j) * kD;
+      double acc = 0.0;
+      for (int c = 0; c < kD; ++c) acc += qd[c] * (double)bf16_to_f32(kr[c]);
+      logit.push_back((double)scale * acc);
+      src.push_back({nullptr, 0});
+      fprow.push_back(R.fpv.data() + ((size_t)t * nsel + j) * kD);
+      alive.push_back(true);
     }
     double* o = out + (size_t)i * kD;
     for (int c = 0; c < kD; ++c) o[c] = 0.0;
@@ -575,6 +656,10 @@ int orc_decode(void* h, const uint16_t* q, const int32_t* req, int B, int Hq, fl
         const double w = std::exp(logit[t] - m);
         l += w;
         if (!alive[t]) continue;                           // V = 0 at the dead slot
+        if (fprow[t]) {
+          for (int c = 0; c < kD; ++c) acc[c] += w * (double)bf16_to_f32(fprow[t][c]);
+          continue;
+        }
         const HeadBlock& hb = *src[t].first;
         const int s = src[t].second;
         for (int c = 0; c < kD; ++c) {
