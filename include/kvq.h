@@ -125,6 +125,47 @@ KVQ_API kv_status_t kv_reorder_pages(kv_pool_t* pool, const int32_t* req_ids, in
 KVQ_API kv_status_t kv_evict_slots(kv_pool_t* pool, const int32_t* req_ids, const int64_t* token_pos, int64_t n,
                            void* stream);
 
+/* Per-head exclusion (HyQuant, core method: each key position belongs to
+ * exactly one of the quantized set, the vertical-line set and the window of a
+ * head, and vertical lines are chosen per kv head).  For each i, slot
+ * token_pos[i] of request req_ids[i] reads as the sentinel dead slot for kv
+ * head kv_heads[i] only; the other heads still read it.  The exclusion moves
+ * with the slot when a staging page is requantized to INT2.
+ * req_ids, kv_heads: host int32 [n]; token_pos: host int64 [n].  The first call
+ * allocates one 32-bit word per (page, kv head) on the device and makes both
+ * decode scans read it.  Excluding twice is a no-op; an invalid entry fails
+ * the call before any change (KV_ERR_INVALID_ARG). */
+KVQ_API kv_status_t kv_evict_slots_head(kv_pool_t* pool, const int32_t* req_ids, const int64_t* token_pos,
+                                        const int32_t* kv_heads, int64_t n, void* stream);
+
+/* Full-precision token lists (HyQuant, Algorithm 3 and Algorithm 4 FREEZE:
+ * the vertical-line tokens, the staging buffer and the window stay in full
+ * precision and are scanned after the quantized prefix under the same online
+ * softmax state).  Each request has one ordered list per kv head, every head
+ * the same length and its own rows; kv_decode_attn scans the quantized pages,
+ * then the list, and merges both with the split partials.  Which tokens a list
+ * holds is the caller's choice (e.g. a head's vertical lines, excluded from
+ * its quantized set with kv_evict_slots_head, and the most recent tokens).
+ *
+ * kv_fp_configure: capacity of every list in tokens (device memory:
+ * 2 x max_requests x num_kv_heads x max_tokens x 256 bytes); 0 frees it.
+ * Every list must be empty.  Synchronizes the device. */
+KVQ_API kv_status_t kv_fp_configure(kv_pool_t* pool, int32_t max_tokens);
+
+/* Append n_tok tokens to request req_id's lists.
+ *   k, v  device, bf16 [n_tok][num_kv_heads][128] (row h of token t goes to
+ *         kv head h's list); any 2-byte alignment.
+ * The values are used as given.  KV_ERR_OOM past the capacity (no change). */
+KVQ_API kv_status_t kv_fp_append(kv_pool_t* pool, int32_t req_id, const void* k, const void* v, int64_t n_tok,
+                                 void* stream);
+
+/* Remove list tokens [first, first + n_tok) of every head of a request; the
+ * rest keep their order.  A range outside the list is KV_ERR_INVALID_ARG. */
+KVQ_API kv_status_t kv_fp_drop(kv_pool_t* pool, int32_t req_id, int64_t first, int64_t n_tok, void* stream);
+
+/* Host output: the length of a request's lists. */
+KVQ_API kv_status_t kv_fp_count(kv_pool_t* pool, int32_t req_id, int64_t* n_tok);
+
 /* Decode-step GQA attention over the page tables (TriAxialKV key design 4,
  * HyQuant Algorithm 3).
  *   q        device, bf16 [batch][num_q_heads][128]
@@ -184,7 +225,8 @@ KVQ_API kv_status_t kv_export_request(kv_pool_t* pool, int32_t req_id, int32_t* 
 
 /* Algorithmic bytes and split count of the most recent kv_decode_attn call:
  * codes + scale/zero of every page block read (partial INT4 pages count their
- * filled prefix), 8 bytes per table entry, q (bf16) and out (fp32). */
+ * filled prefix), 8 bytes per table entry, q (bf16) and out (fp32), and the
+ * bf16 K and V rows of the full-precision lists. */
 KVQ_API kv_status_t kv_last_decode_stats(kv_pool_t* pool, int64_t* kv_bytes, int32_t* n_splits, int64_t* n_pages);
 
 /* Device-time measurement of the decode kernels.  enable = N >= 1 starts (or

@@ -25,7 +25,8 @@ HEAD_DIM, PAGE_TOKENS, GROUP = 128, 32, 32
 EXPORTED = ["kv_pool_create", "kv_pool_destroy", "kv_request_open", "kv_request_close", "kv_append_quant",
             "kv_reorder_pages", "kv_evict_slots", "kv_decode_attn", "kv_set_decode_impl", "kv_pool_sync",
             "kv_request_info", "kv_export_request", "kv_last_decode_stats", "kv_pool_launch_count", "kv_alloc_bits",
-            "kv_last_error", "kv_decode_attn_noalloc", "kv_decode_timing"]
+            "kv_last_error", "kv_decode_attn_noalloc", "kv_decode_timing", "kv_evict_slots_head", "kv_fp_configure",
+            "kv_fp_append", "kv_fp_drop", "kv_fp_count"]
 
 _P = ctypes.c_void_p
 _I32, _I64 = ctypes.c_int32, ctypes.c_int64
@@ -63,6 +64,11 @@ def load_library(path: str = LIB_PATH):
             "kv_append_quant": [_P, _P, _P, _P, _P, _I64, _P],
             "kv_reorder_pages": [_P, _P, _I32, _P],
             "kv_evict_slots": [_P, _P, _P, _I64, _P],
+            "kv_evict_slots_head": [_P, _P, _P, _P, _I64, _P],
+            "kv_fp_configure": [_P, _I32],
+            "kv_fp_append": [_P, _I32, _P, _P, _I64, _P],
+            "kv_fp_drop": [_P, _I32, _I64, _I64, _P],
+            "kv_fp_count": [_P, _I32, _P],
             "kv_decode_attn": [_P, _P, _P, _I32, _I32, ctypes.c_float, _P, _P],
             "kv_decode_attn_noalloc": [_P, _P, _P, _I32, _I32, ctypes.c_float, _P, _P],
             "kv_set_decode_impl": [_P, _I32],
@@ -206,6 +212,39 @@ class KVPool:
             raise ValueError("req_ids and token_pos differ in length")
         _check(load_library().kv_evict_slots(self._h, _ptr(req_ids), _ptr(token_pos), req_ids.size,
                                              _stream(stream, self.device)), "kv_evict_slots")
+
+    def evict_head(self, req_ids, token_pos, kv_heads, stream=None):
+        """kv_evict_slots_head: each (request, position) reads as dead for one kv head."""
+        req_ids = _np(req_ids, np.int32)
+        token_pos = _np(token_pos, np.int64)
+        kv_heads = _np(kv_heads, np.int32)
+        if not (req_ids.size == token_pos.size == kv_heads.size):
+            raise ValueError("req_ids, token_pos and kv_heads differ in length")
+        _check(load_library().kv_evict_slots_head(self._h, _ptr(req_ids), _ptr(token_pos), _ptr(kv_heads),
+                                                  req_ids.size, _stream(stream, self.device)), "kv_evict_slots_head")
+
+    def fp_configure(self, max_tokens):
+        """kv_fp_configure: capacity of every request's full-precision lists."""
+        _check(load_library().kv_fp_configure(self._h, int(max_tokens)), "kv_fp_configure")
+
+    def fp_append(self, rid, k, v, stream=None):
+        """kv_fp_append: k, v torch bf16 CUDA tensors [n][Hkv][128]."""
+        n = int(k.shape[0])
+        if n:
+            self._check_kv(k, n)
+            self._check_kv(v, n)
+        _check(load_library().kv_fp_append(self._h, int(rid), k.data_ptr() if n else None,
+                                           v.data_ptr() if n else None, n, _stream(stream, self.device)),
+               "kv_fp_append")
+
+    def fp_drop(self, rid, first, n, stream=None):
+        _check(load_library().kv_fp_drop(self._h, int(rid), int(first), int(n), _stream(stream, self.device)),
+               "kv_fp_drop")
+
+    def fp_count(self, rid) -> int:
+        n = ctypes.c_int64(0)
+        _check(load_library().kv_fp_count(self._h, int(rid), ctypes.byref(n)), "kv_fp_count")
+        return int(n.value)
 
     def decode(self, q, req_ids, softmax_scale, out=None, stream=None):
         """q: torch bf16 CUDA [B][Hq][128] -> out fp32 [B][Hq][128]."""

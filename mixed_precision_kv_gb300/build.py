@@ -9,7 +9,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 SO = os.path.join(HERE, "libkvq.so")
-SOURCES = ["kvq_pool.cu", "kvq_quant.cu", "kvq_decode_simt.cu", "kvq_decode_mma.cu", "kvq_noalloc.cu"]
+SOURCES = ["kvq_pool.cu", "kvq_quant.cu", "kvq_decode_simt.cu", "kvq_decode_mma.cu", "kvq_noalloc.cu", "kvq_fp.cu"]
 HEADERS = ["kvq_internal.h", "kvq_layout.cuh"]
 NVCC_FLAGS = ["-std=c++17", "-O3", "-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo",
               "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden"]

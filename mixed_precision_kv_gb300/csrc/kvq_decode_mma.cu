@@ -724,13 +724,16 @@ __global__ void __launch_bounds__(256) frag_kernel(const __nv_bfloat16* __restri
 // ---- persistent scan: warp gw = blockIdx.x * kWarps + w of the n_workers
 // workers owns the splits [wsplit[gw], wsplit[gw + 1]): contiguous page ranges
 // of consecutive units, cut so that every warp gets about the same cost.  The
-// warp writes one partial per split.
-template <int G>
+// warp writes one partial per split.  kHead: some slots are excluded for
+// single kv heads (hdead, one word per page id x kv head); without it the
+// scan does not carry the extra pointer.
+template <int G, bool kHead>
 __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(
     const uint8_t* __restrict__ pool, size_t int4_off, int64_t n2, int hkv, int max_pages,
     const Entry* __restrict__ table, const UnitFrag* __restrict__ frags, const Split* __restrict__ splits,
-    const int32_t* __restrict__ wsplit, int n_workers, const int32_t* __restrict__ ntab, float* __restrict__ part,
-    const uint32_t* __restrict__ smax_bits, uint32_t* __restrict__ status) {
+    const int32_t* __restrict__ wsplit, int n_workers, const int32_t* __restrict__ ntab,
+    const uint32_t* __restrict__ hdead, float* __restrict__ part, const uint32_t* __restrict__ smax_bits,
+    uint32_t* __restrict__ status) {
   constexpr bool kPair = Cols<G>::kPair;
   constexpr int NH = Cols<G>::NH;
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -799,7 +802,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(
       }
       const Entry e = ltab[idx];
       bid = e.id;
-      blive = e.live;
+      // slots excluded for this kv head only read as dead slots too
+      if constexpr (kHead) blive = e.live & ~hdead[(size_t)e.id * hkv + lkvh];
+      else blive = e.live;
       btag = (lsg << 6) | lkvh;
       const uint8_t* src = e.id < n2 ? pool + ((size_t)e.id * hkv + lkvh) * kInt2Block
                                      : pool + int4_off + ((size_t)(e.id - n2) * hkv + lkvh) * kInt4Block;
@@ -975,9 +980,9 @@ constexpr int kScanSmem = kWarps * (int)sizeof(WarpSmem);
 // shares the SM's memory with shared memory: ask for the smallest shared
 // carveout that holds one CTA (the default takes the largest, leaving L1 too
 // small for 16 warps' q operands; the scan then ran up to 1.45x slower).
-template <int G>
+template <int G, bool kHead>
 cudaError_t set_scan_attributes() {
-  cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, kScanSmem);
+  cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<G, kHead>, cudaFuncAttributeMaxDynamicSharedMemorySize, kScanSmem);
   if (e != cudaSuccess) return e;
   int dev = 0, per_sm = 0, reserved = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
@@ -985,7 +990,7 @@ cudaError_t set_scan_attributes() {
   if ((e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev)) != cudaSuccess) return e;
   if (per_sm <= 0) return cudaErrorInvalidValue;
   const int pct = std::min(100, (int)(((int64_t)(kScanSmem + reserved) * 100 + per_sm - 1) / per_sm));
-  return cudaFuncSetAttribute(decode_mma_kernel<G>, cudaFuncAttributePreferredSharedMemoryCarveout, pct);
+  return cudaFuncSetAttribute(decode_mma_kernel<G, kHead>, cudaFuncAttributePreferredSharedMemoryCarveout, pct);
 }
 
 template <int G>
@@ -994,7 +999,8 @@ cudaError_t launch_mma_g(kv_pool* P, const void* q, int32_t hq, float scale_log2
                          cudaStream_t s) {
   static bool attr_set = false;
   if (!attr_set) {
-    const cudaError_t e = set_scan_attributes<G>();
+    cudaError_t e = set_scan_attributes<G, false>();
+    if (e == cudaSuccess) e = set_scan_attributes<G, true>();
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -1005,17 +1011,18 @@ cudaError_t launch_mma_g(kv_pool* P, const void* q, int32_t hq, float scale_log2
                              (int)hq, scale_log2, d_units, smax, (UnitFrag*)d_frags);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)((n_workers + kWarps - 1) / kWarps);
-  return launch_pdl(decode_mma_kernel<G>, dim3(grid), dim3(kThreads), (size_t)kScanSmem, s,
-                    (const uint8_t*)P->d_pool, P->int4_offset, (int64_t)P->cfg.n_int2_pages, P->cfg.num_kv_heads,
-                    P->cfg.max_pages_per_request, (const Entry*)P->d_table, (const UnitFrag*)d_frags, d_splits,
-                    d_wsplit, n_workers, (const int32_t*)P->d_ntab, d_part, smax, P->d_status);
+  auto* kernel = P->hdead.empty() ? decode_mma_kernel<G, false> : decode_mma_kernel<G, true>;
+  return launch_pdl(kernel, dim3(grid), dim3(kThreads), (size_t)kScanSmem, s, (const uint8_t*)P->d_pool,
+                    P->int4_offset, (int64_t)P->cfg.n_int2_pages, P->cfg.num_kv_heads, P->cfg.max_pages_per_request,
+                    (const Entry*)P->d_table, (const UnitFrag*)d_frags, d_splits, d_wsplit, n_workers,
+                    (const int32_t*)P->d_ntab, (const uint32_t*)P->d_hdead, d_part, smax, P->d_status);
 }
 
 template <int G>
 int mma_occupancy() {
   int n = 0;
-  if (set_scan_attributes<G>() != cudaSuccess) return 1;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<G>, kThreads, kScanSmem) != cudaSuccess)
+  if (set_scan_attributes<G, false>() != cudaSuccess) return 1;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<G, false>, kThreads, kScanSmem) != cudaSuccess)
     return 1;
   return n > 0 ? n : 1;
 }

@@ -43,7 +43,7 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(
     const uint8_t* __restrict__ pool, size_t int4_off, int64_t n2, int hkv, int max_pages,
     const Entry* __restrict__ table, const __nv_bfloat16* __restrict__ q, int hq, float scale_log2,
     const Unit* __restrict__ units, const Split* __restrict__ splits, const int32_t* __restrict__ cta_split,
-    const int32_t* __restrict__ ntab, float* __restrict__ part) {
+    const int32_t* __restrict__ ntab, const uint32_t* __restrict__ hdead, float* __restrict__ part) {
   asm volatile("griddepcontrol.wait;" ::: "memory");   // the appends before this decode are done
   asm volatile("griddepcontrol.launch_dependents;");   // the merge may be scheduled as CTAs retire
   __shared__ float qs[G][kHeadDim];
@@ -75,6 +75,8 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(
   uint8_t* bw = buf[w];
   for (int pi = sp.page_begin + w; pi < page_end; pi += kWarps) {
     const Entry e = tab[pi];
+    // slots excluded for this kv head only read as dead slots too
+    const uint32_t live = hdead ? e.live & ~hdead[(size_t)e.id * hkv + u.kvh] : e.live;
     const bool i2 = e.id < n2;
     const uint8_t* blk = i2 ? pool + ((size_t)e.id * hkv + u.kvh) * kInt2Block
                             : pool + int4_off + ((size_t)(e.id - n2) * hkv + u.kvh) * kInt4Block;
@@ -109,7 +111,7 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(
         }
       }
     }
-    const bool alive = (e.live >> t) & 1u;
+    const bool alive = (live >> t) & 1u;
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       const float lg = alive ? s[h] * scale_log2 : kDeadLogit2;
@@ -198,8 +200,11 @@ __global__ void __launch_bounds__(256) merge_kernel(const Unit* __restrict__ uni
   asm volatile("griddepcontrol.launch_dependents;");   // the next call's kernels may be staged
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
   const size_t rs = (size_t)G * kPartStride;          // stride between splits
+  // the unit's page splits, then its full-precision splits
   const float* base = part + ((size_t)u.split_begin * G + h) * kPartStride;
-  const int n = u.n_splits;
+  const float* fbase = part + ((size_t)u.fp_begin * G + h) * kPartStride;
+  const int nq = u.n_splits, n = nq + u.n_fp_splits;
+  auto split_at = [&](int s) { return s < nq ? base + (size_t)s * rs : fbase + (size_t)(s - nq) * rs; };
   float Mw = -INFINITY, Lw = 0.0f;
   float4 A = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
   constexpr int kOne = 8;   // splits per warp read in one round (units of up to kW * kOne splits)
@@ -214,7 +219,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const Unit* __restrict__ uni
       l[j] = 0.0f;
       a[j] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
       if (j < mine) {
-        const float* ps = base + (size_t)(w + kW * j) * rs;
+        const float* ps = split_at(w + kW * j);
         m[j] = ps[kHeadDim];
         l[j] = ps[kHeadDim + 1];
         a[j] = *reinterpret_cast<const float4*>(ps + 4 * lane);
@@ -236,8 +241,8 @@ __global__ void __launch_bounds__(256) merge_kernel(const Unit* __restrict__ uni
     const int s = s0 + kW * lane;
     float m = -INFINITY, l = 0.0f;
     if (s < n) {
-      m = base[s * rs + kHeadDim];
-      l = base[s * rs + kHeadDim + 1];
+      m = split_at(s)[kHeadDim];
+      l = split_at(s)[kHeadDim + 1];
     }
     float mx = m;
 #pragma unroll
@@ -255,7 +260,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const Unit* __restrict__ uni
 #pragma unroll 8
     for (int j = 0; j < cnt; ++j) {
       const float fj = __shfl_sync(0xFFFFFFFFu, f, j);
-      const float4 a = *reinterpret_cast<const float4*>(base + (size_t)(s0 + kW * j) * rs + 4 * lane);
+      const float4 a = *reinterpret_cast<const float4*>(split_at(s0 + kW * j) + 4 * lane);
       A.x = fmaf(a.x, fj, A.x);
       A.y = fmaf(a.y, fj, A.y);
       A.z = fmaf(a.z, fj, A.z);
@@ -297,7 +302,8 @@ cudaError_t launch_g(kv_pool* P, const void* q, int32_t hq, float scale_log2, co
                                      (const uint8_t*)P->d_pool, P->int4_offset, (int64_t)P->cfg.n_int2_pages,
                                      P->cfg.num_kv_heads, P->cfg.max_pages_per_request, (const Entry*)P->d_table,
                                      (const __nv_bfloat16*)q, (int)hq, scale_log2, d_units, d_splits, d_cta,
-                                     (const int32_t*)P->d_ntab, d_part);
+                                     (const int32_t*)P->d_ntab, (const uint32_t*)(P->hdead.empty() ? nullptr : P->d_hdead),
+                                     d_part);
     if (e != cudaSuccess) return e;
   }
   if (P->merge_event) {

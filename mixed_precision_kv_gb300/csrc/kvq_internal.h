@@ -25,9 +25,9 @@ struct Entry {
 
 // Host -> device table update, applied by a scatter kernel.
 struct TableUpd {
-  uint32_t index;   // kind 0: flat entry index r * max_pages + i; kind 1: request r
-  int32_t a;        // kind 0: page id; kind 1: table length
-  uint32_t b;       // kind 0: live mask
+  uint32_t index;   // kind 0: flat entry index r * max_pages + i; kind 1: request r; kind 2: page id
+  int32_t a;        // kind 0: page id; kind 1: table length; kind 2: kv head
+  uint32_t b;       // kind 0: live mask; kind 2: the page's slots excluded for that head
   uint32_t kind;
 };
 
@@ -64,15 +64,23 @@ struct DirectJob {
 };
 
 // Work unit of the decode: one (batch row, kv head).  Its splits (page ranges,
-// one partial each) are contiguous in the split list.
+// one partial each) are contiguous in the split list, and so are the splits
+// of its full-precision tokens (after every unit's page splits).
 struct Unit {
   int32_t b;            // batch row
   int32_t req;          // request id
   int32_t kvh;          // kv head
   int32_t split_begin;  // first split of this unit
   int32_t n_splits;     // number of splits (0 = no tokens)
-  int32_t pad[3];
+  int32_t fp_begin;     // first full-precision split of this unit
+  int32_t n_fp_splits;  // number of full-precision splits
+  int32_t pad;
 };
+
+// Full-precision tokens per full-precision split.  Such a split is a Split
+// whose page_begin / page_end are token indices of the request's list
+// (page_end < 0: to the list's length at launch).
+constexpr int kFpChunk = 64;
 
 // A split: a range of one unit's pages in scan order, scanned by one worker
 // (a CTA of the CUDA-core scan, a warp of the tensor-core scan).  Worker k
@@ -139,7 +147,8 @@ constexpr int64_t kTimingRing = 2048;
 // Decode plan on the host (see plan_decode).
 struct HostPlan {
   std::vector<Unit> units;
-  std::vector<Split> splits;
+  std::vector<Split> splits;        // page splits, then full-precision splits
+  int32_t n_page_splits = 0;
   std::vector<int32_t> cta_split;   // n_workers + 1 entries
   int64_t n_ctas() const { return (int64_t)cta_split.size() - 1; }   // workers
 };
@@ -226,6 +235,17 @@ struct kv_pool {
   kvq::DevBuf plan;                   // decode plan (units, splits)
   kvq::DevBuf partials;               // decode split partials
   kvq::DevBuf frags;                  // per-unit q operands of the tensor-core scan
+  // per-head exclusion (allocated by the first kv_evict_slots_head): per page
+  // id x kv head, the slots that read as dead for that head only
+  uint32_t* d_hdead = nullptr;
+  std::vector<uint32_t> hdead;
+  // full-precision token lists: K and V bf16 [max_requests][kv head][fp_cap][128]
+  uint16_t* d_fpk = nullptr;
+  uint16_t* d_fpv = nullptr;
+  int32_t* d_nfp = nullptr;           // [max_requests] list lengths, written in stream order
+  int32_t fp_cap = 0;
+  std::vector<int32_t> n_fp;          // host mirror of the lengths
+  kvq::DevBuf fp_scratch;             // kv_fp_drop staging
   // host mirror
   std::vector<kvq::Request> reqs;
   std::vector<uint8_t> fill;          // per page id
@@ -237,10 +257,12 @@ struct kv_pool {
   // decode plan cache
   std::vector<int32_t> plan_req;
   std::vector<int32_t> plan_len;      // table lengths of plan_req when the plan was built
+  std::vector<int32_t> plan_nfp;      // full-precision list lengths when the plan was built
   int32_t plan_slack = 0;             // pages a table may grow before the plan is rebuilt
   int32_t plan_hq = 0;
   int32_t plan_impl = -1;
   int32_t n_units = 0, n_splits = 0;
+  int32_t n_page_splits = 0;          // splits [0, n_page_splits) are page splits, the rest full-precision
   size_t plan_units_off = 0, plan_splits_off = 0, plan_cta_off = 0;
   int32_t n_ctas = 0;
   std::vector<int32_t> stat_req;      // request ids of the last decode (for kv_last_decode_stats)
@@ -296,6 +318,17 @@ cudaError_t launch_scatter(kv_pool* P, const TableUpd* d_upd, int n, cudaStream_
 // otherwise in table order.
 void plan_decode(const kv_pool* P, const int32_t* req_ids, int32_t batch, int64_t n_workers, int64_t min_pages,
                  PageCost cost, bool spread, HostPlan& out);
+
+// Full-precision splits (kvq_fp.cu): one partial per split of kFpChunk tokens,
+// written at split index first_split + i of d_part.  Launched in stream order
+// (no programmatic overlap).
+cudaError_t launch_fp_segments(kv_pool* P, const void* q, int32_t hq, float scale_log2, const Unit* d_units,
+                               const Split* d_fsplits, int n_fsplits, int first_split, float* d_part, cudaStream_t s);
+// Copies into / within the full-precision lists (kvq_fp.cu).
+cudaError_t launch_fp_store(kv_pool* P, int32_t req, const void* k, const void* v, int64_t n, int32_t at,
+                            cudaStream_t s);
+cudaError_t launch_fp_move(kv_pool* P, int32_t req, int32_t from, int32_t to, int32_t n, int32_t new_len,
+                           cudaStream_t s);
 
 // Launchers (kvq_decode_simt.cu / kvq_decode_mma.cu)
 cudaError_t launch_decode_simt(kv_pool* P, const void* q, int32_t hq, float scale_log2, const Unit* d_units,

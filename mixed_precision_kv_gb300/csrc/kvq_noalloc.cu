@@ -92,7 +92,7 @@ extern "C" kv_status_t kv_decode_attn_noalloc(kv_pool_t* P, const void* q, const
 
   // Plan: the same balanced plan as kv_decode_attn, with the worker count
   // capped so that plan + partials fit the scratch (a plan of n workers has
-  // at most n + units - 1 splits).
+  // at most n + units - 1 page splits, plus the full-precision splits).
   const int32_t impl = P->decode_impl == KV_DECODE_AUTO ? KV_DECODE_MMA : P->decode_impl;
   const bool mma = impl == KV_DECODE_MMA;
   const int per_sm = mma ? decode_mma_workers_per_sm(g) : decode_simt_ctas_per_sm(g);
@@ -101,7 +101,10 @@ extern "C" kv_status_t kv_decode_attn_noalloc(kv_pool_t* P, const void* q, const
   const size_t frags_bytes = mma ? align256((size_t)n_units * decode_mma_frag_bytes()) : 0;
   const int64_t budget = (int64_t)((kScratchBytes - units_bytes - frags_bytes - 1024) /
                                    (sizeof(Split) + sizeof(int32_t) + part_bytes));
-  const int64_t n_workers = std::min<int64_t>((int64_t)P->sm_count * per_sm, budget - n_units);
+  int64_t n_fsplits = 0;   // full-precision splits the plan adds (kFpChunk tokens each)
+  for (int32_t b = 0; b < batch && !P->n_fp.empty(); ++b)
+    n_fsplits += (int64_t)hkv * ((P->n_fp[req_ids[b]] + kFpChunk - 1) / kFpChunk);
+  const int64_t n_workers = std::min<int64_t>((int64_t)P->sm_count * per_sm, budget - n_units - n_fsplits);
   if (n_workers < 1)
     return nfail(KV_ERR_INVALID_ARG, "kv_decode_attn_noalloc: the plan does not fit the fixed scratch");
   HostPlan hp;
@@ -124,6 +127,13 @@ extern "C" kv_status_t kv_decode_attn_noalloc(kv_pool_t* P, const void* q, const
   if (cudaMemcpyAsync(base, host.data(), frags_off, cudaMemcpyHostToDevice, s) != cudaSuccess)
     return nfail(KV_ERR_CUDA, "kv_decode_attn_noalloc: plan upload failed");
   const float scale_log2 = softmax_scale * 1.4426950408889634f;
+  const int n_fp_splits = (int)hp.splits.size() - hp.n_page_splits;
+  if (n_fp_splits > 0) {
+    const cudaError_t ef = launch_fp_segments(P, q, hq, scale_log2, (const Unit*)base,
+                                              (const Split*)(base + splits_off) + hp.n_page_splits, n_fp_splits,
+                                              hp.n_page_splits, (float*)(base + part_off), s);
+    if (ef != cudaSuccess) return nfail(KV_ERR_CUDA, cudaGetErrorString(ef));
+  }
   const cudaError_t e =
       impl == KV_DECODE_MMA
           ? launch_decode_mma(P, q, hq, scale_log2, (const Unit*)base, (int)n_units, (const Split*)(base + splits_off),

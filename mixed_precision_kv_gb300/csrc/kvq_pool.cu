@@ -60,6 +60,36 @@ bool req_ok(const kv_pool* P, int32_t r) {
 
 bool is_int2(const kv_pool* P, int32_t id) { return id < P->cfg.n_int2_pages; }
 
+// Per-head exclusion words (kept once kv_evict_slots_head has been used):
+// host mirror changes, each queued as a kind-2 table update for the device.
+void hdead_set(kv_pool* P, int32_t id, int h, uint32_t val, std::vector<TableUpd>& hu) {
+  uint32_t& w = P->hdead[(size_t)id * P->cfg.num_kv_heads + h];
+  if (w != val) {
+    w = val;
+    hu.push_back(TableUpd{(uint32_t)id, h, val, 2u});
+  }
+}
+void hdead_copy(kv_pool* P, int32_t dst, int32_t src, std::vector<TableUpd>& hu) {
+  if (P->hdead.empty()) return;
+  for (int h = 0; h < P->cfg.num_kv_heads; ++h)
+    hdead_set(P, dst, h, P->hdead[(size_t)src * P->cfg.num_kv_heads + h], hu);
+}
+void hdead_clear(kv_pool* P, int32_t id, std::vector<TableUpd>& hu) {
+  if (P->hdead.empty()) return;
+  for (int h = 0; h < P->cfg.num_kv_heads; ++h) hdead_set(P, id, h, 0u, hu);
+}
+// One update per word, carrying its final value: the scatter kernel applies
+// updates in no particular order.
+void hdead_final(const kv_pool* P, std::vector<TableUpd>& hu) {
+  std::sort(hu.begin(), hu.end(), [](const TableUpd& x, const TableUpd& y) {
+    return x.index != y.index ? x.index < y.index : x.a < y.a;
+  });
+  hu.erase(std::unique(hu.begin(), hu.end(),
+                       [](const TableUpd& x, const TableUpd& y) { return x.index == y.index && x.a == y.a; }),
+           hu.end());
+  for (auto& u : hu) u.b = P->hdead[(size_t)u.index * P->cfg.num_kv_heads + u.a];
+}
+
 
 // Grow a device buffer to at least `bytes` (contents are not kept).
 kv_status_t ensure(DevBuf& b, size_t bytes) {
@@ -263,6 +293,20 @@ void kvq::plan_decode(const kv_pool* P, const int32_t* req_ids, int32_t batch, i
     }
   }
   while (cur < n) out.cta_split[++cur] = (int32_t)out.splits.size();
+  // full-precision splits: kFpChunk tokens each, after all page splits; a
+  // unit's last one runs to the list's length at launch
+  out.n_page_splits = (int32_t)out.splits.size();
+  for (int32_t b = 0; b < batch; ++b) {
+    const int32_t nf = P->n_fp.empty() ? 0 : P->n_fp[req_ids[b]];
+    for (int h = 0; h < hkv; ++h) {
+      Unit& u = out.units[(size_t)b * hkv + h];
+      u.fp_begin = (int32_t)out.splits.size();
+      for (int32_t t = 0; t < nf; t += kFpChunk)
+        out.splits.push_back(Split{b * hkv + h, t, std::min(nf, t + kFpChunk), req_ids[b], 0, 0, {0, 0}});
+      u.n_fp_splits = (int32_t)out.splits.size() - u.fp_begin;
+      if (u.n_fp_splits > 0) out.splits.back().page_end = -1;
+    }
+  }
 }
 
 extern "C" {
@@ -376,6 +420,11 @@ kv_status_t kv_pool_destroy(kv_pool_t* P) {
   cudaFree(P->plan.ptr);
   cudaFree(P->partials.ptr);
   cudaFree(P->frags.ptr);
+  cudaFree(P->d_hdead);
+  cudaFree(P->d_fpk);
+  cudaFree(P->d_fpv);
+  cudaFree(P->d_nfp);
+  cudaFree(P->fp_scratch.ptr);
   for (cudaEvent_t e : P->tev)
     if (e) cudaEventDestroy(e);
   for (auto& sl : P->pinned) {
@@ -402,11 +451,24 @@ kv_status_t kv_request_open(kv_pool_t* P, int32_t* req_id) {
 
 kv_status_t kv_request_close(kv_pool_t* P, int32_t r) {
   if (!P || !req_ok(P, r)) return fail(KV_ERR_INVALID_ARG, "kv_request_close: request %d is not open", r);
+  if (!P->hdead.empty()) {
+    // the device words of freed pages are cleared before their ids return
+    DeviceGuard dg(P->cfg.device);
+    const int hkv = P->cfg.num_kv_heads;
+    for (int32_t id : P->reqs[r].table) {
+      uint32_t* w = &P->hdead[(size_t)id * hkv];
+      if (std::any_of(w, w + hkv, [](uint32_t x) { return x != 0u; })) {
+        std::fill(w, w + hkv, 0u);
+        KV_CUDA(cudaMemsetAsync(P->d_hdead + (size_t)id * hkv, 0, (size_t)hkv * sizeof(uint32_t), P->last_stream));
+      }
+    }
+  }
   for (int32_t id : P->reqs[r].table) {
     P->fill[id] = 0;
     P->live[id] = 0;
     (is_int2(P, id) ? P->free2 : P->free4).insert(id);
   }
+  if (!P->n_fp.empty()) P->n_fp[r] = 0;
   const uint64_t v = P->reqs[r].version;
   P->reqs[r] = Request();
   P->reqs[r].version = v + 1;
@@ -599,6 +661,7 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
   toks.clear();
   std::vector<int32_t> deferred;
   Dirty dirty;   // table rewrites the append kernel does not cover (repacks)
+  std::vector<TableUpd> hupd;   // per-head exclusion words carried by repacks / cleared by frees
   if (bulk) {
     const int32_t r = req_ids[0];
     Request& R = P->reqs[r];
@@ -666,6 +729,7 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
       const int32_t sp = R.staging;
       P->fill[nid_rep] = kPage;
       P->live[nid_rep] = P->live[sp];
+      hdead_copy(P, nid_rep, sp, hupd);
       for (int sl = 0; sl < kPage; ++sl) {
         const int32_t pp = P->pos[(size_t)sp * kPage + sl];
         P->pos[(size_t)nid_rep * kPage + sl] = pp;
@@ -759,6 +823,7 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
       const int32_t nid = P->free2.take_lowest();
       P->fill[nid] = kPage;
       P->live[nid] = P->live[cur];
+      hdead_copy(P, nid, cur, hupd);
       for (int sl = 0; sl < kPage; ++sl) {
         const int32_t p = P->pos[(size_t)cur * kPage + sl];
         P->pos[(size_t)nid * kPage + sl] = p;
@@ -796,6 +861,7 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
   for (int32_t id : deferred) {
     P->fill[id] = 0;
     P->live[id] = 0;
+    hdead_clear(P, id, hupd);
     P->free4.insert(id);
   }
   // Table entries the append kernel writes: each job's page where it sits in
@@ -838,6 +904,8 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
   }
   std::vector<TableUpd> upd;
   emit_updates(P, dirty, upd);
+  hdead_final(P, hupd);
+  upd.insert(upd.end(), hupd.begin(), hupd.end());
 
   const bool small = jobs.size() <= (size_t)SmallAppend::kMaxJobs && off <= SmallAppend::kMaxToks;
   Upload u;
@@ -930,6 +998,131 @@ kv_status_t kv_evict_slots(kv_pool_t* P, const int32_t* req_ids, const int64_t* 
   return KV_OK;
 }
 
+kv_status_t kv_evict_slots_head(kv_pool_t* P, const int32_t* req_ids, const int64_t* token_pos,
+                                const int32_t* kv_heads, int64_t n, void* stream) {
+  if (!P || n < 0 || (n > 0 && (!req_ids || !token_pos || !kv_heads)))
+    return fail(KV_ERR_INVALID_ARG, "kv_evict_slots_head: bad arguments");
+  const int hkv = P->cfg.num_kv_heads;
+  for (int64_t i = 0; i < n; ++i) {
+    if (!req_ok(P, req_ids[i])) return fail(KV_ERR_INVALID_ARG, "kv_evict_slots_head: request %d not open", req_ids[i]);
+    if (token_pos[i] < 0 || token_pos[i] >= (int64_t)P->reqs[req_ids[i]].loc.size())
+      return fail(KV_ERR_INVALID_ARG, "kv_evict_slots_head: position %lld out of range", (long long)token_pos[i]);
+    if (kv_heads[i] < 0 || kv_heads[i] >= hkv)
+      return fail(KV_ERR_INVALID_ARG, "kv_evict_slots_head: kv head %d out of range", kv_heads[i]);
+  }
+  if (n == 0) return KV_OK;
+  DeviceGuard dg(P->cfg.device);
+  cudaStream_t s = (cudaStream_t)stream;
+  kv_status_t st = order_after_previous(P, s);
+  if (st != KV_OK) return st;
+  if (P->hdead.empty()) {
+    // first use: one exclusion word per (page id, kv head), all clear
+    const size_t words = P->fill.size() * (size_t)hkv;
+    if (cudaMalloc(&P->d_hdead, words * sizeof(uint32_t)) != cudaSuccess) {
+      cudaGetLastError();
+      P->d_hdead = nullptr;
+      return fail(KV_ERR_OOM, "kv_evict_slots_head: cannot allocate %zu exclusion words", words);
+    }
+    KV_CUDA(cudaMemsetAsync(P->d_hdead, 0, words * sizeof(uint32_t), s));
+    try {
+      P->hdead.assign(words, 0u);
+    } catch (...) {
+      cudaFree(P->d_hdead);
+      P->d_hdead = nullptr;
+      return fail(KV_ERR_OOM, "kv_evict_slots_head: host allocation failed");
+    }
+  }
+  std::vector<TableUpd> upd;
+  for (int64_t i = 0; i < n; ++i) {
+    const uint32_t l = P->reqs[req_ids[i]].loc[token_pos[i]];
+    const int32_t id = (int32_t)(l >> 5);
+    hdead_set(P, id, kv_heads[i], P->hdead[(size_t)id * hkv + kv_heads[i]] | (1u << (l & 31u)), upd);
+  }
+  if (upd.empty()) return KV_OK;
+  hdead_final(P, upd);
+  Upload u;
+  const size_t o = u.add(upd.data(), upd.size() * sizeof(TableUpd));
+  if ((st = upload(P, u, s)) != KV_OK) return st;
+  KV_CUDA(launch_scatter(P, (const TableUpd*)((uint8_t*)P->upload.ptr + o), (int)upd.size(), s));
+  return KV_OK;
+}
+
+kv_status_t kv_fp_configure(kv_pool_t* P, int32_t max_tokens) {
+  if (!P || max_tokens < 0) return fail(KV_ERR_INVALID_ARG, "kv_fp_configure: bad arguments");
+  for (int32_t x : P->n_fp)
+    if (x > 0) return fail(KV_ERR_INVALID_ARG, "kv_fp_configure: a full-precision list is not empty");
+  DeviceGuard dg(P->cfg.device);
+  if (P->last_stream) KV_CUDA(cudaStreamSynchronize(P->last_stream));
+  KV_CUDA(cudaDeviceSynchronize());
+  cudaFree(P->d_fpk);
+  cudaFree(P->d_fpv);
+  cudaFree(P->d_nfp);
+  P->d_fpk = P->d_fpv = nullptr;
+  P->d_nfp = nullptr;
+  P->fp_cap = 0;
+  P->n_fp.clear();
+  if (max_tokens == 0) return KV_OK;
+  const size_t rows = (size_t)P->cfg.max_requests * P->cfg.num_kv_heads * (size_t)max_tokens;
+  const size_t bytes = rows * kHeadDim * sizeof(uint16_t);
+  if (cudaMalloc(&P->d_fpk, bytes) != cudaSuccess || cudaMalloc(&P->d_fpv, bytes) != cudaSuccess ||
+      cudaMalloc(&P->d_nfp, (size_t)P->cfg.max_requests * sizeof(int32_t)) != cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(P->d_fpk);
+    cudaFree(P->d_fpv);
+    cudaFree(P->d_nfp);
+    P->d_fpk = P->d_fpv = nullptr;
+    P->d_nfp = nullptr;
+    return fail(KV_ERR_OOM, "kv_fp_configure: cannot allocate 2 x %zu bytes of lists", bytes);
+  }
+  KV_CUDA(cudaMemset(P->d_nfp, 0, (size_t)P->cfg.max_requests * sizeof(int32_t)));
+  KV_CUDA(cudaDeviceSynchronize());
+  P->fp_cap = max_tokens;
+  P->n_fp.assign((size_t)P->cfg.max_requests, 0);
+  return KV_OK;
+}
+
+kv_status_t kv_fp_append(kv_pool_t* P, int32_t r, const void* k, const void* v, int64_t n_tok, void* stream) {
+  if (!P || !req_ok(P, r) || n_tok < 0 || (n_tok > 0 && (!k || !v)))
+    return fail(KV_ERR_INVALID_ARG, "kv_fp_append: bad arguments (request %d)", P ? r : -1);
+  if (P->fp_cap == 0) return fail(KV_ERR_INVALID_ARG, "kv_fp_append: kv_fp_configure has not been called");
+  if ((int64_t)P->n_fp[r] + n_tok > P->fp_cap)
+    return fail(KV_ERR_OOM, "kv_fp_append: %lld tokens exceed the list capacity %d", (long long)(P->n_fp[r] + n_tok),
+                P->fp_cap);
+  if (n_tok == 0) return KV_OK;
+  DeviceGuard dg(P->cfg.device);
+  cudaStream_t s = (cudaStream_t)stream;
+  kv_status_t st = order_after_previous(P, s);
+  if (st != KV_OK) return st;
+  KV_CUDA(launch_fp_store(P, r, k, v, n_tok, P->n_fp[r], s));
+  P->n_fp[r] += (int32_t)n_tok;
+  return KV_OK;
+}
+
+kv_status_t kv_fp_drop(kv_pool_t* P, int32_t r, int64_t first, int64_t n_tok, void* stream) {
+  if (!P || !req_ok(P, r)) return fail(KV_ERR_INVALID_ARG, "kv_fp_drop: request %d not open", P ? r : -1);
+  const int64_t len = P->n_fp.empty() ? 0 : P->n_fp[r];
+  if (first < 0 || n_tok < 0 || first + n_tok > len)
+    return fail(KV_ERR_INVALID_ARG, "kv_fp_drop: range [%lld, %lld) outside the list of %lld tokens", (long long)first,
+                (long long)(first + n_tok), (long long)len);
+  if (n_tok == 0) return KV_OK;
+  DeviceGuard dg(P->cfg.device);
+  cudaStream_t s = (cudaStream_t)stream;
+  kv_status_t st = order_after_previous(P, s);
+  if (st != KV_OK) return st;
+  const int64_t tail = len - first - n_tok;
+  if ((st = ensure(P->fp_scratch, (size_t)std::max<int64_t>(1, 2 * tail * P->cfg.num_kv_heads * kHeadDim * 2))) != KV_OK)
+    return st;
+  KV_CUDA(launch_fp_move(P, r, (int32_t)(first + n_tok), (int32_t)first, (int32_t)tail, (int32_t)(len - n_tok), s));
+  P->n_fp[r] = (int32_t)(len - n_tok);
+  return KV_OK;
+}
+
+kv_status_t kv_fp_count(kv_pool_t* P, int32_t r, int64_t* n_tok) {
+  if (!P || !req_ok(P, r) || !n_tok) return fail(KV_ERR_INVALID_ARG, "kv_fp_count: bad arguments");
+  *n_tok = P->n_fp.empty() ? 0 : P->n_fp[r];
+  return KV_OK;
+}
+
 kv_status_t kv_export_request(kv_pool_t* P, int32_t r, int32_t* ids, uint8_t* is2, uint8_t* fill, uint32_t* live,
                               uint8_t* kc, uint8_t* vc, uint16_t* km, uint16_t* vm) {
   if (!P || !req_ok(P, r)) return fail(KV_ERR_INVALID_ARG, "kv_export_request: request %d not open", r);
@@ -1007,10 +1200,15 @@ kv_status_t build_plan(kv_pool* P, const int32_t* req_ids, int32_t batch, int32_
   // Tables that grew add their new pages to the tail CTA, so the plan is
   // rebuilt once a table has grown past the slack (or an empty table gained
   // pages, which has no split yet).
+  // Full-precision splits follow the same rule: a unit's last one is
+  // open-ended, and the plan is rebuilt once a list has grown by a chunk, has
+  // shrunk, or was empty.
   bool same = P->plan_impl == impl && P->plan_hq == hq && (int32_t)P->plan_req.size() == batch;
   for (int32_t b = 0; same && b < batch; ++b) {
     const int32_t len = (int32_t)P->reqs[req_ids[b]].table.size(), len0 = P->plan_len[b];
     same = P->plan_req[b] == req_ids[b] && len >= len0 && len - len0 <= P->plan_slack && (len0 > 0 || len == 0);
+    const int32_t nf = P->n_fp.empty() ? 0 : P->n_fp[req_ids[b]], nf0 = P->plan_nfp[b];
+    same = same && nf >= nf0 && nf - nf0 < kFpChunk && (nf0 > 0 || nf == 0);
   }
   if (same) return KV_OK;
 
@@ -1031,9 +1229,12 @@ kv_status_t build_plan(kv_pool* P, const int32_t* req_ids, int32_t batch, int32_
   P->plan_cta_off = oc;
   P->n_units = (int32_t)hp.units.size();
   P->n_splits = (int32_t)hp.splits.size();
+  P->n_page_splits = hp.n_page_splits;
   P->n_ctas = (int32_t)hp.n_ctas();
   P->plan_req.assign(req_ids, req_ids + batch);
   P->plan_len.resize(batch);
+  P->plan_nfp.resize(batch);
+  for (int32_t b = 0; b < batch; ++b) P->plan_nfp[b] = P->n_fp.empty() ? 0 : P->n_fp[req_ids[b]];
   int64_t total_pages = 0;
   for (int32_t b = 0; b < batch; ++b) {
     P->plan_len[b] = (int32_t)P->reqs[req_ids[b]].table.size();
@@ -1080,6 +1281,8 @@ kv_status_t kv_decode_attn(kv_pool_t* P, const void* q, const int32_t* req_ids, 
   cudaEvent_t* tv = rec ? &P->tev[3 * (size_t)(P->timed_calls % kTimingRing)] : nullptr;
   if (tv) KV_CUDA(cudaEventRecord(tv[0], s));
   P->merge_event = tv ? tv[1] : nullptr;
+  KV_CUDA(launch_fp_segments(P, q, hq, scale_log2, du, dsp + P->n_page_splits, P->n_splits - P->n_page_splits,
+                             P->n_page_splits, (float*)P->partials.ptr, s));
   if (impl == KV_DECODE_MMA)
     KV_CUDA(launch_decode_mma(P, q, hq, scale_log2, du, P->n_units, dsp, dct, P->n_ctas, P->frags.ptr,
                               (float*)P->partials.ptr, out, s));
@@ -1148,6 +1351,7 @@ kv_status_t kv_last_decode_stats(kv_pool_t* P, int64_t* kv_bytes, int32_t* n_spl
       ++pages;
     }
     bytes += (int64_t)P->stat_hq * kHeadDim * (2 + 4);
+    if (!P->n_fp.empty()) bytes += (int64_t)P->n_fp[r] * hkv * kHeadDim * 2 * 2;   // full-precision K and V
   }
   if (kv_bytes) *kv_bytes = bytes;
   if (n_splits) *n_splits = P->n_splits;

@@ -383,13 +383,14 @@ __global__ void __launch_bounds__(kThreads) direct_int2_kernel(
     reinterpret_cast<uint4*>(dblk)[i] = reinterpret_cast<const uint4*>(dst)[i];
 }
 
-__global__ void scatter_kernel(Entry* __restrict__ table, int32_t* __restrict__ ntab,
-                               const TableUpd* __restrict__ upd, int n) {
+__global__ void scatter_kernel(Entry* __restrict__ table, int32_t* __restrict__ ntab, uint32_t* __restrict__ hdead,
+                               int hkv, const TableUpd* __restrict__ upd, int n) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n) return;
   const TableUpd u = upd[i];
   if (u.kind == 0) table[u.index] = Entry{u.a, u.b};
-  else ntab[u.index] = u.a;
+  else if (u.kind == 1) ntab[u.index] = u.a;
+  else if (hdead) hdead[(size_t)u.index * hkv + u.a] = u.b;   // kind 2: per-head exclusion word
 }
 
 }  // namespace
@@ -433,7 +434,7 @@ cudaError_t launch_direct_int2(kv_pool* P, const void* k, const void* v, const D
 cudaError_t launch_scatter(kv_pool* P, const TableUpd* d_upd, int n, cudaStream_t s) {
   if (n <= 0) return cudaSuccess;
   ++P->launches;
-  scatter_kernel<<<(n + 255) / 256, 256, 0, s>>>(P->d_table, P->d_ntab, d_upd, n);
+  scatter_kernel<<<(n + 255) / 256, 256, 0, s>>>(P->d_table, P->d_ntab, P->d_hdead, P->cfg.num_kv_heads, d_upd, n);
   return cudaGetLastError();
 }
 
