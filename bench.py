@@ -261,6 +261,10 @@ def main():
     ap.add_argument("--config", type=int, default=2)
     ap.add_argument("--decode-impl", default="auto", choices=["auto", "simt", "mma"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--segments", action="store_true",
+                    help="decode with full-precision segments: per kv head 5%% vertical-line tokens excluded from "
+                         "its quantized set, a 128-token window and a 128-token staging buffer in bf16; every "
+                         "128 steps the staging buffer is quantized into the pool")
     ap.add_argument("--mode", default="decode", choices=["decode", "prefill"],
                     help="decode: the decode-step line (default); prefill: bulk quantization of the workload's "
                          "prompts through kv_append_quant")
@@ -283,11 +287,16 @@ def main():
         dist.init_process_group("nccl")
     e2e_steps = max(args.steps // 4, 10)
     total_steps = args.warmup + args.steps + 3 + e2e_steps
+    SEG_W = SEG_WS = 128   # HyQuant window W and staging capacity W_s
+    extra = SEG_W if args.segments else 0   # the frozen window is quantized again by the first flush
     w = kvsynth.make_workload(args.config, steps=total_steps)
-    gw = GPUWorkload(w, device=local, steps=total_steps)
+    gw = GPUWorkload(w, device=local, steps=total_steps, extra_tokens=extra)
     gw.pool.set_decode_impl({"auto": 0, "simt": 1, "mma": 2}[args.decode_impl])
     gw.prefill()
     gw.evict()
+    n_vl = []
+    if args.segments:
+        win_k, win_v, n_vl = gw.freeze_segments(rho=0.05, window=SEG_W, staging=SEG_WS)
     gw.reorder()
     gw.pool.sync()
     B, Hkv, Hq = len(gw.rids), w.num_kv_heads, w.num_q_heads
@@ -315,6 +324,41 @@ def main():
         gw.pool.reorder(rids)
         return gw.pool.decode(qs[s] if q is None else q, rids, w.softmax_scale, out=out)
 
+    # Decode step with full-precision segments (HyQuant, Algorithm 3): the new
+    # token joins the window; once window + staging hold W + W_s tokens, the
+    # oldest W_s (the staging buffer) leave the lists and are quantized into
+    # the pool.  The lists' non-vertical-line part is a queue of W_s-token
+    # blocks: the frozen prefill window first, then blocks of step tokens.
+    seg = {"fill": SEG_W, "blocks": [None], "cur": 0, "cur_len": 0, "fp_tok": 0}
+    if args.segments:
+        win_bits = np.stack([gw.bits[r][w.requests[r].n_prefill - SEG_W:w.requests[r].n_prefill] for r in range(B)], 1)
+        rids_blk = np.tile(rids, SEG_WS)
+
+    def seg_step(s, k=None, v=None, q=None):
+        gw.pool.fp_append(rids, ks[s] if k is None else k, vs[s] if v is None else v)
+        if seg["cur_len"] == 0:
+            seg["cur"] = s
+        seg["cur_len"] += 1
+        if seg["cur_len"] == SEG_WS:
+            seg["blocks"].append(seg["cur"])
+            seg["cur_len"] = 0
+        seg["fill"] += 1
+        if seg["fill"] == SEG_W + SEG_WS:
+            a = seg["blocks"].pop(0)
+            kb, vb, bb = (win_k, win_v, win_bits) if a is None else (ks[a:a + SEG_WS], vs[a:a + SEG_WS],
+                                                                    bits[a:a + SEG_WS])
+            for r in range(B):
+                gw.pool.fp_drop(rids[r], n_vl[r], SEG_WS)
+            gw.pool.append(kb.reshape(SEG_WS * B, Hkv, 128), vb.reshape(SEG_WS * B, Hkv, 128), rids_blk,
+                           np.ascontiguousarray(bb).reshape(-1))
+            gw.pool.reorder(rids)
+            seg["fill"] -= SEG_WS
+        seg["fp_tok"] += sum(n_vl) + B * seg["fill"]
+        return gw.pool.decode(qs[s] if q is None else q, rids, w.softmax_scale, out=out)
+
+    if args.segments:
+        step = seg_step
+
     for s in range(args.warmup):
         step(s)
     gw.pool.sync()
@@ -325,7 +369,9 @@ def main():
     # kv bytes per step: host accounting of the tables, read before and after
     # the timed steps (a step adds one token per request, so bytes grow
     # linearly and the mean of the two ends is the mean step)
-    kv_first = gw.pool.last_decode_stats()["kv_bytes"]
+    fp_row = Hkv * 128 * 2 * 2   # bf16 K and V of one list token, all kv heads
+    kv_first = gw.pool.last_decode_stats()["kv_bytes"] - (sum(n_vl) + B * seg["fill"]) * fp_row * args.segments
+    seg["fp_tok"] = 0
     launches0 = gw.pool.launch_count()
     # library-recorded events around the scan and merge of every 8th timed
     # decode (an event between scan and merge stops the merge's launch from
@@ -336,26 +382,31 @@ def main():
         torch.cuda.synchronize()
         torch.cuda.nvtx.range_push("timed")
         start.record(stream)
-        for i in range(args.steps):
-            s = s0 + i
-            gw.pool.append(ks[s], vs[s], rids, bits[s])
-            gw.pool.reorder(rids)
-            gw.pool.decode(qs[s], rids, w.softmax_scale, out=out)
+        if args.segments:
+            for i in range(args.steps):
+                seg_step(s0 + i)
+        else:
+            for i in range(args.steps):
+                s = s0 + i
+                gw.pool.append(ks[s], vs[s], rids, bits[s])
+                gw.pool.reorder(rids)
+                gw.pool.decode(qs[s], rids, w.softmax_scale, out=out)
         end.record(stream)
         torch.cuda.synchronize()
         torch.cuda.nvtx.range_pop()
     if dist:
         dist.barrier()
-    kv_last = gw.pool.last_decode_stats()["kv_bytes"]
+    kv_last = gw.pool.last_decode_stats()["kv_bytes"] - (sum(n_vl) + B * seg["fill"]) * fp_row * args.segments
+    fp_mean = seg["fp_tok"] / args.steps * fp_row if args.segments else 0.0
     launches = gw.pool.launch_count() - launches0
     n_timed, scan_ms, dec_ms = gw.pool.decode_timing(False)
     gw.pool.sync()
     t_ms = reduce_max_time(start.elapsed_time(end), dist, dev)
-    step_bytes = 0.5 * (kv_first + kv_last)
+    step_bytes = 0.5 * (kv_first + kv_last) + fp_mean
     value = job_throughput(step_bytes, args.steps, ws, t_ms)
     achieved = step_bytes / (scan_ms / 1e3) / 1e9
     peak, peak_kind = measured_peak()
-    traffic = recorded_traffic(step_bytes, w.name, args.decode_impl)
+    traffic = None if args.segments else recorded_traffic(step_bytes, w.name, args.decode_impl)
 
     # End to end: host (pinned) inputs copied in and the output copied out every step.
     s_e = s0 + args.steps + 3
@@ -390,7 +441,7 @@ def main():
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": t_ms / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "u4/u2 codes, f16 meta, f32 accum", "data": "synthetic",
-            "config": {"workload": w.name, "batch": B, "num_q_heads": Hq, "num_kv_heads": Hkv, "head_dim": 128,
+            "config": {"workload": w.name + ("+fp-segments" if args.segments else ""), "batch": B, "num_q_heads": Hq, "num_kv_heads": Hkv, "head_dim": 128,
                        "context": w.requests[0].n_prefill, "page_tokens": 32, "budget_bits": "3.0",
                        "decode_impl": args.decode_impl, "l2": "inputs larger than L2 (%.0f MB per step)"
                                                              % (step_bytes / 1e6),
@@ -403,6 +454,10 @@ def main():
                                    "the launch stream around every 8th launch of the timed region"},
             "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches,
+            **({"segments": {"vertical_lines": "5% of the non-window prefix per kv head (seeded synthetic score)",
+                             "window": SEG_W, "staging": SEG_WS, "list_bytes_per_step": fp_mean,
+                             "kernels": "fp_segment_kernel + decode_mma_kernel, one scan time"}}
+               if args.segments else {}),
             "clocks": clk.summary()}
     if rank == 0 and not args.no_cpu_baseline:
         try:

@@ -152,12 +152,15 @@ KVQ_API kv_status_t kv_evict_slots_head(kv_pool_t* pool, const int32_t* req_ids,
  * Every list must be empty.  Synchronizes the device. */
 KVQ_API kv_status_t kv_fp_configure(kv_pool_t* pool, int32_t max_tokens);
 
-/* Append n_tok tokens to request req_id's lists.
- *   k, v  device, bf16 [n_tok][num_kv_heads][128] (row h of token t goes to
- *         kv head h's list); any 2-byte alignment.
- * The values are used as given.  KV_ERR_OOM past the capacity (no change). */
-KVQ_API kv_status_t kv_fp_append(kv_pool_t* pool, int32_t req_id, const void* k, const void* v, int64_t n_tok,
-                                 void* stream);
+/* Append n_tok tokens to the lists: token t goes to the end of request
+ * req_ids[t]'s lists, tokens of one request in order.
+ *   k, v     device, bf16 [n_tok][num_kv_heads][128] (row h of token t goes to
+ *            kv head h's list); any 2-byte alignment.
+ *   req_ids  host, int32 [n_tok].
+ * The values are used as given.  KV_ERR_OOM past a list's capacity and
+ * KV_ERR_INVALID_ARG for a request that is not open, both before any change. */
+KVQ_API kv_status_t kv_fp_append(kv_pool_t* pool, const void* k, const void* v, const int32_t* req_ids,
+                                 int64_t n_tok, void* stream);
 
 /* Remove list tokens [first, first + n_tok) of every head of a request; the
  * rest keep their order.  A range outside the list is KV_ERR_INVALID_ARG. */

@@ -66,7 +66,7 @@ def load_library(path: str = LIB_PATH):
             "kv_evict_slots": [_P, _P, _P, _I64, _P],
             "kv_evict_slots_head": [_P, _P, _P, _P, _I64, _P],
             "kv_fp_configure": [_P, _I32],
-            "kv_fp_append": [_P, _I32, _P, _P, _I64, _P],
+            "kv_fp_append": [_P, _P, _P, _P, _I64, _P],
             "kv_fp_drop": [_P, _I32, _I64, _I64, _P],
             "kv_fp_count": [_P, _I32, _P],
             "kv_decode_attn": [_P, _P, _P, _I32, _I32, ctypes.c_float, _P, _P],
@@ -227,15 +227,18 @@ class KVPool:
         """kv_fp_configure: capacity of every request's full-precision lists."""
         _check(load_library().kv_fp_configure(self._h, int(max_tokens)), "kv_fp_configure")
 
-    def fp_append(self, rid, k, v, stream=None):
-        """kv_fp_append: k, v torch bf16 CUDA tensors [n][Hkv][128]."""
+    def fp_append(self, req_ids, k, v, stream=None):
+        """kv_fp_append: k, v torch bf16 CUDA tensors [n][Hkv][128]; req_ids: a request id
+        (every token) or a host sequence [n]."""
         n = int(k.shape[0])
+        req_ids = np.full(n, int(req_ids), np.int32) if np.ndim(req_ids) == 0 else _np(req_ids, np.int32)
+        if req_ids.size != n:
+            raise ValueError("req_ids and k differ in length")
         if n:
             self._check_kv(k, n)
             self._check_kv(v, n)
-        _check(load_library().kv_fp_append(self._h, int(rid), k.data_ptr() if n else None,
-                                           v.data_ptr() if n else None, n, _stream(stream, self.device)),
-               "kv_fp_append")
+        _check(load_library().kv_fp_append(self._h, k.data_ptr() if n else None, v.data_ptr() if n else None,
+                                           _ptr(req_ids), n, _stream(stream, self.device)), "kv_fp_append")
 
     def fp_drop(self, rid, first, n, stream=None):
         _check(load_library().kv_fp_drop(self._h, int(rid), int(first), int(n), _stream(stream, self.device)),

@@ -77,10 +77,13 @@ struct Unit {
   int32_t pad;
 };
 
-// Full-precision tokens per full-precision split.  Such a split is a Split
-// whose page_begin / page_end are token indices of the request's list
-// (page_end < 0: to the list's length at launch).
-constexpr int kFpChunk = 64;
+// Full-precision splits: a Split whose page_begin / page_end are token
+// indices of the request's lists (page_end < 0: to the list's length at
+// launch).  The list tokens of all units, in unit order, are cut into ranges
+// of about equal length, one per warp of the full-precision scan (at least
+// kFpMinTokens tokens each), each range split further at unit boundaries.
+constexpr int kFpWarpsPerCta = 12;
+constexpr int kFpMinTokens = 32;
 
 // A split: a range of one unit's pages in scan order, scanned by one worker
 // (a CTA of the CUDA-core scan, a warp of the tensor-core scan).  Worker k
@@ -149,6 +152,7 @@ struct HostPlan {
   std::vector<Unit> units;
   std::vector<Split> splits;        // page splits, then full-precision splits
   int32_t n_page_splits = 0;
+  std::vector<int32_t> fp_wsplit;   // full-precision workers + 1 entries (split indices from n_page_splits)
   std::vector<int32_t> cta_split;   // n_workers + 1 entries
   int64_t n_ctas() const { return (int64_t)cta_split.size() - 1; }   // workers
 };
@@ -263,6 +267,8 @@ struct kv_pool {
   int32_t plan_impl = -1;
   int32_t n_units = 0, n_splits = 0;
   int32_t n_page_splits = 0;          // splits [0, n_page_splits) are page splits, the rest full-precision
+  size_t plan_fpw_off = 0;            // full-precision worker split ranges in the plan buffer
+  int32_t n_fpw = 0;
   size_t plan_units_off = 0, plan_splits_off = 0, plan_cta_off = 0;
   int32_t n_ctas = 0;
   std::vector<int32_t> stat_req;      // request ids of the last decode (for kv_last_decode_stats)
@@ -318,14 +324,18 @@ cudaError_t launch_scatter(kv_pool* P, const TableUpd* d_upd, int n, cudaStream_
 // otherwise in table order.
 void plan_decode(const kv_pool* P, const int32_t* req_ids, int32_t batch, int64_t n_workers, int64_t min_pages,
                  PageCost cost, bool spread, HostPlan& out);
+int fp_workers(const kv_pool* P);   // warps of the full-precision scan (one CTA per SM)
 
-// Full-precision splits (kvq_fp.cu): one partial per split of kFpChunk tokens,
-// written at split index first_split + i of d_part.  Launched in stream order
-// (no programmatic overlap).
+// Full-precision scan (kvq_fp.cu): warp k scans the splits
+// [d_fpw[k], d_fpw[k + 1]) of d_fsplits and writes one partial per split at
+// split index first_split + i of d_part.  Launched in stream order (no
+// programmatic overlap).
 cudaError_t launch_fp_segments(kv_pool* P, const void* q, int32_t hq, float scale_log2, const Unit* d_units,
-                               const Split* d_fsplits, int n_fsplits, int first_split, float* d_part, cudaStream_t s);
+                               const Split* d_fsplits, const int32_t* d_fpw, int n_fpw, int first_split, float* d_part,
+                               cudaStream_t s);
 // Copies into / within the full-precision lists (kvq_fp.cu).
-cudaError_t launch_fp_store(kv_pool* P, int32_t req, const void* k, const void* v, int64_t n, int32_t at,
+cudaError_t launch_fp_store(kv_pool* P, const void* k, const void* v, int64_t n, const int32_t* d_req,
+                            const int32_t* d_slot, const int32_t* d_len_req, const int32_t* d_len_val, int n_len,
                             cudaStream_t s);
 cudaError_t launch_fp_move(kv_pool* P, int32_t req, int32_t from, int32_t to, int32_t n, int32_t new_len,
                            cudaStream_t s);

@@ -101,10 +101,9 @@ extern "C" kv_status_t kv_decode_attn_noalloc(kv_pool_t* P, const void* q, const
   const size_t frags_bytes = mma ? align256((size_t)n_units * decode_mma_frag_bytes()) : 0;
   const int64_t budget = (int64_t)((kScratchBytes - units_bytes - frags_bytes - 1024) /
                                    (sizeof(Split) + sizeof(int32_t) + part_bytes));
-  int64_t n_fsplits = 0;   // full-precision splits the plan adds (kFpChunk tokens each)
-  for (int32_t b = 0; b < batch && !P->n_fp.empty(); ++b)
-    n_fsplits += (int64_t)hkv * ((P->n_fp[req_ids[b]] + kFpChunk - 1) / kFpChunk);
-  const int64_t n_workers = std::min<int64_t>((int64_t)P->sm_count * per_sm, budget - n_units - n_fsplits);
+  // full-precision splits: at most one per full-precision worker plus one per unit
+  const int64_t n_fsplits = P->n_fp.empty() ? 0 : (int64_t)fp_workers(P) + n_units;
+  const int64_t n_workers = std::min<int64_t>((int64_t)P->sm_count * per_sm, budget - n_units - 2 * n_fsplits);
   if (n_workers < 1)
     return nfail(KV_ERR_INVALID_ARG, "kv_decode_attn_noalloc: the plan does not fit the fixed scratch");
   HostPlan hp;
@@ -114,7 +113,8 @@ extern "C" kv_status_t kv_decode_attn_noalloc(kv_pool_t* P, const void* q, const
   // per-unit q operands and the partials (written on the device)
   const size_t splits_off = units_bytes;
   const size_t cta_off = align256(splits_off + hp.splits.size() * sizeof(Split));
-  const size_t frags_off = align256(cta_off + hp.cta_split.size() * sizeof(int32_t));
+  const size_t fpw_off = align256(cta_off + hp.cta_split.size() * sizeof(int32_t));
+  const size_t frags_off = align256(fpw_off + hp.fp_wsplit.size() * sizeof(int32_t));
   const size_t part_off = frags_off + frags_bytes;
   if (part_off + hp.splits.size() * part_bytes > kScratchBytes)
     return nfail(KV_ERR_INVALID_ARG, "kv_decode_attn_noalloc: the plan does not fit the fixed scratch");
@@ -122,16 +122,19 @@ extern "C" kv_status_t kv_decode_attn_noalloc(kv_pool_t* P, const void* q, const
   std::memcpy(host.data(), hp.units.data(), hp.units.size() * sizeof(Unit));
   if (!hp.splits.empty()) std::memcpy(host.data() + splits_off, hp.splits.data(), hp.splits.size() * sizeof(Split));
   std::memcpy(host.data() + cta_off, hp.cta_split.data(), hp.cta_split.size() * sizeof(int32_t));
+  if (!hp.fp_wsplit.empty())
+    std::memcpy(host.data() + fpw_off, hp.fp_wsplit.data(), hp.fp_wsplit.size() * sizeof(int32_t));
   cudaStream_t s = (cudaStream_t)stream;
   uint8_t* base = (uint8_t*)scratch;
   if (cudaMemcpyAsync(base, host.data(), frags_off, cudaMemcpyHostToDevice, s) != cudaSuccess)
     return nfail(KV_ERR_CUDA, "kv_decode_attn_noalloc: plan upload failed");
   const float scale_log2 = softmax_scale * 1.4426950408889634f;
-  const int n_fp_splits = (int)hp.splits.size() - hp.n_page_splits;
-  if (n_fp_splits > 0) {
+  const int n_fpw = (int)hp.fp_wsplit.size() - 1;
+  if (n_fpw > 0) {
     const cudaError_t ef = launch_fp_segments(P, q, hq, scale_log2, (const Unit*)base,
-                                              (const Split*)(base + splits_off) + hp.n_page_splits, n_fp_splits,
-                                              hp.n_page_splits, (float*)(base + part_off), s);
+                                              (const Split*)(base + splits_off) + hp.n_page_splits,
+                                              (const int32_t*)(base + fpw_off), n_fpw, hp.n_page_splits,
+                                              (float*)(base + part_off), s);
     if (ef != cudaSuccess) return nfail(KV_ERR_CUDA, cudaGetErrorString(ef));
   }
   const cudaError_t e =

@@ -293,20 +293,37 @@ void kvq::plan_decode(const kv_pool* P, const int32_t* req_ids, int32_t batch, i
     }
   }
   while (cur < n) out.cta_split[++cur] = (int32_t)out.splits.size();
-  // full-precision splits: kFpChunk tokens each, after all page splits; a
-  // unit's last one runs to the list's length at launch
+  // full-precision splits, after all page splits: the list tokens of all
+  // units, in unit order, cut into fp_workers(P) ranges of about equal
+  // length (at least kFpMinTokens each), split at unit boundaries; a unit's
+  // last split runs to the list's length at launch
   out.n_page_splits = (int32_t)out.splits.size();
+  int64_t T = 0;
+  for (int32_t b = 0; b < batch; ++b) T += (int64_t)hkv * (P->n_fp.empty() ? 0 : P->n_fp[req_ids[b]]);
+  const int64_t nw = T > 0 ? std::max<int64_t>(1, std::min<int64_t>(fp_workers(P), (T + kFpMinTokens - 1) / kFpMinTokens))
+                           : 0;
+  out.fp_wsplit.assign((size_t)nw + 1, 0);
+  int64_t fcur = 0, FU = 0;   // worker receiving the current split; tokens before the current unit
   for (int32_t b = 0; b < batch; ++b) {
     const int32_t nf = P->n_fp.empty() ? 0 : P->n_fp[req_ids[b]];
     for (int h = 0; h < hkv; ++h) {
       Unit& u = out.units[(size_t)b * hkv + h];
       u.fp_begin = (int32_t)out.splits.size();
-      for (int32_t t = 0; t < nf; t += kFpChunk)
-        out.splits.push_back(Split{b * hkv + h, t, std::min(nf, t + kFpChunk), req_ids[b], 0, 0, {0, 0}});
+      for (int32_t t = 0; t < nf;) {
+        const int64_t j = (FU + t) * nw / T;   // worker of token t
+        while (fcur < j) out.fp_wsplit[(size_t)++fcur] = (int32_t)out.splits.size() - out.n_page_splits;
+        // first token of worker j + 1: ceil((j + 1) T / nw)
+        const int64_t lim = ((j + 1) * T + nw - 1) / nw - FU;
+        const int32_t e = (int32_t)std::min<int64_t>(nf, lim);
+        out.splits.push_back(Split{b * hkv + h, t, e, req_ids[b], 0, 0, {0, 0}});
+        t = e;
+      }
+      FU += nf;
       u.n_fp_splits = (int32_t)out.splits.size() - u.fp_begin;
       if (u.n_fp_splits > 0) out.splits.back().page_end = -1;
     }
   }
+  while (fcur < nw) out.fp_wsplit[(size_t)++fcur] = (int32_t)out.splits.size() - out.n_page_splits;
 }
 
 extern "C" {
@@ -1081,20 +1098,44 @@ kv_status_t kv_fp_configure(kv_pool_t* P, int32_t max_tokens) {
   return KV_OK;
 }
 
-kv_status_t kv_fp_append(kv_pool_t* P, int32_t r, const void* k, const void* v, int64_t n_tok, void* stream) {
-  if (!P || !req_ok(P, r) || n_tok < 0 || (n_tok > 0 && (!k || !v)))
-    return fail(KV_ERR_INVALID_ARG, "kv_fp_append: bad arguments (request %d)", P ? r : -1);
+kv_status_t kv_fp_append(kv_pool_t* P, const void* k, const void* v, const int32_t* req_ids, int64_t n_tok,
+                         void* stream) {
+  if (!P || n_tok < 0 || (n_tok > 0 && (!k || !v || !req_ids)))
+    return fail(KV_ERR_INVALID_ARG, "kv_fp_append: bad arguments");
   if (P->fp_cap == 0) return fail(KV_ERR_INVALID_ARG, "kv_fp_append: kv_fp_configure has not been called");
-  if ((int64_t)P->n_fp[r] + n_tok > P->fp_cap)
-    return fail(KV_ERR_OOM, "kv_fp_append: %lld tokens exceed the list capacity %d", (long long)(P->n_fp[r] + n_tok),
-                P->fp_cap);
   if (n_tok == 0) return KV_OK;
+  if (n_tok > INT32_MAX) return fail(KV_ERR_INVALID_ARG, "kv_fp_append: too many tokens");
+  // destination slots: each token goes to the end of its request's lists, in order
+  std::vector<int32_t> meta((size_t)n_tok * 2);
+  std::vector<int32_t> len_req, len_val;
+  std::unordered_map<int32_t, int32_t> grow;
+  for (int64_t t = 0; t < n_tok; ++t) {
+    const int32_t r = req_ids[t];
+    if (!req_ok(P, r)) return fail(KV_ERR_INVALID_ARG, "kv_fp_append: request %d not open", r);
+    const int32_t at = P->n_fp[r] + grow[r]++;
+    if (at >= P->fp_cap)
+      return fail(KV_ERR_OOM, "kv_fp_append: request %d's lists would exceed their capacity %d", r, P->fp_cap);
+    meta[(size_t)t] = r;
+    meta[(size_t)(n_tok + t)] = at;
+  }
+  for (const auto& g : grow) {
+    len_req.push_back(g.first);
+    len_val.push_back(P->n_fp[g.first] + g.second);
+  }
   DeviceGuard dg(P->cfg.device);
   cudaStream_t s = (cudaStream_t)stream;
   kv_status_t st = order_after_previous(P, s);
   if (st != KV_OK) return st;
-  KV_CUDA(launch_fp_store(P, r, k, v, n_tok, P->n_fp[r], s));
-  P->n_fp[r] += (int32_t)n_tok;
+  Upload u;
+  const size_t om = u.add(meta.data(), meta.size() * sizeof(int32_t));
+  const size_t olr = u.add(len_req.data(), len_req.size() * sizeof(int32_t));
+  const size_t olv = u.add(len_val.data(), len_val.size() * sizeof(int32_t));
+  if ((st = upload(P, u, s)) != KV_OK) return st;
+  const uint8_t* base = (const uint8_t*)P->upload.ptr;
+  const int32_t* d_meta = (const int32_t*)(base + om);
+  KV_CUDA(launch_fp_store(P, k, v, n_tok, d_meta, d_meta + n_tok, (const int32_t*)(base + olr),
+                          (const int32_t*)(base + olv), (int)len_req.size(), s));
+  for (size_t i = 0; i < len_req.size(); ++i) P->n_fp[len_req[i]] = len_val[i];
   return KV_OK;
 }
 
@@ -1201,14 +1242,14 @@ kv_status_t build_plan(kv_pool* P, const int32_t* req_ids, int32_t batch, int32_
   // rebuilt once a table has grown past the slack (or an empty table gained
   // pages, which has no split yet).
   // Full-precision splits follow the same rule: a unit's last one is
-  // open-ended, and the plan is rebuilt once a list has grown by a chunk, has
+  // open-ended, and the plan is rebuilt once a list has grown by 64 tokens, has
   // shrunk, or was empty.
   bool same = P->plan_impl == impl && P->plan_hq == hq && (int32_t)P->plan_req.size() == batch;
   for (int32_t b = 0; same && b < batch; ++b) {
     const int32_t len = (int32_t)P->reqs[req_ids[b]].table.size(), len0 = P->plan_len[b];
     same = P->plan_req[b] == req_ids[b] && len >= len0 && len - len0 <= P->plan_slack && (len0 > 0 || len == 0);
     const int32_t nf = P->n_fp.empty() ? 0 : P->n_fp[req_ids[b]], nf0 = P->plan_nfp[b];
-    same = same && nf >= nf0 && nf - nf0 < kFpChunk && (nf0 > 0 || nf == 0);
+    same = same && nf >= nf0 && nf - nf0 < 2 * kFpMinTokens && (nf0 > 0 || nf == 0);
   }
   if (same) return KV_OK;
 
@@ -1221,6 +1262,7 @@ kv_status_t build_plan(kv_pool* P, const int32_t* req_ids, int32_t batch, int32_
   const size_t ou = up.add(hp.units.data(), hp.units.size() * sizeof(Unit));
   const size_t os = up.add(hp.splits.data(), hp.splits.size() * sizeof(Split));
   const size_t oc = up.add(hp.cta_split.data(), hp.cta_split.size() * sizeof(int32_t));
+  const size_t of = up.add(hp.fp_wsplit.data(), hp.fp_wsplit.size() * sizeof(int32_t));
   kv_status_t st = ensure(P->plan, up.size);
   if (st != KV_OK) return st;
   if ((st = h2d(P, P->plan.ptr, up, s)) != KV_OK) return st;
@@ -1230,6 +1272,8 @@ kv_status_t build_plan(kv_pool* P, const int32_t* req_ids, int32_t batch, int32_
   P->n_units = (int32_t)hp.units.size();
   P->n_splits = (int32_t)hp.splits.size();
   P->n_page_splits = hp.n_page_splits;
+  P->plan_fpw_off = of;
+  P->n_fpw = (int32_t)hp.fp_wsplit.size() - 1;
   P->n_ctas = (int32_t)hp.n_ctas();
   P->plan_req.assign(req_ids, req_ids + batch);
   P->plan_len.resize(batch);
@@ -1281,8 +1325,8 @@ kv_status_t kv_decode_attn(kv_pool_t* P, const void* q, const int32_t* req_ids, 
   cudaEvent_t* tv = rec ? &P->tev[3 * (size_t)(P->timed_calls % kTimingRing)] : nullptr;
   if (tv) KV_CUDA(cudaEventRecord(tv[0], s));
   P->merge_event = tv ? tv[1] : nullptr;
-  KV_CUDA(launch_fp_segments(P, q, hq, scale_log2, du, dsp + P->n_page_splits, P->n_splits - P->n_page_splits,
-                             P->n_page_splits, (float*)P->partials.ptr, s));
+  KV_CUDA(launch_fp_segments(P, q, hq, scale_log2, du, dsp + P->n_page_splits, (const int32_t*)(base + P->plan_fpw_off),
+                             P->n_fpw, P->n_page_splits, (float*)P->partials.ptr, s));
   if (impl == KV_DECODE_MMA)
     KV_CUDA(launch_decode_mma(P, q, hq, scale_log2, du, P->n_units, dsp, dct, P->n_ctas, P->frags.ptr,
                               (float*)P->partials.ptr, out, s));

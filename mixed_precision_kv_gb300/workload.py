@@ -25,31 +25,34 @@ def request_bits(w: Workload, r: int, allocator=alloc_bits) -> np.ndarray:
     return bits
 
 
-def pool_size(w: Workload, bits_list, chunk: int, steps: int):
+def pool_size(w: Workload, bits_list, chunk: int, steps: int, extra: int = 0):
     """INT2 / INT4 page counts and table capacity for a workload appended in
-    `chunk`-token calls and then `steps` one-token-per-request calls."""
+    `chunk`-token calls and then `steps` one-token-per-request calls, with room
+    for `extra` more tokens per request of either width."""
     n2 = n4 = max_tab = 0
+    xp = -(-extra // 32) + 1 if extra else 0
     for spec, bits in zip(w.requests, bits_list):
         total = spec.n_prefill + steps
         b2 = int((bits[:total] == 2).sum())
         b4 = total - b2
-        n2 += b2 // 32 + 1
-        n4 += -(-b4 // 32) + 2
-        max_tab = max(max_tab, b2 // 32 + -(-b4 // 32) + 3)
+        n2 += b2 // 32 + 1 + xp
+        n4 += -(-b4 // 32) + 2 + xp
+        max_tab = max(max_tab, b2 // 32 + -(-b4 // 32) + 3 + 2 * xp)
     # staging pages repacked during one call are freed only when it returns
     n4 += chunk // 32 + len(w.requests) + 8
     return n2, n4, max_tab
 
 
 class GPUWorkload:
-    def __init__(self, w: Workload, device: int = 0, chunk: int = 16384, steps: int | None = None):
+    def __init__(self, w: Workload, device: int = 0, chunk: int = 16384, steps: int | None = None,
+                 extra_tokens: int = 0):
         import torch
         self.w = w
         self.device = device
         self.chunk = chunk
         self.steps = w.steps if steps is None else steps
         self.bits = [request_bits(w, r) for r in range(len(w.requests))]
-        n2, n4, max_tab = pool_size(w, self.bits, chunk, self.steps)
+        n2, n4, max_tab = pool_size(w, self.bits, chunk, self.steps, extra_tokens)
         self.pool = KVPool(w.num_kv_heads, n2, n4, len(w.requests), max_tab, device=device)
         self.rids = [self.pool.open() for _ in w.requests]
         self.dev = torch.device("cuda", device)
@@ -112,6 +115,38 @@ class GPUWorkload:
         self.pool.append(k, v, req_ids, bits)
         for r in range(len(self.rids)):
             self.pos[r] += 1
+
+    def freeze_segments(self, rho: float = 0.05, window: int = 128, staging: int = 128):
+        """Full-precision segments on the prefilled pool (HyQuant, Algorithm 4
+        FREEZE): per request and kv head the top-rho positions of a seeded
+        synthetic column score over the non-window prefix leave that head's
+        quantized set (per-head exclusion) for its full-precision list; the
+        last `window` prefill positions leave every head's quantized set
+        (eviction) and follow in the lists.  The lists hold room for the
+        staging buffer.  Returns the window tokens' rows [window][B][Hkv][128]
+        (K, V) and the number of vertical-line tokens per request."""
+        import torch
+        H, B = self.w.num_kv_heads, len(self.rids)
+        n_vl = [int(rho * (spec.n_prefill - window)) for spec in self.w.requests]
+        self.pool.fp_configure(max(n_vl) + window + staging)
+        wk = torch.empty((window, B, H, 128), dtype=torch.bfloat16, device=self.dev)
+        wv = torch.empty_like(wk)
+        for r, spec in enumerate(self.w.requests):
+            n, pre, nv = spec.n_prefill, spec.n_prefill - window, n_vl[r]
+            rid = self.rids[r]
+            k_all, v_all = self.kv_rows(r, 0, n)
+            score = np.random.default_rng([self.w.seed, 77, r]).random((H, pre))
+            pos = [np.sort(np.argpartition(score[h], pre - nv)[pre - nv:]) for h in range(H)]
+            idx = [torch.from_numpy(p_).to(self.dev) for p_ in pos]
+            kf = torch.stack([k_all[idx[h], h] for h in range(H)], dim=1).contiguous()
+            vf = torch.stack([v_all[idx[h], h] for h in range(H)], dim=1).contiguous()
+            self.pool.evict_head(np.full(nv * H, rid), np.concatenate(pos), np.repeat(np.arange(H), nv))
+            self.pool.evict(np.full(window, rid), np.arange(pre, n))
+            self.pool.fp_append(rid, kf, vf)
+            self.pool.fp_append(rid, k_all[pre:n].contiguous(), v_all[pre:n].contiguous())
+            wk[:, r] = k_all[pre:n]
+            wv[:, r] = v_all[pre:n]
+        return wk, wv, n_vl
 
     def decode(self, q, out=None):
         return self.pool.decode(q, self.rids, self.w.softmax_scale, out=out)

@@ -190,3 +190,22 @@ def test_list_errors(kvq):
     sc.gpu.fp_drop(g, 0, 5)
     assert sc.gpu.fp_count(g) == 0
     sc.gpu.fp_configure(16)
+
+
+def test_batched_append_interleaves_requests(kvq):
+    """One kv_fp_append call whose tokens belong to several requests, in mixed
+    order: each request's tokens land at the end of its lists, in order."""
+    bits = [_mixed(100, 0.5, 1), _mixed(60, 0.5, 2), _mixed(33, 0.5, 3)]
+    sc = Scenario(kvq, 2, 8, bits, chunk=64)
+    sc.gpu.fp_configure(64)
+    _append_window(sc, 1, 5, 400)                  # request 1 already has a list
+    order = np.array([0, 1, 0, 2, 1, 0, 0, 2, 1, 1, 0])
+    k = kvsynth.fill_bf16_host(order.size, 2, 128, SEED, kvsynth.TENSOR_K, 401)
+    v = kvsynth.fill_bf16_host(order.size, 2, 128, SEED, kvsynth.TENSOR_V, 401)
+    sc.gpu.fp_append(np.array(sc.g_ids)[order], _dev(k), _dev(v))
+    for r in range(3):
+        sel = np.flatnonzero(order == r)
+        assert sc.orc.fp_append(sc.o_ids[r], k[sel], v[sel]) == oracle.OK
+    assert [sc.gpu.fp_count(g) for g in sc.g_ids] == [5, 9, 2]
+    sc.gpu.sync()
+    sc.check_decode(what="batched append")
