@@ -73,6 +73,7 @@ struct alignas(16) WarpSmem {
   uint8_t stage[kStages][kStageBytes];
   float pbuf[8][kPage];                // P [head][slot] of the current page; V zero terms at a flush
   unsigned long long bar[kStages];
+  const uint32_t* hdead;               // exclusion words (read from here at each refill, not kept in a register)
 };
 static_assert(sizeof(WarpSmem) % 16 == 0 && kStageBytes % 16 == 0, "stage buffers must stay 16-byte aligned");
 
@@ -754,6 +755,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(
   const float pscale = ldexpf(1.0f, sv), oscale = ldexpf(1.0f, -sv);
   if (lane == 0) {
     for (int st = 0; st < kStages; ++st) bar_init(&WS.bar[st]);
+    if constexpr (kHead) WS.hdead = hdead;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncwarp();
@@ -803,7 +805,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(
       const Entry e = ltab[idx];
       bid = e.id;
       // slots excluded for this kv head only read as dead slots too
-      if constexpr (kHead) blive = e.live & ~hdead[(size_t)e.id * hkv + lkvh];
+      if constexpr (kHead) {
+        const uint32_t* hd = *reinterpret_cast<const uint32_t* const volatile*>(&WS.hdead);
+        blive = e.live & ~hd[(size_t)e.id * hkv + lkvh];
+      }
       else blive = e.live;
       btag = (lsg << 6) | lkvh;
       const uint8_t* src = e.id < n2 ? pool + ((size_t)e.id * hkv + lkvh) * kInt2Block

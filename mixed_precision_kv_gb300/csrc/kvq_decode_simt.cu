@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const Unit* __restrict__ uni
   auto split_at = [&](int s) { return s < nq ? base + (size_t)s * rs : fbase + (size_t)(s - nq) * rs; };
   float Mw = -INFINITY, Lw = 0.0f;
   float4 A = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-  constexpr int kOne = 8;   // splits per warp read in one round (units of up to kW * kOne splits)
+  constexpr int kOne = 12;  // splits per warp read in one round (units of up to kW * kOne splits)
   if (n <= kW * kOne) {
     // every load of the warp's splits at once, then the weights
     const int mine = n > w ? (n - w + kW - 1) / kW : 0;
