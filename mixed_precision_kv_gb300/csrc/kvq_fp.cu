@@ -8,12 +8,13 @@
 // fp_segment_kernel: persistent warps, one CTA per SM.  Warp gw scans the
 // splits [fpw[gw], fpw[gw + 1]): contiguous token ranges of consecutive units
 // cut so that every warp gets about the same number of tokens.  Rows stream
-// through shared memory in 16-token chunks, two chunks per warp in flight: K
-// and V of a chunk are one bulk copy each (a unit's rows are contiguous), and
-// chunk c + 2 is issued into the stage of chunk c once c is consumed.  Logits
-// are q . k summed in fp32 over exact bf16 x bf16 products; one partial per
-// split (acc[128], m, l in the log2 domain), in the format of the page scans,
-// so the split merge combines both.
+// through shared memory in 16-token chunks, three chunks per warp in flight:
+// K and V of a chunk are one bulk copy each (a unit's rows are contiguous),
+// and chunk c + 3 is issued into the stage of chunk c once c is consumed.
+// Logits and P.V run on the tensor cores (bf16 operands, fp32 accumulation;
+// P split into bf16 hi + lo parts); one partial per split (acc[128], m, l in
+// the log2 domain), in the format of the page scans, so the split merge
+// combines both.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -28,30 +29,48 @@ namespace {
 constexpr int kFpWarps = kFpWarpsPerCta;
 constexpr int kFpPartStride = kHeadDim + 4;   // the page scans' partial stride
 constexpr int kFpTok = 16;                    // tokens per streamed chunk
+constexpr int kFpStages = 3;                  // chunks in flight per warp
 constexpr int kRowBytes = kHeadDim * 2;
 constexpr int kChunkBytes = kFpTok * kRowBytes;
 constexpr uint32_t kFpSpinLimit = 1u << 22;
 
 struct alignas(128) FpWarpSmem {   // bulk copy destinations start on 128-byte boundaries
-  uint8_t k[2][kChunkBytes];       // two stages
-  uint8_t v[2][kChunkBytes];
-  unsigned long long bar[2][2];    // [stage][K, V]
+  uint8_t k[kFpStages][kChunkBytes];
+  uint8_t v[kFpStages][kChunkBytes];
+  unsigned long long bar[kFpStages][2];   // [stage][K, V]
+  float ps[8][kFpTok];             // P [head][token] of the current chunk
+  float corr[8];                   // per-head rescale of the current chunk
 };
-
-template <int G>
-constexpr size_t fp_smem_bytes() {
-  return kFpWarps * (sizeof(FpWarpSmem) + (size_t)G * kHeadDim * 2 + (size_t)G * kFpTok * 4);
-}
+constexpr size_t kFpSmem = kFpWarps * sizeof(FpWarpSmem);
 
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 __device__ __forceinline__ uint32_t sa(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-// acc + lo(a) lo(b) + hi(a) hi(b) for bf16 pairs: exact products, two fp32 roundings
-__device__ __forceinline__ float fma2_bf16(uint32_t a, uint32_t b, float acc) {
-  asm("{.reg .b16 al, ah, bl, bh;\n mov.b32 {al, ah}, %1;\n mov.b32 {bl, bh}, %2;\n"
-      " fma.rn.f32.bf16 %0, al, bl, %0;\n fma.rn.f32.bf16 %0, ah, bh, %0;}"
-      : "+f"(acc) : "r"(a), "r"(b));
-  return acc;
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(sa(p)) : "memory");
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(sa(p)) : "memory");
+}
+// d += A B, bf16 operands (exact products), fp32 accumulation
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// two floats as a bf16 pair (round to nearest even): lo -> bits 0..15
+__device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+// p = hi + lo with hi = bf16(p), lo = bf16(p - hi): 16 significant bits
+__device__ __forceinline__ void split_bf2(float x, float y, uint32_t& hi, uint32_t& lo) {
+  hi = pack_bf2(x, y);
+  lo = pack_bf2(x - bf_lo(hi), y - bf_hi(hi));
 }
 
 __device__ __forceinline__ void fbar_init(unsigned long long* b) {
@@ -93,9 +112,8 @@ __global__ void __launch_bounds__(kFpWarps * 32, 1)
   const int sb = fpw[gw], se = fpw[gw + 1];
   if (sb >= se) return;
   FpWarpSmem& S = reinterpret_cast<FpWarpSmem*>(smem)[w];
-  uint32_t* qs = reinterpret_cast<uint32_t*>(smem + kFpWarps * sizeof(FpWarpSmem)) + (size_t)w * G * kHeadDim / 2;
-  float* ps = reinterpret_cast<float*>(smem + kFpWarps * (sizeof(FpWarpSmem) + (size_t)G * kHeadDim * 2)) +
-              (size_t)w * G * kFpTok;
+  const int r = lane >> 2, i = lane & 3;   // mma fragment coordinates
+  const int mi = lane >> 3, mr = lane & 7;   // ldmatrix: the lane addresses row mr of matrix mi
   // token range of a split (its end read at launch when open-ended)
   auto range = [&](int sidx, int& a, int& e) {
     const Split sp = fsplits[sidx];
@@ -121,164 +139,168 @@ __global__ void __launch_bounds__(kFpWarps * 32, 1)
     fbulk(S.k[st], fpk + c.row * kHeadDim, (uint32_t)c.n * kRowBytes, &S.bar[st][0]);
     fbulk(S.v[st], fpv + c.row * kHeadDim, (uint32_t)c.n * kRowBytes, &S.bar[st][1]);
   };
+  // rows past a short chunk's end keep earlier chunks' values: start from zeros
+  for (int x = lane; x < (int)(2 * kFpStages * kChunkBytes / 16); x += 32)
+    reinterpret_cast<uint4*>(&S.k[0][0])[x] = make_uint4(0u, 0u, 0u, 0u);   // k and v are adjacent
   if (lane == 0) {
-    fbar_init(&S.bar[0][0]);
-    fbar_init(&S.bar[0][1]);
-    fbar_init(&S.bar[1][0]);
-    fbar_init(&S.bar[1][1]);
+    for (int st = 0; st < kFpStages; ++st) {
+      fbar_init(&S.bar[st][0]);
+      fbar_init(&S.bar[st][1]);
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncwarp();
-  // chunks c and c + 1 in flight: stage c & 1, barrier phase (c >> 1) & 1
-  FpChunk cur = chunk_at(sb, 0);   // the first chunk of split sb (or of a later split; the ones before are empty)
-  FpChunk ahead = cur.split < se ? chunk_at(cur.split, cur.t0 + kFpTok) : cur;
+  // chunks c .. c + kFpStages - 1 in flight: chunk c in stage c mod kFpStages,
+  // barrier phase (c / kFpStages) & 1; ring[x] is chunk c + x
+  FpChunk ring[kFpStages];
+  ring[0] = chunk_at(sb, 0);   // the first chunk of split sb (or of a later split; the ones before are empty)
+#pragma unroll
+  for (int x = 1; x < kFpStages; ++x)
+    ring[x] = ring[x - 1].split < se ? chunk_at(ring[x - 1].split, ring[x - 1].t0 + kFpTok) : ring[x - 1];
   if (lane == 0) {
-    if (cur.split < se) issue(cur, 0);
-    if (ahead.split < se) issue(ahead, 1);
+#pragma unroll
+    for (int x = 0; x < kFpStages; ++x)
+      if (ring[x].split < se) issue(ring[x], x);
   }
+  FpChunk& cur = ring[0];
   uint32_t n_chunk = 0;   // chunks consumed
-  const int j = lane & 15, hf = lane >> 4;   // logits: lanes j and j + 16 share token j, 64 channels each
   bool ok = true;
   for (int sidx = sb; sidx < se; ++sidx) {
     const Unit u = units[fsplits[sidx].unit];
     float* out = part + (size_t)(first_split + sidx) * G * kFpPartStride;
-    float m[G], lsum[G], acc[G][4];
+    // lane (r, i): softmax state of heads 2i, 2i + 1; O rows r (head r, the
+    // hi part of P) and r + 8 (the lo part) of channels 8j + 2i, 8j + 2i + 1
+    float m2[2] = {-INFINITY, -INFINITY}, l2[2] = {0.0f, 0.0f};
+    float acc[16][4];
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      m[h] = -INFINITY;
-      lsum[h] = 0.0f;
-      acc[h][0] = acc[h][1] = acc[h][2] = acc[h][3] = 0.0f;
-    }
-    if (cur.split == sidx) {
-      // the unit's q rows (bf16 pairs; the scale is applied to the sums)
-      __syncwarp();
-      const uint32_t* qg = reinterpret_cast<const uint32_t*>(q + ((size_t)u.b * hq + (size_t)u.kvh * G) * kHeadDim);
-      for (int x = lane; x < G * kHeadDim / 2; x += 32) qs[x] = qg[x];
-      __syncwarp();
+    for (int jt = 0; jt < 16; ++jt) acc[jt][0] = acc[jt][1] = acc[jt][2] = acc[jt][3] = 0.0f;
+    // B operand of the logits: column n = head n, k = channel; lane (r, i)
+    // holds q[r][16kk + 2i, +1] and q[r][16kk + 2i + 8, +9] (0 past g heads)
+    uint32_t qb[8][2];
+    {
+      const uint32_t* qr = reinterpret_cast<const uint32_t*>(q + ((size_t)u.b * hq + (size_t)u.kvh * G + r) * kHeadDim);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        qb[kk][0] = (r < G && cur.split == sidx) ? qr[8 * kk + i] : 0u;
+        qb[kk][1] = (r < G && cur.split == sidx) ? qr[8 * kk + i + 4] : 0u;
+      }
     }
     while (cur.split == sidx) {
-      const int st = (int)(n_chunk & 1u);
-      const uint32_t ph = (n_chunk >> 1) & 1u;
+      const int st = (int)(n_chunk % kFpStages);
+      const uint32_t ph = (n_chunk / kFpStages) & 1u;
       if (!__all_sync(0xFFFFFFFFu, fbar_wait(&S.bar[st][0], ph))) {
         ok = false;
         break;
       }
-      // logits: lane (j, hf) reads 16-byte piece (x + j) mod 8 of its half row
-      // at step x, so the 8 lanes of a shared-memory phase hit 8 bank groups
-      const bool live = j < cur.n;
-      float lg[G];
+      // logits D[token][head] = K q^T on the tensor cores; the list stores
+      // 16-byte piece c of row t at piece c ^ (t & 7), so the eight rows of
+      // an 8x8 ldmatrix tile sit in eight different bank groups
+      const int tk = (mi & 1) * 8 + mr;   // token row this lane addresses
+      const int key = (cur.t0 + tk) & 7;
+      const uint8_t* krow = S.k[st] + tk * kRowBytes;
+      float d0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, d1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-      for (int h = 0; h < G; ++h) lg[h] = 0.0f;
-      if (live) {
-        const uint8_t* kr = S.k[st] + j * kRowBytes + hf * (kRowBytes / 2);
-        const uint32_t* qh = qs + hf * (kHeadDim / 4);
-#pragma unroll 2
-        for (int x = 0; x < 8; ++x) {
-          const int c = (x + j) & 7;
-          const uint4 kk = *reinterpret_cast<const uint4*>(kr + 16 * c);
-#pragma unroll
-          for (int h = 0; h < G; ++h) {
-            const uint4 qq = *reinterpret_cast<const uint4*>(qh + h * (kHeadDim / 2) + 4 * c);
-            float t = lg[h];
-            t = fma2_bf16(kk.x, qq.x, t);
-            t = fma2_bf16(kk.y, qq.y, t);
-            t = fma2_bf16(kk.z, qq.z, t);
-            t = fma2_bf16(kk.w, qq.w, t);
-            lg[h] = t;
-          }
-        }
+      for (int kk = 0; kk < 8; ++kk) {
+        uint32_t a[4];
+        ldsm_x4(a, krow + 16 * ((2 * kk + (mi >> 1)) ^ key));
+        if (kk & 1) mma_bf16(d1, a[0], a[1], a[2], a[3], qb[kk][0], qb[kk][1]);
+        else mma_bf16(d0, a[0], a[1], a[2], a[3], qb[kk][0], qb[kk][1]);
       }
+      // online softmax: lane (r, i) holds tokens r, r + 8 of heads 2i, 2i + 1
+      const bool va = r < cur.n, vb = r + 8 < cur.n;
 #pragma unroll
-      for (int h = 0; h < G; ++h) lg[h] = (lg[h] + __shfl_xor_sync(0xFFFFFFFFu, lg[h], 16)) * scale_log2;
-      // online softmax: the chunk's maximum per head (warp-uniform), the
-      // rescale of what earlier chunks added, this chunk's weights
-      float corr[G];
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        float mx = live ? lg[h] : -INFINITY;
-#pragma unroll
-        for (int o = 8; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
-        const float mn = fmaxf(m[h], mx);   // finite: token 0 of the chunk is live
-        corr[h] = m[h] == -INFINITY ? 0.0f : exp2f(m[h] - mn);
-        m[h] = mn;
-        const float p = live ? exp2f(lg[h] - mn) : 0.0f;
-        lsum[h] = fmaf(lsum[h], corr[h], hf == 0 ? p : 0.0f);   // per-lane sums, rescaled alike
-        if (hf == 0) ps[h * kFpTok + j] = p;
+      for (int e = 0; e < 2; ++e) {
+        const float la = (d0[e] + d1[e]) * scale_log2, lb = (d0[2 + e] + d1[2 + e]) * scale_log2;
+        float mx = fmaxf(va ? la : -INFINITY, vb ? lb : -INFINITY);
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
+        const float mn = fmaxf(m2[e], mx);   // finite: token 0 of the chunk is live
+        const float cr = m2[e] == -INFINITY ? 0.0f : exp2f(m2[e] - mn);
+        m2[e] = mn;
+        const float pa = va ? exp2f(la - mn) : 0.0f, pb = vb ? exp2f(lb - mn) : 0.0f;
+        l2[e] = fmaf(l2[e], cr, pa + pb);   // per-lane sums over its two tokens, rescaled alike
+        S.ps[2 * i + e][r] = pa;
+        S.ps[2 * i + e][r + 8] = pb;
+        if (r == 0) S.corr[2 * i + e] = cr;
       }
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        acc[h][0] *= corr[h];
-        acc[h][1] *= corr[h];
-        acc[h][2] *= corr[h];
-        acc[h][3] *= corr[h];
-      }
-      if (!__all_sync(0xFFFFFFFFu, fbar_wait(&S.bar[st][1], ph))) {   // also orders ps
+      __syncwarp();   // K read: the next chunk's K may land; P and the rescale are visible
+      if (!__all_sync(0xFFFFFFFFu, fbar_wait(&S.bar[st][1], ph))) {
         ok = false;
         break;
       }
-      // P.V: lane owns channels 4 lane .. 4 lane + 3
-      const uint8_t* vr = S.v[st] + 8 * lane;
-      int t = 0;
-      for (; t + 4 <= cur.n; t += 4) {
-        uint2 vv[4];
+      // P.V on the tensor cores: A = [P_hi; P_lo] (rows r, r + 8: head r),
+      // B = V from transposed ldmatrix tiles, 16 channel tiles of 8
+      uint32_t a0 = 0u, a1 = 0u, a2 = 0u, a3 = 0u;
+      float cr = 1.0f;
+      if (r < G) {
+        const float2 p01 = *reinterpret_cast<const float2*>(&S.ps[r][2 * i]);
+        const float2 p89 = *reinterpret_cast<const float2*>(&S.ps[r][2 * i + 8]);
+        split_bf2(p01.x, p01.y, a0, a1);
+        split_bf2(p89.x, p89.y, a2, a3);
+        cr = S.corr[r];
+      }
+      if (__any_sync(0xFFFFFFFFu, cr != 1.0f)) {
 #pragma unroll
-        for (int u4 = 0; u4 < 4; ++u4) vv[u4] = *reinterpret_cast<const uint2*>(vr + (t + u4) * kRowBytes);
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float4 p4 = *reinterpret_cast<const float4*>(ps + h * kFpTok + t);
-          const float pp[4] = {p4.x, p4.y, p4.z, p4.w};
-#pragma unroll
-          for (int u4 = 0; u4 < 4; ++u4) {
-            acc[h][0] = fmaf(pp[u4], bf_lo(vv[u4].x), acc[h][0]);
-            acc[h][1] = fmaf(pp[u4], bf_hi(vv[u4].x), acc[h][1]);
-            acc[h][2] = fmaf(pp[u4], bf_lo(vv[u4].y), acc[h][2]);
-            acc[h][3] = fmaf(pp[u4], bf_hi(vv[u4].y), acc[h][3]);
-          }
+        for (int jt = 0; jt < 16; ++jt) {
+          acc[jt][0] *= cr;
+          acc[jt][1] *= cr;
+          acc[jt][2] *= cr;
+          acc[jt][3] *= cr;
         }
       }
-      for (; t < cur.n; ++t) {
-        const uint2 vv = *reinterpret_cast<const uint2*>(vr + t * kRowBytes);
+      const int tv = (mi & 1) * 8 + mr;
+      const int vkey = (cur.t0 + tv) & 7;
+      const uint8_t* vrow = S.v[st] + tv * kRowBytes;
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float p = ps[h * kFpTok + t];
-          acc[h][0] = fmaf(p, bf_lo(vv.x), acc[h][0]);
-          acc[h][1] = fmaf(p, bf_hi(vv.x), acc[h][1]);
-          acc[h][2] = fmaf(p, bf_lo(vv.y), acc[h][2]);
-          acc[h][3] = fmaf(p, bf_hi(vv.y), acc[h][3]);
-        }
+      for (int jj = 0; jj < 8; ++jj) {
+        uint32_t b[4];
+        ldsm_x4_t(b, vrow + 16 * ((2 * jj + (mi >> 1)) ^ vkey));
+        mma_bf16(acc[2 * jj], a0, a1, a2, a3, b[0], b[1]);
+        mma_bf16(acc[2 * jj + 1], a0, a1, a2, a3, b[2], b[3]);
       }
-      __syncwarp();   // stage st and ps read: chunk c + 2 may land in the stage
-      const FpChunk nxt = ahead.split < se ? chunk_at(ahead.split, ahead.t0 + kFpTok) : ahead;
+      __syncwarp();   // stage st, P and the rescale read: chunk c + kFpStages may land in the stage
+      const FpChunk& last = ring[kFpStages - 1];
+      const FpChunk nxt = last.split < se ? chunk_at(last.split, last.t0 + kFpTok) : last;
       if (nxt.split < se && lane == 0) issue(nxt, st);
       ++n_chunk;
-      cur = ahead;
-      ahead = nxt;
+#pragma unroll
+      for (int x = 0; x + 1 < kFpStages; ++x) ring[x] = ring[x + 1];
+      ring[kFpStages - 1] = nxt;
     }
     if (!ok) break;
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      float l = lsum[h];
+    for (int e = 0; e < 2; ++e) {
+      l2[e] += __shfl_xor_sync(0xFFFFFFFFu, l2[e], 4);
+      l2[e] += __shfl_xor_sync(0xFFFFFFFFu, l2[e], 8);
+      l2[e] += __shfl_xor_sync(0xFFFFFFFFu, l2[e], 16);
+    }
+    if (r < G) {
 #pragma unroll
-      for (int o = 16; o; o >>= 1) l += __shfl_xor_sync(0xFFFFFFFFu, l, o);
-      *reinterpret_cast<float4*>(out + h * kFpPartStride + 4 * lane) =
-          make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
-      if (lane == 0) {
-        out[h * kFpPartStride + kHeadDim] = m[h];
-        out[h * kFpPartStride + kHeadDim + 1] = l;
-      }
+      for (int jt = 0; jt < 16; ++jt)
+        *reinterpret_cast<float2*>(out + r * kFpPartStride + 8 * jt + 2 * i) =
+            make_float2(acc[jt][0] + acc[jt][2], acc[jt][1] + acc[jt][3]);
+    }
+    if (r == 0) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e)
+        if (2 * i + e < G) {
+          out[(2 * i + e) * kFpPartStride + kHeadDim] = m2[e];
+          out[(2 * i + e) * kFpPartStride + kHeadDim + 1] = l2[e];
+        }
     }
   }
   if (!ok) {
     if (lane == 0) atomicOr(status, kStatusTimeout);
     // let the copies in flight land (bounded) before the warp leaves: chunks
-    // n_chunk and n_chunk + 1 (if issued); the splits not finished read as empty
-    const uint32_t c0 = n_chunk, c1 = n_chunk + 1;
-    fbar_wait(&S.bar[c0 & 1u][0], (c0 >> 1) & 1u);
-    fbar_wait(&S.bar[c0 & 1u][1], (c0 >> 1) & 1u);
-    if (ahead.split < se) {
-      fbar_wait(&S.bar[c1 & 1u][0], (c1 >> 1) & 1u);
-      fbar_wait(&S.bar[c1 & 1u][1], (c1 >> 1) & 1u);
-    }
+    // n_chunk .. n_chunk + kFpStages - 1 that were issued; the splits not
+    // finished read as empty
+    for (int x = 0; x < kFpStages; ++x)
+      if (ring[x].split < se) {
+        const uint32_t c = n_chunk + (uint32_t)x;
+        fbar_wait(&S.bar[c % kFpStages][0], (c / kFpStages) & 1u);
+        fbar_wait(&S.bar[c % kFpStages][1], (c / kFpStages) & 1u);
+      }
     for (int sidx = max(sb, cur.split); sidx < se; ++sidx)
       for (int h = lane; h < G; h += 32) {
         part[((size_t)(first_split + sidx) * G + h) * kFpPartStride + kHeadDim] = -INFINITY;
@@ -289,7 +311,8 @@ __global__ void __launch_bounds__(kFpWarps * 32, 1)
 
 // Rows src [n][hkv][128] -> row slot[t] of the lists of request req[t] (one
 // per kv head); then the new list lengths (len_req[i] <- len_val[i]).  V = 8:
-// 16-byte pieces (both sides 16-byte aligned), V = 1: single elements.
+// 16-byte pieces (both sides 16-byte aligned), V = 1: single elements.  A
+// list row t keeps its 16-byte piece c at piece c ^ (t & 7).
 template <int V>
 __global__ void fp_store_kernel(const uint16_t* __restrict__ k, const uint16_t* __restrict__ v,
                                 uint16_t* __restrict__ fpk, uint16_t* __restrict__ fpv, int32_t* __restrict__ nfp,
@@ -304,7 +327,9 @@ __global__ void fp_store_kernel(const uint16_t* __restrict__ k, const uint16_t* 
     const int piece = (int)(x - row * kPer);
     const int64_t t = row / hkv;
     const int h = (int)(row - t * hkv);
-    const size_t dst = ((((size_t)req[t] * hkv + h) * fp_cap) + (size_t)slot[t]) * kHeadDim + (size_t)piece * V;
+    const int sw = slot[t] & 7;
+    const int dpos = V == 8 ? ((piece ^ sw) * 8) : ((((piece >> 3) ^ sw) << 3) | (piece & 7));
+    const size_t dst = ((((size_t)req[t] * hkv + h) * fp_cap) + (size_t)slot[t]) * kHeadDim + (size_t)dpos;
     const size_t src = (size_t)row * kHeadDim + (size_t)piece * V;
     if constexpr (V == 8) {
       *reinterpret_cast<uint4*>(fpk + dst) = *reinterpret_cast<const uint4*>(k + src);
@@ -332,8 +357,10 @@ __global__ void fp_move_kernel(uint16_t* __restrict__ fpk, uint16_t* __restrict_
     const int64_t row = y / kPer;   // (head, token) in scratch order
     const int piece = (int)(y - row * kPer);
     const int h = (int)(row / n), t = (int)(row - (int64_t)h * n);
+    // the scratch holds pieces in channel order; the list row (at + t) holds
+    // piece c at c ^ ((at + t) & 7)
     uint4* list = reinterpret_cast<uint4*>(which ? fpv : fpk) +
-                  ((((size_t)req * hkv + h) * fp_cap) + (size_t)(at + t)) * kPer + piece;
+                  ((((size_t)req * hkv + h) * fp_cap) + (size_t)(at + t)) * kPer + (piece ^ ((at + t) & 7));
     if (dir == 0) scratch[x] = *list;
     else *list = scratch[x];
   }
@@ -352,12 +379,12 @@ cudaError_t launch_fp_g(kv_pool* P, const uint16_t* q, int32_t hq, float scale_l
   static bool attr_set = false;
   if (!attr_set) {
     const cudaError_t e =
-        cudaFuncSetAttribute(fp_segment_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fp_smem_bytes<G>());
+        cudaFuncSetAttribute(fp_segment_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFpSmem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   const dim3 grid((unsigned)((n_fpw + kFpWarps - 1) / kFpWarps)), block(kFpWarps * 32);
-  fp_segment_kernel<G><<<grid, block, fp_smem_bytes<G>(), s>>>(q, hq, scale_log2, d_units, d_fsplits, d_fpw, n_fpw,
+  fp_segment_kernel<G><<<grid, block, kFpSmem, s>>>(q, hq, scale_log2, d_units, d_fsplits, d_fpw, n_fpw,
                                                               first_split, P->d_fpk, P->d_fpv, P->fp_cap,
                                                               P->cfg.num_kv_heads, P->d_nfp, d_part, P->d_status);
   return cudaGetLastError();

@@ -82,7 +82,7 @@ struct Unit {
 // launch).  The list tokens of all units, in unit order, are cut into ranges
 // of about equal length, one per warp of the full-precision scan (at least
 // kFpMinTokens tokens each), each range split further at unit boundaries.
-constexpr int kFpWarpsPerCta = 12;
+constexpr int kFpWarpsPerCta = 8;
 constexpr int kFpMinTokens = 32;
 
 // A split: a range of one unit's pages in scan order, scanned by one worker
