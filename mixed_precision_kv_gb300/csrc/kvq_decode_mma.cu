@@ -1057,6 +1057,7 @@ cudaError_t launch_decode_mma(kv_pool* P, const void* q, int32_t hq, float scale
   }
 #undef KVQ_MMA_CASE
   if (e != cudaSuccess) return e;
+  if ((e = launch_fp_pending(P, q, hq, scale_log2, d_units, d_part, s)) != cudaSuccess) return e;
   if (P->merge_event && (e = cudaEventRecord(P->merge_event, s)) != cudaSuccess) return e;
   return launch_merge(P, hq / P->cfg.num_kv_heads, d_units, n_units, d_part, hq, out, s);
 }

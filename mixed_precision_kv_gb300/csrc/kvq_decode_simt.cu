@@ -306,6 +306,10 @@ cudaError_t launch_g(kv_pool* P, const void* q, int32_t hq, float scale_log2, co
                                      d_part);
     if (e != cudaSuccess) return e;
   }
+  {
+    const cudaError_t e = launch_fp_pending(P, q, hq, scale_log2, d_units, d_part, s);
+    if (e != cudaSuccess) return e;
+  }
   if (P->merge_event) {
     const cudaError_t e = cudaEventRecord(P->merge_event, s);
     if (e != cudaSuccess) return e;

@@ -100,12 +100,13 @@ struct FpChunk {
 };
 
 template <int G>
-__global__ void __launch_bounds__(kFpWarps * 32, 1)
-    fp_segment_kernel(const uint16_t* __restrict__ q, int hq, float scale_log2, const Unit* __restrict__ units,
-                      const Split* __restrict__ fsplits, const int32_t* __restrict__ fpw, int n_fpw, int first_split,
-                      const uint16_t* __restrict__ fpk, const uint16_t* __restrict__ fpv, int fp_cap, int hkv,
-                      const int32_t* __restrict__ nfp, float* __restrict__ part, uint32_t* __restrict__ status) {
-  extern __shared__ __align__(128) uint8_t smem[];
+__device__ __forceinline__ void fp_segment_warp(uint8_t* smem, const uint16_t* __restrict__ q, int hq,
+                                                float scale_log2, const Unit* __restrict__ units,
+                                                const Split* __restrict__ fsplits, const int32_t* __restrict__ fpw,
+                                                int n_fpw, int first_split, const uint16_t* __restrict__ fpk,
+                                                const uint16_t* __restrict__ fpv, int fp_cap, int hkv,
+                                                const int32_t* __restrict__ nfp, float* __restrict__ part,
+                                                uint32_t* __restrict__ status) {
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gw = blockIdx.x * kFpWarps + w;
   if (gw >= n_fpw) return;   // warps are independent: no block barrier below
@@ -309,6 +310,24 @@ __global__ void __launch_bounds__(kFpWarps * 32, 1)
   }
 }
 
+// Launched as a programmatic dependent of the page scan: the scan's CTAs
+// signal at their start, so these CTAs take SMs as the scan's CTAs retire.
+// Everything read here was written before the scan began.  Every thread
+// waits for the scan grid before it exits, so that the merge's single wait
+// (on this grid) covers both.
+template <int G>
+__global__ void __launch_bounds__(kFpWarps * 32, 1)
+    fp_segment_kernel(const uint16_t* __restrict__ q, int hq, float scale_log2, const Unit* __restrict__ units,
+                      const Split* __restrict__ fsplits, const int32_t* __restrict__ fpw, int n_fpw, int first_split,
+                      const uint16_t* __restrict__ fpk, const uint16_t* __restrict__ fpv, int fp_cap, int hkv,
+                      const int32_t* __restrict__ nfp, float* __restrict__ part, uint32_t* __restrict__ status) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  asm volatile("griddepcontrol.launch_dependents;");   // the merge may be staged
+  fp_segment_warp<G>(smem, q, hq, scale_log2, units, fsplits, fpw, n_fpw, first_split, fpk, fpv, fp_cap, hkv, nfp,
+                     part, status);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Rows src [n][hkv][128] -> row slot[t] of the lists of request req[t] (one
 // per kv head); then the new list lengths (len_req[i] <- len_val[i]).  V = 8:
 // 16-byte pieces (both sides 16-byte aligned), V = 1: single elements.  A
@@ -384,10 +403,9 @@ cudaError_t launch_fp_g(kv_pool* P, const uint16_t* q, int32_t hq, float scale_l
     attr_set = true;
   }
   const dim3 grid((unsigned)((n_fpw + kFpWarps - 1) / kFpWarps)), block(kFpWarps * 32);
-  fp_segment_kernel<G><<<grid, block, kFpSmem, s>>>(q, hq, scale_log2, d_units, d_fsplits, d_fpw, n_fpw,
-                                                              first_split, P->d_fpk, P->d_fpv, P->fp_cap,
-                                                              P->cfg.num_kv_heads, P->d_nfp, d_part, P->d_status);
-  return cudaGetLastError();
+  return launch_pdl(fp_segment_kernel<G>, grid, block, kFpSmem, s, q, hq, scale_log2, d_units, d_fsplits, d_fpw,
+                    n_fpw, first_split, (const uint16_t*)P->d_fpk, (const uint16_t*)P->d_fpv, P->fp_cap,
+                    P->cfg.num_kv_heads, (const int32_t*)P->d_nfp, d_part, P->d_status);
 }
 
 }  // namespace
@@ -418,6 +436,13 @@ cudaError_t launch_fp_segments(kv_pool* P, const void* q, int32_t hq, float scal
 #undef KVQ_FP_CASE
   ++P->launches;
   return e;
+}
+
+cudaError_t launch_fp_pending(kv_pool* P, const void* q, int32_t hq, float scale_log2, const Unit* d_units,
+                              float* d_part, cudaStream_t s) {
+  const FpLaunch f = P->fp_pending;
+  P->fp_pending = FpLaunch{};
+  return launch_fp_segments(P, q, hq, scale_log2, d_units, f.d_fsplits, f.d_fpw, f.n_fpw, f.first_split, d_part, s);
 }
 
 cudaError_t launch_fp_store(kv_pool* P, const void* k, const void* v, int64_t n, const int32_t* d_req,

@@ -98,6 +98,15 @@ struct Split {
   int32_t pad[2];
 };
 
+// A full-precision scan to run between the page scan and the merge of the
+// next decode launch (set by the caller of launch_decode_*).
+struct FpLaunch {
+  const Split* d_fsplits = nullptr;
+  const int32_t* d_fpw = nullptr;
+  int n_fpw = 0;
+  int first_split = 0;
+};
+
 // Scan order of a unit: position p < n visits table index
 //   lead  floor(p m / n)                 if floor((p+1) m / n) > floor(p m / n)
 //   tail  m + p - floor((p+1) m / n)     otherwise,
@@ -268,6 +277,7 @@ struct kv_pool {
   int32_t n_units = 0, n_splits = 0;
   int32_t n_page_splits = 0;          // splits [0, n_page_splits) are page splits, the rest full-precision
   size_t plan_fpw_off = 0;            // full-precision worker split ranges in the plan buffer
+  kvq::FpLaunch fp_pending;           // launched by the next launch_decode_* between scan and merge
   int32_t n_fpw = 0;
   size_t plan_units_off = 0, plan_splits_off = 0, plan_cta_off = 0;
   int32_t n_ctas = 0;
@@ -328,11 +338,15 @@ int fp_workers(const kv_pool* P);   // warps of the full-precision scan (one CTA
 
 // Full-precision scan (kvq_fp.cu): warp k scans the splits
 // [d_fpw[k], d_fpw[k + 1]) of d_fsplits and writes one partial per split at
-// split index first_split + i of d_part.  Launched in stream order (no
-// programmatic overlap).
+// split index first_split + i of d_part.  Launched as a programmatic
+// dependent of the page scan (it reads nothing the scan writes and waits for
+// the scan grid before it exits).  launch_fp_pending launches P->fp_pending
+// and clears it.
 cudaError_t launch_fp_segments(kv_pool* P, const void* q, int32_t hq, float scale_log2, const Unit* d_units,
                                const Split* d_fsplits, const int32_t* d_fpw, int n_fpw, int first_split, float* d_part,
                                cudaStream_t s);
+cudaError_t launch_fp_pending(kv_pool* P, const void* q, int32_t hq, float scale_log2, const Unit* d_units,
+                              float* d_part, cudaStream_t s);
 // Copies into / within the full-precision lists (kvq_fp.cu).
 cudaError_t launch_fp_store(kv_pool* P, const void* k, const void* v, int64_t n, const int32_t* d_req,
                             const int32_t* d_slot, const int32_t* d_len_req, const int32_t* d_len_val, int n_len,

@@ -130,13 +130,8 @@ extern "C" kv_status_t kv_decode_attn_noalloc(kv_pool_t* P, const void* q, const
     return nfail(KV_ERR_CUDA, "kv_decode_attn_noalloc: plan upload failed");
   const float scale_log2 = softmax_scale * 1.4426950408889634f;
   const int n_fpw = (int)hp.fp_wsplit.size() - 1;
-  if (n_fpw > 0) {
-    const cudaError_t ef = launch_fp_segments(P, q, hq, scale_log2, (const Unit*)base,
-                                              (const Split*)(base + splits_off) + hp.n_page_splits,
-                                              (const int32_t*)(base + fpw_off), n_fpw, hp.n_page_splits,
-                                              (float*)(base + part_off), s);
-    if (ef != cudaSuccess) return nfail(KV_ERR_CUDA, cudaGetErrorString(ef));
-  }
+  P->fp_pending = FpLaunch{(const Split*)(base + splits_off) + hp.n_page_splits, (const int32_t*)(base + fpw_off),
+                           n_fpw, hp.n_page_splits};
   const cudaError_t e =
       impl == KV_DECODE_MMA
           ? launch_decode_mma(P, q, hq, scale_log2, (const Unit*)base, (int)n_units, (const Split*)(base + splits_off),

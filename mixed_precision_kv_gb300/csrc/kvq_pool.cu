@@ -1325,8 +1325,8 @@ kv_status_t kv_decode_attn(kv_pool_t* P, const void* q, const int32_t* req_ids, 
   cudaEvent_t* tv = rec ? &P->tev[3 * (size_t)(P->timed_calls % kTimingRing)] : nullptr;
   if (tv) KV_CUDA(cudaEventRecord(tv[0], s));
   P->merge_event = tv ? tv[1] : nullptr;
-  KV_CUDA(launch_fp_segments(P, q, hq, scale_log2, du, dsp + P->n_page_splits, (const int32_t*)(base + P->plan_fpw_off),
-                             P->n_fpw, P->n_page_splits, (float*)P->partials.ptr, s));
+  P->fp_pending = FpLaunch{dsp + P->n_page_splits, (const int32_t*)(base + P->plan_fpw_off), P->n_fpw,
+                            P->n_page_splits};
   if (impl == KV_DECODE_MMA)
     KV_CUDA(launch_decode_mma(P, q, hq, scale_log2, du, P->n_units, dsp, dct, P->n_ctas, P->frags.ptr,
                               (float*)P->partials.ptr, out, s));
