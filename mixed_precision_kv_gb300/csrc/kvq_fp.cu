@@ -97,6 +97,7 @@ __device__ __forceinline__ bool fbar_wait(unsigned long long* b, uint32_t phase)
 struct FpChunk {
   int split, t0, n;
   size_t row;   // index of the chunk's first row in the lists (rows of 128)
+  int e;        // end of the chunk's split
 };
 
 template <int G>
@@ -129,12 +130,20 @@ __device__ __forceinline__ void fp_segment_warp(uint8_t* smem, const uint16_t* _
     range(sidx, a, e);
     t0 = max(t0, a);
     while (t0 >= e) {
-      if (++sidx >= se) return FpChunk{se, 0, 0, 0};
+      if (++sidx >= se) return FpChunk{se, 0, 0, 0, 0};
       range(sidx, a, e);
       t0 = a;
     }
     const Unit u = units[fsplits[sidx].unit];
-    return FpChunk{sidx, t0, min(kFpTok, e - t0), ((size_t)u.req * hkv + u.kvh) * (size_t)fp_cap + (size_t)t0};
+    return FpChunk{sidx, t0, min(kFpTok, e - t0), ((size_t)u.req * hkv + u.kvh) * (size_t)fp_cap + (size_t)t0, e};
+  };
+  // the chunk after c: the next kFpTok tokens of its split without a load,
+  // else the first chunk of a later split
+  auto chunk_after = [&](const FpChunk& c) -> FpChunk {
+    if (c.split >= se) return c;
+    const int t0 = c.t0 + kFpTok;
+    if (t0 < c.e) return FpChunk{c.split, t0, min(kFpTok, c.e - t0), c.row + kFpTok, c.e};
+    return c.split + 1 < se ? chunk_at(c.split + 1, 0) : FpChunk{se, 0, 0, 0, 0};
   };
   auto issue = [&](const FpChunk& c, int st) {   // lane 0
     fbulk(S.k[st], fpk + c.row * kHeadDim, (uint32_t)c.n * kRowBytes, &S.bar[st][0]);
@@ -157,7 +166,7 @@ __device__ __forceinline__ void fp_segment_warp(uint8_t* smem, const uint16_t* _
   ring[0] = chunk_at(sb, 0);   // the first chunk of split sb (or of a later split; the ones before are empty)
 #pragma unroll
   for (int x = 1; x < kFpStages; ++x)
-    ring[x] = ring[x - 1].split < se ? chunk_at(ring[x - 1].split, ring[x - 1].t0 + kFpTok) : ring[x - 1];
+    ring[x] = chunk_after(ring[x - 1]);
   if (lane == 0) {
 #pragma unroll
     for (int x = 0; x < kFpStages; ++x)
@@ -262,7 +271,7 @@ __device__ __forceinline__ void fp_segment_warp(uint8_t* smem, const uint16_t* _
       }
       __syncwarp();   // stage st, P and the rescale read: chunk c + kFpStages may land in the stage
       const FpChunk& last = ring[kFpStages - 1];
-      const FpChunk nxt = last.split < se ? chunk_at(last.split, last.t0 + kFpTok) : last;
+      const FpChunk nxt = chunk_after(last);
       if (nxt.split < se && lane == 0) issue(nxt, st);
       ++n_chunk;
 #pragma unroll
