@@ -265,6 +265,9 @@ def main():
                     help="decode with full-precision segments: per kv head 5%% vertical-line tokens excluded from "
                          "its quantized set, a 128-token window and a 128-token staging buffer in bf16; every "
                          "128 steps the staging buffer is quantized into the pool")
+    ap.add_argument("--ragged-heads", action="store_true",
+                    help="per-head budgets: kv head h keeps the most recent (h+1)/num_kv_heads of every prompt; "
+                         "the older positions are excluded for that head only (whole pages are skipped)")
     ap.add_argument("--mode", default="decode", choices=["decode", "prefill"],
                     help="decode: the decode-step line (default); prefill: bulk quantization of the workload's "
                          "prompts through kv_append_quant")
@@ -295,6 +298,14 @@ def main():
     gw.prefill()
     gw.evict()
     n_vl = []
+    if args.ragged_heads:
+        H = w.num_kv_heads
+        for r, spec in enumerate(w.requests):
+            n = spec.n_prefill
+            cuts = [n - int(round(n * (h + 1) / H)) for h in range(H)]
+            pos = np.concatenate([np.arange(c, dtype=np.int64) for c in cuts])
+            heads = np.concatenate([np.full(c, h, np.int32) for h, c in enumerate(cuts)])
+            gw.pool.evict_head(np.full(pos.size, gw.rids[r], np.int32), pos, heads)
     if args.segments:
         win_k, win_v, n_vl = gw.freeze_segments(rho=0.05, window=SEG_W, staging=SEG_WS)
     gw.reorder()
@@ -406,7 +417,7 @@ def main():
     value = job_throughput(step_bytes, args.steps, ws, t_ms)
     achieved = step_bytes / (scan_ms / 1e3) / 1e9
     peak, peak_kind = measured_peak()
-    traffic = None if args.segments else recorded_traffic(step_bytes, w.name, args.decode_impl)
+    traffic = None if (args.segments or args.ragged_heads) else recorded_traffic(step_bytes, w.name, args.decode_impl)
 
     # End to end: host (pinned) inputs copied in and the output copied out every
     # step.  A step's K, V and q sit in one pinned buffer and go in one copy.
@@ -441,7 +452,8 @@ def main():
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": t_ms / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "u4/u2 codes, f16 meta, f32 accum", "data": "synthetic",
-            "config": {"workload": w.name + ("+fp-segments" if args.segments else ""), "batch": B, "num_q_heads": Hq, "num_kv_heads": Hkv, "head_dim": 128,
+            "config": {"workload": w.name + ("+fp-segments" if args.segments else "") +
+                                   ("+ragged-heads" if args.ragged_heads else ""), "batch": B, "num_q_heads": Hq, "num_kv_heads": Hkv, "head_dim": 128,
                        "context": w.requests[0].n_prefill, "page_tokens": 32, "budget_bits": "3.0",
                        "decode_impl": args.decode_impl, "l2": "inputs larger than L2 (%.0f MB per step)"
                                                              % (step_bytes / 1e6),

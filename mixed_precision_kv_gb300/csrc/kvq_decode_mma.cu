@@ -785,13 +785,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(
   int bbase = 0, bcount = 0;   // the batch holds stream pages [bbase, bbase + bcount)
   int32_t bid = -1, btag = 0;
   uint32_t blive = 0u;
+  int32_t brank = -1;   // kHead: rank of this lane's page among the batch's pages with a live slot (-1: none)
   unsigned long long bsrc = 0ull;
+  // kHead: a page whose every slot is dead for this kv head is skipped (no
+  // copy, no work): it would add nothing, since a dead slot's weight
+  // 2^(-1e4 log2 e - m) is 0 and its V is 0.  A unit left with no page reads
+  // as empty, as an all-dead unit does.
   auto refill = [&](int k) {
+    for (;;) {
     while (lpos >= lend && lsg + 1 < s_end) enter(++lsg);
     const int nb = max(0, min(32, lend - lpos));
     bbase = k;
     bcount = nb;
     bid = -1;
+    if constexpr (kHead) blive = 0u;
     if (lane < nb) {
       // scan-order position p -> table index: the next INT2-first entry when
       // floor((p+1) m / n) > floor(p m / n), else the next of the others
@@ -816,6 +823,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(
       bsrc = (unsigned long long)(uintptr_t)src;
     }
     lpos += nb;
+    if constexpr (kHead) {
+      const bool keep = lane < nb && blive != 0u;
+      const uint32_t kept = __ballot_sync(0xFFFFFFFFu, keep);
+      brank = keep ? __popc(kept & ((1u << lane) - 1u)) : -1;
+      bcount = __popc(kept);
+      if (bcount > 0 || nb == 0) break;   // else the whole batch is dead: the next one
+    } else {
+      break;
+    }
+    }
   };
   bool more = true;   // the stream may hold pages past the current batch
   // ticket of stream page k (k >= bbase; refills when k is past the batch)
@@ -828,7 +845,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(
         return Ticket{-1, 0u, 0};
       }
     }
-    const int j = k - bbase;
+    int j = k - bbase;
+    if constexpr (kHead) j = __ffs(__ballot_sync(0xFFFFFFFFu, brank == j)) - 1;   // the lane of the j-th page kept
     src = __shfl_sync(0xFFFFFFFFu, bsrc, j);
     return Ticket{__shfl_sync(0xFFFFFFFFu, bid, j), __shfl_sync(0xFFFFFFFFu, blive, j),
                   __shfl_sync(0xFFFFFFFFu, btag, j)};

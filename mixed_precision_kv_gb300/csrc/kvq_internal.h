@@ -173,6 +173,7 @@ struct Request {
   std::vector<uint32_t> loc;        // token position -> page_id << 5 | slot
   uint64_t version = 0;             // bumped whenever the table's entries change
   uint64_t ordered_version = ~0ull; // version at which the table was last seen INT2-first
+  uint64_t shape = 0;               // pool clock at the last open, erase or reorder of entries (not appends)
 };
 
 // Free page ids of one class, handed out lowest id first (a bitset with a
@@ -271,6 +272,8 @@ struct kv_pool {
   std::vector<int32_t> plan_req;
   std::vector<int32_t> plan_len;      // table lengths of plan_req when the plan was built
   std::vector<int32_t> plan_nfp;      // full-precision list lengths when the plan was built
+  std::vector<uint64_t> plan_ver;     // table shapes (Request::shape) when the plan was built
+  uint64_t shape_clock = 0;
   int32_t plan_slack = 0;             // pages a table may grow before the plan is rebuilt
   int32_t plan_hq = 0;
   int32_t plan_impl = -1;

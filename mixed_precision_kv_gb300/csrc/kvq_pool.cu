@@ -223,31 +223,39 @@ void kvq::plan_decode(const kv_pool* P, const int32_t* req_ids, int32_t batch, i
   auto cost = [&](int32_t id) { return id < n2 ? pc.int2 : pc.int4; };
   // Per request: the cost of its first i pages in scan order (shared by the
   // request's kv heads), so that worker boundaries are found by binary search
-  // instead of a walk over every (page, kv head).
-  std::vector<int64_t> off((size_t)batch + 1, 0);
+  // instead of a walk over every (page, kv head).  With per-head exclusion
+  // the prefix is per unit: a full page with no live slot for the head costs
+  // nothing (the tensor-core scan skips it; a page still being filled keeps
+  // its cost, since appends may give it live slots).
+  const bool per_head = !P->hdead.empty();
+  const int np = per_head ? hkv : 1;   // prefixes per request
+  std::vector<int64_t> off((size_t)batch * np + 1, 0);
   std::vector<int32_t> lead((size_t)batch, 0);
   for (int32_t b = 0; b < batch; ++b) {
     const auto& tb = P->reqs[req_ids[b]].table;
     if (spread)
       for (int32_t id : tb) lead[b] += id < n2 ? 1 : 0;
-    off[b + 1] = off[b] + (int64_t)tb.size() + 1;
+    for (int x = 0; x < np; ++x) off[(size_t)b * np + x + 1] = off[(size_t)b * np + x] + (int64_t)tb.size() + 1;
   }
-  std::vector<double> pre((size_t)off[batch]);
+  std::vector<double> pre((size_t)off[(size_t)batch * np]);
   double total = 0.0;
   int64_t pages = 0;
   for (int32_t b = 0; b < batch; ++b) {
     const auto& tb = P->reqs[req_ids[b]].table;
     const int32_t npos = (int32_t)tb.size();
-    double* pb = &pre[off[b]];
     ScanOrder so;
     so.start(0, npos, lead[b]);
-    double c = 0.0;
-    pb[0] = 0.0;
+    for (int x = 0; x < np; ++x) pre[off[(size_t)b * np + x]] = 0.0;
     for (int32_t i = 0; i < npos; ++i) {
-      c += cost(tb[so.next()]);
-      pb[i + 1] = c;
+      const int32_t id = tb[so.next()];
+      const double c = cost(id);
+      for (int x = 0; x < np; ++x) {
+        double* pb = &pre[off[(size_t)b * np + x]];
+        const bool dead = per_head && P->fill[id] == kPage && (P->live[id] & ~P->hdead[(size_t)id * hkv + x]) == 0u;
+        pb[i + 1] = pb[i] + (dead ? 0.0 : c);
+      }
     }
-    total += c * hkv;
+    for (int x = 0; x < np; ++x) total += pre[off[(size_t)b * np + x] + npos] * (per_head ? 1 : hkv);
     pages += (int64_t)npos * hkv;
   }
   // at least min_pages pages per worker, so small batches do not pay a
@@ -263,8 +271,8 @@ void kvq::plan_decode(const kv_pool* P, const int32_t* req_ids, int32_t batch, i
   double U = 0.0;         // cost before the current unit
   for (int32_t b = 0; b < batch; ++b) {
     const int32_t npos = (int32_t)P->reqs[req_ids[b]].table.size();
-    const double* pb = &pre[off[b]];
     for (int h = 0; h < hkv; ++h) {
+      const double* pb = &pre[off[(size_t)b * np + (per_head ? h : 0)]];
       const int32_t ui = b * hkv + h;
       Unit& u = out.units[ui];
       u.b = b;
@@ -272,6 +280,21 @@ void kvq::plan_decode(const kv_pool* P, const int32_t* req_ids, int32_t batch, i
       u.kvh = h;
       u.split_begin = (int32_t)out.splits.size();
       int32_t i = 0;
+      if (per_head) {
+        // leading full pages with no live slot for this head (a head that keeps
+        // only recent tokens) are left out of the splits: no worker walks them.
+        // The plan is rebuilt whenever a table's entries are erased or moved,
+        // so the pages at those positions stay the ones found dead here (new
+        // pages go to the end; exclusions and evictions only kill slots).
+        while (i < npos && pb[i + 1] == pb[i]) ++i;
+        if (i == npos && npos > 0) {
+          // nothing live: one empty split, open-ended so that pages appended
+          // after planning are scanned
+          const int64_t j = worker(U + pb[npos]);
+          while (cur < j) out.cta_split[++cur] = (int32_t)out.splits.size();
+          out.splits.push_back(Split{ui, npos, npos, req_ids[b], npos, lead[b], {0, 0}});
+        }
+      }
       while (i < npos) {
         const int64_t j = worker(U + pb[i]);
         while (cur < j) out.cta_split[++cur] = (int32_t)out.splits.size();
@@ -459,6 +482,7 @@ kv_status_t kv_request_open(kv_pool_t* P, int32_t* req_id) {
       const uint64_t v = P->reqs[r].version;
       P->reqs[r] = Request();
       P->reqs[r].open = true;
+      P->reqs[r].shape = ++P->shape_clock;
       P->reqs[r].version = v + 1;
       *req_id = r;
       return KV_OK;
@@ -756,6 +780,7 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
       const auto it = std::next(rit).base();
       dirty.structural(r, (int32_t)(it - R.table.begin()));
       R.table.erase(it);
+      R.shape = ++P->shape_clock;
       repacks.push_back(RepackJob{sp, nid_rep});
       deferred.push_back(sp);
       app.emplace_back(i2[(size_t)(b_e - 1)], nid_rep);
@@ -850,6 +875,7 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
       const auto it = std::next(rit).base();
       dirty.structural(r, (int32_t)(it - R.table.begin()));
       R.table.erase(it);
+      R.shape = ++P->shape_clock;
       R.table.push_back(nid);
       if (c.stag_direct) {
         directs.push_back(DirectJob{nid, (int32_t)dtoks.size()});
@@ -963,6 +989,7 @@ kv_status_t kv_reorder_pages(kv_pool_t* P, const int32_t* req_ids, int32_t n_req
     if (std::find_if(first_int4, R.table.end(), [&](int32_t id) { return is_int2(P, id); }) != R.table.end()) {
       const int32_t from = (int32_t)(first_int4 - R.table.begin());
       std::stable_partition(R.table.begin(), R.table.end(), [&](int32_t id) { return is_int2(P, id); });
+      R.shape = ++P->shape_clock;
       dirty.structural(req_ids[i], from);
       ++R.version;
     }
@@ -1056,6 +1083,7 @@ kv_status_t kv_evict_slots_head(kv_pool_t* P, const int32_t* req_ids, const int6
     hdead_set(P, id, kv_heads[i], P->hdead[(size_t)id * hkv + kv_heads[i]] | (1u << (l & 31u)), upd);
   }
   if (upd.empty()) return KV_OK;
+  P->plan_impl = -1;   // page costs per head changed: plan again at the next decode
   hdead_final(P, upd);
   Upload u;
   const size_t o = u.add(upd.data(), upd.size() * sizeof(TableUpd));
@@ -1250,6 +1278,9 @@ kv_status_t build_plan(kv_pool* P, const int32_t* req_ids, int32_t batch, int32_
     same = P->plan_req[b] == req_ids[b] && len >= len0 && len - len0 <= P->plan_slack && (len0 > 0 || len == 0);
     const int32_t nf = P->n_fp.empty() ? 0 : P->n_fp[req_ids[b]], nf0 = P->plan_nfp[b];
     same = same && nf >= nf0 && nf - nf0 < 2 * kFpMinTokens && (nf0 > 0 || nf == 0);
+    // with per-head exclusion, splits may leave out positions found dead: an
+    // entry erased or moved (not an append at the end) plans again
+    same = same && (P->hdead.empty() || P->plan_ver[b] == P->reqs[req_ids[b]].shape);
   }
   if (same) return KV_OK;
 
@@ -1278,6 +1309,8 @@ kv_status_t build_plan(kv_pool* P, const int32_t* req_ids, int32_t batch, int32_
   P->plan_req.assign(req_ids, req_ids + batch);
   P->plan_len.resize(batch);
   P->plan_nfp.resize(batch);
+  P->plan_ver.resize(batch);
+  for (int32_t b = 0; b < batch; ++b) P->plan_ver[b] = P->reqs[req_ids[b]].shape;
   for (int32_t b = 0; b < batch; ++b) P->plan_nfp[b] = P->n_fp.empty() ? 0 : P->n_fp[req_ids[b]];
   int64_t total_pages = 0;
   for (int32_t b = 0; b < batch; ++b) {
@@ -1390,7 +1423,11 @@ kv_status_t kv_last_decode_stats(kv_pool_t* P, int64_t* kv_bytes, int32_t* n_spl
   for (int32_t r : P->stat_req) {
     if (!req_ok(P, r)) continue;
     for (int32_t id : P->reqs[r].table) {
-      bytes += is_int2(P, id) ? (int64_t)kInt2Block * hkv : (int64_t)P->fill[id] * 160 * hkv;
+      // with per-head exclusion, a page with no live slot for a head is not read for it
+      int64_t heads = hkv;
+      if (!P->hdead.empty())
+        for (int h = 0; h < hkv; ++h) heads -= (P->live[id] & ~P->hdead[(size_t)id * hkv + h]) == 0u ? 1 : 0;
+      bytes += is_int2(P, id) ? (int64_t)kInt2Block * heads : (int64_t)P->fill[id] * 160 * heads;
       bytes += 8;
       ++pages;
     }

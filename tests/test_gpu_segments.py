@@ -209,3 +209,32 @@ def test_batched_append_interleaves_requests(kvq):
     assert [sc.gpu.fp_count(g) for g in sc.g_ids] == [5, 9, 2]
     sc.gpu.sync()
     sc.check_decode(what="batched append")
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_ragged_head_retention(kvq, impl):
+    """Heads keep different amounts of context (a per-head budget): head h
+    drops every position before its cut, so whole pages are dead for it and
+    the tensor-core scan skips them; one head of one request drops all."""
+    bits = [_mixed(900, 0.6, 1), _mixed(400, 0.5, 2)]
+    hkv, hq = 4, 16
+    sc = Scenario(kvq, hkv, hq, bits, chunk=128, impl=impl)
+    for r, (g, o) in enumerate(zip(sc.g_ids, sc.o_ids)):
+        n = bits[r].size
+        cuts = [0, n // 4, n // 2, n if r == 1 else (7 * n) // 8]
+        pos = np.concatenate([np.arange(c) for c in cuts])
+        heads = np.concatenate([np.full(c, h) for h, c in enumerate(cuts)])
+        sc.gpu.evict_head(np.full(pos.size, g), pos, heads)
+        assert sc.orc.evict_head(np.full(pos.size, o), pos, heads) == oracle.OK
+    sc.gpu.sync()
+    sc.check_decode(what=f"ragged retention impl={impl}")
+    stats = sc.gpu.last_decode_stats()
+    assert stats["kv_bytes"] > 0
+    # appends after the cut are read by every head
+    k = kvsynth.fill_bf16_host(40, hkv, 128, SEED, kvsynth.TENSOR_K, 70)
+    v = kvsynth.fill_bf16_host(40, hkv, 128, SEED, kvsynth.TENSOR_V, 70)
+    b = _mixed(40, 0.5, 71)
+    sc.gpu.append(_dev(k), _dev(v), np.full(40, sc.g_ids[1]), b)
+    assert sc.orc.append(np.full(40, sc.o_ids[1]), b, k, v) == oracle.OK
+    sc.gpu.sync()
+    sc.check_decode(step=1, what=f"ragged retention after append impl={impl}")
