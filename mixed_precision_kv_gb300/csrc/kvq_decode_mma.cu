@@ -44,6 +44,7 @@
 // mbarrier completion; the ring runs across unit boundaries.  Every wait is
 // bounded and reports a timeout status.
 #include <algorithm>
+#include <atomic>
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -1020,12 +1021,15 @@ template <int G>
 cudaError_t launch_mma_g(kv_pool* P, const void* q, int32_t hq, float scale_log2, const Unit* d_units, int n_units,
                          const Split* d_splits, const int32_t* d_wsplit, int n_workers, void* d_frags, float* d_part,
                          cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
+  // function attributes are set once per device (bit = device ordinal)
+  static std::atomic<uint64_t> attr_set{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!(attr_set.load() >> dev & 1u)) {
     cudaError_t e = set_scan_attributes<G, false>();
     if (e == cudaSuccess) e = set_scan_attributes<G, true>();
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    attr_set.fetch_or(uint64_t(1) << dev);
   }
   if (n_workers <= 0 || n_units <= 0) return cudaSuccess;
   const uint32_t* smax = P->d_status + 1;

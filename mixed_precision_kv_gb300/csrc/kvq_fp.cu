@@ -17,6 +17,8 @@
 // combines both.
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
@@ -404,12 +406,15 @@ template <int G>
 cudaError_t launch_fp_g(kv_pool* P, const uint16_t* q, int32_t hq, float scale_log2, const Unit* d_units,
                         const Split* d_fsplits, const int32_t* d_fpw, int n_fpw, int first_split, float* d_part,
                         cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
+  // function attributes are set once per device (bit = device ordinal)
+  static std::atomic<uint64_t> attr_set{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!(attr_set.load() >> dev & 1u)) {
     const cudaError_t e =
         cudaFuncSetAttribute(fp_segment_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFpSmem);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    attr_set.fetch_or(uint64_t(1) << dev);
   }
   const dim3 grid((unsigned)((n_fpw + kFpWarps - 1) / kFpWarps)), block(kFpWarps * 32);
   return launch_pdl(fp_segment_kernel<G>, grid, block, kFpSmem, s, q, hq, scale_log2, d_units, d_fsplits, d_fpw,
