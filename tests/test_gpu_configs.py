@@ -155,3 +155,49 @@ def test_config4_full_size_sampled(kvq):
     got = np.stack([out[b, h] for b, h in pairs])
     assert_outputs_close(got, ref, "config 4 full size, sampled")
     assert rng is not None
+
+
+def test_config2_full_size_segments_and_budgets(kvq):
+    """The 32K-token batch-8 workload with per-head budgets (kv head h keeps the
+    most recent (h + 1)/8 of each prompt; whole pages are skipped) and
+    full-precision segments (5 % vertical lines per kv head, a 128-token
+    window), both as the bench sets them up; sampled units against the oracle."""
+    w = kvsynth.make_workload(2)
+    rng = np.random.default_rng(22)
+    reqs, heads, pairs = _sampled(w, rng, 1)
+    gw, ow = _pair(w, chunk=16384, sel_heads=heads, content_reqs=reqs)
+    _build(gw, ow)
+    H = w.num_kv_heads
+    for r, spec in enumerate(w.requests):
+        n = spec.n_prefill
+        cuts = [n - int(round(n * (h + 1) / H)) for h in range(H)]
+        pos = np.concatenate([np.arange(c, dtype=np.int64) for c in cuts])
+        hh = np.concatenate([np.full(c, h, np.int32) for h, c in enumerate(cuts)])
+        gw.pool.evict_head(np.full(pos.size, gw.rids[r], np.int32), pos, hh)
+        if r in reqs:
+            assert ow.P.evict_head(np.full(pos.size, ow.rids[r]), pos, hh) == 0
+    window, rho = 128, 0.05
+    gw.freeze_segments(rho=rho, window=window, staging=128)
+    for r in reqs:
+        n = w.requests[r].n_prefill
+        pre = n - window
+        nv = int(rho * pre)
+        score = np.random.default_rng([w.seed, 77, r]).random((H, pre))
+        pos = [np.sort(np.argpartition(score[h], pre - nv)[pre - nv:]) for h in range(H)]
+        o = ow.rids[r]
+        assert ow.P.evict_head(np.full(nv * H, o), np.concatenate(pos), np.repeat(np.arange(H), nv)) == 0
+        assert ow.P.evict(np.full(window, o), np.arange(pre, n)) == 0
+        k_all, v_all = ow.kv_rows(r, 0, n)
+        kf = np.stack([k_all[pos[h], j] for j, h in enumerate(ow.sel)], axis=1)
+        vf = np.stack([v_all[pos[h], j] for j, h in enumerate(ow.sel)], axis=1)
+        assert ow.P.fp_append(o, kf, vf) == 0
+        assert ow.P.fp_append(o, k_all[pre:n], v_all[pre:n]) == 0
+    gw.reorder()
+    ow.reorder()
+    gw.pool.sync()
+    out = gw.decode(gw.q(0)).cpu().numpy()
+    gw.pool.sync()
+    ref = ow.decode(ow.q(0), pairs=np.array(pairs, np.int32))
+    got = np.stack([out[b, h] for b, h in pairs])
+    assert np.isfinite(got).all()
+    assert_outputs_close(got, ref, "config 2 full size, budgets + segments, sampled")
