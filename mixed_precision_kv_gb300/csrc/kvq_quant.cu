@@ -358,7 +358,13 @@ __global__ void __launch_bounds__(kThreads) repack_int2_kernel(uint8_t* __restri
 // within one call.  The staging page's INT4 image is built in shared memory
 // exactly as the append kernel builds a new page (a warp per token), then
 // requantized to INT2 as the repack kernel does; only the INT2 block is
-// written to memory.
+// written to memory.  Launched as a programmatic dependent of the append
+// kernel, which signals after its own wait: the earlier work on the stream
+// (the previous decode, the uploads) is complete when this grid starts, and
+// it touches nothing the append kernel writes, so the two run side by side.
+// Every thread waits for the append grid before it exits, so the kernels
+// that follow in stream order (the repack reads staging pages the append
+// kernel fills) see both.
 __global__ void __launch_bounds__(kThreads) direct_int2_kernel(
     uint8_t* __restrict__ pool, int hkv, const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
     const DirectJob* __restrict__ jobs, const int32_t* __restrict__ toks, uint32_t* __restrict__ status) {
@@ -381,6 +387,7 @@ __global__ void __launch_bounds__(kThreads) direct_int2_kernel(
   uint8_t* dblk = pool + ((size_t)job.dst * hkv + h) * kInt2Block;
   for (int i = threadIdx.x; i < kInt2Block / 16; i += kThreads)
     reinterpret_cast<uint4*>(dblk)[i] = reinterpret_cast<const uint4*>(dst)[i];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 __global__ void scatter_kernel(Entry* __restrict__ table, int32_t* __restrict__ ntab, uint32_t* __restrict__ hdead,
@@ -426,9 +433,8 @@ cudaError_t launch_direct_int2(kv_pool* P, const void* k, const void* v, const D
   if (n_jobs <= 0) return cudaSuccess;
   dim3 grid((unsigned)n_jobs, (unsigned)P->cfg.num_kv_heads);
   ++P->launches;
-  direct_int2_kernel<<<grid, kThreads, 0, s>>>(P->d_pool, P->cfg.num_kv_heads, (const __nv_bfloat16*)k,
-                                               (const __nv_bfloat16*)v, d_jobs, d_toks, P->d_status);
-  return cudaGetLastError();
+  return launch_pdl(direct_int2_kernel, grid, dim3(kThreads), 0, s, P->d_pool, P->cfg.num_kv_heads,
+                    (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, d_jobs, d_toks, P->d_status);
 }
 
 cudaError_t launch_scatter(kv_pool* P, const TableUpd* d_upd, int n, cudaStream_t s) {
