@@ -640,8 +640,13 @@ __global__ void __launch_bounds__(256) frag_kernel(const __nv_bfloat16* __restri
                                                    UnitFrag* __restrict__ frags) {
   constexpr bool kPair = Cols<G>::kPair;
   __shared__ FragSmem S;
-  const Unit u = units[blockIdx.x];   // the plan is copied in before the launch (not by a kernel): read it first
-  asm volatile("griddepcontrol.wait;" ::: "memory");   // the appends before this decode are done (scale maxima)
+  // Launched as a programmatic dependent of the last kernel before the decode
+  // (normally the append kernel, which signals after its own wait).  Nothing
+  // it reads is written by that kernel: q and the plan are in place before
+  // it, and the INT2 K scale maximum changes only in repacks, which finish
+  // before their dependents start.  It waits for that grid only before it
+  // exits, so the scan's wait (on this grid) covers the appends too.
+  const Unit u = units[blockIdx.x];
   asm volatile("griddepcontrol.launch_dependents;");   // the scan may be staged
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
   const float smax = fmaxf(__uint_as_float(smax_bits[0]), 1.0f);
@@ -721,6 +726,7 @@ __global__ void __launch_bounds__(256) frag_kernel(const __nv_bfloat16* __restri
   const uint4* src = reinterpret_cast<const uint4*>(&S.f);
   uint4* dst = reinterpret_cast<uint4*>(frags + blockIdx.x);
   for (int x = tid; x < (int)(sizeof(UnitFrag) / 16); x += 256) dst[x] = src[x];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // ---- persistent scan: warp gw = blockIdx.x * kWarps + w of the n_workers
