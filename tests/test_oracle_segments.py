@@ -211,3 +211,30 @@ def test_mixed_request_split_invariance(orc):
     base = P.decode(q, [r], SCALE)
     for s in (2, 5, 64, 1000):
         np.testing.assert_allclose(P.decode(q, [r], SCALE, n_splits=s), base, rtol=1e-12, atol=1e-14)
+
+
+def test_head_budget_all_excluded_head_reads_zero(orc):
+    """Per-head budgets: a head that keeps nothing outputs 0 (every slot is a
+    dead slot for it), a head that keeps a suffix equals attention over that
+    suffix alone, and the other heads are untouched."""
+    rng = np.random.default_rng(31)
+    hkv, n = 3, 160
+    k, v = _rows(n, hkv, kvsynth.TENSOR_K), _rows(n, hkv, kvsynth.TENSOR_V)
+    bits = np.where(rng.random(n) < 0.5, 2, 4).astype(np.uint8)
+    q = _q(1, 2 * hkv)
+    A = orc.OraclePool(hkv, 64, 64, 1, 64)
+    ra = A.open()
+    assert A.append(np.full(n, ra), bits, k, v) == orc.OK
+    full = A.decode(q, [ra], SCALE)
+    cut = 100
+    assert A.evict_head(np.full(n, ra), np.arange(n), np.zeros(n)) == orc.OK          # head 0 keeps nothing
+    assert A.evict_head(np.full(cut, ra), np.arange(cut), np.ones(cut)) == orc.OK     # head 1 keeps the last 60
+    out = A.decode(q, [ra], SCALE)
+    np.testing.assert_array_equal(out[0:2], np.zeros((2, 128)))
+    np.testing.assert_array_equal(out[4:6], full[4:6])
+    # head 1 = the same pool with the first `cut` positions evicted for every head
+    B = orc.OraclePool(hkv, 64, 64, 1, 64)
+    rb = B.open()
+    assert B.append(np.full(n, rb), bits, k, v) == orc.OK
+    assert B.evict(np.full(cut, rb), np.arange(cut)) == orc.OK
+    np.testing.assert_array_equal(out[2:4], B.decode(q, [rb], SCALE)[2:4])
