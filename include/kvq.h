@@ -134,7 +134,11 @@ KVQ_API kv_status_t kv_evict_slots(kv_pool_t* pool, const int32_t* req_ids, cons
  * req_ids, kv_heads: host int32 [n]; token_pos: host int64 [n].  The first call
  * allocates one 32-bit word per (page, kv head) on the device and makes both
  * decode scans read it.  Excluding twice is a no-op; an invalid entry fails
- * the call before any change (KV_ERR_INVALID_ARG). */
+ * the call before any change (KV_ERR_INVALID_ARG).
+ * Per-head budgets (Tangram: head groups keep different amounts of context)
+ * are this call applied to the positions outside a head's budget: the
+ * tensor-core decode then skips every full page with no live slot for the
+ * head, and the split plan balances the pages each head still reads. */
 KVQ_API kv_status_t kv_evict_slots_head(kv_pool_t* pool, const int32_t* req_ids, const int64_t* token_pos,
                                         const int32_t* kv_heads, int64_t n, void* stream);
 
