@@ -1,12 +1,13 @@
 """Benchmark: one decode step of the mixed INT2/INT4 paged-KV path.
 
-A step = append one new token per request (INT4 quantize-on-append into the
-tail page) + INT2-first reorder + split-KV fused-dequant decode attention with
-log-sum-exp merge, over the Qwen3-8B-shaped single-layer workload (batch 8,
-32 query / 8 KV heads, head_dim 128, 32K context per request, INT2:INT4 from
-the greedy allocator at B = 3).  The metric is algorithmic KV bytes per step
-(codes + binary16 scale/zero of every page block read, table entries, q, out)
-divided by the step time.
+A step = append one new token per request (quantize-on-append) + INT2-first
+reorder + split-KV fused-dequant decode attention with log-sum-exp merge.  The
+default workload is the Llama-3-70B-shaped single layer at long agentic
+context (batch 16, 64 query / 8 KV heads, head_dim 128, 100K tokens per
+request, INT2:INT4 from the greedy allocator at B = 2.5, 1 % of token rows
+x8); `--config N` selects another of the five workloads.  The metric is
+algorithmic KV bytes per step (codes + binary16 scale/zero of every page block
+read, table entries, q, out) divided by the step time.
 
 Launch: `python bench.py [--gpus 1] [--steps K] [--warmup W]`; for N > 1 under
 torchrun each rank runs its own replica of the workload (requests are
@@ -45,20 +46,23 @@ def measured_peak():
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    """nvidia-smi samples of SM clock, utilization and throttle reasons, taken
+    from before the warm-up to the end of the timed region; the summary keeps
+    the samples taken while the GPU was busy."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-         "clocks_event_reasons.sw_power_cap")
+         "clocks_event_reasons.sw_power_cap,utilization.gpu")
 
-    def __init__(self, gpu_index):
+    def __init__(self, gpu_index, period_ms=50):
         self.gpu = gpu_index
+        self.period = period_ms
         self.proc = None
         self.lines = []
 
-    def __enter__(self):
+    def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                                          "-lms", "100", "-i", str(self.gpu)], stdout=subprocess.PIPE,
+                                          "-lms", str(self.period), "-i", str(self.gpu)], stdout=subprocess.PIPE,
                                          stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -70,7 +74,7 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
-    def __exit__(self, *a):
+    def stop(self):
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -78,24 +82,36 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
             self.t.join(timeout=2)
+            self.proc = None
+
+    def __enter__(self):
+        return self.start()
+
+    def __exit__(self, *a):
+        self.stop()
 
     def summary(self):
-        sm, mx, reasons = [], [], set()
+        sm, mx, reasons, busy = [], [], set(), 0
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
         for ln in self.lines:
             f = [x.strip() for x in ln.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
                 continue
             try:
-                sm.append(float(f[1]))
-                mx.append(float(f[2]))
+                rows.append((float(f[1]), float(f[2]), float(f[9]), f[5:9]))
             except ValueError:
                 continue
-            for n, v in zip(names, f[5:9]):
+        loaded = [r for r in rows if r[2] > 0]
+        for clk, cmax, _, rs in (loaded or rows):
+            sm.append(clk)
+            mx.append(cmax)
+            for n, v in zip(names, rs):
                 if v.lower().startswith("active"):
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(rows), "samples_under_load": len(loaded),
+                "window": "from before the warm-up to the end of the timed region, every %d ms" % self.period}
 
 
 def dist_setup():
@@ -144,59 +160,134 @@ def recorded_traffic(step_bytes, workload, decode_impl):
     return traffic / rec["algorithmic_bytes"] * step_bytes
 
 
-def cpu_baseline(w, seconds=12.0):
-    """The oracle as it stands, on this host's cores, over one request (all
-    heads) of the same workload: KV-bytes GB/s of its decode."""
+def _oracle_quant_rate(w, n_tok, threads):
+    """bf16 K/V bytes in + page-block bytes out per second of the oracle's
+    quantize-on-append (request 0's first n_tok tokens, every kv head), with
+    `threads` independent oracle pools appending at once (one per thread)."""
+    from concurrent.futures import ThreadPoolExecutor
+    import oracle
+    from oracle.workload import kv_rows, request_bits
+    H = w.num_kv_heads
+    bits = request_bits(w, 0)[:n_tok]
+    k, v = kv_rows(w, 0, 0, n_tok, list(range(H)))
+    n2 = int((bits == 2).sum()) // 32 + 2
+    n4 = -(-int((bits == 4).sum()) // 32) + n_tok // 32 + 4
+    pools = [oracle.OraclePool(H, n2, n4, 1, n2 + n4) for _ in range(threads)]
+    rids = [P.open() for P in pools]
+
+    def one(i):
+        assert pools[i].append(np.full(n_tok, rids[i]), bits, k, v) == oracle.OK
+
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(threads) as ex:      # the oracle's calls release the GIL
+        list(ex.map(one, range(threads)))
+    dt = time.perf_counter() - t0
+    ex0 = pools[0].export(rids[0], content=False)
+    out_bytes = sum(3072 if is2 else 160 * int(f) for is2, f in zip(ex0["is_int2"], ex0["fill"])) * H
+    in_bytes = n_tok * H * 128 * 2 * 2
+    return (in_bytes + out_bytes) * threads / dt / 1e9, dt
+
+
+def cpu_baseline(w, quant_tokens=8192):
+    """The oracle as it stands, on this host's cores, over a bounded sample of
+    the same workload, timed in two parts:
+      quantize-on-append: request 0's first `quant_tokens` tokens (all kv
+        heads) into a fresh oracle pool, one thread, then one pool per core
+        appending at once (GB/s of bf16 K/V in + page blocks out);
+      decode: fp64 attention of request 0 at its full context for the units
+        (kv heads) of the sample, one thread over one unit, then all cores
+        over two units with the oracle's OpenMP loop (KV-bytes GB/s, the
+        metric's unit).
+    value = the all-cores decode figure."""
     import oracle
     from oracle.workload import oracle_twin_for
-    ow, pairs, nbytes = oracle_twin_for(w)
-    cores = min(os.cpu_count() or 1, len(pairs))
+    nproc = os.cpu_count() or 1
+    q1, tq1 = _oracle_quant_rate(w, quant_tokens, 1)
+    qn, tqn = _oracle_quant_rate(w, quant_tokens, nproc)
+    heads = [0, 1] if w.num_kv_heads > 1 else [0]
+    ow, pairs, nbytes = oracle_twin_for(w, heads=heads)
     q = ow.q(0)
+    unit_pairs = pairs[:w.g]
     t0 = time.perf_counter()
-    reps = 0
-    while True:
-        ow.P.decode(q[:1], [ow.rids[0]], w.softmax_scale, pairs=pairs, n_threads=cores)
-        reps += 1
-        if time.perf_counter() - t0 > seconds:
-            break
-    dt = time.perf_counter() - t0
-    return {"value": nbytes * reps / dt / 1e9, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"request 0 ({w.requests[0].n_prefill} tokens), all {w.num_q_heads} q heads, fp64 decode "
-                      f"x{reps} in {dt:.1f}s"}
+    ow.P.decode(q[:1], [ow.rids[0]], w.softmax_scale, pairs=unit_pairs, n_threads=1)
+    td1 = time.perf_counter() - t0
+    d1 = nbytes / len(heads) / td1 / 1e9
+    cores = min(nproc, len(pairs))
+    t0 = time.perf_counter()
+    ow.P.decode(q[:1], [ow.rids[0]], w.softmax_scale, pairs=pairs, n_threads=cores)
+    tdn = time.perf_counter() - t0
+    dn = nbytes / tdn / 1e9
+    ctx = w.requests[0].n_prefill
+    return {"value": dn, "unit": UNIT, "cores": cores, "kind": "oracle", "nproc": nproc,
+            "sample": f"request 0 of {w.name}: quantize-on-append of its first {quant_tokens} tokens x "
+                      f"{w.num_kv_heads} kv heads; fp64 decode of {len(heads)} kv-head unit(s) x {w.g} q heads "
+                      f"at its full {ctx}-token context",
+            "decode": {"single_thread_gbs": d1, "all_cores_gbs": dn, "threads": cores,
+                       "single_thread_s": td1, "all_cores_s": tdn, "units": len(heads)},
+            "quant": {"single_thread_gbs": q1, "all_cores_gbs": qn, "threads": nproc,
+                      "single_thread_s": tq1, "all_cores_s": tqn, "tokens_per_pool": quant_tokens,
+                      "unit": "GB/s of bf16 K/V in + page blocks out"}}
 
 
 def run_reference(args):
-    """Reference arm: the CPU oracle (the only reference this path has)."""
+    """Reference arm: the CPU oracle (the only reference this path has), as it
+    stands, on this host's cores.  A step decodes one (request 0, kv head)
+    unit at its full context: all g q heads on min(cores, g) OpenMP threads,
+    or one q head when K such steps would take more than about two minutes."""
     ws, rank, _ = dist_setup()
     if rank != 0:
         return 0
     import kvsynth
     from oracle.workload import oracle_twin_for
     w = kvsynth.make_workload(args.config)
-    ow, pairs, nbytes_all = oracle_twin_for(w)
     g = w.g
-    unit_bytes = nbytes_all / w.num_kv_heads          # one kv head of request 0 (+ q/out share)
-    cores = 1
+    ow, pairs, unit_bytes = oracle_twin_for(w, heads=[0])
+    nproc = os.cpu_count() or 1
+    cores = min(nproc, g)
     q = ow.q(0)
-    rng = np.random.default_rng(0)
+    t0 = time.perf_counter()
+    ow.P.decode(q[:1], [ow.rids[0]], w.softmax_scale, pairs=pairs, n_threads=cores)
+    t_unit = time.perf_counter() - t0
+    sample = pairs
+    if args.steps * t_unit > 120.0:
+        sample, cores = pairs[:1], 1
+    step_bytes = unit_bytes * len(sample) / len(pairs)
     for _ in range(args.warmup):
-        ow.P.decode(q[:1], [ow.rids[0]], w.softmax_scale, pairs=pairs[:1], n_threads=1)
+        ow.P.decode(q[:1], [ow.rids[0]], w.softmax_scale, pairs=sample, n_threads=cores)
     t0 = time.perf_counter()
     for s in range(args.steps):
-        p = pairs[rng.integers(0, len(pairs))][None]
-        ow.P.decode(q[:1], [ow.rids[0]], w.softmax_scale, pairs=p, n_threads=1)
+        ow.P.decode(q[:1], [ow.rids[0]], w.softmax_scale, pairs=sample, n_threads=cores)
     dt = time.perf_counter() - t0
-    value = unit_bytes * args.steps / dt / 1e9
+    value = step_bytes * args.steps / dt / 1e9
+    desc = (f"one (request 0, kv head 0) unit of {w.name} per step at its full {w.requests[0].n_prefill}-token "
+            f"context: {len(sample)} of its {g} q heads, fp64")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "sample": f"one (request 0, q head) pair per step, 1 of {g} heads "
-                                                     f"sharing a kv head; {w.requests[0].n_prefill} tokens"},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": "one q head of request 0 per step"},
+            "config": {"workload": w.name, "sample": desc},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc,
+                             "nproc": nproc},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
+
+
+def context_desc(w):
+    """Prefill context of the workload's requests: one length, or the range."""
+    n = [r.n_prefill for r in w.requests]
+    return n[0] if min(n) == max(n) else {"min": min(n), "max": max(n), "mean": float(np.mean(n))}
+
+
+def budget_desc(w):
+    """Average-bit budget B of the greedy allocator: one value, or the range over requests."""
+    b = [num / den for num, den in (r.budget for r in w.requests)]
+    return b[0] if min(b) == max(b) else {"min": min(b), "max": max(b), "mean": float(np.mean(b))}
+
+
+def int2_fraction(gw):
+    """Fraction of prefill tokens the allocator sent to INT2."""
+    n2 = sum(int((b[:r.n_prefill] == 2).sum()) for b, r in zip(gw.bits, gw.w.requests))
+    return n2 / max(1, sum(r.n_prefill for r in gw.w.requests))
 
 
 def run_prefill(args):
@@ -258,7 +349,12 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--config", type=int, default=3,
+                    help="workload 1..5 (default 3: batch 16, 64/8 heads, 100K tokens per request)")
+    ap.add_argument("--requests", type=int, default=0,
+                    help="run only the workload's first N requests (smaller cases for profiling)")
+    ap.add_argument("--q-heads", type=int, default=0,
+                    help="override the workload's number of query heads (GQA ratio = q heads / kv heads)")
     ap.add_argument("--decode-impl", default="auto", choices=["auto", "simt", "mma"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--segments", action="store_true",
@@ -288,11 +384,21 @@ def main():
     if ws > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
+    # clocks are sampled from here (workload build and warm-up included) to the
+    # end of the timed region, so that a short timed region still has samples
+    clk = ClockSampler(local).start()
     e2e_steps = max(args.steps // 4, 10)
     total_steps = args.warmup + args.steps + 3 + e2e_steps
     SEG_W = SEG_WS = 128   # HyQuant window W and staging capacity W_s
     extra = SEG_W if args.segments else 0   # the frozen window is quantized again by the first flush
-    w = kvsynth.make_workload(args.config, steps=total_steps)
+    w = kvsynth.make_workload(args.config, steps=total_steps, n_req=args.requests or None)
+    if args.requests:
+        w.name = f"{w.name}-first{args.requests}"
+    if args.q_heads:
+        if args.q_heads % w.num_kv_heads or not 1 <= args.q_heads // w.num_kv_heads <= 8:
+            raise SystemExit("--q-heads must be 1..8 times the workload's kv heads")
+        w.name = f"{w.name}-q{args.q_heads}"
+        w.num_q_heads = args.q_heads
     gw = GPUWorkload(w, device=local, steps=total_steps, extra_tokens=extra)
     gw.pool.set_decode_impl({"auto": 0, "simt": 1, "mma": 2}[args.decode_impl])
     gw.prefill()
@@ -384,27 +490,29 @@ def main():
     kv_first = gw.pool.last_decode_stats()["kv_bytes"] - (sum(n_vl) + B * seg["fill"]) * fp_row * args.segments
     seg["fp_tok"] = 0
     launches0 = gw.pool.launch_count()
-    # library-recorded events around the scan and merge of every 8th timed
-    # decode (an event between scan and merge stops the merge's launch from
-    # overlapping the scan's drain, so the other calls run without one)
-    gw.pool.decode_timing(True, every=8)
+    # library-recorded events around the scan and merge of the timed decodes:
+    # every call when the timed region is short, else every 8th (an event
+    # between scan and merge stops the merge's launch from overlapping the
+    # scan's drain, so the other calls run without one)
+    timing_every = 1 if args.steps < 200 else 8
+    gw.pool.decode_timing(True, every=timing_every)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
-        torch.cuda.synchronize()
-        torch.cuda.nvtx.range_push("timed")
-        start.record(stream)
-        if args.segments:
-            for i in range(args.steps):
-                seg_step(s0 + i)
-        else:
-            for i in range(args.steps):
-                s = s0 + i
-                gw.pool.append(ks[s], vs[s], rids, bits[s])
-                gw.pool.reorder(rids)
-                gw.pool.decode(qs[s], rids, w.softmax_scale, out=out)
-        end.record(stream)
-        torch.cuda.synchronize()
-        torch.cuda.nvtx.range_pop()
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("timed")
+    start.record(stream)
+    if args.segments:
+        for i in range(args.steps):
+            seg_step(s0 + i)
+    else:
+        for i in range(args.steps):
+            s = s0 + i
+            gw.pool.append(ks[s], vs[s], rids, bits[s])
+            gw.pool.reorder(rids)
+            gw.pool.decode(qs[s], rids, w.softmax_scale, out=out)
+    end.record(stream)
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
+    clk.stop()
     if dist:
         dist.barrier()
     kv_last = gw.pool.last_decode_stats()["kv_bytes"] - (sum(n_vl) + B * seg["fill"]) * fp_row * args.segments
@@ -454,7 +562,8 @@ def main():
             "vs_baseline": None, "dtype": "u4/u2 codes, f16 meta, f32 accum", "data": "synthetic",
             "config": {"workload": w.name + ("+fp-segments" if args.segments else "") +
                                    ("+ragged-heads" if args.ragged_heads else ""), "batch": B, "num_q_heads": Hq, "num_kv_heads": Hkv, "head_dim": 128,
-                       "context": w.requests[0].n_prefill, "page_tokens": 32, "budget_bits": "3.0",
+                       "context": context_desc(w), "page_tokens": 32, "budget_bits": budget_desc(w),
+                       "int2_token_fraction": int2_fraction(gw),
                        "decode_impl": args.decode_impl, "l2": "inputs larger than L2 (%.0f MB per step)"
                                                              % (step_bytes / 1e6),
                        "us_per_layer_step": t_ms / args.steps * 1e3, "decode_us": dec_ms * 1e3,
@@ -463,7 +572,8 @@ def main():
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic, "peak_source": peak_kind,
                          "kernel": "decode_mma_kernel (split scan); CUDA events recorded by the library on "
-                                   "the launch stream around every 8th launch of the timed region"},
+                                   "the launch stream around %s launch of the timed region"
+                                   % ("every" if timing_every == 1 else "every 8th")},
             "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches,
             **({"segments": {"vertical_lines": "5% of the non-window prefix per kv head (seeded synthetic score)",

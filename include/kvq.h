@@ -192,20 +192,41 @@ KVQ_API kv_status_t kv_decode_attn(kv_pool_t* pool, const void* q, const int32_t
  * cudaMalloc/cudaFree, which may synchronize the device, is not acceptable.
  * Same arguments, results and error rules as kv_decode_attn, except:
  *   - the split plan, the per-unit q operands and the split partials live in
- *     one fixed 64 MiB array inside
- *     the library (held on every GPU that loads it until the process exits)
- *     instead of pool buffers that grow with cudaMalloc;
- *   - batch x num_kv_heads must be <= 4096 and the plan must fit the array;
- *     otherwise KV_ERR_INVALID_ARG with a message, before any device work;
+ *     one fixed 64 MiB array inside the library (held on every GPU that loads
+ *     it until the process exits) instead of pool buffers that grow with
+ *     cudaMalloc; the call allocates nothing and frees nothing;
+ *   - batch x num_kv_heads must be <= 4096 and the plan must fit the array
+ *     (the worker count is lowered until it does); otherwise
+ *     KV_ERR_INVALID_ARG with a message, before any device work;
  *   - the first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress); make that first call before any stream capture;
- *   - every call shares the array: calls whose device work overlaps (other
- *     streams, other pools) race, so serialize them on one stream;
- *   - the pool's own stream ordering and kv_last_decode_stats are not updated:
- *     issue it on the stream that carries the pool's other work.
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture begins;
+ *   - each call copies its plan from pageable host memory with
+ *     cudaMemcpyAsync on `stream`;
+ *   - every call shares the array, which keeps the last call's contents;
+ *     nothing in it has to start at zero (each call copies its plan in, and
+ *     its scan writes every partial its merge reads); calls whose device work
+ *     overlaps (other streams, other pools) race, so serialize them;
+ *   - `stream` must be the stream that carries the pool's other work: this
+ *     call neither waits for work the pool issued on another stream nor makes
+ *     later pool calls wait for it, so on any other stream its ordering
+ *     against appends, reorders and evictions is undefined;
+ *   - kv_last_decode_stats and kv_decode_timing do not cover it.
  * The caller still provides q, out and the pool, as for kv_decode_attn. */
 KVQ_API kv_status_t kv_decode_attn_noalloc(kv_pool_t* pool, const void* q, const int32_t* req_ids, int32_t batch,
                                            int32_t num_q_heads, float softmax_scale, float* out, void* stream);
+
+/* Testing aid for the device-timeout path (off by default).  Every copy wait
+ * in the scans is bounded; first_wait_spins >= 0 makes the first copy wait of
+ * every warp of the tensor-core page scan and of the full-precision list scan
+ * give up after that many polls (0: at once) instead of the normal bound;
+ * -1 restores the normal bound.  A warp whose wait gives up records
+ * KV_ERR_DEVICE_TIMEOUT in the pool's status, still waits (with the normal
+ * bound) for every copy it issued, writes empty partials and exits, so the
+ * device stays usable: kv_pool_sync() then returns KV_ERR_DEVICE_TIMEOUT once
+ * and the decode's output is unspecified.  Values outside [-1, 2^32) are
+ * KV_ERR_INVALID_ARG. */
+KVQ_API kv_status_t kv_set_wait_limit(kv_pool_t* pool, int64_t first_wait_spins);
 
 /* Choose the decode implementation (kv_decode_impl_t). */
 KVQ_API kv_status_t kv_set_decode_impl(kv_pool_t* pool, int32_t impl);

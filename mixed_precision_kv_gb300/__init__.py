@@ -26,7 +26,7 @@ EXPORTED = ["kv_pool_create", "kv_pool_destroy", "kv_request_open", "kv_request_
             "kv_reorder_pages", "kv_evict_slots", "kv_decode_attn", "kv_set_decode_impl", "kv_pool_sync",
             "kv_request_info", "kv_export_request", "kv_last_decode_stats", "kv_pool_launch_count", "kv_alloc_bits",
             "kv_last_error", "kv_decode_attn_noalloc", "kv_decode_timing", "kv_evict_slots_head", "kv_fp_configure",
-            "kv_fp_append", "kv_fp_drop", "kv_fp_count"]
+            "kv_fp_append", "kv_fp_drop", "kv_fp_count", "kv_set_wait_limit"]
 
 _P = ctypes.c_void_p
 _I32, _I64 = ctypes.c_int32, ctypes.c_int64
@@ -72,6 +72,7 @@ def load_library(path: str = LIB_PATH):
             "kv_decode_attn": [_P, _P, _P, _I32, _I32, ctypes.c_float, _P, _P],
             "kv_decode_attn_noalloc": [_P, _P, _P, _I32, _I32, ctypes.c_float, _P, _P],
             "kv_set_decode_impl": [_P, _I32],
+            "kv_set_wait_limit": [_P, _I64],
             "kv_pool_sync": [_P],
             "kv_request_info": [_P, _I32, _P, _P],
             "kv_export_request": [_P, _I32, _P, _P, _P, _P, _P, _P, _P, _P],
@@ -195,9 +196,10 @@ class KVPool:
 
     def _check_kv(self, t, n):
         torch = _torch_mod()
-        if t.dtype is not torch.bfloat16 or not t.is_cuda or t.shape != (n, self.num_kv_heads, HEAD_DIM) or \
-                not t.is_contiguous():
-            raise ValueError(f"expected a contiguous CUDA bf16 tensor [{n}][{self.num_kv_heads}][128]")
+        if t.dtype is not torch.bfloat16 or not self._on_pool_device(t) or \
+                t.shape != (n, self.num_kv_heads, HEAD_DIM) or not t.is_contiguous():
+            raise ValueError(f"expected a contiguous bf16 tensor [{n}][{self.num_kv_heads}][128] on the pool's "
+                             f"device")
 
     def reorder(self, req_ids, stream=None):
         req_ids = _np(req_ids, np.int32)
@@ -249,18 +251,23 @@ class KVPool:
         _check(load_library().kv_fp_count(self._h, int(rid), ctypes.byref(n)), "kv_fp_count")
         return int(n.value)
 
+    def _on_pool_device(self, t):
+        return t.is_cuda and t.device.index == self.device
+
     def decode(self, q, req_ids, softmax_scale, out=None, stream=None):
-        """q: torch bf16 CUDA [B][Hq][128] -> out fp32 [B][Hq][128]."""
+        """q: torch bf16 CUDA [B][Hq][128] -> out fp32 [B][Hq][128], both on the pool's device."""
         torch = _torch_mod()
         req_ids = _np(req_ids, np.int32)
         B, Hq, D = q.shape
-        if q.dtype is not torch.bfloat16 or not q.is_cuda or D != HEAD_DIM or B != req_ids.size or \
+        if q.dtype is not torch.bfloat16 or not self._on_pool_device(q) or D != HEAD_DIM or B != req_ids.size or \
                 not q.is_contiguous():
-            raise ValueError("q must be a contiguous CUDA bf16 tensor [B][Hq][128] with B == len(req_ids)")
+            raise ValueError("q must be a contiguous bf16 tensor [B][Hq][128] on the pool's device with "
+                             "B == len(req_ids)")
         if out is None:
             out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
-        elif out.dtype is not torch.float32 or out.shape != q.shape or not out.is_cuda or not out.is_contiguous():
-            raise ValueError("out must be a contiguous fp32 CUDA tensor shaped like q")
+        elif out.dtype is not torch.float32 or out.shape != q.shape or not self._on_pool_device(out) or \
+                not out.is_contiguous():
+            raise ValueError("out must be a contiguous fp32 tensor shaped like q on the pool's device")
         rc = self._L.kv_decode_attn(self._h, q.data_ptr(), req_ids.ctypes.data, B, Hq, softmax_scale,
                                     out.data_ptr(), _stream(stream, self.device))
         if rc:
@@ -269,18 +276,27 @@ class KVPool:
 
     def decode_noalloc(self, q, req_ids, softmax_scale, out, stream=None):
         """kv_decode_attn_noalloc: like decode(), but the library allocates no device
-        memory (fixed internal scratch); the caller passes a preallocated `out`."""
-        import torch
+        memory (fixed internal scratch); the caller passes a preallocated `out`.
+        Issue it on the stream that carries the pool's other work."""
+        torch = _torch_mod()
         req_ids = _np(req_ids, np.int32)
         B, Hq, D = q.shape
-        if q.dtype != torch.bfloat16 or not q.is_cuda or not q.is_contiguous() or D != HEAD_DIM or B != req_ids.size:
-            raise ValueError("q must be a contiguous CUDA bf16 tensor [B][Hq][128] with B == len(req_ids)")
-        if out.dtype != torch.float32 or not out.is_contiguous() or tuple(out.shape) != (B, Hq, D):
-            raise ValueError("out must be a contiguous fp32 tensor shaped like q")
+        if q.dtype is not torch.bfloat16 or not self._on_pool_device(q) or not q.is_contiguous() or \
+                D != HEAD_DIM or B != req_ids.size:
+            raise ValueError("q must be a contiguous bf16 tensor [B][Hq][128] on the pool's device with "
+                             "B == len(req_ids)")
+        if out.dtype is not torch.float32 or not self._on_pool_device(out) or not out.is_contiguous() or \
+                tuple(out.shape) != (B, Hq, D):
+            raise ValueError("out must be a contiguous fp32 tensor shaped like q on the pool's device")
         _check(load_library().kv_decode_attn_noalloc(self._h, ctypes.c_void_p(q.data_ptr()), _ptr(req_ids), B, Hq,
                                                      float(softmax_scale), ctypes.c_void_p(out.data_ptr()),
                                                      _stream(stream, self.device)), "kv_decode_attn_noalloc")
         return out
+
+    def set_wait_limit(self, first_wait_spins):
+        """kv_set_wait_limit: bound of the scans' first copy wait (testing the timeout
+        path); -1 restores the normal bound."""
+        _check(load_library().kv_set_wait_limit(self._h, int(first_wait_spins)), "kv_set_wait_limit")
 
     def set_decode_impl(self, impl):
         _check(load_library().kv_set_decode_impl(self._h, int(impl)), "kv_set_decode_impl")

@@ -200,8 +200,8 @@ __device__ __forceinline__ bool bar_try(unsigned long long* b, uint32_t phase) {
       : "=r"(ok) : "r"(su32(b)), "r"(phase) : "memory");
   return ok != 0;
 }
-__device__ __forceinline__ bool bar_wait(unsigned long long* b, uint32_t phase) {
-  for (uint32_t it = 0; it < kSpinLimit; ++it)
+__device__ __forceinline__ bool bar_wait(unsigned long long* b, uint32_t phase, uint32_t limit = kSpinLimit) {
+  for (uint32_t it = 0; it < limit; ++it)
     if (bar_try(b, phase)) return true;
   return false;
 }
@@ -741,7 +741,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(
     const Entry* __restrict__ table, const UnitFrag* __restrict__ frags, const Split* __restrict__ splits,
     const int32_t* __restrict__ wsplit, int n_workers, const int32_t* __restrict__ ntab,
     const uint32_t* __restrict__ hdead, float* __restrict__ part, const uint32_t* __restrict__ smax_bits,
-    uint32_t* __restrict__ status) {
+    uint32_t* __restrict__ status, uint32_t first_spins) {
   constexpr bool kPair = Cols<G>::kPair;
   constexpr int NH = Cols<G>::NH;
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -969,7 +969,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(
       begin_split(sg);
     }
     const uint32_t st = c & (kStages - 1);
-    const bool got = bar_wait(&WS.bar[st], (c >> 1) & 1u);
+    // the first wait's bound is kSpinLimit unless a test shortens it
+    const bool got = bar_wait(&WS.bar[st], (c >> 1) & 1u, c == 0 ? first_spins : kSpinLimit);
     if (!__all_sync(0xFFFFFFFFu, got)) {
       ok = false;
       break;
@@ -1048,7 +1049,8 @@ cudaError_t launch_mma_g(kv_pool* P, const void* q, int32_t hq, float scale_log2
   return launch_pdl(kernel, dim3(grid), dim3(kThreads), (size_t)kScanSmem, s, (const uint8_t*)P->d_pool,
                     P->int4_offset, (int64_t)P->cfg.n_int2_pages, P->cfg.num_kv_heads, P->cfg.max_pages_per_request,
                     (const Entry*)P->d_table, (const UnitFrag*)d_frags, d_splits, d_wsplit, n_workers,
-                    (const int32_t*)P->d_ntab, (const uint32_t*)P->d_hdead, d_part, smax, P->d_status);
+                    (const int32_t*)P->d_ntab, (const uint32_t*)P->d_hdead, d_part, smax, P->d_status,
+                    P->first_wait_spins < 0 ? kSpinLimit : (uint32_t)P->first_wait_spins);
 }
 
 template <int G>

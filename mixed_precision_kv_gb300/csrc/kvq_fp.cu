@@ -84,8 +84,8 @@ __device__ __forceinline__ void fbulk(void* dst, const void* src, uint32_t bytes
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                ::"r"(sa(dst)), "l"(src), "r"(bytes), "r"(sa(b)) : "memory");
 }
-__device__ __forceinline__ bool fbar_wait(unsigned long long* b, uint32_t phase) {
-  for (uint32_t it = 0; it < kFpSpinLimit; ++it) {
+__device__ __forceinline__ bool fbar_wait(unsigned long long* b, uint32_t phase, uint32_t limit = kFpSpinLimit) {
+  for (uint32_t it = 0; it < limit; ++it) {
     uint32_t ok;
     asm volatile(
         "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
@@ -109,7 +109,7 @@ __device__ __forceinline__ void fp_segment_warp(uint8_t* smem, const uint16_t* _
                                                 int n_fpw, int first_split, const uint16_t* __restrict__ fpk,
                                                 const uint16_t* __restrict__ fpv, int fp_cap, int hkv,
                                                 const int32_t* __restrict__ nfp, float* __restrict__ part,
-                                                uint32_t* __restrict__ status) {
+                                                uint32_t* __restrict__ status, uint32_t first_spins) {
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gw = blockIdx.x * kFpWarps + w;
   if (gw >= n_fpw) return;   // warps are independent: no block barrier below
@@ -200,7 +200,8 @@ __device__ __forceinline__ void fp_segment_warp(uint8_t* smem, const uint16_t* _
     while (cur.split == sidx) {
       const int st = (int)(n_chunk % kFpStages);
       const uint32_t ph = (n_chunk / kFpStages) & 1u;
-      if (!__all_sync(0xFFFFFFFFu, fbar_wait(&S.bar[st][0], ph))) {
+      // the first wait's bound is kFpSpinLimit unless a test shortens it
+      if (!__all_sync(0xFFFFFFFFu, fbar_wait(&S.bar[st][0], ph, n_chunk == 0 ? first_spins : kFpSpinLimit))) {
         ok = false;
         break;
       }
@@ -331,11 +332,12 @@ __global__ void __launch_bounds__(kFpWarps * 32, 1)
     fp_segment_kernel(const uint16_t* __restrict__ q, int hq, float scale_log2, const Unit* __restrict__ units,
                       const Split* __restrict__ fsplits, const int32_t* __restrict__ fpw, int n_fpw, int first_split,
                       const uint16_t* __restrict__ fpk, const uint16_t* __restrict__ fpv, int fp_cap, int hkv,
-                      const int32_t* __restrict__ nfp, float* __restrict__ part, uint32_t* __restrict__ status) {
+                      const int32_t* __restrict__ nfp, float* __restrict__ part, uint32_t* __restrict__ status,
+                      uint32_t first_spins) {
   extern __shared__ __align__(128) uint8_t smem[];
   asm volatile("griddepcontrol.launch_dependents;");   // the merge may be staged
   fp_segment_warp<G>(smem, q, hq, scale_log2, units, fsplits, fpw, n_fpw, first_split, fpk, fpv, fp_cap, hkv, nfp,
-                     part, status);
+                     part, status, first_spins);
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
@@ -419,7 +421,8 @@ cudaError_t launch_fp_g(kv_pool* P, const uint16_t* q, int32_t hq, float scale_l
   const dim3 grid((unsigned)((n_fpw + kFpWarps - 1) / kFpWarps)), block(kFpWarps * 32);
   return launch_pdl(fp_segment_kernel<G>, grid, block, kFpSmem, s, q, hq, scale_log2, d_units, d_fsplits, d_fpw,
                     n_fpw, first_split, (const uint16_t*)P->d_fpk, (const uint16_t*)P->d_fpv, P->fp_cap,
-                    P->cfg.num_kv_heads, (const int32_t*)P->d_nfp, d_part, P->d_status);
+                    P->cfg.num_kv_heads, (const int32_t*)P->d_nfp, d_part, P->d_status,
+                    P->first_wait_spins < 0 ? kFpSpinLimit : (uint32_t)P->first_wait_spins);
 }
 
 }  // namespace

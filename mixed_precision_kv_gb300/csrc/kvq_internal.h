@@ -295,6 +295,7 @@ struct kv_pool {
   int64_t timed_calls = 0;            // decode calls recorded since timing started
   std::vector<cudaEvent_t> tev;       // ring of [before scan, after scan, after merge] per call
   cudaEvent_t merge_event = nullptr;  // recorded by the launchers between scan and merge when timing
+  int64_t first_wait_spins = -1;      // kv_set_wait_limit: bound of the scans' first copy wait (-1: normal)
 };
 
 namespace kvq {

@@ -529,6 +529,14 @@ kv_status_t kv_set_decode_impl(kv_pool_t* P, int32_t impl) {
   return KV_OK;
 }
 
+kv_status_t kv_set_wait_limit(kv_pool_t* P, int64_t first_wait_spins) {
+  if (!P) return fail(KV_ERR_INVALID_ARG, "kv_set_wait_limit: null pool");
+  if (first_wait_spins < -1 || first_wait_spins > (int64_t)UINT32_MAX)
+    return fail(KV_ERR_INVALID_ARG, "kv_set_wait_limit: first_wait_spins must be -1 or in [0, 2^32)");
+  P->first_wait_spins = first_wait_spins;
+  return KV_OK;
+}
+
 kv_status_t kv_pool_sync(kv_pool_t* P) {
   if (!P) return fail(KV_ERR_INVALID_ARG, "kv_pool_sync: null pool");
   DeviceGuard dg(P->cfg.device);

@@ -1,5 +1,5 @@
-"""Oracle pool for one request of a kvsynth workload (test infrastructure:
-used by the benchmark's CPU-baseline leg and its reference arm)."""
+"""Oracle pools for samples of a kvsynth workload (test infrastructure: used
+by the benchmark's CPU-baseline leg and its reference arm)."""
 from __future__ import annotations
 
 import numpy as np
@@ -19,32 +19,50 @@ class OracleRequest:
                                       kvsynth.TENSOR_Q, step)
 
 
-def oracle_twin_for(w, r=0, chunk=16384):
-    """Build request r of workload w in an oracle pool (all kv heads), reorder
-    it, and return (handle, (b=0, q head) pairs, algorithmic decode bytes)."""
+def request_bits(w, r):
+    """Bit width of every prefill position of request r (greedy allocation over its tags)."""
     spec = w.requests[r]
     b = alloc_bits(tag_counts(spec.tags[:spec.n_prefill]), w.D2, w.D4, spec.budget)
-    bits = b[spec.tags[:spec.n_prefill]].astype(np.uint8)
-    n = spec.n_prefill
+    return b[spec.tags[:spec.n_prefill]].astype(np.uint8)
+
+
+def kv_rows(w, r, tok0, n, heads):
+    """bf16 K and V rows [n][len(heads)][128] of request r from position tok0."""
+    spec = w.requests[r]
+    rm = None if spec.row_mult is None else spec.row_mult[tok0:tok0 + n]
+    k = kvsynth.fill_bf16_host_heads(n, w.num_kv_heads, 128, w.seed, kvsynth.TENSOR_K, spec.stream, heads,
+                                     tok0=tok0, chan_mult=w.k_chan_mult, row_mult=rm)
+    v = kvsynth.fill_bf16_host_heads(n, w.num_kv_heads, 128, w.seed, kvsynth.TENSOR_V, spec.stream, heads,
+                                     tok0=tok0, row_mult=rm)
+    return k, v
+
+
+def oracle_twin_for(w, r=0, chunk=16384, heads=None, n_tok=None):
+    """Build request r of workload w in an oracle pool (the listed kv heads,
+    all by default; its first n_tok prefill tokens, all by default), reorder
+    it, and return (handle, (b=0, q head) pairs of the listed kv heads,
+    algorithmic decode bytes of those units)."""
+    spec = w.requests[r]
+    bits = request_bits(w, r)
+    n = spec.n_prefill if n_tok is None else min(n_tok, spec.n_prefill)
     H = w.num_kv_heads
-    n2 = int((bits == 2).sum()) // 32 + 2
-    n4 = -(-int((bits == 4).sum()) // 32) + chunk // 32 + 4
-    P = OraclePool(H, n2, n4, 1, n2 + n4)
+    heads = list(range(H)) if heads is None else list(heads)
+    n2 = int((bits[:n] == 2).sum()) // 32 + 2
+    n4 = -(-int((bits[:n] == 4).sum()) // 32) + chunk // 32 + 4
+    P = OraclePool(H, n2, n4, 1, n2 + n4, sel_heads=heads)
     rid = P.open()
     for t0 in range(0, n, chunk):
         m = min(chunk, n - t0)
-        rm = None if spec.row_mult is None else spec.row_mult[t0:t0 + m]
-        k = kvsynth.fill_bf16_host(m, H, 128, w.seed, kvsynth.TENSOR_K, spec.stream, t0, chan_mult=w.k_chan_mult,
-                                   row_mult=rm)
-        v = kvsynth.fill_bf16_host(m, H, 128, w.seed, kvsynth.TENSOR_V, spec.stream, t0, row_mult=rm)
+        k, v = kv_rows(w, r, t0, m, heads)
         assert P.append(np.full(m, rid), bits[t0:t0 + m], k, v) == OK
     if spec.evict.size:
-        assert P.evict(np.full(spec.evict.size, rid), spec.evict) == OK
+        ev = spec.evict[spec.evict < n]
+        assert P.evict(np.full(ev.size, rid), ev) == OK
     assert P.reorder([rid]) == OK
     ex = P.export(rid, content=False)
     nbytes = 0
     for is2, f in zip(ex["is_int2"], ex["fill"]):
-        nbytes += (3072 if is2 else 160 * int(f)) * H + 8
-    nbytes += w.num_q_heads * 128 * 6
-    pairs = np.array([(0, h) for h in range(w.num_q_heads)], np.int32)
+        nbytes += (3072 if is2 else 160 * int(f)) * len(heads) + 8
+    nbytes += len(heads) * w.g * 128 * 6
+    pairs = np.array([(0, h * w.g + j) for h in heads for j in range(w.g)], np.int32)
     return OracleRequest(P, rid, w), pairs, nbytes

@@ -201,3 +201,62 @@ def test_config2_full_size_segments_and_budgets(kvq):
     got = np.stack([out[b, h] for b, h in pairs])
     assert np.isfinite(got).all()
     assert_outputs_close(got, ref, "config 2 full size, budgets + segments, sampled")
+
+
+def test_config5_full_size_every_step(kvq):
+    """The serving loop at its stated size: 256 requests with contexts
+    U[4K, 64K], 64 steps of append (one token per request into the INT4 tail
+    or staging page) -> repack of every staging page that reaches 32 tokens ->
+    INT2-first reorder -> decode.  Every step: all 256 page tables (ids,
+    precision, fill, live masks) bit-exact against the oracle, which keeps
+    codes only for the sampled requests and kv heads.  At steps 0, 31 and 63,
+    at the first step after a repack in a sampled request, and every 8th step:
+    codes and binary16 scale/zero of 4 sampled requests x 2 kv heads, and
+    their outputs within max-abs 1e-3 / relative-L2 1e-4 of the fp64 oracle."""
+    w = kvsynth.make_workload(5)
+    assert len(w.requests) == 256 and w.steps == 64
+    rng = np.random.default_rng(55)
+    # two requests whose staging page fills during the 64 steps (INT2 tokens
+    # wait in it, 32 at a time), two drawn at random
+    from harness import oracle_bits
+    fills = []
+    for r, spec in enumerate(w.requests):
+        b = oracle_bits(w, r)
+        n = spec.n_prefill
+        fills.append(int((b[:n] == 2).sum()) % 32 + int((b[n:n + w.steps] == 2).sum()) >= 32)
+    repacking = [r for r in range(len(w.requests)) if fills[r]]
+    reqs = rng.choice(repacking, 2, replace=False).tolist()
+    rest = [r for r in range(len(w.requests)) if r not in reqs]
+    reqs = sorted(reqs + rng.choice(rest, 2, replace=False).tolist())
+    heads = sorted(rng.choice(w.num_kv_heads, 2, replace=False).tolist())
+    pairs = np.array([(b, h * w.g + j) for b in reqs for h in heads for j in range(w.g)], np.int32)
+    gw, ow = _pair(w, chunk=16384, sel_heads=heads, content_reqs=reqs)
+    _build(gw, ow)
+    _check_all(gw, ow, content=False)
+
+    def n_int2(r):
+        return int(gw.pool.export(gw.rids[r], content=False)["is_int2"].sum())
+
+    int2_before = {r: n_int2(r) for r in reqs}
+    repack_seen = False
+    checked, repacks = [], 0
+    for step in range(w.steps):
+        k, v, rids, bits = gw.step_inputs()
+        gw.append_step(k, v, rids, bits)
+        ow.append_step()
+        gw.reorder()
+        ow.reorder()
+        _check_all(gw, ow, content=False)                     # all 256 tables, every step
+        repacks += int((bits == 2).sum())
+        after = {r: n_int2(r) for r in reqs}
+        first_repack = not repack_seen and any(after[r] > int2_before[r] for r in reqs)
+        repack_seen = repack_seen or first_repack
+        if step in (0, 31, 63) or first_repack or step % 8 == 7:
+            _check_all(gw, ow, reqs=reqs, content=True)
+            _decode_check(gw, ow, step, pairs=pairs, what=f"config 5 full size, step {step}")
+            checked.append(step)
+        else:
+            gw.decode(gw.q(step))
+    gw.pool.sync()
+    assert repack_seen, "no sampled request repacked a staging page in 64 steps"
+    assert {0, 31, 63} <= set(checked)
