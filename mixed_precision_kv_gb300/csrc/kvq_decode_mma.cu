@@ -123,6 +123,13 @@ __device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
   asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
   return d;
 }
+// -x for both binary16 halves (an fp16 negation, which ptxas can fold into
+// the operand of the instruction that consumes it)
+__device__ __forceinline__ uint32_t hneg2(uint32_t x) {
+  uint32_t d;
+  asm("neg.f16x2 %0, %1;" : "=r"(d) : "r"(x));
+  return d;
+}
 // pack two floats as binary16 (round to nearest even): lo -> bits 0..15
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
   uint32_t d;
@@ -339,11 +346,11 @@ __device__ __forceinline__ void qk_int2(const uint8_t* blk, const UnitFrag* __re
       u1 = hfma2(q1, s1, hmul2(n1, s1));
       b0 = b1 = 0u;
     } else {
-      // lo = fma(q, s, -hi), with -hi = rn(-q s) by sign symmetry
+      // lo = fma(q, s, -hi)
       b0 = hmul2(q0, s0);
       b1 = hmul2(q1, s1);
-      u0 = hfma2(q0, s0, b0 ^ 0x80008000u);
-      u1 = hfma2(q1, s1, b1 ^ 0x80008000u);
+      u0 = hfma2(q0, s0, hneg2(b0));
+      u1 = hfma2(q1, s1, hneg2(b1));
     }
 #pragma unroll
     for (int m = 0; m < 2; ++m) {
@@ -507,10 +514,11 @@ __device__ __forceinline__ void softmax_pv(const uint8_t* blk, uint32_t live, fl
     sub2(pav[k], pbv[k], h_lo(ph[k]), h_hi(ph[k]), ra, rb);
     pl[k] = pack_h2(ra, rb);
   }
-  // V zero term: rows = groups (lanes r < 4), k = slots
+  // V zero term: rows = groups (lanes r < 4), k = slots.  Lanes r >= 4 load
+  // group r - 4 as well (no branch): their rows 4..7 of the product are
+  // finite and never read (only lanes r < 4 store the zero terms).
   {
-    uint4 zz = make_uint4(0u, 0u, 0u, 0u);
-    if (r < 4) zz = *reinterpret_cast<const uint4*>(blk + vmeta + 256 + 64 * r + 16 * i);
+    uint4 zz = *reinterpret_cast<const uint4*>(blk + vmeta + 256 + 64 * (r & 3) + 16 * i);
     if (kInt2) {   // undo the 2^-2 of the even slots' P: words 0 and 2 hold slot pairs (8i, 8i+4), (8i+2, 8i+6)
       zz.x = hmul2(zz.x, 0x44004400u);
       zz.z = hmul2(zz.z, 0x44004400u);
@@ -528,17 +536,19 @@ __device__ __forceinline__ void softmax_pv(const uint8_t* blk, uint32_t live, fl
     add2(zv[0], zv[1], zt[0], zt[1]);
     add2(zv[2], zv[3], zt[2], zt[3]);
   }
-  // Fold operands: u = fma(p_hi, s, rn(x3 * s)) with x3 = -p_hi where the lo
-  // part is wanted (else 0), then lo = rn(p_lo s + u):
-  //   g <= 4, hi columns: x3 = x1 = 0 -> B = rn(p_hi s);
-  //   lo columns (and the lo pass of g > 4): x3 = -p_hi, x1 = p_lo ->
-  //   B = rn(p_lo s + (p_hi s - rn(p_hi s))).
-  const uint32_t lomask = (!kPair || lo_col) ? 0xFFFFFFFFu : 0u;
+  // Fold operands, hi = rn(p_hi s) and lo = rn(p_lo s + (p_hi s - hi)) (the
+  // bracket is exact: the rounding error of an fp16 product).  g <= 4: one
+  // B per lane, u = fma(p_hi, s, rn(x3 s)) with x3 = -p_hi in the lo columns
+  // and 0 in the hi columns, then B = rn(x1 s + u) with x1 = p_lo or 0;
+  // g > 4: hi and lo both, lo from -hi directly.
   uint32_t x3[4], x1[4];
+  if constexpr (kPair) {
+    const uint32_t lomask = lo_col ? 0xFFFFFFFFu : 0u;
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    x3[k] = (ph[k] ^ 0x80008000u) & lomask;
-    x1[k] = pl[k] & lomask;
+    for (int k = 0; k < 4; ++k) {
+      x3[k] = (ph[k] ^ 0x80008000u) & lomask;   // -p_hi or 0 (one logic op)
+      x1[k] = pl[k] & lomask;
+    }
   }
 #pragma unroll
   for (int gr = 0; gr < 4; ++gr) {
@@ -547,12 +557,11 @@ __device__ __forceinline__ void softmax_pv(const uint8_t* blk, uint32_t live, fl
     uint32_t bh[4], bl[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const uint32_t u = hfma2(ph[k], sk[k], hmul2(x3[k], sk[k]));
       if constexpr (kPair) {
-        bh[k] = hfma2(x1[k], sk[k], u);
+        bh[k] = hfma2(x1[k], sk[k], hfma2(ph[k], sk[k], hmul2(x3[k], sk[k])));
       } else {
         bh[k] = hmul2(ph[k], sk[k]);
-        bl[k] = hfma2(x1[k], sk[k], u);
+        bl[k] = hfma2(pl[k], sk[k], hfma2(ph[k], sk[k], hneg2(bh[k])));
       }
     }
     uint32_t wv[4];
