@@ -53,7 +53,7 @@ class ClockSampler:
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
          "clocks_event_reasons.sw_power_cap,utilization.gpu")
 
-    def __init__(self, gpu_index, period_ms=50):
+    def __init__(self, gpu_index, period_ms=20):
         self.gpu = gpu_index
         self.period = period_ms
         self.proc = None
@@ -141,9 +141,10 @@ TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "decode_mma_traffic.json")
 
 
 def recorded_traffic(step_bytes, workload, decode_impl):
-    """DRAM bytes per scan launch from the committed ncu capture, scaled from the
-    captured launch's algorithmic bytes to this run's mean step bytes; None when
-    the kernel sources changed since the capture or the run differs from it."""
+    """DRAM bytes per scan launch from the committed ncu capture of this
+    workload, scaled from the captured launch's algorithmic bytes to this
+    run's mean step bytes; None when the kernel sources changed since the
+    capture or no capture covers the run."""
     import hashlib
     try:
         with open(TRAFFIC_RECORD) as f:
@@ -154,10 +155,12 @@ def recorded_traffic(step_bytes, workload, decode_impl):
                 h.update(f.read())
     except Exception:
         return None
-    if h.hexdigest() != rec["sources_sha256"] or rec["workload"] != workload or decode_impl == "simt":
+    if h.hexdigest() != rec["sources_sha256"] or decode_impl == "simt":
         return None
-    traffic = rec["dram_bytes_read"] + rec["dram_bytes_write"]
-    return traffic / rec["algorithmic_bytes"] * step_bytes
+    for r in rec["records"]:
+        if r["applies_to"] == workload:
+            return (r["dram_bytes_read"] + r["dram_bytes_write"]) / r["algorithmic_bytes"] * step_bytes
+    return None
 
 
 def _oracle_quant_rate(w, n_tok, threads):
@@ -487,7 +490,8 @@ def main():
     # the timed steps (a step adds one token per request, so bytes grow
     # linearly and the mean of the two ends is the mean step)
     fp_row = Hkv * 128 * 2 * 2   # bf16 K and V of one list token, all kv heads
-    kv_first = gw.pool.last_decode_stats()["kv_bytes"] - (sum(n_vl) + B * seg["fill"]) * fp_row * args.segments
+    kv_raw_first = gw.pool.last_decode_stats()["kv_bytes"]   # the last warm-up decode's algorithmic bytes
+    kv_first = kv_raw_first - (sum(n_vl) + B * seg["fill"]) * fp_row * args.segments
     seg["fp_tok"] = 0
     launches0 = gw.pool.launch_count()
     # library-recorded events around the scan and merge of the timed decodes:
@@ -568,6 +572,7 @@ def main():
                                                              % (step_bytes / 1e6),
                        "us_per_layer_step": t_ms / args.steps * 1e3, "decode_us": dec_ms * 1e3,
                        "scan_us": scan_ms * 1e3, "decode_calls_timed": n_timed,
+                       "kv_bytes_last_warmup_decode": kv_raw_first,
                        "pct_of_8000_gbs": value / ws / 8000 * 100},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic, "peak_source": peak_kind,
