@@ -330,6 +330,12 @@ cudaError_t launch_repack(kv_pool* P, const RepackJob* d_jobs, int n_jobs, cudaS
 cudaError_t launch_direct_int2(kv_pool* P, const void* k, const void* v, const DirectJob* d_jobs, int n_jobs,
                                const int32_t* d_toks, cudaStream_t s);
 cudaError_t launch_scatter(kv_pool* P, const TableUpd* d_upd, int n, cudaStream_t s);
+// Bulk forms (a warp per 32-channel group, a lane per token; K/V rows 16-byte
+// aligned): fresh INT4 pages of 32 tokens, and direct INT2 groups.
+cudaError_t launch_bulk_int4(kv_pool* P, const void* k, const void* v, const AppendJob* d_jobs, int n_jobs,
+                             const int32_t* d_toks, cudaStream_t s);
+cudaError_t launch_bulk_int2(kv_pool* P, const void* k, const void* v, const DirectJob* d_jobs, int n_jobs,
+                             const int32_t* d_toks, cudaStream_t s);
 
 // Balanced decode plan: units (batch row, kv head) in order, their pages cut
 // into n_workers contiguous ranges of about equal cost (at least min_pages

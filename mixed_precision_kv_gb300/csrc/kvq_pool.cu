@@ -959,6 +959,15 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
   upd.insert(upd.end(), hupd.begin(), hupd.end());
 
   const bool small = jobs.size() <= (size_t)SmallAppend::kMaxJobs && off <= SmallAppend::kMaxToks;
+  // Large calls with 16-byte aligned K/V rows: fresh pages filled with 32
+  // tokens go to the bulk INT4 kernel, direct groups to the bulk INT2 kernel.
+  const bool aligned = ((uintptr_t)k % 16 == 0) && ((uintptr_t)v % 16 == 0);
+  const bool use_bulk = !small && aligned;
+  size_t n_full = 0;
+  if (use_bulk) {
+    std::stable_partition(jobs.begin(), jobs.end(), [](const AppendJob& j) { return !(j.first_slot == 0 && j.n_slots == kPage); });
+    for (const auto& j : jobs) n_full += (j.first_slot == 0 && j.n_slots == kPage) ? 1 : 0;
+  }
   Upload u;
   const size_t o_jobs = small ? 0 : u.add(jobs.data(), jobs.size() * sizeof(AppendJob));
   const size_t o_toks = small ? 0 : u.add(toks.data(), toks.size() * sizeof(int32_t));
@@ -975,11 +984,19 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
     std::copy(toks.begin(), toks.end(), sa.toks);
     KV_CUDA(launch_append(P, k, v, nullptr, (int)jobs.size(), nullptr, &sa, s));
   } else {
-    KV_CUDA(launch_append(P, k, v, (const AppendJob*)(base + o_jobs), (int)jobs.size(), (const int32_t*)(base + o_toks),
+    const int n_part = (int)(jobs.size() - n_full);
+    KV_CUDA(launch_append(P, k, v, (const AppendJob*)(base + o_jobs), n_part, (const int32_t*)(base + o_toks),
                           nullptr, s));
+    if (n_full)
+      KV_CUDA(launch_bulk_int4(P, k, v, (const AppendJob*)(base + o_jobs) + n_part, (int)n_full,
+                               (const int32_t*)(base + o_toks), s));
   }
-  KV_CUDA(launch_direct_int2(P, k, v, (const DirectJob*)(base + o_dir), (int)directs.size(),
+  if (use_bulk)
+    KV_CUDA(launch_bulk_int2(P, k, v, (const DirectJob*)(base + o_dir), (int)directs.size(),
                              (const int32_t*)(base + o_dtok), s));
+  else
+    KV_CUDA(launch_direct_int2(P, k, v, (const DirectJob*)(base + o_dir), (int)directs.size(),
+                               (const int32_t*)(base + o_dtok), s));
   KV_CUDA(launch_repack(P, (const RepackJob*)(base + o_rep), (int)repacks.size(), s));
   KV_CUDA(launch_scatter(P, (const TableUpd*)(base + o_upd), (int)upd.size(), s));
   return KV_OK;

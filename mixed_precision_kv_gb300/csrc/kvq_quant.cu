@@ -390,6 +390,352 @@ __global__ void __launch_bounds__(kThreads) direct_int2_kernel(
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// ---- bulk kernels: a CTA of 4 warps per (page, kv head), warp gr = the
+// 32-channel group gr, lane t = slot t (its token's 32 channels of the group
+// held in registers).  A token's group is quantized without any cross-lane
+// step; INT4 metadata comes from packed bf16 min/max, per-channel INT2 K
+// statistics from warp reductions across the 32 tokens.  The arithmetic of
+// every code, scale and zero is the one qcode_fast / make_meta apply (same
+// operations, same order), so the results are bit-identical.
+constexpr int kBulkThreads = 128;
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ uint32_t bf2_min(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("min.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t bf2_max(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ float redux_min(float x) {
+  float d;
+  asm volatile("redux.sync.min.f32 %0, %1, 0xffffffff;" : "=f"(d) : "f"(x));
+  return d;
+}
+__device__ __forceinline__ float redux_max(float x) {
+  float d;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(d) : "f"(x));
+  return d;
+}
+
+// The 32 bf16 channels 32gr .. 32gr + 31 of token T, kv head h (16 words).
+__device__ __forceinline__ void load_group(const __nv_bfloat16* __restrict__ src, int T, int h, int hkv, int gr,
+                                           uint32_t (&w)[16]) {
+  const uint4* p = reinterpret_cast<const uint4*>(src + ((size_t)T * hkv + h) * kHeadDim + 32 * gr);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4 v = __ldg(p + q);
+    w[4 * q] = v.x; w[4 * q + 1] = v.y; w[4 * q + 2] = v.z; w[4 * q + 3] = v.w;
+  }
+}
+
+// Group metadata of 32 bf16 values (INT4): min / max exactly, NaN carried so
+// that the range check sees it (NaN, Inf or |x| > 65504 sets `bad`).
+__device__ __forceinline__ GroupMeta meta_i4(const uint32_t (&w)[16], bool& bad) {
+  uint32_t mn2 = w[0], mx2 = w[0];
+#pragma unroll
+  for (int j = 1; j < 16; ++j) {
+    mn2 = bf2_min(mn2, w[j]);
+    mx2 = bf2_max(mx2, w[j]);
+  }
+  const float a = bf_lo(mn2), b = bf_hi(mn2), c = bf_lo(mx2), d = bf_hi(mx2);
+  bad |= out_of_range(a) | out_of_range(b) | out_of_range(c) | out_of_range(d);
+  return make_meta(fminf(a, b), fmaxf(c, d), 15.0f);
+}
+
+// Codes of 32 values of one group: qcode_fast for each, with its exact
+// fallback taken once, after the pass, for the values near a rounding tie.
+template <int QMAX>
+__device__ __forceinline__ void codes32(const float (&x)[32], const GroupMeta& m, float (&c)[32]) {
+  if (!m.nz) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) c[j] = 0.0f;
+    return;
+  }
+  const float rs = approx_rcp(m.sf);
+  uint32_t ties = 0u;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const float u = __fsub_rn(x[j], m.zf);
+    const float q0 = u * rs;
+    const float r = rintf(q0);
+    ties |= (fabsf(fabsf(q0 - r) - 0.5f) > 1e-5f ? 0u : 1u) << j;
+    c[j] = fminf(fmaxf(r, 0.0f), (float)QMAX);
+  }
+  while (ties) {
+    const int j = __ffs(ties) - 1;
+    ties &= ties - 1;
+    float u = 0.0f, xv = 0.0f;
+#pragma unroll
+    for (int q = 0; q < 32; ++q) xv = q == j ? x[q] : xv;   // register select, no local memory
+    u = __fsub_rn(xv, m.zf);
+    const float r = fminf(fmaxf(rintf(__fdiv_rn(u, m.sf)), 0.0f), (float)QMAX);
+#pragma unroll
+    for (int q = 0; q < 32; ++q) c[q] = q == j ? r : c[q];
+  }
+}
+
+// Pack 8 integer-valued floats c[o .. o + 7] (0..15) as nibbles 0..7 of a word.
+__device__ __forceinline__ uint32_t pack_nib8(const float (&c)[32], int o) {
+  float lo = c[o], hi = c[o + 4];
+#pragma unroll
+  for (int n = 1; n < 4; ++n) {
+    lo = fmaf(c[o + n], (float)(1 << (4 * n)), lo);
+    hi = fmaf(c[o + 4 + n], (float)(1 << (4 * n)), hi);
+  }
+  // exact integers below 2^16: add 2^23 and take the mantissa bits
+  const uint32_t l = __float_as_uint(lo + 8388608.0f) & 0xFFFFu, h = __float_as_uint(hi + 8388608.0f) & 0xFFFFu;
+  return l | (h << 16);
+}
+// Pack 16 integer-valued floats c[o .. o + 15] (0..3) as 2-bit fields 0..15 of a word.
+__device__ __forceinline__ uint32_t pack_crumb16(const float (&c)[32], int o) {
+  float lo = c[o], hi = c[o + 8];
+#pragma unroll
+  for (int n = 1; n < 8; ++n) {
+    lo = fmaf(c[o + n], (float)(1 << (2 * n)), lo);
+    hi = fmaf(c[o + 8 + n], (float)(1 << (2 * n)), hi);
+  }
+  const uint32_t l = __float_as_uint(lo + 8388608.0f) & 0xFFFFu, h = __float_as_uint(hi + 8388608.0f) & 0xFFFFu;
+  return l | (h << 16);
+}
+
+// Transpose of an 8 x 8 matrix of nibbles held in 8 words (word k = row k,
+// nibble n = column n): on return word n holds column n (nibble k = row k).
+__device__ __forceinline__ void transpose_nib8x8(uint32_t (&r)[8]) {
+#pragma unroll
+  for (int k = 0; k < 8; k += 2) {
+    const uint32_t t = ((r[k] >> 4) ^ r[k + 1]) & 0x0F0F0F0Fu;
+    r[k + 1] ^= t;
+    r[k] ^= t << 4;
+  }
+#pragma unroll
+  for (int k = 0; k < 8; k += 4)
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const uint32_t t = ((r[k + q] >> 8) ^ r[k + q + 2]) & 0x00FF00FFu;
+      r[k + q + 2] ^= t;
+      r[k + q] ^= t << 8;
+    }
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint32_t t = ((r[q] >> 16) ^ r[q + 4]) & 0x0000FFFFu;
+    r[q + 4] ^= t;
+    r[q] ^= t << 16;
+  }
+}
+
+// INT4 V codes of one group into the block image: lane t holds its slot's
+// codes c[0..31] (channels 32gr + c'); word (channel, slot chunk j) gets
+// slots 8j .. 8j + 7 in nibbles 0..7.  `wbuf`: 128 words of the warp's own
+// shared memory.
+__device__ __forceinline__ void store_i4v_group(uint8_t* img, const float (&c)[32], int gr, uint32_t* wbuf) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 0; o < 4; ++o) wbuf[32 * o + lane] = pack_nib8(c, 8 * o);   // channels 8o .. 8o+7 of slot lane
+  __syncwarp();
+  if (lane < 16) {
+    const int o = lane >> 2, j = lane & 3;
+    const uint4 a = *reinterpret_cast<const uint4*>(wbuf + 32 * o + 8 * j);
+    const uint4 b = *reinterpret_cast<const uint4*>(wbuf + 32 * o + 8 * j + 4);
+    uint32_t r[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};   // row k = slot 8j + k
+    transpose_nib8x8(r);
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      *reinterpret_cast<uint32_t*>(img + i4v_byte(8 * j, 32 * gr + 8 * o + k)) = r[k];
+  }
+  __syncwarp();
+}
+
+// INT4 quantization of one token's group (K or V): metadata, codes, and the
+// dequantized values fmaf(code, scale, zero) when `deq` is set.
+struct I4Group {
+  GroupMeta m;
+  float c[32];
+};
+__device__ __forceinline__ void quant_i4_group(const uint32_t (&w)[16], I4Group& q, bool& bad) {
+  q.m = meta_i4(w, bad);
+  float x[32];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    x[2 * j] = bf_lo(w[j]);
+    x[2 * j + 1] = bf_hi(w[j]);
+  }
+  codes32<15>(x, q.m, q.c);
+}
+
+// Fresh INT4 pages filled with 32 tokens within one call.  Grid (jobs, kv heads).
+__global__ void __launch_bounds__(kBulkThreads) bulk_int4_kernel(
+    uint8_t* __restrict__ pool, size_t int4_off, int64_t n2, int hkv, const __nv_bfloat16* __restrict__ k,
+    const __nv_bfloat16* __restrict__ v, const AppendJob* __restrict__ jobs, const int32_t* __restrict__ toks,
+    Entry* __restrict__ table, int32_t* __restrict__ ntab, uint32_t* __restrict__ status) {
+  __shared__ __align__(16) uint8_t img[kInt4Block];
+  __shared__ __align__(16) uint32_t wbuf[4][128];
+  asm volatile("griddepcontrol.wait;" ::: "memory");   // token lists and earlier stream work are done
+  asm volatile("griddepcontrol.launch_dependents;");
+  const AppendJob job = jobs[blockIdx.x];
+  const int h = blockIdx.y, gr = threadIdx.x >> 5, t = threadIdx.x & 31;
+  const int T = toks[job.tok_off + t];
+  uint32_t kw[16], vw[16];
+  load_group(k, T, h, hkv, gr, kw);
+  load_group(v, T, h, hkv, gr, vw);
+  bool bad = false;
+  I4Group q;
+  // K: slot t's row, words (i, gr) i = 0..3 hold channels 32gr + 8i + n in nibble n
+  quant_i4_group(kw, q, bad);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) *reinterpret_cast<uint32_t*>(img + kI4KCodes + 64 * t + 16 * i + 4 * gr) = pack_nib8(q.c, 8 * i);
+  *reinterpret_cast<uint32_t*>(img + kI4KMeta + 16 * t + 4 * gr) =
+      (uint32_t)__half_as_ushort(q.m.s) | ((uint32_t)__half_as_ushort(q.m.z) << 16);
+  // V
+  quant_i4_group(vw, q, bad);
+  store_i4v_group(img, q.c, gr, wbuf[gr]);
+  st_half(img, kI4VMeta + 2 * v_meta_index(t, gr), q.m.s);
+  st_half(img, kI4VMeta + 256 + 2 * v_meta_index(t, gr), q.m.z);
+  flush_vmax(q.m.sf, status);
+  if (__any_sync(0xFFFFFFFFu, bad) && t == 0) atomicOr(status, kStatusRange);
+  __syncthreads();
+  uint4* out4 = reinterpret_cast<uint4*>(pool + int4_off + ((size_t)(job.page - n2) * hkv + h) * kInt4Block);
+  const uint4* img4 = reinterpret_cast<const uint4*>(img);
+  for (int x = threadIdx.x; x < kInt4Block / 16; x += kBulkThreads) out4[x] = img4[x];
+  if (h == 0 && threadIdx.x == 0) {
+    if (job.tab_index >= 0) table[job.tab_index] = Entry{job.page, job.live};
+    if (job.ntab_req >= 0) ntab[job.ntab_req] = job.ntab_len;
+  }
+}
+
+// Direct INT2 groups: 32 tokens that fill a staging page within one call,
+// quantized to INT4 (per token and group), dequantized with fmaf(code, scale,
+// zero) and requantized to INT2: K per channel across the 32 tokens, V per
+// token and group.  Only the INT2 block is written.  Grid (jobs, kv heads).
+// Launched as a programmatic dependent of the INT4 kernels, as the
+// warp-per-token direct kernel is (it touches nothing they write).
+__global__ void __launch_bounds__(kBulkThreads) bulk_int2_kernel(
+    uint8_t* __restrict__ pool, int hkv, const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
+    const DirectJob* __restrict__ jobs, const int32_t* __restrict__ toks, uint32_t* __restrict__ status) {
+  __shared__ __align__(16) uint8_t img[kInt2Block];
+  __shared__ __align__(16) float4 kmeta[4][32];          // per channel of the warp's group: zero, 1/scale, scale
+  __shared__ __align__(16) uint32_t vbuf[4][32][9];      // INT2 V codes [slot][word] (padded)
+  const DirectJob job = jobs[blockIdx.x];
+  const int h = blockIdx.y, gr = threadIdx.x >> 5, t = threadIdx.x & 31;
+  const int T = toks[job.tok_off + t];
+  uint32_t kw[16], vw[16];
+  load_group(k, T, h, hkv, gr, kw);
+  load_group(v, T, h, hkv, gr, vw);
+  bool bad = false;
+  float xq[32];   // INT4-dequantized values of slot t's group
+  I4Group q;
+  // ---- K: INT4 per token, then INT2 per channel across the 32 slots
+  quant_i4_group(kw, q, bad);
+  {
+    const float sf = q.m.sf, zf = q.m.zf;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) xq[j] = __fmaf_rn(q.c[j], sf, zf);
+  }
+  {
+    float my_mn = 0.0f, my_mx = 0.0f;   // channel t of the group: min / max over the 32 slots
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      const float a = redux_min(xq[c]), b = redux_max(xq[c]);
+      my_mn = t == c ? a : my_mn;
+      my_mx = t == c ? b : my_mx;
+    }
+    const GroupMeta m2 = make_meta(my_mn, my_mx, 3.0f);
+    kmeta[gr][t] = make_float4(m2.zf, approx_rcp(m2.sf), m2.sf, m2.nz ? 1.0f : 0.0f);
+    const int ch = 32 * gr + t;
+    st_half(img, kI2KMeta + 2 * i2k_meta_index(ch), m2.s);
+    st_half(img, kI2KMeta + 256 + 2 * i2k_meta_index(ch), m2.z);
+    float smx = m2.sf;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) smx = fmaxf(smx, __shfl_xor_sync(0xFFFFFFFFu, smx, o));
+    if (t == 0) atomicMax(status + 1, __float_as_uint(smx));
+  }
+  __syncwarp();
+  {
+    // codes of slot t: channel c with its own metadata (the repack's rule, per element)
+    float c2[32];
+    uint32_t ties = 0u;
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      const float4 mm = kmeta[gr][c];
+      const float u = __fsub_rn(xq[c], mm.x);
+      const float q0 = u * mm.y;
+      const float r = rintf(q0);
+      ties |= (mm.w != 0.0f && !(fabsf(fabsf(q0 - r) - 0.5f) > 1e-5f) ? 1u : 0u) << c;
+      c2[c] = mm.w != 0.0f ? fminf(fmaxf(r, 0.0f), 3.0f) : 0.0f;
+    }
+    while (ties) {
+      const int j = __ffs(ties) - 1;
+      ties &= ties - 1;
+      float xv = 0.0f;
+#pragma unroll
+      for (int q2 = 0; q2 < 32; ++q2) xv = q2 == j ? xq[q2] : xv;
+      const float4 mm = kmeta[gr][j];
+      const float r = fminf(fmaxf(rintf(__fdiv_rn(__fsub_rn(xv, mm.x), mm.z)), 0.0f), 3.0f);
+#pragma unroll
+      for (int q2 = 0; q2 < 32; ++q2) c2[q2] = q2 == j ? r : c2[q2];
+    }
+    // slot t's row: channel c at byte c >> 2, bits 2 (c & 3): the group's 8 bytes
+    *reinterpret_cast<uint2*>(img + kI2KCodes + 32 * t + 8 * gr) = make_uint2(pack_crumb16(c2, 0), pack_crumb16(c2, 16));
+  }
+  // ---- V: INT4 per token, then INT2 per token on the dequantized values
+  quant_i4_group(vw, q, bad);
+  flush_vmax(q.m.sf, status);   // the INT4 V scales count toward the pool's V-scale maximum too
+  {
+    const float sf = q.m.sf, zf = q.m.zf;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) xq[j] = __fmaf_rn(q.c[j], sf, zf);
+    float mn = xq[0], mx = xq[0];
+#pragma unroll
+    for (int j = 1; j < 32; ++j) {
+      mn = fminf(mn, xq[j]);
+      mx = fmaxf(mx, xq[j]);
+    }
+    const GroupMeta m2 = make_meta(mn, mx, 3.0f);
+    float c2[32];
+    codes32<3>(xq, m2, c2);
+    st_half(img, kI2VMeta + 2 * v_meta_index(t, gr), m2.s);
+    st_half(img, kI2VMeta + 256 + 2 * v_meta_index(t, gr), m2.z);
+    float vmx = m2.sf;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) vmx = fmaxf(vmx, __shfl_xor_sync(0xFFFFFFFFu, vmx, o));
+    if (t == 0) atomicMax(status + 2, __float_as_uint(vmx));
+    // codes [slot][channel] as 2-bit fields: 2 words per slot (channels 0..15, 16..31)
+    vbuf[gr][t][0] = pack_crumb16(c2, 0);
+    vbuf[gr][t][1] = pack_crumb16(c2, 16);
+  }
+  __syncwarp();
+  // INT2 V bytes: lane = (channel cc of the group); the 4 slot chunks i
+  {
+    const int c = 32 * gr + t;
+    const int w = t >> 4, sh = 2 * (t & 15);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int b0 = i2v_byte(8 * i, c);
+      int b1 = b0;
+      uint32_t v0 = 0u, v1 = 0u;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const int tt = 8 * i + kk, b = i2v_byte(tt, c);
+        const uint32_t code = ((vbuf[gr][tt][w] >> sh) & 3u) << i2v_shift(tt);
+        if (b == b0) v0 |= code;
+        else { v1 |= code; b1 = b; }
+      }
+      img[b0] = (uint8_t)v0;
+      img[b1] = (uint8_t)v1;
+    }
+  }
+  if (__any_sync(0xFFFFFFFFu, bad) && t == 0) atomicOr(status, kStatusRange);
+  __syncthreads();
+  uint4* out4 = reinterpret_cast<uint4*>(pool + ((size_t)job.dst * hkv + h) * kInt2Block);
+  const uint4* img4 = reinterpret_cast<const uint4*>(img);
+  for (int x = threadIdx.x; x < kInt2Block / 16; x += kBulkThreads) out4[x] = img4[x];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __global__ void scatter_kernel(Entry* __restrict__ table, int32_t* __restrict__ ntab, uint32_t* __restrict__ hdead,
                                int hkv, const TableUpd* __restrict__ upd, int n) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
@@ -417,6 +763,24 @@ cudaError_t launch_append(kv_pool* P, const void* k, const void* v, const Append
   return launch_pdl(append_int4_kernel<false>, grid, dim3(kThreads), 0, s, P->d_pool, P->int4_offset,
                     P->cfg.n_int2_pages, P->cfg.num_kv_heads, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v,
                     d_jobs, d_toks, P->d_table, P->d_ntab, P->d_status, none);
+}
+
+cudaError_t launch_bulk_int4(kv_pool* P, const void* k, const void* v, const AppendJob* d_jobs, int n_jobs,
+                             const int32_t* d_toks, cudaStream_t s) {
+  if (n_jobs <= 0) return cudaSuccess;
+  ++P->launches;
+  return launch_pdl(bulk_int4_kernel, dim3((unsigned)n_jobs, (unsigned)P->cfg.num_kv_heads), dim3(kBulkThreads), 0,
+                    s, P->d_pool, P->int4_offset, P->cfg.n_int2_pages, P->cfg.num_kv_heads, (const __nv_bfloat16*)k,
+                    (const __nv_bfloat16*)v, d_jobs, d_toks, P->d_table, P->d_ntab, P->d_status);
+}
+
+cudaError_t launch_bulk_int2(kv_pool* P, const void* k, const void* v, const DirectJob* d_jobs, int n_jobs,
+                             const int32_t* d_toks, cudaStream_t s) {
+  if (n_jobs <= 0) return cudaSuccess;
+  ++P->launches;
+  return launch_pdl(bulk_int2_kernel, dim3((unsigned)n_jobs, (unsigned)P->cfg.num_kv_heads), dim3(kBulkThreads), 0,
+                    s, P->d_pool, P->cfg.num_kv_heads, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, d_jobs, d_toks,
+                    P->d_status);
 }
 
 cudaError_t launch_repack(kv_pool* P, const RepackJob* d_jobs, int n_jobs, cudaStream_t s) {
