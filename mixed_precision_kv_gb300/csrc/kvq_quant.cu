@@ -447,60 +447,62 @@ __device__ __forceinline__ GroupMeta meta_i4(const uint32_t (&w)[16], bool& bad)
   return make_meta(fminf(a, b), fmaxf(c, d), 15.0f);
 }
 
-// Codes of 32 values of one group: qcode_fast for each, with its exact
-// fallback taken once, after the pass, for the values near a rounding tie.
+// Codes of 8 values of one group: qcode_fast for each (same operations), the
+// exact division redone for the whole chunk when any of its quotients lies
+// near a rounding tie (rare).
 template <int QMAX>
-__device__ __forceinline__ void codes32(const float (&x)[32], const GroupMeta& m, float (&c)[32]) {
-  if (!m.nz) {
+__device__ __forceinline__ void codes8(const float (&x)[8], const GroupMeta& m, float rs, float (&c)[8]) {
+  bool tie = false;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) c[j] = 0.0f;
-    return;
-  }
-  const float rs = approx_rcp(m.sf);
-  uint32_t ties = 0u;
-#pragma unroll
-  for (int j = 0; j < 32; ++j) {
+  for (int j = 0; j < 8; ++j) {
     const float u = __fsub_rn(x[j], m.zf);
     const float q0 = u * rs;
     const float r = rintf(q0);
-    ties |= (fabsf(fabsf(q0 - r) - 0.5f) > 1e-5f ? 0u : 1u) << j;
+    tie |= !(fabsf(fabsf(q0 - r) - 0.5f) > 1e-5f);
     c[j] = fminf(fmaxf(r, 0.0f), (float)QMAX);
   }
-  while (ties) {
-    const int j = __ffs(ties) - 1;
-    ties &= ties - 1;
-    float u = 0.0f, xv = 0.0f;
+  if (tie) {
 #pragma unroll
-    for (int q = 0; q < 32; ++q) xv = q == j ? x[q] : xv;   // register select, no local memory
-    u = __fsub_rn(xv, m.zf);
-    const float r = fminf(fmaxf(rintf(__fdiv_rn(u, m.sf)), 0.0f), (float)QMAX);
+    for (int j = 0; j < 8; ++j) {
+      const float u = __fsub_rn(x[j], m.zf);
+      const float q0 = u * rs;
+      float r = rintf(q0);
+      if (!(fabsf(fabsf(q0 - r) - 0.5f) > 1e-5f)) r = rintf(__fdiv_rn(u, m.sf));
+      c[j] = fminf(fmaxf(r, 0.0f), (float)QMAX);
+    }
+  }
+  if (!m.nz) {
 #pragma unroll
-    for (int q = 0; q < 32; ++q) c[q] = q == j ? r : c[q];
+    for (int j = 0; j < 8; ++j) c[j] = 0.0f;
+  }
+}
+// 8 bf16 values of words w[4q .. 4q + 3] as floats
+__device__ __forceinline__ void bf8(const uint32_t (&w)[16], int q, float (&x)[8]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    x[2 * j] = bf_lo(w[4 * q + j]);
+    x[2 * j + 1] = bf_hi(w[4 * q + j]);
   }
 }
 
-// Pack 8 integer-valued floats c[o .. o + 7] (0..15) as nibbles 0..7 of a word.
-__device__ __forceinline__ uint32_t pack_nib8(const float (&c)[32], int o) {
-  float lo = c[o], hi = c[o + 4];
+// Pack 8 integer-valued floats (0..15) as nibbles 0..7 of a word (exact:
+// the two halves are integers below 2^16, read off after adding 2^23).
+__device__ __forceinline__ uint32_t pack_nib8(const float (&c)[8]) {
+  float lo = c[0], hi = c[4];
 #pragma unroll
   for (int n = 1; n < 4; ++n) {
-    lo = fmaf(c[o + n], (float)(1 << (4 * n)), lo);
-    hi = fmaf(c[o + 4 + n], (float)(1 << (4 * n)), hi);
+    lo = fmaf(c[n], (float)(1 << (4 * n)), lo);
+    hi = fmaf(c[4 + n], (float)(1 << (4 * n)), hi);
   }
-  // exact integers below 2^16: add 2^23 and take the mantissa bits
   const uint32_t l = __float_as_uint(lo + 8388608.0f) & 0xFFFFu, h = __float_as_uint(hi + 8388608.0f) & 0xFFFFu;
   return l | (h << 16);
 }
-// Pack 16 integer-valued floats c[o .. o + 15] (0..3) as 2-bit fields 0..15 of a word.
-__device__ __forceinline__ uint32_t pack_crumb16(const float (&c)[32], int o) {
-  float lo = c[o], hi = c[o + 8];
+// Pack 8 integer-valued floats (0..3) as 2-bit fields 0..7 (16 bits).
+__device__ __forceinline__ uint32_t pack_crumb8(const float (&c)[8]) {
+  float a = c[0];
 #pragma unroll
-  for (int n = 1; n < 8; ++n) {
-    lo = fmaf(c[o + n], (float)(1 << (2 * n)), lo);
-    hi = fmaf(c[o + 8 + n], (float)(1 << (2 * n)), hi);
-  }
-  const uint32_t l = __float_as_uint(lo + 8388608.0f) & 0xFFFFu, h = __float_as_uint(hi + 8388608.0f) & 0xFFFFu;
-  return l | (h << 16);
+  for (int n = 1; n < 8; ++n) a = fmaf(c[n], (float)(1 << (2 * n)), a);
+  return __float_as_uint(a + 8388608.0f) & 0xFFFFu;
 }
 
 // Transpose of an 8 x 8 matrix of nibbles held in 8 words (word k = row k,
@@ -529,13 +531,13 @@ __device__ __forceinline__ void transpose_nib8x8(uint32_t (&r)[8]) {
 }
 
 // INT4 V codes of one group into the block image: lane t holds its slot's
-// codes c[0..31] (channels 32gr + c'); word (channel, slot chunk j) gets
+// codes as nibbles of cw[o] (channels 32gr + 8o + n); word (channel, slot chunk j) gets
 // slots 8j .. 8j + 7 in nibbles 0..7.  `wbuf`: 128 words of the warp's own
 // shared memory.
-__device__ __forceinline__ void store_i4v_group(uint8_t* img, const float (&c)[32], int gr, uint32_t* wbuf) {
+__device__ __forceinline__ void store_i4v_group(uint8_t* img, const uint32_t (&cw)[4], int gr, uint32_t* wbuf) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
-  for (int o = 0; o < 4; ++o) wbuf[32 * o + lane] = pack_nib8(c, 8 * o);   // channels 8o .. 8o+7 of slot lane
+  for (int o = 0; o < 4; ++o) wbuf[32 * o + lane] = cw[o];   // channels 8o .. 8o+7 of slot lane, as nibbles
   __syncwarp();
   if (lane < 16) {
     const int o = lane >> 2, j = lane & 3;
@@ -550,25 +552,28 @@ __device__ __forceinline__ void store_i4v_group(uint8_t* img, const float (&c)[3
   __syncwarp();
 }
 
-// INT4 quantization of one token's group (K or V): metadata, codes, and the
-// dequantized values fmaf(code, scale, zero) when `deq` is set.
-struct I4Group {
-  GroupMeta m;
-  float c[32];
-};
-__device__ __forceinline__ void quant_i4_group(const uint32_t (&w)[16], I4Group& q, bool& bad) {
-  q.m = meta_i4(w, bad);
-  float x[32];
+// INT4 quantization of one token's group (K or V): the metadata and the codes
+// as nibble words cw[q] (channels 8q .. 8q + 7 of the group in nibbles 0..7).
+__device__ __forceinline__ GroupMeta quant_i4_words(const uint32_t (&w)[16], uint32_t (&cw)[4], bool& bad) {
+  const GroupMeta m = meta_i4(w, bad);
+  const float rs = approx_rcp(m.sf);
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    x[2 * j] = bf_lo(w[j]);
-    x[2 * j + 1] = bf_hi(w[j]);
+  for (int q = 0; q < 4; ++q) {
+    float x[8], c[8];
+    bf8(w, q, x);
+    codes8<15>(x, m, rs, c);
+    cw[q] = pack_nib8(c);
   }
-  codes32<15>(x, q.m, q.c);
+  return m;
+}
+// fmaf(code, scale, zero) of the 8 nibbles of a code word
+__device__ __forceinline__ void deq8(uint32_t cw, const GroupMeta& m, float (&y)[8]) {
+#pragma unroll
+  for (int n = 0; n < 8; ++n) y[n] = __fmaf_rn((float)((cw >> (4 * n)) & 15u), m.sf, m.zf);
 }
 
 // Fresh INT4 pages filled with 32 tokens within one call.  Grid (jobs, kv heads).
-__global__ void __launch_bounds__(kBulkThreads) bulk_int4_kernel(
+__global__ void __launch_bounds__(kBulkThreads, 8) bulk_int4_kernel(
     uint8_t* __restrict__ pool, size_t int4_off, int64_t n2, int hkv, const __nv_bfloat16* __restrict__ k,
     const __nv_bfloat16* __restrict__ v, const AppendJob* __restrict__ jobs, const int32_t* __restrict__ toks,
     Entry* __restrict__ table, int32_t* __restrict__ ntab, uint32_t* __restrict__ status) {
@@ -579,23 +584,26 @@ __global__ void __launch_bounds__(kBulkThreads) bulk_int4_kernel(
   const AppendJob job = jobs[blockIdx.x];
   const int h = blockIdx.y, gr = threadIdx.x >> 5, t = threadIdx.x & 31;
   const int T = toks[job.tok_off + t];
-  uint32_t kw[16], vw[16];
-  load_group(k, T, h, hkv, gr, kw);
-  load_group(v, T, h, hkv, gr, vw);
   bool bad = false;
-  I4Group q;
-  // K: slot t's row, words (i, gr) i = 0..3 hold channels 32gr + 8i + n in nibble n
-  quant_i4_group(kw, q, bad);
+  {
+    // K: slot t's row, words (i, gr) i = 0..3 hold channels 32gr + 8i + n in nibble n
+    uint32_t w[16], cw[4];
+    load_group(k, T, h, hkv, gr, w);
+    const GroupMeta m = quant_i4_words(w, cw, bad);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) *reinterpret_cast<uint32_t*>(img + kI4KCodes + 64 * t + 16 * i + 4 * gr) = pack_nib8(q.c, 8 * i);
-  *reinterpret_cast<uint32_t*>(img + kI4KMeta + 16 * t + 4 * gr) =
-      (uint32_t)__half_as_ushort(q.m.s) | ((uint32_t)__half_as_ushort(q.m.z) << 16);
-  // V
-  quant_i4_group(vw, q, bad);
-  store_i4v_group(img, q.c, gr, wbuf[gr]);
-  st_half(img, kI4VMeta + 2 * v_meta_index(t, gr), q.m.s);
-  st_half(img, kI4VMeta + 256 + 2 * v_meta_index(t, gr), q.m.z);
-  flush_vmax(q.m.sf, status);
+    for (int i = 0; i < 4; ++i) *reinterpret_cast<uint32_t*>(img + kI4KCodes + 64 * t + 16 * i + 4 * gr) = cw[i];
+    *reinterpret_cast<uint32_t*>(img + kI4KMeta + 16 * t + 4 * gr) =
+        (uint32_t)__half_as_ushort(m.s) | ((uint32_t)__half_as_ushort(m.z) << 16);
+  }
+  {
+    uint32_t w[16], cw[4];
+    load_group(v, T, h, hkv, gr, w);
+    const GroupMeta m = quant_i4_words(w, cw, bad);
+    store_i4v_group(img, cw, gr, wbuf[gr]);
+    st_half(img, kI4VMeta + 2 * v_meta_index(t, gr), m.s);
+    st_half(img, kI4VMeta + 256 + 2 * v_meta_index(t, gr), m.z);
+    flush_vmax(m.sf, status);
+  }
   if (__any_sync(0xFFFFFFFFu, bad) && t == 0) atomicOr(status, kStatusRange);
   __syncthreads();
   uint4* out4 = reinterpret_cast<uint4*>(pool + int4_off + ((size_t)(job.page - n2) * hkv + h) * kInt4Block);
@@ -613,29 +621,31 @@ __global__ void __launch_bounds__(kBulkThreads) bulk_int4_kernel(
 // token and group.  Only the INT2 block is written.  Grid (jobs, kv heads).
 // Launched as a programmatic dependent of the INT4 kernels, as the
 // warp-per-token direct kernel is (it touches nothing they write).
-__global__ void __launch_bounds__(kBulkThreads) bulk_int2_kernel(
+__global__ void __launch_bounds__(kBulkThreads, 6) bulk_int2_kernel(
     uint8_t* __restrict__ pool, int hkv, const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
     const DirectJob* __restrict__ jobs, const int32_t* __restrict__ toks, uint32_t* __restrict__ status) {
   __shared__ __align__(16) uint8_t img[kInt2Block];
-  __shared__ __align__(16) float4 kmeta[4][32];          // per channel of the warp's group: zero, 1/scale, scale
-  __shared__ __align__(16) uint32_t vbuf[4][32][9];      // INT2 V codes [slot][word] (padded)
+  __shared__ __align__(16) float4 kmeta[4][32];          // per channel of the warp's group: zero, 1/scale, scale, nz
+  __shared__ __align__(16) uint32_t vbuf[4][32][3];      // INT2 V codes [slot][channels 0..15, 16..31] (padded)
   const DirectJob job = jobs[blockIdx.x];
   const int h = blockIdx.y, gr = threadIdx.x >> 5, t = threadIdx.x & 31;
   const int T = toks[job.tok_off + t];
-  uint32_t kw[16], vw[16];
-  load_group(k, T, h, hkv, gr, kw);
-  load_group(v, T, h, hkv, gr, vw);
   bool bad = false;
-  float xq[32];   // INT4-dequantized values of slot t's group
-  I4Group q;
-  // ---- K: INT4 per token, then INT2 per channel across the 32 slots
-  quant_i4_group(kw, q, bad);
+  // ---- K: INT4 per token, dequantized, then INT2 per channel across the 32 slots
   {
-    const float sf = q.m.sf, zf = q.m.zf;
+    float xq[32];   // INT4-dequantized K of slot t's group
+    {
+      uint32_t w[16], cw[4];
+      load_group(k, T, h, hkv, gr, w);
+      const GroupMeta m = quant_i4_words(w, cw, bad);
 #pragma unroll
-    for (int j = 0; j < 32; ++j) xq[j] = __fmaf_rn(q.c[j], sf, zf);
-  }
-  {
+      for (int q = 0; q < 4; ++q) {
+        float y[8];
+        deq8(cw[q], m, y);
+#pragma unroll
+        for (int n = 0; n < 8; ++n) xq[8 * q + n] = y[n];
+      }
+    }
     float my_mn = 0.0f, my_mx = 0.0f;   // channel t of the group: min / max over the 32 slots
 #pragma unroll
     for (int c = 0; c < 32; ++c) {
@@ -652,66 +662,84 @@ __global__ void __launch_bounds__(kBulkThreads) bulk_int2_kernel(
 #pragma unroll
     for (int o = 16; o; o >>= 1) smx = fmaxf(smx, __shfl_xor_sync(0xFFFFFFFFu, smx, o));
     if (t == 0) atomicMax(status + 1, __float_as_uint(smx));
-  }
-  __syncwarp();
-  {
-    // codes of slot t: channel c with its own metadata (the repack's rule, per element)
-    float c2[32];
-    uint32_t ties = 0u;
+    __syncwarp();
+    // slot t's codes, channel c with channel c's metadata (the repack's rule per element)
+    uint32_t row[2] = {0u, 0u};
 #pragma unroll
-    for (int c = 0; c < 32; ++c) {
-      const float4 mm = kmeta[gr][c];
-      const float u = __fsub_rn(xq[c], mm.x);
-      const float q0 = u * mm.y;
-      const float r = rintf(q0);
-      ties |= (mm.w != 0.0f && !(fabsf(fabsf(q0 - r) - 0.5f) > 1e-5f) ? 1u : 0u) << c;
-      c2[c] = mm.w != 0.0f ? fminf(fmaxf(r, 0.0f), 3.0f) : 0.0f;
-    }
-    while (ties) {
-      const int j = __ffs(ties) - 1;
-      ties &= ties - 1;
-      float xv = 0.0f;
+    for (int q = 0; q < 4; ++q) {
+      float c2[8];
+      bool tie = false;
 #pragma unroll
-      for (int q2 = 0; q2 < 32; ++q2) xv = q2 == j ? xq[q2] : xv;
-      const float4 mm = kmeta[gr][j];
-      const float r = fminf(fmaxf(rintf(__fdiv_rn(__fsub_rn(xv, mm.x), mm.z)), 0.0f), 3.0f);
+      for (int n = 0; n < 8; ++n) {
+        const float4 mm = kmeta[gr][8 * q + n];
+        const float u = __fsub_rn(xq[8 * q + n], mm.x);
+        const float q0 = u * mm.y;
+        const float r = rintf(q0);
+        tie |= mm.w != 0.0f && !(fabsf(fabsf(q0 - r) - 0.5f) > 1e-5f);
+        c2[n] = mm.w != 0.0f ? fminf(fmaxf(r, 0.0f), 3.0f) : 0.0f;
+      }
+      if (tie) {
 #pragma unroll
-      for (int q2 = 0; q2 < 32; ++q2) c2[q2] = q2 == j ? r : c2[q2];
+        for (int n = 0; n < 8; ++n) {
+          const float4 mm = kmeta[gr][8 * q + n];
+          const float u = __fsub_rn(xq[8 * q + n], mm.x);
+          const float q0 = u * mm.y;
+          float r = rintf(q0);
+          if (!(fabsf(fabsf(q0 - r) - 0.5f) > 1e-5f)) r = rintf(__fdiv_rn(u, mm.z));
+          c2[n] = mm.w != 0.0f ? fminf(fmaxf(r, 0.0f), 3.0f) : 0.0f;
+        }
+      }
+      row[q >> 1] |= pack_crumb8(c2) << (16 * (q & 1));
     }
     // slot t's row: channel c at byte c >> 2, bits 2 (c & 3): the group's 8 bytes
-    *reinterpret_cast<uint2*>(img + kI2KCodes + 32 * t + 8 * gr) = make_uint2(pack_crumb16(c2, 0), pack_crumb16(c2, 16));
+    *reinterpret_cast<uint2*>(img + kI2KCodes + 32 * t + 8 * gr) = make_uint2(row[0], row[1]);
   }
   // ---- V: INT4 per token, then INT2 per token on the dequantized values
-  quant_i4_group(vw, q, bad);
-  flush_vmax(q.m.sf, status);   // the INT4 V scales count toward the pool's V-scale maximum too
   {
-    const float sf = q.m.sf, zf = q.m.zf;
+    uint32_t cw[4];
+    GroupMeta m;
+    {
+      uint32_t w[16];
+      load_group(v, T, h, hkv, gr, w);
+      m = quant_i4_words(w, cw, bad);
+    }
+    flush_vmax(m.sf, status);   // the INT4 V scales count toward the pool's V-scale maximum too
+    float mn = 0.0f, mx = 0.0f;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) xq[j] = __fmaf_rn(q.c[j], sf, zf);
-    float mn = xq[0], mx = xq[0];
+    for (int q = 0; q < 4; ++q) {
+      float y[8];
+      deq8(cw[q], m, y);
 #pragma unroll
-    for (int j = 1; j < 32; ++j) {
-      mn = fminf(mn, xq[j]);
-      mx = fmaxf(mx, xq[j]);
+      for (int n = 0; n < 8; ++n) {
+        mn = (q == 0 && n == 0) ? y[0] : fminf(mn, y[n]);
+        mx = (q == 0 && n == 0) ? y[0] : fmaxf(mx, y[n]);
+      }
     }
     const GroupMeta m2 = make_meta(mn, mx, 3.0f);
-    float c2[32];
-    codes32<3>(xq, m2, c2);
+    const float rs2 = approx_rcp(m2.sf);
+    uint32_t row[2] = {0u, 0u};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float y[8], c2[8];
+      deq8(cw[q], m, y);
+      codes8<3>(y, m2, rs2, c2);
+      row[q >> 1] |= pack_crumb8(c2) << (16 * (q & 1));
+    }
     st_half(img, kI2VMeta + 2 * v_meta_index(t, gr), m2.s);
     st_half(img, kI2VMeta + 256 + 2 * v_meta_index(t, gr), m2.z);
     float vmx = m2.sf;
 #pragma unroll
     for (int o = 16; o; o >>= 1) vmx = fmaxf(vmx, __shfl_xor_sync(0xFFFFFFFFu, vmx, o));
     if (t == 0) atomicMax(status + 2, __float_as_uint(vmx));
-    // codes [slot][channel] as 2-bit fields: 2 words per slot (channels 0..15, 16..31)
-    vbuf[gr][t][0] = pack_crumb16(c2, 0);
-    vbuf[gr][t][1] = pack_crumb16(c2, 16);
+    // codes [slot][channels 0..15, 16..31] as 2-bit fields
+    vbuf[gr][t][0] = row[0];
+    vbuf[gr][t][1] = row[1];
   }
   __syncwarp();
-  // INT2 V bytes: lane = (channel cc of the group); the 4 slot chunks i
+  // INT2 V bytes: lane = channel cc of the group; the 4 slot chunks i
   {
     const int c = 32 * gr + t;
-    const int w = t >> 4, sh = 2 * (t & 15);
+    const int wsel = t >> 4, sh = 2 * (t & 15);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int b0 = i2v_byte(8 * i, c);
@@ -720,7 +748,7 @@ __global__ void __launch_bounds__(kBulkThreads) bulk_int2_kernel(
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         const int tt = 8 * i + kk, b = i2v_byte(tt, c);
-        const uint32_t code = ((vbuf[gr][tt][w] >> sh) & 3u) << i2v_shift(tt);
+        const uint32_t code = ((vbuf[gr][tt][wsel] >> sh) & 3u) << i2v_shift(tt);
         if (b == b0) v0 |= code;
         else { v1 |= code; b1 = b; }
       }
