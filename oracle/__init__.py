@@ -56,6 +56,7 @@ def lib():
                 "orc_reorder": (ctypes.c_int, [_P, _P, ctypes.c_int]),
                 "orc_evict": (ctypes.c_int, [_P, _P, _P, _I64]),
                 "orc_evict_head": (ctypes.c_int, [_P, _P, _P, _P, _I64]),
+                "orc_drop_dead_pages": (ctypes.c_int, [_P, _P, ctypes.c_int]),
                 "orc_fp_append": (ctypes.c_int, [_P, _I32, _P, _P, _I64]),
                 "orc_fp_drop": (ctypes.c_int, [_P, _I32, _I64, _I64]),
                 "orc_request_info": (ctypes.c_int, [_P, _I32, _P, _P]),
@@ -184,6 +185,11 @@ class OraclePool:
         pos = np.ascontiguousarray(pos, dtype=np.int64)
         kv_heads = np.ascontiguousarray(kv_heads, dtype=np.int32)
         return lib().orc_evict_head(self.h, _p(req_ids), _p(pos), _p(kv_heads), req_ids.size)
+
+    def drop_dead_pages(self, req_ids):
+        """Drop every full page with no live slot for any kv head from the listed tables."""
+        req_ids = np.ascontiguousarray(req_ids, dtype=np.int32)
+        return lib().orc_drop_dead_pages(self.h, _p(req_ids), req_ids.size)
 
     def fp_append(self, rid, k, v):
         """Full-precision tokens; k, v: bf16 bits [n][len(sel)][128]."""

@@ -64,6 +64,14 @@
  *      tokens keeps the order of the rest.
  *   R9 a slot excluded for one head reads, for that head, as the sentinel
  *      dead slot of R6.
+ *   R10 a full page none of whose 32 slots is live for any kv head may leave
+ *      its request's table: the other entries keep their order and their
+ *      pages do not move, its id returns to the free set, and the positions
+ *      it held read as dropped.  Head groups that keep different amounts of
+ *      context are pools of their own over their kv heads, fed the same
+ *      tokens; a group drops the pages its budget no longer covers
+ *       [Tangram, method steps 6-7: head groups with different retained
+ *        lengths, each holding only its own pages; IntentKV, method 2].
  */
 #include <algorithm>
 #include <cmath>
@@ -293,6 +301,8 @@ void repack_to_int2(const Pool* P, const Page& src, Page& dst) {
   }
 }
 
+constexpr uint32_t kDropped = 0xFFFFFFFFu;   // loc entry of a position whose page was dropped
+
 void free_id(Pool* P, int32_t id) {
   P->pages.erase(id);
   if (id < P->n2) P->free2.insert(id); else P->free4.insert(id);
@@ -485,7 +495,39 @@ int orc_evict(void* h, const int32_t* req, const int64_t* pos, int64_t n) {
   }
   for (int64_t i = 0; i < n; ++i) {
     const uint32_t l = P->reqs[req[i]].loc[pos[i]];
+    if (l == kDropped) continue;                    // its page was dropped: already dead
     P->pages.at((int32_t)(l >> 5)).live &= ~(1u << (l & 31u));
+  }
+  return ORC_OK;
+}
+
+// Drop dead pages (R10).  For each listed request, every full page (32 slots
+// written) none of whose slots is live for any kv head (evicted, or excluded
+// for every head) leaves the table; the other entries keep their order and
+// their pages stay where they are (IntentKV method 2: surviving pages do not
+// move).  The dropped ids return to the free sets, and the positions they
+// held read as dropped (evicting them again changes nothing).
+int orc_drop_dead_pages(void* h, const int32_t* req, int n) {
+  Pool* P = (Pool*)h;
+  for (int i = 0; i < n; ++i)
+    if (req[i] < 0 || req[i] >= P->max_req || !P->reqs[req[i]].open) return ORC_INVALID;
+  for (int i = 0; i < n; ++i) {
+    Req& R = P->reqs[req[i]];
+    std::vector<int32_t> keep;
+    for (int32_t id : R.table) {
+      const Page& pg = P->pages.at(id);
+      bool dead = pg.fill == kP;
+      for (int hh = 0; hh < P->hkv && dead; ++hh) dead = (pg.live & ~pg.hdead[(size_t)hh]) == 0u;
+      if (!dead) {
+        keep.push_back(id);
+        continue;
+      }
+      for (int s = 0; s < kP; ++s) R.loc[(size_t)pg.pos[s]] = kDropped;
+      if (R.tail4 == id) R.tail4 = -1;
+      if (R.staging == id) R.staging = -1;
+      free_id(P, id);
+    }
+    R.table = keep;
   }
   return ORC_OK;
 }
@@ -501,6 +543,7 @@ int orc_evict_head(void* h, const int32_t* req, const int64_t* pos, const int32_
   }
   for (int64_t i = 0; i < n; ++i) {
     const uint32_t l = P->reqs[req[i]].loc[pos[i]];
+    if (l == kDropped) continue;                    // its page was dropped: already dead for every head
     P->pages.at((int32_t)(l >> 5)).hdead[(size_t)kvh[i]] |= 1u << (l & 31u);
   }
   return ORC_OK;
