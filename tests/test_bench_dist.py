@@ -69,14 +69,17 @@ def test_recorded_traffic_follows_the_kernel_sources(tmp_path, monkeypatch):
     import bench
     with open(bench.TRAFFIC_RECORD) as f:
         rec = json.load(f)
-    step = 2 * rec["algorithmic_bytes"]
-    t = bench.recorded_traffic(step, rec["workload"], "auto")
-    if t is not None:   # sources unchanged since the capture
-        assert t == pytest.approx(2 * (rec["dram_bytes_read"] + rec["dram_bytes_write"]))
-    assert bench.recorded_traffic(step, rec["workload"], "simt") is None
-    assert bench.recorded_traffic(step, "some-other-workload", "auto") is None
+    assert rec["records"]
+    for r in rec["records"]:
+        step = 2 * r["algorithmic_bytes"]
+        t = bench.recorded_traffic(step, r["applies_to"], "auto")
+        if t is not None:   # sources unchanged since the capture
+            assert t == pytest.approx(2 * (r["dram_bytes_read"] + r["dram_bytes_write"]))
+        assert bench.recorded_traffic(step, r["applies_to"], "simt") is None
+    assert bench.recorded_traffic(1e9, "some-other-workload", "auto") is None
     stale = dict(rec, sources_sha256="0" * 64)
     p = tmp_path / "traffic.json"
     p.write_text(json.dumps(stale))
     monkeypatch.setattr(bench, "TRAFFIC_RECORD", str(p))
-    assert bench.recorded_traffic(step, rec["workload"], "auto") is None
+    r = rec["records"][0]
+    assert bench.recorded_traffic(2 * r["algorithmic_bytes"], r["applies_to"], "auto") is None
