@@ -142,6 +142,19 @@ KVQ_API kv_status_t kv_evict_slots(kv_pool_t* pool, const int32_t* req_ids, cons
 KVQ_API kv_status_t kv_evict_slots_head(kv_pool_t* pool, const int32_t* req_ids, const int64_t* token_pos,
                                         const int32_t* kv_heads, int64_t n, void* stream);
 
+/* Free the pages nothing reads any more (Tangram: a head group holds only the
+ * pages of its own budget; IntentKV method 2: surviving pages do not move).
+ * For each listed request, every full page (32 tokens written) with no live
+ * slot for any kv head (evicted, or excluded for every head) leaves the
+ * table; the other entries keep their order, so positions and outputs are
+ * unchanged (a dead slot adds exactly 0).  The freed ids return to their free
+ * list and are reused lowest first.  Token positions of a dropped page stay
+ * counted (kv_request_info) and read as gone: evicting or excluding them
+ * again is a no-op.  req_ids: host int32 [n_req]; a request that is not open
+ * fails the call before any change (KV_ERR_INVALID_ARG).  Partial pages (the
+ * INT4 tail, the staging page) are kept. */
+KVQ_API kv_status_t kv_drop_dead_pages(kv_pool_t* pool, const int32_t* req_ids, int32_t n_req, void* stream);
+
 /* Full-precision token lists (HyQuant, Algorithm 3 and Algorithm 4 FREEZE:
  * the vertical-line tokens, the staging buffer and the window stay in full
  * precision and are scanned after the quantized prefix under the same online
@@ -215,6 +228,32 @@ KVQ_API kv_status_t kv_decode_attn(kv_pool_t* pool, const void* q, const int32_t
  * The caller still provides q, out and the pool, as for kv_decode_attn. */
 KVQ_API kv_status_t kv_decode_attn_noalloc(kv_pool_t* pool, const void* q, const int32_t* req_ids, int32_t batch,
                                            int32_t num_q_heads, float softmax_scale, float* out, void* stream);
+
+/* Decode over head groups held in pools of their own (Tangram: head groups
+ * keep different amounts of context).  Pool p holds kv heads
+ * [h_p, h_p + num_kv_heads_p) of the model, h_p the kv heads of the pools
+ * before it, fed the same tokens as the others but evicting (and dropping,
+ * kv_drop_dead_pages) what its own budget leaves out, so it keeps only its
+ * own pages.  One launch of the tensor-core scan walks every pool.
+ *   pools    host [n_pools], 1 <= n_pools <= 8, distinct pools on one device
+ *   q        device, bf16 [batch][num_q_heads][128]
+ *   req_ids  host, int32 [n_pools][batch]: pool p's request of batch row b
+ *   out      device, fp32 [batch][num_q_heads][128]
+ * q head h uses kv head h / (num_q_heads / K) of the model, K the kv heads of
+ * all pools together; num_q_heads must be a multiple of K with a ratio <= 8.
+ * Results equal kv_decode_attn on one pool with all K heads in which each
+ * head's excluded positions read as dead.  The scan skips every page with no
+ * live slot for the head it reads it for.  Always the tensor-core scan,
+ * whatever kv_set_decode_impl chose.  Requests holding full-precision list
+ * tokens are KV_ERR_INVALID_ARG.  The plan, the q operands and the partials
+ * live in pools[0]'s buffers, and a timeout of the scan is reported by
+ * pools[0]'s kv_pool_sync; every pool's later work on another stream waits
+ * for this call.  kv_last_decode_stats of each pool gives the bytes and
+ * pages of its share (its split count is not updated); kv_decode_timing of
+ * pools[0] covers the call. */
+KVQ_API kv_status_t kv_decode_attn_groups(kv_pool_t* const* pools, int32_t n_pools, const void* q,
+                                          const int32_t* req_ids, int32_t batch, int32_t num_q_heads,
+                                          float softmax_scale, float* out, void* stream);
 
 /* Testing aid for the device-timeout path (off by default).  Every copy wait
  * in the scans is bounded; first_wait_spins >= 0 makes the first copy wait of

@@ -26,7 +26,8 @@ EXPORTED = ["kv_pool_create", "kv_pool_destroy", "kv_request_open", "kv_request_
             "kv_reorder_pages", "kv_evict_slots", "kv_decode_attn", "kv_set_decode_impl", "kv_pool_sync",
             "kv_request_info", "kv_export_request", "kv_last_decode_stats", "kv_pool_launch_count", "kv_alloc_bits",
             "kv_last_error", "kv_decode_attn_noalloc", "kv_decode_timing", "kv_evict_slots_head", "kv_fp_configure",
-            "kv_fp_append", "kv_fp_drop", "kv_fp_count", "kv_set_wait_limit"]
+            "kv_fp_append", "kv_fp_drop", "kv_fp_count", "kv_set_wait_limit", "kv_drop_dead_pages",
+            "kv_decode_attn_groups"]
 
 _P = ctypes.c_void_p
 _I32, _I64 = ctypes.c_int32, ctypes.c_int64
@@ -65,6 +66,8 @@ def load_library(path: str = LIB_PATH):
             "kv_reorder_pages": [_P, _P, _I32, _P],
             "kv_evict_slots": [_P, _P, _P, _I64, _P],
             "kv_evict_slots_head": [_P, _P, _P, _P, _I64, _P],
+            "kv_drop_dead_pages": [_P, _P, _I32, _P],
+            "kv_decode_attn_groups": [_P, _I32, _P, _P, _I32, _I32, ctypes.c_float, _P, _P],
             "kv_fp_configure": [_P, _I32],
             "kv_fp_append": [_P, _P, _P, _P, _I64, _P],
             "kv_fp_drop": [_P, _I32, _I64, _I64, _P],
@@ -225,6 +228,12 @@ class KVPool:
         _check(load_library().kv_evict_slots_head(self._h, _ptr(req_ids), _ptr(token_pos), _ptr(kv_heads),
                                                   req_ids.size, _stream(stream, self.device)), "kv_evict_slots_head")
 
+    def drop_dead_pages(self, req_ids, stream=None):
+        """kv_drop_dead_pages: free every full page with no live slot for any kv head."""
+        req_ids = _np(req_ids, np.int32)
+        _check(load_library().kv_drop_dead_pages(self._h, _ptr(req_ids), req_ids.size, _stream(stream, self.device)),
+               "kv_drop_dead_pages")
+
     def fp_configure(self, max_tokens):
         """kv_fp_configure: capacity of every request's full-precision lists."""
         _check(load_library().kv_fp_configure(self._h, int(max_tokens)), "kv_fp_configure")
@@ -291,6 +300,35 @@ class KVPool:
         _check(load_library().kv_decode_attn_noalloc(self._h, ctypes.c_void_p(q.data_ptr()), _ptr(req_ids), B, Hq,
                                                      float(softmax_scale), ctypes.c_void_p(out.data_ptr()),
                                                      _stream(stream, self.device)), "kv_decode_attn_noalloc")
+        return out
+
+    @staticmethod
+    def decode_groups(pools, q, req_ids, softmax_scale, out=None, stream=None):
+        """kv_decode_attn_groups: pools hold consecutive kv head ranges of one model
+        (pools[0]'s first); req_ids [n_pools][B]: each pool's request of batch row b.
+        q: torch bf16 CUDA [B][Hq][128] -> out fp32 [B][Hq][128]."""
+        torch = _torch_mod()
+        pools = list(pools)
+        if not pools:
+            raise ValueError("need at least one pool")
+        req_ids = _np(req_ids, np.int32)
+        B, Hq, D = q.shape
+        dev = pools[0].device
+        if req_ids.shape != (len(pools), B):
+            raise ValueError("req_ids must be [n_pools][B]")
+        if q.dtype is not torch.bfloat16 or not pools[0]._on_pool_device(q) or D != HEAD_DIM or \
+                not q.is_contiguous():
+            raise ValueError("q must be a contiguous bf16 tensor [B][Hq][128] on the pools' device")
+        if out is None:
+            out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+        elif out.dtype is not torch.float32 or out.shape != q.shape or not pools[0]._on_pool_device(out) or \
+                not out.is_contiguous():
+            raise ValueError("out must be a contiguous fp32 tensor shaped like q on the pools' device")
+        handles = (_P * len(pools))(*[p._h for p in pools])
+        _check(load_library().kv_decode_attn_groups(handles, len(pools), ctypes.c_void_p(q.data_ptr()),
+                                                    _ptr(req_ids), B, Hq, float(softmax_scale),
+                                                    ctypes.c_void_p(out.data_ptr()), _stream(stream, dev)),
+               "kv_decode_attn_groups")
         return out
 
     def set_wait_limit(self, first_wait_spins):

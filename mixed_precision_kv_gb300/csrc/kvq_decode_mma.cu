@@ -646,7 +646,8 @@ template <int G>
 __global__ void __launch_bounds__(256) frag_kernel(const __nv_bfloat16* __restrict__ q, int hq, float scale_log2,
                                                    const Unit* __restrict__ units,
                                                    const uint32_t* __restrict__ smax_bits,
-                                                   UnitFrag* __restrict__ frags) {
+                                                   UnitFrag* __restrict__ frags,
+                                                   const GroupPool* __restrict__ gpools) {
   constexpr bool kPair = Cols<G>::kPair;
   __shared__ FragSmem S;
   // Launched as a programmatic dependent of the last kernel before the decode
@@ -658,6 +659,8 @@ __global__ void __launch_bounds__(256) frag_kernel(const __nv_bfloat16* __restri
   const Unit u = units[blockIdx.x];
   asm volatile("griddepcontrol.launch_dependents;");   // the scan may be staged
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+  // a grouped decode: the unit's own pool bounds its INT2 K scales
+  if (gpools) smax_bits = gpools[u.pad].smax;
   const float smax = fmaxf(__uint_as_float(smax_bits[0]), 1.0f);
   {
     // thread (h, 4 channels); q needs only its element alignment
@@ -743,14 +746,17 @@ __global__ void __launch_bounds__(256) frag_kernel(const __nv_bfloat16* __restri
 // of consecutive units, cut so that every warp gets about the same cost.  The
 // warp writes one partial per split.  kHead: some slots are excluded for
 // single kv heads (hdead, one word per page id x kv head); without it the
-// scan does not carry the extra pointer.
-template <int G, bool kHead>
+// scan does not carry the extra pointer.  kMulti: the splits come from
+// several pools (head groups, each with its own pages and tables): a split
+// names its pool and its kv head within the pool, the page stream reads the
+// pool's addresses from gpools, and a page ticket carries its width.
+template <int G, bool kHead, bool kMulti>
 __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(
     const uint8_t* __restrict__ pool, size_t int4_off, int64_t n2, int hkv, int max_pages,
     const Entry* __restrict__ table, const UnitFrag* __restrict__ frags, const Split* __restrict__ splits,
     const int32_t* __restrict__ wsplit, int n_workers, const int32_t* __restrict__ ntab,
     const uint32_t* __restrict__ hdead, float* __restrict__ part, const uint32_t* __restrict__ smax_bits,
-    uint32_t* __restrict__ status, uint32_t first_spins) {
+    uint32_t* __restrict__ status, uint32_t first_spins, const GroupPool* __restrict__ gpools) {
   constexpr bool kPair = Cols<G>::kPair;
   constexpr int NH = Cols<G>::NH;
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -766,7 +772,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(
   if (s_begin >= s_end) return;   // no CTA-wide barrier below: idle warps may leave
   // P is carried as p * 2^sv in the fp16 folds so that p * scale stays clear
   // of the binary16 subnormal range; 2^sv * (largest V scale) <= 2^15.
-  const float vmax = fmaxf(__uint_as_float(smax_bits[1]), 1.0f / 1024.0f);
+  float vmax = fmaxf(__uint_as_float(smax_bits[1]), 1.0f / 1024.0f);
+  if constexpr (kMulti) {
+    // a warp may read pages of every pool: bound the V scales of all of them
+    const int np = gpools[0].n_pools;
+    for (int p = 0; p < np; ++p) vmax = fmaxf(vmax, __uint_as_float(gpools[p].smax[1]));
+  }
   const int sv = max(0, min(15, ilogbf(32768.0f / vmax)));
   const float pscale = ldexpf(1.0f, sv), oscale = ldexpf(1.0f, -sv);
   if (lane == 0) {
@@ -787,15 +798,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(
     int32_t tag;
   };
   int lsg = s_begin, lpos = 0, lend = 0, lkvh = 0, ln = 0, lm = 0;   // reader: split, next position, end, ...
+  int lpl = 0;   // kMulti: pool of the split being read
   const Entry* ltab = table;
   auto enter = [&](int sg) {
     const Split sp = splits[sg];
-    ltab = table + (size_t)sp.req * max_pages;
     lpos = sp.page_begin;
     ln = sp.n_pos;
     lm = sp.n_lead;
-    lend = sp.page_end >= 0 ? sp.page_end : ntab[sp.req];   // open-ended: the table's length now
-    lkvh = sp.unit % hkv;
+    if constexpr (kMulti) {
+      lpl = sp.pad[0];
+      const GroupPool* gp = gpools + lpl;
+      ltab = gp->table + (size_t)sp.req * gp->max_pages;
+      lend = sp.page_end >= 0 ? sp.page_end : gp->ntab[sp.req];
+      lkvh = sp.pad[1];
+    } else {
+      ltab = table + (size_t)sp.req * max_pages;
+      lend = sp.page_end >= 0 ? sp.page_end : ntab[sp.req];   // open-ended: the table's length now
+      lkvh = sp.unit % hkv;
+    }
   };
   enter(lsg);
   int bbase = 0, bcount = 0;   // the batch holds stream pages [bbase, bbase + bcount)
@@ -814,7 +834,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(
     bbase = k;
     bcount = nb;
     bid = -1;
-    if constexpr (kHead) blive = 0u;
+    if constexpr (kHead || kMulti) blive = 0u;
     if (lane < nb) {
       // scan-order position p -> table index: the next INT2-first entry when
       // floor((p+1) m / n) > floor(p m / n), else the next of the others
@@ -827,19 +847,33 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(
       }
       const Entry e = ltab[idx];
       bid = e.id;
-      // slots excluded for this kv head only read as dead slots too
-      if constexpr (kHead) {
-        const uint32_t* hd = *reinterpret_cast<const uint32_t* const volatile*>(&WS.hdead);
-        blive = e.live & ~hd[(size_t)e.id * hkv + lkvh];
+      if constexpr (kMulti) {
+        // the split's pool: width from its INT2 range, exclusion words if it has them
+        const GroupPool* gp = gpools + lpl;
+        const int64_t gn2 = gp->n2;
+        const int ghkv = gp->hkv;
+        const uint32_t* hd = gp->hdead;
+        blive = hd ? e.live & ~hd[(size_t)e.id * ghkv + lkvh] : e.live;
+        const bool i2 = e.id < gn2;
+        btag = (lsg << 7) | (i2 ? 64 : 0) | lkvh;
+        const uint8_t* src = i2 ? gp->pool + ((size_t)e.id * ghkv + lkvh) * kInt2Block
+                                : gp->pool + gp->int4_off + ((size_t)(e.id - gn2) * ghkv + lkvh) * kInt4Block;
+        bsrc = (unsigned long long)(uintptr_t)src;
+      } else {
+        // slots excluded for this kv head only read as dead slots too
+        if constexpr (kHead) {
+          const uint32_t* hd = *reinterpret_cast<const uint32_t* const volatile*>(&WS.hdead);
+          blive = e.live & ~hd[(size_t)e.id * hkv + lkvh];
+        }
+        else blive = e.live;
+        btag = (lsg << 6) | lkvh;
+        const uint8_t* src = e.id < n2 ? pool + ((size_t)e.id * hkv + lkvh) * kInt2Block
+                                       : pool + int4_off + ((size_t)(e.id - n2) * hkv + lkvh) * kInt4Block;
+        bsrc = (unsigned long long)(uintptr_t)src;
       }
-      else blive = e.live;
-      btag = (lsg << 6) | lkvh;
-      const uint8_t* src = e.id < n2 ? pool + ((size_t)e.id * hkv + lkvh) * kInt2Block
-                                     : pool + int4_off + ((size_t)(e.id - n2) * hkv + lkvh) * kInt4Block;
-      bsrc = (unsigned long long)(uintptr_t)src;
     }
     lpos += nb;
-    if constexpr (kHead) {
+    if constexpr (kHead || kMulti) {
       const bool keep = lane < nb && blive != 0u;
       const uint32_t kept = __ballot_sync(0xFFFFFFFFu, keep);
       brank = keep ? __popc(kept & ((1u << lane) - 1u)) : -1;
@@ -862,16 +896,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(
       }
     }
     int j = k - bbase;
-    if constexpr (kHead) j = __ffs(__ballot_sync(0xFFFFFFFFu, brank == j)) - 1;   // the lane of the j-th page kept
+    if constexpr (kHead || kMulti) j = __ffs(__ballot_sync(0xFFFFFFFFu, brank == j)) - 1;   // the lane of the j-th page kept
     src = __shfl_sync(0xFFFFFFFFu, bsrc, j);
     return Ticket{__shfl_sync(0xFFFFFFFFu, bid, j), __shfl_sync(0xFFFFFFFFu, blive, j),
                   __shfl_sync(0xFFFFFFFFu, btag, j)};
   };
+  // a ticket's width and split
+  auto tk_int2 = [&](const Ticket& t) { return kMulti ? ((t.tag >> 6) & 1) != 0 : t.id < n2; };
+  auto tk_split = [&](const Ticket& t) { return kMulti ? t.tag >> 7 : t.tag >> 6; };
   // copy number n goes to stage n & 1 and completes phase (n >> 1) & 1
   auto issue = [&](const Ticket& t, unsigned long long src, uint32_t n) {   // lane 0
     const uint32_t st = n & (kStages - 1);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the stage was read generically
-    bulk_load(WS.stage[st], (const void*)(uintptr_t)src, t.id < n2 ? (uint32_t)kInt2Block : (uint32_t)kInt4Block,
+    bulk_load(WS.stage[st], (const void*)(uintptr_t)src, tk_int2(t) ? (uint32_t)kInt2Block : (uint32_t)kInt4Block,
               &WS.bar[st]);
   };
   static_assert(kStages == 2, "the ticket ring below serves a two-stage copy ring");
@@ -970,7 +1007,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(
   uint32_t c = 0;      // copies consumed
   bool ok = true;
   while (t0.id >= 0) {
-    const int sg = t0.tag >> 6;
+    const int sg = tk_split(t0);
     if (sg != csg) {
       if (csg >= 0) flush(csg);
       for (int x = csg < 0 ? s_begin : csg + 1; x < sg; ++x) flush_empty(x);
@@ -986,7 +1023,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(
     }
     const uint8_t* blk = WS.stage[st];
     float lg[2][2][NH], zc[NH];
-    if (t0.id < n2) {
+    if (tk_int2(t0)) {
       qk_int2<G>(blk, F, acol2, lg, zc);
       softmax_pv<G, true>(blk, t0.live, pscale, lg, zc, o, zv, mrun, lsum, WS.pbuf);
     } else {
@@ -1020,9 +1057,10 @@ constexpr int kScanSmem = kWarps * (int)sizeof(WarpSmem);
 // shares the SM's memory with shared memory: ask for the smallest shared
 // carveout that holds one CTA (the default takes the largest, leaving L1 too
 // small for 16 warps' q operands; the scan then ran up to 1.45x slower).
-template <int G, bool kHead>
+template <int G, bool kHead, bool kMulti>
 cudaError_t set_scan_attributes() {
-  cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<G, kHead>, cudaFuncAttributeMaxDynamicSharedMemorySize, kScanSmem);
+  cudaError_t e =
+      cudaFuncSetAttribute(decode_mma_kernel<G, kHead, kMulti>, cudaFuncAttributeMaxDynamicSharedMemorySize, kScanSmem);
   if (e != cudaSuccess) return e;
   int dev = 0, per_sm = 0, reserved = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
@@ -1030,20 +1068,21 @@ cudaError_t set_scan_attributes() {
   if ((e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev)) != cudaSuccess) return e;
   if (per_sm <= 0) return cudaErrorInvalidValue;
   const int pct = std::min(100, (int)(((int64_t)(kScanSmem + reserved) * 100 + per_sm - 1) / per_sm));
-  return cudaFuncSetAttribute(decode_mma_kernel<G, kHead>, cudaFuncAttributePreferredSharedMemoryCarveout, pct);
+  return cudaFuncSetAttribute(decode_mma_kernel<G, kHead, kMulti>, cudaFuncAttributePreferredSharedMemoryCarveout, pct);
 }
 
 template <int G>
 cudaError_t launch_mma_g(kv_pool* P, const void* q, int32_t hq, float scale_log2, const Unit* d_units, int n_units,
                          const Split* d_splits, const int32_t* d_wsplit, int n_workers, void* d_frags, float* d_part,
-                         cudaStream_t s) {
+                         cudaStream_t s, const GroupPool* d_gpools) {
   // function attributes are set once per device (bit = device ordinal)
   static std::atomic<uint64_t> attr_set{0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!(attr_set.load() >> dev & 1u)) {
-    cudaError_t e = set_scan_attributes<G, false>();
-    if (e == cudaSuccess) e = set_scan_attributes<G, true>();
+    cudaError_t e = set_scan_attributes<G, false, false>();
+    if (e == cudaSuccess) e = set_scan_attributes<G, true, false>();
+    if (e == cudaSuccess) e = set_scan_attributes<G, false, true>();
     if (e != cudaSuccess) return e;
     attr_set.fetch_or(uint64_t(1) << dev);
   }
@@ -1051,22 +1090,24 @@ cudaError_t launch_mma_g(kv_pool* P, const void* q, int32_t hq, float scale_log2
   const uint32_t* smax = P->d_status + 1;
   P->launches += 2;
   cudaError_t e = launch_pdl(frag_kernel<G>, dim3((unsigned)n_units), dim3(256), 0, s, (const __nv_bfloat16*)q,
-                             (int)hq, scale_log2, d_units, smax, (UnitFrag*)d_frags);
+                             (int)hq, scale_log2, d_units, smax, (UnitFrag*)d_frags, d_gpools);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)((n_workers + kWarps - 1) / kWarps);
-  auto* kernel = P->hdead.empty() ? decode_mma_kernel<G, false> : decode_mma_kernel<G, true>;
+  auto* kernel = d_gpools ? decode_mma_kernel<G, false, true>
+                          : (P->hdead.empty() ? decode_mma_kernel<G, false, false> : decode_mma_kernel<G, true, false>);
   return launch_pdl(kernel, dim3(grid), dim3(kThreads), (size_t)kScanSmem, s, (const uint8_t*)P->d_pool,
                     P->int4_offset, (int64_t)P->cfg.n_int2_pages, P->cfg.num_kv_heads, P->cfg.max_pages_per_request,
                     (const Entry*)P->d_table, (const UnitFrag*)d_frags, d_splits, d_wsplit, n_workers,
                     (const int32_t*)P->d_ntab, (const uint32_t*)P->d_hdead, d_part, smax, P->d_status,
-                    P->first_wait_spins < 0 ? kSpinLimit : (uint32_t)P->first_wait_spins);
+                    P->first_wait_spins < 0 ? kSpinLimit : (uint32_t)P->first_wait_spins, d_gpools);
 }
 
 template <int G>
 int mma_occupancy() {
   int n = 0;
-  if (set_scan_attributes<G, false>() != cudaSuccess) return 1;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<G, false>, kThreads, kScanSmem) != cudaSuccess)
+  if (set_scan_attributes<G, false, false>() != cudaSuccess) return 1;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<G, false, false>, kThreads, kScanSmem) !=
+      cudaSuccess)
     return 1;
   return n > 0 ? n : 1;
 }
@@ -1077,13 +1118,16 @@ size_t decode_mma_frag_bytes() { return sizeof(UnitFrag); }
 
 cudaError_t launch_decode_mma(kv_pool* P, const void* q, int32_t hq, float scale_log2, const Unit* d_units, int n_units,
                               const Split* d_splits, const int32_t* d_wsplit, int n_workers, void* d_frags,
-                              float* d_part, float* out, cudaStream_t s) {
+                              float* d_part, float* out, cudaStream_t s, const GroupPool* d_gpools,
+                              int32_t total_kv_heads) {
   cudaError_t e;
-#define KVQ_MMA_CASE(g)                                                                                          \
-  case g:                                                                                                        \
-    e = launch_mma_g<g>(P, q, hq, scale_log2, d_units, n_units, d_splits, d_wsplit, n_workers, d_frags, d_part, s); \
+  const int g = hq / (total_kv_heads > 0 ? total_kv_heads : P->cfg.num_kv_heads);
+#define KVQ_MMA_CASE(gg)                                                                                          \
+  case gg:                                                                                                        \
+    e = launch_mma_g<gg>(P, q, hq, scale_log2, d_units, n_units, d_splits, d_wsplit, n_workers, d_frags, d_part, s, \
+                         d_gpools);                                                                               \
     break;
-  switch (hq / P->cfg.num_kv_heads) {
+  switch (g) {
     KVQ_MMA_CASE(1)
     KVQ_MMA_CASE(2)
     KVQ_MMA_CASE(3)
@@ -1098,7 +1142,7 @@ cudaError_t launch_decode_mma(kv_pool* P, const void* q, int32_t hq, float scale
   if (e != cudaSuccess) return e;
   if ((e = launch_fp_pending(P, q, hq, scale_log2, d_units, d_part, s)) != cudaSuccess) return e;
   if (P->merge_event && (e = cudaEventRecord(P->merge_event, s)) != cudaSuccess) return e;
-  return launch_merge(P, hq / P->cfg.num_kv_heads, d_units, n_units, d_part, hq, out, s);
+  return launch_merge(P, g, d_units, n_units, d_part, hq, out, s);
 }
 
 int decode_mma_workers_per_sm(int g) {

@@ -98,6 +98,25 @@ struct Split {
   int32_t pad[2];
 };
 
+// One pool of a grouped decode (kv_decode_attn_groups): its splits carry the
+// pool's index (Split::pad[0]) and the kv head within the pool (pad[1]), its
+// units the pool's index (Unit::pad), and the kernels read the pool's
+// addresses from an array of these.
+struct GroupPool {
+  const uint8_t* pool;
+  size_t int4_off;
+  int64_t n2;
+  const Entry* table;
+  const int32_t* ntab;
+  const uint32_t* hdead;   // null: no per-head exclusion in this pool
+  const uint32_t* smax;    // the pool's largest INT2 K scale and largest V scale (float bits)
+  int32_t hkv;
+  int32_t max_pages;
+  int32_t n_pools;         // entries in the array (the same in every entry)
+  int32_t pad;
+};
+constexpr int kMaxGroupPools = 8;
+
 // A full-precision scan to run between the page scan and the merge of the
 // next decode launch (set by the caller of launch_decode_*).
 struct FpLaunch {
@@ -286,6 +305,17 @@ struct kv_pool {
   int32_t n_ctas = 0;
   std::vector<int32_t> stat_req;      // request ids of the last decode (for kv_last_decode_stats)
   int32_t stat_hq = 0;
+  bool stat_skip_dead = false;        // the last decode skipped pages with no live slot for a head
+  // grouped decode plan cache (kv_decode_attn_groups with this pool first)
+  uint64_t serial = 0;                        // unique per pool created in this process
+  kvq::DevBuf gplan;
+  std::vector<kvq::GroupPool> gplan_pools;    // the pools' descriptors when the plan was built
+  std::vector<uint64_t> gplan_owner;          // and the pools' serials
+  std::vector<int32_t> gplan_req, gplan_len;  // per (pool, batch row): request id and table length
+  std::vector<uint64_t> gplan_ver;            // per (pool, batch row): table shape
+  int32_t gplan_hq = 0, gplan_slack = 0;
+  int32_t gplan_units = 0, gplan_splits = 0, gplan_workers = 0;
+  size_t gplan_units_off = 0, gplan_splits_off = 0, gplan_wsplit_off = 0, gplan_pools_off = 0;
   int32_t decode_impl = KV_DECODE_AUTO;
   cudaStream_t last_stream = nullptr;
   int64_t launches = 0;               // kernels launched by this pool
@@ -371,9 +401,13 @@ cudaError_t launch_decode_simt(kv_pool* P, const void* q, int32_t hq, float scal
 int decode_simt_ctas_per_sm(int g);
 // Tensor-core scan: workers are warps; d_frags holds decode_mma_frag_bytes()
 // per unit (the q operands its per-unit kernel builds before the scan).
+// Grouped form: d_gpools != null (device array of GroupPool) makes every
+// unit and split name its pool; total_kv_heads is then the kv heads of all
+// pools together (hq / total_kv_heads q heads per kv head).
 cudaError_t launch_decode_mma(kv_pool* P, const void* q, int32_t hq, float scale_log2, const Unit* d_units, int n_units,
                               const Split* d_splits, const int32_t* d_wsplit, int n_workers, void* d_frags,
-                              float* d_part, float* out, cudaStream_t s);
+                              float* d_part, float* out, cudaStream_t s, const GroupPool* d_gpools = nullptr,
+                              int32_t total_kv_heads = 0);
 int decode_mma_workers_per_sm(int g);
 constexpr int kMmaWarpsPerCta = 16;
 size_t decode_mma_frag_bytes();

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <climits>
 #include <cmath>
 #include <cstdarg>
@@ -59,6 +60,9 @@ bool req_ok(const kv_pool* P, int32_t r) {
 }
 
 bool is_int2(const kv_pool* P, int32_t id) { return id < P->cfg.n_int2_pages; }
+
+// Position-map entry of a token whose page was dropped (kv_drop_dead_pages).
+constexpr uint32_t kDroppedLoc = 0xFFFFFFFFu;
 
 // Per-head exclusion words (kept once kv_evict_slots_head has been used):
 // host mirror changes, each queued as a kind-2 table update for the device.
@@ -407,6 +411,8 @@ kv_status_t kv_pool_create(const kv_pool_config_t* cfg, kv_pool_t** out) {
   kv_pool* P = new (std::nothrow) kv_pool();
   if (!P) return fail(KV_ERR_OOM, "kv_pool_create: host allocation failed");
   P->cfg = *cfg;
+  static std::atomic<uint64_t> serials{0};
+  P->serial = ++serials;
   auto cleanup = [&](kv_status_t st) {
     cudaFree(P->d_pool);
     cudaFree(P->d_table);
@@ -460,6 +466,7 @@ kv_status_t kv_pool_destroy(kv_pool_t* P) {
   cudaFree(P->plan.ptr);
   cudaFree(P->partials.ptr);
   cudaFree(P->frags.ptr);
+  cudaFree(P->gplan.ptr);
   cudaFree(P->d_hdead);
   cudaFree(P->d_fpk);
   cudaFree(P->d_fpv);
@@ -1045,6 +1052,7 @@ kv_status_t kv_evict_slots(kv_pool_t* P, const int32_t* req_ids, const int64_t* 
   bool any = false;
   for (int64_t i = 0; i < n; ++i) {
     const uint32_t l = P->reqs[req_ids[i]].loc[token_pos[i]];
+    if (l == kDroppedLoc) continue;   // its page was dropped: already dead
     const int32_t id = (int32_t)(l >> 5);
     const uint32_t bit = 1u << (l & 31u);
     if (P->live[id] & bit) {
@@ -1104,12 +1112,74 @@ kv_status_t kv_evict_slots_head(kv_pool_t* P, const int32_t* req_ids, const int6
   std::vector<TableUpd> upd;
   for (int64_t i = 0; i < n; ++i) {
     const uint32_t l = P->reqs[req_ids[i]].loc[token_pos[i]];
+    if (l == kDroppedLoc) continue;   // its page was dropped: already dead for every head
     const int32_t id = (int32_t)(l >> 5);
     hdead_set(P, id, kv_heads[i], P->hdead[(size_t)id * hkv + kv_heads[i]] | (1u << (l & 31u)), upd);
   }
   if (upd.empty()) return KV_OK;
   P->plan_impl = -1;   // page costs per head changed: plan again at the next decode
   hdead_final(P, upd);
+  Upload u;
+  const size_t o = u.add(upd.data(), upd.size() * sizeof(TableUpd));
+  if ((st = upload(P, u, s)) != KV_OK) return st;
+  KV_CUDA(launch_scatter(P, (const TableUpd*)((uint8_t*)P->upload.ptr + o), (int)upd.size(), s));
+  return KV_OK;
+}
+
+kv_status_t kv_drop_dead_pages(kv_pool_t* P, const int32_t* req_ids, int32_t n_req, void* stream) {
+  if (!P || n_req < 0 || (n_req > 0 && !req_ids)) return fail(KV_ERR_INVALID_ARG, "kv_drop_dead_pages: bad arguments");
+  for (int32_t i = 0; i < n_req; ++i)
+    if (!req_ok(P, req_ids[i])) return fail(KV_ERR_INVALID_ARG, "kv_drop_dead_pages: request %d not open", req_ids[i]);
+  const int hkv = P->cfg.num_kv_heads;
+  Dirty dirty;
+  std::vector<TableUpd> hupd;
+  for (int32_t q = 0; q < n_req; ++q) {
+    const int32_t r = req_ids[q];
+    Request& R = P->reqs[r];
+    int32_t first = -1;
+    size_t w = 0;
+    for (size_t i = 0; i < R.table.size(); ++i) {
+      const int32_t id = R.table[i];
+      bool dead = P->fill[id] == kPage;
+      if (dead) {
+        if (P->hdead.empty()) {
+          dead = P->live[id] == 0u;
+        } else {
+          for (int h = 0; h < hkv && dead; ++h) dead = (P->live[id] & ~P->hdead[(size_t)id * hkv + h]) == 0u;
+        }
+      }
+      if (!dead) {
+        R.table[w++] = id;
+        continue;
+      }
+      if (first < 0) first = (int32_t)i;
+      for (int sl = 0; sl < kPage; ++sl) {
+        const int32_t pp = P->pos[(size_t)id * kPage + sl];
+        if (pp >= 0 && (size_t)pp < R.loc.size()) R.loc[(size_t)pp] = kDroppedLoc;
+      }
+      if (R.tail4 == id) R.tail4 = -1;
+      if (R.staging == id) R.staging = -1;
+      P->fill[id] = 0;
+      P->live[id] = 0u;
+      hdead_clear(P, id, hupd);
+      if (is_int2(P, id)) P->free2.insert(id);
+      else P->free4.insert(id);
+    }
+    if (first < 0) continue;
+    R.table.resize(w);
+    ++R.version;
+    R.shape = ++P->shape_clock;
+    dirty.structural(r, first);
+  }
+  if (dirty.from.empty()) return KV_OK;
+  DeviceGuard dg(P->cfg.device);
+  cudaStream_t s = (cudaStream_t)stream;
+  kv_status_t st = order_after_previous(P, s);
+  if (st != KV_OK) return st;
+  std::vector<TableUpd> upd;
+  emit_updates(P, dirty, upd);
+  hdead_final(P, hupd);
+  upd.insert(upd.end(), hupd.begin(), hupd.end());
   Upload u;
   const size_t o = u.add(upd.data(), upd.size() * sizeof(TableUpd));
   if ((st = upload(P, u, s)) != KV_OK) return st;
@@ -1397,6 +1467,7 @@ kv_status_t kv_decode_attn(kv_pool_t* P, const void* q, const int32_t* req_ids, 
   P->merge_event = nullptr;
   P->stat_req.assign(req_ids, req_ids + batch);
   P->stat_hq = hq;
+  P->stat_skip_dead = false;
   return KV_OK;
 }
 
@@ -1448,10 +1519,13 @@ kv_status_t kv_last_decode_stats(kv_pool_t* P, int64_t* kv_bytes, int32_t* n_spl
   for (int32_t r : P->stat_req) {
     if (!req_ok(P, r)) continue;
     for (int32_t id : P->reqs[r].table) {
-      // with per-head exclusion, a page with no live slot for a head is not read for it
+      // with per-head exclusion (or after a grouped decode), a page with no
+      // live slot for a head is not read for it
       int64_t heads = hkv;
       if (!P->hdead.empty())
         for (int h = 0; h < hkv; ++h) heads -= (P->live[id] & ~P->hdead[(size_t)id * hkv + h]) == 0u ? 1 : 0;
+      else if (P->stat_skip_dead && P->live[id] == 0u)
+        heads = 0;
       bytes += is_int2(P, id) ? (int64_t)kInt2Block * heads : (int64_t)P->fill[id] * 160 * heads;
       bytes += 8;
       ++pages;
@@ -1466,3 +1540,255 @@ kv_status_t kv_last_decode_stats(kv_pool_t* P, int64_t* kv_bytes, int32_t* n_spl
 }
 
 }  // extern "C"
+
+namespace {
+
+// Grouped split planner (Tangram, head groups with their own budgets: every
+// group is a pool of its own, and one scan walks them all).  The units of all
+// pools in output order: batch row, then kv head across the pools, pool 0's
+// kv heads first; a unit's pages are its pool's table for the row's request.
+// The cut is plan_decode's: every worker gets about the same cost.  The
+// grouped scan skips every page with no live slot for the unit's kv head, so
+// a full such page costs nothing, and a unit's leading ones are left out of
+// its splits (the plan is rebuilt when a table's entries are erased or
+// moved, so those positions keep holding dead pages).
+struct GroupHostPlan {
+  std::vector<Unit> units;
+  std::vector<Split> splits;
+  std::vector<int32_t> wsplit;
+  int64_t pages = 0;
+};
+
+void plan_decode_groups(kv_pool* const* pools, int n_pools, const int32_t* req_ids, int32_t batch, int64_t n_workers,
+                        int64_t min_pages, PageCost pc, GroupHostPlan& out) {
+  int thkv = 0;
+  for (int p = 0; p < n_pools; ++p) thkv += pools[p]->cfg.num_kv_heads;
+  const size_t nu = (size_t)batch * thkv;
+  std::vector<int32_t> u_pool(nu), u_head(nu), u_req(nu), u_npos(nu), u_lead(nu);
+  for (int32_t b = 0; b < batch; ++b) {
+    size_t u = (size_t)b * thkv;
+    for (int p = 0; p < n_pools; ++p) {
+      const kv_pool* P = pools[p];
+      const int32_t r = req_ids[(size_t)p * batch + b];
+      const auto& tb = P->reqs[r].table;
+      int32_t lead = 0;
+      for (int32_t id : tb) lead += id < P->cfg.n_int2_pages ? 1 : 0;
+      for (int h = 0; h < P->cfg.num_kv_heads; ++h, ++u) {
+        u_pool[u] = p;
+        u_head[u] = h;
+        u_req[u] = r;
+        u_npos[u] = (int32_t)tb.size();
+        u_lead[u] = lead;
+      }
+    }
+  }
+  // per unit: the cost of its first i pages in scan order
+  std::vector<int64_t> off(nu + 1, 0);
+  for (size_t u = 0; u < nu; ++u) off[u + 1] = off[u] + u_npos[u] + 1;
+  std::vector<double> pre((size_t)off[nu]);
+  double total = 0.0;
+  int64_t pages = 0;
+  for (size_t u = 0; u < nu; ++u) {
+    const kv_pool* P = pools[u_pool[u]];
+    const auto& tb = P->reqs[u_req[u]].table;
+    const int hkv = P->cfg.num_kv_heads, h = u_head[u];
+    const int64_t n2 = P->cfg.n_int2_pages;
+    double* pb = &pre[(size_t)off[u]];
+    ScanOrder so;
+    so.start(0, u_npos[u], u_lead[u]);
+    pb[0] = 0.0;
+    for (int32_t i = 0; i < u_npos[u]; ++i) {
+      const int32_t id = tb[so.next()];
+      const uint32_t hd = P->hdead.empty() ? 0u : P->hdead[(size_t)id * hkv + h];
+      const bool dead = P->fill[id] == kPage && (P->live[id] & ~hd) == 0u;
+      pb[i + 1] = pb[i] + (dead ? 0.0 : (id < n2 ? pc.int2 : pc.int4));
+    }
+    total += pb[u_npos[u]];
+    pages += u_npos[u];
+  }
+  out.pages = pages;
+  const int64_t n = std::max<int64_t>(1, std::min<int64_t>(n_workers, pages / std::max<int64_t>(1, min_pages)));
+  out.units.assign(nu, Unit{});
+  out.splits.clear();
+  out.wsplit.assign((size_t)n + 1, 0);
+  const double scale = total > 0.0 ? (double)n / total : 0.0;
+  auto worker = [&](double c) { return std::min<int64_t>(n - 1, (int64_t)(c * scale)); };
+  int64_t cur = 0;   // worker receiving the current split
+  double U = 0.0;    // cost before the current unit
+  for (size_t u = 0; u < nu; ++u) {
+    const double* pb = &pre[(size_t)off[u]];
+    const int32_t npos = u_npos[u];
+    Unit& un = out.units[u];
+    un.b = (int32_t)(u / thkv);
+    un.req = u_req[u];
+    un.kvh = (int32_t)(u % thkv);
+    un.pad = u_pool[u];
+    un.split_begin = (int32_t)out.splits.size();
+    auto split = [&](int32_t b0, int32_t e0) {
+      return Split{(int32_t)u, b0, e0, u_req[u], npos, u_lead[u], {u_pool[u], u_head[u]}};
+    };
+    int32_t i = 0;
+    while (i < npos && pb[i + 1] == pb[i]) ++i;
+    if (i == npos && npos > 0) {
+      // nothing live: one empty split, open-ended so that later pages are scanned
+      const int64_t j = worker(U + pb[npos]);
+      while (cur < j) out.wsplit[(size_t)++cur] = (int32_t)out.splits.size();
+      out.splits.push_back(split(npos, npos));
+    }
+    while (i < npos) {
+      const int64_t j = worker(U + pb[i]);
+      while (cur < j) out.wsplit[(size_t)++cur] = (int32_t)out.splits.size();
+      int32_t lo = i + 1, hi = npos;
+      while (lo < hi) {
+        const int32_t mid = lo + (hi - lo) / 2;
+        if (worker(U + pb[mid]) > j) hi = mid;
+        else lo = mid + 1;
+      }
+      out.splits.push_back(split(i, lo));
+      i = lo;
+    }
+    U += pb[npos];
+    un.n_splits = (int32_t)out.splits.size() - un.split_begin;
+    if (un.n_splits > 0) out.splits.back().page_end = -1;   // open-ended: appended pages are scanned
+    un.fp_begin = (int32_t)out.splits.size();
+    un.n_fp_splits = 0;
+  }
+  while (cur < n) out.wsplit[(size_t)++cur] = (int32_t)out.splits.size();
+}
+
+bool same_pools(const std::vector<GroupPool>& a, const std::vector<GroupPool>& b) {
+  return a.size() == b.size() && (a.empty() || std::memcmp(a.data(), b.data(), a.size() * sizeof(GroupPool)) == 0);
+}
+
+// The grouped plan and the pools' descriptors, cached in the first pool under
+// the rules of build_plan (same pools, rows and requests; no table shrunk,
+// erased from or reordered; growth within the slack).
+kv_status_t build_group_plan(kv_pool* const* pools, int n_pools, const int32_t* req_ids, int32_t batch, int32_t hq,
+                             const std::vector<GroupPool>& gp, cudaStream_t s) {
+  kv_pool* P = pools[0];
+  const size_t nr = (size_t)n_pools * batch;
+  bool same = P->gplan_hq == hq && P->gplan_req.size() == nr && P->gplan_owner.size() == (size_t)n_pools &&
+              same_pools(P->gplan_pools, gp);
+  for (int p = 0; same && p < n_pools; ++p) same = P->gplan_owner[p] == pools[p]->serial;
+  for (size_t k = 0; same && k < nr; ++k) {
+    const kv_pool* Q = pools[k / batch];
+    const int32_t r = req_ids[k];
+    const int32_t len = (int32_t)Q->reqs[r].table.size(), len0 = P->gplan_len[k];
+    same = P->gplan_req[k] == r && len >= len0 && len - len0 <= P->gplan_slack && (len0 > 0 || len == 0) &&
+           P->gplan_ver[k] == Q->reqs[r].shape;
+  }
+  if (same) return KV_OK;
+  int thkv = 0;
+  for (int p = 0; p < n_pools; ++p) thkv += pools[p]->cfg.num_kv_heads;
+  const int g = hq / thkv;
+  GroupHostPlan hp;
+  plan_decode_groups(pools, n_pools, req_ids, batch, (int64_t)P->sm_count * decode_mma_workers_per_sm(g),
+                     kMinPagesPerWarp, mma_page_cost(g), hp);
+  Upload up;
+  const size_t ou = up.add(hp.units.data(), hp.units.size() * sizeof(Unit));
+  const size_t os = up.add(hp.splits.data(), hp.splits.size() * sizeof(Split));
+  const size_t ow = up.add(hp.wsplit.data(), hp.wsplit.size() * sizeof(int32_t));
+  const size_t og = up.add(gp.data(), gp.size() * sizeof(GroupPool));
+  kv_status_t st = ensure(P->gplan, up.size);
+  if (st != KV_OK) return st;
+  if ((st = h2d(P, P->gplan.ptr, up, s)) != KV_OK) return st;
+  P->gplan_units_off = ou;
+  P->gplan_splits_off = os;
+  P->gplan_wsplit_off = ow;
+  P->gplan_pools_off = og;
+  P->gplan_units = (int32_t)hp.units.size();
+  P->gplan_splits = (int32_t)hp.splits.size();
+  P->gplan_workers = (int32_t)hp.wsplit.size() - 1;
+  P->gplan_pools = gp;
+  P->gplan_owner.resize(n_pools);
+  for (int p = 0; p < n_pools; ++p) P->gplan_owner[p] = pools[p]->serial;
+  P->gplan_req.assign(req_ids, req_ids + nr);
+  P->gplan_len.resize(nr);
+  P->gplan_ver.resize(nr);
+  for (size_t k = 0; k < nr; ++k) {
+    const kv_pool* Q = pools[k / batch];
+    P->gplan_len[k] = (int32_t)Q->reqs[req_ids[k]].table.size();
+    P->gplan_ver[k] = Q->reqs[req_ids[k]].shape;
+  }
+  // growth a tail worker absorbs before the plan is rebuilt: 5% of a worker's
+  // share of the (page, kv head) pairs
+  P->gplan_slack = (int32_t)std::max<int64_t>(1, hp.pages / std::max<int64_t>(1, P->gplan_workers) / 20);
+  P->gplan_hq = hq;
+  return KV_OK;
+}
+
+}  // namespace
+
+extern "C" kv_status_t kv_decode_attn_groups(kv_pool_t* const* pools, int32_t n_pools, const void* q,
+                                             const int32_t* req_ids, int32_t batch, int32_t hq, float softmax_scale,
+                                             float* out, void* stream) {
+  if (!pools || n_pools < 1 || n_pools > kMaxGroupPools)
+    return fail(KV_ERR_INVALID_ARG, "kv_decode_attn_groups: need 1 to %d pools", kMaxGroupPools);
+  if (!q || !out || !req_ids || batch < 1)
+    return fail(KV_ERR_INVALID_ARG, "kv_decode_attn_groups: null pointer or batch < 1");
+  int thkv = 0;
+  for (int p = 0; p < n_pools; ++p) {
+    if (!pools[p]) return fail(KV_ERR_INVALID_ARG, "kv_decode_attn_groups: pool %d is null", p);
+    for (int o = 0; o < p; ++o)
+      if (pools[o] == pools[p]) return fail(KV_ERR_INVALID_ARG, "kv_decode_attn_groups: pool %d is listed twice", p);
+    if (pools[p]->cfg.device != pools[0]->cfg.device)
+      return fail(KV_ERR_INVALID_ARG, "kv_decode_attn_groups: the pools must be on one device");
+    thkv += pools[p]->cfg.num_kv_heads;
+  }
+  if (hq < thkv || hq % thkv != 0 || hq / thkv > 8)
+    return fail(KV_ERR_INVALID_ARG,
+                "kv_decode_attn_groups: num_q_heads %d must be a multiple of the pools' %d kv heads with ratio <= 8",
+                hq, thkv);
+  if (!std::isfinite(softmax_scale))
+    return fail(KV_ERR_INVALID_ARG, "kv_decode_attn_groups: softmax_scale must be finite");
+  for (int p = 0; p < n_pools; ++p)
+    for (int32_t b = 0; b < batch; ++b) {
+      const int32_t r = req_ids[(size_t)p * batch + b];
+      if (!req_ok(pools[p], r))
+        return fail(KV_ERR_INVALID_ARG, "kv_decode_attn_groups: request %d of pool %d not open", r, p);
+      if (!pools[p]->n_fp.empty() && pools[p]->n_fp[r] > 0)
+        return fail(KV_ERR_INVALID_ARG,
+                    "kv_decode_attn_groups: request %d of pool %d holds full-precision tokens (not read here)", r, p);
+    }
+  kv_pool* P = pools[0];
+  DeviceGuard dg(P->cfg.device);
+  cudaStream_t s = (cudaStream_t)stream;
+  kv_status_t st;
+  for (int p = 0; p < n_pools; ++p)
+    if ((st = order_after_previous(pools[p], s)) != KV_OK) return st;
+  std::vector<GroupPool> gp((size_t)n_pools);
+  for (int p = 0; p < n_pools; ++p) {
+    const kv_pool* Q = pools[p];
+    gp[p] = GroupPool{(const uint8_t*)Q->d_pool, Q->int4_offset, (int64_t)Q->cfg.n_int2_pages,
+                      (const Entry*)Q->d_table, (const int32_t*)Q->d_ntab,
+                      Q->hdead.empty() ? nullptr : (const uint32_t*)Q->d_hdead, Q->d_status + 1,
+                      Q->cfg.num_kv_heads, Q->cfg.max_pages_per_request, n_pools, 0};
+  }
+  if ((st = build_group_plan(pools, n_pools, req_ids, batch, hq, gp, s)) != KV_OK) return st;
+  const int g = hq / thkv;
+  if ((st = ensure(P->partials, (size_t)std::max(P->gplan_splits, 1) * g * (kHeadDim + 4) * sizeof(float))) != KV_OK)
+    return st;
+  if ((st = ensure(P->frags, (size_t)std::max(P->gplan_units, 1) * decode_mma_frag_bytes())) != KV_OK) return st;
+  const uint8_t* base = (const uint8_t*)P->gplan.ptr;
+  const float scale_log2 = softmax_scale * 1.4426950408889634f;
+  const bool rec = P->timing && (P->timing_seen++ % P->timing_every) == 0;
+  cudaEvent_t* tv = rec ? &P->tev[3 * (size_t)(P->timed_calls % kTimingRing)] : nullptr;
+  if (tv) KV_CUDA(cudaEventRecord(tv[0], s));
+  P->merge_event = tv ? tv[1] : nullptr;
+  P->fp_pending = FpLaunch{};
+  KV_CUDA(launch_decode_mma(P, q, hq, scale_log2, (const Unit*)(base + P->gplan_units_off), P->gplan_units,
+                            (const Split*)(base + P->gplan_splits_off), (const int32_t*)(base + P->gplan_wsplit_off),
+                            P->gplan_workers, P->frags.ptr, (float*)P->partials.ptr, out, s,
+                            (const GroupPool*)(base + P->gplan_pools_off), thkv));
+  if (tv) {
+    KV_CUDA(cudaEventRecord(tv[2], s));
+    ++P->timed_calls;
+  }
+  P->merge_event = nullptr;
+  for (int p = 0; p < n_pools; ++p) {
+    pools[p]->stat_req.assign(req_ids + (size_t)p * batch, req_ids + (size_t)(p + 1) * batch);
+    pools[p]->stat_hq = pools[p]->cfg.num_kv_heads * g;
+    pools[p]->stat_skip_dead = true;
+  }
+  return KV_OK;
+}
