@@ -346,6 +346,193 @@ def run_prefill(args):
     return 0
 
 
+def load_workload(args, total_steps):
+    import kvsynth
+    w = kvsynth.make_workload(args.config, steps=total_steps, n_req=args.requests or None)
+    if args.requests:
+        w.name = f"{w.name}-first{args.requests}"
+    if args.q_heads:
+        if args.q_heads % w.num_kv_heads or not 1 <= args.q_heads // w.num_kv_heads <= 8:
+            raise SystemExit("--q-heads must be 1..8 times the workload's kv heads")
+        w.name = f"{w.name}-q{args.q_heads}"
+        w.num_q_heads = args.q_heads
+    return w
+
+
+def run_head_groups(args):
+    """Head groups in pools of their own (Tangram: head groups keep different
+    amounts of context).  The workload's kv heads are cut into N equal
+    groups, one pool each, fed the group's rows of every token; group j keeps
+    the most recent (j+1)/N of every prompt, evicts the older positions and
+    drops its dead pages, so it holds only its own pages.  A step appends the
+    new token to every pool, reorders, and decodes through one grouped call
+    (one tensor-core scan over all pools).  The budgets are those of
+    --ragged-heads when N = num_kv_heads, there held in one shared pool."""
+    import torch
+    import kvsynth
+    import mixed_precision_kv_gb300 as kvq
+    from mixed_precision_kv_gb300.workload import GPUWorkload
+
+    ws, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    clk = ClockSampler(local).start()
+    e2e_steps = max(args.steps // 4, 10)
+    total_steps = args.warmup + args.steps + 3 + e2e_steps
+    w = load_workload(args, total_steps)
+    H, N = w.num_kv_heads, args.head_groups
+    if N < 1 or N > 8 or H % N:
+        raise SystemExit("--head-groups must divide the workload's kv heads, at most 8 groups")
+    hg = H // N
+    lo = [j * hg for j in range(N + 1)]
+    gw = GPUWorkload(w, device=local, steps=total_steps, make_pool=False)
+    n2, n4, max_tab = gw.sizes
+    pools = [kvq.KVPool(hg, n2, n4, len(w.requests), max_tab, device=local) for _ in range(N)]
+    rids = [np.array([p.open() for _ in w.requests], np.int32) for p in pools]
+    B, Hq = len(w.requests), w.num_q_heads
+    for r, spec in enumerate(w.requests):
+        for t0 in range(0, spec.n_prefill, gw.chunk):
+            n = min(gw.chunk, spec.n_prefill - t0)
+            k, v = gw.kv_rows(r, t0, n)
+            for j, p in enumerate(pools):
+                p.append(k[:, lo[j]:lo[j + 1]].contiguous(), v[:, lo[j]:lo[j + 1]].contiguous(),
+                         np.full(n, rids[j][r], np.int32), gw.bits[r][t0:t0 + n])
+    keep = [(j + 1) / N for j in range(N)]
+    for r, spec in enumerate(w.requests):
+        n = spec.n_prefill
+        for j, p in enumerate(pools):
+            pos = np.union1d(spec.evict, np.arange(n - int(round(n * keep[j])), dtype=np.int64))
+            if pos.size:
+                p.evict(np.full(pos.size, rids[j][r], np.int32), pos)
+    blocks_before = sum(p.info(int(x))[0] * hg for p, rs in zip(pools, rids) for x in rs)
+    for j, p in enumerate(pools):
+        p.reorder(rids[j])
+        p.drop_dead_pages(rids[j])
+        p.sync()
+    blocks_after = sum(p.info(int(x))[0] * hg for p, rs in zip(pools, rids) for x in rs)
+    dev = torch.device("cuda", local)
+    kf = torch.empty((total_steps, B, H, 128), dtype=torch.bfloat16, device=dev)
+    vf = torch.empty_like(kf)
+    qs = torch.empty((total_steps, B, Hq, 128), dtype=torch.bfloat16, device=dev)
+    bits = np.zeros((total_steps, B), np.uint8)
+    for s in range(total_steps):
+        for r in range(B):
+            pos = w.requests[r].n_prefill + s
+            kvsynth.fill_bf16_dev(kf[s, r].data_ptr(), 1, H, 128, w.seed, kvsynth.TENSOR_K, w.requests[r].stream,
+                                  pos, gw.chan.data_ptr())
+            kvsynth.fill_bf16_dev(vf[s, r].data_ptr(), 1, H, 128, w.seed, kvsynth.TENSOR_V, w.requests[r].stream,
+                                  pos)
+            bits[s, r] = gw.bits[r][pos]
+        kvsynth.fill_bf16_dev(qs[s].data_ptr(), B, Hq, 128, w.seed, kvsynth.TENSOR_Q, s)
+    ks = [kf[:, :, lo[j]:lo[j + 1]].contiguous() for j in range(N)]   # each group's rows, resident per step
+    vs = [vf[:, :, lo[j]:lo[j + 1]].contiguous() for j in range(N)]
+    del kf, vf
+    rid_mat = np.stack(rids)
+    out = torch.empty((B, Hq, 128), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(s, kk=None, vv=None, q=None):
+        for j, p in enumerate(pools):
+            p.append(ks[j][s] if kk is None else kk[j], vs[j][s] if vv is None else vv[j], rids[j], bits[s])
+            p.reorder(rids[j])
+        return kvq.KVPool.decode_groups(pools, qs[s] if q is None else q, rid_mat, w.softmax_scale, out=out)
+
+    def kv_bytes():
+        return sum(p.last_decode_stats()["kv_bytes"] for p in pools)
+
+    for s in range(args.warmup):
+        step(s)
+    for p in pools:
+        p.sync()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    s0 = args.warmup
+    kv_first = kv_bytes()
+    launches0 = sum(p.launch_count() for p in pools)
+    timing_every = 1 if args.steps < 200 else 8
+    pools[0].decode_timing(True, every=timing_every)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for i in range(args.steps):
+        step(s0 + i)
+    end.record(stream)
+    torch.cuda.synchronize()
+    clk.stop()
+    if dist:
+        dist.barrier()
+    kv_last = kv_bytes()
+    launches = sum(p.launch_count() for p in pools) - launches0
+    n_timed, scan_ms, dec_ms = pools[0].decode_timing(False)
+    for p in pools:
+        p.sync()
+    t_ms = reduce_max_time(start.elapsed_time(end), dist, dev)
+    step_bytes = 0.5 * (kv_first + kv_last)
+    value = job_throughput(step_bytes, args.steps, ws, t_ms)
+    achieved = step_bytes / (scan_ms / 1e3) / 1e9
+    peak, peak_kind = measured_peak()
+
+    # end to end: one pinned host buffer per step (every group's K, then V, then q)
+    s_e = s0 + args.steps + 3
+    nk = B * hg * 128
+    nq = qs[0].numel()
+    parts = [x[s_e:s_e + e2e_steps].reshape(e2e_steps, nk) for x in ks + vs]
+    hbuf = torch.cat(parts + [qs[s_e:s_e + e2e_steps].reshape(e2e_steps, nq)], dim=1).cpu().pin_memory()
+    hout = torch.empty((B, Hq, 128), dtype=torch.float32).pin_memory()
+    dbuf = torch.empty((2 * N * nk + nq,), dtype=torch.bfloat16, device=dev)
+    dk = [dbuf[j * nk:(j + 1) * nk].view(B, hg, 128) for j in range(N)]
+    dv = [dbuf[(N + j) * nk:(N + j + 1) * nk].view(B, hg, 128) for j in range(N)]
+    dq = dbuf[2 * N * nk:].view(qs[0].shape)
+    for i in range(3):
+        step(s0 + args.steps + i)
+    torch.cuda.synchronize()
+    e_first = kv_bytes()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(e2e_steps):
+        dbuf.copy_(hbuf[i], non_blocking=True)
+        step(s_e + i, dk, dv, dq)
+        hout.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e_last = kv_bytes()
+    e_ms = reduce_max_time(e0.elapsed_time(e1), dist, dev)
+    e2e_val = job_throughput(0.5 * (e_first + e_last), e2e_steps, ws, e_ms)
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": t_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "u4/u2 codes, f16 meta, f32 accum", "data": "synthetic",
+            "config": {"workload": f"{w.name}+head-groups{N}", "batch": B, "num_q_heads": Hq, "num_kv_heads": H,
+                       "head_dim": 128, "context": context_desc(w), "page_tokens": 32, "budget_bits": budget_desc(w),
+                       "decode_impl": "mma (grouped scan)",
+                       "l2": "inputs larger than L2 (%.0f MB per step)" % (step_bytes / 1e6),
+                       "us_per_layer_step": t_ms / args.steps * 1e3, "decode_us": dec_ms * 1e3,
+                       "scan_us": scan_ms * 1e3, "decode_calls_timed": n_timed,
+                       "pct_of_8000_gbs": value / ws / 8000 * 100},
+            "head_groups": {"groups": N, "kv_heads_per_group": hg, "keep_fraction_of_prompt": keep,
+                            "page_blocks_before_drop": blocks_before, "page_blocks_after_drop": blocks_after,
+                            "kv_bytes_counted": "page blocks each group reads (its kept pages), table entries, "
+                                                "q and out"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": None, "peak_source": peak_kind,
+                         "kernel": "decode_mma_kernel (grouped split scan); CUDA events recorded by the library "
+                                   "on the launch stream around %s launch of the timed region"
+                                   % ("every" if timing_every == 1 else "every 8th")},
+            "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": dbuf.numel() * 2,
+                    "d2h_bytes_per_step": hout.numel() * 4},
+            "gpu_launches": launches,
+            "clocks": clk.summary()}
+    if rank == 0:
+        print(json.dumps(line))
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -367,6 +554,9 @@ def main():
     ap.add_argument("--ragged-heads", action="store_true",
                     help="per-head budgets: kv head h keeps the most recent (h+1)/num_kv_heads of every prompt; "
                          "the older positions are excluded for that head only (whole pages are skipped)")
+    ap.add_argument("--head-groups", type=int, default=0,
+                    help="N > 0: the kv heads in N pools of their own; group j keeps the most recent (j+1)/N of "
+                         "every prompt and drops its dead pages; one grouped decode per step")
     ap.add_argument("--mode", default="decode", choices=["decode", "prefill"],
                     help="decode: the decode-step line (default); prefill: bulk quantization of the workload's "
                          "prompts through kv_append_quant")
@@ -375,6 +565,8 @@ def main():
         return run_reference(args)
     if args.mode == "prefill":
         return run_prefill(args)
+    if args.head_groups:
+        return run_head_groups(args)
 
     import torch
     import kvsynth
@@ -394,14 +586,7 @@ def main():
     total_steps = args.warmup + args.steps + 3 + e2e_steps
     SEG_W = SEG_WS = 128   # HyQuant window W and staging capacity W_s
     extra = SEG_W if args.segments else 0   # the frozen window is quantized again by the first flush
-    w = kvsynth.make_workload(args.config, steps=total_steps, n_req=args.requests or None)
-    if args.requests:
-        w.name = f"{w.name}-first{args.requests}"
-    if args.q_heads:
-        if args.q_heads % w.num_kv_heads or not 1 <= args.q_heads // w.num_kv_heads <= 8:
-            raise SystemExit("--q-heads must be 1..8 times the workload's kv heads")
-        w.name = f"{w.name}-q{args.q_heads}"
-        w.num_q_heads = args.q_heads
+    w = load_workload(args, total_steps)
     gw = GPUWorkload(w, device=local, steps=total_steps, extra_tokens=extra)
     gw.pool.set_decode_impl({"auto": 0, "simt": 1, "mma": 2}[args.decode_impl])
     gw.prefill()

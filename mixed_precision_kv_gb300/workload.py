@@ -45,16 +45,19 @@ def pool_size(w: Workload, bits_list, chunk: int, steps: int, extra: int = 0):
 
 class GPUWorkload:
     def __init__(self, w: Workload, device: int = 0, chunk: int = 16384, steps: int | None = None,
-                 extra_tokens: int = 0):
+                 extra_tokens: int = 0, make_pool: bool = True):
         import torch
         self.w = w
         self.device = device
         self.chunk = chunk
         self.steps = w.steps if steps is None else steps
         self.bits = [request_bits(w, r) for r in range(len(w.requests))]
-        n2, n4, max_tab = pool_size(w, self.bits, chunk, self.steps, extra_tokens)
-        self.pool = KVPool(w.num_kv_heads, n2, n4, len(w.requests), max_tab, device=device)
-        self.rids = [self.pool.open() for _ in w.requests]
+        self.sizes = pool_size(w, self.bits, chunk, self.steps, extra_tokens)
+        n2, n4, max_tab = self.sizes
+        # make_pool=False: the caller builds its own pools (e.g. one per head
+        # group) and uses this object for the bit allocation and the rows
+        self.pool = KVPool(w.num_kv_heads, n2, n4, len(w.requests), max_tab, device=device) if make_pool else None
+        self.rids = [self.pool.open() for _ in w.requests] if make_pool else []
         self.dev = torch.device("cuda", device)
         self.chan = torch.from_numpy(w.k_chan_mult).to(self.dev)
         self.row = [None if s.row_mult is None else torch.from_numpy(s.row_mult).to(self.dev) for s in w.requests]
