@@ -48,7 +48,7 @@ def lib():
                 "orc_quant_group": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int, _P, _P, _P]),
                 "orc_dequant": (_F32, [ctypes.c_uint8, ctypes.c_uint16, ctypes.c_uint16]),
                 "orc_alloc_bits": (ctypes.c_int, [_P, _P, _P, ctypes.c_int, _I64, _I64, _P]),
-                "orc_pool_new": (_P, [ctypes.c_int, _I64, _I64, ctypes.c_int, ctypes.c_int, _P, ctypes.c_int]),
+                "orc_pool_new": (_P, [ctypes.c_int, _I64, _I64, _I64, ctypes.c_int, ctypes.c_int, _P, ctypes.c_int]),
                 "orc_pool_free": (None, [_P]),
                 "orc_request_open": (ctypes.c_int, [_P, _P]),
                 "orc_request_close": (ctypes.c_int, [_P, _I32]),
@@ -128,15 +128,17 @@ def alloc_bits(N, D2, D4, budget):
 
 
 class OraclePool:
-    """Model of the paged pool.  sel_heads: kv heads whose codes are kept."""
+    """Model of the paged pool.  sel_heads: kv heads whose codes are kept;
+    n_int3_pages: INT3 page ids [n2, n2 + n3), INT4 ids after them."""
 
     def __init__(self, num_kv_heads, n_int2_pages, n_int4_pages, max_requests, max_pages_per_request,
-                 sel_heads=None):
+                 sel_heads=None, n_int3_pages=0):
         self.hkv = num_kv_heads
         self.sel = list(range(num_kv_heads)) if sel_heads is None else list(sel_heads)
         sel = np.array(self.sel, dtype=np.int32)
         self.n2 = n_int2_pages
-        self.h = lib().orc_pool_new(num_kv_heads, n_int2_pages, n_int4_pages, max_requests,
+        self.n3 = n_int3_pages
+        self.h = lib().orc_pool_new(num_kv_heads, n_int2_pages, n_int3_pages, n_int4_pages, max_requests,
                                     max_pages_per_request, _p(sel), sel.size)
         if not self.h:
             raise OracleError(INVALID, "orc_pool_new")

@@ -1,6 +1,6 @@
 /*
  * kvq_oracle.cpp -- plain, slow CPU oracle for decode attention over a paged,
- * mixed INT2/INT4 quantized KV cache.
+ * mixed INT2/INT3/INT4 quantized KV cache.
  *
  * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the
  * benchmark's CPU-baseline leg may load this library.  It shares no code with
@@ -51,7 +51,8 @@
  *      after the call.  All 32 stored slots take part in the requantization;
  *      the live mask is carried over unchanged.
  *   R5 a page id is taken as the lowest free id of its class (INT2 ids
- *      [0, n2), INT4 ids [n2, n2 + n4)).
+ *      [0, n2), INT4 ids [n2, n2 + n4); with INT3 pages (R11) INT3 ids
+ *      [n2, n2 + n3) come between them).
  *   R6 the dead slot's logit is -1e4 after scaling and its V is 0; slots never
  *      written are not tokens and are skipped.
  *   R7 the greedy scan skips a tag that does not fit the budget and continues;
@@ -64,6 +65,17 @@
  *      tokens keeps the order of the rest.
  *   R9 a slot excluded for one head reads, for that head, as the sentinel
  *      dead slot of R6.
+ *   R11 INT3 pages.  The pages name three-bit integers only as a further width
+ *      the two-way INT2/INT4 choice could gain.  Read as a third width beside
+ *      them: K and V per token in groups of 32 channels exactly as INT4 (R2,
+ *      R3 with b = 3: codes 0..7, scale (max - min) / 7), on pages of their
+ *      own class (ids [n2, n2 + n3), INT4 ids [n2 + n3, n2 + n3 + n4)); a
+ *      request's INT3 tokens fill its own INT3 tail page in arrival order, as
+ *      INT4 tokens fill the INT4 tail; the phase-1 reorder sorts each table
+ *      stably by width (INT2, INT3, INT4 entries, each in table order); the
+ *      greedy allocation stays the pages' INT2/INT4 one (R7), and INT3 widths
+ *      come from the caller
+ *       [TriAxialKV, limitations and outlook: INT3 as a further width].
  *   R10 a full page none of whose 32 slots is live for any kv head may leave
  *      its request's table: the other entries keep their order and their
  *      pages do not move, its id returns to the free set, and the positions
@@ -202,7 +214,7 @@ struct HeadBlock {
 
 struct Page {
   int32_t id = -1;
-  bool int2 = false;
+  int bits = 4;                   // 2, 3 or 4 (the id's class)
   int fill = 0;
   uint32_t live = 0;
   std::vector<uint32_t> hdead;    // per kv head: slots excluded for that head only (R9)
@@ -214,7 +226,7 @@ struct Page {
 struct Req {
   bool open = false;
   std::vector<int32_t> table;
-  int32_t tail4 = -1, staging = -1;
+  int32_t tail4 = -1, tail3 = -1, staging = -1;
   std::vector<uint32_t> loc;      // token position -> page_id << 5 | slot
   int64_t n_fp = 0;               // full-precision tokens (R8)
   std::vector<uint16_t> fpk, fpv; // their bf16 bits [n_fp][n_sel][128]
@@ -223,9 +235,9 @@ struct Req {
 struct Pool {
   int hkv = 0;
   std::vector<int> sel;           // kv heads whose content is kept
-  int64_t n2 = 0, n4 = 0;
+  int64_t n2 = 0, n3 = 0, n4 = 0;
   int max_req = 0, max_pages = 0;
-  std::set<int32_t> free2, free4;
+  std::set<int32_t> free2, free3, free4;
   std::unordered_map<int32_t, Page> pages;
   std::vector<Req> reqs;
 };
@@ -240,12 +252,12 @@ int32_t take_lowest(std::set<int32_t>& s) {
   return id;
 }
 
-Page& new_page(Pool* P, bool int2, bool content) {
-  const int32_t id = take_lowest(int2 ? P->free2 : P->free4);
+Page& new_page(Pool* P, int bits, bool content) {
+  const int32_t id = take_lowest(bits == 2 ? P->free2 : (bits == 3 ? P->free3 : P->free4));
   Page& pg = P->pages[id];
   pg = Page();
   pg.id = id;
-  pg.int2 = int2;
+  pg.bits = bits;
   pg.hdead.assign((size_t)P->hkv, 0u);
   pg.content = content;
   if (content) {
@@ -255,8 +267,10 @@ Page& new_page(Pool* P, bool int2, bool content) {
   return pg;
 }
 
-// INT4 per-token quantization of one token into `slot` (key design 3).
-void write_int4_token(const Pool* P, Page& pg, int slot, const uint16_t* k, const uint16_t* v) {
+// Per-token quantization of one token into `slot` at the page's width, 4 or 3
+// (key design 3; R11).
+void write_token(const Pool* P, Page& pg, int slot, const uint16_t* k, const uint16_t* v) {
+  const int b = pg.bits;
   float xk[kD], xv[kD];
   for (size_t j = 0; j < P->sel.size(); ++j) {
     HeadBlock& hb = pg.heads[j];
@@ -265,9 +279,9 @@ void write_int4_token(const Pool* P, Page& pg, int slot, const uint16_t* k, cons
       xv[c] = bf16_to_f32(v[j * kD + c]);
     }
     for (int gr = 0; gr < kD / kG; ++gr) {
-      quant_group(xk + gr * kG, kG, 1, 4, hb.kc + slot * kD + gr * kG, 1,
+      quant_group(xk + gr * kG, kG, 1, b, hb.kc + slot * kD + gr * kG, 1,
                   &hb.km[(slot * 4 + gr) * 2], &hb.km[(slot * 4 + gr) * 2 + 1]);
-      quant_group(xv + gr * kG, kG, 1, 4, hb.vc + slot * kD + gr * kG, 1,
+      quant_group(xv + gr * kG, kG, 1, b, hb.vc + slot * kD + gr * kG, 1,
                   &hb.vm[(slot * 4 + gr) * 2], &hb.vm[(slot * 4 + gr) * 2 + 1]);
     }
   }
@@ -305,7 +319,9 @@ constexpr uint32_t kDropped = 0xFFFFFFFFu;   // loc entry of a position whose pa
 
 void free_id(Pool* P, int32_t id) {
   P->pages.erase(id);
-  if (id < P->n2) P->free2.insert(id); else P->free4.insert(id);
+  if (id < P->n2) P->free2.insert(id);
+  else if (id < P->n2 + P->n3) P->free3.insert(id);
+  else P->free4.insert(id);
 }
 
 }  // namespace
@@ -319,9 +335,9 @@ void orc_f32_to_f16(const float* x, uint16_t* out, int64_t n) {
 void orc_f16_to_f32(const uint16_t* x, float* out, int64_t n) {
   for (int64_t i = 0; i < n; ++i) out[i] = f16_to_f32(x[i]);
 }
-// One group of n values at `bits` (2 or 4).
+// One group of n values at `bits` (2, 3 or 4).
 int orc_quant_group(const float* x, int n, int bits, uint16_t* s, uint16_t* z, uint8_t* codes) {
-  if (n <= 0 || (bits != 2 && bits != 4)) return ORC_INVALID;
+  if (n <= 0 || bits < 2 || bits > 4) return ORC_INVALID;
   for (int i = 0; i < n; ++i) if (!in_range(x[i])) return ORC_RANGE;
   quant_group(x, n, 1, bits, codes, 1, s, z);
   return ORC_OK;
@@ -361,18 +377,20 @@ int orc_alloc_bits(const int64_t* N, const double* D2, const double* D4, int n_t
 // ---- pool --------------------------------------------------------------------
 // sel_heads: kv heads whose codes are materialized (n_sel of them); page ids,
 // tables, fills and live masks are modelled for every head regardless.
-void* orc_pool_new(int hkv, int64_t n2, int64_t n4, int max_req, int max_pages,
+void* orc_pool_new(int hkv, int64_t n2, int64_t n3, int64_t n4, int max_req, int max_pages,
                    const int* sel_heads, int n_sel) {
-  if (hkv <= 0 || n2 < 0 || n4 < 0 || max_req <= 0 || max_pages <= 0) return nullptr;
+  if (hkv <= 0 || n2 < 0 || n3 < 0 || n4 < 0 || max_req <= 0 || max_pages <= 0) return nullptr;
   Pool* P = new Pool();
   P->hkv = hkv;
   P->n2 = n2;
+  P->n3 = n3;
   P->n4 = n4;
   P->max_req = max_req;
   P->max_pages = max_pages;
   for (int i = 0; i < n_sel; ++i) P->sel.push_back(sel_heads[i]);
   for (int64_t i = 0; i < n2; ++i) P->free2.insert((int32_t)i);
-  for (int64_t i = 0; i < n4; ++i) P->free4.insert((int32_t)(n2 + i));
+  for (int64_t i = 0; i < n3; ++i) P->free3.insert((int32_t)(n2 + i));
+  for (int64_t i = 0; i < n4; ++i) P->free4.insert((int32_t)(n2 + n3 + i));
   P->reqs.resize(max_req);
   return P;
 }
@@ -399,7 +417,7 @@ int orc_request_close(void* h, int32_t id) {
   return ORC_OK;
 }
 
-// Append n tokens in arrival order (TriAxialKV key designs 3-4; readings R4, R5).
+// Append n tokens in arrival order (TriAxialKV key designs 3-4; readings R4, R5, R11).
 // k, v: bf16 bits [n][n_sel][128] for the selected heads, or both NULL to model
 // page ids and tables only.  Returns ORC_INVALID / ORC_RANGE / ORC_OOM with no
 // change to the pool.
@@ -410,21 +428,25 @@ int orc_append(void* h, const uint16_t* k, const uint16_t* v, const int32_t* req
   const size_t nsel = P->sel.size();
   for (int64_t t = 0; t < n; ++t) {
     if (req[t] < 0 || req[t] >= P->max_req || !P->reqs[req[t]].open) return ORC_INVALID;
-    if (bits[t] != 2 && bits[t] != 4) return ORC_INVALID;
+    if (bits[t] < 2 || bits[t] > 4) return ORC_INVALID;
   }
   if (content)
     for (int64_t i = 0; i < n * (int64_t)nsel * kD; ++i)
       if (!in_range(bf16_to_f32(k[i])) || !in_range(bf16_to_f32(v[i]))) return ORC_RANGE;
   // Dry run: count the pages this call takes and the table growth.
-  struct Sim { bool tail = false; int tailfill = 0; bool stag = false; int stagfill = 0; int64_t tablen = 0; };
+  struct Sim {
+    bool tail = false; int tailfill = 0; bool tail3 = false; int tail3fill = 0; bool stag = false; int stagfill = 0;
+    int64_t tablen = 0;
+  };
   std::unordered_map<int32_t, Sim> sim;
-  int64_t need4 = 0, need2 = 0;
+  int64_t need4 = 0, need3 = 0, need2 = 0;
   for (int64_t t = 0; t < n; ++t) {
     auto it = sim.find(req[t]);
     if (it == sim.end()) {
       const Req& R = P->reqs[req[t]];
       Sim s;
       if (R.tail4 >= 0) { s.tail = true; s.tailfill = P->pages.at(R.tail4).fill; }
+      if (R.tail3 >= 0) { s.tail3 = true; s.tail3fill = P->pages.at(R.tail3).fill; }
       if (R.staging >= 0) { s.stag = true; s.stagfill = P->pages.at(R.staging).fill; }
       s.tablen = (int64_t)R.table.size();
       it = sim.emplace(req[t], s).first;
@@ -433,13 +455,17 @@ int orc_append(void* h, const uint16_t* k, const uint16_t* v, const int32_t* req
     if (bits[t] == 4) {
       if (!s.tail || s.tailfill == kP) { ++need4; ++s.tablen; s.tail = true; s.tailfill = 0; }
       ++s.tailfill;
+    } else if (bits[t] == 3) {
+      if (!s.tail3 || s.tail3fill == kP) { ++need3; ++s.tablen; s.tail3 = true; s.tail3fill = 0; }
+      ++s.tail3fill;
     } else {
       if (!s.stag) { ++need4; ++s.tablen; s.stag = true; s.stagfill = 0; }
       if (++s.stagfill == kP) { ++need2; s.stag = false; }
     }
     if (s.tablen > P->max_pages) return ORC_OOM;
   }
-  if (need4 > (int64_t)P->free4.size() || need2 > (int64_t)P->free2.size()) return ORC_OOM;
+  if (need4 > (int64_t)P->free4.size() || need3 > (int64_t)P->free3.size() || need2 > (int64_t)P->free2.size())
+    return ORC_OOM;
 
   std::vector<int32_t> deferred;
   for (int64_t t = 0; t < n; ++t) {
@@ -447,9 +473,10 @@ int orc_append(void* h, const uint16_t* k, const uint16_t* v, const int32_t* req
     const int64_t pos = (int64_t)R.loc.size();
     const uint16_t* kt = content ? k + (size_t)t * nsel * kD : nullptr;
     const uint16_t* vt = content ? v + (size_t)t * nsel * kD : nullptr;
-    int32_t& cur = (bits[t] == 4) ? R.tail4 : R.staging;
+    // INT4 and INT2 tokens go to INT4 pages (the tail, the staging page); INT3 to the INT3 tail
+    int32_t& cur = bits[t] == 4 ? R.tail4 : (bits[t] == 3 ? R.tail3 : R.staging);
     if (cur < 0 || P->pages.at(cur).fill == kP) {
-      Page& pg = new_page(P, false, content);
+      Page& pg = new_page(P, bits[t] == 3 ? 3 : 4, content);
       cur = pg.id;
       R.table.push_back(pg.id);
     }
@@ -457,11 +484,11 @@ int orc_append(void* h, const uint16_t* k, const uint16_t* v, const int32_t* req
     const int slot = pg.fill++;
     pg.live |= 1u << slot;
     pg.pos[slot] = pos;
-    if (pg.content && content) write_int4_token(P, pg, slot, kt, vt);
+    if (pg.content && content) write_token(P, pg, slot, kt, vt);
     else if (pg.content) { pg.content = false; pg.heads.clear(); }
     R.loc.push_back(((uint32_t)pg.id << 5) | (uint32_t)slot);
     if (bits[t] == 2 && pg.fill == kP) {
-      Page& np = new_page(P, true, pg.content);
+      Page& np = new_page(P, 2, pg.content);
       repack_to_int2(P, pg, np);
       for (int s = 0; s < kP; ++s) R.loc[np.pos[s]] = ((uint32_t)np.id << 5) | (uint32_t)s;
       R.table.erase(std::find(R.table.begin(), R.table.end(), pg.id));
@@ -474,14 +501,16 @@ int orc_append(void* h, const uint16_t* k, const uint16_t* v, const int32_t* req
   return ORC_OK;
 }
 
-// INT2-first stable reorder of each listed request's table (TriAxialKV key design 4, phase 1).
+// INT2-first stable reorder of each listed request's table (TriAxialKV key
+// design 4, phase 1); with INT3 pages the table is sorted stably by width (R11).
 int orc_reorder(void* h, const int32_t* req, int n) {
   Pool* P = (Pool*)h;
   for (int i = 0; i < n; ++i)
     if (req[i] < 0 || req[i] >= P->max_req || !P->reqs[req[i]].open) return ORC_INVALID;
   for (int i = 0; i < n; ++i) {
     auto& tb = P->reqs[req[i]].table;
-    std::stable_partition(tb.begin(), tb.end(), [P](int32_t id) { return id < P->n2; });
+    std::stable_sort(tb.begin(), tb.end(),
+                     [P](int32_t a, int32_t b) { return P->pages.at(a).bits < P->pages.at(b).bits; });
   }
   return ORC_OK;
 }
@@ -524,6 +553,7 @@ int orc_drop_dead_pages(void* h, const int32_t* req, int n) {
       }
       for (int s = 0; s < kP; ++s) R.loc[(size_t)pg.pos[s]] = kDropped;
       if (R.tail4 == id) R.tail4 = -1;
+      if (R.tail3 == id) R.tail3 = -1;
       if (R.staging == id) R.staging = -1;
       free_id(P, id);
     }
@@ -596,7 +626,7 @@ int orc_export(void* h, int32_t id, int32_t* ids, uint8_t* is_int2, uint8_t* fil
   for (size_t i = 0; i < tb.size(); ++i) {
     const Page& pg = P->pages.at(tb[i]);
     ids[i] = pg.id;
-    is_int2[i] = pg.int2 ? 1 : 0;
+    is_int2[i] = pg.bits == 2 ? 1 : 0;
     fill[i] = (uint8_t)pg.fill;
     live[i] = pg.live;
     if (kc) {
@@ -662,7 +692,7 @@ int orc_decode(void* h, const uint16_t* q, const int32_t* req, int B, int Hq, fl
         if (lv) {
           double acc = 0.0;
           for (int c = 0; c < kD; ++c) {
-            const int mi = pg.int2 ? c * 2 : (s * 4 + c / kG) * 2;
+            const int mi = pg.bits == 2 ? c * 2 : (s * 4 + c / kG) * 2;
             acc += qd[c] * (double)dequant(hb.kc[s * kD + c], hb.km[mi], hb.km[mi + 1]);
           }
           l = (double)scale * acc;

@@ -42,17 +42,23 @@ def attention_from_export(ex, sel_index, q_row, scale):
     return (w[:, None] * np.array(vals)).sum(0) / w.sum()
 
 
-def quant_int4_tokens_np(x):
-    """Uniform per-token INT4 quantization, fp32 numpy arithmetic, G = 32.
-    x: fp32 [T][128] -> fp32 dequantized [T][128]."""
+def quant_tokens_np(x, bits):
+    """Uniform per-token asymmetric quantization at `bits` (2..4), fp32 numpy
+    arithmetic, G = 32.  x: fp32 [T][128] -> fp32 dequantized [T][128]."""
+    qmax = (1 << bits) - 1
     x = x.astype(np.float32).reshape(-1, 4, 32)
     mn = x.min(axis=2, keepdims=True)
     mx = x.max(axis=2, keepdims=True)
-    s32 = ((mx - mn).astype(np.float32) / np.float32(15)).astype(np.float32)
+    s32 = ((mx - mn).astype(np.float32) / np.float32(qmax)).astype(np.float32)
     sf = s32.astype(np.float16).astype(np.float32)
     zf = mn.astype(np.float16).astype(np.float32)
     with np.errstate(divide="ignore", invalid="ignore"):
         u = ((x - zf).astype(np.float32) / sf).astype(np.float32)
-    c = np.where(sf == 0, 0, np.clip(np.rint(u), 0, 15))
+    c = np.where(sf == 0, 0, np.clip(np.rint(u), 0, qmax))
     xh = (c.astype(np.float64) * sf.astype(np.float64) + zf.astype(np.float64)).astype(np.float32)
     return xh.reshape(-1, 128)
+
+
+def quant_int4_tokens_np(x):
+    """Uniform per-token INT4 quantization (quant_tokens_np at 4 bits)."""
+    return quant_tokens_np(x, 4)

@@ -92,7 +92,8 @@ def test_oom_and_invalid_leave_state_unchanged(orc):
     assert P.append(np.full(40, r), np.full(40, 4, np.uint8)) == orc.OK   # 2 INT4 pages
     before = P.export(r, content=False)
     assert P.append(np.full(64, r), np.full(64, 4, np.uint8)) == orc.OOM  # needs 2 more, 1 free
-    assert P.append(np.full(1, r), np.full(1, 3, np.uint8)) == orc.INVALID
+    assert P.append(np.full(1, r), np.full(1, 5, np.uint8)) == orc.INVALID
+    assert P.append(np.full(1, r), np.full(1, 3, np.uint8)) == orc.OOM       # no INT3 pages in this pool
     assert P.append(np.full(1, 1), np.full(1, 4, np.uint8)) == orc.INVALID  # request 1 not open
     after = P.export(r, content=False)
     for key in before:

@@ -32,7 +32,7 @@ def test_golden_cases(orc):
         assert (s, z) == (int(s_hex, 16), int(z_hex, 16)), name
         assert np.array_equal(c, want), name
         n += 1
-    assert n == 4
+    assert n == 6
 
 
 def _groups(rng, n_groups, n=32):
@@ -54,7 +54,7 @@ def _groups(rng, n_groups, n=32):
     return kinds
 
 
-@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("bits", [2, 3, 4])
 def test_codes_are_nearest_levels(orc, bits):
     """Brute force over all 2^b codes: the chosen level is the nearest one,
     up to the two fp32 roundings in (x - z) / s."""
@@ -77,7 +77,7 @@ def test_codes_are_nearest_levels(orc, bits):
         assert np.array_equal(xh, _dequant_exact(c, s, z))
 
 
-@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("bits", [2, 3, 4])
 def test_roundtrip_error_bound(orc, bits):
     """|x - x^| <= s/2 inside the covered range; outside it the excess is bounded
     by the binary16 rounding of the zero and of the scale."""
@@ -96,7 +96,7 @@ def test_roundtrip_error_bound(orc, bits):
         assert (np.abs(xd - xh) <= sf / 2 + excess + 2 * ulp + 1e-30).all()
 
 
-@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("bits", [2, 3, 4])
 def test_exact_grid_roundtrip(orc, bits):
     """Values on a grid z + c*s with binary16-exact s, z and codes 0 and 2^b-1
     present: the quantizer must return exactly that s, z and those codes."""
