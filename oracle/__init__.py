@@ -129,7 +129,7 @@ def alloc_bits(N, D2, D4, budget):
 
 class OraclePool:
     """Model of the paged pool.  sel_heads: kv heads whose codes are kept;
-    n_int3_pages: INT3 page ids [n2, n2 + n3), INT4 ids after them."""
+    n_int3_pages: INT3 page ids [n2 + n4, n2 + n4 + n3), after the INT4 ids."""
 
     def __init__(self, num_kv_heads, n_int2_pages, n_int4_pages, max_requests, max_pages_per_request,
                  sel_heads=None, n_int3_pages=0):

@@ -52,7 +52,7 @@
  *      the live mask is carried over unchanged.
  *   R5 a page id is taken as the lowest free id of its class (INT2 ids
  *      [0, n2), INT4 ids [n2, n2 + n4); with INT3 pages (R11) INT3 ids
- *      [n2, n2 + n3) come between them).
+ *      [n2 + n4, n2 + n4 + n3) follow them).
  *   R6 the dead slot's logit is -1e4 after scaling and its V is 0; slots never
  *      written are not tokens and are skipped.
  *   R7 the greedy scan skips a tag that does not fit the budget and continues;
@@ -69,7 +69,7 @@
  *      the two-way INT2/INT4 choice could gain.  Read as a third width beside
  *      them: K and V per token in groups of 32 channels exactly as INT4 (R2,
  *      R3 with b = 3: codes 0..7, scale (max - min) / 7), on pages of their
- *      own class (ids [n2, n2 + n3), INT4 ids [n2 + n3, n2 + n3 + n4)); a
+ *      own class (ids [n2 + n4, n2 + n4 + n3), after the INT4 ids); a
  *      request's INT3 tokens fill its own INT3 tail page in arrival order, as
  *      INT4 tokens fill the INT4 tail; the phase-1 reorder sorts each table
  *      stably by width (INT2, INT3, INT4 entries, each in table order); the
@@ -320,8 +320,8 @@ constexpr uint32_t kDropped = 0xFFFFFFFFu;   // loc entry of a position whose pa
 void free_id(Pool* P, int32_t id) {
   P->pages.erase(id);
   if (id < P->n2) P->free2.insert(id);
-  else if (id < P->n2 + P->n3) P->free3.insert(id);
-  else P->free4.insert(id);
+  else if (id < P->n2 + P->n4) P->free4.insert(id);
+  else P->free3.insert(id);
 }
 
 }  // namespace
@@ -389,8 +389,8 @@ void* orc_pool_new(int hkv, int64_t n2, int64_t n3, int64_t n4, int max_req, int
   P->max_pages = max_pages;
   for (int i = 0; i < n_sel; ++i) P->sel.push_back(sel_heads[i]);
   for (int64_t i = 0; i < n2; ++i) P->free2.insert((int32_t)i);
-  for (int64_t i = 0; i < n3; ++i) P->free3.insert((int32_t)(n2 + i));
-  for (int64_t i = 0; i < n4; ++i) P->free4.insert((int32_t)(n2 + n3 + i));
+  for (int64_t i = 0; i < n4; ++i) P->free4.insert((int32_t)(n2 + i));
+  for (int64_t i = 0; i < n3; ++i) P->free3.insert((int32_t)(n2 + n4 + i));
   P->reqs.resize(max_req);
   return P;
 }

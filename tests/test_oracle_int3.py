@@ -1,7 +1,7 @@
 """Oracle pins for INT3 pages, the further width the TriAxialKV page's
 limitations and outlook section names beside INT2 and INT4 (reading: K and V
-per token in 32-channel groups as INT4, codes 0..7; INT3 page ids between
-the INT2 and INT4 ranges; a request's INT3 tokens fill its own INT3 tail;
+per token in 32-channel groups as INT4, codes 0..7; INT3 page ids after the
+INT2 and INT4 ranges; a request's INT3 tokens fill its own INT3 tail;
 the phase-1 reorder sorts tables stably by width).
 
 What fixes the results here: closed forms of ids, fills and table order;
@@ -34,18 +34,19 @@ def test_routing_ids_and_width_sorted_reorder(orc):
     k, v = _kv(bits.size, 2, 0)
     assert P.append(np.full(bits.size, r), bits, k, v) == orc.OK
     ex = P.export(r, content=False)
-    # INT3 ids [4, 12): pages 4 (32 tokens) and 5 (8); INT4 ids from 12: the
-    # tail 12 (10) and the staging page 13, repacked into INT2 id 0 and freed
-    assert ex["ids"].tolist() == [4, 5, 12, 0]
+    # INT4 ids [4, 12), INT3 ids [12, 20): INT3 pages 12 (32 tokens) and 13
+    # (8); the INT4 tail 4 (10) and the staging page 5, repacked into INT2
+    # id 0 and freed
+    assert ex["ids"].tolist() == [12, 13, 4, 0]
     assert ex["fill"].tolist() == [32, 8, 10, 32]
     assert ex["is_int2"].tolist() == [0, 0, 0, 1]
     assert P.reorder([r]) == orc.OK
-    assert P.export(r, content=False)["ids"].tolist() == [0, 4, 5, 12]
-    # the next staging page takes the freed INT4 id 13; INT3 tokens continue in page 5
+    assert P.export(r, content=False)["ids"].tolist() == [0, 12, 13, 4]
+    # the next staging page takes the freed INT4 id 5; INT3 tokens continue in page 13
     k2, v2 = _kv(3, 2, 0, tok0=bits.size)
     assert P.append(np.full(3, r), np.array([2, 3, 4], np.uint8), k2, v2) == orc.OK
     ex = P.export(r, content=False)
-    assert ex["ids"].tolist() == [0, 4, 5, 12, 13]
+    assert ex["ids"].tolist() == [0, 12, 13, 4, 5]
     assert ex["fill"].tolist() == [32, 32, 9, 11, 1]
 
 
@@ -60,9 +61,11 @@ def test_reorder_is_a_stable_sort_by_width(orc):
         assert P.append(np.full(n, r), np.full(n, b, np.uint8), k, v) == orc.OK
         t0 += n
     before = P.export(r, content=False)["ids"].tolist()
-    assert before == [24, 8, 0, 25, 9, 1]
+    # INT4 ids [8, 24), INT3 ids [24, 40); each staging page (9, then 10) is
+    # repacked into INT2 (0, 1) and its id freed for the next INT4 page
+    assert before == [8, 24, 0, 9, 25, 1]
     assert P.reorder([r]) == orc.OK
-    assert P.export(r, content=False)["ids"].tolist() == [0, 1, 8, 9, 24, 25]
+    assert P.export(r, content=False)["ids"].tolist() == [0, 1, 24, 25, 8, 9]
 
 
 def _mixed3(n, rng):
@@ -84,7 +87,7 @@ def test_decode_brute_force_with_int3_pages(orc, n):
     out = P.decode(q, rids, SCALE)
     for b, r in enumerate(rids):
         ex = P.export(r)
-        i3 = (ex["ids"] >= 64) & (ex["ids"] < 128)                 # INT3 ids [n2, n2 + n3)
+        i3 = (ex["ids"] >= 128) & (ex["ids"] < 192)                # INT3 ids [n2 + n4, n2 + n4 + n3)
         assert i3.any() and int(ex["kc"][i3].max()) <= 7 and int(ex["vc"][i3].max()) <= 7
         for hq in range(8):
             ref = attention_from_export(ex, hq // 4, kvsynth.bf16_to_f32(q[b, hq]), SCALE)
@@ -102,7 +105,7 @@ def test_int3_codes_stay_below_eight(orc):
     k, v = _kv(96, 2, 3)
     assert P.append(np.full(96, r), np.full(96, 3, np.uint8), k, v) == orc.OK
     ex = P.export(r)
-    assert ex["ids"].tolist() == [4, 5, 6]
+    assert ex["ids"].tolist() == [8, 9, 10]
     assert int(ex["kc"].max()) == 7 and int(ex["vc"].max()) == 7
 
 
@@ -151,13 +154,13 @@ def test_int3_oom_invalid_drop_and_close(orc):
     assert P.info(r) == (0, 0)
     assert P.append(np.full(1, r), np.array([5], np.uint8), k[:1], v[:1]) == orc.INVALID
     assert P.append(np.full(64, r), np.full(64, 3, np.uint8), k[:64], v[:64]) == orc.OK
-    assert P.export(r, content=False)["ids"].tolist() == [2, 3]
+    assert P.export(r, content=False)["ids"].tolist() == [4, 5]                  # INT3 ids [4, 6)
     assert P.evict(np.full(32, r), np.arange(32)) == orc.OK
     assert P.drop_dead_pages([r]) == orc.OK
-    assert P.export(r, content=False)["ids"].tolist() == [3]
+    assert P.export(r, content=False)["ids"].tolist() == [5]
     s = P.open()
     assert P.append(np.full(1, s), np.array([3], np.uint8), k[:1], v[:1]) == orc.OK
-    assert P.export(s, content=False)["ids"].tolist() == [2]                     # the dropped id, lowest free
+    assert P.export(s, content=False)["ids"].tolist() == [4]                     # the dropped id, lowest free
     P.close_request(r)
     assert P.append(np.full(33, s), np.full(33, 3, np.uint8), k[:33], v[:33]) == orc.OK
-    assert P.export(s, content=False)["ids"].tolist() == [2, 3]
+    assert P.export(s, content=False)["ids"].tolist() == [4, 5]
