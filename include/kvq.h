@@ -85,11 +85,14 @@ typedef struct {
   int32_t max_requests;           /* request ids are [0, max_requests) */
   int32_t max_pages_per_request;  /* table capacity of one request */
   int32_t device;                 /* CUDA device ordinal */
+  int64_t n_int3_pages;           /* INT3 page ids are [n2 + n4, n2 + n4 + n_int3_pages); 0: none */
 } kv_pool_config_t;
 
 /* Create a pool: one device allocation holding the INT2 region followed by the
- * INT4 region (TriAxialKV key design 4), plus the device page tables.
- * out: host pointer receiving the handle. */
+ * INT4 region (TriAxialKV key design 4) and, with n_int3_pages > 0, the INT3
+ * region (TriAxialKV, limitations and outlook: INT3 as a further width; an
+ * INT3 block is 4096 bytes per page and kv head), plus the device page
+ * tables.  out: host pointer receiving the handle. */
 KVQ_API kv_status_t kv_pool_create(const kv_pool_config_t* cfg, kv_pool_t** out);
 
 /* Free everything the pool owns.  Synchronizes with the pool's device work. */
@@ -105,6 +108,8 @@ KVQ_API kv_status_t kv_request_close(kv_pool_t* pool, int32_t req_id);
  *   k, v     device, bf16 [n_tok][num_kv_heads][128], tokens in arrival order.
  *   req_ids  host, int32 [n_tok]: open request of each token.
  *   bits     host, uint8 [n_tok]: 4 -> the request's INT4 tail page;
+ *            3 -> the request's INT3 tail page (K and V per token in groups of
+ *            32 channels, codes 0..7, as INT4; needs n_int3_pages > 0);
  *            2 -> the request's INT4 staging page, which is requantized into a
  *            new INT2 page (K per channel, V per token) as soon as it holds 32
  *            tokens; that INT2 page is appended to the request's table.
@@ -115,7 +120,8 @@ KVQ_API kv_status_t kv_append_quant(kv_pool_t* pool, const void* k, const void* 
                             const uint8_t* bits, int64_t n_tok, void* stream);
 
 /* Phase-1 reorder (TriAxialKV key design 4): stable partition of each listed
- * request's table so INT2 entries precede INT4 entries.  req_ids: host [n_req]. */
+ * request's table so INT2 entries precede INT4 entries; with INT3 pages, a
+ * stable sort by width (INT2, INT3, INT4).  req_ids: host [n_req]. */
 KVQ_API kv_status_t kv_reorder_pages(kv_pool_t* pool, const int32_t* req_ids, int32_t n_req, void* stream);
 
 /* Layout-preserving eviction (IntentKV method 2): clear the live bit of each

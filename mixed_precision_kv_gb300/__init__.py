@@ -39,7 +39,7 @@ class KVConfig(ctypes.Structure):
     _fields_ = [("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("page_tokens", ctypes.c_int32),
                 ("group", ctypes.c_int32), ("n_int2_pages", ctypes.c_int64), ("n_int4_pages", ctypes.c_int64),
                 ("max_requests", ctypes.c_int32), ("max_pages_per_request", ctypes.c_int32),
-                ("device", ctypes.c_int32)]
+                ("device", ctypes.c_int32), ("n_int3_pages", ctypes.c_int64)]
 
 
 class KVError(RuntimeError):
@@ -147,16 +147,18 @@ def alloc_bits(N, D2, D4, budget):
 class KVPool:
     """A paged INT2/INT4 pool on one GPU (see include/kvq.h for every call's contract)."""
 
-    def __init__(self, num_kv_heads, n_int2_pages, n_int4_pages, max_requests, max_pages_per_request, device=0):
+    def __init__(self, num_kv_heads, n_int2_pages, n_int4_pages, max_requests, max_pages_per_request, device=0,
+                 n_int3_pages=0):
         L = load_library()
         cfg = KVConfig(num_kv_heads, HEAD_DIM, PAGE_TOKENS, GROUP, n_int2_pages, n_int4_pages, max_requests,
-                       max_pages_per_request, device)
+                       max_pages_per_request, device, n_int3_pages)
         h = _P()
         _check(L.kv_pool_create(ctypes.byref(cfg), ctypes.byref(h)), "kv_pool_create")
         self._h = h
         self._L = L
         self.num_kv_heads = num_kv_heads
         self.n_int2_pages = n_int2_pages
+        self.n_int3_pages = n_int3_pages
         self.device = device
 
     @property

@@ -65,6 +65,7 @@ constexpr uint32_t kN4 = 0x00F000F0u;   // 4-bit field at bit 4 of each half
 constexpr uint32_t kN6 = 0x03C003C0u;   // 4-bit field at bit 6 of each half
 constexpr uint32_t kC6 = 0x00C000C0u;   // 2-bit field at bit 6 of each half
 constexpr uint32_t kC8 = 0x03000300u;   // 2-bit field at bit 8 of each half
+constexpr uint32_t kB8 = 0x01000100u;   // 1-bit field at bit 8 of each half (INT3 code bit 2)
 constexpr float kCodeUnit = 262144.0f;  // 2^18: a field at bit 6 is code * 2^-18
 
 // One warp's shared memory: its copy ring and its P staging buffer.  Every
@@ -77,6 +78,7 @@ struct alignas(16) WarpSmem {
   const uint32_t* hdead;               // exclusion words (read from here at each refill, not kept in a register)
 };
 static_assert(sizeof(WarpSmem) % 16 == 0 && kStageBytes % 16 == 0, "stage buffers must stay 16-byte aligned");
+static_assert(kInt2Block <= kStageBytes && kInt3Block <= kStageBytes, "every block fits a stage");
 
 // q-side operands of one unit (batch row, kv head), built by frag_kernel.
 struct alignas(16) UnitFrag {
@@ -86,6 +88,7 @@ struct alignas(16) UnitFrag {
   float acol2[8], acol4[8];            // 2^(18 - E) * scale * log2(e) for INT2 / INT4 K pages
   float qzs[8];                        // 2^(-Ez) * scale * log2(e)
   uint32_t bz[8][4];                   // fp16 pairs: hi(Q0,Q1), hi(Q2,Q3), lo(Q0,Q1), lo(Q2,Q3) of scale*log2(e)*Q_{h,group}
+  uint4 bq3[4][32];                    // INT3 K q fragments (every field at bit 6)
 };
 static_assert(sizeof(UnitFrag) % 16 == 0, "unit fragments are copied as 16-byte words");
 
@@ -110,6 +113,14 @@ __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
   return d;
 }
 __device__ __forceinline__ uint32_t rotr8(uint32_t x) { return __funnelshift_r(x, x, 8); }
+// x << s, or x >> -s for s < 0 (s is a constant once the callers unroll)
+__device__ __forceinline__ uint32_t shl_s(uint32_t x, int s) { return s >= 0 ? x << s : x >> -s; }
+// An INT3 A register: the low plane shifted by sl puts the code's low bits at
+// bits 6..7 of both halves, the high plane shifted by sh puts bit 2 at bit 8:
+// the 3-bit code at bit 6, as an INT4 code at bit 6.
+__device__ __forceinline__ uint32_t i3reg(uint32_t lo, int sl, uint32_t hi, int sh) {
+  return (shl_s(lo, sl) & kC6) | (shl_s(hi, sh) & kB8);
+}
 // INT2 code word variants: variant jj puts two 2-bit fields of each half at
 // bits 6 and 8.  Scale/zero pair index (register j of the pair order) of the
 // field at bit 6 and at bit 8 of variant jj.
@@ -226,9 +237,10 @@ struct Cols {
   static constexpr int NH = kPair ? 1 : 2;
 };
 
-// ---- logits of one INT4 page: lg[m][e][hh] for token 16m + r + 8e and the
-// lane's head hh (log2 units, scale folded in)
-template <int G>
+// ---- logits of one INT4 (kI3: INT3) page: lg[m][e][hh] for token 16m + r + 8e
+// and the lane's head hh (log2 units, scale folded in).  An INT3 page has the
+// INT4 page's per-token groups and scale/zero; only its code words differ.
+template <int G, bool kI3 = false>
 __device__ __forceinline__ void qk_int4(const uint8_t* blk, const uint4* bq4, const uint32_t (&bz)[2],
                                         const float (&acol)[Cols<G>::NH], float (&lg)[2][2][Cols<G>::NH]) {
   constexpr bool kPair = Cols<G>::kPair;
@@ -242,18 +254,37 @@ __device__ __forceinline__ void qk_int4(const uint8_t* blk, const uint4* bq4, co
 #pragma unroll
   for (int m = 0; m < 2; ++m) {
     uint4 kw[2], km[2];
+    uint2 kl[2];
+    uint32_t kh[2];
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       const int t = 16 * m + r + 8 * e;
-      kw[e] = *reinterpret_cast<const uint4*>(blk + kI4KCodes + 64 * t + 16 * i);
-      km[e] = *reinterpret_cast<const uint4*>(blk + kI4KMeta + 16 * t);
+      if constexpr (kI3) {
+        kl[e] = *reinterpret_cast<const uint2*>(blk + kI3KCodes + 48 * t + 8 * i);
+        kh[e] = *reinterpret_cast<const uint32_t*>(blk + kI3KCodes + 48 * t + 32 + 4 * i);
+        km[e] = *reinterpret_cast<const uint4*>(blk + kI3KMeta + 16 * t);
+      } else {
+        kw[e] = *reinterpret_cast<const uint4*>(blk + kI4KCodes + 64 * t + 16 * i);
+        km[e] = *reinterpret_cast<const uint4*>(blk + kI4KMeta + 16 * t);
+      }
     }
     // Group gr's k-steps: nibbles 0/4 at p = 6, 1/5 at p = 4, then 2/6 and 3/7 at p = 6.
+    // INT3: channels n / n + 4 at p = 6 for every n (the q fragments carry no 2^2).
     auto group_mma = [&](float (&acc)[4], int gr) {
-      const uint32_t x0 = comp(kw[0], gr), x1 = comp(kw[1], gr);   // tokens r, r + 8
-      mma16816(acc, (x0 << 6) & kN6, (x1 << 6) & kN6, x0 & kN4, x1 & kN4, bq[4 * gr], bq[4 * gr + 1]);
-      mma16816(acc, (x0 >> 2) & kN6, (x1 >> 2) & kN6, (x0 >> 6) & kN6, (x1 >> 6) & kN6, bq[4 * gr + 2],
-               bq[4 * gr + 3]);
+      if constexpr (kI3) {
+        const uint32_t l0 = gr < 2 ? kl[0].x : kl[0].y, l1 = gr < 2 ? kl[1].x : kl[1].y;
+        const int o = 8 * (gr & 1);
+        auto reg = [&](uint32_t l, uint32_t h, int n) { return i3reg(l, 6 - o - 2 * n, h, 8 - 4 * gr - n); };
+        mma16816(acc, reg(l0, kh[0], 0), reg(l1, kh[1], 0), reg(l0, kh[0], 1), reg(l1, kh[1], 1), bq[4 * gr],
+                 bq[4 * gr + 1]);
+        mma16816(acc, reg(l0, kh[0], 2), reg(l1, kh[1], 2), reg(l0, kh[0], 3), reg(l1, kh[1], 3), bq[4 * gr + 2],
+                 bq[4 * gr + 3]);
+      } else {
+        const uint32_t x0 = comp(kw[0], gr), x1 = comp(kw[1], gr);   // tokens r, r + 8
+        mma16816(acc, (x0 << 6) & kN6, (x1 << 6) & kN6, x0 & kN4, x1 & kN4, bq[4 * gr], bq[4 * gr + 1]);
+        mma16816(acc, (x0 >> 2) & kN6, (x1 >> 2) & kN6, (x0 >> 6) & kN6, (x1 >> 6) & kN6, bq[4 * gr + 2],
+                 bq[4 * gr + 3]);
+      }
     };
     // zero term sum_g zero_tg * (scale log2e Q_g) by one mma: every lane feeds
     // (zero_0, zero_1) in k-slots 2i, 2i+1 and (zero_2, zero_3) in 2i+8, 2i+9;
@@ -423,8 +454,9 @@ __device__ __forceinline__ void qk_int2(const uint8_t* blk, const UnitFrag* __re
   }
 }
 
-// ---- online softmax update and P.V for one page (either width)
-template <int G, bool kInt2>
+// ---- online softmax update and P.V for one page (any width; kInt3: an INT3
+// page, read as an INT4 page with INT3 code words)
+template <int G, bool kInt2, bool kInt3 = false>
 __device__ __forceinline__ void softmax_pv(const uint8_t* blk, uint32_t live, float pscale,
                                            float (&lg)[2][2][Cols<G>::NH], const float (&zc)[Cols<G>::NH],
                                            float (&o)[8][4], float (&zv)[4],
@@ -432,7 +464,7 @@ __device__ __forceinline__ void softmax_pv(const uint8_t* blk, uint32_t live, fl
                                            float (*pbuf)[kPage]) {
   constexpr bool kPair = Cols<G>::kPair;
   constexpr int NH = Cols<G>::NH;
-  constexpr int vmeta = kInt2 ? kI2VMeta : kI4VMeta;
+  constexpr int vmeta = kInt2 ? kI2VMeta : (kInt3 ? kI3VMeta : kI4VMeta);
   const int lane = threadIdx.x & 31, r = lane >> 2, i = lane & 3;
   const bool full = live == 0xFFFFFFFFu;   // warp-uniform: no dead slot on this page
   if (!full) {
@@ -565,9 +597,15 @@ __device__ __forceinline__ void softmax_pv(const uint8_t* blk, uint32_t live, fl
       }
     }
     uint32_t wv[4];
+    uint32_t vh3 = 0u;
     if (kInt2) {
       const uint2 v2 = *reinterpret_cast<const uint2*>(blk + kI2VCodes + 16 * (32 * (gr >> 1) + 4 * r + i) + 8 * (gr & 1));
       wv[0] = v2.x; wv[1] = v2.y;
+    } else if (kInt3) {
+      const int X = 32 * gr + 4 * r + i;
+      const uint2 v3 = *reinterpret_cast<const uint2*>(blk + kI3VCodes + 8 * X);
+      wv[0] = v3.x; wv[1] = v3.y;
+      vh3 = *reinterpret_cast<const uint32_t*>(blk + kI3VHigh + 4 * X);
     } else {
       const uint4 v4 = *reinterpret_cast<const uint4*>(blk + kI4VCodes + 16 * (32 * gr + 4 * r + i));
       wv[0] = v4.x; wv[1] = v4.y; wv[2] = v4.z; wv[3] = v4.w;
@@ -583,6 +621,14 @@ __device__ __forceinline__ void softmax_pv(const uint8_t* blk, uint32_t live, fl
         a[0][2] = xl & kC6; a[0][3] = xr & kC6;    // slots (8i+1, 8i+5), p = 6
         a[1][0] = xl & kC8; a[1][1] = xr & kC8;    // slots (8i+2, 8i+6), p = 8
         a[1][2] = x & kC6; a[1][3] = xo & kC6;     // slots (8i+3, 8i+7), p = 6
+      } else if (kInt3) {
+        // channel 16m+r (e = 0) and 16m+r+8 (e = 1): slot 8i+k's low bits at
+        // 8e + 2k of plane word mm, bit 2 at 4(2mm + e) + k of the high word
+        const uint32_t x = wv[mm];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) a[k >> 1][2 * (k & 1) + e] = i3reg(x, 6 - 8 * e - 2 * k, vh3, 8 - 4 * (2 * mm + e) - k);
       } else {
         // slot 8i+k in nibble k; nibbles k and k+4 moved to bit 6 of each half
         const uint32_t w0 = wv[2 * mm], w1 = wv[2 * mm + 1];   // channels 16m+r, 16m+r+8
@@ -636,6 +682,17 @@ __device__ __forceinline__ uint32_t frag_q4(const FragSmem& S, int L, int x) {
   const int c = 32 * gr + 8 * i + 2 * hf + e;
   const int ex = S.eh4[h] + ((hf == 0 && e == 1) ? 2 : 0);
   return pack_h2(pow2_scale(S.qraw[h][c], ex), pow2_scale(S.qraw[h][c + 4], ex));
+}
+// INT3 K word x: the INT4 word's channels, every field at bit 6 (no 2^2)
+template <int G>
+__device__ __forceinline__ uint32_t frag_q3(const FragSmem& S, int L, int x) {
+  const int r = L >> 2, i = L & 3;
+  const int gr = x >> 2, hf = (x >> 1) & 1, e = x & 1;
+  if (Cols<G>::kPair && (gr & 1) != (r & 1)) return 0u;
+  const int h = Cols<G>::kPair ? (r >> 1) : r;
+  if (h >= G) return 0u;
+  const int c = 32 * gr + 8 * i + 2 * hf + e;
+  return pack_h2(pow2_scale(S.qraw[h][c], S.eh4[h]), pow2_scale(S.qraw[h][c + 4], S.eh4[h]));
 }
 
 // ---- per-unit q operands: one CTA of 8 warps per unit (batch row, kv head).
@@ -725,6 +782,7 @@ __global__ void __launch_bounds__(256) frag_kernel(const __nv_bfloat16* __restri
     uint32_t* f2 = reinterpret_cast<uint32_t*>(&S.f.bq2[0][0]);
     uint32_t* fn = reinterpret_cast<uint32_t*>(&S.f.bqn[0][0]);
     uint32_t* f4 = reinterpret_cast<uint32_t*>(&S.f.bq4[0][0]);
+    uint32_t* f3 = reinterpret_cast<uint32_t*>(&S.f.bq3[0][0]);
     for (int y = tid; y < 16 * 32; y += 256) {
       const int x = 4 * (y >> 7) + (y & 3), L = (y >> 2) & 31;
       const uint32_t v2 = frag_q2<G>(S, L, x);
@@ -732,6 +790,7 @@ __global__ void __launch_bounds__(256) frag_kernel(const __nv_bfloat16* __restri
       // negated copy for the exact hi/lo split (g <= 4: lo columns only)
       fn[y] = (!kPair || ((L >> 2) & 1)) ? (v2 ^ 0x80008000u) : 0u;
       f4[y] = frag_q4<G>(S, L, x);
+      f3[y] = frag_q3<G>(S, L, x);
     }
   }
   __syncthreads();
@@ -749,14 +808,16 @@ __global__ void __launch_bounds__(256) frag_kernel(const __nv_bfloat16* __restri
 // scan does not carry the extra pointer.  kMulti: the splits come from
 // several pools (head groups, each with its own pages and tables): a split
 // names its pool and its kv head within the pool, the page stream reads the
-// pool's addresses from gpools, and a page ticket carries its width.
-template <int G, bool kHead, bool kMulti>
+// pool's addresses from gpools, and a page ticket carries its width.  kI3:
+// the pool has INT3 pages (ids from n3b, blocks from int3_off).
+template <int G, bool kHead, bool kMulti, bool kI3>
 __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(
     const uint8_t* __restrict__ pool, size_t int4_off, int64_t n2, int hkv, int max_pages,
     const Entry* __restrict__ table, const UnitFrag* __restrict__ frags, const Split* __restrict__ splits,
     const int32_t* __restrict__ wsplit, int n_workers, const int32_t* __restrict__ ntab,
     const uint32_t* __restrict__ hdead, float* __restrict__ part, const uint32_t* __restrict__ smax_bits,
-    uint32_t* __restrict__ status, uint32_t first_spins, const GroupPool* __restrict__ gpools) {
+    uint32_t* __restrict__ status, uint32_t first_spins, const GroupPool* __restrict__ gpools, size_t int3_off,
+    int64_t n3b) {
   constexpr bool kPair = Cols<G>::kPair;
   constexpr int NH = Cols<G>::NH;
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -869,6 +930,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(
         btag = (lsg << 6) | lkvh;
         const uint8_t* src = e.id < n2 ? pool + ((size_t)e.id * hkv + lkvh) * kInt2Block
                                        : pool + int4_off + ((size_t)(e.id - n2) * hkv + lkvh) * kInt4Block;
+        if constexpr (kI3)
+          if (e.id >= n3b) src = pool + int3_off + ((size_t)(e.id - n3b) * hkv + lkvh) * kInt3Block;
         bsrc = (unsigned long long)(uintptr_t)src;
       }
     }
@@ -904,11 +967,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(
   // a ticket's width and split
   auto tk_int2 = [&](const Ticket& t) { return kMulti ? ((t.tag >> 6) & 1) != 0 : t.id < n2; };
   auto tk_split = [&](const Ticket& t) { return kMulti ? t.tag >> 7 : t.tag >> 6; };
+  auto tk_int3 = [&](const Ticket& t) { return kI3 && t.id >= n3b; };
   // copy number n goes to stage n & 1 and completes phase (n >> 1) & 1
   auto issue = [&](const Ticket& t, unsigned long long src, uint32_t n) {   // lane 0
     const uint32_t st = n & (kStages - 1);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the stage was read generically
-    bulk_load(WS.stage[st], (const void*)(uintptr_t)src, tk_int2(t) ? (uint32_t)kInt2Block : (uint32_t)kInt4Block,
+    bulk_load(WS.stage[st], (const void*)(uintptr_t)src,
+              tk_int2(t) ? (uint32_t)kInt2Block : (tk_int3(t) ? (uint32_t)kInt3Block : (uint32_t)kInt4Block),
               &WS.bar[st]);
   };
   static_assert(kStages == 2, "the ticket ring below serves a two-stage copy ring");
@@ -1026,6 +1091,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(
     if (tk_int2(t0)) {
       qk_int2<G>(blk, F, acol2, lg, zc);
       softmax_pv<G, true>(blk, t0.live, pscale, lg, zc, o, zv, mrun, lsum, WS.pbuf);
+    } else if (tk_int3(t0)) {
+      if constexpr (kI3) {
+        qk_int4<G, true>(blk, &F->bq3[0][0], bz, acol4, lg);
+#pragma unroll
+        for (int hh = 0; hh < NH; ++hh) zc[hh] = 0.0f;
+        softmax_pv<G, false, true>(blk, t0.live, pscale, lg, zc, o, zv, mrun, lsum, WS.pbuf);
+      }
     } else {
       qk_int4<G>(blk, &F->bq4[0][0], bz, acol4, lg);
 #pragma unroll
@@ -1057,10 +1129,10 @@ constexpr int kScanSmem = kWarps * (int)sizeof(WarpSmem);
 // shares the SM's memory with shared memory: ask for the smallest shared
 // carveout that holds one CTA (the default takes the largest, leaving L1 too
 // small for 16 warps' q operands; the scan then ran up to 1.45x slower).
-template <int G, bool kHead, bool kMulti>
+template <int G, bool kHead, bool kMulti, bool kI3>
 cudaError_t set_scan_attributes() {
-  cudaError_t e =
-      cudaFuncSetAttribute(decode_mma_kernel<G, kHead, kMulti>, cudaFuncAttributeMaxDynamicSharedMemorySize, kScanSmem);
+  cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<G, kHead, kMulti, kI3>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kScanSmem);
   if (e != cudaSuccess) return e;
   int dev = 0, per_sm = 0, reserved = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
@@ -1068,7 +1140,8 @@ cudaError_t set_scan_attributes() {
   if ((e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev)) != cudaSuccess) return e;
   if (per_sm <= 0) return cudaErrorInvalidValue;
   const int pct = std::min(100, (int)(((int64_t)(kScanSmem + reserved) * 100 + per_sm - 1) / per_sm));
-  return cudaFuncSetAttribute(decode_mma_kernel<G, kHead, kMulti>, cudaFuncAttributePreferredSharedMemoryCarveout, pct);
+  return cudaFuncSetAttribute(decode_mma_kernel<G, kHead, kMulti, kI3>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              pct);
 }
 
 template <int G>
@@ -1080,9 +1153,11 @@ cudaError_t launch_mma_g(kv_pool* P, const void* q, int32_t hq, float scale_log2
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!(attr_set.load() >> dev & 1u)) {
-    cudaError_t e = set_scan_attributes<G, false, false>();
-    if (e == cudaSuccess) e = set_scan_attributes<G, true, false>();
-    if (e == cudaSuccess) e = set_scan_attributes<G, false, true>();
+    cudaError_t e = set_scan_attributes<G, false, false, false>();
+    if (e == cudaSuccess) e = set_scan_attributes<G, true, false, false>();
+    if (e == cudaSuccess) e = set_scan_attributes<G, false, true, false>();
+    if (e == cudaSuccess) e = set_scan_attributes<G, false, false, true>();
+    if (e == cudaSuccess) e = set_scan_attributes<G, true, false, true>();
     if (e != cudaSuccess) return e;
     attr_set.fetch_or(uint64_t(1) << dev);
   }
@@ -1093,21 +1168,28 @@ cudaError_t launch_mma_g(kv_pool* P, const void* q, int32_t hq, float scale_log2
                              (int)hq, scale_log2, d_units, smax, (UnitFrag*)d_frags, d_gpools);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)((n_workers + kWarps - 1) / kWarps);
-  auto* kernel = d_gpools ? decode_mma_kernel<G, false, true>
-                          : (P->hdead.empty() ? decode_mma_kernel<G, false, false> : decode_mma_kernel<G, true, false>);
+  // pools with INT3 pages take the variant that reads them (grouped decodes
+  // take no such pool)
+  const bool i3 = P->cfg.n_int3_pages > 0;
+  auto* kernel = d_gpools ? decode_mma_kernel<G, false, true, false>
+                 : i3     ? (P->hdead.empty() ? decode_mma_kernel<G, false, false, true>
+                                              : decode_mma_kernel<G, true, false, true>)
+                          : (P->hdead.empty() ? decode_mma_kernel<G, false, false, false>
+                                              : decode_mma_kernel<G, true, false, false>);
   return launch_pdl(kernel, dim3(grid), dim3(kThreads), (size_t)kScanSmem, s, (const uint8_t*)P->d_pool,
                     P->int4_offset, (int64_t)P->cfg.n_int2_pages, P->cfg.num_kv_heads, P->cfg.max_pages_per_request,
                     (const Entry*)P->d_table, (const UnitFrag*)d_frags, d_splits, d_wsplit, n_workers,
                     (const int32_t*)P->d_ntab, (const uint32_t*)P->d_hdead, d_part, smax, P->d_status,
-                    P->first_wait_spins < 0 ? kSpinLimit : (uint32_t)P->first_wait_spins, d_gpools);
+                    P->first_wait_spins < 0 ? kSpinLimit : (uint32_t)P->first_wait_spins, d_gpools, P->int3_offset,
+                    (int64_t)(P->cfg.n_int2_pages + P->cfg.n_int4_pages));
 }
 
 template <int G>
 int mma_occupancy() {
   int n = 0;
-  if (set_scan_attributes<G, false, false>() != cudaSuccess) return 1;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<G, false, false>, kThreads, kScanSmem) !=
-      cudaSuccess)
+  if (set_scan_attributes<G, false, false, false>() != cudaSuccess) return 1;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<G, false, false, false>, kThreads,
+                                                    kScanSmem) != cudaSuccess)
     return 1;
   return n > 0 ? n : 1;
 }

@@ -40,6 +40,23 @@
 //                = channel 4*(8i + 4wi + (j>>2)) + (j&3), high half = that + 8;
 //                pair j = 0 has the two halves the other way round.
 //   [2560, 3072) V scale/zero: as in the INT4 block.
+// INT3 block (4096 B): the INT4 block's code words with each 4-bit field cut
+// into a 2-bit plane (the code's low bits) and a 1-bit plane (bit 2), so
+// that one shift + mask of each plane puts both parts of a code at bits
+// 6..8 of a 16-bit half, the same A-register fields as INT4 (at bit 6).
+//   [   0, 1536) K codes: slot t row at 48*t.  Low plane at 8*i (chunk i):
+//                word h (groups 2h, 2h+1) holds the low bits of channel
+//                c = 32*gr + 8*i + n at bit 8*(gr&1) + 2*(n&3) + 16*(n>>2).
+//                High plane at 32 + 4*i: bit 2 of channel c at bit
+//                4*gr + (n&3) + 16*(n>>2).
+//   [1536, 3072) V codes, channel-major: INT4 V chunk X = 32*(m>>1) + 4*r + j
+//                (channels c = 16m + 8e + r, slots 8j..8j+7, INT4 word
+//                w = 2*(m&1) + e) becomes a low-plane uint2 at 1536 + 8*X, word
+//                m&1 holding slot 8j+k of channel e at bit
+//                8*e + 2*(k&3) + 16*(k>>2), and a high-plane word at
+//                2560 + 4*X with bit 4*w + (k&3) + 16*(k>>2).
+//   [3072, 3584) K scale/zero: as in the INT4 block ([slot][group] {s, z}).
+//   [3584, 4096) V scale/zero: as in the INT4 block.
 #pragma once
 #include <stdint.h>
 
@@ -56,11 +73,14 @@ constexpr int kPage = 32;
 constexpr int kGroup = 32;
 constexpr int kInt4Block = 5120;
 constexpr int kInt2Block = 3072;
+constexpr int kInt3Block = 4096;
 
 // INT4 block offsets
 constexpr int kI4KCodes = 0, kI4VCodes = 2048, kI4KMeta = 4096, kI4VMeta = 4608;
 // INT2 block offsets
 constexpr int kI2KCodes = 0, kI2VCodes = 1024, kI2KMeta = 2048, kI2VMeta = 2560;
+// INT3 block offsets (kI3VHigh: the V high plane)
+constexpr int kI3KCodes = 0, kI3VCodes = 1536, kI3VHigh = 2560, kI3KMeta = 3072, kI3VMeta = 3584;
 
 // ---- INT4 K codes: byte offset and nibble of (slot, channel)
 KVQ_HD int i4k_byte(int t, int c) {
@@ -98,7 +118,39 @@ KVQ_HD int i2k_meta_index(int c) {
   return 2 * ((i * 2 + wi) * 8 + j) + hi;
 }
 
-// ---- V scale/zero (both widths): half index (0..127) of (slot, group)
+// ---- INT3 K codes: byte and bit of the low 2 bits / of bit 2 of (slot, channel)
+KVQ_HD int i3k_lo_byte(int t, int c) {
+  const int gr = c >> 5, i = (c >> 3) & 3, n = c & 7;
+  return kI3KCodes + 48 * t + 8 * i + 4 * (gr >> 1) + (gr & 1) + 2 * (n >> 2);
+}
+KVQ_HD int i3k_lo_shift(int c) { return 2 * (c & 3); }
+KVQ_HD int i3k_hi_byte(int t, int c) {
+  const int gr = c >> 5, i = (c >> 3) & 3, n = c & 7;
+  return kI3KCodes + 48 * t + 32 + 4 * i + (gr >> 1) + 2 * (n >> 2);
+}
+KVQ_HD int i3k_hi_shift(int c) { return 4 * ((c >> 5) & 1) + (c & 3); }
+
+// ---- INT3 V codes
+KVQ_HD int i3v_chunk(int t, int c) {
+  const int m = c >> 4, r = c & 7;
+  return 32 * (m >> 1) + 4 * r + (t >> 3);
+}
+KVQ_HD int i3v_lo_byte(int t, int c) {
+  const int m = c >> 4, e = (c >> 3) & 1, k = t & 7;
+  return kI3VCodes + 8 * i3v_chunk(t, c) + 4 * (m & 1) + e + 2 * (k >> 2);
+}
+KVQ_HD int i3v_lo_shift(int t) { return 2 * (t & 3); }
+KVQ_HD int i3v_hi_byte(int t, int c) {
+  const int m = c >> 4, e = (c >> 3) & 1, k = t & 7;
+  const int w = 2 * (m & 1) + e;
+  return kI3VHigh + 4 * i3v_chunk(t, c) + (w >> 1) + 2 * (k >> 2);
+}
+KVQ_HD int i3v_hi_shift(int t, int c) {
+  const int m = c >> 4, e = (c >> 3) & 1;
+  return 4 * ((2 * (m & 1) + e) & 1) + (t & 3);
+}
+
+// ---- V scale/zero (every width): half index (0..127) of (slot, group)
 KVQ_HD int v_meta_index(int t, int gr) {
   const int j = t >> 3, k = t & 7;
   const int pos = (k < 4) ? 2 * k : 2 * (k - 4) + 1;

@@ -238,6 +238,140 @@ __global__ void __launch_bounds__(kThreads) append_int4_kernel(
   }
 }
 
+// ---- INT3 pages (TriAxialKV, limitations and outlook: INT3 as a further
+// width): the INT4 per-token rule with 2^3 - 1 levels, codes stored as a
+// 2-bit low plane and a 1-bit high plane.  A warp quantizes one token of one
+// kv head, lane = channels 4*lane .. 4*lane+3 (one group per 8 lanes).
+// K: a lane's four low-bit fields are one byte of the token's low plane and
+// its four high bits one nibble of the high plane, whose byte it shares with
+// the lane of the neighbouring group (lane ^ 8): the even group's lane writes
+// the byte.  V (channel-major) goes to vcodes for a fresh page (packed by
+// pack_i3v), else its bits are OR-ed into the block.
+__device__ __forceinline__ bool quantize_rows3(uint8_t* img, const RawRows& rr, int slot, float& vmax,
+                                               uint8_t* vcodes) {
+  const int lane = threadIdx.x & 31, gr = lane >> 3;
+  const uint2 kr = rr.kr, vr = rr.vr;
+  float xk[4], xv[4];
+  xk[0] = __uint_as_float(kr.x << 16); xk[1] = __uint_as_float(kr.x & 0xFFFF0000u);
+  xk[2] = __uint_as_float(kr.y << 16); xk[3] = __uint_as_float(kr.y & 0xFFFF0000u);
+  xv[0] = __uint_as_float(vr.x << 16); xv[1] = __uint_as_float(vr.x & 0xFFFF0000u);
+  xv[2] = __uint_as_float(vr.y << 16); xv[3] = __uint_as_float(vr.y & 0xFFFF0000u);
+  bool bad = false;
+  float kmn = xk[0], kmx = xk[0], vmn = xv[0], vmx = xv[0];
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    bad |= out_of_range(xk[a]) | out_of_range(xv[a]);
+    kmn = fminf(kmn, xk[a]); kmx = fmaxf(kmx, xk[a]);
+    vmn = fminf(vmn, xv[a]); vmx = fmaxf(vmx, xv[a]);
+  }
+  group8_minmax(kmn, kmx);
+  group8_minmax(vmn, vmx);
+  const GroupMeta km = make_meta(kmn, kmx, 7.0f);
+  const GroupMeta vm = make_meta(vmn, vmx, 7.0f);
+  uint32_t ck[4], cv[4];
+  const float krs = approx_rcp(km.sf), vrs = approx_rcp(vm.sf);
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    ck[a] = qcode_fast(xk[a], km, krs, 7.0f);
+    cv[a] = qcode_fast(xv[a], vm, vrs, 7.0f);
+  }
+  const int c0 = 4 * lane;
+  img[i3k_lo_byte(slot, c0)] = (uint8_t)((ck[0] & 3u) | ((ck[1] & 3u) << 2) | ((ck[2] & 3u) << 4) | ((ck[3] & 3u) << 6));
+  const uint32_t hi = (ck[0] >> 2) | ((ck[1] >> 2) << 1) | ((ck[2] >> 2) << 2) | ((ck[3] >> 2) << 3);
+  const uint32_t hi_odd = __shfl_xor_sync(0xFFFFFFFFu, hi, 8);
+  if ((gr & 1) == 0) img[i3k_hi_byte(slot, c0)] = (uint8_t)(hi | (hi_odd << 4));
+  if (vcodes) {
+    *reinterpret_cast<uint32_t*>(vcodes + kHeadDim * slot + c0) = cv[0] | (cv[1] << 8) | (cv[2] << 16) | (cv[3] << 24);
+  } else {
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      const int c = c0 + a;
+      or_bits(img, i3v_lo_byte(slot, c), i3v_lo_shift(slot), cv[a] & 3u);
+      or_bits(img, i3v_hi_byte(slot, c), i3v_hi_shift(slot, c), cv[a] >> 2);
+    }
+  }
+  vmax = fmaxf(vmax, vm.sf);
+  if ((lane & 7) == 0) {
+    st_half(img, kI3KMeta + 16 * slot + 4 * gr, km.s);
+    st_half(img, kI3KMeta + 16 * slot + 4 * gr + 2, km.z);
+    st_half(img, kI3VMeta + 2 * v_meta_index(slot, gr), vm.s);
+    st_half(img, kI3VMeta + 256 + 2 * v_meta_index(slot, gr), vm.z);
+  }
+  return bad;
+}
+
+// INT3 V planes from [slot][channel] code bytes, every word by one thread:
+// low-plane word (chunk X, h) and high-plane word X of the layout.
+__device__ __forceinline__ void pack_i3v(uint8_t* __restrict__ img, const uint8_t* __restrict__ vcodes) {
+  for (int x = threadIdx.x; x < 3 * 128; x += kThreads) {
+    const int X = x < 256 ? x >> 1 : x - 256;
+    const int mh = X >> 5, r = (X >> 2) & 7, j = X & 3;   // chunk X = 32 (m >> 1) + 4 r + j
+    uint32_t w = 0u;
+    if (x < 256) {
+      const int h = x & 1, m = 2 * mh + h;
+#pragma unroll
+      for (int e = 0; e < 2; ++e)
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          w |= ((uint32_t)vcodes[kHeadDim * (8 * j + k) + 16 * m + 8 * e + r] & 3u) << (8 * e + 2 * (k & 3) + 16 * (k >> 2));
+      *reinterpret_cast<uint32_t*>(img + kI3VCodes + 8 * X + 4 * h) = w;
+    } else {
+#pragma unroll
+      for (int wd = 0; wd < 4; ++wd) {
+        const int m = 2 * mh + (wd >> 1), e = wd & 1;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          w |= ((uint32_t)vcodes[kHeadDim * (8 * j + k) + 16 * m + 8 * e + r] >> 2) << (4 * wd + (k & 3) + 16 * (k >> 2));
+      }
+      *reinterpret_cast<uint32_t*>(img + kI3VHigh + 4 * X) = w;
+    }
+  }
+}
+
+// One CTA per (job, kv head) of INT3 tail pages, a warp per token; a new page
+// is built in shared memory from zeros and written whole, a page that
+// already holds tokens gets its new slots in place (V bits by atomic OR).
+// Table entry and length as in append_int4_kernel.
+__global__ void __launch_bounds__(kThreads) append_int3_kernel(
+    uint8_t* __restrict__ pool, size_t int3_off, int64_t n3b, int hkv, const __nv_bfloat16* __restrict__ k,
+    const __nv_bfloat16* __restrict__ v, const AppendJob* __restrict__ jobs, const int32_t* __restrict__ toks,
+    Entry* __restrict__ table, int32_t* __restrict__ ntab, uint32_t* __restrict__ status) {
+  __shared__ __align__(16) uint8_t img[kInt3Block];
+  __shared__ __align__(16) uint8_t vcodes[kPage * kHeadDim];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
+  const AppendJob job = jobs[blockIdx.x];
+  const int h = blockIdx.y;
+  uint8_t* blk = pool + int3_off + ((size_t)(job.page - n3b) * hkv + h) * kInt3Block;
+  const bool fresh = job.first_slot == 0;
+  uint8_t* dst = fresh ? img : blk;
+  if (fresh) {
+    for (int i = threadIdx.x; i < kInt3Block / 16; i += kThreads) reinterpret_cast<uint4*>(img)[i] = make_uint4(0, 0, 0, 0);
+    for (int i = threadIdx.x; i < kPage * kHeadDim / 16; i += kThreads)
+      reinterpret_cast<uint4*>(vcodes)[i] = make_uint4(0, 0, 0, 0);
+    __syncthreads();
+  }
+  const int warp = threadIdx.x >> 5;
+  const int32_t* tk = toks + job.tok_off;
+  bool bad = false;
+  float vmax = 0.0f;
+  for (int q = warp; q < job.n_slots; q += kThreads / 32)
+    bad |= quantize_rows3(dst, load_rows(k, v, tk[q], h, hkv), job.first_slot + q, vmax, fresh ? vcodes : nullptr);
+  if (fresh) {
+    __syncthreads();
+    pack_i3v(img, vcodes);
+    __syncthreads();
+    for (int i = threadIdx.x; i < kInt3Block / 16; i += kThreads)
+      reinterpret_cast<uint4*>(blk)[i] = reinterpret_cast<const uint4*>(img)[i];
+  }
+  flush_vmax(vmax, status);
+  if (bad) atomicOr(status, kStatusRange);
+  if (h == 0 && threadIdx.x == 0) {
+    if (job.tab_index >= 0) table[job.tab_index] = Entry{job.page, job.live};
+    if (job.ntab_req >= 0) ntab[job.ntab_req] = job.ntab_len;
+  }
+}
+
 // Requantize a 32-token INT4 block image (shared memory) into an INT2 block
 // image (shared memory): K per channel across the 32 tokens, V per token and
 // group, both from the INT4-dequantized values fmaf(code, scale, zero); tracks
@@ -791,6 +925,16 @@ cudaError_t launch_append(kv_pool* P, const void* k, const void* v, const Append
   return launch_pdl(append_int4_kernel<false>, grid, dim3(kThreads), 0, s, P->d_pool, P->int4_offset,
                     P->cfg.n_int2_pages, P->cfg.num_kv_heads, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v,
                     d_jobs, d_toks, P->d_table, P->d_ntab, P->d_status, none);
+}
+
+cudaError_t launch_append_int3(kv_pool* P, const void* k, const void* v, const AppendJob* d_jobs, int n_jobs,
+                               const int32_t* d_toks, cudaStream_t s) {
+  if (n_jobs <= 0) return cudaSuccess;
+  ++P->launches;
+  return launch_pdl(append_int3_kernel, dim3((unsigned)n_jobs, (unsigned)P->cfg.num_kv_heads), dim3(kThreads), 0, s,
+                    P->d_pool, P->int3_offset, (int64_t)(P->cfg.n_int2_pages + P->cfg.n_int4_pages),
+                    P->cfg.num_kv_heads, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, d_jobs, d_toks,
+                    P->d_table, P->d_ntab, P->d_status);
 }
 
 cudaError_t launch_bulk_int4(kv_pool* P, const void* k, const void* v, const AppendJob* d_jobs, int n_jobs,
