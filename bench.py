@@ -557,6 +557,8 @@ def main():
     ap.add_argument("--head-groups", type=int, default=0,
                     help="N > 0: the kv heads in N pools of their own; group j keeps the most recent (j+1)/N of "
                          "every prompt and drops its dead pages; one grouped decode per step")
+    ap.add_argument("--int3-share", type=float, default=0.0,
+                    help="make a seeded fraction of the INT4 tokens INT3 (three-width pool; prefill and steps)")
     ap.add_argument("--mode", default="decode", choices=["decode", "prefill"],
                     help="decode: the decode-step line (default); prefill: bulk quantization of the workload's "
                          "prompts through kv_append_quant")
@@ -587,7 +589,9 @@ def main():
     SEG_W = SEG_WS = 128   # HyQuant window W and staging capacity W_s
     extra = SEG_W if args.segments else 0   # the frozen window is quantized again by the first flush
     w = load_workload(args, total_steps)
-    gw = GPUWorkload(w, device=local, steps=total_steps, extra_tokens=extra)
+    if args.int3_share > 0:
+        w.name = f"{w.name}+int3-{args.int3_share:g}"
+    gw = GPUWorkload(w, device=local, steps=total_steps, extra_tokens=extra, int3_share=args.int3_share)
     gw.pool.set_decode_impl({"auto": 0, "simt": 1, "mma": 2}[args.decode_impl])
     gw.prefill()
     gw.evict()
@@ -771,7 +775,9 @@ def main():
                              "kernels": "fp_segment_kernel + decode_mma_kernel, one scan time"}}
                if args.segments else {}),
             "clocks": clk.summary()}
-    if rank == 0 and not args.no_cpu_baseline:
+    if args.int3_share > 0:
+        line["config"]["int3_token_fraction"] = float(np.mean(np.concatenate(gw.bits) == 3))
+    if rank == 0 and not args.no_cpu_baseline and args.int3_share <= 0:
         try:
             line["cpu_baseline"] = cpu_baseline(w)
         except Exception as e:  # reported, not fatal

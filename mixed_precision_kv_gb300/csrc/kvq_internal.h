@@ -169,9 +169,10 @@ struct ScanOrder {
 struct PageCost {
   double int2, int4, int3;
 };
-// INT3 pages: the INT4 page's work plus about 300 more instructions to
-// assemble the codes from two planes
-inline PageCost mma_page_cost(int g) { return g <= 4 ? PageCost{1.18, 1.00, 1.30} : PageCost{1.50, 1.00, 1.30}; }
+// INT3 pages: the INT4 page's work plus the assembly of every code from two
+// planes; fitted the same way (32K-token batch-8 and 100K-token batch-16
+// steps with every INT4 token made INT3): 1.28x and 1.40x an INT4 page.
+inline PageCost mma_page_cost(int g) { return g <= 4 ? PageCost{1.18, 1.00, 1.28} : PageCost{1.50, 1.00, 1.40}; }
 constexpr PageCost kSimtPageCost{3072.0 + 2048.0, 5120.0 + 2048.0, 4096.0 + 2048.0};
 constexpr int64_t kMinPagesPerCta = 16;    // CUDA-core scan: pages per CTA at least
 constexpr int64_t kMinPagesPerWarp = 1;    // tensor-core scan: pages per warp at least (small batches: more warps, less latency)

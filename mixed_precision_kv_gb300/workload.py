@@ -25,19 +25,41 @@ def request_bits(w: Workload, r: int, allocator=alloc_bits) -> np.ndarray:
     return bits
 
 
+def int3_share_bits(w: Workload, r: int, bits: np.ndarray, share: float) -> np.ndarray:
+    """A seeded fraction `share` of request r's INT4 tokens made INT3 (a
+    synthetic three-width mix: the greedy allocation itself has two widths)."""
+    if share <= 0.0:
+        return bits
+    u = np.random.default_rng([w.seed, 33, r]).random(bits.size)
+    out = bits.copy()
+    out[(bits == 4) & (u < share)] = 3
+    return out
+
+
+def int3_pages(w: Workload, bits_list, steps: int) -> int:
+    """INT3 pages the workload's INT3 tokens take (prefill and steps)."""
+    n3 = 0
+    for spec, bits in zip(w.requests, bits_list):
+        b3 = int((bits[:spec.n_prefill + steps] == 3).sum())
+        n3 += -(-b3 // 32) + 1 if b3 else 0
+    return n3
+
+
 def pool_size(w: Workload, bits_list, chunk: int, steps: int, extra: int = 0):
     """INT2 / INT4 page counts and table capacity for a workload appended in
     `chunk`-token calls and then `steps` one-token-per-request calls, with room
-    for `extra` more tokens per request of either width."""
+    for `extra` more tokens per request of either width (INT3 pages:
+    int3_pages)."""
     n2 = n4 = max_tab = 0
     xp = -(-extra // 32) + 1 if extra else 0
     for spec, bits in zip(w.requests, bits_list):
         total = spec.n_prefill + steps
         b2 = int((bits[:total] == 2).sum())
-        b4 = total - b2
+        b3 = int((bits[:total] == 3).sum())
+        b4 = total - b2 - b3
         n2 += b2 // 32 + 1 + xp
         n4 += -(-b4 // 32) + 2 + xp
-        max_tab = max(max_tab, b2 // 32 + -(-b4 // 32) + 3 + 2 * xp)
+        max_tab = max(max_tab, b2 // 32 + -(-b4 // 32) + -(-b3 // 32) + 3 + 2 * xp)
     # staging pages repacked during one call are freed only when it returns
     n4 += chunk // 32 + len(w.requests) + 8
     return n2, n4, max_tab
@@ -45,18 +67,20 @@ def pool_size(w: Workload, bits_list, chunk: int, steps: int, extra: int = 0):
 
 class GPUWorkload:
     def __init__(self, w: Workload, device: int = 0, chunk: int = 16384, steps: int | None = None,
-                 extra_tokens: int = 0, make_pool: bool = True):
+                 extra_tokens: int = 0, make_pool: bool = True, int3_share: float = 0.0):
         import torch
         self.w = w
         self.device = device
         self.chunk = chunk
         self.steps = w.steps if steps is None else steps
-        self.bits = [request_bits(w, r) for r in range(len(w.requests))]
+        self.bits = [int3_share_bits(w, r, request_bits(w, r), int3_share) for r in range(len(w.requests))]
         self.sizes = pool_size(w, self.bits, chunk, self.steps, extra_tokens)
         n2, n4, max_tab = self.sizes
+        n3 = int3_pages(w, self.bits, self.steps)
         # make_pool=False: the caller builds its own pools (e.g. one per head
         # group) and uses this object for the bit allocation and the rows
-        self.pool = KVPool(w.num_kv_heads, n2, n4, len(w.requests), max_tab, device=device) if make_pool else None
+        self.pool = (KVPool(w.num_kv_heads, n2, n4, len(w.requests), max_tab, device=device, n_int3_pages=n3)
+                     if make_pool else None)
         self.rids = [self.pool.open() for _ in w.requests] if make_pool else []
         self.dev = torch.device("cuda", device)
         self.chan = torch.from_numpy(w.k_chan_mult).to(self.dev)
