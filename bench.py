@@ -371,7 +371,7 @@ def run_head_groups(args):
     import torch
     import kvsynth
     import mixed_precision_kv_gb300 as kvq
-    from mixed_precision_kv_gb300.workload import GPUWorkload
+    from mixed_precision_kv_gb300.workload import GroupWorkload
 
     ws, rank, local = dist_setup()
     torch.cuda.set_device(local)
@@ -386,33 +386,14 @@ def run_head_groups(args):
     H, N = w.num_kv_heads, args.head_groups
     if N < 1 or N > 8 or H % N:
         raise SystemExit("--head-groups must divide the workload's kv heads, at most 8 groups")
-    hg = H // N
-    lo = [j * hg for j in range(N + 1)]
-    gw = GPUWorkload(w, device=local, steps=total_steps, make_pool=False)
-    n2, n4, max_tab = gw.sizes
-    pools = [kvq.KVPool(hg, n2, n4, len(w.requests), max_tab, device=local) for _ in range(N)]
-    rids = [np.array([p.open() for _ in w.requests], np.int32) for p in pools]
+    G = GroupWorkload(w, N, device=local, steps=total_steps)
+    gw, pools, rids, hg, lo, keep = G.gw, G.pools, G.rids, G.hg, G.lo, G.keep
     B, Hq = len(w.requests), w.num_q_heads
-    for r, spec in enumerate(w.requests):
-        for t0 in range(0, spec.n_prefill, gw.chunk):
-            n = min(gw.chunk, spec.n_prefill - t0)
-            k, v = gw.kv_rows(r, t0, n)
-            for j, p in enumerate(pools):
-                p.append(k[:, lo[j]:lo[j + 1]].contiguous(), v[:, lo[j]:lo[j + 1]].contiguous(),
-                         np.full(n, rids[j][r], np.int32), gw.bits[r][t0:t0 + n])
-    keep = [(j + 1) / N for j in range(N)]
-    for r, spec in enumerate(w.requests):
-        n = spec.n_prefill
-        for j, p in enumerate(pools):
-            pos = np.union1d(spec.evict, np.arange(n - int(round(n * keep[j])), dtype=np.int64))
-            if pos.size:
-                p.evict(np.full(pos.size, rids[j][r], np.int32), pos)
-    blocks_before = sum(p.info(int(x))[0] * hg for p, rs in zip(pools, rids) for x in rs)
-    for j, p in enumerate(pools):
-        p.reorder(rids[j])
-        p.drop_dead_pages(rids[j])
-        p.sync()
-    blocks_after = sum(p.info(int(x))[0] * hg for p, rs in zip(pools, rids) for x in rs)
+    G.prefill()
+    blocks_before = G.blocks()
+    G.evict_and_drop()
+    G.sync()
+    blocks_after = G.blocks()
     dev = torch.device("cuda", local)
     kf = torch.empty((total_steps, B, H, 128), dtype=torch.bfloat16, device=dev)
     vf = torch.empty_like(kf)

@@ -181,3 +181,93 @@ class GPUWorkload:
     def kv_bytes(self) -> int:
         return self.pool.last_decode_stats()["kv_bytes"]
 
+
+class GroupWorkload:
+    """The workload's kv heads cut into `n_groups` equal head groups, one pool
+    each (Tangram: head groups keep different amounts of context), fed the
+    group's rows of every token in the same calls.  Group j keeps the most
+    recent keep[j] of every prompt (default (j + 1) / n_groups): its pool
+    evicts the older positions (and the workload's own evictions) and drops
+    the pages no kv head of the group reads any more."""
+
+    def __init__(self, w: Workload, n_groups: int, device: int = 0, chunk: int = 16384, steps: int | None = None,
+                 keep=None):
+        import torch
+        H = w.num_kv_heads
+        if n_groups < 1 or n_groups > 8 or H % n_groups:
+            raise ValueError("n_groups must divide the kv heads, at most 8 groups")
+        self.w, self.N, self.hg = w, n_groups, H // n_groups
+        self.lo = [j * self.hg for j in range(n_groups + 1)]
+        self.keep = [(j + 1) / n_groups for j in range(n_groups)] if keep is None else list(keep)
+        self.gw = GPUWorkload(w, device=device, chunk=chunk, steps=steps, make_pool=False)
+        self.bits, self.chunk, self.dev = self.gw.bits, chunk, self.gw.dev
+        n2, n4, max_tab = self.gw.sizes
+        self.pools = [KVPool(self.hg, n2, n4, len(w.requests), max_tab, device=device) for _ in range(n_groups)]
+        self.rids = [np.array([p.open() for _ in w.requests], np.int32) for p in self.pools]
+        self.pos = [0] * len(w.requests)
+        self.torch = torch
+
+    def rows(self, k, j):
+        return k[:, self.lo[j]:self.lo[j + 1]].contiguous()
+
+    def prefill(self):
+        for r, spec in enumerate(self.w.requests):
+            for t0 in range(0, spec.n_prefill, self.chunk):
+                n = min(self.chunk, spec.n_prefill - t0)
+                k, v = self.gw.kv_rows(r, t0, n)
+                for j, p in enumerate(self.pools):
+                    p.append(self.rows(k, j), self.rows(v, j), np.full(n, self.rids[j][r], np.int32),
+                             self.bits[r][t0:t0 + n])
+            self.pos[r] = spec.n_prefill
+
+    def cut(self, r, j):
+        """Positions group j leaves out of request r's prompt."""
+        spec = self.w.requests[r]
+        n = spec.n_prefill
+        return np.union1d(spec.evict, np.arange(n - int(round(n * self.keep[j])), dtype=np.int64))
+
+    def evict_and_drop(self):
+        for r in range(len(self.w.requests)):
+            for j, p in enumerate(self.pools):
+                pos = self.cut(r, j)
+                if pos.size:
+                    p.evict(np.full(pos.size, self.rids[j][r], np.int32), pos)
+        for j, p in enumerate(self.pools):
+            p.reorder(self.rids[j])
+            p.drop_dead_pages(self.rids[j])
+
+    def blocks(self):
+        """(page, kv head) blocks the group pools hold."""
+        return sum(p.info(int(x))[0] * self.hg for p, rs in zip(self.pools, self.rids) for x in rs)
+
+    def append_step(self, k, v, bits):
+        """One token per request: k, v [B][Hkv][128] on the device."""
+        for j, p in enumerate(self.pools):
+            p.append(self.rows(k, j), self.rows(v, j), self.rids[j], bits)
+            p.reorder(self.rids[j])
+        for r in range(len(self.pos)):
+            self.pos[r] += 1
+
+    def step_inputs(self):
+        ks, vs = [], []
+        for r in range(len(self.w.requests)):
+            k, v = self.gw.kv_rows(r, self.pos[r], 1)
+            ks.append(k)
+            vs.append(v)
+        bits = np.array([self.bits[r][self.pos[r]] for r in range(len(self.w.requests))], np.uint8)
+        return self.torch.cat(ks), self.torch.cat(vs), bits
+
+    def q(self, step: int):
+        torch = self.torch
+        B, Hq = len(self.w.requests), self.w.num_q_heads
+        out = torch.empty((B, Hq, 128), dtype=torch.bfloat16, device=self.dev)
+        kvsynth.fill_bf16_dev(out.data_ptr(), B, Hq, 128, self.w.seed, kvsynth.TENSOR_Q, step, 0, 0, 0,
+                              torch.cuda.current_stream(self.dev).cuda_stream)
+        return out
+
+    def decode(self, q, out=None):
+        return KVPool.decode_groups(self.pools, q, np.stack(self.rids), self.w.softmax_scale, out=out)
+
+    def sync(self):
+        for p in self.pools:
+            p.sync()

@@ -310,3 +310,64 @@ def test_grouped_decode_rejects_bad_calls(kvq):
     sc.gpu[1].fp_drop(sc.g_ids[1][0], 0, 3)
     sc.sync()
     sc.decode(0, "after the rejected calls")
+
+
+def test_config2_full_size_head_groups(kvq):
+    """The 32K-token batch-8 workload (8 kv heads) as 2 head-group pools built,
+    evicted and dropped exactly as `bench.py --head-groups 2` builds them
+    (group 0 keeps the most recent half of every prompt, group 1 all of it),
+    then 3 decode steps.  Oracle twins model each group's pool as a shared
+    pool over all heads with the group's positions evicted and its dead pages
+    dropped (ids and tables do not depend on the heads a pool holds): every
+    table of both pools bit-exact, sampled units' codes and outputs within the
+    tolerance."""
+    from harness import OracleWorkload, oracle_bits
+    from mixed_precision_kv_gb300.workload import GroupWorkload, pool_size
+    steps = 3
+    w = kvsynth.make_workload(2, steps=steps)
+    G = GroupWorkload(w, 2, steps=steps)
+    for r in range(len(w.requests)):
+        assert np.array_equal(G.bits[r], oracle_bits(w, r))
+    G.prefill()
+    G.evict_and_drop()
+    G.sync()
+    sampled = {0: [1], 1: [6]}   # global kv heads (group 0: heads 0-3, group 1: heads 4-7)
+    reqs = [0, 5]
+    twins = []
+    for j in range(2):
+        ow = OracleWorkload(w, pool_size(w, G.bits, G.chunk, G.gw.steps), G.chunk, sel_heads=sampled[j],
+                            content_reqs=reqs)
+        ow.prefill()
+        for r in range(len(w.requests)):
+            pos = G.cut(r, j)
+            assert ow.P.evict(np.full(pos.size, ow.rids[r]), pos) == oracle.OK
+        ow.reorder()
+        assert ow.P.drop_dead_pages(ow.rids) == oracle.OK
+        twins.append(ow)
+    B, g = len(w.requests), w.g
+
+    def check(step, content):
+        out = G.decode(G.q(step)).cpu().numpy()
+        G.sync()
+        for j, ow in enumerate(twins):
+            for r in range(B):
+                compare_tables(G.pools[j].export(int(G.rids[j][r]), content=False),
+                               ow.P.export(ow.rids[r], content=False))
+            if content:
+                for r in reqs:
+                    compare_content(G.pools[j].export(int(G.rids[j][r])), ow.P.export(ow.rids[r]),
+                                    [h - G.lo[j] for h in sampled[j]])
+            pairs = np.array([(b, h * g + x) for b in reqs for h in sampled[j] for x in range(g)], np.int32)
+            ref = ow.decode(ow.q(step), pairs=pairs)
+            got = np.stack([out[b, hq] for b, hq in pairs])
+            assert np.isfinite(got).all()
+            assert_outputs_close(got, ref, f"32K batch 8, group {j}, step {step}")
+
+    check(0, True)
+    for step in range(1, steps + 1):
+        k, v, bits = G.step_inputs()
+        G.append_step(k, v, bits)
+        for ow in twins:
+            ow.append_step()
+            ow.reorder()
+        check(step, step == steps)
