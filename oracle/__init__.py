@@ -22,6 +22,7 @@ _lock = threading.Lock()
 _lib = None
 
 OK, INVALID, OOM, RANGE, STATE = 0, 1, 2, 3, 6
+FP4 = 0xF4   # width value of FP4 (E2M1) tokens
 
 _P = ctypes.c_void_p
 _I32, _I64, _F32 = ctypes.c_int32, ctypes.c_int64, ctypes.c_float
@@ -48,7 +49,10 @@ def lib():
                 "orc_quant_group": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int, _P, _P, _P]),
                 "orc_dequant": (_F32, [ctypes.c_uint8, ctypes.c_uint16, ctypes.c_uint16]),
                 "orc_alloc_bits": (ctypes.c_int, [_P, _P, _P, ctypes.c_int, _I64, _I64, _P]),
-                "orc_pool_new": (_P, [ctypes.c_int, _I64, _I64, _I64, ctypes.c_int, ctypes.c_int, _P, ctypes.c_int]),
+                "orc_pool_new": (_P, [ctypes.c_int, _I64, _I64, _I64, _I64, ctypes.c_int, ctypes.c_int, _P,
+                                      ctypes.c_int]),
+                "orc_fp4_group": (ctypes.c_int, [_P, ctypes.c_int, _P, _P]),
+                "orc_e2m1_value": (ctypes.c_double, [ctypes.c_int]),
                 "orc_pool_free": (None, [_P]),
                 "orc_request_open": (ctypes.c_int, [_P, _P]),
                 "orc_request_close": (ctypes.c_int, [_P, _I32]),
@@ -112,6 +116,19 @@ def quant_group(x, bits):
     return codes, int(s[0]), int(z[0])
 
 
+def fp4_group(x):
+    """FP4 (E2M1) group -> (codes uint8[n], s_bits uint16); raises OracleError on range errors."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    codes = np.empty(x.size, dtype=np.uint8)
+    s = np.zeros(1, dtype=np.uint16)
+    _check(lib().orc_fp4_group(_p(x), x.size, _p(s), _p(codes)), "fp4_group")
+    return codes, int(s[0])
+
+
+def e2m1_value(code):
+    return float(lib().orc_e2m1_value(int(code)))
+
+
 def dequant(code, s_bits, z_bits):
     return np.float32(lib().orc_dequant(int(code), int(s_bits), int(z_bits)))
 
@@ -129,17 +146,19 @@ def alloc_bits(N, D2, D4, budget):
 
 class OraclePool:
     """Model of the paged pool.  sel_heads: kv heads whose codes are kept;
-    n_int3_pages: INT3 page ids [n2 + n4, n2 + n4 + n3), after the INT4 ids."""
+    n_int3_pages: INT3 page ids [n2 + n4, n2 + n4 + n3), after the INT4 ids;
+    n_fp4_pages: FP4 page ids after those."""
 
     def __init__(self, num_kv_heads, n_int2_pages, n_int4_pages, max_requests, max_pages_per_request,
-                 sel_heads=None, n_int3_pages=0):
+                 sel_heads=None, n_int3_pages=0, n_fp4_pages=0):
         self.hkv = num_kv_heads
         self.sel = list(range(num_kv_heads)) if sel_heads is None else list(sel_heads)
         sel = np.array(self.sel, dtype=np.int32)
         self.n2 = n_int2_pages
         self.n3 = n_int3_pages
-        self.h = lib().orc_pool_new(num_kv_heads, n_int2_pages, n_int3_pages, n_int4_pages, max_requests,
-                                    max_pages_per_request, _p(sel), sel.size)
+        self.nf = n_fp4_pages
+        self.h = lib().orc_pool_new(num_kv_heads, n_int2_pages, n_int3_pages, n_fp4_pages, n_int4_pages,
+                                    max_requests, max_pages_per_request, _p(sel), sel.size)
         if not self.h:
             raise OracleError(INVALID, "orc_pool_new")
 

@@ -1,6 +1,6 @@
 /*
  * kvq_oracle.cpp -- plain, slow CPU oracle for decode attention over a paged,
- * mixed INT2/INT3/INT4 quantized KV cache.
+ * mixed INT2/INT3/INT4/FP4 quantized KV cache.
  *
  * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the
  * benchmark's CPU-baseline leg may load this library.  It shares no code with
@@ -76,6 +76,22 @@
  *      greedy allocation stays the pages' INT2/INT4 one (R7), and INT3 widths
  *      come from the caller
  *       [TriAxialKV, limitations and outlook: INT3 as a further width].
+ *   R12 FP4 pages.  The pages name non-uniform floating formats as a further
+ *      option and compare against a uniform FP4 cache.  Read as a fourth page
+ *      class holding E2M1 values (sign, 2 exponent bits with bias 1, 1
+ *      mantissa bit: magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6; code = sign << 3 |
+ *      exponent << 1 | mantissa), K and V per token in groups of 32 channels,
+ *      symmetric with the scale of the HyQuant background, s = max|x| / c_B
+ *      with c_B = 6 the format's largest value (fp32 division, stored as
+ *      binary16 as R1), no zero point; a value is coded as the E2M1 value
+ *      nearest to x / s (fp32 division), ties to the even mantissa, magnitudes
+ *      above 6 saturating to 6, zero coded +0; s = 0 codes every value 0;
+ *      dequantization x^ = s * value (exact in fp32).  Ids after the INT3 ids;
+ *      a request's FP4 tokens fill its own FP4 tail page; the reorder puts FP4
+ *      entries after INT4 entries; FP4 widths come from the caller
+ *       [TriAxialKV, limitations and outlook: non-uniform FP formats;
+ *        comparison with a uniform FP4 cache; HyQuant, background on
+ *        low-bit quantization: s = max|X| / c_B].
  *   R10 a full page none of whose 32 slots is live for any kv head may leave
  *      its request's table: the other entries keep their order and their
  *      pages do not move, its id returns to the free set, and the positions
@@ -100,6 +116,7 @@
 namespace {
 
 enum { ORC_OK = 0, ORC_INVALID = 1, ORC_OOM = 2, ORC_RANGE = 3, ORC_STATE = 6 };
+constexpr int kFP4 = 0xF4;     // the width value of FP4 (E2M1) tokens and pages (R12)
 constexpr int kD = 128;        // head dim
 constexpr int kP = 32;         // tokens per page
 constexpr int kG = 32;         // group size
@@ -199,6 +216,42 @@ inline float dequant(uint8_t code, uint16_t s, uint16_t z) {
 }
 
 // ---------------------------------------------------------------------------
+// FP4 (E2M1) group quantization (reading R12).
+// ---------------------------------------------------------------------------
+// magnitude of E2M1 code bits (exponent << 1 | mantissa): exponent 0 holds
+// 0 and the subnormal 0.5, exponent e > 0 holds (1 + mantissa / 2) * 2^(e-1)
+double e2m1_magnitude(int m) {
+  const int e = m >> 1, f = m & 1;
+  return e == 0 ? 0.5 * f : (1.0 + 0.5 * f) * std::ldexp(1.0, e - 1);
+}
+double e2m1_value(uint8_t code) { return (code & 8 ? -1.0 : 1.0) * e2m1_magnitude(code & 7); }
+
+void fp4_group(const float* x, int n, int stride, uint8_t* codes, int cstride, uint16_t* s_out) {
+  float amax = 0.0f;
+  for (int i = 0; i < n; ++i) amax = std::max(amax, std::fabs(x[(size_t)i * stride]));
+  volatile float s32 = amax / 6.0f;                 // one fp32 rounding
+  const uint16_t sh = f32_to_f16(s32);
+  const float sf = f16_to_f32(sh);
+  for (int i = 0; i < n; ++i) {
+    uint8_t c = 0;
+    if ((sh & 0x7FFFu) != 0) {
+      const float u = x[(size_t)i * stride] / sf;   // one fp32 rounding
+      const double a = std::fabs((double)u);
+      int best = 0;                                 // nearest magnitude, ties to the even mantissa
+      for (int m = 1; m < 8; ++m) {
+        const double d = std::fabs(a - e2m1_magnitude(m)), db = std::fabs(a - e2m1_magnitude(best));
+        if (d < db || (d == db && (m & 1) == 0)) best = m;
+      }
+      c = (uint8_t)(best == 0 ? 0 : ((u < 0.0f ? 8 : 0) | best));
+    }
+    codes[(size_t)i * cstride] = c;
+  }
+  *s_out = sh;
+}
+
+inline float dequant_fp4(uint8_t code, uint16_t s) { return (float)(e2m1_value(code) * (double)f16_to_f32(s)); }
+
+// ---------------------------------------------------------------------------
 // Pool model.
 // Canonical content of one (page, kv-head) block:
 //   kc[slot][ch], vc[slot][ch]      codes, one byte each
@@ -214,7 +267,7 @@ struct HeadBlock {
 
 struct Page {
   int32_t id = -1;
-  int bits = 4;                   // 2, 3 or 4 (the id's class)
+  int bits = 4;                   // 2, 3, 4 or kFP4 (the id's class)
   int fill = 0;
   uint32_t live = 0;
   std::vector<uint32_t> hdead;    // per kv head: slots excluded for that head only (R9)
@@ -226,7 +279,7 @@ struct Page {
 struct Req {
   bool open = false;
   std::vector<int32_t> table;
-  int32_t tail4 = -1, tail3 = -1, staging = -1;
+  int32_t tail4 = -1, tail3 = -1, tailf = -1, staging = -1;
   std::vector<uint32_t> loc;      // token position -> page_id << 5 | slot
   int64_t n_fp = 0;               // full-precision tokens (R8)
   std::vector<uint16_t> fpk, fpv; // their bf16 bits [n_fp][n_sel][128]
@@ -235,9 +288,9 @@ struct Req {
 struct Pool {
   int hkv = 0;
   std::vector<int> sel;           // kv heads whose content is kept
-  int64_t n2 = 0, n3 = 0, n4 = 0;
+  int64_t n2 = 0, n3 = 0, n4 = 0, nf = 0;
   int max_req = 0, max_pages = 0;
-  std::set<int32_t> free2, free3, free4;
+  std::set<int32_t> free2, free3, free4, freef;
   std::unordered_map<int32_t, Page> pages;
   std::vector<Req> reqs;
 };
@@ -253,7 +306,8 @@ int32_t take_lowest(std::set<int32_t>& s) {
 }
 
 Page& new_page(Pool* P, int bits, bool content) {
-  const int32_t id = take_lowest(bits == 2 ? P->free2 : (bits == 3 ? P->free3 : P->free4));
+  const int32_t id =
+      take_lowest(bits == 2 ? P->free2 : (bits == 3 ? P->free3 : (bits == kFP4 ? P->freef : P->free4)));
   Page& pg = P->pages[id];
   pg = Page();
   pg.id = id;
@@ -268,7 +322,7 @@ Page& new_page(Pool* P, int bits, bool content) {
 }
 
 // Per-token quantization of one token into `slot` at the page's width, 4 or 3
-// (key design 3; R11).
+// (key design 3; R11), or FP4 (R12: scale in the s entry, zero entry 0).
 void write_token(const Pool* P, Page& pg, int slot, const uint16_t* k, const uint16_t* v) {
   const int b = pg.bits;
   float xk[kD], xv[kD];
@@ -279,6 +333,13 @@ void write_token(const Pool* P, Page& pg, int slot, const uint16_t* k, const uin
       xv[c] = bf16_to_f32(v[j * kD + c]);
     }
     for (int gr = 0; gr < kD / kG; ++gr) {
+      if (b == kFP4) {
+        fp4_group(xk + gr * kG, kG, 1, hb.kc + slot * kD + gr * kG, 1, &hb.km[(slot * 4 + gr) * 2]);
+        fp4_group(xv + gr * kG, kG, 1, hb.vc + slot * kD + gr * kG, 1, &hb.vm[(slot * 4 + gr) * 2]);
+        hb.km[(slot * 4 + gr) * 2 + 1] = 0;
+        hb.vm[(slot * 4 + gr) * 2 + 1] = 0;
+        continue;
+      }
       quant_group(xk + gr * kG, kG, 1, b, hb.kc + slot * kD + gr * kG, 1,
                   &hb.km[(slot * 4 + gr) * 2], &hb.km[(slot * 4 + gr) * 2 + 1]);
       quant_group(xv + gr * kG, kG, 1, b, hb.vc + slot * kD + gr * kG, 1,
@@ -321,7 +382,8 @@ void free_id(Pool* P, int32_t id) {
   P->pages.erase(id);
   if (id < P->n2) P->free2.insert(id);
   else if (id < P->n2 + P->n4) P->free4.insert(id);
-  else P->free3.insert(id);
+  else if (id < P->n2 + P->n4 + P->n3) P->free3.insert(id);
+  else P->freef.insert(id);
 }
 
 }  // namespace
@@ -335,6 +397,15 @@ void orc_f32_to_f16(const float* x, uint16_t* out, int64_t n) {
 void orc_f16_to_f32(const uint16_t* x, float* out, int64_t n) {
   for (int64_t i = 0; i < n; ++i) out[i] = f16_to_f32(x[i]);
 }
+// One FP4 group of n values (R12): codes and the binary16 scale.
+int orc_fp4_group(const float* x, int n, uint16_t* s, uint8_t* codes) {
+  if (n <= 0) return ORC_INVALID;
+  for (int i = 0; i < n; ++i) if (!in_range(x[i])) return ORC_RANGE;
+  fp4_group(x, n, 1, codes, 1, s);
+  return ORC_OK;
+}
+double orc_e2m1_value(int code) { return e2m1_value((uint8_t)code); }
+
 // One group of n values at `bits` (2, 3 or 4).
 int orc_quant_group(const float* x, int n, int bits, uint16_t* s, uint16_t* z, uint8_t* codes) {
   if (n <= 0 || bits < 2 || bits > 4) return ORC_INVALID;
@@ -377,13 +448,14 @@ int orc_alloc_bits(const int64_t* N, const double* D2, const double* D4, int n_t
 // ---- pool --------------------------------------------------------------------
 // sel_heads: kv heads whose codes are materialized (n_sel of them); page ids,
 // tables, fills and live masks are modelled for every head regardless.
-void* orc_pool_new(int hkv, int64_t n2, int64_t n3, int64_t n4, int max_req, int max_pages,
+void* orc_pool_new(int hkv, int64_t n2, int64_t n3, int64_t nf, int64_t n4, int max_req, int max_pages,
                    const int* sel_heads, int n_sel) {
-  if (hkv <= 0 || n2 < 0 || n3 < 0 || n4 < 0 || max_req <= 0 || max_pages <= 0) return nullptr;
+  if (hkv <= 0 || n2 < 0 || n3 < 0 || nf < 0 || n4 < 0 || max_req <= 0 || max_pages <= 0) return nullptr;
   Pool* P = new Pool();
   P->hkv = hkv;
   P->n2 = n2;
   P->n3 = n3;
+  P->nf = nf;
   P->n4 = n4;
   P->max_req = max_req;
   P->max_pages = max_pages;
@@ -391,6 +463,7 @@ void* orc_pool_new(int hkv, int64_t n2, int64_t n3, int64_t n4, int max_req, int
   for (int64_t i = 0; i < n2; ++i) P->free2.insert((int32_t)i);
   for (int64_t i = 0; i < n4; ++i) P->free4.insert((int32_t)(n2 + i));
   for (int64_t i = 0; i < n3; ++i) P->free3.insert((int32_t)(n2 + n4 + i));
+  for (int64_t i = 0; i < nf; ++i) P->freef.insert((int32_t)(n2 + n4 + n3 + i));
   P->reqs.resize(max_req);
   return P;
 }
@@ -428,18 +501,18 @@ int orc_append(void* h, const uint16_t* k, const uint16_t* v, const int32_t* req
   const size_t nsel = P->sel.size();
   for (int64_t t = 0; t < n; ++t) {
     if (req[t] < 0 || req[t] >= P->max_req || !P->reqs[req[t]].open) return ORC_INVALID;
-    if (bits[t] < 2 || bits[t] > 4) return ORC_INVALID;
+    if ((bits[t] < 2 || bits[t] > 4) && bits[t] != kFP4) return ORC_INVALID;
   }
   if (content)
     for (int64_t i = 0; i < n * (int64_t)nsel * kD; ++i)
       if (!in_range(bf16_to_f32(k[i])) || !in_range(bf16_to_f32(v[i]))) return ORC_RANGE;
   // Dry run: count the pages this call takes and the table growth.
   struct Sim {
-    bool tail = false; int tailfill = 0; bool tail3 = false; int tail3fill = 0; bool stag = false; int stagfill = 0;
-    int64_t tablen = 0;
+    bool tail = false; int tailfill = 0; bool tail3 = false; int tail3fill = 0; bool tailf = false; int tailffill = 0;
+    bool stag = false; int stagfill = 0; int64_t tablen = 0;
   };
   std::unordered_map<int32_t, Sim> sim;
-  int64_t need4 = 0, need3 = 0, need2 = 0;
+  int64_t need4 = 0, need3 = 0, needf = 0, need2 = 0;
   for (int64_t t = 0; t < n; ++t) {
     auto it = sim.find(req[t]);
     if (it == sim.end()) {
@@ -447,6 +520,7 @@ int orc_append(void* h, const uint16_t* k, const uint16_t* v, const int32_t* req
       Sim s;
       if (R.tail4 >= 0) { s.tail = true; s.tailfill = P->pages.at(R.tail4).fill; }
       if (R.tail3 >= 0) { s.tail3 = true; s.tail3fill = P->pages.at(R.tail3).fill; }
+      if (R.tailf >= 0) { s.tailf = true; s.tailffill = P->pages.at(R.tailf).fill; }
       if (R.staging >= 0) { s.stag = true; s.stagfill = P->pages.at(R.staging).fill; }
       s.tablen = (int64_t)R.table.size();
       it = sim.emplace(req[t], s).first;
@@ -458,13 +532,17 @@ int orc_append(void* h, const uint16_t* k, const uint16_t* v, const int32_t* req
     } else if (bits[t] == 3) {
       if (!s.tail3 || s.tail3fill == kP) { ++need3; ++s.tablen; s.tail3 = true; s.tail3fill = 0; }
       ++s.tail3fill;
+    } else if (bits[t] == kFP4) {
+      if (!s.tailf || s.tailffill == kP) { ++needf; ++s.tablen; s.tailf = true; s.tailffill = 0; }
+      ++s.tailffill;
     } else {
       if (!s.stag) { ++need4; ++s.tablen; s.stag = true; s.stagfill = 0; }
       if (++s.stagfill == kP) { ++need2; s.stag = false; }
     }
     if (s.tablen > P->max_pages) return ORC_OOM;
   }
-  if (need4 > (int64_t)P->free4.size() || need3 > (int64_t)P->free3.size() || need2 > (int64_t)P->free2.size())
+  if (need4 > (int64_t)P->free4.size() || need3 > (int64_t)P->free3.size() || needf > (int64_t)P->freef.size() ||
+      need2 > (int64_t)P->free2.size())
     return ORC_OOM;
 
   std::vector<int32_t> deferred;
@@ -473,10 +551,11 @@ int orc_append(void* h, const uint16_t* k, const uint16_t* v, const int32_t* req
     const int64_t pos = (int64_t)R.loc.size();
     const uint16_t* kt = content ? k + (size_t)t * nsel * kD : nullptr;
     const uint16_t* vt = content ? v + (size_t)t * nsel * kD : nullptr;
-    // INT4 and INT2 tokens go to INT4 pages (the tail, the staging page); INT3 to the INT3 tail
-    int32_t& cur = bits[t] == 4 ? R.tail4 : (bits[t] == 3 ? R.tail3 : R.staging);
+    // INT4 and INT2 tokens go to INT4 pages (the tail, the staging page); INT3
+    // and FP4 tokens to their own tails
+    int32_t& cur = bits[t] == 4 ? R.tail4 : (bits[t] == 3 ? R.tail3 : (bits[t] == kFP4 ? R.tailf : R.staging));
     if (cur < 0 || P->pages.at(cur).fill == kP) {
-      Page& pg = new_page(P, bits[t] == 3 ? 3 : 4, content);
+      Page& pg = new_page(P, bits[t] == 2 ? 4 : bits[t], content);
       cur = pg.id;
       R.table.push_back(pg.id);
     }
@@ -502,7 +581,8 @@ int orc_append(void* h, const uint16_t* k, const uint16_t* v, const int32_t* req
 }
 
 // INT2-first stable reorder of each listed request's table (TriAxialKV key
-// design 4, phase 1); with INT3 pages the table is sorted stably by width (R11).
+// design 4, phase 1); with INT3 or FP4 pages the table is sorted stably by
+// width: INT2, INT3, INT4, FP4 (R11, R12).
 int orc_reorder(void* h, const int32_t* req, int n) {
   Pool* P = (Pool*)h;
   for (int i = 0; i < n; ++i)
@@ -510,7 +590,7 @@ int orc_reorder(void* h, const int32_t* req, int n) {
   for (int i = 0; i < n; ++i) {
     auto& tb = P->reqs[req[i]].table;
     std::stable_sort(tb.begin(), tb.end(),
-                     [P](int32_t a, int32_t b) { return P->pages.at(a).bits < P->pages.at(b).bits; });
+                     [P](int32_t a, int32_t b) { return P->pages.at(a).bits < P->pages.at(b).bits; });   // kFP4 > 4
   }
   return ORC_OK;
 }
@@ -554,6 +634,7 @@ int orc_drop_dead_pages(void* h, const int32_t* req, int n) {
       for (int s = 0; s < kP; ++s) R.loc[(size_t)pg.pos[s]] = kDropped;
       if (R.tail4 == id) R.tail4 = -1;
       if (R.tail3 == id) R.tail3 = -1;
+      if (R.tailf == id) R.tailf = -1;
       if (R.staging == id) R.staging = -1;
       free_id(P, id);
     }
@@ -681,7 +762,7 @@ int orc_decode(void* h, const uint16_t* q, const int32_t* req, int B, int Hq, fl
     std::vector<double> logit;
     std::vector<std::pair<const HeadBlock*, int>> src;
     std::vector<const uint16_t*> fprow;
-    std::vector<bool> alive;
+    std::vector<bool> alive, vfp4;   // vfp4: V of an FP4 page (R12)
     for (int32_t pid : R.table) {
       const Page& pg = P->pages.at(pid);
       const HeadBlock& hb = pg.heads[j];
@@ -693,7 +774,9 @@ int orc_decode(void* h, const uint16_t* q, const int32_t* req, int B, int Hq, fl
           double acc = 0.0;
           for (int c = 0; c < kD; ++c) {
             const int mi = pg.bits == 2 ? c * 2 : (s * 4 + c / kG) * 2;
-            acc += qd[c] * (double)dequant(hb.kc[s * kD + c], hb.km[mi], hb.km[mi + 1]);
+            const float kh = pg.bits == kFP4 ? dequant_fp4(hb.kc[s * kD + c], hb.km[mi])
+                                             : dequant(hb.kc[s * kD + c], hb.km[mi], hb.km[mi + 1]);
+            acc += qd[c] * (double)kh;
           }
           l = (double)scale * acc;
         }
@@ -701,6 +784,7 @@ int orc_decode(void* h, const uint16_t* q, const int32_t* req, int B, int Hq, fl
         src.push_back({&hb, s});
         fprow.push_back(nullptr);
         alive.push_back(lv);
+        vfp4.push_back(pg.bits == kFP4);
       }
     }
     const size_t nsel = P->sel.size();
@@ -712,6 +796,7 @@ int orc_decode(void* h, const uint16_t* q, const int32_t* req, int B, int Hq, fl
       src.push_back({nullptr, 0});
       fprow.push_back(R.fpv.data() + ((size_t)t * nsel + j) * kD);
       alive.push_back(true);
+      vfp4.push_back(false);
     }
     double* o = out + (size_t)i * kD;
     for (int c = 0; c < kD; ++c) o[c] = 0.0;
@@ -735,9 +820,11 @@ int orc_decode(void* h, const uint16_t* q, const int32_t* req, int B, int Hq, fl
         }
         const HeadBlock& hb = *src[t].first;
         const int s = src[t].second;
+        const bool f4 = vfp4[t];
         for (int c = 0; c < kD; ++c) {
           const int mi = (s * 4 + c / kG) * 2;
-          acc[c] += w * (double)dequant(hb.vc[s * kD + c], hb.vm[mi], hb.vm[mi + 1]);
+          acc[c] += w * (double)(f4 ? dequant_fp4(hb.vc[s * kD + c], hb.vm[mi])
+                                    : dequant(hb.vc[s * kD + c], hb.vm[mi], hb.vm[mi + 1]));
         }
       }
       ms.push_back(m);
