@@ -86,13 +86,19 @@ typedef struct {
   int32_t max_pages_per_request;  /* table capacity of one request */
   int32_t device;                 /* CUDA device ordinal */
   int64_t n_int3_pages;           /* INT3 page ids are [n2 + n4, n2 + n4 + n_int3_pages); 0: none */
+  int64_t n_fp4_pages;            /* FP4 (E2M1) page ids follow the INT3 ids; 0: none */
 } kv_pool_config_t;
+
+/* Width value of FP4 (E2M1) tokens in kv_append_quant's bits array. */
+#define KV_WIDTH_FP4 0xF4
 
 /* Create a pool: one device allocation holding the INT2 region followed by the
  * INT4 region (TriAxialKV key design 4) and, with n_int3_pages > 0, the INT3
  * region (TriAxialKV, limitations and outlook: INT3 as a further width; an
- * INT3 block is 4096 bytes per page and kv head), plus the device page
- * tables.  out: host pointer receiving the handle. */
+ * INT3 block is 4096 bytes per page and kv head) and, with n_fp4_pages > 0,
+ * the FP4 region (the same section's non-uniform FP formats; 4608 bytes per
+ * block), plus the device page tables.  out: host pointer receiving the
+ * handle. */
 KVQ_API kv_status_t kv_pool_create(const kv_pool_config_t* cfg, kv_pool_t** out);
 
 /* Free everything the pool owns.  Synchronizes with the pool's device work. */
@@ -110,6 +116,10 @@ KVQ_API kv_status_t kv_request_close(kv_pool_t* pool, int32_t req_id);
  *   bits     host, uint8 [n_tok]: 4 -> the request's INT4 tail page;
  *            3 -> the request's INT3 tail page (K and V per token in groups of
  *            32 channels, codes 0..7, as INT4; needs n_int3_pages > 0);
+ *            KV_WIDTH_FP4 -> the request's FP4 tail page (E2M1 values, K and V
+ *            per token in groups of 32 channels with a binary16 scale
+ *            max|x| / 6 and no zero point; the nearest value, ties to the even
+ *            mantissa; needs n_fp4_pages > 0);
  *            2 -> the request's INT4 staging page, which is requantized into a
  *            new INT2 page (K per channel, V per token) as soon as it holds 32
  *            tokens; that INT2 page is appended to the request's table.
@@ -120,8 +130,8 @@ KVQ_API kv_status_t kv_append_quant(kv_pool_t* pool, const void* k, const void* 
                             const uint8_t* bits, int64_t n_tok, void* stream);
 
 /* Phase-1 reorder (TriAxialKV key design 4): stable partition of each listed
- * request's table so INT2 entries precede INT4 entries; with INT3 pages, a
- * stable sort by width (INT2, INT3, INT4).  req_ids: host [n_req]. */
+ * request's table so INT2 entries precede INT4 entries; with INT3 or FP4
+ * pages, a stable sort by width (INT2, INT3, INT4, FP4).  req_ids: host [n_req]. */
 KVQ_API kv_status_t kv_reorder_pages(kv_pool_t* pool, const int32_t* req_ids, int32_t n_req, void* stream);
 
 /* Layout-preserving eviction (IntentKV method 2): clear the live bit of each

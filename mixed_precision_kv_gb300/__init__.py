@@ -21,6 +21,7 @@ LIB_PATH = os.path.join(_HERE, "libkvq.so")
 KV_OK, KV_ERR_INVALID_ARG, KV_ERR_OOM, KV_ERR_RANGE, KV_ERR_CUDA, KV_ERR_DEVICE_TIMEOUT, KV_ERR_STATE = range(7)
 KV_DECODE_AUTO, KV_DECODE_SIMT, KV_DECODE_MMA = 0, 1, 2
 HEAD_DIM, PAGE_TOKENS, GROUP = 128, 32, 32
+KV_WIDTH_FP4 = 0xF4   # width value of FP4 (E2M1) tokens
 
 EXPORTED = ["kv_pool_create", "kv_pool_destroy", "kv_request_open", "kv_request_close", "kv_append_quant",
             "kv_reorder_pages", "kv_evict_slots", "kv_decode_attn", "kv_set_decode_impl", "kv_pool_sync",
@@ -39,7 +40,7 @@ class KVConfig(ctypes.Structure):
     _fields_ = [("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("page_tokens", ctypes.c_int32),
                 ("group", ctypes.c_int32), ("n_int2_pages", ctypes.c_int64), ("n_int4_pages", ctypes.c_int64),
                 ("max_requests", ctypes.c_int32), ("max_pages_per_request", ctypes.c_int32),
-                ("device", ctypes.c_int32), ("n_int3_pages", ctypes.c_int64)]
+                ("device", ctypes.c_int32), ("n_int3_pages", ctypes.c_int64), ("n_fp4_pages", ctypes.c_int64)]
 
 
 class KVError(RuntimeError):
@@ -148,10 +149,10 @@ class KVPool:
     """A paged INT2/INT4 pool on one GPU (see include/kvq.h for every call's contract)."""
 
     def __init__(self, num_kv_heads, n_int2_pages, n_int4_pages, max_requests, max_pages_per_request, device=0,
-                 n_int3_pages=0):
+                 n_int3_pages=0, n_fp4_pages=0):
         L = load_library()
         cfg = KVConfig(num_kv_heads, HEAD_DIM, PAGE_TOKENS, GROUP, n_int2_pages, n_int4_pages, max_requests,
-                       max_pages_per_request, device, n_int3_pages)
+                       max_pages_per_request, device, n_int3_pages, n_fp4_pages)
         h = _P()
         _check(L.kv_pool_create(ctypes.byref(cfg), ctypes.byref(h)), "kv_pool_create")
         self._h = h
@@ -159,6 +160,7 @@ class KVPool:
         self.num_kv_heads = num_kv_heads
         self.n_int2_pages = n_int2_pages
         self.n_int3_pages = n_int3_pages
+        self.n_fp4_pages = n_fp4_pages
         self.device = device
 
     @property

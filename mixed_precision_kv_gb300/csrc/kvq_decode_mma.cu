@@ -78,7 +78,8 @@ struct alignas(16) WarpSmem {
   const uint32_t* hdead;               // exclusion words (read from here at each refill, not kept in a register)
 };
 static_assert(sizeof(WarpSmem) % 16 == 0 && kStageBytes % 16 == 0, "stage buffers must stay 16-byte aligned");
-static_assert(kInt2Block <= kStageBytes && kInt3Block <= kStageBytes, "every block fits a stage");
+static_assert(kInt2Block <= kStageBytes && kInt3Block <= kStageBytes && kFp4Block <= kStageBytes,
+              "every block fits a stage");
 
 // q-side operands of one unit (batch row, kv head), built by frag_kernel.
 struct alignas(16) UnitFrag {
@@ -121,6 +122,16 @@ __device__ __forceinline__ uint32_t shl_s(uint32_t x, int s) { return s >= 0 ? x
 __device__ __forceinline__ uint32_t i3reg(uint32_t lo, int sl, uint32_t hi, int sh) {
   return (shl_s(lo, sl) & kC6) | (shl_s(hi, sh) & kB8);
 }
+// An FP4 A register: the two E2M1 codes of the low byte of x (low nibble ->
+// low half) as binary16 values (exact: E2M1 values have 2 significant bits).
+// FP4 products are therefore 2^18 larger than the code * 2^-18 fields of the
+// integer widths; the callers rescale them in fp32.
+__device__ __forceinline__ uint32_t f4reg(uint32_t x) {
+  uint32_t d;
+  asm("{.reg .b8 t;\n cvt.u8.u32 t, %1;\n cvt.rn.f16x2.e2m1x2 %0, t;\n}" : "=r"(d) : "r"(x));
+  return d;
+}
+constexpr float kFp4Unit = 1.0f / 262144.0f;   // 2^-18: FP4 products in the integer widths' units
 // INT2 code word variants: variant jj puts two 2-bit fields of each half at
 // bits 6 and 8.  Scale/zero pair index (register j of the pair order) of the
 // field at bit 6 and at bit 8 of variant jj.
@@ -240,7 +251,7 @@ struct Cols {
 // ---- logits of one INT4 (kI3: INT3) page: lg[m][e][hh] for token 16m + r + 8e
 // and the lane's head hh (log2 units, scale folded in).  An INT3 page has the
 // INT4 page's per-token groups and scale/zero; only its code words differ.
-template <int G, bool kI3 = false>
+template <int G, bool kI3 = false, bool kF4 = false>
 __device__ __forceinline__ void qk_int4(const uint8_t* blk, const uint4* bq4, const uint32_t (&bz)[2],
                                         const float (&acol)[Cols<G>::NH], float (&lg)[2][2][Cols<G>::NH]) {
   constexpr bool kPair = Cols<G>::kPair;
@@ -254,12 +265,15 @@ __device__ __forceinline__ void qk_int4(const uint8_t* blk, const uint4* bq4, co
 #pragma unroll
   for (int m = 0; m < 2; ++m) {
     uint4 kw[2], km[2];
-    uint2 kl[2];
+    uint2 kl[2], ks[2];
     uint32_t kh[2];
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       const int t = 16 * m + r + 8 * e;
-      if constexpr (kI3) {
+      if constexpr (kF4) {
+        kw[e] = *reinterpret_cast<const uint4*>(blk + kF4KCodes + 64 * t + 16 * i);
+        ks[e] = *reinterpret_cast<const uint2*>(blk + kF4KScale + 8 * t);
+      } else if constexpr (kI3) {
         kl[e] = *reinterpret_cast<const uint2*>(blk + kI3KCodes + 48 * t + 8 * i);
         kh[e] = *reinterpret_cast<const uint32_t*>(blk + kI3KCodes + 48 * t + 32 + 4 * i);
         km[e] = *reinterpret_cast<const uint4*>(blk + kI3KMeta + 16 * t);
@@ -271,7 +285,13 @@ __device__ __forceinline__ void qk_int4(const uint8_t* blk, const uint4* bq4, co
     // Group gr's k-steps: nibbles 0/4 at p = 6, 1/5 at p = 4, then 2/6 and 3/7 at p = 6.
     // INT3: channels n / n + 4 at p = 6 for every n (the q fragments carry no 2^2).
     auto group_mma = [&](float (&acc)[4], int gr) {
-      if constexpr (kI3) {
+      if constexpr (kF4) {
+        // FP4: byte n of a word holds channels n and n + 4
+        const uint32_t x0 = comp(kw[0], gr), x1 = comp(kw[1], gr);
+        mma16816(acc, f4reg(x0), f4reg(x1), f4reg(x0 >> 8), f4reg(x1 >> 8), bq[4 * gr], bq[4 * gr + 1]);
+        mma16816(acc, f4reg(x0 >> 16), f4reg(x1 >> 16), f4reg(x0 >> 24), f4reg(x1 >> 24), bq[4 * gr + 2],
+                 bq[4 * gr + 3]);
+      } else if constexpr (kI3) {
         const uint32_t l0 = gr < 2 ? kl[0].x : kl[0].y, l1 = gr < 2 ? kl[1].x : kl[1].y;
         const int o = 8 * (gr & 1);
         auto reg = [&](uint32_t l, uint32_t h, int n) { return i3reg(l, 6 - o - 2 * n, h, 8 - 4 * gr - n); };
@@ -289,9 +309,21 @@ __device__ __forceinline__ void qk_int4(const uint8_t* blk, const uint4* bq4, co
     // zero term sum_g zero_tg * (scale log2e Q_g) by one mma: every lane feeds
     // (zero_0, zero_1) in k-slots 2i, 2i+1 and (zero_2, zero_3) in 2i+8, 2i+9;
     // B rows 0, 1 / 8, 9 hold the hi parts of Q, rows 2, 3 / 10, 11 the lo
-    // parts, the other rows zero.
-    const uint32_t az0 = __byte_perm(km[0].x, km[0].y, 0x7632), az2 = __byte_perm(km[0].z, km[0].w, 0x7632);
-    const uint32_t az1 = __byte_perm(km[1].x, km[1].y, 0x7632), az3 = __byte_perm(km[1].z, km[1].w, 0x7632);
+    // parts, the other rows zero.  FP4 groups have no zero point.
+    uint32_t az0 = 0u, az1 = 0u, az2 = 0u, az3 = 0u;
+    if constexpr (!kF4) {
+      az0 = __byte_perm(km[0].x, km[0].y, 0x7632); az2 = __byte_perm(km[0].z, km[0].w, 0x7632);
+      az1 = __byte_perm(km[1].x, km[1].y, 0x7632); az3 = __byte_perm(km[1].z, km[1].w, 0x7632);
+    }
+    // the scale of group gr of token e (FP4: the products carry 2^18 more)
+    auto ksc = [&](int e, int gr) -> float {
+      if constexpr (kF4) {
+        const uint32_t w = gr < 2 ? ks[e].x : ks[e].y;
+        return ((gr & 1) ? h_hi(w) : h_lo(w)) * kFp4Unit;
+      } else {
+        return h_lo(comp(km[e], gr));
+      }
+    };
     if constexpr (kPair) {
       // acc[0]: groups 0 / 1 in columns 2h / 2h+1, acc[1]: groups 2 / 3
       float acc[2][4];
@@ -304,13 +336,13 @@ __device__ __forceinline__ void qk_int4(const uint8_t* blk, const uint4* bq4, co
       float T[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        float v = h_lo(km[e].x) * acc[0][2 * e];
-        v = fmaf(h_lo(km[e].y), acc[0][2 * e + 1], v);
-        v = fmaf(h_lo(km[e].z), acc[1][2 * e], v);
-        v = fmaf(h_lo(km[e].w), acc[1][2 * e + 1], v);
+        float v = ksc(e, 0) * acc[0][2 * e];
+        v = fmaf(ksc(e, 1), acc[0][2 * e + 1], v);
+        v = fmaf(ksc(e, 2), acc[1][2 * e], v);
+        v = fmaf(ksc(e, 3), acc[1][2 * e + 1], v);
         T[2 * e] = v * acol[0];
       }
-      mma16816(T, az0, az1, az2, az3, bz[0], bz[1]);   // B: even columns only
+      if constexpr (!kF4) mma16816(T, az0, az1, az2, az3, bz[0], bz[1]);   // B: even columns only
       lg[m][0][0] = T[0];
       lg[m][1][0] = T[2];
     } else {
@@ -326,10 +358,10 @@ __device__ __forceinline__ void qk_int4(const uint8_t* blk, const uint4* bq4, co
         const int e = c >> 1;
         float v = 0.0f;
 #pragma unroll
-        for (int gr = 0; gr < 4; ++gr) v = fmaf(h_lo(comp(km[e], gr)), acc[gr][c], v);
+        for (int gr = 0; gr < 4; ++gr) v = fmaf(ksc(e, gr), acc[gr][c], v);
         T[c] = v * acol[c & 1];
       }
-      mma16816(T, az0, az1, az2, az3, bz[0], bz[1]);
+      if constexpr (!kF4) mma16816(T, az0, az1, az2, az3, bz[0], bz[1]);
 #pragma unroll
       for (int c = 0; c < 4; ++c) lg[m][c >> 1][c & 1] = T[c];
     }
@@ -456,7 +488,7 @@ __device__ __forceinline__ void qk_int2(const uint8_t* blk, const UnitFrag* __re
 
 // ---- online softmax update and P.V for one page (any width; kInt3: an INT3
 // page, read as an INT4 page with INT3 code words)
-template <int G, bool kInt2, bool kInt3 = false>
+template <int G, bool kInt2, bool kInt3 = false, bool kFp4 = false>
 __device__ __forceinline__ void softmax_pv(const uint8_t* blk, uint32_t live, float pscale,
                                            float (&lg)[2][2][Cols<G>::NH], const float (&zc)[Cols<G>::NH],
                                            float (&o)[8][4], float (&zv)[4],
@@ -464,7 +496,7 @@ __device__ __forceinline__ void softmax_pv(const uint8_t* blk, uint32_t live, fl
                                            float (*pbuf)[kPage]) {
   constexpr bool kPair = Cols<G>::kPair;
   constexpr int NH = Cols<G>::NH;
-  constexpr int vmeta = kInt2 ? kI2VMeta : (kInt3 ? kI3VMeta : kI4VMeta);
+  constexpr int vmeta = kInt2 ? kI2VMeta : (kInt3 ? kI3VMeta : (kFp4 ? kF4VScale : kI4VMeta));
   const int lane = threadIdx.x & 31, r = lane >> 2, i = lane & 3;
   const bool full = live == 0xFFFFFFFFu;   // warp-uniform: no dead slot on this page
   if (!full) {
@@ -548,8 +580,9 @@ __device__ __forceinline__ void softmax_pv(const uint8_t* blk, uint32_t live, fl
   }
   // V zero term: rows = groups (lanes r < 4), k = slots.  Lanes r >= 4 load
   // group r - 4 as well (no branch): their rows 4..7 of the product are
-  // finite and never read (only lanes r < 4 store the zero terms).
-  {
+  // finite and never read (only lanes r < 4 store the zero terms).  FP4
+  // groups have no zero point.
+  if constexpr (!kFp4) {
     uint4 zz = *reinterpret_cast<const uint4*>(blk + vmeta + 256 + 64 * (r & 3) + 16 * i);
     if (kInt2) {   // undo the 2^-2 of the even slots' P: words 0 and 2 hold slot pairs (8i, 8i+4), (8i+2, 8i+6)
       zz.x = hmul2(zz.x, 0x44004400u);
@@ -601,6 +634,9 @@ __device__ __forceinline__ void softmax_pv(const uint8_t* blk, uint32_t live, fl
     if (kInt2) {
       const uint2 v2 = *reinterpret_cast<const uint2*>(blk + kI2VCodes + 16 * (32 * (gr >> 1) + 4 * r + i) + 8 * (gr & 1));
       wv[0] = v2.x; wv[1] = v2.y;
+    } else if (kFp4) {
+      const uint4 v4 = *reinterpret_cast<const uint4*>(blk + kF4VCodes + 16 * (32 * gr + 4 * r + i));
+      wv[0] = v4.x; wv[1] = v4.y; wv[2] = v4.z; wv[3] = v4.w;
     } else if (kInt3) {
       const int X = 32 * gr + 4 * r + i;
       const uint2 v3 = *reinterpret_cast<const uint2*>(blk + kI3VCodes + 8 * X);
@@ -621,6 +657,11 @@ __device__ __forceinline__ void softmax_pv(const uint8_t* blk, uint32_t live, fl
         a[0][2] = xl & kC6; a[0][3] = xr & kC6;    // slots (8i+1, 8i+5), p = 6
         a[1][0] = xl & kC8; a[1][1] = xr & kC8;    // slots (8i+2, 8i+6), p = 8
         a[1][2] = x & kC6; a[1][3] = xo & kC6;     // slots (8i+3, 8i+7), p = 6
+      } else if (kFp4) {
+        // slot 8i+k and 8i+k+4 of channel 16m+r (+8 for e = 1) in byte k of the word
+        const uint32_t w0 = wv[2 * mm], w1 = wv[2 * mm + 1];
+        a[0][0] = f4reg(w0); a[0][1] = f4reg(w1); a[0][2] = f4reg(w0 >> 8); a[0][3] = f4reg(w1 >> 8);
+        a[1][0] = f4reg(w0 >> 16); a[1][1] = f4reg(w1 >> 16); a[1][2] = f4reg(w0 >> 24); a[1][3] = f4reg(w1 >> 24);
       } else if (kInt3) {
         // channel 16m+r (e = 0) and 16m+r+8 (e = 1): slot 8i+k's low bits at
         // 8e + 2k of plane word mm, bit 2 at 4(2mm + e) + k of the high word
@@ -646,8 +687,13 @@ __device__ __forceinline__ void softmax_pv(const uint8_t* blk, uint32_t live, fl
         mma16816(t, a[0][0], a[0][1], a[0][2], a[0][3], bl[0], bl[1]);
         mma16816(t, a[1][0], a[1][1], a[1][2], a[1][3], bl[2], bl[3]);
       }
-      add2(o[m][0], o[m][1], t[0], t[1]);
-      add2(o[m][2], o[m][3], t[2], t[3]);
+      if constexpr (kFp4) {
+#pragma unroll
+        for (int x = 0; x < 4; ++x) o[m][x] = fmaf(t[x], kFp4Unit, o[m][x]);
+      } else {
+        add2(o[m][0], o[m][1], t[0], t[1]);
+        add2(o[m][2], o[m][3], t[2], t[3]);
+      }
     }
   }
   __syncwarp();
@@ -809,7 +855,8 @@ __global__ void __launch_bounds__(256) frag_kernel(const __nv_bfloat16* __restri
 // several pools (head groups, each with its own pages and tables): a split
 // names its pool and its kv head within the pool, the page stream reads the
 // pool's addresses from gpools, and a page ticket carries its width.  kI3:
-// the pool has INT3 pages (ids from n3b, blocks from int3_off).
+// the pool has INT3 pages (ids [n3b, nfb), blocks from int3_off) or FP4
+// pages (ids from nfb, blocks from fp4_off).
 template <int G, bool kHead, bool kMulti, bool kI3>
 __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(
     const uint8_t* __restrict__ pool, size_t int4_off, int64_t n2, int hkv, int max_pages,
@@ -817,7 +864,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(
     const int32_t* __restrict__ wsplit, int n_workers, const int32_t* __restrict__ ntab,
     const uint32_t* __restrict__ hdead, float* __restrict__ part, const uint32_t* __restrict__ smax_bits,
     uint32_t* __restrict__ status, uint32_t first_spins, const GroupPool* __restrict__ gpools, size_t int3_off,
-    int64_t n3b) {
+    int64_t n3b, size_t fp4_off, int64_t nfb) {
   constexpr bool kPair = Cols<G>::kPair;
   constexpr int NH = Cols<G>::NH;
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -930,8 +977,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(
         btag = (lsg << 6) | lkvh;
         const uint8_t* src = e.id < n2 ? pool + ((size_t)e.id * hkv + lkvh) * kInt2Block
                                        : pool + int4_off + ((size_t)(e.id - n2) * hkv + lkvh) * kInt4Block;
-        if constexpr (kI3)
-          if (e.id >= n3b) src = pool + int3_off + ((size_t)(e.id - n3b) * hkv + lkvh) * kInt3Block;
+        if constexpr (kI3) {
+          if (e.id >= nfb) src = pool + fp4_off + ((size_t)(e.id - nfb) * hkv + lkvh) * kFp4Block;
+          else if (e.id >= n3b) src = pool + int3_off + ((size_t)(e.id - n3b) * hkv + lkvh) * kInt3Block;
+        }
         bsrc = (unsigned long long)(uintptr_t)src;
       }
     }
@@ -967,13 +1016,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(
   // a ticket's width and split
   auto tk_int2 = [&](const Ticket& t) { return kMulti ? ((t.tag >> 6) & 1) != 0 : t.id < n2; };
   auto tk_split = [&](const Ticket& t) { return kMulti ? t.tag >> 7 : t.tag >> 6; };
-  auto tk_int3 = [&](const Ticket& t) { return kI3 && t.id >= n3b; };
+  auto tk_int3 = [&](const Ticket& t) { return kI3 && t.id >= n3b && t.id < nfb; };
+  auto tk_fp4 = [&](const Ticket& t) { return kI3 && t.id >= nfb; };
   // copy number n goes to stage n & 1 and completes phase (n >> 1) & 1
   auto issue = [&](const Ticket& t, unsigned long long src, uint32_t n) {   // lane 0
     const uint32_t st = n & (kStages - 1);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the stage was read generically
     bulk_load(WS.stage[st], (const void*)(uintptr_t)src,
-              tk_int2(t) ? (uint32_t)kInt2Block : (tk_int3(t) ? (uint32_t)kInt3Block : (uint32_t)kInt4Block),
+              tk_int2(t)   ? (uint32_t)kInt2Block
+              : tk_int3(t) ? (uint32_t)kInt3Block
+              : tk_fp4(t)  ? (uint32_t)kFp4Block
+                           : (uint32_t)kInt4Block,
               &WS.bar[st]);
   };
   static_assert(kStages == 2, "the ticket ring below serves a two-stage copy ring");
@@ -1098,6 +1151,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(
         for (int hh = 0; hh < NH; ++hh) zc[hh] = 0.0f;
         softmax_pv<G, false, true>(blk, t0.live, pscale, lg, zc, o, zv, mrun, lsum, WS.pbuf);
       }
+    } else if (tk_fp4(t0)) {
+      if constexpr (kI3) {
+        // FP4 codes pair channels n, n + 4 with no 2^2: the INT3 q fragments
+        qk_int4<G, false, true>(blk, &F->bq3[0][0], bz, acol4, lg);
+#pragma unroll
+        for (int hh = 0; hh < NH; ++hh) zc[hh] = 0.0f;
+        softmax_pv<G, false, false, true>(blk, t0.live, pscale, lg, zc, o, zv, mrun, lsum, WS.pbuf);
+      }
     } else {
       qk_int4<G>(blk, &F->bq4[0][0], bz, acol4, lg);
 #pragma unroll
@@ -1168,9 +1229,9 @@ cudaError_t launch_mma_g(kv_pool* P, const void* q, int32_t hq, float scale_log2
                              (int)hq, scale_log2, d_units, smax, (UnitFrag*)d_frags, d_gpools);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)((n_workers + kWarps - 1) / kWarps);
-  // pools with INT3 pages take the variant that reads them (grouped decodes
-  // take no such pool)
-  const bool i3 = P->cfg.n_int3_pages > 0;
+  // pools with INT3 or FP4 pages take the variant that reads them (grouped
+  // decodes take no such pool)
+  const bool i3 = P->cfg.n_int3_pages > 0 || P->cfg.n_fp4_pages > 0;
   auto* kernel = d_gpools ? decode_mma_kernel<G, false, true, false>
                  : i3     ? (P->hdead.empty() ? decode_mma_kernel<G, false, false, true>
                                               : decode_mma_kernel<G, true, false, true>)
@@ -1181,7 +1242,8 @@ cudaError_t launch_mma_g(kv_pool* P, const void* q, int32_t hq, float scale_log2
                     (const Entry*)P->d_table, (const UnitFrag*)d_frags, d_splits, d_wsplit, n_workers,
                     (const int32_t*)P->d_ntab, (const uint32_t*)P->d_hdead, d_part, smax, P->d_status,
                     P->first_wait_spins < 0 ? kSpinLimit : (uint32_t)P->first_wait_spins, d_gpools, P->int3_offset,
-                    (int64_t)(P->cfg.n_int2_pages + P->cfg.n_int4_pages));
+                    (int64_t)(P->cfg.n_int2_pages + P->cfg.n_int4_pages), P->fp4_offset,
+                    (int64_t)(P->cfg.n_int2_pages + P->cfg.n_int4_pages + P->cfg.n_int3_pages));
 }
 
 template <int G>

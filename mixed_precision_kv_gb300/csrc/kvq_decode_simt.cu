@@ -44,7 +44,7 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(
     const Entry* __restrict__ table, const __nv_bfloat16* __restrict__ q, int hq, float scale_log2,
     const Unit* __restrict__ units, const Split* __restrict__ splits, const int32_t* __restrict__ cta_split,
     const int32_t* __restrict__ ntab, const uint32_t* __restrict__ hdead, float* __restrict__ part, size_t int3_off,
-    int64_t n3b) {
+    int64_t n3b, size_t fp4_off, int64_t nfb) {
   asm volatile("griddepcontrol.wait;" ::: "memory");   // the appends before this decode are done
   asm volatile("griddepcontrol.launch_dependents;");   // the merge may be scheduled as CTAs retire
   __shared__ float qs[G][kHeadDim];
@@ -78,11 +78,13 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(
     const Entry e = tab[pi];
     // slots excluded for this kv head only read as dead slots too
     const uint32_t live = hdead ? e.live & ~hdead[(size_t)e.id * hkv + u.kvh] : e.live;
-    const bool i2 = e.id < n2, i3 = e.id >= n3b;   // INT3 ids follow the INT4 ids
+    // INT3 ids follow the INT4 ids, FP4 ids the INT3 ids
+    const bool i2 = e.id < n2, f4 = e.id >= nfb, i3 = e.id >= n3b && !f4;
     const uint8_t* blk = i2   ? pool + ((size_t)e.id * hkv + u.kvh) * kInt2Block
                          : i3 ? pool + int3_off + ((size_t)(e.id - n3b) * hkv + u.kvh) * kInt3Block
+                         : f4 ? pool + fp4_off + ((size_t)(e.id - nfb) * hkv + u.kvh) * kFp4Block
                               : pool + int4_off + ((size_t)(e.id - n2) * hkv + u.kvh) * kInt4Block;
-    const int nbytes = i2 ? kInt2Block : (i3 ? kInt3Block : kInt4Block);
+    const int nbytes = i2 ? kInt2Block : (i3 ? kInt3Block : (f4 ? kFp4Block : kInt4Block));
     for (int o = lane * 16; o < nbytes; o += 512)
       *reinterpret_cast<uint4*>(bw + o) = *reinterpret_cast<const uint4*>(blk + o);
     __syncwarp();
@@ -99,6 +101,16 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(
         const float kh = __fmaf_rn((float)code, ld_half(bw + kI2KMeta + 2 * mi), ld_half(bw + kI2KMeta + 256 + 2 * mi));
 #pragma unroll
         for (int h = 0; h < G; ++h) s[h] = __fmaf_rn(qs[h][c], kh, s[h]);
+      }
+    } else if (f4) {
+      for (int gr = 0; gr < 4; ++gr) {
+        const float sf = ld_half(bw + kF4KScale + 8 * t + 2 * gr);
+        for (int cc = 0; cc < kGroup; ++cc) {
+          const int c = kGroup * gr + cc;
+          const float kh = e2m1_value(((uint32_t)bw[f4k_byte(t, c)] >> f4k_shift(c)) & 15u) * sf;
+#pragma unroll
+          for (int h = 0; h < G; ++h) s[h] = __fmaf_rn(qs[h][c], kh, s[h]);
+        }
       }
     } else {
       const int kmeta = i3 ? kI3KMeta : kI4KMeta;
@@ -133,18 +145,19 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(
 
     // ---- P.V: lane owns channels 4*lane .. 4*lane+3 (one group)
     const int gr = lane >> 3;
-    const int vmeta = i2 ? kI2VMeta : (i3 ? kI3VMeta : kI4VMeta);
+    const int vmeta = i2 ? kI2VMeta : (i3 ? kI3VMeta : (f4 ? kF4VScale : kI4VMeta));
     for (int t2 = 0; t2 < kPage; ++t2) {
       const int mi = v_meta_index(t2, gr);
-      const float sf = ld_half(bw + vmeta + 2 * mi), zf = ld_half(bw + vmeta + 256 + 2 * mi);
+      const float sf = ld_half(bw + vmeta + 2 * mi), zf = f4 ? 0.0f : ld_half(bw + vmeta + 256 + 2 * mi);
 #pragma unroll
       for (int a = 0; a < 4; ++a) {
         const int c = 4 * lane + a;
         const uint32_t code = i2   ? (bw[i2v_byte(t2, c)] >> i2v_shift(t2)) & 3u
                               : i3 ? (((uint32_t)bw[i3v_lo_byte(t2, c)] >> i3v_lo_shift(t2)) & 3u) |
                                          ((((uint32_t)bw[i3v_hi_byte(t2, c)] >> i3v_hi_shift(t2, c)) & 1u) << 2)
+                              : f4 ? ((uint32_t)bw[f4v_byte(t2, c)] >> f4v_shift(t2)) & 15u
                                    : (bw[i4v_byte(t2, c)] >> i4v_shift(t2)) & 15u;
-        const float vh = __fmaf_rn((float)code, sf, zf);
+        const float vh = f4 ? e2m1_value(code) * sf : __fmaf_rn((float)code, sf, zf);
 #pragma unroll
         for (int h = 0; h < G; ++h) acc[h][a] = __fmaf_rn(pb[w][t2][h], vh, acc[h][a]);
       }
@@ -310,7 +323,9 @@ cudaError_t launch_g(kv_pool* P, const void* q, int32_t hq, float scale_log2, co
                                      P->cfg.num_kv_heads, P->cfg.max_pages_per_request, (const Entry*)P->d_table,
                                      (const __nv_bfloat16*)q, (int)hq, scale_log2, d_units, d_splits, d_cta,
                                      (const int32_t*)P->d_ntab, (const uint32_t*)(P->hdead.empty() ? nullptr : P->d_hdead),
-                                     d_part, P->int3_offset, (int64_t)(P->cfg.n_int2_pages + P->cfg.n_int4_pages));
+                                     d_part, P->int3_offset, (int64_t)(P->cfg.n_int2_pages + P->cfg.n_int4_pages),
+                                     P->fp4_offset,
+                                     (int64_t)(P->cfg.n_int2_pages + P->cfg.n_int4_pages + P->cfg.n_int3_pages));
     if (e != cudaSuccess) return e;
   }
   {

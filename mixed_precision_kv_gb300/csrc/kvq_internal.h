@@ -167,13 +167,13 @@ struct ScanOrder {
 // 1.18x and 1.5x an INT4 page.  The CUDA-core scan is charged its block
 // bytes plus 2048.
 struct PageCost {
-  double int2, int4, int3;
+  double int2, int4, int3, fp4 = 1.0;
 };
 // INT3 pages: the INT4 page's work plus the assembly of every code from two
 // planes; fitted the same way (32K-token batch-8 and 100K-token batch-16
 // steps with every INT4 token made INT3): 1.28x and 1.40x an INT4 page.
 inline PageCost mma_page_cost(int g) { return g <= 4 ? PageCost{1.18, 1.00, 1.28} : PageCost{1.50, 1.00, 1.40}; }
-constexpr PageCost kSimtPageCost{3072.0 + 2048.0, 5120.0 + 2048.0, 4096.0 + 2048.0};
+constexpr PageCost kSimtPageCost{3072.0 + 2048.0, 5120.0 + 2048.0, 4096.0 + 2048.0, 4608.0 + 2048.0};
 constexpr int64_t kMinPagesPerCta = 16;    // CUDA-core scan: pages per CTA at least
 constexpr int64_t kMinPagesPerWarp = 1;    // tensor-core scan: pages per warp at least (small batches: more warps, less latency)
 constexpr int64_t kTimingRing = 2048;
@@ -191,7 +191,7 @@ struct HostPlan {
 struct Request {
   bool open = false;
   std::vector<int32_t> table;       // page ids in table order
-  int32_t tail4 = -1, tail3 = -1, staging = -1;
+  int32_t tail4 = -1, tail3 = -1, tailf = -1, staging = -1;
   std::vector<uint32_t> loc;        // token position -> page_id << 5 | slot
   uint64_t version = 0;             // bumped whenever the table's entries change
   uint64_t ordered_version = ~0ull; // version at which the table was last seen INT2-first
@@ -251,6 +251,7 @@ struct kv_pool {
   size_t pool_bytes = 0;
   size_t int4_offset = 0;             // byte offset of the INT4 region
   size_t int3_offset = 0;             // byte offset of the INT3 region (after the INT4 region)
+  size_t fp4_offset = 0;              // byte offset of the FP4 region (after the INT3 region)
   kvq::Entry* d_table = nullptr;      // [max_requests][max_pages]
   int32_t* d_ntab = nullptr;          // [max_requests]
   uint32_t* d_status = nullptr;       // [0] status bits, [1] largest INT2 K scale, [2] largest V scale (fp32 bits)
@@ -288,7 +289,7 @@ struct kv_pool {
   std::vector<uint8_t> fill;          // per page id
   std::vector<uint32_t> live;         // per page id
   std::vector<int32_t> pos;           // per page id x 32 slots: token position
-  kvq::FreeIds free2, free3, free4;
+  kvq::FreeIds free2, free3, free4, freef;
   std::vector<int32_t> call_slot;     // per request: index of its state inside the running append call (-1 outside)
   std::vector<int32_t> page_job;      // per page id: its append job inside the running call (-1 outside)
   // decode plan cache
@@ -363,6 +364,9 @@ cudaError_t launch_append(kv_pool* P, const void* k, const void* v, const Append
 // INT3 tail pages (jobs whose page is an INT3 id)
 cudaError_t launch_append_int3(kv_pool* P, const void* k, const void* v, const AppendJob* d_jobs, int n_jobs,
                                const int32_t* d_toks, cudaStream_t s);
+// FP4 tail pages (jobs whose page is an FP4 id)
+cudaError_t launch_append_fp4(kv_pool* P, const void* k, const void* v, const AppendJob* d_jobs, int n_jobs,
+                              const int32_t* d_toks, cudaStream_t s);
 cudaError_t launch_repack(kv_pool* P, const RepackJob* d_jobs, int n_jobs, cudaStream_t s);
 cudaError_t launch_direct_int2(kv_pool* P, const void* k, const void* v, const DirectJob* d_jobs, int n_jobs,
                                const int32_t* d_toks, cudaStream_t s);

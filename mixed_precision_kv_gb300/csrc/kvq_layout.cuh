@@ -57,6 +57,17 @@
 //                2560 + 4*X with bit 4*w + (k&3) + 16*(k>>2).
 //   [3072, 3584) K scale/zero: as in the INT4 block ([slot][group] {s, z}).
 //   [3584, 4096) V scale/zero: as in the INT4 block.
+// FP4 block (4608 B): E2M1 codes (sign << 3 | exponent << 1 | mantissa) in
+// the INT4 block's code words, but with the two channels (K) or slots (V)
+// that one mma A register pairs sharing a byte, so that one e2m1x2 -> f16x2
+// conversion yields the register: byte n of a word holds element n (low
+// nibble) and element n + 4 (high nibble).  Symmetric groups: scales only.
+//   [   0, 2048) K codes: slot t row at 64*t, chunk i at 16*i, word gr holds
+//                channel 32*gr + 8*i + n in byte n & 3, nibble n >> 2.
+//   [2048, 4096) V codes: INT4 V chunk X and word w as in the INT4 block,
+//                slot 8j + k in byte k & 3, nibble k >> 2.
+//   [4096, 4352) K scales: [slot][group] half.
+//   [4352, 4608) V scales: [group][32] half in the INT4 V scale order.
 #pragma once
 #include <stdint.h>
 
@@ -74,6 +85,7 @@ constexpr int kGroup = 32;
 constexpr int kInt4Block = 5120;
 constexpr int kInt2Block = 3072;
 constexpr int kInt3Block = 4096;
+constexpr int kFp4Block = 4608;
 
 // INT4 block offsets
 constexpr int kI4KCodes = 0, kI4VCodes = 2048, kI4KMeta = 4096, kI4VMeta = 4608;
@@ -81,6 +93,8 @@ constexpr int kI4KCodes = 0, kI4VCodes = 2048, kI4KMeta = 4096, kI4VMeta = 4608;
 constexpr int kI2KCodes = 0, kI2VCodes = 1024, kI2KMeta = 2048, kI2VMeta = 2560;
 // INT3 block offsets (kI3VHigh: the V high plane)
 constexpr int kI3KCodes = 0, kI3VCodes = 1536, kI3VHigh = 2560, kI3KMeta = 3072, kI3VMeta = 3584;
+// FP4 block offsets
+constexpr int kF4KCodes = 0, kF4VCodes = 2048, kF4KScale = 4096, kF4VScale = 4352;
 
 // ---- INT4 K codes: byte offset and nibble of (slot, channel)
 KVQ_HD int i4k_byte(int t, int c) {
@@ -148,6 +162,25 @@ KVQ_HD int i3v_hi_byte(int t, int c) {
 KVQ_HD int i3v_hi_shift(int t, int c) {
   const int m = c >> 4, e = (c >> 3) & 1;
   return 4 * ((2 * (m & 1) + e) & 1) + (t & 3);
+}
+
+// ---- FP4 K / V codes: byte and nibble shift of (slot, channel)
+KVQ_HD int f4k_byte(int t, int c) {
+  const int gr = c >> 5, i = (c >> 3) & 3, n = c & 7;
+  return kF4KCodes + 64 * t + 16 * i + 4 * gr + (n & 3);
+}
+KVQ_HD int f4k_shift(int c) { return 4 * ((c >> 2) & 1); }
+KVQ_HD int f4v_byte(int t, int c) {
+  const int j = t >> 3, k = t & 7;
+  const int m = c >> 4, e = (c >> 3) & 1, r = c & 7;
+  return kF4VCodes + 16 * (32 * (m >> 1) + 4 * r + j) + 4 * (2 * (m & 1) + e) + (k & 3);
+}
+KVQ_HD int f4v_shift(int t) { return 4 * ((t >> 2) & 1); }
+// E2M1 value of a code (exponent 0: 0 or the subnormal 0.5)
+KVQ_HD float e2m1_value(uint32_t code) {
+  const uint32_t e = (code >> 1) & 3u, f = code & 1u;
+  const float mag = e == 0 ? 0.5f * (float)f : (1.0f + 0.5f * (float)f) * (float)(1u << (e - 1));
+  return (code & 8u) ? -mag : mag;
 }
 
 // ---- V scale/zero (every width): half index (0..127) of (slot, group)

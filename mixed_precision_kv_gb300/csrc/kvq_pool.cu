@@ -60,11 +60,15 @@ bool req_ok(const kv_pool* P, int32_t r) {
 }
 
 bool is_int2(const kv_pool* P, int32_t id) { return id < P->cfg.n_int2_pages; }
-// INT3 ids follow the INT2 and INT4 ids
-bool is_int3(const kv_pool* P, int32_t id) { return id >= P->cfg.n_int2_pages + P->cfg.n_int4_pages; }
-int width_of(const kv_pool* P, int32_t id) { return is_int2(P, id) ? 2 : (is_int3(P, id) ? 3 : 4); }
+// INT3 ids follow the INT2 and INT4 ids, FP4 ids the INT3 ids
+int64_t first_int3(const kv_pool* P) { return P->cfg.n_int2_pages + P->cfg.n_int4_pages; }
+int64_t first_fp4(const kv_pool* P) { return first_int3(P) + P->cfg.n_int3_pages; }
+bool is_fp4(const kv_pool* P, int32_t id) { return id >= first_fp4(P); }
+bool is_int3(const kv_pool* P, int32_t id) { return id >= first_int3(P) && id < first_fp4(P); }
+// sort key of the reorder: INT2, INT3, INT4, FP4
+int width_of(const kv_pool* P, int32_t id) { return is_int2(P, id) ? 2 : (is_int3(P, id) ? 3 : (is_fp4(P, id) ? 5 : 4)); }
 FreeIds& free_list(kv_pool* P, int32_t id) {
-  return is_int2(P, id) ? P->free2 : (is_int3(P, id) ? P->free3 : P->free4);
+  return is_int2(P, id) ? P->free2 : (is_int3(P, id) ? P->free3 : (is_fp4(P, id) ? P->freef : P->free4));
 }
 
 // Position-map entry of a token whose page was dropped (kv_drop_dead_pages).
@@ -229,8 +233,8 @@ void kvq::set_last_error(const char* msg) { g_err = msg; }
 void kvq::plan_decode(const kv_pool* P, const int32_t* req_ids, int32_t batch, int64_t n_ctas, int64_t min_pages,
                        PageCost pc, bool spread, HostPlan& out) {
   const int hkv = P->cfg.num_kv_heads;
-  const int64_t n2 = P->cfg.n_int2_pages, n3b = n2 + P->cfg.n_int4_pages;
-  auto cost = [&](int32_t id) { return id < n2 ? pc.int2 : (id >= n3b ? pc.int3 : pc.int4); };
+  const int64_t n2 = P->cfg.n_int2_pages, n3b = n2 + P->cfg.n_int4_pages, nfb = n3b + P->cfg.n_int3_pages;
+  auto cost = [&](int32_t id) { return id < n2 ? pc.int2 : (id >= nfb ? pc.fp4 : (id >= n3b ? pc.int3 : pc.int4)); };
   // Per request: the cost of its first i pages in scan order (shared by the
   // request's kv heads), so that worker boundaries are found by binary search
   // instead of a walk over every (page, kv head).  With per-head exclusion
@@ -403,10 +407,10 @@ kv_status_t kv_pool_create(const kv_pool_config_t* cfg, kv_pool_t** out) {
     return fail(KV_ERR_INVALID_ARG, "kv_pool_create: head_dim, page_tokens and group must be 128, 32, 32");
   if (cfg->num_kv_heads < 1 || cfg->num_kv_heads > 64)
     return fail(KV_ERR_INVALID_ARG, "kv_pool_create: num_kv_heads must be in [1, 64]");
-  if (cfg->n_int2_pages < 0 || cfg->n_int4_pages < 1 || cfg->n_int3_pages < 0 ||
-      cfg->n_int2_pages + cfg->n_int4_pages + cfg->n_int3_pages > (int64_t(1) << 27))
-    return fail(KV_ERR_INVALID_ARG,
-                "kv_pool_create: need n_int4_pages >= 1, n_int3_pages >= 0 and at most 2^27 pages in total");
+  if (cfg->n_int2_pages < 0 || cfg->n_int4_pages < 1 || cfg->n_int3_pages < 0 || cfg->n_fp4_pages < 0 ||
+      cfg->n_int2_pages + cfg->n_int4_pages + cfg->n_int3_pages + cfg->n_fp4_pages > (int64_t(1) << 27))
+    return fail(KV_ERR_INVALID_ARG, "kv_pool_create: need n_int4_pages >= 1, n_int3_pages, n_fp4_pages >= 0 and "
+                                    "at most 2^27 pages in total");
   if (cfg->max_requests < 1 || cfg->max_pages_per_request < 1 ||
       (int64_t)cfg->max_requests * cfg->max_pages_per_request > (int64_t(1) << 32) - 1)
     return fail(KV_ERR_INVALID_ARG, "kv_pool_create: bad max_requests / max_pages_per_request");
@@ -434,7 +438,8 @@ kv_status_t kv_pool_create(const kv_pool_config_t* cfg, kv_pool_t** out) {
   const size_t hkv = (size_t)cfg->num_kv_heads;
   P->int4_offset = (size_t)cfg->n_int2_pages * hkv * kInt2Block;
   P->int3_offset = P->int4_offset + (size_t)cfg->n_int4_pages * hkv * kInt4Block;
-  P->pool_bytes = P->int3_offset + (size_t)cfg->n_int3_pages * hkv * kInt3Block;
+  P->fp4_offset = P->int3_offset + (size_t)cfg->n_int3_pages * hkv * kInt3Block;
+  P->pool_bytes = P->fp4_offset + (size_t)cfg->n_fp4_pages * hkv * kFp4Block;
   if (cudaMalloc(&P->d_pool, P->pool_bytes) != cudaSuccess) {
     cudaGetLastError();
     return cleanup(fail(KV_ERR_OOM, "kv_pool_create: cannot allocate %zu bytes of pool", P->pool_bytes));
@@ -448,7 +453,7 @@ kv_status_t kv_pool_create(const kv_pool_config_t* cfg, kv_pool_t** out) {
   if (cudaMemset(P->d_table, 0xFF, tab) != cudaSuccess || cudaMemset(P->d_ntab, 0, cfg->max_requests * 4) != cudaSuccess ||
       cudaMemset(P->d_status, 0, 16) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)
     return cleanup(fail(KV_ERR_CUDA, "kv_pool_create: initialisation failed"));
-  const size_t npages = (size_t)(cfg->n_int2_pages + cfg->n_int4_pages + cfg->n_int3_pages);
+  const size_t npages = (size_t)(cfg->n_int2_pages + cfg->n_int4_pages + cfg->n_int3_pages + cfg->n_fp4_pages);
   try {
     P->reqs.resize(cfg->max_requests);
     P->fill.assign(npages, 0);
@@ -457,6 +462,7 @@ kv_status_t kv_pool_create(const kv_pool_config_t* cfg, kv_pool_t** out) {
     P->free2.init(0, (int32_t)cfg->n_int2_pages);
     P->free4.init((int32_t)cfg->n_int2_pages, (int32_t)cfg->n_int4_pages);
     P->free3.init((int32_t)(cfg->n_int2_pages + cfg->n_int4_pages), (int32_t)cfg->n_int3_pages);
+    P->freef.init((int32_t)(cfg->n_int2_pages + cfg->n_int4_pages + cfg->n_int3_pages), (int32_t)cfg->n_fp4_pages);
   } catch (...) {
     return cleanup(fail(KV_ERR_OOM, "kv_pool_create: host allocation failed"));
   }
@@ -584,12 +590,14 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
     int32_t q_left;        // INT2-tagged tokens of r not yet routed in this call
     int32_t tail_job;      // append job of the current INT4 tail page (-1: none yet)
     int32_t tail3_job;     // append job of the current INT3 tail page (-1: none yet)
+    int32_t tailf_job;     // append job of the current FP4 tail page (-1: none yet)
     int32_t stag_job;      // append job of the current staging page (-1: none / direct)
     bool stag_direct;      // the current staging page fills within this call: quantized directly to INT2
     int32_t ngrp;          // tokens collected for it so far
     int32_t grp[kPage];    // their token indices, in slot order
     // dry-run state
-    bool tail; int tailfill; bool tail3; int tail3fill; bool stag; int stagfill; int64_t tablen;
+    bool tail; int tailfill; bool tail3; int tail3fill; bool tailf; int tailffill; bool stag; int stagfill;
+    int64_t tablen;
   };
   std::vector<CallReq> cr;
   if (P->call_slot.size() != (size_t)P->cfg.max_requests) P->call_slot.assign((size_t)P->cfg.max_requests, -1);
@@ -601,11 +609,13 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
       CallReq c{};
       c.r = r;
       c.old_len = (int32_t)R.table.size();
-      c.tail_job = c.tail3_job = c.stag_job = -1;
+      c.tail_job = c.tail3_job = c.tailf_job = c.stag_job = -1;
       c.tail = R.tail4 >= 0;
       c.tailfill = c.tail ? (int)P->fill[R.tail4] : 0;
       c.tail3 = R.tail3 >= 0;
       c.tail3fill = c.tail3 ? (int)P->fill[R.tail3] : 0;
+      c.tailf = R.tailf >= 0;
+      c.tailffill = c.tailf ? (int)P->fill[R.tailf] : 0;
       c.stag = R.staging >= 0;
       c.stagfill = c.stag ? (int)P->fill[R.staging] : 0;
       c.tablen = (int64_t)R.table.size();
@@ -681,12 +691,13 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
   }
   // Dry run: pages taken and table growth, so that OOM changes nothing.
   if (!bulk) {
-    int64_t need4 = 0, need3 = 0, need2 = 0;
+    int64_t need4 = 0, need3 = 0, needf = 0, need2 = 0;
     for (int64_t t = 0; t < n_tok; ++t) {
       if (!req_ok(P, req_ids[t]))
         return fail(KV_ERR_INVALID_ARG, "kv_append_quant: token %lld: request %d not open", (long long)t, req_ids[t]);
-      if (bits[t] < 2 || bits[t] > 4)
-        return fail(KV_ERR_INVALID_ARG, "kv_append_quant: token %lld: bits must be 2, 3 or 4", (long long)t);
+      if ((bits[t] < 2 || bits[t] > 4) && bits[t] != KV_WIDTH_FP4)
+        return fail(KV_ERR_INVALID_ARG, "kv_append_quant: token %lld: bits must be 2, 3, 4 or KV_WIDTH_FP4",
+                    (long long)t);
       CallReq& c = slot_of(req_ids[t]);
       if (bits[t] == 4) {
         if (!c.tail || c.tailfill == kPage) { ++need4; ++c.tablen; c.tail = true; c.tailfill = 0; }
@@ -694,6 +705,9 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
       } else if (bits[t] == 3) {
         if (!c.tail3 || c.tail3fill == kPage) { ++need3; ++c.tablen; c.tail3 = true; c.tail3fill = 0; }
         ++c.tail3fill;
+      } else if (bits[t] == KV_WIDTH_FP4) {
+        if (!c.tailf || c.tailffill == kPage) { ++needf; ++c.tablen; c.tailf = true; c.tailffill = 0; }
+        ++c.tailffill;
       } else {
         ++c.q_left;
         if (!c.stag) { ++need4; ++c.tablen; c.stag = true; c.stagfill = 0; }
@@ -707,6 +721,8 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
                   (long long)need2, P->free4.size(), P->free2.size());
     if (need3 > (int64_t)P->free3.size())
       return fail(KV_ERR_OOM, "kv_append_quant: needs %lld INT3 pages, %zu free", (long long)need3, P->free3.size());
+    if (needf > (int64_t)P->freef.size())
+      return fail(KV_ERR_OOM, "kv_append_quant: needs %lld FP4 pages, %zu free", (long long)needf, P->freef.size());
   }
   // room for this call's tokens in each position map; growth is geometric
   // (reserving just the new size on every call would copy the whole map)
@@ -859,11 +875,11 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
     Request& R = P->reqs[r];
     CallReq& c = cr[(size_t)P->call_slot[(size_t)r]];
     const int64_t pos = (int64_t)R.loc.size();
-    const bool b4 = bits[t] == 4, b3 = bits[t] == 3;
-    // INT4 tokens fill the INT4 tail, INT3 tokens the INT3 tail, INT2 tokens the (INT4) staging page
-    int32_t& cur = b4 ? R.tail4 : (b3 ? R.tail3 : R.staging);
+    const bool b4 = bits[t] == 4, b3 = bits[t] == 3, bf = bits[t] == KV_WIDTH_FP4;
+    // INT4 tokens fill the INT4 tail, INT3 and FP4 tokens their own tails, INT2 tokens the (INT4) staging page
+    int32_t& cur = b4 ? R.tail4 : (b3 ? R.tail3 : (bf ? R.tailf : R.staging));
     if (cur < 0 || P->fill[cur] == kPage) {
-      cur = (b3 ? P->free3 : P->free4).take_lowest();
+      cur = (b3 ? P->free3 : (bf ? P->freef : P->free4)).take_lowest();
       P->fill[cur] = 0;
       P->live[cur] = 0;
       R.table.push_back(cur);
@@ -872,6 +888,8 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
         c.tail_job = -1;
       } else if (b3) {
         c.tail3_job = -1;
+      } else if (bf) {
+        c.tailf_job = -1;
       } else {
         c.stag_job = -1;
         c.stag_direct = c.q_left >= kPage;
@@ -882,12 +900,12 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
     P->live[cur] |= 1u << slot;
     P->pos[(size_t)cur * kPage + slot] = (int32_t)pos;
     R.loc.push_back(((uint32_t)cur << 5) | (uint32_t)slot);
-    const bool b2 = !b4 && !b3;
+    const bool b2 = !b4 && !b3 && !bf;
     if (b2) --c.q_left;
     if (b2 && c.stag_direct) {
       c.grp[c.ngrp++] = (int32_t)t;
     } else {
-      int32_t& jb = b4 ? c.tail_job : (b3 ? c.tail3_job : c.stag_job);
+      int32_t& jb = b4 ? c.tail_job : (b3 ? c.tail3_job : (bf ? c.tailf_job : c.stag_job));
       if (jb < 0) {
         jb = (int32_t)jobs.size();
         jobs.push_back(AppendJob{cur, slot, 0, 0, -1, 0u, -1, 0});
@@ -987,17 +1005,25 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
   hdead_final(P, hupd);
   upd.insert(upd.end(), hupd.begin(), hupd.end());
 
-  // INT3 jobs go last, to their own kernel
-  size_t n_i3 = 0;
-  for (const auto& j : jobs) n_i3 += is_int3(P, j.page) ? 1 : 0;
-  if (n_i3) std::stable_partition(jobs.begin(), jobs.end(), [&](const AppendJob& j) { return !is_int3(P, j.page); });
-  const bool small = n_i3 == 0 && jobs.size() <= (size_t)SmallAppend::kMaxJobs && off <= SmallAppend::kMaxToks;
+  // INT3 and FP4 jobs go last (INT3, then FP4), to their own kernels
+  size_t n_i3 = 0, n_f4 = 0;
+  for (const auto& j : jobs) {
+    n_i3 += is_int3(P, j.page) ? 1 : 0;
+    n_f4 += is_fp4(P, j.page) ? 1 : 0;
+  }
+  if (n_i3 + n_f4) {
+    std::stable_partition(jobs.begin(), jobs.end(), [&](const AppendJob& j) { return width_of(P, j.page) == 2 ||
+                                                                                      width_of(P, j.page) == 4; });
+    std::stable_partition(jobs.end() - (ptrdiff_t)(n_i3 + n_f4), jobs.end(),
+                          [&](const AppendJob& j) { return is_int3(P, j.page); });
+  }
+  const bool small = n_i3 + n_f4 == 0 && jobs.size() <= (size_t)SmallAppend::kMaxJobs && off <= SmallAppend::kMaxToks;
   // Large calls with 16-byte aligned K/V rows: fresh pages filled with 32
   // tokens go to the bulk INT4 kernel, direct groups to the bulk INT2 kernel.
   const bool aligned = ((uintptr_t)k % 16 == 0) && ((uintptr_t)v % 16 == 0);
   const bool use_bulk = !small && aligned;
   size_t n_full = 0;
-  const auto jobs4_end = jobs.end() - (ptrdiff_t)n_i3;
+  const auto jobs4_end = jobs.end() - (ptrdiff_t)(n_i3 + n_f4);
   if (use_bulk) {
     std::stable_partition(jobs.begin(), jobs4_end, [](const AppendJob& j) { return !(j.first_slot == 0 && j.n_slots == kPage); });
     for (auto it = jobs.begin(); it != jobs4_end; ++it) n_full += (it->first_slot == 0 && it->n_slots == kPage) ? 1 : 0;
@@ -1018,15 +1044,18 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
     std::copy(toks.begin(), toks.end(), sa.toks);
     KV_CUDA(launch_append(P, k, v, nullptr, (int)jobs.size(), nullptr, &sa, s));
   } else {
-    const int n_part = (int)(jobs.size() - n_i3 - n_full);
+    const int n_part = (int)(jobs.size() - n_i3 - n_f4 - n_full);
     KV_CUDA(launch_append(P, k, v, (const AppendJob*)(base + o_jobs), n_part, (const int32_t*)(base + o_toks),
                           nullptr, s));
     if (n_full)
       KV_CUDA(launch_bulk_int4(P, k, v, (const AppendJob*)(base + o_jobs) + n_part, (int)n_full,
                                (const int32_t*)(base + o_toks), s));
     if (n_i3)
-      KV_CUDA(launch_append_int3(P, k, v, (const AppendJob*)(base + o_jobs) + (jobs.size() - n_i3), (int)n_i3,
-                                 (const int32_t*)(base + o_toks), s));
+      KV_CUDA(launch_append_int3(P, k, v, (const AppendJob*)(base + o_jobs) + (jobs.size() - n_i3 - n_f4),
+                                 (int)n_i3, (const int32_t*)(base + o_toks), s));
+    if (n_f4)
+      KV_CUDA(launch_append_fp4(P, k, v, (const AppendJob*)(base + o_jobs) + (jobs.size() - n_f4), (int)n_f4,
+                                (const int32_t*)(base + o_toks), s));
   }
   if (use_bulk)
     KV_CUDA(launch_bulk_int2(P, k, v, (const DirectJob*)(base + o_dir), (int)directs.size(),
@@ -1047,8 +1076,8 @@ kv_status_t kv_reorder_pages(kv_pool_t* P, const int32_t* req_ids, int32_t n_req
   for (int32_t i = 0; i < n_req; ++i) {
     Request& R = P->reqs[req_ids[i]];
     if (R.ordered_version == R.version) continue;   // unchanged since it was last found INT2-first
-    if (P->cfg.n_int3_pages > 0) {
-      // three widths: a stable sort by width (INT2, INT3, INT4)
+    if (P->cfg.n_int3_pages > 0 || P->cfg.n_fp4_pages > 0) {
+      // more widths: a stable sort by width (INT2, INT3, INT4, FP4)
       auto by_width = [&](int32_t a, int32_t b) { return width_of(P, a) < width_of(P, b); };
       if (!std::is_sorted(R.table.begin(), R.table.end(), by_width)) {
         std::vector<int32_t> old = R.table;
@@ -1204,6 +1233,7 @@ kv_status_t kv_drop_dead_pages(kv_pool_t* P, const int32_t* req_ids, int32_t n_r
       }
       if (R.tail4 == id) R.tail4 = -1;
       if (R.tail3 == id) R.tail3 = -1;
+      if (R.tailf == id) R.tailf = -1;
       if (R.staging == id) R.staging = -1;
       P->fill[id] = 0;
       P->live[id] = 0u;
@@ -1352,11 +1382,12 @@ kv_status_t kv_export_request(kv_pool_t* P, int32_t r, int32_t* ids, uint8_t* is
   std::vector<uint8_t> raw((size_t)hkv * kInt4Block);
   for (size_t i = 0; i < tb.size(); ++i) {
     const int32_t id = tb[i];
-    const bool i2 = is_int2(P, id), i3 = is_int3(P, id);
-    const size_t bs = i2 ? kInt2Block : (i3 ? kInt3Block : kInt4Block);
+    const bool i2 = is_int2(P, id), i3 = is_int3(P, id), f4 = is_fp4(P, id);
+    const size_t bs = i2 ? kInt2Block : (i3 ? kInt3Block : (f4 ? kFp4Block : kInt4Block));
     const uint8_t* src =
         i2   ? P->d_pool + (size_t)id * hkv * kInt2Block
-        : i3 ? P->d_pool + P->int3_offset + (size_t)(id - P->cfg.n_int2_pages - P->cfg.n_int4_pages) * hkv * kInt3Block
+        : i3 ? P->d_pool + P->int3_offset + (size_t)(id - first_int3(P)) * hkv * kInt3Block
+        : f4 ? P->d_pool + P->fp4_offset + (size_t)(id - first_fp4(P)) * hkv * kFp4Block
              : P->d_pool + P->int4_offset + (size_t)(id - P->cfg.n_int2_pages) * hkv * kInt4Block;
     KV_CUDA(cudaMemcpy(raw.data(), src, bs * hkv, cudaMemcpyDeviceToHost));
     for (int h = 0; h < hkv; ++h) {
@@ -1367,6 +1398,22 @@ kv_status_t kv_export_request(kv_pool_t* P, int32_t r, int32_t* ids, uint8_t* is
       uint16_t* kmo = km + o * 256;
       uint16_t* vmo = vm + o * 256;
       auto h16 = [&](int off) { uint16_t x; std::memcpy(&x, b + off, 2); return x; };
+      if (f4) {
+        // E2M1 codes; scale/zero pairs {s, 0} (symmetric groups)
+        for (int t = 0; t < kPage; ++t)
+          for (int c = 0; c < kHeadDim; ++c) {
+            kco[t * kHeadDim + c] = (b[f4k_byte(t, c)] >> f4k_shift(c)) & 15;
+            vco[t * kHeadDim + c] = (b[f4v_byte(t, c)] >> f4v_shift(t)) & 15;
+          }
+        for (int t = 0; t < kPage; ++t)
+          for (int gr = 0; gr < 4; ++gr) {
+            kmo[(t * 4 + gr) * 2] = h16(kF4KScale + 8 * t + 2 * gr);
+            kmo[(t * 4 + gr) * 2 + 1] = 0;
+            vmo[(t * 4 + gr) * 2] = h16(kF4VScale + 2 * v_meta_index(t, gr));
+            vmo[(t * 4 + gr) * 2 + 1] = 0;
+          }
+        continue;
+      }
       for (int t = 0; t < kPage; ++t)
         for (int c = 0; c < kHeadDim; ++c) {
           if (i3) {
@@ -1581,9 +1628,9 @@ kv_status_t kv_last_decode_stats(kv_pool_t* P, int64_t* kv_bytes, int32_t* n_spl
         for (int h = 0; h < hkv; ++h) heads -= (P->live[id] & ~P->hdead[(size_t)id * hkv + h]) == 0u ? 1 : 0;
       else if (P->stat_skip_dead && P->live[id] == 0u)
         heads = 0;
-      // INT4: 160 bytes per written slot (codes 128, scale/zero 32); INT3: 128 (96 + 32)
+      // INT4: 160 bytes per written slot (codes 128, scale/zero 32); INT3: 128 (96 + 32); FP4: 144 (128 + 16)
       bytes += is_int2(P, id) ? (int64_t)kInt2Block * heads
-                              : (int64_t)P->fill[id] * (is_int3(P, id) ? 128 : 160) * heads;
+                              : (int64_t)P->fill[id] * (is_int3(P, id) ? 128 : (is_fp4(P, id) ? 144 : 160)) * heads;
       bytes += 8;
       ++pages;
     }
@@ -1790,8 +1837,9 @@ extern "C" kv_status_t kv_decode_attn_groups(kv_pool_t* const* pools, int32_t n_
       if (pools[o] == pools[p]) return fail(KV_ERR_INVALID_ARG, "kv_decode_attn_groups: pool %d is listed twice", p);
     if (pools[p]->cfg.device != pools[0]->cfg.device)
       return fail(KV_ERR_INVALID_ARG, "kv_decode_attn_groups: the pools must be on one device");
-    if (pools[p]->cfg.n_int3_pages > 0)
-      return fail(KV_ERR_INVALID_ARG, "kv_decode_attn_groups: pool %d has INT3 pages (not read by the grouped scan)", p);
+    if (pools[p]->cfg.n_int3_pages > 0 || pools[p]->cfg.n_fp4_pages > 0)
+      return fail(KV_ERR_INVALID_ARG,
+                  "kv_decode_attn_groups: pool %d has INT3 or FP4 pages (not read by the grouped scan)", p);
     thkv += pools[p]->cfg.num_kv_heads;
   }
   if (hq < thkv || hq % thkv != 0 || hq / thkv > 8)

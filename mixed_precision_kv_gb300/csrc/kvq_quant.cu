@@ -372,6 +372,127 @@ __global__ void __launch_bounds__(kThreads) append_int3_kernel(
   }
 }
 
+// ---- FP4 pages (TriAxialKV, limitations and outlook: non-uniform FP
+// formats; HyQuant background: s = max|X| / c_B with c_B = 6 for E2M1):
+// per token and 32-channel group s = half_rn(max|x| / 6), code = the E2M1
+// value nearest to x / s (IEEE fp32 quotient), ties to the even mantissa,
+// saturating at 6, zero coded +0; s = 0 codes everything 0.  The midpoints of
+// the E2M1 grid are exact in fp32, so comparisons decide the rounding.
+__device__ __forceinline__ uint32_t e2m1_code(float x, float sf, bool nz) {
+  if (!nz) return 0u;
+  const float u = __fdiv_rn(x, sf);
+  const float a = fabsf(u);
+  const uint32_t m = a <= 0.25f ? 0u : a < 0.75f ? 1u : a <= 1.25f ? 2u : a < 1.75f ? 3u
+                   : a <= 2.5f  ? 4u : a < 3.5f  ? 5u : a <= 5.0f  ? 6u : 7u;
+  return m == 0u ? 0u : ((u < 0.0f ? 8u : 0u) | m);
+}
+
+// A warp quantizes one token of one kv head (lane = channels 4*lane ..
+// 4*lane+3).  K: a lane's four codes are the low (lane even) or high (lane
+// odd) nibbles of one word; the even lane writes the word with its
+// neighbour's nibbles.  V as in quantize_rows3.
+__device__ __forceinline__ bool quantize_rows_fp4(uint8_t* img, const RawRows& rr, int slot, float& vmax,
+                                                  uint8_t* vcodes) {
+  const int lane = threadIdx.x & 31, gr = lane >> 3;
+  const uint2 kr = rr.kr, vr = rr.vr;
+  float xk[4], xv[4];
+  xk[0] = __uint_as_float(kr.x << 16); xk[1] = __uint_as_float(kr.x & 0xFFFF0000u);
+  xk[2] = __uint_as_float(kr.y << 16); xk[3] = __uint_as_float(kr.y & 0xFFFF0000u);
+  xv[0] = __uint_as_float(vr.x << 16); xv[1] = __uint_as_float(vr.x & 0xFFFF0000u);
+  xv[2] = __uint_as_float(vr.y << 16); xv[3] = __uint_as_float(vr.y & 0xFFFF0000u);
+  bool bad = false;
+  float kmn = xk[0], kmx = xk[0], vmn = xv[0], vmx = xv[0];
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    bad |= out_of_range(xk[a]) | out_of_range(xv[a]);
+    kmn = fminf(kmn, xk[a]); kmx = fmaxf(kmx, xk[a]);
+    vmn = fminf(vmn, xv[a]); vmx = fmaxf(vmx, xv[a]);
+  }
+  group8_minmax(kmn, kmx);
+  group8_minmax(vmn, vmx);
+  const __half ks = __float2half_rn(__fdiv_rn(fmaxf(-kmn, kmx), 6.0f));
+  const __half vs = __float2half_rn(__fdiv_rn(fmaxf(-vmn, vmx), 6.0f));
+  const float ksf = __half2float(ks), vsf = __half2float(vs);
+  const bool knz = (__half_as_ushort(ks) & 0x7FFFu) != 0, vnz = (__half_as_ushort(vs) & 0x7FFFu) != 0;
+  uint32_t ck[4], cv[4];
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    ck[a] = e2m1_code(xk[a], ksf, knz);
+    cv[a] = e2m1_code(xv[a], vsf, vnz);
+  }
+  const int c0 = 4 * lane;
+  const uint32_t kw = ck[0] | (ck[1] << 8) | (ck[2] << 16) | (ck[3] << 24);
+  const uint32_t kw_odd = __shfl_xor_sync(0xFFFFFFFFu, kw, 1);
+  if ((lane & 1) == 0) *reinterpret_cast<uint32_t*>(img + f4k_byte(slot, c0)) = kw | (kw_odd << 4);
+  if (vcodes) {
+    *reinterpret_cast<uint32_t*>(vcodes + kHeadDim * slot + c0) = cv[0] | (cv[1] << 8) | (cv[2] << 16) | (cv[3] << 24);
+  } else {
+#pragma unroll
+    for (int a = 0; a < 4; ++a) or_bits(img, f4v_byte(slot, c0 + a), f4v_shift(slot), cv[a]);
+  }
+  vmax = fmaxf(vmax, vsf);
+  if ((lane & 7) == 0) {
+    st_half(img, kF4KScale + 8 * slot + 2 * gr, ks);
+    st_half(img, kF4VScale + 2 * v_meta_index(slot, gr), vs);
+  }
+  return bad;
+}
+
+// FP4 V words from [slot][channel] code bytes, each word by one thread.
+__device__ __forceinline__ void pack_f4v(uint8_t* __restrict__ img, const uint8_t* __restrict__ vcodes) {
+  for (int x = threadIdx.x; x < 512; x += kThreads) {
+    const int X = x >> 2, w = x & 3;
+    const int m = 2 * (X >> 5) + (w >> 1), e = w & 1, r = (X >> 2) & 7, j = X & 3;
+    const int c = 16 * m + 8 * e + r;
+    uint32_t v = 0u;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) v |= (uint32_t)vcodes[kHeadDim * (8 * j + k) + c] << (8 * (k & 3) + 4 * (k >> 2));
+    *reinterpret_cast<uint32_t*>(img + kF4VCodes + 16 * X + 4 * w) = v;
+  }
+}
+
+// One CTA per (job, kv head) of FP4 tail pages, a warp per token (as
+// append_int3_kernel).
+__global__ void __launch_bounds__(kThreads) append_fp4_kernel(
+    uint8_t* __restrict__ pool, size_t fp4_off, int64_t nfb, int hkv, const __nv_bfloat16* __restrict__ k,
+    const __nv_bfloat16* __restrict__ v, const AppendJob* __restrict__ jobs, const int32_t* __restrict__ toks,
+    Entry* __restrict__ table, int32_t* __restrict__ ntab, uint32_t* __restrict__ status) {
+  __shared__ __align__(16) uint8_t img[kFp4Block];
+  __shared__ __align__(16) uint8_t vcodes[kPage * kHeadDim];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
+  const AppendJob job = jobs[blockIdx.x];
+  const int h = blockIdx.y;
+  uint8_t* blk = pool + fp4_off + ((size_t)(job.page - nfb) * hkv + h) * kFp4Block;
+  const bool fresh = job.first_slot == 0;
+  uint8_t* dst = fresh ? img : blk;
+  if (fresh) {
+    for (int i = threadIdx.x; i < kFp4Block / 16; i += kThreads) reinterpret_cast<uint4*>(img)[i] = make_uint4(0, 0, 0, 0);
+    for (int i = threadIdx.x; i < kPage * kHeadDim / 16; i += kThreads)
+      reinterpret_cast<uint4*>(vcodes)[i] = make_uint4(0, 0, 0, 0);
+    __syncthreads();
+  }
+  const int warp = threadIdx.x >> 5;
+  const int32_t* tk = toks + job.tok_off;
+  bool bad = false;
+  float vmax = 0.0f;
+  for (int q = warp; q < job.n_slots; q += kThreads / 32)
+    bad |= quantize_rows_fp4(dst, load_rows(k, v, tk[q], h, hkv), job.first_slot + q, vmax, fresh ? vcodes : nullptr);
+  if (fresh) {
+    __syncthreads();
+    pack_f4v(img, vcodes);
+    __syncthreads();
+    for (int i = threadIdx.x; i < kFp4Block / 16; i += kThreads)
+      reinterpret_cast<uint4*>(blk)[i] = reinterpret_cast<const uint4*>(img)[i];
+  }
+  flush_vmax(vmax, status);
+  if (bad) atomicOr(status, kStatusRange);
+  if (h == 0 && threadIdx.x == 0) {
+    if (job.tab_index >= 0) table[job.tab_index] = Entry{job.page, job.live};
+    if (job.ntab_req >= 0) ntab[job.ntab_req] = job.ntab_len;
+  }
+}
+
 // Requantize a 32-token INT4 block image (shared memory) into an INT2 block
 // image (shared memory): K per channel across the 32 tokens, V per token and
 // group, both from the INT4-dequantized values fmaf(code, scale, zero); tracks
@@ -935,6 +1056,17 @@ cudaError_t launch_append_int3(kv_pool* P, const void* k, const void* v, const A
                     P->d_pool, P->int3_offset, (int64_t)(P->cfg.n_int2_pages + P->cfg.n_int4_pages),
                     P->cfg.num_kv_heads, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, d_jobs, d_toks,
                     P->d_table, P->d_ntab, P->d_status);
+}
+
+cudaError_t launch_append_fp4(kv_pool* P, const void* k, const void* v, const AppendJob* d_jobs, int n_jobs,
+                              const int32_t* d_toks, cudaStream_t s) {
+  if (n_jobs <= 0) return cudaSuccess;
+  ++P->launches;
+  return launch_pdl(append_fp4_kernel, dim3((unsigned)n_jobs, (unsigned)P->cfg.num_kv_heads), dim3(kThreads), 0, s,
+                    P->d_pool, P->fp4_offset,
+                    (int64_t)(P->cfg.n_int2_pages + P->cfg.n_int4_pages + P->cfg.n_int3_pages), P->cfg.num_kv_heads,
+                    (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, d_jobs, d_toks, P->d_table, P->d_ntab,
+                    P->d_status);
 }
 
 cudaError_t launch_bulk_int4(kv_pool* P, const void* k, const void* v, const AppendJob* d_jobs, int n_jobs,

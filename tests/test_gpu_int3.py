@@ -37,12 +37,13 @@ def _mixed3(n, seed, p=(0.4, 0.35, 0.25)):
 class Pools:
     """One GPU pool and its oracle twin with INT3 pages, fed the same calls."""
 
-    def __init__(self, kvq, hkv, hq, n_req, n2, n3, n4, max_tab, impl=None):
+    def __init__(self, kvq, hkv, hq, n_req, n2, n3, n4, max_tab, impl=None, nf=0):
         self.kvq, self.hkv, self.hq = kvq, hkv, hq
-        self.gpu = kvq.KVPool(hkv, n2, n4, n_req, max_tab, n_int3_pages=n3)
+        self.nf_first = n2 + n4 + n3 if nf else None   # FP4 ids follow the INT3 ids
+        self.gpu = kvq.KVPool(hkv, n2, n4, n_req, max_tab, n_int3_pages=n3, n_fp4_pages=nf)
         if impl is not None:
             self.gpu.set_decode_impl(impl)
-        self.orc = oracle.OraclePool(hkv, n2, n4, n_req, max_tab, n_int3_pages=n3)
+        self.orc = oracle.OraclePool(hkv, n2, n4, n_req, max_tab, n_int3_pages=n3, n_fp4_pages=nf)
         self.g = [self.gpu.open() for _ in range(n_req)]
         self.o = [self.orc.open() for _ in range(n_req)]
         self.n = [0] * n_req
