@@ -540,6 +540,8 @@ def main():
                          "every prompt and drops its dead pages; one grouped decode per step")
     ap.add_argument("--int3-share", type=float, default=0.0,
                     help="make a seeded fraction of the INT4 tokens INT3 (three-width pool; prefill and steps)")
+    ap.add_argument("--fp4-share", type=float, default=0.0,
+                    help="make a seeded fraction of the INT4 tokens FP4 (E2M1) (prefill and steps)")
     ap.add_argument("--mode", default="decode", choices=["decode", "prefill"],
                     help="decode: the decode-step line (default); prefill: bulk quantization of the workload's "
                          "prompts through kv_append_quant")
@@ -572,7 +574,10 @@ def main():
     w = load_workload(args, total_steps)
     if args.int3_share > 0:
         w.name = f"{w.name}+int3-{args.int3_share:g}"
-    gw = GPUWorkload(w, device=local, steps=total_steps, extra_tokens=extra, int3_share=args.int3_share)
+    if args.fp4_share > 0:
+        w.name = f"{w.name}+fp4-{args.fp4_share:g}"
+    gw = GPUWorkload(w, device=local, steps=total_steps, extra_tokens=extra, int3_share=args.int3_share,
+                     fp4_share=args.fp4_share)
     gw.pool.set_decode_impl({"auto": 0, "simt": 1, "mma": 2}[args.decode_impl])
     gw.prefill()
     gw.evict()
@@ -758,7 +763,9 @@ def main():
             "clocks": clk.summary()}
     if args.int3_share > 0:
         line["config"]["int3_token_fraction"] = float(np.mean(np.concatenate(gw.bits) == 3))
-    if rank == 0 and not args.no_cpu_baseline and args.int3_share <= 0:
+    if args.fp4_share > 0:
+        line["config"]["fp4_token_fraction"] = float(np.mean(np.concatenate(gw.bits) == 0xF4))
+    if rank == 0 and not args.no_cpu_baseline and args.int3_share <= 0 and args.fp4_share <= 0:
         try:
             line["cpu_baseline"] = cpu_baseline(w)
         except Exception as e:  # reported, not fatal

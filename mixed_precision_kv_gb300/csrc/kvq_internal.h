@@ -172,7 +172,11 @@ struct PageCost {
 // INT3 pages: the INT4 page's work plus the assembly of every code from two
 // planes; fitted the same way (32K-token batch-8 and 100K-token batch-16
 // steps with every INT4 token made INT3): 1.28x and 1.40x an INT4 page.
-inline PageCost mma_page_cost(int g) { return g <= 4 ? PageCost{1.18, 1.00, 1.28} : PageCost{1.50, 1.00, 1.40}; }
+// FP4 pages: a conversion per A register and no zero term, 1.06x an INT4
+// page at g = 4 (the g = 8 figure assumed a little higher).
+inline PageCost mma_page_cost(int g) {
+  return g <= 4 ? PageCost{1.18, 1.00, 1.28, 1.06} : PageCost{1.50, 1.00, 1.40, 1.10};
+}
 constexpr PageCost kSimtPageCost{3072.0 + 2048.0, 5120.0 + 2048.0, 4096.0 + 2048.0, 4608.0 + 2048.0};
 constexpr int64_t kMinPagesPerCta = 16;    // CUDA-core scan: pages per CTA at least
 constexpr int64_t kMinPagesPerWarp = 1;    // tensor-core scan: pages per warp at least (small batches: more warps, less latency)

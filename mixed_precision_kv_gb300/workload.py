@@ -25,22 +25,28 @@ def request_bits(w: Workload, r: int, allocator=alloc_bits) -> np.ndarray:
     return bits
 
 
-def int3_share_bits(w: Workload, r: int, bits: np.ndarray, share: float) -> np.ndarray:
-    """A seeded fraction `share` of request r's INT4 tokens made INT3 (a
-    synthetic three-width mix: the greedy allocation itself has two widths)."""
-    if share <= 0.0:
+FP4 = 0xF4   # width value of FP4 (E2M1) tokens
+
+
+def int3_share_bits(w: Workload, r: int, bits: np.ndarray, share: float, fp4_share: float = 0.0) -> np.ndarray:
+    """Seeded fractions of request r's INT4 tokens made INT3 (`share`) and FP4
+    (`fp4_share`): synthetic mixes of more widths (the greedy allocation
+    itself has two)."""
+    if share <= 0.0 and fp4_share <= 0.0:
         return bits
     u = np.random.default_rng([w.seed, 33, r]).random(bits.size)
     out = bits.copy()
     out[(bits == 4) & (u < share)] = 3
+    out[(bits == 4) & (u >= share) & (u < share + fp4_share)] = FP4
     return out
 
 
-def int3_pages(w: Workload, bits_list, steps: int) -> int:
-    """INT3 pages the workload's INT3 tokens take (prefill and steps)."""
+def int3_pages(w: Workload, bits_list, steps: int, width: int = 3) -> int:
+    """Pages the workload's tokens of one tail width (INT3 or FP4) take
+    (prefill and steps)."""
     n3 = 0
     for spec, bits in zip(w.requests, bits_list):
-        b3 = int((bits[:spec.n_prefill + steps] == 3).sum())
+        b3 = int((bits[:spec.n_prefill + steps] == width).sum())
         n3 += -(-b3 // 32) + 1 if b3 else 0
     return n3
 
@@ -55,7 +61,7 @@ def pool_size(w: Workload, bits_list, chunk: int, steps: int, extra: int = 0):
     for spec, bits in zip(w.requests, bits_list):
         total = spec.n_prefill + steps
         b2 = int((bits[:total] == 2).sum())
-        b3 = int((bits[:total] == 3).sum())
+        b3 = int((bits[:total] == 3).sum()) + int((bits[:total] == FP4).sum())
         b4 = total - b2 - b3
         n2 += b2 // 32 + 1 + xp
         n4 += -(-b4 // 32) + 2 + xp
@@ -67,20 +73,21 @@ def pool_size(w: Workload, bits_list, chunk: int, steps: int, extra: int = 0):
 
 class GPUWorkload:
     def __init__(self, w: Workload, device: int = 0, chunk: int = 16384, steps: int | None = None,
-                 extra_tokens: int = 0, make_pool: bool = True, int3_share: float = 0.0):
+                 extra_tokens: int = 0, make_pool: bool = True, int3_share: float = 0.0, fp4_share: float = 0.0):
         import torch
         self.w = w
         self.device = device
         self.chunk = chunk
         self.steps = w.steps if steps is None else steps
-        self.bits = [int3_share_bits(w, r, request_bits(w, r), int3_share) for r in range(len(w.requests))]
+        self.bits = [int3_share_bits(w, r, request_bits(w, r), int3_share, fp4_share) for r in range(len(w.requests))]
         self.sizes = pool_size(w, self.bits, chunk, self.steps, extra_tokens)
         n2, n4, max_tab = self.sizes
         n3 = int3_pages(w, self.bits, self.steps)
+        nf = int3_pages(w, self.bits, self.steps, FP4)
         # make_pool=False: the caller builds its own pools (e.g. one per head
         # group) and uses this object for the bit allocation and the rows
-        self.pool = (KVPool(w.num_kv_heads, n2, n4, len(w.requests), max_tab, device=device, n_int3_pages=n3)
-                     if make_pool else None)
+        self.pool = (KVPool(w.num_kv_heads, n2, n4, len(w.requests), max_tab, device=device, n_int3_pages=n3,
+                            n_fp4_pages=nf) if make_pool else None)
         self.rids = [self.pool.open() for _ in w.requests] if make_pool else []
         self.dev = torch.device("cuda", device)
         self.chan = torch.from_numpy(w.k_chan_mult).to(self.dev)
