@@ -144,3 +144,20 @@ def make_workload(cfg_id: int, n_req: Optional[int] = None, ctx: Optional[int] =
 
 def tag_counts(tags: np.ndarray) -> np.ndarray:
     return np.bincount(tags, minlength=N_TAGS).astype(np.int64)
+
+
+FP4_WIDTH = 0xF4   # width value of FP4 (E2M1) tokens
+
+
+def width_mix(w: Workload, r: int, bits: np.ndarray, int3_share: float, fp4_share: float = 0.0) -> np.ndarray:
+    """Input recipe for workloads with more widths than the two-way
+    allocation gives: a seeded fraction `int3_share` of request r's INT4
+    tokens made INT3 and a further `fp4_share` made FP4 (one uniform draw per
+    position, seeded by the workload seed and the request)."""
+    if int3_share <= 0.0 and fp4_share <= 0.0:
+        return bits
+    u = np.random.default_rng([w.seed, 33, r]).random(bits.size)
+    out = bits.copy()
+    out[(bits == 4) & (u < int3_share)] = 3
+    out[(bits == 4) & (u >= int3_share) & (u < int3_share + fp4_share)] = FP4_WIDTH
+    return out

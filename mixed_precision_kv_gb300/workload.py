@@ -10,7 +10,7 @@ from __future__ import annotations
 import numpy as np
 
 import kvsynth
-from kvsynth.recipes import Workload, tag_counts
+from kvsynth.recipes import FP4_WIDTH, Workload, tag_counts, width_mix
 
 from . import KVPool, alloc_bits
 
@@ -25,20 +25,7 @@ def request_bits(w: Workload, r: int, allocator=alloc_bits) -> np.ndarray:
     return bits
 
 
-FP4 = 0xF4   # width value of FP4 (E2M1) tokens
-
-
-def int3_share_bits(w: Workload, r: int, bits: np.ndarray, share: float, fp4_share: float = 0.0) -> np.ndarray:
-    """Seeded fractions of request r's INT4 tokens made INT3 (`share`) and FP4
-    (`fp4_share`): synthetic mixes of more widths (the greedy allocation
-    itself has two)."""
-    if share <= 0.0 and fp4_share <= 0.0:
-        return bits
-    u = np.random.default_rng([w.seed, 33, r]).random(bits.size)
-    out = bits.copy()
-    out[(bits == 4) & (u < share)] = 3
-    out[(bits == 4) & (u >= share) & (u < share + fp4_share)] = FP4
-    return out
+FP4 = FP4_WIDTH   # width value of FP4 (E2M1) tokens
 
 
 def int3_pages(w: Workload, bits_list, steps: int, width: int = 3) -> int:
@@ -79,7 +66,7 @@ class GPUWorkload:
         self.device = device
         self.chunk = chunk
         self.steps = w.steps if steps is None else steps
-        self.bits = [int3_share_bits(w, r, request_bits(w, r), int3_share, fp4_share) for r in range(len(w.requests))]
+        self.bits = [width_mix(w, r, request_bits(w, r), int3_share, fp4_share) for r in range(len(w.requests))]
         self.sizes = pool_size(w, self.bits, chunk, self.steps, extra_tokens)
         n2, n4, max_tab = self.sizes
         n3 = int3_pages(w, self.bits, self.steps)

@@ -6,7 +6,7 @@ import numpy as np
 
 import kvsynth
 import oracle
-from kvsynth.recipes import tag_counts
+from kvsynth.recipes import tag_counts, width_mix
 
 MAX_ABS_TOL = 1e-3     # attention output, fp32 vs fp64 oracle on the same dequantized values
 REL_L2_TOL = 1e-4
@@ -24,15 +24,17 @@ def oracle_bits(w, r):
 class OracleWorkload:
     """Oracle twin of mixed_precision_kv_gb300.workload.GPUWorkload."""
 
-    def __init__(self, w, sizes, chunk, sel_heads=None, content_reqs=None):
+    def __init__(self, w, sizes, chunk, sel_heads=None, content_reqs=None, n_int3_pages=0, n_fp4_pages=0,
+                 int3_share=0.0, fp4_share=0.0):
         n2, n4, max_tab = sizes
         self.w = w
         self.chunk = chunk
         self.sel = list(range(w.num_kv_heads)) if sel_heads is None else list(sel_heads)
         self.content = set(range(len(w.requests))) if content_reqs is None else set(content_reqs)
-        self.P = oracle.OraclePool(w.num_kv_heads, n2, n4, len(w.requests), max_tab, sel_heads=self.sel)
+        self.P = oracle.OraclePool(w.num_kv_heads, n2, n4, len(w.requests), max_tab, sel_heads=self.sel,
+                                   n_int3_pages=n_int3_pages, n_fp4_pages=n_fp4_pages)
         self.rids = [self.P.open() for _ in w.requests]
-        self.bits = [oracle_bits(w, r) for r in range(len(w.requests))]
+        self.bits = [width_mix(w, r, oracle_bits(w, r), int3_share, fp4_share) for r in range(len(w.requests))]
         self.pos = [0] * len(w.requests)
 
     def kv_rows(self, r, tok0, n):

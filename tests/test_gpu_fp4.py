@@ -140,3 +140,62 @@ def test_fp4_errors(kvq):
     with pytest.raises(kvq.KVError) as e:
         gpu.append(k, k, [r], [0xF3])
     assert e.value.status == kvq.KV_ERR_INVALID_ARG
+
+
+def test_config2_full_size_four_widths(kvq):
+    """The 32K-token batch-8 workload at full size with 30 % of its INT4
+    tokens made INT3 and 30 % FP4 (`bench.py --config 2 --int3-share 0.3
+    --fp4-share 0.3` builds the same pool), then 4 decode steps: every table
+    bit-exact, sampled units' codes and outputs against the oracle."""
+    from harness import OracleWorkload, compare_content
+    from mixed_precision_kv_gb300.workload import GPUWorkload, int3_pages, pool_size
+    steps = 4
+    w = kvsynth.make_workload(2, steps=steps)
+    gw = GPUWorkload(w, steps=steps, int3_share=0.3, fp4_share=0.3)
+    n3, nf = int3_pages(w, gw.bits, steps), int3_pages(w, gw.bits, steps, FP4)
+    assert n3 > 0 and nf > 0
+    sel, reqs = [2, 7], [1, 6]
+    ow = OracleWorkload(w, pool_size(w, gw.bits, gw.chunk, gw.steps), gw.chunk, sel_heads=sel, content_reqs=reqs,
+                        n_int3_pages=n3, n_fp4_pages=nf, int3_share=0.3, fp4_share=0.3)
+    for a, b in zip(gw.bits, ow.bits):
+        assert np.array_equal(a, b)
+    gw.prefill()
+    ow.prefill()
+    gw.evict()
+    ow.evict()
+    gw.reorder()
+    ow.reorder()
+    gw.pool.sync()
+    g = w.g
+
+    def check(step, content):
+        out = gw.decode(gw.q(step)).cpu().numpy()
+        gw.pool.sync()
+        for r in range(len(gw.rids)):
+            compare_tables(gw.pool.export(gw.rids[r], content=False), ow.P.export(ow.rids[r], content=False))
+        if content:
+            for r in reqs:
+                ge, oe = gw.pool.export(gw.rids[r]), ow.P.export(ow.rids[r])
+                compare_tables(ge, oe)
+                for i in range(oe["ids"].size):
+                    f = int(oe["fill"][i])
+                    for j, h in enumerate(sel):
+                        for key in ("kc", "vc"):
+                            assert np.array_equal(ge[key][i, h, :f], oe[key][i, j, :f]), (r, i, h, key)
+                        if not oe["is_int2"][i]:
+                            assert np.array_equal(ge["km"][i, h, :8 * f], oe["km"][i, j, :8 * f]), (r, i, h)
+                        assert np.array_equal(ge["vm"][i, h, :8 * f], oe["vm"][i, j, :8 * f]), (r, i, h)
+        pairs = np.array([(b, h * g + x) for b in reqs for h in sel for x in range(g)], np.int32)
+        ref = ow.decode(ow.q(step), pairs=pairs)
+        got = np.stack([out[b, hq] for b, hq in pairs])
+        assert np.isfinite(got).all()
+        assert_outputs_close(got, ref, f"32K batch 8 four widths, step {step}")
+
+    check(0, True)
+    for step in range(1, steps + 1):
+        k, v, _, bits = gw.step_inputs()
+        gw.append_step(k, v, np.array(gw.rids, np.int32), bits)
+        ow.append_step()
+        gw.reorder()
+        ow.reorder()
+        check(step, step == steps)
