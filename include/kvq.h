@@ -1,6 +1,6 @@
 /*
- * kvq.h -- C ABI of the GB300 (sm_103a) mixed INT2/INT4 paged KV cache and its
- * decode-step attention.
+ * kvq.h -- C ABI of the GB300 (sm_103a) mixed INT2/INT4 paged KV cache (with INT3
+ * and FP4 pages as further widths) and its decode-step attention.
  *
  * The problem these calls follow:
  *   - TriAxialKV, key design 3 (custom mixed-precision cache layout and
@@ -37,9 +37,10 @@
  *   - No C++ exception crosses this boundary.
  *
  * Fixed format: head_dim 128, 32 tokens per page, group size 32.  Page block
- * of one (page, kv head): INT2 = 3072 bytes, INT4 = 5120 bytes (codes plus
- * binary16 scale/zero).  The physical byte order inside a block is private to
- * the library; kv_export_request() returns the canonical content.
+ * of one (page, kv head): INT2 = 3072 bytes, INT4 = 5120 bytes, INT3 = 4096
+ * bytes, FP4 = 4608 bytes (codes plus binary16 scale/zero; FP4 scales only).
+ * The physical byte order inside a block is private to the library;
+ * kv_export_request() returns the canonical content.
  */
 #ifndef KVQ_H
 #define KVQ_H
@@ -297,19 +298,24 @@ KVQ_API kv_status_t kv_request_info(kv_pool_t* pool, int32_t req_id, int32_t* n_
  * buffers sized from kv_request_info):
  *   ids [n], is_int2 [n], fill [n] (tokens written), live [n] (bit t = slot t live)
  *   k_codes, v_codes  uint8 [n][num_kv_heads][32][128]  (slot, channel)
- *   k_meta            uint16 [n][num_kv_heads][256]: INT4 page -> [slot][group]{scale, zero},
+ *   k_meta            uint16 [n][num_kv_heads][256]: INT4 / INT3 / FP4 page -> [slot][group]{scale, zero},
  *                     INT2 page -> [channel]{scale, zero}   (binary16 bits)
  *   v_meta            uint16 [n][num_kv_heads][256]: [slot][group]{scale, zero}
- * The four content pointers may all be NULL to export the table only.  Slots
- * at or past `fill` hold unspecified content. */
+ * An INT3 page's codes are 0..7; an FP4 page's codes are E2M1 codes (sign <<
+ * 3 | exponent << 1 | mantissa) with zero entries 0, its value = scale *
+ * E2M1(code).  The width of a page follows from its id (n_int2_pages,
+ * n_int4_pages, n_int3_pages ranges).  The four content pointers may all be
+ * NULL to export the table only.  Slots at or past `fill` hold unspecified
+ * content. */
 KVQ_API kv_status_t kv_export_request(kv_pool_t* pool, int32_t req_id, int32_t* ids, uint8_t* is_int2, uint8_t* fill,
                               uint32_t* live, uint8_t* k_codes, uint8_t* v_codes, uint16_t* k_meta,
                               uint16_t* v_meta);
 
 /* Algorithmic bytes and split count of the most recent kv_decode_attn call:
- * codes + scale/zero of every page block read (partial INT4 pages count their
- * filled prefix), 8 bytes per table entry, q (bf16) and out (fp32), and the
- * bf16 K and V rows of the full-precision lists. */
+ * codes + scale/zero of every page block read (partial INT4, INT3 and FP4
+ * pages count their filled prefix: 160, 128 and 144 bytes per token and kv
+ * head), 8 bytes per table entry, q (bf16) and out (fp32), and the bf16 K and
+ * V rows of the full-precision lists. */
 KVQ_API kv_status_t kv_last_decode_stats(kv_pool_t* pool, int64_t* kv_bytes, int32_t* n_splits, int64_t* n_pages);
 
 /* Device-time measurement of the decode kernels.  enable = N >= 1 starts (or
