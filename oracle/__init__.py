@@ -49,6 +49,7 @@ def lib():
                 "orc_quant_group": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int, _P, _P, _P]),
                 "orc_dequant": (_F32, [ctypes.c_uint8, ctypes.c_uint16, ctypes.c_uint16]),
                 "orc_alloc_bits": (ctypes.c_int, [_P, _P, _P, ctypes.c_int, _I64, _I64, _P]),
+                "orc_alloc_bits3": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_int, _I64, _I64, _P]),
                 "orc_pool_new": (_P, [ctypes.c_int, _I64, _I64, _I64, _I64, ctypes.c_int, ctypes.c_int, _P,
                                       ctypes.c_int]),
                 "orc_fp4_group": (ctypes.c_int, [_P, ctypes.c_int, _P, _P]),
@@ -141,6 +142,16 @@ def alloc_bits(N, D2, D4, budget):
     out = np.empty(N.size, dtype=np.uint8)
     _check(lib().orc_alloc_bits(_p(N), _p(D2), _p(D4), N.size, int(budget[0]), int(budget[1]), _p(out)),
            "alloc_bits")
+    return out
+
+
+def alloc_bits3(N, D2, D3, D4, budget):
+    """Greedy INT2/INT3/INT4 allocation over one-bit steps; budget = (num, den) average bits."""
+    N = np.ascontiguousarray(N, dtype=np.int64)
+    D2, D3, D4 = (np.ascontiguousarray(d, dtype=np.float64) for d in (D2, D3, D4))
+    out = np.empty(N.size, dtype=np.uint8)
+    _check(lib().orc_alloc_bits3(_p(N), _p(D2), _p(D3), _p(D4), N.size, int(budget[0]), int(budget[1]), _p(out)),
+           "alloc_bits3")
     return out
 
 

@@ -92,6 +92,18 @@
  *       [TriAxialKV, limitations and outlook: non-uniform FP formats;
  *        comparison with a uniform FP4 cache; HyQuant, background on
  *        low-bit quantization: s = max|X| / c_B].
+ *   R13 bit allocation over three widths (the limitations section: the
+ *      two-way INT2/INT4 choice is what INT3 would widen).  Read as the same
+ *      greedy over one-bit steps: every tag starts at 2 bits and has a
+ *      2 -> 3 step and a 3 -> 4 step, each costing N_k bit-tokens and saving
+ *      D_k(2) - D_k(3) and D_k(3) - D_k(4); the available step with the most
+ *      distortion saved per bit-token, (saving) / N_k in fp64, is taken next
+ *      (a 3 -> 4 step becomes available once its 2 -> 3 step is taken; ties:
+ *      the lower tag); a step that does not fit the budget (R7's exact
+ *      integer test) is dropped and the scan continues.  With one 2 -> 4 step
+ *      per tag (saving D(2) - D(4) over 2 N_k bit-tokens) this is key design
+ *      2's rule
+ *       [TriAxialKV, key design 2; limitations and outlook].
  *   R10 a full page none of whose 32 slots is live for any kv head may leave
  *      its request's table: the other entries keep their order and their
  *      pages do not move, its id returns to the free set, and the positions
@@ -440,6 +452,41 @@ int orc_alloc_bits(const int64_t* N, const double* D2, const double* D4, int n_t
     if ((used + extra) * B_den <= B_num * total) {
       bits_out[e.second] = 4;
       used += extra;
+    }
+  }
+  return ORC_OK;
+}
+
+// Greedy allocation over three widths (R13): bits_out[k] in {2, 3, 4}.
+int orc_alloc_bits3(const int64_t* N, const double* D2, const double* D3, const double* D4, int n_tags,
+                    int64_t B_num, int64_t B_den, uint8_t* bits_out) {
+  if (n_tags <= 0 || B_den <= 0 || B_num < 0) return ORC_INVALID;
+  int64_t total = 0;
+  for (int k = 0; k < n_tags; ++k) {
+    if (N[k] < 0) return ORC_INVALID;
+    total += N[k];
+    bits_out[k] = 2;
+  }
+  // open[k]: the width tag k's next step starts from (2 or 3), 0 when it has none
+  std::vector<int> open(n_tags, 0);
+  for (int k = 0; k < n_tags; ++k) open[k] = N[k] > 0 ? 2 : 0;
+  int64_t used = 2 * total;
+  for (;;) {
+    int best = -1;
+    double best_rho = 0.0;
+    for (int k = 0; k < n_tags; ++k) {
+      if (!open[k]) continue;
+      const double saving = open[k] == 2 ? D2[k] - D3[k] : D3[k] - D4[k];
+      const double rho = saving / (double)N[k];
+      if (best < 0 || rho > best_rho) { best = k; best_rho = rho; }   // ties keep the lower tag
+    }
+    if (best < 0) break;
+    if ((used + N[best]) * B_den <= B_num * total) {
+      used += N[best];
+      bits_out[best] = (uint8_t)(open[best] + 1);
+      open[best] = open[best] == 2 ? 3 : 0;
+    } else {
+      open[best] = 0;                                 // dropped: and so is its 3 -> 4 step
     }
   }
   return ORC_OK;
