@@ -344,6 +344,19 @@ KVQ_API kv_status_t kv_pool_launch_count(kv_pool_t* pool, int64_t* n_launches);
 KVQ_API kv_status_t kv_alloc_bits(const int64_t* N, const double* D2, const double* D4, int32_t n_tags, int64_t B_num,
                           int64_t B_den, uint8_t* bits_out);
 
+/* Greedy allocation over three widths (TriAxialKV, key design 2, with the
+ * INT3 width its limitations and outlook section names): every tag starts at
+ * 2 bits; its 2 -> 3 step saves D2[k] - D3[k], its 3 -> 4 step
+ * D3[k] - D4[k], each costing N_k bit-tokens.  The available step with the
+ * most distortion saved per bit-token goes first (a tag's 3 -> 4 step
+ * becomes available once its 2 -> 3 step is taken; ties: the lower tag); a
+ * step that does not fit sum_k N_k b_k <= (B_num / B_den) sum_k N_k (exact
+ * integer test) is dropped and the scan continues.  With D3 = (D2 + D4) / 2
+ * and room for whole upgrades only, the result is kv_alloc_bits's.
+ *   N, D2, D3, D4  host [n_tags];  bits_out  host uint8 [n_tags] in {2, 3, 4}. */
+KVQ_API kv_status_t kv_alloc_bits3(const int64_t* N, const double* D2, const double* D3, const double* D4,
+                                   int32_t n_tags, int64_t B_num, int64_t B_den, uint8_t* bits_out);
+
 /* Message for the calling thread's most recent failure ("" if none). */
 KVQ_API const char* kv_last_error(void);
 

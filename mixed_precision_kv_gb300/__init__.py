@@ -28,7 +28,7 @@ EXPORTED = ["kv_pool_create", "kv_pool_destroy", "kv_request_open", "kv_request_
             "kv_request_info", "kv_export_request", "kv_last_decode_stats", "kv_pool_launch_count", "kv_alloc_bits",
             "kv_last_error", "kv_decode_attn_noalloc", "kv_decode_timing", "kv_evict_slots_head", "kv_fp_configure",
             "kv_fp_append", "kv_fp_drop", "kv_fp_count", "kv_set_wait_limit", "kv_drop_dead_pages",
-            "kv_decode_attn_groups"]
+            "kv_decode_attn_groups", "kv_alloc_bits3"]
 
 _P = ctypes.c_void_p
 _I32, _I64 = ctypes.c_int32, ctypes.c_int64
@@ -84,6 +84,7 @@ def load_library(path: str = LIB_PATH):
             "kv_pool_launch_count": [_P, _P],
             "kv_decode_timing": [_P, _I32, _P, _P, _P],
             "kv_alloc_bits": [_P, _P, _P, _I32, _I64, _I64, _P],
+            "kv_alloc_bits3": [_P, _P, _P, _P, _I32, _I64, _I64, _P],
         }
         for name, args in sig.items():
             fn = getattr(L, name)
@@ -142,6 +143,16 @@ def alloc_bits(N, D2, D4, budget):
     out = np.empty(N.size, dtype=np.uint8)
     _check(load_library().kv_alloc_bits(_ptr(N), _ptr(D2), _ptr(D4), N.size, int(budget[0]), int(budget[1]),
                                         _ptr(out)), "kv_alloc_bits")
+    return out
+
+
+def alloc_bits3(N, D2, D3, D4, budget):
+    """Greedy INT2/INT3/INT4 bit allocation over one-bit steps (host); budget = (num, den)."""
+    N = _np(N, np.int64)
+    D2, D3, D4 = _np(D2, np.float64), _np(D3, np.float64), _np(D4, np.float64)
+    out = np.empty(N.size, dtype=np.uint8)
+    _check(load_library().kv_alloc_bits3(_ptr(N), _ptr(D2), _ptr(D3), _ptr(D4), N.size, int(budget[0]),
+                                         int(budget[1]), _ptr(out)), "kv_alloc_bits3")
     return out
 
 

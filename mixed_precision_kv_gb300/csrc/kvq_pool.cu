@@ -400,6 +400,49 @@ kv_status_t kv_alloc_bits(const int64_t* N, const double* D2, const double* D4, 
   return KV_OK;
 }
 
+kv_status_t kv_alloc_bits3(const int64_t* N, const double* D2, const double* D3, const double* D4, int32_t n_tags,
+                           int64_t B_num, int64_t B_den, uint8_t* bits_out) {
+  if (!N || !D2 || !D3 || !D4 || !bits_out || n_tags <= 0)
+    return fail(KV_ERR_INVALID_ARG, "kv_alloc_bits3: bad pointer or n_tags");
+  if (B_den <= 0 || B_num < 0) return fail(KV_ERR_INVALID_ARG, "kv_alloc_bits3: budget must be num >= 0, den > 0");
+  int64_t total = 0;
+  for (int32_t k = 0; k < n_tags; ++k) {
+    if (N[k] < 0) return fail(KV_ERR_INVALID_ARG, "kv_alloc_bits3: negative count");
+    total += N[k];
+    bits_out[k] = 2;
+  }
+  // One-bit steps in a max-heap keyed by distortion saved per bit-token
+  // (ties: lower tag first); a tag's 3 -> 4 step enters once its 2 -> 3 step
+  // is taken.  Integer budget test: (used + N_k) * den <= num * total.
+  struct Step {
+    double rho;
+    int32_t tag;
+  };
+  auto later = [](const Step& a, const Step& b) { return a.rho != b.rho ? a.rho < b.rho : a.tag > b.tag; };
+  std::vector<Step> heap;
+  heap.reserve((size_t)n_tags);
+  for (int32_t k = 0; k < n_tags; ++k)
+    if (N[k] > 0) heap.push_back(Step{(D2[k] - D3[k]) / (double)N[k], k});
+  std::make_heap(heap.begin(), heap.end(), later);
+  int64_t used = 2 * total;
+  while (!heap.empty()) {
+    std::pop_heap(heap.begin(), heap.end(), later);
+    const Step st = heap.back();
+    heap.pop_back();
+    const int32_t k = st.tag;
+    if ((used + N[k]) * B_den > B_num * total) continue;   // dropped, with any later step of the tag
+    used += N[k];
+    if (bits_out[k] == 2) {
+      bits_out[k] = 3;
+      heap.push_back(Step{(D3[k] - D4[k]) / (double)N[k], k});
+      std::push_heap(heap.begin(), heap.end(), later);
+    } else {
+      bits_out[k] = 4;
+    }
+  }
+  return KV_OK;
+}
+
 kv_status_t kv_pool_create(const kv_pool_config_t* cfg, kv_pool_t** out) {
   if (!cfg || !out) return fail(KV_ERR_INVALID_ARG, "kv_pool_create: null argument");
   *out = nullptr;

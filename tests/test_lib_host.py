@@ -61,3 +61,21 @@ def test_workload_bits_agree_between_sides(kvq, orc):
         w = kvsynth.make_workload(cfg, n_req=3, ctx=3000 if cfg != 4 else None)
         for r in range(3):
             assert np.array_equal(request_bits(w, r), oracle_bits(w, r))
+
+
+def test_alloc_bits3_matches_oracle(kvq, orc):
+    rng = np.random.default_rng(31)
+    for _ in range(300):
+        n = int(rng.integers(1, 57))
+        N = rng.integers(0, 300, n).astype(np.int64)
+        if rng.integers(0, 4) == 0:
+            N[:] = int(rng.integers(1, 40))            # equal counts: many equal savings per bit-token
+        D4 = rng.uniform(0.01, 1, n)
+        D2 = D4 * (1 + rng.uniform(0.5, 20, n))
+        D3 = D4 + (D2 - D4) * rng.uniform(0.0, 1.0, n)
+        if rng.integers(0, 4) == 0:
+            D3 = (D2 + D4) / 2
+        B = (int(rng.integers(18, 42)), 10)
+        assert np.array_equal(kvq.alloc_bits3(N, D2, D3, D4, B), orc.alloc_bits3(N, D2, D3, D4, B))
+    with pytest.raises(kvq.KVError):
+        kvq.alloc_bits3([1, 2], [1.0, 2.0], [0.7, 1.5], [0.5, 1.0], (3, 0))
