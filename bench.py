@@ -346,6 +346,30 @@ def run_prefill(args):
     return 0
 
 
+def alloc_quality(w):
+    """Synthetic distortion sum_k N_k D_k(b_k) of the prompts under the
+    two-width and the three-width allocation at the same budget, and their
+    average bits (the recipe's D tables stand in for a calibration)."""
+    import mixed_precision_kv_gb300 as kvq
+    from kvsynth.recipes import d3_table, tag_counts
+    D3 = d3_table(w)
+    D = np.stack([w.D2, D3, w.D4], 1)
+    out = {"distortion_2w": 0.0, "distortion_3w": 0.0, "bits_2w": 0.0, "bits_3w": 0.0, "tokens": 0}
+    for spec in w.requests:
+        N = tag_counts(spec.tags[:spec.n_prefill])
+        b2 = kvq.alloc_bits(N, w.D2, w.D4, spec.budget).astype(np.int64)
+        b3 = kvq.alloc_bits3(N, w.D2, D3, w.D4, spec.budget).astype(np.int64)
+        k = np.arange(N.size)
+        out["distortion_2w"] += float((N * D[k, b2 - 2]).sum())
+        out["distortion_3w"] += float((N * D[k, b3 - 2]).sum())
+        out["bits_2w"] += float((N * b2).sum())
+        out["bits_3w"] += float((N * b3).sum())
+        out["tokens"] += int(N.sum())
+    out["bits_2w"] /= out["tokens"]
+    out["bits_3w"] /= out["tokens"]
+    return out
+
+
 def load_workload(args, total_steps):
     import kvsynth
     w = kvsynth.make_workload(args.config, steps=total_steps, n_req=args.requests or None)
@@ -542,6 +566,9 @@ def main():
                     help="make a seeded fraction of the INT4 tokens INT3 (three-width pool; prefill and steps)")
     ap.add_argument("--fp4-share", type=float, default=0.0,
                     help="make a seeded fraction of the INT4 tokens FP4 (E2M1) (prefill and steps)")
+    ap.add_argument("--alloc3", action="store_true",
+                    help="allocate INT2/INT3/INT4 with the three-width greedy over the same budget (D(3) from "
+                         "the input recipe)")
     ap.add_argument("--mode", default="decode", choices=["decode", "prefill"],
                     help="decode: the decode-step line (default); prefill: bulk quantization of the workload's "
                          "prompts through kv_append_quant")
@@ -576,8 +603,10 @@ def main():
         w.name = f"{w.name}+int3-{args.int3_share:g}"
     if args.fp4_share > 0:
         w.name = f"{w.name}+fp4-{args.fp4_share:g}"
+    if args.alloc3:
+        w.name = f"{w.name}+alloc3"
     gw = GPUWorkload(w, device=local, steps=total_steps, extra_tokens=extra, int3_share=args.int3_share,
-                     fp4_share=args.fp4_share)
+                     fp4_share=args.fp4_share, three_widths=args.alloc3)
     gw.pool.set_decode_impl({"auto": 0, "simt": 1, "mma": 2}[args.decode_impl])
     gw.prefill()
     gw.evict()
@@ -765,7 +794,10 @@ def main():
         line["config"]["int3_token_fraction"] = float(np.mean(np.concatenate(gw.bits) == 3))
     if args.fp4_share > 0:
         line["config"]["fp4_token_fraction"] = float(np.mean(np.concatenate(gw.bits) == 0xF4))
-    if rank == 0 and not args.no_cpu_baseline and args.int3_share <= 0 and args.fp4_share <= 0:
+    if args.alloc3:
+        line["config"]["int3_token_fraction"] = float(np.mean(np.concatenate(gw.bits) == 3))
+        line["config"]["allocation"] = alloc_quality(w)
+    if rank == 0 and not args.no_cpu_baseline and args.int3_share <= 0 and args.fp4_share <= 0 and not args.alloc3:
         try:
             line["cpu_baseline"] = cpu_baseline(w)
         except Exception as e:  # reported, not fatal

@@ -161,3 +161,14 @@ def width_mix(w: Workload, r: int, bits: np.ndarray, int3_share: float, fp4_shar
     out[(bits == 4) & (u < int3_share)] = 3
     out[(bits == 4) & (u >= int3_share) & (u < int3_share + fp4_share)] = FP4_WIDTH
     return out
+
+
+_PART_TABLE3 = 4
+
+
+def d3_table(w: Workload) -> np.ndarray:
+    """D_k(3) for the three-width allocation: between D_k(4) and D_k(2), the
+    2 -> 3 step saving 55..80 % of the 2 -> 4 saving (a convex distortion
+    curve), from its own seeded stream (the two-width tables are unchanged)."""
+    r = _rng(w.seed, _PART_TABLE3)
+    return w.D4 + (w.D2 - w.D4) * r.uniform(0.2, 0.45, w.D2.size)

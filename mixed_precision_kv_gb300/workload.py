@@ -10,15 +10,19 @@ from __future__ import annotations
 import numpy as np
 
 import kvsynth
-from kvsynth.recipes import FP4_WIDTH, Workload, tag_counts, width_mix
+from kvsynth.recipes import FP4_WIDTH, Workload, d3_table, tag_counts, width_mix
 
-from . import KVPool, alloc_bits
+from . import KVPool, alloc_bits, alloc_bits3
 
 
-def request_bits(w: Workload, r: int, allocator=alloc_bits) -> np.ndarray:
-    """Bit width of every token position of request r (prefill and decode steps)."""
+def request_bits(w: Workload, r: int, allocator=alloc_bits, three_widths: bool = False) -> np.ndarray:
+    """Bit width of every token position of request r (prefill and decode
+    steps); three_widths: the INT2/INT3/INT4 allocation over the same budget."""
     spec = w.requests[r]
-    b = allocator(tag_counts(spec.tags[:spec.n_prefill]), w.D2, w.D4, spec.budget)
+    if three_widths:
+        b = alloc_bits3(tag_counts(spec.tags[:spec.n_prefill]), w.D2, d3_table(w), w.D4, spec.budget)
+    else:
+        b = allocator(tag_counts(spec.tags[:spec.n_prefill]), w.D2, w.D4, spec.budget)
     bits = b[spec.tags].astype(np.uint8)
     if w.force_int4_decode:
         bits[spec.n_prefill:] = 4
@@ -60,13 +64,15 @@ def pool_size(w: Workload, bits_list, chunk: int, steps: int, extra: int = 0):
 
 class GPUWorkload:
     def __init__(self, w: Workload, device: int = 0, chunk: int = 16384, steps: int | None = None,
-                 extra_tokens: int = 0, make_pool: bool = True, int3_share: float = 0.0, fp4_share: float = 0.0):
+                 extra_tokens: int = 0, make_pool: bool = True, int3_share: float = 0.0, fp4_share: float = 0.0,
+                 three_widths: bool = False):
         import torch
         self.w = w
         self.device = device
         self.chunk = chunk
         self.steps = w.steps if steps is None else steps
-        self.bits = [width_mix(w, r, request_bits(w, r), int3_share, fp4_share) for r in range(len(w.requests))]
+        self.bits = [width_mix(w, r, request_bits(w, r, three_widths=three_widths), int3_share, fp4_share)
+                     for r in range(len(w.requests))]
         self.sizes = pool_size(w, self.bits, chunk, self.steps, extra_tokens)
         n2, n4, max_tab = self.sizes
         n3 = int3_pages(w, self.bits, self.steps)

@@ -6,15 +6,18 @@ import numpy as np
 
 import kvsynth
 import oracle
-from kvsynth.recipes import tag_counts, width_mix
+from kvsynth.recipes import d3_table, tag_counts, width_mix
 
 MAX_ABS_TOL = 1e-3     # attention output, fp32 vs fp64 oracle on the same dequantized values
 REL_L2_TOL = 1e-4
 
 
-def oracle_bits(w, r):
+def oracle_bits(w, r, three_widths=False):
     spec = w.requests[r]
-    b = oracle.alloc_bits(tag_counts(spec.tags[:spec.n_prefill]), w.D2, w.D4, spec.budget)
+    if three_widths:
+        b = oracle.alloc_bits3(tag_counts(spec.tags[:spec.n_prefill]), w.D2, d3_table(w), w.D4, spec.budget)
+    else:
+        b = oracle.alloc_bits(tag_counts(spec.tags[:spec.n_prefill]), w.D2, w.D4, spec.budget)
     bits = b[spec.tags].astype(np.uint8)
     if w.force_int4_decode:
         bits[spec.n_prefill:] = 4
@@ -25,7 +28,7 @@ class OracleWorkload:
     """Oracle twin of mixed_precision_kv_gb300.workload.GPUWorkload."""
 
     def __init__(self, w, sizes, chunk, sel_heads=None, content_reqs=None, n_int3_pages=0, n_fp4_pages=0,
-                 int3_share=0.0, fp4_share=0.0):
+                 int3_share=0.0, fp4_share=0.0, three_widths=False):
         n2, n4, max_tab = sizes
         self.w = w
         self.chunk = chunk
@@ -34,7 +37,8 @@ class OracleWorkload:
         self.P = oracle.OraclePool(w.num_kv_heads, n2, n4, len(w.requests), max_tab, sel_heads=self.sel,
                                    n_int3_pages=n_int3_pages, n_fp4_pages=n_fp4_pages)
         self.rids = [self.P.open() for _ in w.requests]
-        self.bits = [width_mix(w, r, oracle_bits(w, r), int3_share, fp4_share) for r in range(len(w.requests))]
+        self.bits = [width_mix(w, r, oracle_bits(w, r, three_widths), int3_share, fp4_share)
+                     for r in range(len(w.requests))]
         self.pos = [0] * len(w.requests)
 
     def kv_rows(self, r, tok0, n):

@@ -214,3 +214,55 @@ def test_int3_errors(kvq):
     q = _dev(kvsynth.fill_bf16_host(1, 2, 128, SEED, kvsynth.TENSOR_Q, 0))
     with pytest.raises(kvq.KVError):
         kvq.KVPool.decode_groups([a, b], q, np.array([[ra], [rb]], np.int32), SCALE)
+
+
+def test_config2_full_size_three_width_allocation(kvq):
+    """The 32K-token batch-8 workload at full size with the three-width
+    allocation (kv_alloc_bits3 over the same budget; `bench.py --config 2
+    --alloc3` builds the same pool): the widths equal the oracle's
+    allocation, every table bit-exact, sampled units' codes and outputs
+    within the tolerance, over 3 decode steps."""
+    from harness import OracleWorkload
+    from mixed_precision_kv_gb300.workload import GPUWorkload, int3_pages, pool_size
+    steps = 3
+    w = kvsynth.make_workload(2, steps=steps)
+    gw = GPUWorkload(w, steps=steps, three_widths=True)
+    n3 = int3_pages(w, gw.bits, steps)
+    assert n3 > 0
+    sel, reqs = [0, 5], [2, 7]
+    ow = OracleWorkload(w, pool_size(w, gw.bits, gw.chunk, gw.steps), gw.chunk, sel_heads=sel, content_reqs=reqs,
+                        n_int3_pages=n3, three_widths=True)
+    for a, b in zip(gw.bits, ow.bits):
+        assert np.array_equal(a, b)
+    assert any((b == 3).any() for b in gw.bits)
+    gw.prefill()
+    ow.prefill()
+    gw.evict()
+    ow.evict()
+    gw.reorder()
+    ow.reorder()
+    gw.pool.sync()
+    g = w.g
+
+    def check(step, content):
+        out = gw.decode(gw.q(step)).cpu().numpy()
+        gw.pool.sync()
+        for r in range(len(gw.rids)):
+            compare_tables(gw.pool.export(gw.rids[r], content=False), ow.P.export(ow.rids[r], content=False))
+        if content:
+            for r in reqs:
+                compare_content(gw.pool.export(gw.rids[r]), ow.P.export(ow.rids[r]), sel)
+        pairs = np.array([(b, h * g + x) for b in reqs for h in sel for x in range(g)], np.int32)
+        ref = ow.decode(ow.q(step), pairs=pairs)
+        got = np.stack([out[b, hq] for b, hq in pairs])
+        assert np.isfinite(got).all()
+        assert_outputs_close(got, ref, f"32K batch 8 three-width allocation, step {step}")
+
+    check(0, True)
+    for step in range(1, steps + 1):
+        k, v, _, bits = gw.step_inputs()
+        gw.append_step(k, v, np.array(gw.rids, np.int32), bits)
+        ow.append_step()
+        gw.reorder()
+        ow.reorder()
+        check(step, step == steps)
