@@ -48,6 +48,35 @@ def test_noalloc_decode_matches_decode_on_two_calls(kvq, impl):
         assert_outputs_close(got, orc, f"noalloc vs oracle, call {step}")
 
 
+@pytest.mark.parametrize("impl", [2, 1])
+def test_noalloc_decode_with_int3_and_fp4_pages(kvq, impl):
+    """The same two-call comparison on a pool that also holds INT3 and FP4
+    pages (the scan variant that reads them)."""
+    from mixed_precision_kv_gb300.workload import GPUWorkload, int3_pages, pool_size
+    w = kvsynth.make_workload(3, n_req=3, ctx=5000)
+    gw = GPUWorkload(w, chunk=2048, int3_share=0.4, fp4_share=0.4)
+    gw.pool.set_decode_impl(impl)
+    n3, nf = int3_pages(w, gw.bits, gw.steps), int3_pages(w, gw.bits, gw.steps, 0xF4)
+    assert n3 > 0 and nf > 0
+    ow = OracleWorkload(w, pool_size(w, gw.bits, 2048, gw.steps), 2048, n_int3_pages=n3, n_fp4_pages=nf,
+                        int3_share=0.4, fp4_share=0.4)
+    for o in (gw, ow):
+        o.prefill()
+        o.reorder()
+    gw.pool.sync()
+    for step in (0, 1):
+        q = gw.q(step)
+        ref = gw.decode(q).clone()
+        out = torch.full_like(ref, float("nan"))
+        gw.pool.decode_noalloc(q, gw.rids, w.softmax_scale, out)
+        gw.pool.sync()
+        got = out.cpu().numpy()
+        assert np.isfinite(got).all()
+        assert_outputs_close(got, ref.cpu().numpy(), f"noalloc vs decode with INT3/FP4, call {step}")
+        orc = ow.decode(ow.q(step)).reshape(got.shape)
+        assert_outputs_close(got, orc, f"noalloc vs oracle with INT3/FP4, call {step}")
+
+
 def _many_short_requests(kvq, n_req, hkv=8, hq=64, n_tok=70, fp_tokens=2):
     """n_req requests of n_tok mixed INT2/INT4 tokens on both sides, every
     request with `fp_tokens` full-precision list tokens per kv head."""
