@@ -261,8 +261,8 @@ KVQ_API kv_status_t kv_decode_attn_noalloc(kv_pool_t* pool, const void* q, const
  * Results equal kv_decode_attn on one pool with all K heads in which each
  * head's excluded positions read as dead.  The scan skips every page with no
  * live slot for the head it reads it for.  Always the tensor-core scan,
- * whatever kv_set_decode_impl chose.  Requests holding full-precision list
- * tokens are KV_ERR_INVALID_ARG.  The plan, the q operands and the partials
+ * whatever kv_set_decode_impl chose; pools may hold INT3 and FP4 pages.
+ * Requests holding full-precision list tokens are KV_ERR_INVALID_ARG.  The plan, the q operands and the partials
  * live in pools[0]'s buffers, and a timeout of the scan is reported by
  * pools[0]'s kv_pool_sync; every pool's later work on another stream waits
  * for this call.  kv_last_decode_stats of each pool gives the bytes and

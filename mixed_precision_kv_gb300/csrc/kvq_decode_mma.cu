@@ -963,9 +963,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(
         const uint32_t* hd = gp->hdead;
         blive = hd ? e.live & ~hd[(size_t)e.id * ghkv + lkvh] : e.live;
         const bool i2 = e.id < gn2;
-        btag = (lsg << 7) | (i2 ? 64 : 0) | lkvh;
+        int cls = i2 ? 1 : 0;   // width class in the ticket: 0 INT4, 1 INT2, 2 INT3, 3 FP4
         const uint8_t* src = i2 ? gp->pool + ((size_t)e.id * ghkv + lkvh) * kInt2Block
                                 : gp->pool + gp->int4_off + ((size_t)(e.id - gn2) * ghkv + lkvh) * kInt4Block;
+        if constexpr (kI3) {
+          if (e.id >= gp->nfb) {
+            cls = 3;
+            src = gp->pool + gp->fp4_off + ((size_t)(e.id - gp->nfb) * ghkv + lkvh) * kFp4Block;
+          } else if (e.id >= gp->n3b) {
+            cls = 2;
+            src = gp->pool + gp->int3_off + ((size_t)(e.id - gp->n3b) * ghkv + lkvh) * kInt3Block;
+          }
+        }
+        btag = (lsg << 8) | (cls << 6) | lkvh;
         bsrc = (unsigned long long)(uintptr_t)src;
       } else {
         // slots excluded for this kv head only read as dead slots too
@@ -1014,10 +1024,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(
                   __shfl_sync(0xFFFFFFFFu, btag, j)};
   };
   // a ticket's width and split
-  auto tk_int2 = [&](const Ticket& t) { return kMulti ? ((t.tag >> 6) & 1) != 0 : t.id < n2; };
-  auto tk_split = [&](const Ticket& t) { return kMulti ? t.tag >> 7 : t.tag >> 6; };
-  auto tk_int3 = [&](const Ticket& t) { return kI3 && t.id >= n3b && t.id < nfb; };
-  auto tk_fp4 = [&](const Ticket& t) { return kI3 && t.id >= nfb; };
+  auto tk_int2 = [&](const Ticket& t) { return kMulti ? ((t.tag >> 6) & 3) == 1 : t.id < n2; };
+  auto tk_split = [&](const Ticket& t) { return kMulti ? t.tag >> 8 : t.tag >> 6; };
+  auto tk_int3 = [&](const Ticket& t) {
+    return kI3 && (kMulti ? ((t.tag >> 6) & 3) == 2 : (t.id >= n3b && t.id < nfb));
+  };
+  auto tk_fp4 = [&](const Ticket& t) { return kI3 && (kMulti ? ((t.tag >> 6) & 3) == 3 : t.id >= nfb); };
   // copy number n goes to stage n & 1 and completes phase (n >> 1) & 1
   auto issue = [&](const Ticket& t, unsigned long long src, uint32_t n) {   // lane 0
     const uint32_t st = n & (kStages - 1);
@@ -1208,7 +1220,7 @@ cudaError_t set_scan_attributes() {
 template <int G>
 cudaError_t launch_mma_g(kv_pool* P, const void* q, int32_t hq, float scale_log2, const Unit* d_units, int n_units,
                          const Split* d_splits, const int32_t* d_wsplit, int n_workers, void* d_frags, float* d_part,
-                         cudaStream_t s, const GroupPool* d_gpools) {
+                         cudaStream_t s, const GroupPool* d_gpools, bool groups_extra) {
   // function attributes are set once per device (bit = device ordinal)
   static std::atomic<uint64_t> attr_set{0};
   int dev = 0;
@@ -1219,6 +1231,7 @@ cudaError_t launch_mma_g(kv_pool* P, const void* q, int32_t hq, float scale_log2
     if (e == cudaSuccess) e = set_scan_attributes<G, false, true, false>();
     if (e == cudaSuccess) e = set_scan_attributes<G, false, false, true>();
     if (e == cudaSuccess) e = set_scan_attributes<G, true, false, true>();
+    if (e == cudaSuccess) e = set_scan_attributes<G, false, true, true>();
     if (e != cudaSuccess) return e;
     attr_set.fetch_or(uint64_t(1) << dev);
   }
@@ -1232,7 +1245,8 @@ cudaError_t launch_mma_g(kv_pool* P, const void* q, int32_t hq, float scale_log2
   // pools with INT3 or FP4 pages take the variant that reads them (grouped
   // decodes take no such pool)
   const bool i3 = P->cfg.n_int3_pages > 0 || P->cfg.n_fp4_pages > 0;
-  auto* kernel = d_gpools ? decode_mma_kernel<G, false, true, false>
+  auto* kernel = d_gpools ? (groups_extra ? decode_mma_kernel<G, false, true, true>
+                                          : decode_mma_kernel<G, false, true, false>)
                  : i3     ? (P->hdead.empty() ? decode_mma_kernel<G, false, false, true>
                                               : decode_mma_kernel<G, true, false, true>)
                           : (P->hdead.empty() ? decode_mma_kernel<G, false, false, false>
@@ -1263,13 +1277,13 @@ size_t decode_mma_frag_bytes() { return sizeof(UnitFrag); }
 cudaError_t launch_decode_mma(kv_pool* P, const void* q, int32_t hq, float scale_log2, const Unit* d_units, int n_units,
                               const Split* d_splits, const int32_t* d_wsplit, int n_workers, void* d_frags,
                               float* d_part, float* out, cudaStream_t s, const GroupPool* d_gpools,
-                              int32_t total_kv_heads) {
+                              int32_t total_kv_heads, bool groups_extra) {
   cudaError_t e;
   const int g = hq / (total_kv_heads > 0 ? total_kv_heads : P->cfg.num_kv_heads);
 #define KVQ_MMA_CASE(gg)                                                                                          \
   case gg:                                                                                                        \
     e = launch_mma_g<gg>(P, q, hq, scale_log2, d_units, n_units, d_splits, d_wsplit, n_workers, d_frags, d_part, s, \
-                         d_gpools);                                                                               \
+                         d_gpools, groups_extra);                                                                 \
     break;
   switch (g) {
     KVQ_MMA_CASE(1)

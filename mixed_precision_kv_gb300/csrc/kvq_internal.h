@@ -110,6 +110,8 @@ struct GroupPool {
   const int32_t* ntab;
   const uint32_t* hdead;   // null: no per-head exclusion in this pool
   const uint32_t* smax;    // the pool's largest INT2 K scale and largest V scale (float bits)
+  size_t int3_off, fp4_off;  // INT3 / FP4 regions
+  int64_t n3b, nfb;        // first INT3 and first FP4 id (no such pages: ids never reach them)
   int32_t hkv;
   int32_t max_pages;
   int32_t n_pools;         // entries in the array (the same in every entry)
@@ -418,11 +420,12 @@ int decode_simt_ctas_per_sm(int g);
 // per unit (the q operands its per-unit kernel builds before the scan).
 // Grouped form: d_gpools != null (device array of GroupPool) makes every
 // unit and split name its pool; total_kv_heads is then the kv heads of all
-// pools together (hq / total_kv_heads q heads per kv head).
+// pools together (hq / total_kv_heads q heads per kv head); groups_extra:
+// some pool holds INT3 or FP4 pages.
 cudaError_t launch_decode_mma(kv_pool* P, const void* q, int32_t hq, float scale_log2, const Unit* d_units, int n_units,
                               const Split* d_splits, const int32_t* d_wsplit, int n_workers, void* d_frags,
                               float* d_part, float* out, cudaStream_t s, const GroupPool* d_gpools = nullptr,
-                              int32_t total_kv_heads = 0);
+                              int32_t total_kv_heads = 0, bool groups_extra = false);
 int decode_mma_workers_per_sm(int g);
 constexpr int kMmaWarpsPerCta = 16;
 size_t decode_mma_frag_bytes();

@@ -1739,7 +1739,7 @@ void plan_decode_groups(kv_pool* const* pools, int n_pools, const int32_t* req_i
     const kv_pool* P = pools[u_pool[u]];
     const auto& tb = P->reqs[u_req[u]].table;
     const int hkv = P->cfg.num_kv_heads, h = u_head[u];
-    const int64_t n2 = P->cfg.n_int2_pages;
+    const int64_t n2 = P->cfg.n_int2_pages, n3b = first_int3(P), nfb = first_fp4(P);
     double* pb = &pre[(size_t)off[u]];
     ScanOrder so;
     so.start(0, u_npos[u], u_lead[u]);
@@ -1748,7 +1748,8 @@ void plan_decode_groups(kv_pool* const* pools, int n_pools, const int32_t* req_i
       const int32_t id = tb[so.next()];
       const uint32_t hd = P->hdead.empty() ? 0u : P->hdead[(size_t)id * hkv + h];
       const bool dead = P->fill[id] == kPage && (P->live[id] & ~hd) == 0u;
-      pb[i + 1] = pb[i] + (dead ? 0.0 : (id < n2 ? pc.int2 : pc.int4));   // grouped pools hold no INT3 pages
+      const double c = id < n2 ? pc.int2 : (id >= nfb ? pc.fp4 : (id >= n3b ? pc.int3 : pc.int4));
+      pb[i + 1] = pb[i] + (dead ? 0.0 : c);
     }
     total += pb[u_npos[u]];
     pages += u_npos[u];
@@ -1880,9 +1881,6 @@ extern "C" kv_status_t kv_decode_attn_groups(kv_pool_t* const* pools, int32_t n_
       if (pools[o] == pools[p]) return fail(KV_ERR_INVALID_ARG, "kv_decode_attn_groups: pool %d is listed twice", p);
     if (pools[p]->cfg.device != pools[0]->cfg.device)
       return fail(KV_ERR_INVALID_ARG, "kv_decode_attn_groups: the pools must be on one device");
-    if (pools[p]->cfg.n_int3_pages > 0 || pools[p]->cfg.n_fp4_pages > 0)
-      return fail(KV_ERR_INVALID_ARG,
-                  "kv_decode_attn_groups: pool %d has INT3 or FP4 pages (not read by the grouped scan)", p);
     thkv += pools[p]->cfg.num_kv_heads;
   }
   if (hq < thkv || hq % thkv != 0 || hq / thkv > 8)
@@ -1912,6 +1910,7 @@ extern "C" kv_status_t kv_decode_attn_groups(kv_pool_t* const* pools, int32_t n_
     gp[p] = GroupPool{(const uint8_t*)Q->d_pool, Q->int4_offset, (int64_t)Q->cfg.n_int2_pages,
                       (const Entry*)Q->d_table, (const int32_t*)Q->d_ntab,
                       Q->hdead.empty() ? nullptr : (const uint32_t*)Q->d_hdead, Q->d_status + 1,
+                      Q->int3_offset, Q->fp4_offset, first_int3(Q), first_fp4(Q),
                       Q->cfg.num_kv_heads, Q->cfg.max_pages_per_request, n_pools, 0};
   }
   if ((st = build_group_plan(pools, n_pools, req_ids, batch, hq, gp, s)) != KV_OK) return st;
@@ -1926,10 +1925,12 @@ extern "C" kv_status_t kv_decode_attn_groups(kv_pool_t* const* pools, int32_t n_
   if (tv) KV_CUDA(cudaEventRecord(tv[0], s));
   P->merge_event = tv ? tv[1] : nullptr;
   P->fp_pending = FpLaunch{};
+  bool extra = false;   // some pool holds INT3 or FP4 pages: the scan variant that reads them
+  for (int p = 0; p < n_pools; ++p) extra |= pools[p]->cfg.n_int3_pages > 0 || pools[p]->cfg.n_fp4_pages > 0;
   KV_CUDA(launch_decode_mma(P, q, hq, scale_log2, (const Unit*)(base + P->gplan_units_off), P->gplan_units,
                             (const Split*)(base + P->gplan_splits_off), (const int32_t*)(base + P->gplan_wsplit_off),
                             P->gplan_workers, P->frags.ptr, (float*)P->partials.ptr, out, s,
-                            (const GroupPool*)(base + P->gplan_pools_off), thkv));
+                            (const GroupPool*)(base + P->gplan_pools_off), thkv, extra));
   if (tv) {
     KV_CUDA(cudaEventRecord(tv[2], s));
     ++P->timed_calls;

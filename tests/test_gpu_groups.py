@@ -47,8 +47,14 @@ def _sizes(bits_list, chunk):
     n_req = len(bits_list)
     n2 = sum(int((b == 2).sum()) for b in bits_list) // 32 + 4
     n4 = sum(int((b == 4).sum()) for b in bits_list) // 32 + 2 * n_req + chunk // 32 + 8
-    max_tab = max(int((b == 2).sum()) // 32 + int((b == 4).sum()) // 32 + 4 for b in bits_list)
+    max_tab = max(len(b) // 32 + 8 for b in bits_list)
     return n2, n4, max_tab
+
+
+def _extra(bits_list, width):
+    """Pages for the tokens of one tail width (INT3 or FP4), 0 if none."""
+    n = sum(int((b == width).sum()) for b in bits_list)
+    return n // 32 + 2 * len(bits_list) + 4 if n else 0
 
 
 class Groups:
@@ -68,10 +74,12 @@ class Groups:
         self.stream0 = stream0
         n2, n4, max_tab = _sizes(bits_list, chunk)
         n2, n4, max_tab = n2 + extra, n4 + extra, max_tab + extra
+        n3, nf = _extra(bits_list, 3), _extra(bits_list, 0xF4)
+        n3, nf = n3 + (extra if n3 else 0), nf + (extra if nf else 0)
         n_req = len(bits_list)
-        self.gpu = [kvq.KVPool(h, n2, n4, n_req, max_tab) for h in groups]
-        self.og = [oracle.OraclePool(h, n2, n4, n_req, max_tab) for h in groups]
-        self.S = oracle.OraclePool(self.hkv, n2, n4, n_req, max_tab)
+        self.gpu = [kvq.KVPool(h, n2, n4, n_req, max_tab, n_int3_pages=n3, n_fp4_pages=nf) for h in groups]
+        self.og = [oracle.OraclePool(h, n2, n4, n_req, max_tab, n_int3_pages=n3, n_fp4_pages=nf) for h in groups]
+        self.S = oracle.OraclePool(self.hkv, n2, n4, n_req, max_tab, n_int3_pages=n3, n_fp4_pages=nf)
         self.g_ids = [[p.open() for _ in bits_list] for p in self.gpu]
         self.o_ids = [[p.open() for _ in bits_list] for p in self.og]
         self.s_ids = [self.S.open() for _ in bits_list]
@@ -264,6 +272,30 @@ def test_grouped_decode_matches_shared_pool(kvq, groups, hq, keep):
     sc.sync()
     sc.check_tables(content=False)
     sc.decode(9, f"groups={groups} after 40 appends")
+
+
+@pytest.mark.parametrize("groups,hq", [([2, 2], 8), ([1, 2, 1], 32)])
+def test_grouped_decode_with_int3_and_fp4_pages(kvq, groups, hq):
+    """Group pools holding INT2, INT3, INT4 and FP4 pages (the grouped scan's
+    variant that reads them), budgets per group, a drop, then decode steps."""
+    rng = np.random.default_rng(len(groups))
+    widths = np.array([2, 3, 4, 0xF4], np.uint8)
+    bits = [rng.choice(widths, n, p=[0.4, 0.2, 0.2, 0.2]) for n in (520, 333, 900)]
+    sc = Groups(kvq, groups, hq, bits, stream0=30, extra=12)
+    keep = [1.0, 0.5, 0.3][:len(groups)]
+    for r, n in enumerate(sc.n_tok):
+        for j, kf in enumerate(keep):
+            sc.leave_out(j, r, np.arange(n - int(round(kf * n))))
+    sc.reorder()
+    sc.drop()
+    sc.sync()
+    sc.check_tables()
+    sc.decode(0, f"four widths groups={groups}")
+    for step in range(1, 4):
+        for r in range(len(bits)):
+            sc.append(r, rng.choice(widths, 1))
+        sc.sync()
+        sc.decode(step, f"four widths groups={groups} step {step}")
 
 
 def test_grouped_decode_stats_count_only_pages_read(kvq):

@@ -195,7 +195,8 @@ def test_larger_mixed_workload_sampled(kvq):
 
 def test_int3_errors(kvq):
     """Width 3 in a pool without INT3 pages is out of pages; width 5 is
-    invalid; the grouped decode takes no pool with INT3 pages."""
+    invalid.  A grouped decode over a pool with INT3 pages and one without
+    gives each pool's own decode."""
     gpu = kvq.KVPool(1, 4, 4, 1, 8)
     r = gpu.open()
     k = _dev(kvsynth.fill_bf16_host(1, 1, 128, SEED, kvsynth.TENSOR_K, 0))
@@ -212,8 +213,13 @@ def test_int3_errors(kvq):
     a.append(k, k, [ra], [3])
     b.append(k, k, [rb], [4])
     q = _dev(kvsynth.fill_bf16_host(1, 2, 128, SEED, kvsynth.TENSOR_Q, 0))
-    with pytest.raises(kvq.KVError):
-        kvq.KVPool.decode_groups([a, b], q, np.array([[ra], [rb]], np.int32), SCALE)
+    out = kvq.KVPool.decode_groups([a, b], q, np.array([[ra], [rb]], np.int32), SCALE)
+    oa = a.decode(q[:, :1].contiguous(), [ra], SCALE)
+    ob = b.decode(q[:, 1:].contiguous(), [rb], SCALE)
+    a.sync()
+    got = out.cpu().numpy()
+    assert_outputs_close(got[:, :1], oa.cpu().numpy(), "grouped INT3 pool")
+    assert_outputs_close(got[:, 1:], ob.cpu().numpy(), "grouped INT4 pool")
 
 
 def test_config2_full_size_three_width_allocation(kvq):
