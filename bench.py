@@ -294,8 +294,9 @@ def int2_fraction(gw):
 
 
 def run_prefill(args):
-    """Prefill of the workload's prompts (16K-token append calls), inputs
-    resident in HBM: bf16 K and V rows read, page blocks written."""
+    """Prefill of the workload's prompts (append calls of --chunk tokens of one
+    request, 16K by default), inputs resident in HBM: bf16 K and V rows read,
+    page blocks written."""
     import torch
     import kvsynth
     from mixed_precision_kv_gb300.workload import GPUWorkload
@@ -303,7 +304,7 @@ def run_prefill(args):
     torch.cuda.set_device(local)
     w = kvsynth.make_workload(args.config)
     H = w.num_kv_heads
-    chunk = 16384
+    chunk = args.chunk
     times = []
     for rep_i in range(args.warmup + args.steps):
         gw = GPUWorkload(w, device=local, chunk=chunk)
@@ -569,6 +570,8 @@ def main():
     ap.add_argument("--alloc3", action="store_true",
                     help="allocate INT2/INT3/INT4 with the three-width greedy over the same budget (D(3) from "
                          "the input recipe)")
+    ap.add_argument("--chunk", type=int, default=16384,
+                    help="--mode prefill: tokens per kv_append_quant call (one request per call)")
     ap.add_argument("--mode", default="decode", choices=["decode", "prefill"],
                     help="decode: the decode-step line (default); prefill: bulk quantization of the workload's "
                          "prompts through kv_append_quant")
