@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <memory>
+#include <new>
 #include <string>
 #include <utility>
 #include <vector>
@@ -194,11 +196,33 @@ struct HostPlan {
   int64_t n_ctas() const { return (int64_t)cta_split.size() - 1; }   // workers
 };
 
+// An allocator whose value-initialisation leaves a trivial element
+// unwritten: resize() then grows a map without first storing zeros into
+// entries that the caller writes right after.
+template <class T>
+struct NoFillAlloc : std::allocator<T> {
+  template <class U>
+  struct rebind {
+    using other = NoFillAlloc<U>;
+  };
+  NoFillAlloc() = default;
+  template <class U>
+  NoFillAlloc(const NoFillAlloc<U>&) noexcept {}
+  template <class U>
+  void construct(U* p) noexcept {
+    ::new ((void*)p) U;
+  }
+  template <class U, class... A>
+  void construct(U* p, A&&... a) {
+    ::new ((void*)p) U(std::forward<A>(a)...);
+  }
+};
+
 struct Request {
   bool open = false;
   std::vector<int32_t> table;       // page ids in table order
   int32_t tail4 = -1, tail3 = -1, tailf = -1, staging = -1;
-  std::vector<uint32_t> loc;        // token position -> page_id << 5 | slot
+  std::vector<uint32_t, NoFillAlloc<uint32_t>> loc;   // token position -> page_id << 5 | slot
   uint64_t version = 0;             // bumped whenever the table's entries change
   uint64_t ordered_version = ~0ull; // version at which the table was last seen INT2-first
   uint64_t shape = 0;               // pool clock at the last open, erase or reorder of entries (not appends)

@@ -679,10 +679,11 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
   // then one partial staging page.  Page ids are taken in the same token
   // order as the per-token loop takes them, so both paths give the same pool.
   bool bulk = n_tok >= kPage;
-  std::vector<int32_t>& i4 = P->scr_i4;       // the call's INT4 / INT2 token indices, in order
+  // the call's INT4 / INT2 token indices, in order: the first n4 / n2
+  // entries of scratch lists that only grow (no per-call clearing or filling)
+  std::vector<int32_t>& i4 = P->scr_i4;
   std::vector<int32_t>& i2 = P->scr_i2;
-  i4.clear();
-  i2.clear();
+  int64_t n4 = 0, n2 = 0;
   int64_t b_cap4 = 0, b_new4 = 0, b_e = 0, b_ndirect = 0, b_rem = 0;
   int b_f4 = 0, b_s0 = 0;
   bool b_repack = false;
@@ -690,8 +691,8 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
   if (bulk) {
     // one pass: same request throughout, bits valid; raw pointers and local
     // counts (stores through vectors next to uint8_t loads defeat registers)
-    i4.resize((size_t)n_tok);
-    i2.resize((size_t)n_tok);
+    if (i4.size() < (size_t)n_tok) i4.resize((size_t)n_tok);
+    if (i2.size() < (size_t)n_tok) i2.resize((size_t)n_tok);
     int32_t* p4 = i4.data();
     int32_t* p2 = i2.data();
     const int32_t r0 = req_ids[0];
@@ -707,13 +708,12 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
     }
     // invalid input: the per-token path reports the error (and any earlier one)
     bulk = ok;
-    i4.resize((size_t)c4);
-    i2.resize((size_t)c2);
+    n4 = c4;
+    n2 = c2;
   }
   if (bulk) {
     const int32_t r = req_ids[0];
     const Request& R = P->reqs[r];
-    const int64_t n4 = (int64_t)i4.size(), n2 = (int64_t)i2.size();
     const bool tail_open = R.tail4 >= 0 && P->fill[R.tail4] < kPage;
     b_f4 = tail_open ? (int)P->fill[R.tail4] : 0;
     b_cap4 = tail_open ? std::min<int64_t>(n4, kPage - b_f4) : 0;
@@ -795,36 +795,36 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
   std::vector<int32_t> deferred;
   Dirty dirty;   // table rewrites the append kernel does not cover (repacks)
   std::vector<TableUpd> hupd;   // per-head exclusion words carried by repacks / cleared by frees
+  int64_t bulk_job_toks = 0;    // bulk path: tokens of the append jobs
   if (bulk) {
     const int32_t r = req_ids[0];
     Request& R = P->reqs[r];
-    const int64_t n4 = (int64_t)i4.size(), n2 = (int64_t)i2.size();
     const int64_t T0 = (int64_t)R.loc.size();
-    R.loc.resize((size_t)(T0 + n_tok));
+    R.loc.resize((size_t)(T0 + n_tok));   // every new entry is written below
     auto put = [&](int32_t page, int slot, int32_t t) {
       P->pos[(size_t)page * kPage + slot] = (int32_t)(T0 + t);
       R.loc[(size_t)(T0 + t)] = ((uint32_t)page << 5) | (uint32_t)slot;
     };
     auto slots = [](int first, int64_t n) { return (uint32_t)((n >= kPage ? 0xFFFFFFFFull : ((1ull << n) - 1)) << first); };
-    // an append job over tokens idx[a .. a+n) into slots first .. of page
-    toks.resize((size_t)n_tok);   // at most every token; trimmed below
-    size_t ntoks = 0;
+    // An append job over tokens idx[a .. a+n) into slots first .. of page.
+    // Its tok_off indexes the two lists as if the INT2 list followed the n4
+    // INT4 entries; the upload below places the lists and adjusts the
+    // offsets into the INT2 list.
     int32_t* const pos = P->pos.data();
     uint32_t* const loc = R.loc.data();
     auto add_job = [&](int32_t page, int first, const std::vector<int32_t>& idx, int64_t a, int64_t n) {
-      jobs.push_back(AppendJob{page, first, (int32_t)n, (int32_t)ntoks, -1, 0u, -1, 0});
+      const int64_t off = (&idx == &i4 ? 0 : n4) + a;
+      jobs.push_back(AppendJob{page, first, (int32_t)n, (int32_t)off, -1, 0u, -1, 0});
       job_req.push_back(r);
       const int32_t* src = idx.data() + a;
-      int32_t* dst = toks.data() + ntoks;
       int32_t* pp = pos + (size_t)page * kPage + first;
       const uint32_t base = ((uint32_t)page << 5) | (uint32_t)first;
       for (int64_t q = 0; q < n; ++q) {
         const int32_t t = src[q];
-        dst[q] = t;
         pp[q] = (int32_t)(T0 + t);
         loc[T0 + t] = base + (uint32_t)q;
       }
-      ntoks += (size_t)n;
+      bulk_job_toks += n;
       P->fill[page] = (uint8_t)(first + n);
       P->live[page] |= slots(first, n);
     };
@@ -883,11 +883,7 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
     for (int64_t g = 0; g < b_ndirect; ++g) {
       const int64_t a = b_e + kPage * g;
       const int32_t sg = idS[(size_t)g], nid = idD[(size_t)g];
-      for (int sl = 0; sl < kPage; ++sl) {
-        const int32_t t = i2[(size_t)(a + sl)];
-        P->pos[(size_t)sg * kPage + sl] = (int32_t)(T0 + t);
-        put(nid, sl, t);
-      }
+      for (int sl = 0; sl < kPage; ++sl) put(nid, sl, i2[(size_t)(a + sl)]);
       P->fill[sg] = kPage;
       P->live[sg] = 0xFFFFFFFFu;
       P->fill[nid] = kPage;
@@ -907,7 +903,6 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
       app.emplace_back(i2[(size_t)a], sp);
       R.staging = sp;
     }
-    toks.resize(ntoks);
     std::sort(app.begin(), app.end());
     for (const auto& x : app) R.table.push_back(x.second);
     if (!app.empty() || b_repack) ++R.version;
@@ -998,7 +993,7 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
     toks[(size_t)(j.tok_off + (tok_slot[t] - j.first_slot))] = (int32_t)t;
   }
   }   // per-token path
-  const int32_t off = (int32_t)toks.size();
+  const int64_t off = bulk ? bulk_job_toks : (int64_t)toks.size();
   for (int32_t id : deferred) {
     P->fill[id] = 0;
     P->live[id] = 0;
@@ -1071,13 +1066,34 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
     std::stable_partition(jobs.begin(), jobs4_end, [](const AppendJob& j) { return !(j.first_slot == 0 && j.n_slots == kPage); });
     for (auto it = jobs.begin(); it != jobs4_end; ++it) n_full += (it->first_slot == 0 && it->n_slots == kPage) ? 1 : 0;
   }
+  if (bulk && small) {
+    // the small launch carries its token lists by value: gather each job's tokens
+    toks.clear();
+    for (auto& j : jobs) {
+      const int32_t* src = j.tok_off < n4 ? i4.data() + j.tok_off : i2.data() + (j.tok_off - n4);
+      j.tok_off = (int32_t)toks.size();
+      toks.insert(toks.end(), src, src + j.n_slots);
+    }
+  }
   Upload u;
   const size_t o_jobs = small ? 0 : u.add(jobs.data(), jobs.size() * sizeof(AppendJob));
-  const size_t o_toks = small ? 0 : u.add(toks.data(), toks.size() * sizeof(int32_t));
+  size_t o_toks = 0, o_dtok = 0;
+  if (bulk) {
+    // the call's INT4 and INT2 token lists as they are: the append jobs index
+    // both, the direct INT2 jobs the INT2 list
+    o_toks = small ? 0 : u.add(i4.data(), (size_t)n4 * sizeof(int32_t));
+    o_dtok = u.add(i2.data(), (size_t)n2 * sizeof(int32_t));
+    if (!small) {
+      const int64_t shift = (int64_t)(o_dtok - o_toks) / (int64_t)sizeof(int32_t) - n4;
+      for (auto& j : jobs)
+        if (j.tok_off >= n4) j.tok_off = (int32_t)(j.tok_off + shift);
+    }
+  } else {
+    o_toks = small ? 0 : u.add(toks.data(), toks.size() * sizeof(int32_t));
+    o_dtok = u.add(dtoks.data(), dtoks.size() * sizeof(int32_t));
+  }
   const size_t o_rep = u.add(repacks.data(), repacks.size() * sizeof(RepackJob));
   const size_t o_dir = u.add(directs.data(), directs.size() * sizeof(DirectJob));
-  const std::vector<int32_t>& dtok_list = bulk ? i2 : dtoks;   // the bulk path indexes the INT2 token list
-  const size_t o_dtok = u.add(dtok_list.data(), (directs.empty() ? 0 : dtok_list.size()) * sizeof(int32_t));
   const size_t o_upd = u.add(upd.data(), upd.size() * sizeof(TableUpd));
   if ((st = upload(P, u, s)) != KV_OK) return st;
   uint8_t* base = (uint8_t*)P->upload.ptr;
