@@ -2,8 +2,8 @@
 
 Small instances are compared in full (every code, scale/zero, table entry and
 output).  Full-size instances are compared on every request's page table
-(bit-exact) and on sampled (request, kv head) units whose codes and outputs
-the oracle computes one by one.
+(bit-exact) and on whole requests, all kv heads, whose codes and outputs the
+oracle computes (workload 2: every request).
 """
 import numpy as np
 import pytest
@@ -113,20 +113,23 @@ def test_config5_loop_small(kvq):
     assert repacks > 32
 
 
-def _sampled(w, rng, n_units):
+def _sampled(w, rng, n_units, n_heads=2):
     """Sample (request, kv head) units; return the sampled requests, heads and (b, q head) pairs."""
     reqs = sorted(set(rng.choice(len(w.requests), n_units, replace=False).tolist()))
-    heads = sorted(set(rng.choice(w.num_kv_heads, 2, replace=False).tolist()))
+    heads = sorted(set(rng.choice(w.num_kv_heads, n_heads, replace=False).tolist()))
     g = w.g
     pairs = [(b, h * g + j) for b in reqs for h in heads for j in range(g)]
     return reqs, heads, pairs
 
 
-@pytest.mark.parametrize("cfg", [2, 3])
-def test_configs_full_size_sampled(kvq, cfg):
+@pytest.mark.parametrize("cfg,n_req", [(2, 8), (3, 4)])
+def test_configs_full_size_sampled(kvq, cfg, n_req):
+    """Every table; codes, scale/zero and outputs of n_req requests with all
+    their kv heads: config 2 every output (8 x 32 q heads), config 3 256 of
+    the 1024 (request, q head) outputs."""
     w = kvsynth.make_workload(cfg)
     rng = np.random.default_rng(cfg)
-    reqs, heads, pairs = _sampled(w, rng, 1)
+    reqs, heads, pairs = _sampled(w, rng, n_req, n_heads=w.num_kv_heads)
     gw, ow = _pair(w, chunk=16384, sel_heads=heads, content_reqs=reqs)
     _build(gw, ow)
     _check_all(gw, ow, content=False)                 # every table, bit-exact
@@ -139,12 +142,15 @@ def test_configs_full_size_sampled(kvq, cfg):
 
 
 def test_config4_full_size_sampled(kvq):
+    """Every table; codes, scale/zero and outputs of the shortest, the longest
+    and six seeded requests, with all their kv heads."""
     w = kvsynth.make_workload(4)
     rng = np.random.default_rng(44)
-    # one short and one long request
     lens = np.array([r.n_prefill for r in w.requests])
-    reqs = sorted({int(np.argmin(lens)), int(np.argmax(lens))})
-    heads = [1, 6]
+    ends = {int(np.argmin(lens)), int(np.argmax(lens))}
+    rest = [b for b in range(len(w.requests)) if b not in ends]
+    reqs = sorted(ends | set(rng.choice(rest, 6, replace=False).tolist()))
+    heads = list(range(w.num_kv_heads))
     pairs = [(b, h * w.g + j) for b in reqs for h in heads for j in range(w.g)]
     gw, ow = _pair(w, chunk=16384, sel_heads=heads, content_reqs=reqs)
     _build(gw, ow)
@@ -154,7 +160,6 @@ def test_config4_full_size_sampled(kvq):
     ref = ow.decode(ow.q(0), pairs=np.array(pairs, np.int32))
     got = np.stack([out[b, h] for b, h in pairs])
     assert_outputs_close(got, ref, "config 4 full size, sampled")
-    assert rng is not None
 
 
 def test_config2_full_size_segments_and_budgets(kvq):
@@ -211,13 +216,14 @@ def test_config5_full_size_every_step(kvq):
     precision, fill, live masks) bit-exact against the oracle, which keeps
     codes only for the sampled requests and kv heads.  At steps 0, 31 and 63,
     at the first step after a repack in a sampled request, and every 8th step:
-    codes and binary16 scale/zero of 4 sampled requests x 2 kv heads, and
-    their outputs within max-abs 1e-3 / relative-L2 1e-4 of the fp64 oracle."""
+    codes and binary16 scale/zero of 8 sampled requests with all their kv
+    heads, and their outputs within max-abs 1e-3 / relative-L2 1e-4 of the
+    fp64 oracle."""
     w = kvsynth.make_workload(5)
     assert len(w.requests) == 256 and w.steps == 64
     rng = np.random.default_rng(55)
-    # two requests whose staging page fills during the 64 steps (INT2 tokens
-    # wait in it, 32 at a time), two drawn at random
+    # four requests whose staging page fills during the 64 steps (INT2 tokens
+    # wait in it, 32 at a time), four drawn at random
     from harness import oracle_bits
     fills = []
     for r, spec in enumerate(w.requests):
@@ -225,10 +231,10 @@ def test_config5_full_size_every_step(kvq):
         n = spec.n_prefill
         fills.append(int((b[:n] == 2).sum()) % 32 + int((b[n:n + w.steps] == 2).sum()) >= 32)
     repacking = [r for r in range(len(w.requests)) if fills[r]]
-    reqs = rng.choice(repacking, 2, replace=False).tolist()
+    reqs = rng.choice(repacking, 4, replace=False).tolist()
     rest = [r for r in range(len(w.requests)) if r not in reqs]
-    reqs = sorted(reqs + rng.choice(rest, 2, replace=False).tolist())
-    heads = sorted(rng.choice(w.num_kv_heads, 2, replace=False).tolist())
+    reqs = sorted(reqs + rng.choice(rest, 4, replace=False).tolist())
+    heads = list(range(w.num_kv_heads))
     pairs = np.array([(b, h * w.g + j) for b in reqs for h in heads for j in range(w.g)], np.int32)
     gw, ow = _pair(w, chunk=16384, sel_heads=heads, content_reqs=reqs)
     _build(gw, ow)
