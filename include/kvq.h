@@ -126,7 +126,10 @@ KVQ_API kv_status_t kv_request_close(kv_pool_t* pool, int32_t req_id);
  *            tokens; that INT2 page is appended to the request's table.
  * Page ids are the lowest free ids of their class; staging pages freed by a
  * repack become reusable after the call.  Values are checked on the device:
- * NaN, Inf or |x| > 65504 make kv_pool_sync() return KV_ERR_RANGE. */
+ * NaN, Inf or |x| > 65504 make kv_pool_sync() return KV_ERR_RANGE.  A request
+ * holds at most 2^31 - 1 token positions: a call that would pass it returns
+ * KV_ERR_INVALID_ARG with nothing changed; running out of pages or of the
+ * request's table entries returns KV_ERR_OOM, also with nothing changed. */
 KVQ_API kv_status_t kv_append_quant(kv_pool_t* pool, const void* k, const void* v, const int32_t* req_ids,
                             const uint8_t* bits, int64_t n_tok, void* stream);
 

@@ -196,6 +196,10 @@ struct HostPlan {
   int64_t n_ctas() const { return (int64_t)cta_split.size() - 1; }   // workers
 };
 
+// Token positions of one request are int32 in the position maps: a request
+// holds at most this many (appends past it are rejected before any change).
+constexpr int64_t kMaxPositions = INT32_MAX;
+
 // An allocator whose value-initialisation leaves a trivial element
 // unwritten: resize() then grows a map without first storing zeros into
 // entries that the caller writes right after.

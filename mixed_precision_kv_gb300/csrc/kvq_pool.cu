@@ -641,6 +641,7 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
     // dry-run state
     bool tail; int tailfill; bool tail3; int tail3fill; bool tailf; int tailffill; bool stag; int stagfill;
     int64_t tablen;
+    int64_t npos;          // the request's token positions after the call
   };
   std::vector<CallReq> cr;
   if (P->call_slot.size() != (size_t)P->cfg.max_requests) P->call_slot.assign((size_t)P->cfg.max_requests, -1);
@@ -662,6 +663,7 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
       c.stag = R.staging >= 0;
       c.stagfill = c.stag ? (int)P->fill[R.staging] : 0;
       c.tablen = (int64_t)R.table.size();
+      c.npos = (int64_t)R.loc.size();
       cr.push_back(c);
     }
     return cr[(size_t)sl];
@@ -727,6 +729,9 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
     const int64_t need4 = opens, need2 = b_ndirect + (b_repack ? 1 : 0);
     if ((int64_t)R.table.size() + opens > P->cfg.max_pages_per_request)
       return fail(KV_ERR_OOM, "kv_append_quant: request %d would exceed %d table entries", r, P->cfg.max_pages_per_request);
+    if ((int64_t)R.loc.size() + n_tok > kMaxPositions)
+      return fail(KV_ERR_INVALID_ARG, "kv_append_quant: request %d would exceed %lld token positions", r,
+                  (long long)kMaxPositions);
     if (need4 > (int64_t)P->free4.size() || need2 > (int64_t)P->free2.size())
       return fail(KV_ERR_OOM, "kv_append_quant: needs %lld INT4 + %lld INT2 pages, %zu + %zu free", (long long)need4,
                   (long long)need2, P->free4.size(), P->free2.size());
@@ -758,6 +763,9 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
       }
       if (c.tablen > P->cfg.max_pages_per_request)
         return fail(KV_ERR_OOM, "kv_append_quant: request %d would exceed %d table entries", req_ids[t], P->cfg.max_pages_per_request);
+      if (++c.npos > kMaxPositions)
+        return fail(KV_ERR_INVALID_ARG, "kv_append_quant: request %d would exceed %lld token positions", req_ids[t],
+                    (long long)kMaxPositions);
     }
     if (need4 > (int64_t)P->free4.size() || need2 > (int64_t)P->free2.size())
       return fail(KV_ERR_OOM, "kv_append_quant: needs %lld INT4 + %lld INT2 pages, %zu + %zu free", (long long)need4,
