@@ -674,68 +674,100 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
     ~ResetSlots() { for (const auto& c : *cr) P->call_slot[(size_t)c.r] = -1; }
   } reset_slots{P, &cr};
 
-  // Bulk path: every token of the call belongs to one request (a prefill
-  // chunk).  The per-token rules below then reduce to whole runs: INT4 tokens
-  // fill the tail page and new pages of 32; INT2 tokens fill the open staging
-  // page, then groups of 32 that complete within the call (direct INT2 jobs),
-  // then one partial staging page.  Page ids are taken in the same token
-  // order as the per-token loop takes them, so both paths give the same pool.
+  // Bulk path: the call's tokens come in runs, one per request (a prefill
+  // chunk of one request, or one chunk of each of several requests): every
+  // run at least one page of tokens, no request in two runs.  Within a run
+  // the per-token rules reduce to whole groups: INT4 tokens fill the tail
+  // page and new pages of 32; INT2 tokens fill the open staging page, then
+  // groups of 32 that complete within the call (direct INT2 jobs), then one
+  // partial staging page.  Runs are routed in call order, and page ids are
+  // taken in the same token order as the per-token loop takes them, so both
+  // paths give the same pool.
+  struct BulkRun {
+    int32_t r;
+    int64_t t0, n;            // the call's tokens [t0, t0 + n)
+    int64_t o4, n4, o2, n2;   // its entries in the call's INT4 / INT2 lists
+    // routing, from the request's state before the call
+    int64_t cap4, new4, e, ndirect, rem;
+    int f4, s0;
+    bool repack;
+  };
+  std::vector<BulkRun> runs;
   bool bulk = n_tok >= kPage;
   // the call's INT4 / INT2 token indices, in order: the first n4 / n2
   // entries of scratch lists that only grow (no per-call clearing or filling)
   std::vector<int32_t>& i4 = P->scr_i4;
   std::vector<int32_t>& i2 = P->scr_i2;
   int64_t n4 = 0, n2 = 0;
-  int64_t b_cap4 = 0, b_new4 = 0, b_e = 0, b_ndirect = 0, b_rem = 0;
-  int b_f4 = 0, b_s0 = 0;
-  bool b_repack = false;
-  if (bulk && !req_ok(P, req_ids[0])) bulk = false;   // the per-token path reports the error
   if (bulk) {
-    // one pass: same request throughout, bits valid; raw pointers and local
-    // counts (stores through vectors next to uint8_t loads defeat registers)
+    // one pass: bits valid, run boundaries; raw pointers and local counts
+    // (stores through vectors next to uint8_t loads defeat registers)
     if (i4.size() < (size_t)n_tok) i4.resize((size_t)n_tok);
     if (i2.size() < (size_t)n_tok) i2.resize((size_t)n_tok);
     int32_t* p4 = i4.data();
     int32_t* p2 = i2.data();
-    const int32_t r0 = req_ids[0];
-    int64_t c4 = 0, c2 = 0;
+    int64_t c4 = 0, c2 = 0, tb = 0, b4 = 0, b2 = 0;
+    int32_t rp = req_ids[0];
     bool ok = true;
+    auto close_run = [&](int64_t t) {
+      runs.push_back(BulkRun{rp, tb, t - tb, b4, c4 - b4, b2, c2 - b2, 0, 0, 0, 0, 0, 0, 0, false});
+    };
     for (int64_t t = 0; t < n_tok; ++t) {
       const uint32_t b = bits[t];
-      ok &= (req_ids[t] == r0) & ((b == 2u) | (b == 4u));
+      const int32_t rt = req_ids[t];
+      if (rt != rp) {
+        close_run(t);
+        rp = rt;
+        tb = t;
+        b4 = c4;
+        b2 = c2;
+      }
+      ok &= (b == 2u) | (b == 4u);
       p4[c4] = (int32_t)t;
       p2[c2] = (int32_t)t;
       c4 += b == 4u;
       c2 += b != 4u;
     }
-    // invalid input: the per-token path reports the error (and any earlier one)
+    close_run(n_tok);
+    // each run an open request of its own, at least a page of tokens long
+    // (anything else: the per-token path, which also reports any error)
+    for (const auto& u : runs) {
+      if (!ok || u.n < kPage || !req_ok(P, u.r) || P->call_slot[(size_t)u.r] >= 0) {
+        ok = false;
+        break;
+      }
+      slot_of(u.r);
+    }
     bulk = ok;
     n4 = c4;
     n2 = c2;
   }
   if (bulk) {
-    const int32_t r = req_ids[0];
-    const Request& R = P->reqs[r];
-    const bool tail_open = R.tail4 >= 0 && P->fill[R.tail4] < kPage;
-    b_f4 = tail_open ? (int)P->fill[R.tail4] : 0;
-    b_cap4 = tail_open ? std::min<int64_t>(n4, kPage - b_f4) : 0;
-    b_new4 = (n4 - b_cap4 + kPage - 1) / kPage;
-    b_s0 = R.staging >= 0 ? (int)P->fill[R.staging] : 0;
-    b_e = R.staging >= 0 ? std::min<int64_t>(n2, kPage - b_s0) : 0;
-    b_repack = R.staging >= 0 && b_s0 + b_e == kPage;
-    b_ndirect = (n2 - b_e) / kPage;
-    b_rem = (n2 - b_e) % kPage;
-    const int64_t opens = b_new4 + b_ndirect + (b_rem > 0 ? 1 : 0);
-    const int64_t need4 = opens, need2 = b_ndirect + (b_repack ? 1 : 0);
-    if ((int64_t)R.table.size() + opens > P->cfg.max_pages_per_request)
-      return fail(KV_ERR_OOM, "kv_append_quant: request %d would exceed %d table entries", r, P->cfg.max_pages_per_request);
-    if ((int64_t)R.loc.size() + n_tok > kMaxPositions)
-      return fail(KV_ERR_INVALID_ARG, "kv_append_quant: request %d would exceed %lld token positions", r,
-                  (long long)kMaxPositions);
+    int64_t need4 = 0, need2 = 0;
+    for (auto& u : runs) {
+      const Request& R = P->reqs[u.r];
+      const bool tail_open = R.tail4 >= 0 && P->fill[R.tail4] < kPage;
+      u.f4 = tail_open ? (int)P->fill[R.tail4] : 0;
+      u.cap4 = tail_open ? std::min<int64_t>(u.n4, kPage - u.f4) : 0;
+      u.new4 = (u.n4 - u.cap4 + kPage - 1) / kPage;
+      u.s0 = R.staging >= 0 ? (int)P->fill[R.staging] : 0;
+      u.e = R.staging >= 0 ? std::min<int64_t>(u.n2, kPage - u.s0) : 0;
+      u.repack = R.staging >= 0 && u.s0 + u.e == kPage;
+      u.ndirect = (u.n2 - u.e) / kPage;
+      u.rem = (u.n2 - u.e) % kPage;
+      const int64_t opens = u.new4 + u.ndirect + (u.rem > 0 ? 1 : 0);
+      need4 += opens;
+      need2 += u.ndirect + (u.repack ? 1 : 0);
+      if ((int64_t)R.table.size() + opens > P->cfg.max_pages_per_request)
+        return fail(KV_ERR_OOM, "kv_append_quant: request %d would exceed %d table entries", u.r,
+                    P->cfg.max_pages_per_request);
+      if ((int64_t)R.loc.size() + u.n > kMaxPositions)
+        return fail(KV_ERR_INVALID_ARG, "kv_append_quant: request %d would exceed %lld token positions", u.r,
+                    (long long)kMaxPositions);
+    }
     if (need4 > (int64_t)P->free4.size() || need2 > (int64_t)P->free2.size())
       return fail(KV_ERR_OOM, "kv_append_quant: needs %lld INT4 + %lld INT2 pages, %zu + %zu free", (long long)need4,
                   (long long)need2, P->free4.size(), P->free2.size());
-    slot_of(r);
   }
   // Dry run: pages taken and table growth, so that OOM changes nothing.
   if (!bulk) {
@@ -805,32 +837,36 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
   std::vector<TableUpd> hupd;   // per-head exclusion words carried by repacks / cleared by frees
   int64_t bulk_job_toks = 0;    // bulk path: tokens of the append jobs
   if (bulk) {
-    const int32_t r = req_ids[0];
+  for (const BulkRun& u : runs) {
+    const int32_t r = u.r;
     Request& R = P->reqs[r];
+    const int32_t* const l4 = i4.data() + u.o4;   // the run's INT4 / INT2 tokens (call indices)
+    const int32_t* const l2 = i2.data() + u.o2;
     const int64_t T0 = (int64_t)R.loc.size();
-    R.loc.resize((size_t)(T0 + n_tok));   // every new entry is written below
+    const int64_t P0 = T0 - u.t0;                 // the request's position of call token t: P0 + t
+    R.loc.resize((size_t)(T0 + u.n));   // every new entry is written below
     auto put = [&](int32_t page, int slot, int32_t t) {
-      P->pos[(size_t)page * kPage + slot] = (int32_t)(T0 + t);
-      R.loc[(size_t)(T0 + t)] = ((uint32_t)page << 5) | (uint32_t)slot;
+      P->pos[(size_t)page * kPage + slot] = (int32_t)(P0 + t);
+      R.loc[(size_t)(P0 + t)] = ((uint32_t)page << 5) | (uint32_t)slot;
     };
     auto slots = [](int first, int64_t n) { return (uint32_t)((n >= kPage ? 0xFFFFFFFFull : ((1ull << n) - 1)) << first); };
-    // An append job over tokens idx[a .. a+n) into slots first .. of page.
-    // Its tok_off indexes the two lists as if the INT2 list followed the n4
-    // INT4 entries; the upload below places the lists and adjusts the
-    // offsets into the INT2 list.
+    // An append job over the run's INT4 (int4_list) or INT2 tokens
+    // [a, a + n) into slots first .. of page.  Its tok_off indexes the call's
+    // two lists as if the INT2 list followed the n4 INT4 entries; the upload
+    // below places the lists and adjusts the offsets into the INT2 list.
     int32_t* const pos = P->pos.data();
     uint32_t* const loc = R.loc.data();
-    auto add_job = [&](int32_t page, int first, const std::vector<int32_t>& idx, int64_t a, int64_t n) {
-      const int64_t off = (&idx == &i4 ? 0 : n4) + a;
+    auto add_job = [&](int32_t page, int first, bool int4_list, int64_t a, int64_t n) {
+      const int64_t off = (int4_list ? u.o4 : n4 + u.o2) + a;
       jobs.push_back(AppendJob{page, first, (int32_t)n, (int32_t)off, -1, 0u, -1, 0});
       job_req.push_back(r);
-      const int32_t* src = idx.data() + a;
+      const int32_t* src = (int4_list ? l4 : l2) + a;
       int32_t* pp = pos + (size_t)page * kPage + first;
       const uint32_t base = ((uint32_t)page << 5) | (uint32_t)first;
       for (int64_t q = 0; q < n; ++q) {
         const int32_t t = src[q];
-        pp[q] = (int32_t)(T0 + t);
-        loc[T0 + t] = base + (uint32_t)q;
+        pp[q] = (int32_t)(P0 + t);
+        loc[P0 + t] = base + (uint32_t)q;
       }
       bulk_job_toks += n;
       P->fill[page] = (uint8_t)(first + n);
@@ -838,35 +874,35 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
     };
     // INT4 pages and staging pages take ids in the token order of their
     // first token; INT2 pages in the order their groups complete
-    std::vector<int32_t> id4((size_t)b_new4), idS((size_t)(b_ndirect + (b_rem > 0 ? 1 : 0)));
+    std::vector<int32_t> id4((size_t)u.new4), idS((size_t)(u.ndirect + (u.rem > 0 ? 1 : 0)));
     {
       size_t a = 0, b = 0;
       while (a < id4.size() || b < idS.size()) {
-        const int32_t ta = a < id4.size() ? i4[(size_t)(b_cap4 + kPage * (int64_t)a)] : INT32_MAX;
-        const int32_t tb = b < idS.size() ? i2[(size_t)(b_e + kPage * (int64_t)b)] : INT32_MAX;
+        const int32_t ta = a < id4.size() ? l4[(size_t)(u.cap4 + kPage * (int64_t)a)] : INT32_MAX;
+        const int32_t tb = b < idS.size() ? l2[(size_t)(u.e + kPage * (int64_t)b)] : INT32_MAX;
         if (ta < tb) id4[a++] = P->free4.take_lowest();
         else idS[b++] = P->free4.take_lowest();
       }
     }
-    const int32_t nid_rep = b_repack ? P->free2.take_lowest() : -1;
-    std::vector<int32_t> idD((size_t)b_ndirect);
+    const int32_t nid_rep = u.repack ? P->free2.take_lowest() : -1;
+    std::vector<int32_t> idD((size_t)u.ndirect);
     for (auto& x : idD) x = P->free2.take_lowest();
     // table entries appended in this call, with the token that appends them
     std::vector<std::pair<int32_t, int32_t>> app;   // (token, page id)
     // INT4: the open tail page, then new pages
-    if (b_cap4 > 0) add_job(R.tail4, b_f4, i4, 0, b_cap4);
-    for (int64_t q = 0; q < b_new4; ++q) {
-      const int64_t a = b_cap4 + kPage * q;
+    if (u.cap4 > 0) add_job(R.tail4, u.f4, true, 0, u.cap4);
+    for (int64_t q = 0; q < u.new4; ++q) {
+      const int64_t a = u.cap4 + kPage * q;
       const int32_t pg = id4[(size_t)q];
       P->fill[pg] = 0;
       P->live[pg] = 0u;
-      add_job(pg, 0, i4, a, std::min<int64_t>(kPage, n4 - a));
-      app.emplace_back(i4[(size_t)a], pg);
+      add_job(pg, 0, true, a, std::min<int64_t>(kPage, u.n4 - a));
+      app.emplace_back(l4[(size_t)a], pg);
     }
-    if (b_new4 > 0) R.tail4 = id4[(size_t)(b_new4 - 1)];
+    if (u.new4 > 0) R.tail4 = id4[(size_t)(u.new4 - 1)];
     // INT2: the open staging page
-    if (b_e > 0) add_job(R.staging, b_s0, i2, 0, b_e);
-    if (b_repack) {
+    if (u.e > 0) add_job(R.staging, u.s0, false, 0, u.e);
+    if (u.repack) {
       const int32_t sp = R.staging;
       P->fill[nid_rep] = kPage;
       P->live[nid_rep] = P->live[sp];
@@ -883,37 +919,38 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
       R.shape = ++P->shape_clock;
       repacks.push_back(RepackJob{sp, nid_rep});
       deferred.push_back(sp);
-      app.emplace_back(i2[(size_t)(b_e - 1)], nid_rep);
+      app.emplace_back(l2[(size_t)(u.e - 1)], nid_rep);
       R.staging = -1;
     }
     // groups of 32 completed in this call: direct INT2 jobs (their staging
     // ids are taken and freed, as the per-token path does)
-    for (int64_t g = 0; g < b_ndirect; ++g) {
-      const int64_t a = b_e + kPage * g;
+    for (int64_t g = 0; g < u.ndirect; ++g) {
+      const int64_t a = u.e + kPage * g;
       const int32_t sg = idS[(size_t)g], nid = idD[(size_t)g];
-      for (int sl = 0; sl < kPage; ++sl) put(nid, sl, i2[(size_t)(a + sl)]);
+      for (int sl = 0; sl < kPage; ++sl) put(nid, sl, l2[(size_t)(a + sl)]);
       P->fill[sg] = kPage;
       P->live[sg] = 0xFFFFFFFFu;
       P->fill[nid] = kPage;
       P->live[nid] = 0xFFFFFFFFu;
-      directs.push_back(DirectJob{nid, (int32_t)a});   // its tokens: i2[a .. a+32), uploaded whole
+      directs.push_back(DirectJob{nid, (int32_t)(u.o2 + a)});   // its tokens: the INT2 list, uploaded whole
       deferred.push_back(sg);
-      app.emplace_back(i2[(size_t)(a + kPage - 1)], nid);
+      app.emplace_back(l2[(size_t)(a + kPage - 1)], nid);
     }
-    if (b_ndirect > 0 && !b_repack) dirty.structural(r, (int32_t)R.table.size());
+    if (u.ndirect > 0 && !u.repack) dirty.structural(r, (int32_t)R.table.size());
     // the last, partial staging page
-    if (b_rem > 0) {
-      const int64_t a = b_e + kPage * b_ndirect;
-      const int32_t sp = idS[(size_t)b_ndirect];
+    if (u.rem > 0) {
+      const int64_t a = u.e + kPage * u.ndirect;
+      const int32_t sp = idS[(size_t)u.ndirect];
       P->fill[sp] = 0;
       P->live[sp] = 0u;
-      add_job(sp, 0, i2, a, b_rem);
-      app.emplace_back(i2[(size_t)a], sp);
+      add_job(sp, 0, false, a, u.rem);
+      app.emplace_back(l2[(size_t)a], sp);
       R.staging = sp;
     }
     std::sort(app.begin(), app.end());
     for (const auto& x : app) R.table.push_back(x.second);
-    if (!app.empty() || b_repack) ++R.version;
+    if (!app.empty() || u.repack) ++R.version;
+  }
   } else {
   std::vector<int32_t> tok_job((size_t)n_tok, -1), tok_slot((size_t)n_tok);
   for (int64_t t = 0; t < n_tok; ++t) {
