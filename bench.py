@@ -294,9 +294,11 @@ def int2_fraction(gw):
 
 
 def run_prefill(args):
-    """Prefill of the workload's prompts (append calls of --chunk tokens of one
-    request, 16K by default), inputs resident in HBM: bf16 K and V rows read,
-    page blocks written."""
+    """Prefill of the workload's prompts in append calls of --chunk tokens (16K
+    by default): of one request, or with --interleave one chunk of every
+    request per call (chunk / requests tokens each, the shape of a batched
+    chunked prefill).  Inputs resident in HBM: bf16 K and V rows read, page
+    blocks written."""
     import torch
     import kvsynth
     from mixed_precision_kv_gb300.workload import GPUWorkload
@@ -306,14 +308,30 @@ def run_prefill(args):
     H = w.num_kv_heads
     chunk = args.chunk
     times = []
+    nreq = len(w.requests)
+    per = max(32, chunk // nreq)   # --interleave: tokens of each request per call
     for rep_i in range(args.warmup + args.steps):
         gw = GPUWorkload(w, device=local, chunk=chunk)
         calls = []
-        for r, spec in enumerate(w.requests):
-            for t0 in range(0, spec.n_prefill, chunk):
-                n = min(chunk, spec.n_prefill - t0)
-                k, v = gw.kv_rows(r, t0, n)
-                calls.append((k, v, np.full(n, gw.rids[r], np.int32), np.ascontiguousarray(gw.bits[r][t0:t0 + n])))
+        if args.interleave:
+            for t0 in range(0, max(s.n_prefill for s in w.requests), per):
+                ks, vs, rs, bs = [], [], [], []
+                for r, spec in enumerate(w.requests):
+                    n = min(per, spec.n_prefill - t0)
+                    if n <= 0:
+                        continue
+                    k, v = gw.kv_rows(r, t0, n)
+                    ks.append(k)
+                    vs.append(v)
+                    rs.append(np.full(n, gw.rids[r], np.int32))
+                    bs.append(gw.bits[r][t0:t0 + n])
+                calls.append((torch.cat(ks), torch.cat(vs), np.concatenate(rs), np.ascontiguousarray(np.concatenate(bs))))
+        else:
+            for r, spec in enumerate(w.requests):
+                for t0 in range(0, spec.n_prefill, chunk):
+                    n = min(chunk, spec.n_prefill - t0)
+                    k, v = gw.kv_rows(r, t0, n)
+                    calls.append((k, v, np.full(n, gw.rids[r], np.int32), np.ascontiguousarray(gw.bits[r][t0:t0 + n])))
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
@@ -338,6 +356,8 @@ def run_prefill(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in, u4/u2 + f16 out",
             "data": "synthetic",
             "config": {"workload": w.name, "mode": "prefill", "tokens": n_tok, "num_kv_heads": H, "chunk": chunk,
+                       "calls": ("one chunk of every request per call (%d tokens each)" % per if args.interleave
+                                 else "one request per call"),
                        "tokens_per_s": n_tok / (t_ms / 1e3), "in_bytes": in_bytes, "out_bytes": blk_bytes},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": None, "peak_source": peak_kind,
@@ -570,6 +590,8 @@ def main():
     ap.add_argument("--alloc3", action="store_true",
                     help="allocate INT2/INT3/INT4 with the three-width greedy over the same budget (D(3) from "
                          "the input recipe)")
+    ap.add_argument("--interleave", action="store_true",
+                    help="--mode prefill: every call carries one chunk of each request (--chunk tokens in all)")
     ap.add_argument("--chunk", type=int, default=16384,
                     help="--mode prefill: tokens per kv_append_quant call (one request per call)")
     ap.add_argument("--mode", default="decode", choices=["decode", "prefill"],

@@ -706,29 +706,37 @@ kv_status_t kv_append_quant(kv_pool_t* P, const void* k, const void* v, const in
     if (i2.size() < (size_t)n_tok) i2.resize((size_t)n_tok);
     int32_t* p4 = i4.data();
     int32_t* p2 = i2.data();
-    int64_t c4 = 0, c2 = 0, tb = 0, b4 = 0, b2 = 0;
+    int64_t c4 = 0, c2 = 0, changes = 0;
     int32_t rp = req_ids[0];
     bool ok = true;
-    auto close_run = [&](int64_t t) {
-      runs.push_back(BulkRun{rp, tb, t - tb, b4, c4 - b4, b2, c2 - b2, 0, 0, 0, 0, 0, 0, 0, false});
-    };
     for (int64_t t = 0; t < n_tok; ++t) {
       const uint32_t b = bits[t];
       const int32_t rt = req_ids[t];
-      if (rt != rp) {
-        close_run(t);
-        rp = rt;
-        tb = t;
-        b4 = c4;
-        b2 = c2;
-      }
       ok &= (b == 2u) | (b == 4u);
+      changes += rt != rp;
+      rp = rt;
       p4[c4] = (int32_t)t;
       p2[c2] = (int32_t)t;
       c4 += b == 4u;
       c2 += b != 4u;
     }
-    close_run(n_tok);
+    if (changes == 0) {
+      runs.push_back(BulkRun{req_ids[0], 0, n_tok, 0, c4, 0, c2, 0, 0, 0, 0, 0, 0, 0, false});
+    } else if (ok) {
+      // several requests: a second pass finds the runs (this keeps the first
+      // pass free of branches and calls)
+      int64_t tb = 0, d4 = 0, d2 = 0, b4 = 0, b2 = 0;
+      for (int64_t t = 1; t <= n_tok; ++t) {
+        d4 += bits[t - 1] == 4u;
+        d2 += bits[t - 1] != 4u;
+        if (t == n_tok || req_ids[t] != req_ids[t - 1]) {
+          runs.push_back(BulkRun{req_ids[tb], tb, t - tb, b4, d4 - b4, b2, d2 - b2, 0, 0, 0, 0, 0, 0, 0, false});
+          tb = t;
+          b4 = d4;
+          b2 = d2;
+        }
+      }
+    }
     // each run an open request of its own, at least a page of tokens long
     // (anything else: the per-token path, which also reports any error)
     for (const auto& u : runs) {
