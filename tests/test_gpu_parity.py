@@ -120,7 +120,8 @@ def test_small_requests_codes_tables_outputs(kvq, n, p2, impl):
 
 
 @pytest.mark.parametrize("impl", IMPLS)
-@pytest.mark.parametrize("hkv,hq", [(1, 1), (2, 4), (4, 12), (2, 16), (1, 7), (1, 2), (1, 3), (1, 5), (1, 6), (1, 8)])
+@pytest.mark.parametrize("hkv,hq", [(1, 1), (2, 4), (4, 12), (2, 16), (1, 7), (1, 2), (1, 3), (1, 5), (1, 6), (1, 8),
+                                    (64, 64), (64, 512)])   # the largest kv head count: head 63 fills the ticket's field
 def test_gqa_ratios(kvq, hkv, hq, impl):
     bits = [_mixed(300, 0.6, 1), _mixed(97, 0.3, 2), _mixed(1, 1.0, 3)]
     sc = Scenario(kvq, hkv, hq, bits, chunk=128, impl=impl)
