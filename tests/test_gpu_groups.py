@@ -242,6 +242,7 @@ def test_drop_validates_before_any_change(kvq):
     ([1, 2, 1], 32, [0.25, 1.0, 0.6]),              # g = 8
     ([4], 16, [0.5]),                               # one pool: the grouped scan alone
     ([1] * 8, 8, [1.0, 0.9, 0.7, 0.5, 0.3, 0.2, 0.1, 0.0]),   # g = 1, eight pools, one keeps nothing
+    ([8] * 8, 512, [1.0, 0.8, 0.6, 0.5, 0.4, 0.3, 0.2, 0.1]),  # g = 8, eight pools of 8: 64 kv heads
 ])
 def test_grouped_decode_matches_shared_pool(kvq, groups, hq, keep):
     """Each group keeps the most recent keep[j] of every request, evicts the

@@ -67,7 +67,7 @@ def _append_window(sc, r, n, stream, tok0=0):
 
 
 @pytest.mark.parametrize("impl", IMPLS)
-@pytest.mark.parametrize("hkv,hq", [(2, 8), (1, 8), (4, 8), (2, 2)])
+@pytest.mark.parametrize("hkv,hq", [(2, 8), (1, 8), (4, 8), (2, 2), (64, 512)])
 def test_vertical_lines_and_window(kvq, impl, hkv, hq):
     bits = [_mixed(700, 0.6, 1), _mixed(333, 0.4, 2), _mixed(90, 0.7, 3)]
     sc = Scenario(kvq, hkv, hq, bits, chunk=128, impl=impl,
