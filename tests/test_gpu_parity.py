@@ -207,6 +207,44 @@ def test_close_reuse_and_oom_leave_state(kvq):
     compare_tables(gpu.export(b, content=False), orc.export(ob, content=False))
 
 
+def test_table_capacity_limit_leaves_state(kvq):
+    """A request's table holds at most max_pages_per_request entries: a call
+    that would pass it returns KV_ERR_OOM on both sides (bulk call of one
+    request, and tokens of two requests interleaved) and changes nothing; a
+    call that fits then proceeds as on the oracle."""
+    hkv, cap = 2, 4
+    gpu = kvq.KVPool(hkv, 32, 32, 2, cap)
+    orc = oracle.OraclePool(hkv, 32, 32, 2, cap)
+    g = [gpu.open() for _ in range(2)]
+    o = [orc.open() for _ in range(2)]
+    kh = kvsynth.fill_bf16_host(300, hkv, 128, SEED, kvsynth.TENSOR_K, 5)
+    vh = kvsynth.fill_bf16_host(300, hkv, 128, SEED, kvsynth.TENSOR_V, 5)
+    kd, vd = torch.from_numpy(kh.view(np.int16)).cuda().view(torch.bfloat16), \
+        torch.from_numpy(vh.view(np.int16)).cuda().view(torch.bfloat16)
+    bits = np.full(300, 4, np.uint8)
+    gpu.append(kd[:100], vd[:100], np.full(100, g[0]), bits[:100])            # 4 INT4 pages: the table is full
+    assert orc.append(np.full(100, o[0]), bits[:100], kh[:100], vh[:100]) == oracle.OK
+    gpu.sync()
+    before = [gpu.export(x, content=False) for x in g]
+    with pytest.raises(kvq.KVError) as e:                                      # bulk: one request, 200 tokens
+        gpu.append(kd[100:300], vd[100:300], np.full(200, g[0]), bits[100:300])
+    assert e.value.status == kvq.KV_ERR_OOM
+    assert orc.append(np.full(200, o[0]), bits[100:300], kh[100:300], vh[100:300]) == oracle.OOM
+    req = np.where(np.arange(200) % 2 == 0, 0, 1)                              # per token: interleaved requests
+    with pytest.raises(kvq.KVError) as e:
+        gpu.append(kd[100:300], vd[100:300], np.array(g)[req], bits[100:300])
+    assert e.value.status == kvq.KV_ERR_OOM
+    assert orc.append(np.array(o)[req], bits[100:300], kh[100:300], vh[100:300]) == oracle.OOM
+    gpu.sync()
+    for x, b in zip(g, before):
+        compare_tables(gpu.export(x, content=False), b)
+    gpu.append(kd[100:128], vd[100:128], np.full(28, g[0]), bits[100:128])    # fills the last page's 28 free slots
+    assert orc.append(np.full(28, o[0]), bits[100:128], kh[100:128], vh[100:128]) == oracle.OK
+    gpu.sync()
+    for x, y in zip(g, o):
+        compare_content(gpu.export(x), orc.export(y), [0, 1])
+
+
 def test_range_error_reported_by_sync(kvq):
     gpu = kvq.KVPool(1, 4, 4, 1, 8)
     a = gpu.open()
