@@ -11,7 +11,8 @@ outliers together, q rows from 1e-3 to 1e3, and a pool whose largest INT2 K
 and V scales grow after requests were already decoded.  Each case runs at
 g = 4 and g = 8 over an INT2-only, an INT4-only and a mixed request, on both
 scans; outputs must lie within max-abs 1e-3 and relative-L2 1e-4 of the fp64
-oracle, and codes, scale/zero and tables must match it bit for bit."""
+oracle, and codes, scale/zero and tables must match it bit for bit.  The
+same ranges run on INT3 and FP4 pages too."""
 import numpy as np
 import pytest
 
@@ -47,10 +48,10 @@ def _dev(bits_u16):
 class Pair:
     """A GPU pool and an oracle pool fed the same explicit bf16 rows."""
 
-    def __init__(self, kvq, hkv, n_req, impl, n2=64, n4=64, max_tab=32):
-        self.gpu = kvq.KVPool(hkv, n2, n4, n_req, max_tab)
+    def __init__(self, kvq, hkv, n_req, impl, n2=64, n4=64, max_tab=32, n3=0, nf=0):
+        self.gpu = kvq.KVPool(hkv, n2, n4, n_req, max_tab, n_int3_pages=n3, n_fp4_pages=nf)
         self.gpu.set_decode_impl(impl)
-        self.orc = oracle.OraclePool(hkv, n2, n4, n_req, max_tab)
+        self.orc = oracle.OraclePool(hkv, n2, n4, n_req, max_tab, n_int3_pages=n3, n_fp4_pages=nf)
         self.g = [self.gpu.open() for _ in range(n_req)]
         self.o = [self.orc.open() for _ in range(n_req)]
         self.hkv = hkv
@@ -139,6 +140,25 @@ def test_value_ranges(kvq, case, g, impl):
     P.reorder()
     q = rng.standard_normal((len(bits), HKV * g, 128)).astype(np.float32)
     P.check(q, f"{case} g={g} impl={impl}")
+
+
+@pytest.mark.parametrize("impl", [1, 2])
+@pytest.mark.parametrize("g", [4, 8])
+@pytest.mark.parametrize("case", sorted(CASES))
+def test_value_ranges_int3_fp4(kvq, case, g, impl):
+    """The same value ranges on INT3 and FP4 pages: an INT3-only, an FP4-only
+    and a request mixing all four widths."""
+    from mixed_precision_kv_gb300 import KV_WIDTH_FP4
+    rng = np.random.default_rng([10, g, len(case)])
+    bits = [np.full(200, 3, np.uint8), np.full(160, KV_WIDTH_FP4, np.uint8),
+            rng.choice(np.array([2, 3, 4, KV_WIDTH_FP4], np.uint8), 300)]
+    P = Pair(kvq, HKV, len(bits), impl, n3=32, nf=32)
+    for r, b in enumerate(bits):
+        k, v = CASES[case](rng, b.size)
+        P.append(r, k, v, b)
+    P.reorder()
+    q = rng.standard_normal((len(bits), HKV * g, 128)).astype(np.float32)
+    P.check(q, f"INT3/FP4 {case} g={g} impl={impl}")
 
 
 @pytest.mark.parametrize("impl", [1, 2])
