@@ -36,23 +36,54 @@ def _dev(u16):
     return torch.from_numpy(np.ascontiguousarray(u16).view(np.int16)).cuda().view(torch.bfloat16)
 
 
+FP_CAP = 256   # full-precision list capacity (segments variant)
+
+
 class Lockstep:
-    def __init__(self, kvq, widths, n2, n4, n3, nf, max_tab):
+    def __init__(self, kvq, widths, n2, n4, n3, nf, max_tab, segments=False):
         self.kvq = kvq
         self.gpu = kvq.KVPool(HKV, n2, n4, MAX_REQ, max_tab, n_int3_pages=n3, n_fp4_pages=nf)
         self.orc = oracle.OraclePool(HKV, n2, n4, MAX_REQ, max_tab, n_int3_pages=n3, n_fp4_pages=nf)
+        if segments:
+            self.gpu.fp_configure(FP_CAP)
         self.widths = np.array(widths, np.uint8)
         self.open_ = {}     # gpu id -> [oracle id, tokens appended, data stream]
+        self.fp = {}        # gpu id -> [list tokens now, list tokens ever appended]
         self.streams = 0
 
     def open(self):
         g, o = self.gpu.open(), self.orc.open()
         self.open_[g] = [o, 0, self.streams]
+        self.fp[g] = [0, 0]
         self.streams += 1
 
     def close(self, g):
         self.gpu.close_request(g)
         self.orc.close_request(self.open_.pop(g)[0])
+        del self.fp[g]
+
+    def fp_append(self, g, n):
+        o, _, st = self.open_[g]
+        n = min(n, FP_CAP - self.fp[g][0])
+        if n <= 0:
+            return
+        t0 = 1_000_000 + self.fp[g][1]   # list tokens draw from their own positions of the stream
+        k = kvsynth.fill_bf16_host(n, HKV, 128, SEED, kvsynth.TENSOR_K, st, t0)
+        v = kvsynth.fill_bf16_host(n, HKV, 128, SEED, kvsynth.TENSOR_V, st, t0)
+        self.gpu.fp_append(g, _dev(k), _dev(v))
+        assert self.orc.fp_append(o, k, v) == oracle.OK
+        self.fp[g][0] += n
+        self.fp[g][1] += n
+
+    def fp_drop(self, g, rng):
+        cnt = self.fp[g][0]
+        if cnt == 0:
+            return
+        first = int(rng.integers(0, cnt))
+        n = int(rng.integers(1, cnt - first + 1))
+        self.gpu.fp_drop(g, first, n)
+        assert self.orc.fp_drop(self.open_[g][0], first, n) == oracle.OK
+        self.fp[g][0] -= n
 
     def append(self, runs, rng, interleave=False):
         """runs: [(gpu id, n tokens)]; interleave: tokens of the runs shuffled
@@ -105,6 +136,7 @@ class Lockstep:
         self.gpu.sync()
         for g, (o, n, _) in self.open_.items():
             assert self.gpu.info(g)[1] == n and self.orc.info(o)[1] == n, what
+            assert self.gpu.fp_count(g) == self.fp[g][0], what
             compare_tables(self.gpu.export(g, content=False), self.orc.export(o, content=False))
 
     def check_decode(self, rng, what):
@@ -122,16 +154,22 @@ class Lockstep:
         assert_outputs_close(out, ref, what)
 
 
-@pytest.mark.parametrize("seed,widths", [(1, [2, 4]), (2, [2, 4]), (3, [2, 4]), (4, [2, 4]),
-                                         (5, [2, 3, 4, 0xF4]), (6, [2, 3, 4, 0xF4])])
-def test_random_call_sequences(kvq, seed, widths):
+@pytest.mark.parametrize("seed,widths,segments", [(1, [2, 4], False), (2, [2, 4], False), (3, [2, 4], False),
+                                                  (4, [2, 4], False), (5, [2, 3, 4, 0xF4], False),
+                                                  (6, [2, 3, 4, 0xF4], False), (7, [2, 4], True),
+                                                  (8, [2, 3, 4, 0xF4], True)])
+def test_random_call_sequences(kvq, seed, widths, segments):
+    """segments: full-precision list appends and drops join the calls (the
+    decode then scans the lists after the quantized pages)."""
     rng = np.random.default_rng([91, seed])
-    L = Lockstep(kvq, widths, n2=40, n4=70, n3=24, nf=24, max_tab=30)
+    L = Lockstep(kvq, widths, n2=40, n4=70, n3=24, nf=24, max_tab=30, segments=segments)
     outcomes = {"ok": 0, "oom": 0}
+    ops = ["open", "close", "bulk", "runs", "interleaved", "short", "evict", "evict_head", "drop", "reorder",
+           "fp_append", "fp_drop"]
+    p = np.array([0.08, 0.05, 0.2, 0.17, 0.12, 0.1, 0.1, 0.08, 0.05, 0.05] + ([0.1, 0.05] if segments else [0, 0]))
     for step in range(200):
         ids = list(L.open_)
-        op = rng.choice(["open", "close", "bulk", "runs", "interleaved", "short", "evict", "evict_head", "drop",
-                         "reorder"], p=[0.08, 0.05, 0.2, 0.17, 0.12, 0.1, 0.1, 0.08, 0.05, 0.05])
+        op = rng.choice(ops, p=p / p.sum())
         if op == "open" or not ids:
             if len(L.open_) < MAX_REQ:
                 L.open()
@@ -155,6 +193,10 @@ def test_random_call_sequences(kvq, seed, widths):
                 L.evict(g, pos, heads)
         elif op == "drop":
             L.drop([int(x) for x in rng.choice(ids, int(rng.integers(1, len(ids) + 1)), replace=False)])
+        elif op == "fp_append":
+            L.fp_append(ids[int(rng.integers(0, len(ids)))], int(rng.integers(1, 60)))
+        elif op == "fp_drop":
+            L.fp_drop(ids[int(rng.integers(0, len(ids)))], rng)
         else:
             L.reorder()
         L.check_tables(f"seed {seed} step {step} ({op})")
