@@ -137,6 +137,46 @@ def job_throughput(step_bytes, steps, world, t_ms):
     return step_bytes * steps * world / (t_ms / 1e3) / 1e9
 
 
+def timed_span(stream, dev, n, body, flush):
+    """Milliseconds of body(0) .. body(n - 1) enqueued on `stream`.  Without
+    flush: one event pair around all of them.  With flush (inputs smaller
+    than L2): each call gets its own event pair, and before each a write of
+    twice L2 (outside the pairs) evicts what the previous call left in L2;
+    the result is the sum of the pairs."""
+    import torch
+    if not flush:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(n):
+            body(i)
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    scratch = torch.empty((2 * l2 // 4 + 1024,), dtype=torch.int32, device=dev)
+    pairs = []
+    for i in range(n):
+        scratch.fill_(i)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        body(i)
+        b.record(stream)
+        pairs.append((a, b))
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in pairs)
+
+
+def l2_policy(dev, step_bytes):
+    """(flush, description) for a decode step that reads step_bytes."""
+    import torch
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    if step_bytes < l2:
+        return True, ("L2 flushed before every timed step (a %.0f MB write outside the timed spans; the step reads "
+                      "%.1f MB); each span is the step's device time, since the host issues the next step while "
+                      "the flush runs" % (2 * l2 / 1e6, step_bytes / 1e6))
+    return False, "inputs larger than L2 (%.0f MB per step)" % (step_bytes / 1e6)
+
+
 TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "decode_mma_traffic.json")
 
 
@@ -481,13 +521,9 @@ def run_head_groups(args):
     launches0 = sum(p.launch_count() for p in pools)
     timing_every = 1 if args.steps < 200 else 8
     pools[0].decode_timing(True, every=timing_every)
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    flush, l2_desc = l2_policy(dev, kv_first)
     torch.cuda.synchronize()
-    start.record(stream)
-    for i in range(args.steps):
-        step(s0 + i)
-    end.record(stream)
-    torch.cuda.synchronize()
+    t_loop = timed_span(stream, dev, args.steps, lambda i: step(s0 + i), flush)
     clk.stop()
     if dist:
         dist.barrier()
@@ -496,7 +532,7 @@ def run_head_groups(args):
     n_timed, scan_ms, dec_ms = pools[0].decode_timing(False)
     for p in pools:
         p.sync()
-    t_ms = reduce_max_time(start.elapsed_time(end), dist, dev)
+    t_ms = reduce_max_time(t_loop, dist, dev)
     step_bytes = 0.5 * (kv_first + kv_last)
     value = job_throughput(step_bytes, args.steps, ws, t_ms)
     achieved = step_bytes / (scan_ms / 1e3) / 1e9
@@ -517,16 +553,15 @@ def run_head_groups(args):
         step(s0 + args.steps + i)
     torch.cuda.synchronize()
     e_first = kv_bytes()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(e2e_steps):
+
+    def e2e_step(i):
         dbuf.copy_(hbuf[i], non_blocking=True)
         step(s_e + i, dk, dv, dq)
         hout.copy_(out, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize()
+
+    e_ms = timed_span(stream, dev, e2e_steps, e2e_step, flush)
     e_last = kv_bytes()
-    e_ms = reduce_max_time(e0.elapsed_time(e1), dist, dev)
+    e_ms = reduce_max_time(e_ms, dist, dev)
     e2e_val = job_throughput(0.5 * (e_first + e_last), e2e_steps, ws, e_ms)
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
@@ -535,7 +570,7 @@ def run_head_groups(args):
             "config": {"workload": f"{w.name}+head-groups{N}", "batch": B, "num_q_heads": Hq, "num_kv_heads": H,
                        "head_dim": 128, "context": context_desc(w), "page_tokens": 32, "budget_bits": budget_desc(w),
                        "decode_impl": "mma (grouped scan)",
-                       "l2": "inputs larger than L2 (%.0f MB per step)" % (step_bytes / 1e6),
+                       "l2": l2_desc,
                        "us_per_layer_step": t_ms / args.steps * 1e3, "decode_us": dec_ms * 1e3,
                        "scan_us": scan_ms * 1e3, "decode_calls_timed": n_timed,
                        "pct_of_8000_gbs": value / ws / 8000 * 100},
@@ -729,21 +764,20 @@ def main():
     # scan's drain, so the other calls run without one)
     timing_every = 1 if args.steps < 200 else 8
     gw.pool.decode_timing(True, every=timing_every)
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    torch.cuda.nvtx.range_push("timed")
-    start.record(stream)
-    if args.segments:
-        for i in range(args.steps):
-            seg_step(s0 + i)
-    else:
-        for i in range(args.steps):
-            s = s0 + i
+    flush, l2_desc = l2_policy(dev, kv_raw_first)
+
+    def timed_step(i):
+        s = s0 + i
+        if args.segments:
+            seg_step(s)
+        else:
             gw.pool.append(ks[s], vs[s], rids, bits[s])
             gw.pool.reorder(rids)
             gw.pool.decode(qs[s], rids, w.softmax_scale, out=out)
-    end.record(stream)
+
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("timed")
+    t_loop = timed_span(stream, dev, args.steps, timed_step, flush)
     torch.cuda.nvtx.range_pop()
     clk.stop()
     if dist:
@@ -753,7 +787,7 @@ def main():
     launches = gw.pool.launch_count() - launches0
     n_timed, scan_ms, dec_ms = gw.pool.decode_timing(False)
     gw.pool.sync()
-    t_ms = reduce_max_time(start.elapsed_time(end), dist, dev)
+    t_ms = reduce_max_time(t_loop, dist, dev)
     step_bytes = 0.5 * (kv_first + kv_last) + fp_mean
     value = job_throughput(step_bytes, args.steps, ws, t_ms)
     achieved = step_bytes / (scan_ms / 1e3) / 1e9
@@ -775,17 +809,15 @@ def main():
         step(s0 + args.steps + i)
     torch.cuda.synchronize()
     e_first = gw.pool.last_decode_stats()["kv_bytes"]
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(e2e_steps):
+
+    def e2e_step(i):
         dbuf.copy_(hbuf[i], non_blocking=True)
         step(s_e + i, dk, dv, dq)
         hout.copy_(out, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize()
+
+    e_ms = timed_span(stream, dev, e2e_steps, e2e_step, flush)
     e_last = gw.pool.last_decode_stats()["kv_bytes"]
-    e_ms = reduce_max_time(e0.elapsed_time(e1), dist, dev)
+    e_ms = reduce_max_time(e_ms, dist, dev)
     e2e_val = job_throughput(0.5 * (e_first + e_last), e2e_steps, ws, e_ms)
     h2d = (dk.numel() + dv.numel() + dq.numel()) * 2
     d2h = hout.numel() * 4
@@ -797,8 +829,7 @@ def main():
                                    ("+ragged-heads" if args.ragged_heads else ""), "batch": B, "num_q_heads": Hq, "num_kv_heads": Hkv, "head_dim": 128,
                        "context": context_desc(w), "page_tokens": 32, "budget_bits": budget_desc(w),
                        "int2_token_fraction": int2_fraction(gw),
-                       "decode_impl": args.decode_impl, "l2": "inputs larger than L2 (%.0f MB per step)"
-                                                             % (step_bytes / 1e6),
+                       "decode_impl": args.decode_impl, "l2": l2_desc,
                        "us_per_layer_step": t_ms / args.steps * 1e3, "decode_us": dec_ms * 1e3,
                        "scan_us": scan_ms * 1e3, "decode_calls_timed": n_timed,
                        "kv_bytes_last_warmup_decode": kv_raw_first,
