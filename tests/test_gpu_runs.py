@@ -132,3 +132,46 @@ def test_runs_out_of_pages_change_nothing(kvq):
             assert np.array_equal(a[key], b[key]), key
     P.call([(2, 40), (0, 40)])
     P.check("runs after an OOM")
+
+
+def test_interleaved_prefill_full_size(kvq):
+    """The 32K-token batch-8 prompts appended in calls that carry 4096 tokens
+    of every request: every table bit-exact, codes and scale/zero of two kv
+    heads of every request, and their decode outputs, against the oracle."""
+    from harness import OracleWorkload
+    from mixed_precision_kv_gb300.workload import GPUWorkload, pool_size
+    w = kvsynth.make_workload(2)
+    per, heads = 4096, [1, 6]
+    chunk = per * len(w.requests)
+    gw = GPUWorkload(w, chunk=chunk)
+    ow = OracleWorkload(w, pool_size(w, gw.bits, chunk, gw.steps), chunk, sel_heads=heads)
+    for a, b in zip(gw.bits, ow.bits):
+        assert np.array_equal(a, b)
+    n = max(s.n_prefill for s in w.requests)
+    for t0 in range(0, n, per):
+        gk, gv, ok_, ov, gr, orq, bb = [], [], [], [], [], [], []
+        for r, spec in enumerate(w.requests):
+            m = min(per, spec.n_prefill - t0)
+            if m <= 0:
+                continue
+            k, v = gw.kv_rows(r, t0, m)
+            kh, vh = ow.kv_rows(r, t0, m)
+            gk.append(k); gv.append(v); ok_.append(kh); ov.append(vh)
+            gr.append(np.full(m, gw.rids[r], np.int32))
+            orq.append(np.full(m, ow.rids[r], np.int32))
+            bb.append(gw.bits[r][t0:t0 + m])
+        bits = np.ascontiguousarray(np.concatenate(bb))
+        gw.pool.append(torch.cat(gk), torch.cat(gv), np.concatenate(gr), bits)
+        assert ow.P.append(np.concatenate(orq), bits, np.concatenate(ok_), np.concatenate(ov)) == oracle.OK
+    gw.reorder()
+    ow.reorder()
+    gw.pool.sync()
+    for r in range(len(w.requests)):
+        compare_content(gw.pool.export(gw.rids[r]), ow.P.export(ow.rids[r]), heads)
+    g = w.g
+    pairs = [(b, h * g + j) for b in range(len(w.requests)) for h in heads for j in range(g)]
+    out = gw.decode(gw.q(0)).cpu().numpy()
+    gw.pool.sync()
+    ref = ow.decode(ow.q(0), pairs=np.array(pairs, np.int32))
+    got = np.stack([out[b, h] for b, h in pairs])
+    assert_outputs_close(got, ref, "interleaved prefill, full size")
